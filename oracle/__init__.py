@@ -1,0 +1,190 @@
+"""fp64 CPU oracle for packed variable-length multi-head attention.
+
+TEST INFRASTRUCTURE ONLY.  This package is the independent checker for the CUDA
+library in ``packed_variable_length_varlen_gb300``: only ``tests/``,
+``__graft_entry__.smoke()`` and the ``cpu_baseline`` / ``--impl reference``
+legs of ``bench.py`` may import it.  The product path never calls it, and it
+imports nothing from the product package.
+
+The arithmetic lives in ``varlen_oracle.c`` (plain fp64 loops, OpenMP over
+independent (row, head) pairs); this module compiles it with the host C
+compiler, loads it with ctypes and marshals torch CPU tensors (bf16 or fp64,
+any row / head stride, unit innermost stride) into it.
+
+What it computes is the packed ``cu_seqlens`` attention of the flash-attention
+issue pages ("[FA4] cute varlen backward: int32 overflow in _bwd_preprocess",
+sections "Summary" and "Minimal repro"; "[FA4][SM120] flash_attn_varlen_func
+... illegal memory access", section "Bug 2 details"):
+
+    O_b = softmax(scale * Q_b K_b^T) V_b  per segment b,
+    LSE_i = ln sum_j exp(s_ij)            (natural log; -inf for no keys),
+
+and the gradients dQ, dK, dV of sum(O * dO).  Every function takes explicit
+(row, head) pairs so that large problems can be checked on samples.
+
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
+(torch fp64 SDPA + autograd per segment, closed forms, central finite
+differences, gradient invariants, planted-mistake detection).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import platform
+import subprocess
+import threading
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "varlen_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LOCK = threading.Lock()
+_LIB = None
+
+
+class _Problem(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p),
+        ("v", ctypes.c_void_p), ("dout", ctypes.c_void_p),
+        ("q_rs", ctypes.c_int64), ("q_hs", ctypes.c_int64),
+        ("k_rs", ctypes.c_int64), ("k_hs", ctypes.c_int64),
+        ("v_rs", ctypes.c_int64), ("v_hs", ctypes.c_int64),
+        ("do_rs", ctypes.c_int64), ("do_hs", ctypes.c_int64),
+        ("cu_q", ctypes.c_void_p), ("cu_k", ctypes.c_void_p),
+        ("batch", ctypes.c_int32), ("num_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32),
+        ("scale", ctypes.c_double),
+    ]
+
+
+def library_path(src: str = _SRC, tag: str = "") -> str:
+    name = "liboracle%s_%s.so" % (tag, platform.machine())
+    return os.path.join(_BUILD_DIR, name)
+
+
+def build(src: str = _SRC, out: str | None = None, extra_flags=()) -> str:
+    """Compile the C oracle into a shared library; returns its path."""
+    out = out or library_path(src)
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    if os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src) and not extra_flags:
+        return out
+    tmp = out + ".tmp%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-shared", "-fPIC",
+           *extra_flags, "-o", tmp, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _declare(lib):
+    P = ctypes.POINTER(_Problem)
+    for name in ("oracle_fwd", "oracle_bwd_q", "oracle_bwd_kv"):
+        f = getattr(lib, name)
+        f.restype = ctypes.c_int
+        f.argtypes = [P, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                      ctypes.c_void_p, ctypes.c_void_p]
+    lib.oracle_num_threads.restype = ctypes.c_int
+    return lib
+
+
+def load_library(path: str | None = None):
+    """Load (building if needed) the oracle library.  ``path`` loads a
+    specific build, e.g. a planted-mistake variant compiled by a test."""
+    global _LIB
+    if path is not None:
+        return _declare(ctypes.CDLL(path))
+    with _LOCK:
+        if _LIB is None:
+            _LIB = _declare(ctypes.CDLL(build()))
+        return _LIB
+
+
+def num_threads() -> int:
+    return int(load_library().oracle_num_threads())
+
+
+def _view_args(t: torch.Tensor | None, H: int, D: int):
+    if t is None:
+        return None, 0, 0
+    if t.device.type != "cpu":
+        raise ValueError("oracle inputs must be CPU tensors")
+    if t.dim() != 3 or t.shape[1] != H or t.shape[2] != D or t.stride(2) != 1:
+        raise ValueError("oracle inputs must be [rows, H, D] with unit innermost stride")
+    return t.data_ptr(), t.stride(0), t.stride(1)
+
+
+class Problem:
+    """One packed-attention problem, held as CPU tensors (no copies)."""
+
+    def __init__(self, q, k, v, cu_q, cu_k, scale, dout=None):
+        dt = q.dtype
+        if dt not in (torch.bfloat16, torch.float64):
+            raise ValueError("oracle supports bf16 or fp64 inputs")
+        for t in (k, v, dout):
+            if t is not None and t.dtype != dt:
+                raise ValueError("all oracle inputs must share one dtype")
+        self.H, self.D = int(q.shape[1]), int(q.shape[2])
+        self.cu_q = torch.as_tensor(cu_q, dtype=torch.int32).contiguous()
+        self.cu_k = torch.as_tensor(cu_k, dtype=torch.int32).contiguous()
+        if self.cu_q.numel() != self.cu_k.numel() or self.cu_q.numel() < 1:
+            raise ValueError("cu_seqlens_q and cu_seqlens_k need batch+1 entries each")
+        self._keep = (q, k, v, dout, self.cu_q, self.cu_k)
+        s = _Problem()
+        s.q, s.q_rs, s.q_hs = _view_args(q, self.H, self.D)
+        s.k, s.k_rs, s.k_hs = _view_args(k, self.H, self.D)
+        s.v, s.v_rs, s.v_hs = _view_args(v, self.H, self.D)
+        s.dout, s.do_rs, s.do_hs = _view_args(dout, self.H, self.D)
+        s.cu_q, s.cu_k = self.cu_q.data_ptr(), self.cu_k.data_ptr()
+        s.batch = self.cu_q.numel() - 1
+        s.num_heads, s.head_dim = self.H, self.D
+        s.dtype = 0 if dt == torch.bfloat16 else 1
+        s.scale = float(scale)
+        self._s = s
+        self.has_dout = dout is not None
+
+    def _pairs(self, rows, heads):
+        rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1))
+        heads = np.ascontiguousarray(np.asarray(heads, dtype=np.int32).reshape(-1))
+        if rows.shape != heads.shape:
+            raise ValueError("rows and heads must pair up")
+        if heads.size and (heads.min() < 0 or heads.max() >= self.H):
+            raise ValueError("head index out of range")
+        return rows, heads
+
+    def _call(self, fn, rows, heads, width_a, width_b):
+        rows, heads = self._pairs(rows, heads)
+        n = rows.size
+        a = np.empty((n, width_a), dtype=np.float64)
+        b = np.empty((n, width_b) if width_b > 1 else (n,), dtype=np.float64)
+        if n:
+            fn(ctypes.byref(self._s), n, rows.ctypes.data, heads.ctypes.data,
+               a.ctypes.data, b.ctypes.data)
+        return a, b
+
+    def fwd(self, rows, heads, lib=None):
+        """O rows [n, D] and LSE [n] for (q row, head) pairs."""
+        lib = lib or load_library()
+        return self._call(lib.oracle_fwd, rows, heads, self.D, 1)
+
+    def bwd_q(self, rows, heads, lib=None):
+        """dQ rows [n, D] and delta [n] for (q row, head) pairs."""
+        if not self.has_dout:
+            raise ValueError("backward needs dout")
+        lib = lib or load_library()
+        return self._call(lib.oracle_bwd_q, rows, heads, self.D, 1)
+
+    def bwd_kv(self, rows, heads, lib=None):
+        """dK rows [n, D] and dV rows [n, D] for (kv row, head) pairs."""
+        if not self.has_dout:
+            raise ValueError("backward needs dout")
+        lib = lib or load_library()
+        return self._call(lib.oracle_bwd_kv, rows, heads, self.D, self.D)
+
+
+def all_pairs(total_rows: int, num_heads: int):
+    """Every (row, head) pair of a [total_rows, num_heads, D] tensor."""
+    rows = np.repeat(np.arange(total_rows, dtype=np.int64), num_heads)
+    heads = np.tile(np.arange(num_heads, dtype=np.int32), total_rows)
+    return rows, heads

@@ -1,0 +1,302 @@
+/*
+ * varlen_oracle.c -- plain fp64 CPU oracle for packed variable-length
+ * (cu_seqlens) multi-head scaled-dot-product attention, forward and backward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the independent checker for the CUDA
+ * library in packed_variable_length_varlen_gb300/.  Only tests/, the smoke
+ * check in __graft_entry__.py and the CPU-baseline leg of bench.py may load it.
+ * It shares no code, header, table or helper with the CUDA path.
+ *
+ * What it computes (the definition, written out; no online rescaling, no
+ * tiling, no fusion):
+ *
+ *   Inputs are bf16 (or, for finite-difference pins, fp64) tensors in NHD
+ *   layout: element (row r, head h, dim d) sits at
+ *       base + r*row_stride + h*head_stride + d            (int64 elements).
+ *   Segment b owns q rows [cu_q[b], cu_q[b+1]) and kv rows [cu_k[b], cu_k[b+1]).
+ *   This is the packed "cu_seqlens" interface of flash_attn_varlen_func as used
+ *   on the flash-attention issue pages ("[FA4] cute varlen backward: int32
+ *   overflow in _bwd_preprocess", section "Minimal repro", and "[FA4][SM120]
+ *   flash_attn_varlen_func ... illegal memory access at >=4 varlen segments",
+ *   section "Bug 2 details": cu_seqlens_q / cu_seqlens_k, non-causal).
+ *
+ *   For q row i of segment b, head h, kv rows j of the same segment:
+ *     s_ij   = scale * sum_d q[i,h,d] k[j,h,d]
+ *     m_i    = max_j s_ij
+ *     LSE_i  = m_i + ln sum_j exp(s_ij - m_i)        (natural log)
+ *     P_ij   = exp(s_ij - LSE_i)
+ *     o_i    = sum_j P_ij v_j
+ *   An empty key set (Sk_b = 0) gives LSE_i = -inf and o_i = 0.
+ *
+ *   Backward, for an upstream gradient dO (the varlen backward of the same
+ *   issue page, "Summary": gradients dQ/dK/dV of the attention output):
+ *     delta_i = sum_d dO_i[d] o_i[d]        (exact fp64 o_i)
+ *     dP_ij   = dO_i . v_j
+ *     dS_ij   = P_ij (dP_ij - delta_i)
+ *     dq_i    = scale sum_j dS_ij k_j
+ *     dk_j    = scale sum_i dS_ij q_i
+ *     dv_j    = sum_i P_ij dO_i
+ *   Empty sums are zero (dq of an empty-key segment, dk/dv of an empty-query
+ *   segment).
+ *
+ * All index arithmetic is int64.  Rows are looked up in cu_seqlens by a
+ * linear scan.  OpenMP parallelises over independent (row, head) pairs only.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+typedef struct {
+    const void *q, *k, *v, *dout;   /* element type given by dtype          */
+    int64_t q_rs, q_hs;             /* row / head strides, in elements      */
+    int64_t k_rs, k_hs;
+    int64_t v_rs, v_hs;
+    int64_t do_rs, do_hs;
+    const int32_t *cu_q, *cu_k;     /* batch + 1 entries each               */
+    int32_t batch, num_heads, head_dim;
+    int32_t dtype;                  /* 0 = bf16 bit patterns, 1 = fp64      */
+    double scale;
+} oracle_problem;
+
+/* Exact widening of a bf16 bit pattern: the bf16 bits are the top half of an
+ * IEEE binary32. */
+static double bf16_bits_to_f64(uint16_t bits) {
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double load(const void *base, int32_t dtype, int64_t idx) {
+    if (dtype == 0) return bf16_bits_to_f64(((const uint16_t *)base)[idx]);
+    return ((const double *)base)[idx];
+}
+
+/* Row vector x[d] = T[row, h, :] widened to fp64. */
+static void load_row(const void *base, int32_t dtype, int64_t rs, int64_t hs,
+                     int64_t row, int32_t h, int32_t D, double *x) {
+    int64_t off = row * rs + (int64_t)h * hs;
+    for (int32_t d = 0; d < D; ++d) x[d] = load(base, dtype, off + d);
+}
+
+static double dot(const double *a, const double *b, int32_t D) {
+    double acc = 0.0;
+    for (int32_t d = 0; d < D; ++d) acc += a[d] * b[d];
+    return acc;
+}
+
+/* The segment that holds row i: the b with cu[b] <= i < cu[b+1].  Returns -1
+ * when no segment holds it. */
+static int32_t segment_of(const int32_t *cu, int32_t batch, int64_t i) {
+    for (int32_t b = 0; b < batch; ++b)
+        if ((int64_t)cu[b] <= i && i < (int64_t)cu[b + 1]) return b;
+    return -1;
+}
+
+/* Forward for one (q row, head): s, LSE, P and o by the definition above.
+ * s and p are scratch of length >= Sk.  Returns the segment, -1 if the row is
+ * in none. */
+static int32_t row_forward(const oracle_problem *pb, int64_t i, int32_t h,
+                           double *qi, double *kj, double *s, double *out_o,
+                           double *out_lse) {
+    const int32_t D = pb->head_dim;
+    int32_t b = segment_of(pb->cu_q, pb->batch, i);
+    if (b < 0) return -1;
+    const int64_t k0 = pb->cu_k[b], Sk = (int64_t)pb->cu_k[b + 1] - pb->cu_k[b];
+    load_row(pb->q, pb->dtype, pb->q_rs, pb->q_hs, i, h, D, qi);
+    for (int32_t d = 0; d < D; ++d) out_o[d] = 0.0;
+    if (Sk <= 0) {
+        *out_lse = -INFINITY;
+        return b;
+    }
+    double m = -INFINITY;
+    for (int64_t j = 0; j < Sk; ++j) {
+        load_row(pb->k, pb->dtype, pb->k_rs, pb->k_hs, k0 + j, h, D, kj);
+        s[j] = pb->scale * dot(qi, kj, D);
+        if (s[j] > m) m = s[j];
+    }
+    double sum = 0.0;
+    for (int64_t j = 0; j < Sk; ++j) sum += exp(s[j] - m);
+    const double lse = m + log(sum);
+    for (int64_t j = 0; j < Sk; ++j) {
+        const double p = exp(s[j] - lse);
+        load_row(pb->v, pb->dtype, pb->v_rs, pb->v_hs, k0 + j, h, D, kj);
+        for (int32_t d = 0; d < D; ++d) out_o[d] += p * kj[d];
+    }
+    *out_lse = lse;
+    return b;
+}
+
+static int64_t max_seg_len(const int32_t *cu, int32_t batch) {
+    int64_t mx = 1;
+    for (int32_t b = 0; b < batch; ++b) {
+        int64_t len = (int64_t)cu[b + 1] - cu[b];
+        if (len > mx) mx = len;
+    }
+    return mx;
+}
+
+/*
+ * Forward on selected (q row, head) pairs.
+ *   rows[n], heads[n] : packed q row index and head of each pair.
+ *   out : [n][D] fp64;  lse : [n] fp64.
+ * Rows outside every segment get NaN.  Returns 0.
+ */
+int oracle_fwd(const oracle_problem *pb, int64_t n, const int64_t *rows,
+               const int32_t *heads, double *out, double *lse) {
+    const int32_t D = pb->head_dim;
+    const int64_t smax = max_seg_len(pb->cu_k, pb->batch);
+#pragma omp parallel
+    {
+        double *qi = malloc(sizeof(double) * D), *kj = malloc(sizeof(double) * D);
+        double *s = malloc(sizeof(double) * smax);
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t t = 0; t < n; ++t) {
+            double *o = out + t * D;
+            if (row_forward(pb, rows[t], heads[t], qi, kj, s, o, lse + t) < 0) {
+                for (int32_t d = 0; d < D; ++d) o[d] = NAN;
+                lse[t] = NAN;
+            }
+        }
+        free(qi); free(kj); free(s);
+    }
+    return 0;
+}
+
+/*
+ * Backward, query side, on selected (q row, head) pairs:
+ *   dq    : [n][D]   scale * sum_j dS_ij k_j
+ *   delta : [n]      dO_i . o_i with the exact o_i
+ * Requires pb->dout.
+ */
+int oracle_bwd_q(const oracle_problem *pb, int64_t n, const int64_t *rows,
+                 const int32_t *heads, double *dq, double *delta) {
+    const int32_t D = pb->head_dim;
+    const int64_t smax = max_seg_len(pb->cu_k, pb->batch);
+#pragma omp parallel
+    {
+        double *qi = malloc(sizeof(double) * D), *kj = malloc(sizeof(double) * D);
+        double *oi = malloc(sizeof(double) * D), *doi = malloc(sizeof(double) * D);
+        double *s = malloc(sizeof(double) * smax);
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t t = 0; t < n; ++t) {
+            const int64_t i = rows[t];
+            const int32_t h = heads[t];
+            double *g = dq + t * D, lse;
+            int32_t b = row_forward(pb, i, h, qi, kj, s, oi, &lse);
+            for (int32_t d = 0; d < D; ++d) g[d] = 0.0;
+            if (b < 0) {
+                for (int32_t d = 0; d < D; ++d) g[d] = NAN;
+                delta[t] = NAN;
+                continue;
+            }
+            load_row(pb->dout, pb->dtype, pb->do_rs, pb->do_hs, i, h, D, doi);
+            const double dlt = dot(doi, oi, D);
+            delta[t] = dlt;
+            const int64_t k0 = pb->cu_k[b], Sk = (int64_t)pb->cu_k[b + 1] - pb->cu_k[b];
+            for (int64_t j = 0; j < Sk; ++j) {
+                const double p = exp(s[j] - lse);
+                load_row(pb->v, pb->dtype, pb->v_rs, pb->v_hs, k0 + j, h, D, kj);
+                const double dp = dot(doi, kj, D);
+                const double ds = p * (dp - dlt);
+                load_row(pb->k, pb->dtype, pb->k_rs, pb->k_hs, k0 + j, h, D, kj);
+                for (int32_t d = 0; d < D; ++d) g[d] += pb->scale * ds * kj[d];
+            }
+        }
+        free(qi); free(kj); free(oi); free(doi); free(s);
+    }
+    return 0;
+}
+
+/*
+ * Backward, key/value side, on selected (kv row, head) pairs:
+ *   dk : [n][D]   scale * sum_i dS_ij q_i
+ *   dv : [n][D]   sum_i P_ij dO_i
+ * dk_j and dv_j need LSE_i and delta_i of every q row i of the segment, so
+ * this first runs the row forward for all q rows of each (segment, head)
+ * touched by the request, then sums over i.  Cost: O(Sq_b * Sk_b * D) per
+ * touched (segment, head).
+ */
+int oracle_bwd_kv(const oracle_problem *pb, int64_t n, const int64_t *rows,
+                  const int32_t *heads, double *dk, double *dv) {
+    const int32_t D = pb->head_dim, B = pb->batch, H = pb->num_heads;
+    const int64_t smax = max_seg_len(pb->cu_k, B);
+    int32_t *seg = malloc(sizeof(int32_t) * (n > 0 ? n : 1));
+    /* stats[b*H + h]: LSE_i and delta_i for all q rows of segment b, head h. */
+    double **st_lse = calloc((size_t)B * H, sizeof(double *));
+    double **st_dlt = calloc((size_t)B * H, sizeof(double *));
+    for (int64_t t = 0; t < n; ++t) {
+        seg[t] = segment_of(pb->cu_k, B, rows[t]);
+        if (seg[t] < 0 || heads[t] < 0 || heads[t] >= H) { seg[t] = -1; continue; }
+        const int64_t x = (int64_t)seg[t] * H + heads[t];
+        if (st_lse[x]) continue;
+        const int32_t b = seg[t], h = heads[t];
+        const int64_t q0 = pb->cu_q[b], Sq = (int64_t)pb->cu_q[b + 1] - pb->cu_q[b];
+        double *L = malloc(sizeof(double) * (Sq > 0 ? Sq : 1));
+        double *E = malloc(sizeof(double) * (Sq > 0 ? Sq : 1));
+        st_lse[x] = L;
+        st_dlt[x] = E;
+#pragma omp parallel
+        {
+            double *qi = malloc(sizeof(double) * D), *kj = malloc(sizeof(double) * D);
+            double *oi = malloc(sizeof(double) * D), *doi = malloc(sizeof(double) * D);
+            double *s = malloc(sizeof(double) * smax);
+#pragma omp for schedule(dynamic, 8)
+            for (int64_t ii = 0; ii < Sq; ++ii) {
+                row_forward(pb, q0 + ii, h, qi, kj, s, oi, &L[ii]);
+                load_row(pb->dout, pb->dtype, pb->do_rs, pb->do_hs, q0 + ii, h, D, doi);
+                E[ii] = dot(doi, oi, D);
+            }
+            free(qi); free(kj); free(oi); free(doi); free(s);
+        }
+    }
+#pragma omp parallel
+    {
+        double *qi = malloc(sizeof(double) * D), *kj = malloc(sizeof(double) * D);
+        double *vj = malloc(sizeof(double) * D), *doi = malloc(sizeof(double) * D);
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t t = 0; t < n; ++t) {
+            const int64_t j = rows[t];
+            const int32_t h = heads[t], b = seg[t];
+            double *gk = dk + t * D, *gv = dv + t * D;
+            for (int32_t d = 0; d < D; ++d) gk[d] = gv[d] = 0.0;
+            if (b < 0) {
+                for (int32_t d = 0; d < D; ++d) gk[d] = gv[d] = NAN;
+                continue;
+            }
+            const double *L = st_lse[(int64_t)b * H + h], *E = st_dlt[(int64_t)b * H + h];
+            load_row(pb->k, pb->dtype, pb->k_rs, pb->k_hs, j, h, D, kj);
+            load_row(pb->v, pb->dtype, pb->v_rs, pb->v_hs, j, h, D, vj);
+            const int64_t q0 = pb->cu_q[b], Sq = (int64_t)pb->cu_q[b + 1] - pb->cu_q[b];
+            for (int64_t ii = 0; ii < Sq; ++ii) {
+                load_row(pb->q, pb->dtype, pb->q_rs, pb->q_hs, q0 + ii, h, D, qi);
+                load_row(pb->dout, pb->dtype, pb->do_rs, pb->do_hs, q0 + ii, h, D, doi);
+                const double sij = pb->scale * dot(qi, kj, D);
+                const double p = exp(sij - L[ii]);
+                const double dp = dot(doi, vj, D);
+                const double ds = p * (dp - E[ii]);
+                for (int32_t d = 0; d < D; ++d) {
+                    gv[d] += p * doi[d];
+                    gk[d] += pb->scale * ds * qi[d];
+                }
+            }
+        }
+        free(qi); free(kj); free(vj); free(doi);
+    }
+    for (int64_t x = 0; x < (int64_t)B * H; ++x) { free(st_lse[x]); free(st_dlt[x]); }
+    free(st_lse); free(st_dlt); free(seg);
+    return 0;
+}
+
+/* Number of OpenMP threads a parallel region of this library uses. */
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
