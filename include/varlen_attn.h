@@ -1,0 +1,168 @@
+/*
+ * varlen_attn.h -- C ABI of libvarlen_attn: packed variable-length
+ * (cu_seqlens) multi-head scaled-dot-product attention, forward and backward,
+ * in bf16 with fp32 accumulation, for one NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the packed "varlen" attention of flash_attn_varlen_func
+ * as called on the flash-attention issue pages:
+ *   - "[FA4][SM120] flash_attn_varlen_func / flash_attn_func illegal memory
+ *     access at >=4 varlen segments", section "Bug 2 details" (packed q with
+ *     cu_seqlens_q = [0, 4032, ..., 35280], 17580 kv rows per window, H=56,
+ *     D=128, max_seqlen_q / max_seqlen_k, non-causal), and
+ *   - "[FA4] cute varlen backward: int32 overflow in _bwd_preprocess corrupts
+ *     dQ/dK/dV when dout has a large outer stride", sections "Summary" and
+ *     "Minimal repro" (cu_seqlens_q = cu_seqlens_k, causal=False, gradients
+ *     dQ/dK/dV for an upstream dout whose row stride exceeds H*D).
+ *
+ * For every segment b (q rows [cu_q[b], cu_q[b+1]), kv rows [cu_k[b],
+ * cu_k[b+1])) and head h:
+ *     O_b  = softmax(scale * Q_b K_b^T) V_b,
+ *     LSE  = natural-log log-sum-exp of each score row (-inf for a segment
+ *            with no keys, whose O rows are 0),
+ * and the backward returns dQ, dK, dV of sum(O * dO).
+ *
+ * Conventions shared by every entry point
+ *   Layout.  Every q/k/v/out/dout/dq/dk/dv tensor is "NHD": element (row r,
+ *     head h, dim d) lives at  base + r*stride.row + h*stride.head + d
+ *     (bf16 elements, int64 strides, innermost stride 1).  Row and head
+ *     strides are arbitrary non-negative multiples of 8 elements (16 bytes)
+ *     and base pointers are 16-byte aligned; no tensor is ever copied to make
+ *     it contiguous.  All offset arithmetic is 64-bit, so strides times rows
+ *     may exceed 2^31 elements.
+ *   cu_seqlens_q / cu_seqlens_k: device int32 arrays of batch+1 entries.  The
+ *     host never reads them (no synchronisation); device code clamps every
+ *     entry into [0, total] and never reads index > batch.  Empty segments
+ *     (length 0) are allowed anywhere.
+ *   max_seqlen_q / max_seqlen_k: advisory only, never trusted for
+ *     correctness (a caller that passes a too-small value gets the same
+ *     result).
+ *   lse: fp32, [num_heads, total_q] contiguous (lse[h*total_q + row]).
+ *   head_dim: 64, 96 or 128.  scale: finite and > 0.
+ *   Ownership: every buffer belongs to the caller; the library allocates no
+ *     device memory and keeps only a per-device attribute cache and one
+ *     device error word.
+ *   Streams: `stream` is a cudaStream_t (NULL = legacy default stream).
+ *     Work is enqueued asynchronously; argument errors are returned
+ *     synchronously before anything is enqueued.
+ *   Device-side failures (a bounded wait that timed out) are recorded in a
+ *     device error word; varlen_attn_get_device_status reads it.
+ */
+#ifndef VARLEN_ATTN_H_
+#define VARLEN_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  VARLEN_OK = 0,
+  VARLEN_ERR_NULL = -1,          /* a required pointer is NULL                  */
+  VARLEN_ERR_SHAPE = -2,         /* batch / totals / heads / scale out of range */
+  VARLEN_ERR_HEAD_DIM = -3,      /* head_dim not in {64, 96, 128}               */
+  VARLEN_ERR_ALIGN = -4,         /* base pointer not 16-byte aligned            */
+  VARLEN_ERR_STRIDE = -5,        /* stride negative, not a multiple of 8, too
+                                    large for a TMA descriptor (>= 2^40 bytes) */
+  VARLEN_ERR_WORKSPACE = -6,     /* workspace NULL, misaligned or too small     */
+  VARLEN_ERR_CUDA = -7,          /* a CUDA runtime/driver call failed           */
+  VARLEN_ERR_TIMEOUT = -8,       /* a device-side bounded wait gave up          */
+  VARLEN_ERR_DEVICE_BOUNDS = -9, /* a device-side bounds check failed           */
+  VARLEN_ERR_ARCH = -10          /* current device is not sm_103                 */
+} varlen_status;
+
+/* Row and head strides of one NHD tensor, in elements. */
+typedef struct {
+  int64_t row;
+  int64_t head;
+} varlen_stride;
+
+/*
+ * Forward.  Writes out[total_q, H, D] (bf16, its own strides) and
+ * lse[H, total_q] (fp32).  Rows of a segment with no keys get O = 0 and
+ * LSE = -inf.  Rows of out outside every segment, and padding between rows,
+ * are not written.
+ */
+int varlen_attn_fwd(const void* q, varlen_stride sq, const void* k, varlen_stride sk, const void* v,
+                    varlen_stride sv, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t batch,
+                    int32_t total_q, int32_t total_k, int32_t num_heads, int32_t head_dim, int32_t max_seqlen_q,
+                    int32_t max_seqlen_k, float scale, void* out, varlen_stride so, float* lse, void* stream);
+
+/*
+ * Bytes of device workspace varlen_attn_bwd needs (256-byte aligned base).
+ * It holds the fp32 dQ accumulator ([total_q, H, D] floats) and the per-row
+ * delta and log2-domain LSE ([H, total_q] floats each), each region rounded
+ * up to 256 bytes.  Returns 0 for negative arguments.
+ */
+size_t varlen_attn_bwd_workspace_size(int32_t batch, int32_t total_q, int32_t num_heads, int32_t head_dim);
+
+/*
+ * Backward.  Given q, k, v, the forward's out and lse, and the upstream
+ * gradient dout (each with its own strides), writes dq[total_q,H,D],
+ * dk[total_k,H,D], dv[total_k,H,D] (bf16, their own strides).  Segments with
+ * no queries get dK = dV = 0; segments with no keys get dQ = 0.
+ * Three kernels on `stream`: delta preprocess (delta = rowsum(dO * O)),
+ * the main dQ/dK/dV kernel, and the dQ conversion.  `workspace` is
+ * caller-owned scratch of at least varlen_attn_bwd_workspace_size() bytes;
+ * its contents on entry do not matter.
+ */
+int varlen_attn_bwd(const void* q, varlen_stride sq, const void* k, varlen_stride sk, const void* v,
+                    varlen_stride sv, const void* out, varlen_stride so, const void* dout, varlen_stride sdo,
+                    const float* lse, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t batch,
+                    int32_t total_q, int32_t total_k, int32_t num_heads, int32_t head_dim, int32_t max_seqlen_q,
+                    int32_t max_seqlen_k, float scale, void* dq, varlen_stride sdq, void* dk, varlen_stride sdk,
+                    void* dv, varlen_stride sdv, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word:
+ * VARLEN_OK, VARLEN_ERR_TIMEOUT, VARLEN_ERR_DEVICE_BOUNDS, or VARLEN_ERR_CUDA
+ * if the stream itself reports an error.
+ */
+int varlen_attn_get_device_status(void* stream);
+
+/* Static description of a status code. */
+const char* varlen_attn_status_string(int status);
+
+/* ---------------------------------------------------------------------------
+ * Diagnostics (host logic and scheduler checks; not needed for normal use).
+ */
+
+/*
+ * Exact tile count of the varlen grid: num_heads * sum_b ceil(len_b / tile)
+ * for a HOST copy of cu_seqlens (batch+1 entries, clamped to [0, total] like
+ * the device does).  This is the count the persistent kernels walk; the
+ * "[FA4][SM120] ... >=4 varlen segments" issue (section "Interpretation")
+ * shows the over-provisioned alternative.  Returns -1 on bad arguments.
+ */
+int64_t varlen_attn_tile_count(const int32_t* cu_seqlens_host, int32_t batch, int32_t total, int32_t num_heads,
+                               int32_t tile);
+
+/*
+ * Runs the device tile scheduler alone with `grid` persistent CTAs and writes
+ * one record per visited tile into out_records (device int32, 4 per tile:
+ * segment, row-block, head, cta).  Records are written at their global tile
+ * index; records at index >= max_records are dropped.  Callers compare the
+ * records against varlen_attn_tile_count.  `tile` is the row-block height.
+ */
+int varlen_attn_debug_schedule(const int32_t* cu_seqlens, int32_t batch, int32_t total, int32_t num_heads,
+                               int32_t tile, int32_t grid, int32_t* out_records, int64_t max_records,
+                               void* stream);
+
+/*
+ * Failure-detection self test: launches one CTA whose bounded mbarrier wait
+ * is never satisfied, with a budget of budget_ns nanoseconds.  The kernel
+ * records VARLEN_ERR_TIMEOUT and returns; read it with
+ * varlen_attn_get_device_status.
+ */
+int varlen_attn_selftest_wait_timeout(uint64_t budget_ns, void* stream);
+
+/* Number of streaming multiprocessors the persistent kernels size their grid
+ * by on the current device (cached). Returns <= 0 on failure. */
+int varlen_attn_num_sms(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VARLEN_ATTN_H_ */

@@ -1,0 +1,314 @@
+// varlen_api.cu -- the C ABI of libvarlen_attn (declared in varlen_attn.h):
+// argument validation, 64-bit TMA descriptor encoding, grid sizing, launch,
+// and the device status word.
+//
+// Lessons from the pages built in here:
+//   * Every stride and extent handed to a TMA descriptor is computed in
+//     64-bit (the "NVFP4 sm_120 persist-D path" pull request on ffpa-attn,
+//     sections "Error" and "Root cause": int32 layout extents wrapped and the
+//     descriptor's stride assertion aborted).  Strides are checked against
+//     the real hardware limit (2^40 bytes) instead.
+//   * Every operand, dout included, keeps its own row / head strides; nothing
+//     is made contiguous ("[FA4] cute varlen backward: int32 overflow in
+//     _bwd_preprocess", sections "Root cause" and "User-side workaround").
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "varlen_attn.h"
+#include "varlen_internal.h"
+
+namespace varlen {
+
+__device__ unsigned int g_device_error = 0;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+struct DeviceInfo {
+  int sms = 0;
+  int major = 0, minor = 0;
+  unsigned int* err = nullptr;  // device address of g_device_error
+};
+
+constexpr int kMaxDevices = 64;
+
+// Per-device attribute cache (the only host state of the library).
+int device_info(DeviceInfo* out) {
+  static DeviceInfo cache[kMaxDevices];
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return VARLEN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev].sms == 0) {
+    DeviceInfo d;
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return VARLEN_ERR_CUDA;
+    if (d.major == 10 && d.minor == 3 &&
+        cudaGetSymbolAddress(reinterpret_cast<void**>(&d.err), g_device_error) != cudaSuccess)
+      return VARLEN_ERR_CUDA;
+    cache[dev] = d;
+  }
+  *out = cache[dev];
+  if (out->major != 10 || out->minor != 3) return VARLEN_ERR_ARCH;
+  return VARLEN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Validates one NHD operand (pointer, strides) of `rows` rows.
+int check_operand(const void* ptr, varlen_stride s, int64_t rows, int32_t H, int32_t D) {
+  if (rows > 0 && ptr == nullptr) return VARLEN_ERR_NULL;
+  if (ptr != nullptr && !aligned16(ptr)) return VARLEN_ERR_ALIGN;
+  if (s.row < 0 || s.head < 0 || (s.row & 7) != 0 || (s.head & 7) != 0) return VARLEN_ERR_STRIDE;
+  // Highest element touched must be addressable with a 64-bit offset, and
+  // each byte stride must fit the TMA descriptor's 40-bit field.
+  if (s.row >= (int64_t(1) << 39) || s.head >= (int64_t(1) << 39)) return VARLEN_ERR_STRIDE;
+  (void)H;
+  (void)D;
+  return VARLEN_OK;
+}
+
+// A 3-D bf16 tensor map {D, H, rows} with byte strides {2*head, 2*row} and a
+// {64, 1, box_rows} box in the 128-byte swizzle.  All arithmetic is 64-bit.
+int encode_nhd(CUtensorMap* map, const void* base, varlen_stride s, int64_t rows, int32_t H, int32_t D,
+               int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return VARLEN_ERR_CUDA;
+  // A stride over a dimension of extent 1 is never used; give it a legal value.
+  int64_t hs = (H > 1) ? s.head : (int64_t)D;
+  int64_t rs = (rows > 1) ? s.row : (int64_t)H * hs;
+  if (hs == 0 || rs == 0) return VARLEN_ERR_STRIDE;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)(rows > 0 ? rows : 1)};
+  cuuint64_t strides[2] = {(cuuint64_t)hs * 2u, (cuuint64_t)rs * 2u};
+  cuuint32_t box[3] = {64u, 1u, (cuuint32_t)box_rows};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  // A zero-row operand is never loaded, but the descriptor needs an address.
+  static const uint4 dummy_host = {0, 0, 0, 0};
+  void* addr = const_cast<void*>(base != nullptr ? base : static_cast<const void*>(&dummy_host));
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, addr, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? VARLEN_OK : VARLEN_ERR_STRIDE;
+}
+
+int check_common(const int32_t* cu_q, const int32_t* cu_k, int32_t batch, int32_t total_q, int32_t total_k,
+                 int32_t H, int32_t D, float scale) {
+  if (cu_q == nullptr || cu_k == nullptr) return VARLEN_ERR_NULL;
+  if (batch < 1 || total_q < 0 || total_k < 0 || H < 1) return VARLEN_ERR_SHAPE;
+  if (D != 64 && D != 96 && D != 128) return VARLEN_ERR_HEAD_DIM;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return VARLEN_ERR_SHAPE;
+  // H*total fits comfortably in int64; H itself bounded for TMA (<= 2^32).
+  return VARLEN_OK;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+}  // namespace varlen
+
+using namespace varlen;
+
+extern "C" int varlen_attn_fwd(const void* q, varlen_stride sq, const void* k, varlen_stride sk, const void* v,
+                               varlen_stride sv, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                               int32_t batch, int32_t total_q, int32_t total_k, int32_t num_heads, int32_t head_dim,
+                               int32_t max_seqlen_q, int32_t max_seqlen_k, float scale, void* out,
+                               varlen_stride so, float* lse, void* stream) {
+  (void)max_seqlen_q;  // advisory only: the kernels derive lengths from cu_seqlens
+  (void)max_seqlen_k;
+  int st = check_common(cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads, head_dim, scale);
+  if (st != VARLEN_OK) return st;
+  if ((st = check_operand(q, sq, total_q, num_heads, head_dim)) != VARLEN_OK) return st;
+  if ((st = check_operand(k, sk, total_k, num_heads, head_dim)) != VARLEN_OK) return st;
+  if ((st = check_operand(v, sv, total_k, num_heads, head_dim)) != VARLEN_OK) return st;
+  if ((st = check_operand(out, so, total_q, num_heads, head_dim)) != VARLEN_OK) return st;
+  if (total_q > 0 && lse == nullptr) return VARLEN_ERR_NULL;
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != VARLEN_OK) return st;
+  if (total_q == 0) return VARLEN_OK;
+  FwdLaunch L;
+  std::memset(&L, 0, sizeof(L));
+  if ((st = encode_nhd(&L.tm_q, q, sq, total_q, num_heads, head_dim, kTileM)) != VARLEN_OK) return st;
+  if ((st = encode_nhd(&L.tm_k, k, sk, total_k, num_heads, head_dim, kTileN)) != VARLEN_OK) return st;
+  if ((st = encode_nhd(&L.tm_v, v, sv, total_k, num_heads, head_dim, kTileN)) != VARLEN_OK) return st;
+  L.p.out = static_cast<__nv_bfloat16*>(out);
+  L.p.o_rs = so.row;
+  L.p.o_hs = so.head;
+  L.p.lse = lse;
+  L.p.cu_q = cu_seqlens_q;
+  L.p.cu_k = cu_seqlens_k;
+  L.p.batch = batch;
+  L.p.total_q = total_q;
+  L.p.total_k = total_k;
+  L.p.num_heads = num_heads;
+  L.p.scale_log2 = scale * kLog2e;
+  L.p.err = dev.err;
+  L.head_dim = head_dim;
+  L.grid = dev.sms;
+  cudaError_t e = launch_fwd(L, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? VARLEN_OK : VARLEN_ERR_CUDA;
+}
+
+extern "C" size_t varlen_attn_bwd_workspace_size(int32_t batch, int32_t total_q, int32_t num_heads,
+                                                 int32_t head_dim) {
+  if (batch < 0 || total_q < 0 || num_heads < 0 || head_dim < 0) return 0;
+  const size_t rows = (size_t)total_q;
+  return round256(rows * num_heads * head_dim * sizeof(float)) + 2 * round256(rows * num_heads * sizeof(float));
+}
+
+extern "C" int varlen_attn_bwd(const void* q, varlen_stride sq, const void* k, varlen_stride sk, const void* v,
+                               varlen_stride sv, const void* out, varlen_stride so, const void* dout,
+                               varlen_stride sdo, const float* lse, const int32_t* cu_seqlens_q,
+                               const int32_t* cu_seqlens_k, int32_t batch, int32_t total_q, int32_t total_k,
+                               int32_t num_heads, int32_t head_dim, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                               float scale, void* dq, varlen_stride sdq, void* dk, varlen_stride sdk, void* dv,
+                               varlen_stride sdv, void* workspace, size_t workspace_bytes, void* stream) {
+  (void)max_seqlen_q;
+  (void)max_seqlen_k;
+  int st = check_common(cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads, head_dim, scale);
+  if (st != VARLEN_OK) return st;
+  if ((st = check_operand(q, sq, total_q, num_heads, head_dim)) != VARLEN_OK) return st;
+  if ((st = check_operand(k, sk, total_k, num_heads, head_dim)) != VARLEN_OK) return st;
+  if ((st = check_operand(v, sv, total_k, num_heads, head_dim)) != VARLEN_OK) return st;
+  if ((st = check_operand(out, so, total_q, num_heads, head_dim)) != VARLEN_OK) return st;
+  if ((st = check_operand(dout, sdo, total_q, num_heads, head_dim)) != VARLEN_OK) return st;
+  if ((st = check_operand(dq, sdq, total_q, num_heads, head_dim)) != VARLEN_OK) return st;
+  if ((st = check_operand(dk, sdk, total_k, num_heads, head_dim)) != VARLEN_OK) return st;
+  if ((st = check_operand(dv, sdv, total_k, num_heads, head_dim)) != VARLEN_OK) return st;
+  if (total_q > 0 && lse == nullptr) return VARLEN_ERR_NULL;
+  const size_t need = varlen_attn_bwd_workspace_size(batch, total_q, num_heads, head_dim);
+  if (need > 0 && (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+                   workspace_bytes < need))
+    return VARLEN_ERR_WORKSPACE;
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != VARLEN_OK) return st;
+  if (total_q == 0 && total_k == 0) return VARLEN_OK;
+  BwdLaunch L;
+  std::memset(&L, 0, sizeof(L));
+  if ((st = encode_nhd(&L.tm_q, q, sq, total_q, num_heads, head_dim, kBwdTileQ)) != VARLEN_OK) return st;
+  if ((st = encode_nhd(&L.tm_do, dout, sdo, total_q, num_heads, head_dim, kBwdTileQ)) != VARLEN_OK) return st;
+  if ((st = encode_nhd(&L.tm_k, k, sk, total_k, num_heads, head_dim, kTileM)) != VARLEN_OK) return st;
+  if ((st = encode_nhd(&L.tm_v, v, sv, total_k, num_heads, head_dim, kTileM)) != VARLEN_OK) return st;
+  char* ws = static_cast<char*>(workspace);
+  float* dq_acc = reinterpret_cast<float*>(ws);
+  float* delta = reinterpret_cast<float*>(ws + round256((size_t)total_q * num_heads * head_dim * sizeof(float)));
+  float* lse2 = reinterpret_cast<float*>(reinterpret_cast<char*>(delta) +
+                                         round256((size_t)total_q * num_heads * sizeof(float)));
+  L.prep = PrepParams{static_cast<const __nv_bfloat16*>(out), so.row, so.head,
+                      static_cast<const __nv_bfloat16*>(dout), sdo.row, sdo.head,
+                      lse, delta, lse2, dq_acc, cu_seqlens_q, batch, total_q, num_heads, head_dim};
+  L.p.dk = static_cast<__nv_bfloat16*>(dk);
+  L.p.dk_rs = sdk.row;
+  L.p.dk_hs = sdk.head;
+  L.p.dv = static_cast<__nv_bfloat16*>(dv);
+  L.p.dv_rs = sdv.row;
+  L.p.dv_hs = sdv.head;
+  L.p.delta = delta;
+  L.p.lse2 = lse2;
+  L.p.dq_acc = dq_acc;
+  L.p.cu_q = cu_seqlens_q;
+  L.p.cu_k = cu_seqlens_k;
+  L.p.batch = batch;
+  L.p.total_q = total_q;
+  L.p.total_k = total_k;
+  L.p.num_heads = num_heads;
+  L.p.scale_log2 = scale * kLog2e;
+  L.p.scale = scale;
+  L.p.err = dev.err;
+  L.post = PostParams{dq_acc, static_cast<__nv_bfloat16*>(dq), sdq.row, sdq.head, cu_seqlens_q, batch,
+                      total_q, num_heads, head_dim, scale};
+  L.head_dim = head_dim;
+  L.grid = dev.sms;
+  cudaError_t e = launch_bwd(L, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? VARLEN_OK : VARLEN_ERR_CUDA;
+}
+
+extern "C" int varlen_attn_get_device_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return VARLEN_ERR_CUDA;
+  unsigned int word = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&word, g_device_error, sizeof(word)) != cudaSuccess) return VARLEN_ERR_CUDA;
+  if (word != 0 && cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero)) != cudaSuccess) return VARLEN_ERR_CUDA;
+  if (word & kErrTimeout) return VARLEN_ERR_TIMEOUT;
+  if (word & kErrBounds) return VARLEN_ERR_DEVICE_BOUNDS;
+  return VARLEN_OK;
+}
+
+extern "C" const char* varlen_attn_status_string(int status) {
+  switch (status) {
+    case VARLEN_OK: return "ok";
+    case VARLEN_ERR_NULL: return "required pointer is NULL";
+    case VARLEN_ERR_SHAPE: return "batch, totals, heads or scale out of range";
+    case VARLEN_ERR_HEAD_DIM: return "head_dim must be 64, 96 or 128";
+    case VARLEN_ERR_ALIGN: return "base pointer not 16-byte aligned";
+    case VARLEN_ERR_STRIDE: return "stride negative, not a multiple of 8 elements, or too large for TMA";
+    case VARLEN_ERR_WORKSPACE: return "workspace NULL, not 256-byte aligned, or too small";
+    case VARLEN_ERR_CUDA: return "CUDA runtime or driver call failed";
+    case VARLEN_ERR_TIMEOUT: return "device-side bounded wait timed out";
+    case VARLEN_ERR_DEVICE_BOUNDS: return "device-side bounds check failed";
+    case VARLEN_ERR_ARCH: return "current device is not sm_103";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int64_t varlen_attn_tile_count(const int32_t* cu, int32_t batch, int32_t total, int32_t num_heads,
+                                          int32_t tile) {
+  if (cu == nullptr || batch < 0 || total < 0 || num_heads < 0 || tile <= 0) return -1;
+  int64_t n = 0;
+  for (int32_t b = 0; b < batch; ++b) {
+    int64_t a = std::min<int64_t>(std::max<int64_t>(cu[b], 0), total);
+    int64_t e = std::min<int64_t>(std::max<int64_t>(cu[b + 1], 0), total);
+    int64_t len = std::max<int64_t>(e - a, 0);
+    n += (len + tile - 1) / tile;
+  }
+  return n * num_heads;
+}
+
+extern "C" int varlen_attn_debug_schedule(const int32_t* cu, int32_t batch, int32_t total, int32_t num_heads,
+                                          int32_t tile, int32_t grid, int32_t* out, int64_t max_records,
+                                          void* stream) {
+  if (cu == nullptr || out == nullptr) return VARLEN_ERR_NULL;
+  if (batch < 1 || total < 0 || num_heads < 1 || grid < 1 || max_records < 0) return VARLEN_ERR_SHAPE;
+  if (tile != 64 && tile != 128) return VARLEN_ERR_SHAPE;
+  DeviceInfo dev;
+  int st = device_info(&dev);
+  if (st != VARLEN_OK) return st;
+  cudaError_t e = launch_debug_schedule(cu, batch, total, num_heads, tile, grid, out, max_records,
+                                        static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? VARLEN_OK : VARLEN_ERR_CUDA;
+}
+
+extern "C" int varlen_attn_selftest_wait_timeout(uint64_t budget_ns, void* stream) {
+  DeviceInfo dev;
+  int st = device_info(&dev);
+  if (st != VARLEN_OK) return st;
+  cudaError_t e = launch_selftest_timeout(budget_ns, dev.err, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? VARLEN_OK : VARLEN_ERR_CUDA;
+}
+
+extern "C" int varlen_attn_num_sms(void) {
+  DeviceInfo dev;
+  int st = device_info(&dev);
+  if (st != VARLEN_OK && st != VARLEN_ERR_ARCH) return st;
+  return dev.sms;
+}

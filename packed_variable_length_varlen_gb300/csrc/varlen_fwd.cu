@@ -1,0 +1,396 @@
+// varlen_fwd.cu -- forward kernel of packed variable-length attention on
+// sm_103a: persistent exact tile scheduler, TMA-fed Q tile and K/V ring,
+// tcgen05 MMAs with TMEM accumulators, warp-specialised online softmax.
+//
+// Per CTA (256 threads, one CTA per SM):
+//   warp 0       TMA producer: Q tile, then K_j, V_j tiles into a ring of
+//                shared-memory slots (mbarrier full/empty per slot).
+//   warp 1       MMA issuer (one lane): S_j = Q K_j^T into one of three TMEM
+//                score buffers, then O += P_{j-1} V_{j-1} with P read from
+//                TMEM.  Owns the TMEM allocation.
+//   warps 4..7   softmax / correction / epilogue: thread = one q row = one
+//                TMEM lane.  Masks key columns past the segment end, keeps
+//                the running max m and sum l, writes P = exp2(S*c - m) back
+//                into TMEM as bf16 (aliasing S), rescales O in TMEM when m
+//                grows by more than 2^8 (exact: O and l carry the same
+//                factor), and finally writes O / l (bf16) and LSE.
+//   warps 2,3    idle.
+//
+// Semantics: O = softmax(scale * Q_b K_b^T) V_b per segment b, with the
+// natural-log LSE per row -- the varlen attention called on the
+// "[FA4][SM120] flash_attn_varlen_func ... >=4 varlen segments" issue (section
+// "Bug 2 details").  Differences from the kernels on the pages: the tile
+// count is exact (no tail blocks), no global load is issued before a tile is
+// known to exist, and all row offsets are 64-bit.
+#include "sm103_ptx.cuh"
+#include "varlen_internal.h"
+#include "varlen_sched.cuh"
+
+namespace varlen {
+
+template <int D>
+struct FwdCfg {
+  static constexpr int NC = (D + 63) / 64;              // 64-column chunks of a tile
+  static constexpr int CHUNK = 128 * 128;               // 128 rows x 128 bytes
+  static constexpr int TILE = NC * CHUNK;               // one Q / K / V tile
+  static constexpr int NSLOT = (NC == 1) ? 10 : 5;      // K/V ring slots
+  static constexpr int NSBUF = 3;                       // TMEM score buffers
+  static constexpr int O_COL = 384;                     // TMEM column of O
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int SMEM_BYTES = 1024 + 1024 + TILE * (1 + NSLOT);
+  static constexpr int KSTEPS = D / 16;                 // K-steps of S = Q K^T
+};
+
+struct FwdBarriers {
+  uint64_t q_full, q_empty;
+  uint64_t s_full[3], s_free[3], p_full[3];
+  uint64_t mma_done;
+  uint64_t kv_full[10], kv_empty[10];
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(FwdBarriers) <= 1024, "barrier block too large");
+
+template <int D>
+__global__ void __launch_bounds__(256, 1)
+    varlen_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  FwdBarriers& bar = *reinterpret_cast<FwdBarriers*>(smem);
+  uint8_t* q_smem = smem + 1024;
+  uint8_t* ring = q_smem + C::TILE;
+  volatile int* abort = &bar.abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar.q_full, 1);
+    mbar_init(&bar.q_empty, 1);
+    for (int i = 0; i < 3; ++i) {
+      mbar_init(&bar.s_full[i], 1);
+      mbar_init(&bar.s_free[i], 1);
+      mbar_init(&bar.p_full[i], 128);
+    }
+    mbar_init(&bar.mma_done, 1);
+    for (int i = 0; i < C::NSLOT; ++i) {
+      mbar_init(&bar.kv_full[i], 1);
+      mbar_init(&bar.kv_empty[i], 1);
+    }
+    bar.abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(&bar.tmem_base, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar.tmem_base;
+
+  const int64_t G = gridDim.x;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      SegCursor c;
+      cursor_init<kTileM>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k);
+      uint32_t q_loads = 0;
+      uint32_t ring_pos = 0;  // loads issued into the ring so far
+      bool ok = true;
+      for (int64_t t = blockIdx.x; ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_q, p.cu_k, p.batch, p.total_q,
+                                                               p.total_k);
+           t += G) {
+        if (c.olen == 0) continue;  // no keys: the softmax role writes O = 0, LSE = -inf
+        const Tile tl = cursor_tile(c, t);
+        const int32_t qrow = c.r0 + tl.m * kTileM;
+        if (q_loads > 0 && !mbar_wait(&bar.q_empty, (q_loads - 1) & 1, abort)) break;
+        mbar_arrive_expect_tx(&bar.q_full, C::TILE);
+#pragma unroll
+        for (int cc = 0; cc < C::NC; ++cc) tma_load_3d(q_smem + cc * C::CHUNK, &tm_q, &bar.q_full, cc * 64, tl.h, qrow);
+        ++q_loads;
+        const int32_t nkv = (c.olen + kTileN - 1) / kTileN;
+        for (int32_t j = 0; ok && j < nkv; ++j) {
+          const int32_t krow = c.o0 + j * kTileN;
+#pragma unroll
+          for (int which = 0; which < 2; ++which) {
+            const uint32_t slot = ring_pos % C::NSLOT;
+            const uint32_t phase = (ring_pos / C::NSLOT) & 1;
+            if (!mbar_wait(&bar.kv_empty[slot], phase ^ 1, abort)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&bar.kv_full[slot], C::TILE);
+            uint8_t* dst = ring + slot * C::TILE;
+            const CUtensorMap* m = which ? &tm_v : &tm_k;
+#pragma unroll
+            for (int cc = 0; cc < C::NC; ++cc) tma_load_3d(dst + cc * C::CHUNK, m, &bar.kv_full[slot], cc * 64, tl.h, krow);
+            ++ring_pos;
+          }
+        }
+      }
+      if (*abort) {
+        // Let every copy already issued land before the CTA's shared memory
+        // can be released (bounded; a copy that never lands is reported).
+        for (uint32_t s = 0; s < C::NSLOT && s < ring_pos; ++s) {
+          const uint32_t last = ring_pos - 1 - ((ring_pos - 1 - s) % C::NSLOT);
+          int dummy = 0;
+          mbar_wait(&bar.kv_full[s], (last / C::NSLOT) & 1, &dummy, 100000000ull);
+        }
+        if (q_loads > 0) {
+          int dummy = 0;
+          mbar_wait(&bar.q_full, (q_loads - 1) & 1, &dummy, 100000000ull);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, false, true);
+    SegCursor c;
+    cursor_init<kTileM>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k);
+    uint32_t tiles = 0, g = 0, ring0 = 0;
+    const uint32_t q_base = smem_addr(q_smem);
+    const uint32_t ring_base = smem_addr(ring);
+    bool ok = true;
+    for (int64_t t = blockIdx.x;
+         ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k); t += G) {
+      if (c.olen == 0) continue;
+      if (!mbar_wait(&bar.q_full, tiles & 1, abort)) break;
+      ++tiles;
+      tc_fence_after();
+      const int32_t nkv = (c.olen + kTileN - 1) / kTileN;
+      for (int32_t j = 0; j <= nkv; ++j) {
+        if (j < nkv) {
+          // S_j = Q K_j^T into score buffer (g+j) % 3
+          const uint32_t gj = g + j;
+          const uint32_t sb = gj % C::NSBUF;
+          const uint32_t kpos = ring0 + 2 * j;
+          const uint32_t kslot = kpos % C::NSLOT;
+          if (!mbar_wait(&bar.kv_full[kslot], (kpos / C::NSLOT) & 1, abort)) { ok = false; break; }
+          if (gj >= C::NSBUF && !mbar_wait(&bar.s_free[sb], ((gj / C::NSBUF) - 1) & 1, abort)) { ok = false; break; }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t kaddr = ring_base + kslot * C::TILE;
+#pragma unroll
+            for (int kk = 0; kk < C::KSTEPS; ++kk) {
+              const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
+              mma_ss(tmem + sb * 128, sw128_desc(q_base + off, 16, 1024), sw128_desc(kaddr + off, 16, 1024), kIdescS,
+                     kk > 0);
+            }
+            mma_commit(&bar.s_full[sb]);
+            mma_commit(&bar.kv_empty[kslot]);
+            if (j == nkv - 1) mma_commit(&bar.q_empty);
+          }
+          __syncwarp();
+        }
+        if (j >= 1) {
+          // O += P_{j-1} V_{j-1}
+          const int32_t jj = j - 1;
+          const uint32_t gj = g + jj;
+          const uint32_t sb = gj % C::NSBUF;
+          const uint32_t vpos = ring0 + 2 * jj + 1;
+          const uint32_t vslot = vpos % C::NSLOT;
+          if (!mbar_wait(&bar.p_full[sb], (gj / C::NSBUF) & 1, abort)) { ok = false; break; }
+          if (!mbar_wait(&bar.kv_full[vslot], (vpos / C::NSLOT) & 1, abort)) { ok = false; break; }
+          const int32_t kv_valid = c.olen - jj * kTileN;
+          uint8_t* vtile = ring + vslot * C::TILE;
+          if (kv_valid < kTileN) {
+            // Rows past the segment end hold the next segment's values (or
+            // TMA zero fill).  P is 0 there, but 0 * NaN would still poison
+            // O, so clear those rows before the MMA reads them.
+            for (int r = kv_valid + lane; r < kTileN; r += 32) {
+#pragma unroll
+              for (int cc = 0; cc < C::NC; ++cc) {
+                uint4* row = reinterpret_cast<uint4*>(vtile + cc * C::CHUNK + r * 128);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) row[u] = make_uint4(0, 0, 0, 0);
+              }
+            }
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t vaddr = smem_addr(vtile);
+#pragma unroll
+            for (int kk = 0; kk < kTileN / 16; ++kk) {
+              mma_ts(tmem + C::O_COL, tmem + sb * 128 + kk * 8, sw128_desc(vaddr + kk * 2048, C::CHUNK, 1024),
+                     kIdescO, (jj > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(&bar.kv_empty[vslot]);
+            mma_commit(&bar.s_free[sb]);
+          }
+          __syncwarp();
+        }
+      }
+      g += nkv;
+      ring0 += 2 * nkv;
+    }
+    // Drain: every MMA this thread issued completes before TMEM is freed.
+    if (lane == 0) {
+      mma_commit(&bar.mma_done);
+      int dummy = 0;
+      mbar_wait(&bar.mma_done, 0, &dummy);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int row = threadIdx.x - 128;                 // TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
+    const float c2 = p.scale_log2;
+    SegCursor c;
+    cursor_init<kTileM>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k);
+    uint32_t g = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x;
+         ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k); t += G) {
+      const Tile tl = cursor_tile(c, t);
+      const int32_t r_in_seg = tl.m * kTileM + row;
+      const bool row_valid = r_in_seg < c.len;
+      const int64_t grow = (int64_t)c.r0 + r_in_seg;
+      __nv_bfloat16* orow = p.out + grow * p.o_rs + (int64_t)tl.h * p.o_hs;
+      float* lse_out = p.lse + (int64_t)tl.h * p.total_q + grow;
+      if (c.olen == 0) {
+        if (row_valid) {
+#pragma unroll
+          for (int d = 0; d < D; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0, 0, 0, 0);
+          *lse_out = -INFINITY;
+        }
+        continue;
+      }
+      const int32_t nkv = (c.olen + kTileN - 1) / kTileN;
+      float m_use = -INFINITY, l = 0.f;
+      for (int32_t j = 0; j < nkv; ++j) {
+        const uint32_t gj = g + j;
+        const uint32_t sb = gj % C::NSBUF;
+        if (!mbar_wait(&bar.s_full[sb], (gj / C::NSBUF) & 1, abort)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t s[128];
+        {
+          uint32_t(&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[0]);
+          uint32_t(&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[32]);
+          uint32_t(&s2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[64]);
+          uint32_t(&s3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[96]);
+          const uint32_t ta = tmem + lane_off + sb * 128;
+          tmem_ld32(ta + 0, s0);
+          tmem_ld32(ta + 32, s1);
+          tmem_ld32(ta + 64, s2);
+          tmem_ld32(ta + 96, s3);
+          tmem_wait_ld();
+        }
+        float x[128];
+#pragma unroll
+        for (int i = 0; i < 128; ++i) x[i] = __uint_as_float(s[i]);
+        const int32_t kv_valid = c.olen - j * kTileN;
+        if (kv_valid < kTileN) {
+#pragma unroll
+          for (int i = 0; i < 128; ++i) x[i] = (i < kv_valid) ? x[i] : -INFINITY;
+        }
+        float mx = x[0];
+#pragma unroll
+        for (int i = 1; i < 128; ++i) mx = fmaxf(mx, x[i]);
+        const float m_new = fmaxf(m_use, mx * c2);
+        float alpha = 1.f;
+        bool rescale = false;
+        if (j == 0) {
+          m_use = m_new;
+        } else if (m_new > m_use + 8.0f) {
+          alpha = ex2(m_use - m_new);
+          m_use = m_new;
+          rescale = true;
+        }
+        float rs = 0.f;
+        uint32_t pk[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          const float p0 = ex2(fmaf(x[2 * i], c2, -m_use));
+          const float p1 = ex2(fmaf(x[2 * i + 1], c2, -m_use));
+          rs += p0 + p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        l = fmaf(l, alpha, rs);
+        {
+          const uint32_t ta = tmem + lane_off + sb * 128;
+          tmem_st32(ta + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+          tmem_st32(ta + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+          // O must hold P_{j-1} V_{j-1} before it is rescaled.
+          const uint32_t gp = gj - 1;
+          if (!mbar_wait(&bar.s_free[gp % C::NSBUF], (gp / C::NSBUF) & 1, abort)) { ok = false; }
+          tc_fence_after();
+#pragma unroll
+          for (int d0 = 0; d0 < D; d0 += 32) {
+            uint32_t o[32];
+            tmem_ld32(tmem + lane_off + C::O_COL + d0, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tmem + lane_off + C::O_COL + d0, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bar.p_full[sb]);
+        if (!ok) break;
+      }
+      if (!ok) break;
+      // epilogue: wait for the last O += P V, then O / l and LSE
+      const uint32_t gl = g + nkv - 1;
+      if (!mbar_wait(&bar.s_free[gl % C::NSBUF], (gl / C::NSBUF) & 1, abort)) break;
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+#pragma unroll
+      for (int d0 = 0; d0 < D; d0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_off + C::O_COL + d0, o);
+        tmem_wait_ld();
+        if (row_valid) {
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+          uint4* dst = reinterpret_cast<uint4*>(orow + d0);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+      if (row_valid) *lse_out = (m_use + __log2f(l)) * 0.69314718055994531f;
+      tc_fence_before();
+      g += nkv;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+  if (threadIdx.x == 0 && bar.abort) record_error(p.err, kErrTimeout);
+}
+
+template <int D>
+static cudaError_t launch_fwd_d(const FwdLaunch& L, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  auto kern = varlen_fwd_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  kern<<<L.grid, 256, C::SMEM_BYTES, stream>>>(L.tm_q, L.tm_k, L.tm_v, L.p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd(const FwdLaunch& L, cudaStream_t stream) {
+  switch (L.head_dim) {
+    case 64: return launch_fwd_d<64>(L, stream);
+    case 96: return launch_fwd_d<96>(L, stream);
+    case 128: return launch_fwd_d<128>(L, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace varlen

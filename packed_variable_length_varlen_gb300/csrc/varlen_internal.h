@@ -1,0 +1,97 @@
+// varlen_internal.h -- declarations shared by the C-ABI layer and the
+// kernel translation units (not part of the public ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+namespace varlen {
+
+// Bits of the device error word (read and cleared by
+// varlen_attn_get_device_status).
+enum : unsigned int {
+  kErrTimeout = 1u,  // a bounded mbarrier wait gave up
+  kErrBounds = 2u,   // a debug bounds check failed
+};
+
+constexpr int kTileM = 128;  // q rows per forward tile / kv rows per backward tile
+constexpr int kTileN = 128;  // kv rows per forward inner step
+constexpr int kBwdTileQ = 64; // q rows per backward inner step
+
+struct FwdParams {
+  __nv_bfloat16* out;
+  int64_t o_rs, o_hs;
+  float* lse;
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int32_t batch, total_q, total_k, num_heads;
+  float scale_log2;  // softmax scale * log2(e)
+  unsigned int* err; // device error word
+};
+
+struct FwdLaunch {
+  CUtensorMap tm_q, tm_k, tm_v;
+  FwdParams p;
+  int head_dim;
+  int grid;
+};
+
+cudaError_t launch_fwd(const FwdLaunch& L, cudaStream_t stream);
+
+struct PrepParams {
+  const __nv_bfloat16* out;
+  int64_t o_rs, o_hs;
+  const __nv_bfloat16* dout;
+  int64_t do_rs, do_hs;
+  const float* lse;
+  float* delta;     // [H, total_q]
+  float* lse2;      // [H, total_q]
+  float* dq_acc;    // [total_q, H, D]
+  const int32_t* cu_q;
+  int32_t batch, total_q, num_heads, head_dim;
+};
+
+struct BwdParams {
+  __nv_bfloat16* dk;
+  int64_t dk_rs, dk_hs;
+  __nv_bfloat16* dv;
+  int64_t dv_rs, dv_hs;
+  const float* delta;
+  const float* lse2;
+  float* dq_acc;
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int32_t batch, total_q, total_k, num_heads;
+  float scale_log2;  // softmax scale * log2(e)
+  float scale;       // softmax scale (applied to dK)
+  unsigned int* err; // device error word
+};
+
+struct PostParams {
+  const float* dq_acc;
+  __nv_bfloat16* dq;
+  int64_t dq_rs, dq_hs;
+  const int32_t* cu_q;
+  int32_t batch, total_q, num_heads, head_dim;
+  float scale;
+};
+
+struct BwdLaunch {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  PrepParams prep;
+  BwdParams p;
+  PostParams post;
+  int head_dim;
+  int grid;
+};
+
+cudaError_t launch_bwd(const BwdLaunch& L, cudaStream_t stream);
+
+cudaError_t launch_debug_schedule(const int32_t* cu, int32_t batch, int32_t total, int32_t num_heads, int32_t tile,
+                                  int32_t grid, int32_t* out, int64_t max_records, cudaStream_t stream);
+
+cudaError_t launch_selftest_timeout(uint64_t budget_ns, unsigned int* err, cudaStream_t stream);
+
+}  // namespace varlen

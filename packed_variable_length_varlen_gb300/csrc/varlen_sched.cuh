@@ -1,0 +1,88 @@
+// varlen_sched.cuh -- exact persistent tile scheduler for packed varlen work.
+//
+// The work of one launch is the list of tiles
+//     (segment b, row-block m, head h),  m < ceil(len_b / TILE),
+// ordered segment-major, then head, then row-block, so that the tiles of one
+// (segment, head) -- which read the same K/V (forward) or Q/dO (backward)
+// rows -- are adjacent and run concurrently on neighbouring CTAs, sharing
+// those rows through L2.  There are exactly H * sum_b ceil(len_b / TILE)
+// tiles: nothing is over-provisioned, so no CTA ever decodes a tile that does
+// not exist (the failure described on the "[FA4][SM120] flash_attn_varlen_func
+// ... illegal memory access at >=4 varlen segments" issue, sections
+// "Interpretation" and "Practical workaround": a grid of 15840 blocks for
+// 15680 valid tiles whose tail blocks read cu_seqlens past its end).
+//
+// CTA c of G visits global tiles c, c+G, c+2G, ...; since that sequence
+// increases, each role of the CTA walks the segments with a forward-only
+// cursor and reads cu_seqlens[b], cu_seqlens[b+1] for b < batch only.  Every
+// cu_seqlens entry is clamped into [0, total] before use, so a malformed
+// array cannot produce an out-of-range row.
+#pragma once
+
+#include <cstdint>
+
+namespace varlen {
+
+struct SegCursor {
+  int32_t b;        // current segment
+  int64_t first;    // global index of segment b's first tile
+  int32_t nb;       // row-blocks per head in segment b (on the scheduled side)
+  int32_t r0, len;  // scheduled side: first row and length of segment b
+  int32_t o0, olen; // other side: first row and length of segment b
+};
+
+__device__ __forceinline__ int32_t clamp_row(int32_t v, int32_t total) { return min(max(v, 0), total); }
+
+template <int TILE>
+__device__ __forceinline__ void cursor_load(SegCursor& c, const int32_t* __restrict__ cu_s,
+                                            const int32_t* __restrict__ cu_o, int32_t total_s, int32_t total_o) {
+  const int32_t a = clamp_row(__ldg(cu_s + c.b), total_s);
+  const int32_t e = clamp_row(__ldg(cu_s + c.b + 1), total_s);
+  c.r0 = a;
+  c.len = max(e - a, 0);
+  const int32_t ao = clamp_row(__ldg(cu_o + c.b), total_o);
+  const int32_t eo = clamp_row(__ldg(cu_o + c.b + 1), total_o);
+  c.o0 = ao;
+  c.olen = max(eo - ao, 0);
+  c.nb = (c.len + TILE - 1) / TILE;
+}
+
+template <int TILE>
+__device__ __forceinline__ void cursor_init(SegCursor& c, const int32_t* cu_s, const int32_t* cu_o, int32_t batch,
+                                            int32_t total_s, int32_t total_o) {
+  c.b = 0;
+  c.first = 0;
+  c.nb = 0;
+  c.r0 = c.len = c.o0 = c.olen = 0;
+  if (batch > 0) cursor_load<TILE>(c, cu_s, cu_o, total_s, total_o);
+}
+
+// Moves the cursor to the segment holding global tile t (t never decreases
+// between calls).  Returns false when t is past the last tile.
+template <int TILE>
+__device__ __forceinline__ bool cursor_seek(SegCursor& c, int64_t t, int32_t num_heads, const int32_t* cu_s,
+                                            const int32_t* cu_o, int32_t batch, int32_t total_s, int32_t total_o) {
+  while (c.b < batch) {
+    const int64_t span = (int64_t)num_heads * c.nb;
+    if (t < c.first + span) return true;
+    c.first += span;
+    ++c.b;
+    if (c.b < batch) cursor_load<TILE>(c, cu_s, cu_o, total_s, total_o);
+  }
+  return false;
+}
+
+struct Tile {
+  int32_t b, m, h;
+};
+
+__device__ __forceinline__ Tile cursor_tile(const SegCursor& c, int64_t t) {
+  const int64_t local = t - c.first;
+  Tile x;
+  x.b = c.b;
+  x.h = (int32_t)(local / c.nb);
+  x.m = (int32_t)(local - (int64_t)x.h * c.nb);
+  return x;
+}
+
+}  // namespace varlen

@@ -1,0 +1,196 @@
+"""Python binding of libvarlen_attn (the C ABI in include/varlen_attn.h).
+
+Argument marshalling only: torch tensors become device pointers and int64
+(row, head) strides, streams become cudaStream_t handles.  Every step of the
+computation runs in the library's CUDA kernels; there is no fallback.  If the
+library is missing or cannot be loaded, importing this module raises.
+
+The raw entry points keep the C names (``varlen_attn_fwd`` ...) and return
+the C status code.  ``attention_fwd`` / ``attention_bwd`` are conveniences
+that allocate outputs / workspace with torch on the inputs' device and raise
+``VarlenError`` on a non-zero status.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+VARLEN_OK = 0
+VARLEN_ERR_NULL = -1
+VARLEN_ERR_SHAPE = -2
+VARLEN_ERR_HEAD_DIM = -3
+VARLEN_ERR_ALIGN = -4
+VARLEN_ERR_STRIDE = -5
+VARLEN_ERR_WORKSPACE = -6
+VARLEN_ERR_CUDA = -7
+VARLEN_ERR_TIMEOUT = -8
+VARLEN_ERR_DEVICE_BOUNDS = -9
+VARLEN_ERR_ARCH = -10
+
+
+class VarlenStride(ctypes.Structure):
+    _fields_ = [("row", ctypes.c_int64), ("head", ctypes.c_int64)]
+
+
+class VarlenError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__("%s failed: %d (%s)" % (where, status, varlen_attn_status_string(status)))
+        self.status = status
+
+
+def _load() -> ctypes.CDLL:
+    path = os.environ.get("VARLEN_ATTN_LIB", _build.LIB)
+    if not os.path.exists(path):
+        raise ImportError("libvarlen_attn not built at %s: run __graft_entry__.build() or "
+                          "python -m packed_variable_length_varlen_gb300.build" % path)
+    lib = ctypes.CDLL(path)
+    S = VarlenStride
+    vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    lib.varlen_attn_fwd.restype = ctypes.c_int
+    lib.varlen_attn_fwd.argtypes = [vp, S, vp, S, vp, S, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32,
+                                    vp, S, vp, vp]
+    lib.varlen_attn_bwd_workspace_size.restype = sz
+    lib.varlen_attn_bwd_workspace_size.argtypes = [i32, i32, i32, i32]
+    lib.varlen_attn_bwd.restype = ctypes.c_int
+    lib.varlen_attn_bwd.argtypes = [vp, S, vp, S, vp, S, vp, S, vp, S, vp, vp, vp, i32, i32, i32, i32, i32, i32,
+                                    i32, f32, vp, S, vp, S, vp, S, vp, sz, vp]
+    lib.varlen_attn_get_device_status.restype = ctypes.c_int
+    lib.varlen_attn_get_device_status.argtypes = [vp]
+    lib.varlen_attn_status_string.restype = ctypes.c_char_p
+    lib.varlen_attn_status_string.argtypes = [ctypes.c_int]
+    lib.varlen_attn_tile_count.restype = i64
+    lib.varlen_attn_tile_count.argtypes = [vp, i32, i32, i32, i32]
+    lib.varlen_attn_debug_schedule.restype = ctypes.c_int
+    lib.varlen_attn_debug_schedule.argtypes = [vp, i32, i32, i32, i32, i32, vp, i64, vp]
+    lib.varlen_attn_selftest_wait_timeout.restype = ctypes.c_int
+    lib.varlen_attn_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+    lib.varlen_attn_num_sms.restype = ctypes.c_int
+    lib.varlen_attn_num_sms.argtypes = []
+    return lib
+
+
+LIB = _load()
+LIB_PATH = LIB._name
+
+EXPORTED = ("varlen_attn_fwd", "varlen_attn_bwd_workspace_size", "varlen_attn_bwd",
+            "varlen_attn_get_device_status", "varlen_attn_status_string", "varlen_attn_tile_count",
+            "varlen_attn_debug_schedule", "varlen_attn_selftest_wait_timeout", "varlen_attn_num_sms")
+
+
+# ---------------------------------------------------------------- marshalling
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stride(t) -> VarlenStride:
+    if t is None:
+        return VarlenStride(0, 0)
+    if t.dim() != 3 or t.stride(2) != 1:
+        raise ValueError("NHD tensors must be [rows, heads, head_dim] with unit innermost stride")
+    return VarlenStride(t.stride(0), t.stride(1))
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        stream = stream.cuda_stream
+    return ctypes.c_void_p(int(stream))
+
+
+# ---------------------------------------------------------------- raw ABI
+
+def varlen_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads, head_dim,
+                    max_seqlen_q, max_seqlen_k, scale, out, lse, stream=None) -> int:
+    return LIB.varlen_attn_fwd(_ptr(q), _stride(q), _ptr(k), _stride(k), _ptr(v), _stride(v),
+                               _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), batch, total_q, total_k, num_heads,
+                               head_dim, max_seqlen_q, max_seqlen_k, scale, _ptr(out), _stride(out), _ptr(lse),
+                               _stream(stream))
+
+
+def varlen_attn_bwd_workspace_size(batch, total_q, num_heads, head_dim) -> int:
+    return int(LIB.varlen_attn_bwd_workspace_size(batch, total_q, num_heads, head_dim))
+
+
+def varlen_attn_bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads,
+                    head_dim, max_seqlen_q, max_seqlen_k, scale, dq, dk, dv, workspace, workspace_bytes,
+                    stream=None) -> int:
+    return LIB.varlen_attn_bwd(_ptr(q), _stride(q), _ptr(k), _stride(k), _ptr(v), _stride(v), _ptr(out),
+                               _stride(out), _ptr(dout), _stride(dout), _ptr(lse), _ptr(cu_seqlens_q),
+                               _ptr(cu_seqlens_k), batch, total_q, total_k, num_heads, head_dim, max_seqlen_q,
+                               max_seqlen_k, scale, _ptr(dq), _stride(dq), _ptr(dk), _stride(dk), _ptr(dv),
+                               _stride(dv), _ptr(workspace), workspace_bytes, _stream(stream))
+
+
+def varlen_attn_get_device_status(stream=None) -> int:
+    return LIB.varlen_attn_get_device_status(_stream(stream))
+
+
+def varlen_attn_status_string(status: int) -> str:
+    return LIB.varlen_attn_status_string(status).decode()
+
+
+def varlen_attn_tile_count(cu_seqlens_host, batch, total, num_heads, tile) -> int:
+    cu = torch.as_tensor(cu_seqlens_host, dtype=torch.int32).contiguous()
+    return int(LIB.varlen_attn_tile_count(ctypes.c_void_p(cu.data_ptr()), batch, total, num_heads, tile))
+
+
+def varlen_attn_debug_schedule(cu_seqlens, batch, total, num_heads, tile, grid, out_records, max_records,
+                               stream=None) -> int:
+    return LIB.varlen_attn_debug_schedule(_ptr(cu_seqlens), batch, total, num_heads, tile, grid,
+                                          _ptr(out_records), max_records, _stream(stream))
+
+
+def varlen_attn_selftest_wait_timeout(budget_ns: int, stream=None) -> int:
+    return LIB.varlen_attn_selftest_wait_timeout(budget_ns, _stream(stream))
+
+
+def varlen_attn_num_sms() -> int:
+    return LIB.varlen_attn_num_sms()
+
+
+# ---------------------------------------------------------------- conveniences
+
+def _check(status, where):
+    if status != VARLEN_OK:
+        raise VarlenError(status, where)
+
+
+def attention_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q=0, max_seqlen_k=0, scale=None,
+                  out=None, lse=None, stream=None):
+    """O and LSE for packed q/k/v ([rows, H, D] bf16 on one CUDA device)."""
+    total_q, H, D = q.shape
+    total_k = k.shape[0]
+    batch = cu_seqlens_q.numel() - 1
+    scale = float(D ** -0.5) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q, memory_format=torch.contiguous_format)
+    if lse is None:
+        lse = torch.empty(H, total_q, dtype=torch.float32, device=q.device)
+    _check(varlen_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, H, D, max_seqlen_q,
+                           max_seqlen_k, scale, out, lse, stream), "varlen_attn_fwd")
+    return out, lse
+
+
+def attention_bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q=0, max_seqlen_k=0,
+                  scale=None, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """dQ, dK, dV for the forward above (every operand keeps its strides)."""
+    total_q, H, D = q.shape
+    total_k = k.shape[0]
+    batch = cu_seqlens_q.numel() - 1
+    scale = float(D ** -0.5) if scale is None else float(scale)
+    dq = torch.empty_like(q, memory_format=torch.contiguous_format) if dq is None else dq
+    dk = torch.empty_like(k, memory_format=torch.contiguous_format) if dk is None else dk
+    dv = torch.empty_like(v, memory_format=torch.contiguous_format) if dv is None else dv
+    nbytes = varlen_attn_bwd_workspace_size(batch, total_q, H, D)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    _check(varlen_attn_bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, H, D,
+                           max_seqlen_q, max_seqlen_k, scale, dq, dk, dv, workspace, workspace.numel(), stream),
+           "varlen_attn_bwd")
+    return dq, dk, dv

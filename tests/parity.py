@@ -1,0 +1,108 @@
+"""Shared helpers for the GPU parity tests: run the CUDA path through the C
+ABI binding, run the oracle on the same inputs, compare with the tolerances
+of the hot-path contract:
+
+* forward O: max|delta| <= 1e-2 and cosine >= 0.9999 against the oracle's O
+  rounded to bf16 (round-to-nearest-even);
+* LSE: |delta| <= 1e-3;
+* dQ, dK, dV: relative Frobenius error <= 1e-2 (exact zeros where the oracle
+  is exactly zero: empty segments).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import oracle
+from packed_variable_length_varlen_gb300 import workloads as W
+
+O_MAX_ABS = 1e-2
+O_COSINE = 0.9999
+LSE_MAX_ABS = 1e-3
+GRAD_REL_FRO = 1e-2
+
+
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16).double().numpy()
+
+
+def bf16_ulp(x: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 values at |x| (8 significant bits)."""
+    ax = np.maximum(np.abs(x), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(ax)) - 7)
+
+
+def gather(t: torch.Tensor, rows: np.ndarray, heads: np.ndarray) -> np.ndarray:
+    """t[rows[i], heads[i], :] as fp64 numpy (t on CPU)."""
+    r = torch.from_numpy(rows)
+    h = torch.from_numpy(heads.astype(np.int64))
+    return t[r, h].double().numpy()
+
+
+def run_fwd(inp_dev: W.Inputs, out: torch.Tensor, lse: torch.Tensor, max_seqlen_q=None, max_seqlen_k=None):
+    from packed_variable_length_varlen_gb300 import varlen_attn as va
+    w = inp_dev.workload
+    st = va.varlen_attn_fwd(inp_dev.q, inp_dev.k, inp_dev.v, inp_dev.cu_q, inp_dev.cu_k, w.batch, w.total_q,
+                            w.total_k, w.num_heads, w.head_dim,
+                            w.max_q() if max_seqlen_q is None else max_seqlen_q,
+                            w.max_k() if max_seqlen_k is None else max_seqlen_k,
+                            w.softmax_scale, out, lse)
+    assert st == 0, va.varlen_attn_status_string(st)
+    st = va.varlen_attn_get_device_status()
+    assert st == 0, va.varlen_attn_status_string(st)
+
+
+def fwd_metrics(out_gpu: np.ndarray, lse_gpu: np.ndarray, o_ref: np.ndarray, lse_ref: np.ndarray) -> dict:
+    ref_b = bf16_round(o_ref)
+    d = np.abs(out_gpu - ref_b)
+    finite_l = np.isfinite(lse_ref)
+    m = {
+        "pairs": int(o_ref.shape[0]),
+        "o_max_abs": float(d.max()) if d.size else 0.0,
+        "o_max_ulps": float((d / bf16_ulp(ref_b)).max()) if d.size else 0.0,
+        "o_cosine": float((out_gpu * ref_b).sum() / max(np.linalg.norm(out_gpu) * np.linalg.norm(ref_b), 1e-300))
+        if d.size and np.linalg.norm(ref_b) > 0 else 1.0,
+        "lse_max_abs": float(np.abs(lse_gpu[finite_l] - lse_ref[finite_l]).max()) if finite_l.any() else 0.0,
+        "lse_inf_match": bool(np.array_equal(lse_gpu[~finite_l], lse_ref[~finite_l])),
+        "o_beyond_bound": int((d > O_MAX_ABS).sum()),
+        "o_beyond_bound_gt_1ulp": int(((d > O_MAX_ABS) & (d > bf16_ulp(ref_b))).sum()),
+    }
+    return m
+
+
+def assert_fwd(m: dict, allow_one_ulp_above: float | None = None):
+    """Literal bounds; with allow_one_ulp_above, elements whose reference has
+    |value| >= that threshold may exceed 1e-2 by at most one bf16 ulp (the
+    bf16 spacing there is itself above 1e-2)."""
+    assert m["lse_inf_match"], m
+    assert m["lse_max_abs"] <= LSE_MAX_ABS, m
+    assert m["o_cosine"] >= O_COSINE, m
+    if allow_one_ulp_above is None:
+        assert m["o_max_abs"] <= O_MAX_ABS, m
+    else:
+        assert m["o_beyond_bound_gt_1ulp"] == 0, m
+
+
+def rel_fro(a: np.ndarray, ref: np.ndarray) -> float:
+    n = np.linalg.norm(ref)
+    if n == 0:
+        return 0.0 if np.all(a == 0) else math.inf
+    return float(np.linalg.norm(a - ref) / n)
+
+
+def oracle_problem(inp_cpu: W.Inputs) -> oracle.Problem:
+    w = inp_cpu.workload
+    return oracle.Problem(inp_cpu.q, inp_cpu.k, inp_cpu.v, inp_cpu.cu_q, inp_cpu.cu_k, w.softmax_scale,
+                          dout=inp_cpu.dout)
+
+
+def padding_untouched(t_dev: torch.Tensor, w: W.Workload, canary: float) -> bool:
+    """For padded-row outputs: every element of the buffer outside the
+    [rows, H*D] view still holds the canary."""
+    if t_dev._base is None:
+        return True
+    buf = t_dev._base
+    pad = buf[:, w.num_heads * w.head_dim:]
+    return bool((pad.float() == canary).all().item())

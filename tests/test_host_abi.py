@@ -1,0 +1,134 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every function include/varlen_attn.h declares, validates arguments with the
+documented status codes before touching a device, and its host tile count
+matches the page values.  Pointers passed here are never dereferenced: every
+call either fails validation or stops at the device query (no GPU here)."""
+import json
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "varlen_attn.h")
+GOLDEN = os.path.join(ROOT, "tests", "golden", "page_values.json")
+
+
+@pytest.fixture(scope="module")
+def va():
+    from packed_variable_length_varlen_gb300 import build
+    build.build()
+    from packed_variable_length_varlen_gb300 import varlen_attn
+    return varlen_attn
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(varlen_attn_\w+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(va):
+    names = _declared()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(va.LIB, n), n
+    assert sorted(va.EXPORTED) == names
+
+
+def test_status_strings(va):
+    for code in range(0, -11, -1):
+        s = va.varlen_attn_status_string(code)
+        assert s and s != "unknown status"
+    assert va.varlen_attn_status_string(5) == "unknown status"
+
+
+def test_tile_count_page_values(va):
+    g = json.load(open(GOLDEN))["windowed_tile_count"]
+    cu = g["cu_seqlens_q"]
+    assert va.varlen_attn_tile_count(cu, len(cu) - 1, cu[-1], g["num_heads"], g["tile_m"]) == g["valid_tiles"]
+
+
+def test_tile_count_edge_cases(va):
+    # empty, one-row, tile multiples +-1, trailing empty pair
+    cu = [0, 0, 1, 128, 256, 385, 385, 385]
+    assert va.varlen_attn_tile_count(cu, 7, 385, 2, 128) == 2 * (0 + 1 + 1 + 1 + 2 + 0 + 0)
+    # clamping: entries beyond total or decreasing count as empty
+    assert va.varlen_attn_tile_count([0, 500, 100, 2 ** 30, -5, 260], 5, 260, 1, 128) == 3 + 0 + 2 + 0 + 3
+    rng = np.random.default_rng(3)
+    for _ in range(50):
+        lens = rng.integers(0, 1000, size=int(rng.integers(1, 30)))
+        cu = [0] + list(np.cumsum(lens))
+        for tile in (64, 128):
+            exp = sum(-(-int(x) // tile) for x in lens) * 3
+            assert va.varlen_attn_tile_count(cu, len(lens), int(cu[-1]), 3, tile) == exp
+    assert va.varlen_attn_tile_count([0, 1], 1, 1, 1, 0) == -1
+
+
+def test_workspace_size(va):
+    n = va.varlen_attn_bwd_workspace_size(2, 410923, 16, 96)
+    r = lambda x: (x + 255) // 256 * 256
+    assert n == r(410923 * 16 * 96 * 4) + 2 * r(410923 * 16 * 4)
+    assert n > 2 ** 31  # a 64-bit size
+    assert va.varlen_attn_bwd_workspace_size(-1, 10, 1, 64) == 0
+
+
+class _Fake:
+    """Stands in for a tensor: a data pointer and (row, head, 1) strides."""
+
+    def __init__(self, ptr, row, head, rows=10, H=2, D=64):
+        self._p, self._s, self.shape = ptr, (row, head, 1), (rows, H, D)
+
+    def data_ptr(self):
+        return self._p
+
+    def stride(self, i=None):
+        return self._s if i is None else self._s[i]
+
+    def dim(self):
+        return 3
+
+
+def _fwd(va, q=None, cu=0x2000, B=1, tq=10, tk=10, H=2, D=64, scale=0.125, out=None, lse=0x3000, stride=None):
+    st = stride or (H * D, D)
+    q = q or _Fake(0x1000, *st)
+    out = out or _Fake(0x1000, *st)
+
+    class _P:
+        def __init__(self, p):
+            self._p = p
+
+        def data_ptr(self):
+            return self._p
+    return va.varlen_attn_fwd(q, q, q, _P(cu), _P(cu), B, tq, tk, H, D, 0, 0, scale, out, _P(lse), 0)
+
+
+def test_validation_codes(va):
+    assert _fwd(va, D=80) == va.VARLEN_ERR_HEAD_DIM
+    assert _fwd(va, B=0) == va.VARLEN_ERR_SHAPE
+    assert _fwd(va, scale=0.0) == va.VARLEN_ERR_SHAPE
+    assert _fwd(va, scale=float("nan")) == va.VARLEN_ERR_SHAPE
+    assert _fwd(va, H=0) == va.VARLEN_ERR_SHAPE
+    assert _fwd(va, tq=-1) == va.VARLEN_ERR_SHAPE
+    assert _fwd(va, q=_Fake(0x1008, 128, 64)) == va.VARLEN_ERR_ALIGN
+    assert _fwd(va, stride=(130, 64)) == va.VARLEN_ERR_STRIDE
+    assert _fwd(va, stride=(128, -8)) == va.VARLEN_ERR_STRIDE
+    assert _fwd(va, stride=(1 << 40, 64)) == va.VARLEN_ERR_STRIDE
+    assert _fwd(va, lse=0) == va.VARLEN_ERR_NULL
+    assert _fwd(va, q=_Fake(0, 128, 64)) == va.VARLEN_ERR_NULL
+
+
+def test_large_strides_pass_validation(va):
+    """The strided-dout layout of the "[FA4] cute varlen backward: int32
+    overflow" issue (row stride 9728, 410923 rows: offsets past 2^31) is
+    accepted; without a GPU the call stops at the device query."""
+    st = _fwd(va, tq=410923, tk=410923, H=16, D=96, stride=(9728, 96))
+    assert st in (va.VARLEN_ERR_CUDA, va.VARLEN_ERR_ARCH)
+
+
+def test_int64_offsets_page_value():
+    g = json.load(open(GOLDEN))["dout_offset_wrap"]
+    # the library's offsets are int64 products of row index and row stride
+    off = np.int64(g["coord"]) * np.int64(g["dout_stride"][0])
+    assert int(off) == g["true_offset"] and int(off) != g["off_signed_i32"]
