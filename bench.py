@@ -1,0 +1,392 @@
+"""Benchmark: packed varlen bf16 attention, forward + backward, on the
+windowed workload (8 segments, cu_seqlens_q = [0, 4032, ..., 35280], 17580 kv
+rows per segment, H=56, D=128), as TFLOP/s:
+
+    forward  4 * sum_b Sq_b * Sk_b * H * D   per step
+    backward 2.5 x the forward count
+
+One step = varlen_attn_fwd then varlen_attn_bwd over one batch of synthetic
+inputs (seeded N(0,1) bf16) resident in HBM.  Inputs (q 0.5 GB, k and v 2 GB
+each) are larger than L2, so no flush is needed between iterations.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs the same workload on its own GPU (independent
+batches, no collective on the data path): weak scaling.  Rank 0 prints one
+JSON line.  ``--impl reference`` times the fp64 CPU oracle (the only other
+implementation of this operation here) on a bounded sample of the same
+workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np
+import torch
+
+from packed_variable_length_varlen_gb300 import workloads as W
+
+METRIC = "varlen attention TFLOP/s (fwd, bwd) bf16 H=56 D=128; % of GB300 bf16 TC peak"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons for one GPU."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.uuid = None
+        try:
+            self.uuid = str(torch.cuda.get_device_properties(device).uuid)
+            if not self.uuid.startswith("GPU-"):
+                self.uuid = "GPU-" + self.uuid
+        except Exception:
+            pass
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + self.Q, "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(local)
+    return ws, rank, local
+
+
+def _barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU side
+
+def _oracle_rate(w: W.Workload, target_s: float, seed: int = 0):
+    """Times the oracle (forward + query-side backward) on sampled (row, head)
+    pairs of the workload.  Credits each pair with its share of the step's
+    algorithmic flops: 4*Sk*D (forward) + 10*Sk*D (backward)."""
+    import oracle
+    inp = W.make_inputs(w, seed)
+    pb = oracle.Problem(inp.q, inp.k, inp.v, inp.cu_q, inp.cu_k, w.softmax_scale, dout=inp.dout)
+    rng = np.random.default_rng(5)
+    seg_k = {b: w.cu_k[b + 1] - w.cu_k[b] for b in range(w.batch)}
+
+    def sample(n):
+        rows = rng.integers(0, w.total_q, size=n).astype(np.int64)
+        heads = rng.integers(0, w.num_heads, size=n).astype(np.int32)
+        return rows, heads
+
+    def flops(rows):
+        b = np.searchsorted(np.asarray(w.cu_q), rows, side="right") - 1
+        sk = np.array([seg_k[int(x)] for x in b], dtype=np.float64)
+        return float((14.0 * sk * w.head_dim).sum())
+
+    def run(n):
+        rows, heads = sample(n)
+        t0 = time.perf_counter()
+        pb.fwd(rows, heads)
+        pb.bwd_q(rows, heads)
+        return time.perf_counter() - t0, flops(rows), n
+
+    t, f, n = run(32)
+    n = int(max(32, min(200000, 32 * target_s / max(t, 1e-3))))
+    return run, n, oracle.num_threads()
+
+
+def reference_arm(args, w, ws, rank):
+    """The oracle, as it stands, on the host cores: each step one bounded
+    sample of the workload."""
+    if rank != 0:
+        return
+    run, n, cores = _oracle_rate(w, target_s=max(2.0, 150.0 / max(args.steps + args.warmup, 1)))
+    for _ in range(args.warmup):
+        run(n)
+    tot_t = tot_f = 0.0
+    for _ in range(args.steps):
+        t, f, _ = run(n)
+        tot_t += t
+        tot_f += f
+    val = tot_f / tot_t / 1e12
+    sample = "oracle fwd + dQ backward on %d random (row, head) pairs of the %s workload per step" % (n, w.name)
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name, "sample": sample},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU side
+
+def ours(args, w, ws, rank, local):
+    from packed_variable_length_varlen_gb300 import varlen_attn as va
+    dev = torch.device("cuda", local)
+    cpu = W.make_inputs(w, seed=0)
+    d = cpu.to(dev)
+    H, D = w.num_heads, w.head_dim
+    out = torch.empty_like(d.q)
+    lse = torch.empty(H, w.total_q, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(d.q), torch.empty_like(d.k), torch.empty_like(d.v)
+    ws_bytes = va.varlen_attn_bwd_workspace_size(w.batch, w.total_q, H, D)
+    wsp = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    scale = w.softmax_scale
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd():
+        st = va.varlen_attn_fwd(d.q, d.k, d.v, d.cu_q, d.cu_k, w.batch, w.total_q, w.total_k, H, D, w.max_q(),
+                                w.max_k(), scale, out, lse, stream)
+        assert st == 0, va.varlen_attn_status_string(st)
+
+    def bwd():
+        st = va.varlen_attn_bwd(d.q, d.k, d.v, out, d.dout, lse, d.cu_q, d.cu_k, w.batch, w.total_q, w.total_k,
+                                H, D, w.max_q(), w.max_k(), scale, dq, dk, dv, wsp, ws_bytes, stream)
+        assert st == 0, va.varlen_attn_status_string(st)
+
+    # does the backward exist in this build?
+    fwd()
+    has_bwd = va.varlen_attn_bwd(d.q, d.k, d.v, out, d.dout, lse, d.cu_q, d.cu_k, w.batch, w.total_q, w.total_k,
+                                 H, D, w.max_q(), w.max_k(), scale, dq, dk, dv, wsp, ws_bytes, stream) == 0
+    torch.cuda.synchronize()
+    assert va.varlen_attn_get_device_status(stream) == 0
+
+    K, Wm = args.steps, args.warmup
+    for _ in range(Wm):
+        fwd()
+        if has_bwd:
+            bwd()
+    torch.cuda.synchronize()
+    assert va.varlen_attn_get_device_status(stream) == 0
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    # per-kernel events inside varlen_attn_bwd: before prep / after prep /
+    # after main / after the dQ conversion
+    pev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local) if rank == 0 else None
+    _barrier(ws)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    e_start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        fwd()
+        ev[i][1].record(stream)
+        if has_bwd:
+            va.varlen_attn_debug_set_phase_events(pev[i])
+            bwd()
+        ev[i][2].record(stream)
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    _barrier(ws)
+    clocks = sampler.stop() if sampler else None
+    va.varlen_attn_debug_set_phase_events(None)
+    status = va.varlen_attn_get_device_status(stream)
+    assert status == 0, va.varlen_attn_status_string(status)
+
+    ms_total = _max_over_ranks(e_start.elapsed_time(e_end), ws)
+    t_fwd = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    t_bwd = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    f_fwd, f_bwd = w.fwd_flops(), (w.bwd_flops() if has_bwd else 0.0)
+    step_flops = f_fwd + f_bwd
+    value = ws * K * step_flops / (ms_total * 1e-3) / 1e12
+    fwd_tflops = f_fwd / (statistics.mean(t_fwd) * 1e-3) / 1e12
+    bwd_tflops = f_bwd / (statistics.mean(t_bwd) * 1e-3) / 1e12 if has_bwd else None
+
+    # ---- end to end through the C ABI with host buffers (pinned)
+    e2e = None
+    if not args.no_e2e:
+        host = {n: getattr(cpu, n).pin_memory() if getattr(cpu, n)._base is None
+                else getattr(cpu, n)._base.pin_memory() for n in ("q", "k", "v", "dout")}
+        hcu_q, hcu_k = cpu.cu_q.pin_memory(), cpu.cu_k.pin_memory()
+        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        h_dq, h_dk, h_dv = (torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv))
+        dbufs = {"q": d.q, "k": d.k, "v": d.v, "dout": d.dout}
+        h2d = sum(t.numel() * t.element_size() for t in host.values()) + 2 * hcu_q.numel() * 4
+        d2h = sum(t.numel() * t.element_size() for t in (h_out, h_lse)) + (
+            sum(t.numel() * t.element_size() for t in (h_dq, h_dk, h_dv)) if has_bwd else 0)
+
+        def e2e_step():
+            for n, h in host.items():
+                tgt = dbufs[n] if dbufs[n]._base is None else dbufs[n]._base
+                tgt.copy_(h, non_blocking=True)
+            d.cu_q.copy_(hcu_q, non_blocking=True)
+            d.cu_k.copy_(hcu_k, non_blocking=True)
+            fwd()
+            if has_bwd:
+                bwd()
+            h_out.copy_(out, non_blocking=True)
+            h_lse.copy_(lse, non_blocking=True)
+            if has_bwd:
+                h_dq.copy_(dq, non_blocking=True)
+                h_dk.copy_(dk, non_blocking=True)
+                h_dv.copy_(dv, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        _barrier(ws)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ke = max(2, min(K, 5))
+        a.record(stream)
+        for _ in range(ke):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = _max_over_ranks(a.elapsed_time(b), ws)
+        e2e = {"value": ws * ke * step_flops / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": ms_e2e / ke}
+
+    peaks, src = _peaks()
+    if rank != 0:
+        return
+    # roofline of the dominant kernel (the one launch that does the most flops)
+    t_prep = t_main = t_post = None
+    if has_bwd:
+        t_prep = statistics.mean(pev[i][0].elapsed_time(pev[i][1]) for i in range(K))
+        t_main = statistics.mean(pev[i][1].elapsed_time(pev[i][2]) for i in range(K))
+        t_post = statistics.mean(pev[i][2].elapsed_time(pev[i][3]) for i in range(K))
+        dom_name, dom_flops, dom_ms = "varlen_bwd_main_kernel", f_bwd, t_main
+    else:
+        dom_name, dom_flops, dom_ms = "varlen_fwd_kernel", f_fwd, statistics.mean(t_fwd)
+    ach = dom_flops / (dom_ms * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    roof = {"kernel": dom_name, "bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+            "frac": ach / peak, "peak_source": "%s bf16_tflops_sustained" % src, "traffic": None}
+
+    cpu_base = None
+    if not args.no_cpu_baseline and ws >= 1:
+        run, n, cores = _oracle_rate(w, target_s=12.0)
+        t, f, n = run(n)
+        cpu_base = {"value": f / t / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                    "sample": "oracle fwd + dQ backward on %d random (row, head) pairs of the %s workload "
+                              "(%.1f s); each pair credited with 14*Sk*D flops" % (n, w.name, t)}
+
+    burst = float(peaks.get("bf16_tflops"))
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": K, "warmup": Wm,
+        "ms_per_step": ms_total / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "batch_segments": w.batch, "total_q": w.total_q, "total_k": w.total_k,
+                   "num_heads": H, "head_dim": D, "step": "fwd+bwd" if has_bwd else "fwd only (bwd missing)",
+                   "l2": "inputs larger than L2 (k, v 2 GB each); no flush",
+                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+        "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
+        "fwd_frac_of_burst_peak": fwd_tflops / burst,
+        "bwd_frac_of_burst_peak": (bwd_tflops / burst) if bwd_tflops else None,
+        "fwd_ms": statistics.mean(t_fwd), "bwd_ms": statistics.mean(t_bwd) if has_bwd else None,
+        "bwd_kernel_ms": {"prep": t_prep, "main": t_main, "post": t_post} if has_bwd else None,
+        "fwd_kernel_roofline": {"achieved": fwd_tflops, "peak": peak, "frac": fwd_tflops / peak},
+        "clocks": clocks, "e2e": e2e, "gpu_launches": K * (1 + (3 if has_bwd else 0)),
+        "roofline": roof, "cpu_baseline": cpu_base,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="windowed", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3  # timing rule: at least three warm-up steps
+    w = W.get(args.workload)
+    if args.impl == "reference":
+        ws = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        reference_arm(args, w, ws, rank)
+        return
+    ws, rank, local = _dist()
+    ours(args, w, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

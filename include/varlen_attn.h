@@ -157,6 +157,15 @@ int varlen_attn_debug_schedule(const int32_t* cu_seqlens, int32_t batch, int32_t
  */
 int varlen_attn_selftest_wait_timeout(uint64_t budget_ns, void* stream);
 
+/*
+ * Profiling hook: with count == 4, every later varlen_attn_bwd call records
+ * events[0] before its preprocess kernel, events[1] after it, events[2] after
+ * the main kernel and events[3] after the dQ conversion, on the call's
+ * stream (cudaEvent_t handles owned by the caller; they must outlive their
+ * use).  count == 0 turns it off.  Process-wide setting.
+ */
+int varlen_attn_debug_set_phase_events(void* const* events, int count);
+
 /* Number of streaming multiprocessors the persistent kernels size their grid
  * by on the current device (cached). Returns <= 0 on failure. */
 int varlen_attn_num_sms(void);

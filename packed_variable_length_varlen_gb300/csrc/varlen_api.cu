@@ -123,6 +123,10 @@ int check_common(const int32_t* cu_q, const int32_t* cu_k, int32_t batch, int32_
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Optional profiling events for the three backward kernels (process-wide).
+cudaEvent_t g_phase_events[4] = {nullptr, nullptr, nullptr, nullptr};
+std::mutex g_phase_mu;
+
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 }  // namespace
@@ -240,6 +244,10 @@ extern "C" int varlen_attn_bwd(const void* q, varlen_stride sq, const void* k, v
                       total_q, num_heads, head_dim, scale};
   L.head_dim = head_dim;
   L.grid = dev.sms;
+  {
+    std::lock_guard<std::mutex> lock(g_phase_mu);
+    for (int i = 0; i < 4; ++i) L.phase_events[i] = g_phase_events[i];
+  }
   cudaError_t e = launch_bwd(L, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? VARLEN_OK : VARLEN_ERR_CUDA;
 }
@@ -304,6 +312,14 @@ extern "C" int varlen_attn_selftest_wait_timeout(uint64_t budget_ns, void* strea
   if (st != VARLEN_OK) return st;
   cudaError_t e = launch_selftest_timeout(budget_ns, dev.err, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? VARLEN_OK : VARLEN_ERR_CUDA;
+}
+
+extern "C" int varlen_attn_debug_set_phase_events(void* const* events, int count) {
+  if (count != 0 && count != 4) return VARLEN_ERR_SHAPE;
+  if (count == 4 && events == nullptr) return VARLEN_ERR_NULL;
+  std::lock_guard<std::mutex> lock(g_phase_mu);
+  for (int i = 0; i < 4; ++i) g_phase_events[i] = count ? static_cast<cudaEvent_t>(events[i]) : nullptr;
+  return VARLEN_OK;
 }
 
 extern "C" int varlen_attn_num_sms(void) {

@@ -1,5 +1,485 @@
-// varlen_bwd.cu -- placeholder until the backward kernels land.
+// varlen_bwd.cu -- backward of packed variable-length attention on sm_103a.
+//
+// Three kernels on the caller's stream:
+//
+//  1. varlen_bwd_prep_kernel (HBM-bound): for every q row i and head h,
+//       delta[h,i] = sum_d dO[i,h,d] * O[i,h,d]      (fp32, from bf16)
+//       lse2[h,i]  = LSE[h,i] * log2(e)
+//     and zero the fp32 dQ accumulator.  dO and O are read through their own
+//     row / head strides with 64-bit offsets: the preprocess is where the
+//     "[FA4] cute varlen backward: int32 overflow in _bwd_preprocess" issue
+//     (sections "Summary", "Root cause") wrapped cu_seqlens[b]*stride past
+//     2^31.
+//
+//  2. varlen_bwd_main_kernel (tensor-bound), persistent over kv tiles
+//     (segment b, 128 kv rows, head h) of an exact varlen schedule.  K and V
+//     stay in shared memory; for each 64-row q step of the segment it issues
+//     five tcgen05 MMAs (TMEM accumulators):
+//         S^T  = K Q^T          (128 x 64, K = D)
+//         dP^T = V dO^T         (128 x 64, K = D)
+//         dV  += P^T dO         (128 x D,  K = 64)
+//         dK  += dS^T Q         (128 x D,  K = 64)
+//         dQ^T = K^T dS^T       (128(d) x 64, K = 128)
+//     where P^T = exp2(S^T * scale*log2e - lse2) and dS^T = P^T (dP^T - delta)
+//     are computed by eight compute warps (thread = kv row, half of the q
+//     columns) and written to shared memory as bf16.  dQ^T is added into the
+//     fp32 accumulator with coalesced reductions (a warp covers 32
+//     consecutive d of one q row).  At the end of a kv tile, dK * scale and
+//     dV go to their strided outputs; a segment without queries writes zeros.
+//
+//  3. varlen_bwd_post_kernel (HBM-bound): dq = bf16(scale * dq_acc), strided.
+//
+// The gradient formulas are the standard ones for O = softmax(scale QK^T) V:
+// dP = dO V^T, dS = P (dP - rowsum(dO o O)), dQ = scale dS K,
+// dK = scale dS^T Q, dV = P^T dO.
+#include "sm103_ptx.cuh"
 #include "varlen_internal.h"
+#include "varlen_sched.cuh"
+
 namespace varlen {
-cudaError_t launch_bwd(const BwdLaunch&, cudaStream_t) { return cudaErrorNotSupported; }
+
+// ------------------------------------------------------------------ prep
+
+__global__ void __launch_bounds__(256) varlen_bwd_prep_kernel(const PrepParams p) {
+  const int32_t B = p.batch;
+  const int32_t lo = clamp_row(__ldg(p.cu_q), p.total_q);
+  const int32_t hi = clamp_row(__ldg(p.cu_q + B), p.total_q);
+  if (hi <= lo) return;
+  const int H = p.num_heads, D = p.head_dim;
+  const int64_t n = (int64_t)(hi - lo) * H;
+  const float kLog2e = 1.4426950408889634f;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n; t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = lo + t / H;
+    const int h = (int)(t % H);
+    const __nv_bfloat16* o = p.out + row * p.o_rs + (int64_t)h * p.o_hs;
+    const __nv_bfloat16* g = p.dout + row * p.do_rs + (int64_t)h * p.do_hs;
+    float acc = 0.f;
+    for (int d = 0; d < D; d += 8) {
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + d));
+      const uint4 b = __ldg(reinterpret_cast<const uint4*>(g + d));
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 x = __bfloat1622float2(a2[i]);
+        const float2 y = __bfloat1622float2(b2[i]);
+        acc = fmaf(x.x, y.x, acc);
+        acc = fmaf(x.y, y.y, acc);
+      }
+    }
+    const int64_t hi_idx = (int64_t)h * p.total_q + row;
+    p.delta[hi_idx] = acc;
+    p.lse2[hi_idx] = p.lse[hi_idx] * kLog2e;
+    float4* z = reinterpret_cast<float4*>(p.dq_acc + (row * H + h) * D);
+    for (int d = 0; d < D; d += 4) *z++ = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// ------------------------------------------------------------------ post
+
+__global__ void __launch_bounds__(256) varlen_bwd_post_kernel(const PostParams p) {
+  const int32_t B = p.batch;
+  const int32_t lo = clamp_row(__ldg(p.cu_q), p.total_q);
+  const int32_t hi = clamp_row(__ldg(p.cu_q + B), p.total_q);
+  if (hi <= lo) return;
+  const int H = p.num_heads, D = p.head_dim, V = D / 8;
+  const int64_t n = (int64_t)(hi - lo) * H * V;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n; t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t rh = t / V;
+    const int v = (int)(t - rh * V);
+    const int64_t row = lo + rh / H;
+    const int h = (int)(rh % H);
+    const float4* s = reinterpret_cast<const float4*>(p.dq_acc + (row * H + h) * D + v * 8);
+    const float4 a = s[0], b = s[1];
+    uint4 w;
+    w.x = pack_bf16x2(a.x * p.scale, a.y * p.scale);
+    w.y = pack_bf16x2(a.z * p.scale, a.w * p.scale);
+    w.z = pack_bf16x2(b.x * p.scale, b.y * p.scale);
+    w.w = pack_bf16x2(b.z * p.scale, b.w * p.scale);
+    *reinterpret_cast<uint4*>(p.dq + row * p.dq_rs + (int64_t)h * p.dq_hs + v * 8) = w;
+  }
+}
+
+// ------------------------------------------------------------------ main
+
+template <int D>
+struct BwdCfg {
+  static constexpr int NC = (D + 63) / 64;       // 64-column chunks of Q / dO / V
+  static constexpr int KCH = 2;                  // K tile always holds 128 columns (dQ^T uses M = 128)
+  static constexpr int KV_CHUNK = 128 * 128;     // 128 kv rows x 128 B
+  static constexpr int Q_CHUNK = 64 * 128;       // 64 q rows x 128 B
+  static constexpr int K_BYTES = KCH * KV_CHUNK;
+  static constexpr int V_BYTES = NC * KV_CHUNK;
+  static constexpr int Q_BYTES = NC * Q_CHUNK;   // one Q or dO tile
+  static constexpr int NSTAGE = 2;
+  static constexpr int PS_BYTES = 128 * 128;     // P^T or dS^T: 128 kv rows x 64 q (bf16)
+  static constexpr int SMEM_BYTES = 1024 + 1024 + K_BYTES + V_BYTES + NSTAGE * 2 * Q_BYTES + 2 * PS_BYTES;
+  static constexpr int S_COL = 0, DP_COL = 64, DQ_COL = 128, DV_COL = 256, DK_COL = 384;
+  static constexpr int TMEM_COLS = 512;
+};
+
+struct BwdBarriers {
+  uint64_t kv_full, kv_empty;
+  uint64_t qd_full[2], qd_empty[2];
+  uint64_t sp_full, ds_ready, step_done, mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ void zero_rows(uint8_t* tile, int chunks, int chunk_bytes, int row_from, int row_to,
+                                          int lane) {
+  for (int r = row_from + lane; r < row_to; r += 32) {
+    for (int cc = 0; cc < chunks; ++cc) {
+      uint4* row = reinterpret_cast<uint4*>(tile + cc * chunk_bytes + r * 128);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) row[u] = make_uint4(0, 0, 0, 0);
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(384, 1)
+    varlen_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                           const BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  BwdBarriers& bar = *reinterpret_cast<BwdBarriers*>(smem);
+  uint8_t* k_smem = smem + 1024;
+  uint8_t* v_smem = k_smem + C::K_BYTES;
+  uint8_t* qd_smem = v_smem + C::V_BYTES;                 // [stage][Q, dO]
+  uint8_t* pt_smem = qd_smem + C::NSTAGE * 2 * C::Q_BYTES;
+  uint8_t* dst_smem = pt_smem + C::PS_BYTES;
+  volatile int* abort = &bar.abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar.kv_full, 1);
+    mbar_init(&bar.kv_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar.qd_full[i], 1);
+      mbar_init(&bar.qd_empty[i], 1);
+    }
+    mbar_init(&bar.sp_full, 1);
+    mbar_init(&bar.ds_ready, 256);
+    mbar_init(&bar.step_done, 1);
+    mbar_init(&bar.mma_done, 1);
+    bar.abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(&bar.tmem_base, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar.tmem_base;
+  const int64_t G = gridDim.x;
+  constexpr int QT = kBwdTileQ;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      SegCursor c;
+      cursor_init<kTileM>(c, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q);
+      uint32_t tiles = 0, gs = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x;
+           ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q); t += G) {
+        if (c.olen == 0) continue;  // no queries: dK = dV = 0, written by the compute warps
+        const Tile tl = cursor_tile(c, t);
+        const int32_t krow = c.r0 + tl.m * kTileM;
+        if (tiles > 0 && !mbar_wait(&bar.kv_empty, (tiles - 1) & 1, abort)) break;
+        mbar_arrive_expect_tx(&bar.kv_full, C::K_BYTES + C::V_BYTES);
+#pragma unroll
+        for (int cc = 0; cc < C::KCH; ++cc)
+          tma_load_3d(k_smem + cc * C::KV_CHUNK, &tm_k, &bar.kv_full, cc * 64, tl.h, krow);
+#pragma unroll
+        for (int cc = 0; cc < C::NC; ++cc)
+          tma_load_3d(v_smem + cc * C::KV_CHUNK, &tm_v, &bar.kv_full, cc * 64, tl.h, krow);
+        ++tiles;
+        const int32_t nq = (c.olen + QT - 1) / QT;
+        for (int32_t j = 0; j < nq; ++j, ++gs) {
+          const uint32_t st = gs & 1;
+          if (!mbar_wait(&bar.qd_empty[st], ((gs >> 1) & 1) ^ 1, abort)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bar.qd_full[st], 2 * C::Q_BYTES);
+          uint8_t* qs = qd_smem + st * 2 * C::Q_BYTES;
+          const int32_t qrow = c.o0 + j * QT;
+#pragma unroll
+          for (int cc = 0; cc < C::NC; ++cc) {
+            tma_load_3d(qs + cc * C::Q_CHUNK, &tm_q, &bar.qd_full[st], cc * 64, tl.h, qrow);
+            tma_load_3d(qs + C::Q_BYTES + cc * C::Q_CHUNK, &tm_do, &bar.qd_full[st], cc * 64, tl.h, qrow);
+          }
+        }
+      }
+      if (*abort) {
+        int dummy = 0;
+        if (tiles > 0) mbar_wait(&bar.kv_full, (tiles - 1) & 1, &dummy, 100000000ull);
+        for (uint32_t s = 0; s < 2 && s < gs; ++s) {
+          const uint32_t last = gs - 1 - ((gs - 1 - s) & 1);
+          mbar_wait(&bar.qd_full[s], (last >> 1) & 1, &dummy, 100000000ull);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t kIdS = idesc_bf16_f32(128, QT, false, false);   // S^T, dP^T
+    constexpr uint32_t kIdG = idesc_bf16_f32(128, D, false, true);     // dV, dK
+    constexpr uint32_t kIdQ = idesc_bf16_f32(128, QT, true, true);     // dQ^T
+    SegCursor c;
+    cursor_init<kTileM>(c, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q);
+    uint32_t tiles = 0, gs = 0;
+    const uint32_t k_base = smem_addr(k_smem), v_base = smem_addr(v_smem);
+    const uint32_t pt_base = smem_addr(pt_smem), dst_base = smem_addr(dst_smem);
+    bool ok = true;
+    for (int64_t t = blockIdx.x;
+         ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q); t += G) {
+      if (c.olen == 0) continue;
+      const Tile tl = cursor_tile(c, t);
+      if (!mbar_wait(&bar.kv_full, tiles & 1, abort)) break;
+      ++tiles;
+      const int32_t kv_valid = c.len - tl.m * kTileM;
+      if (kv_valid < kTileM) {
+        // K rows past the segment end would meet dS^T = 0 in dQ^T = K^T dS^T;
+        // clear them so that 0 * NaN cannot occur.
+        zero_rows(k_smem, C::KCH, C::KV_CHUNK, kv_valid, kTileM, lane);
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      const int32_t nq = (c.olen + QT - 1) / QT;
+      for (int32_t j = 0; j < nq; ++j, ++gs) {
+        const uint32_t st = gs & 1;
+        if (!mbar_wait(&bar.qd_full[st], (gs >> 1) & 1, abort)) { ok = false; break; }
+        uint8_t* qs = qd_smem + st * 2 * C::Q_BYTES;
+        const int32_t q_valid = c.olen - j * QT;
+        if (q_valid < QT) {
+          // Q / dO rows past the segment end meet P^T = dS^T = 0 in dK / dV.
+          zero_rows(qs, 2 * C::NC, C::Q_CHUNK, q_valid, QT, lane);
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        tc_fence_after();
+        const uint32_t q_base = smem_addr(qs), do_base = q_base + C::Q_BYTES;
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ko = (kk >> 2) * C::KV_CHUNK + (kk & 3) * 32;
+            const uint32_t qo = (kk >> 2) * C::Q_CHUNK + (kk & 3) * 32;
+            mma_ss(tmem + C::S_COL, sw128_desc(k_base + ko, 16, 1024), sw128_desc(q_base + qo, 16, 1024), kIdS,
+                   kk > 0);
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ko = (kk >> 2) * C::KV_CHUNK + (kk & 3) * 32;
+            const uint32_t qo = (kk >> 2) * C::Q_CHUNK + (kk & 3) * 32;
+            mma_ss(tmem + C::DP_COL, sw128_desc(v_base + ko, 16, 1024), sw128_desc(do_base + qo, 16, 1024), kIdS,
+                   kk > 0);
+          }
+          mma_commit(&bar.sp_full);
+        }
+        __syncwarp();
+        if (!mbar_wait(&bar.ds_ready, gs & 1, abort)) { ok = false; break; }
+        tc_fence_after();
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < QT / 16; ++kk) {
+            mma_ss(tmem + C::DV_COL, sw128_desc(pt_base + kk * 32, 16, 1024),
+                   sw128_desc(do_base + kk * 2048, C::Q_CHUNK, 1024), kIdG, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < QT / 16; ++kk) {
+            mma_ss(tmem + C::DK_COL, sw128_desc(dst_base + kk * 32, 16, 1024),
+                   sw128_desc(q_base + kk * 2048, C::Q_CHUNK, 1024), kIdG, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < kTileM / 16; ++kk) {
+            mma_ss(tmem + C::DQ_COL, sw128_desc(k_base + kk * 2048, C::KV_CHUNK, 1024),
+                   sw128_desc(dst_base + kk * 2048, C::PS_BYTES, 1024), kIdQ, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&bar.qd_empty[st]);
+          mma_commit(&bar.step_done);
+          if (j == nq - 1) mma_commit(&bar.kv_empty);
+        }
+        __syncwarp();
+      }
+    }
+    if (lane == 0) {
+      mma_commit(&bar.mma_done);
+      int dummy = 0;
+      mbar_wait(&bar.mma_done, 0, &dummy);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ compute
+    const int quad = warp & 3;
+    const int half = (warp - 4) >> 2;              // which 32 q columns (and half of D in the epilogue)
+    const int r = quad * 32 + lane;                // kv row in the tile / d index for dQ^T
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const float c2 = p.scale_log2;
+    const int H = p.num_heads;
+    SegCursor c;
+    cursor_init<kTileM>(c, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q);
+    uint32_t gs = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x;
+         ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q); t += G) {
+      const Tile tl = cursor_tile(c, t);
+      const int32_t kv_valid = c.len - tl.m * kTileM;
+      const bool row_valid = r < kv_valid;
+      const int64_t krow = (int64_t)c.r0 + tl.m * kTileM + r;
+      const int32_t nq = (c.olen + QT - 1) / QT;
+      const float* lse2 = p.lse2 + (int64_t)tl.h * p.total_q;
+      const float* delta = p.delta + (int64_t)tl.h * p.total_q;
+      for (int32_t j = 0; j <= nq; ++j) {
+        // ---- dQ^T of step j-1: wait for it, add it into the accumulator
+        if (j > 0) {
+          const uint32_t gp = gs - 1;
+          if (!mbar_wait(&bar.step_done, gp & 1, abort)) { ok = false; break; }
+          tc_fence_after();
+          uint32_t q32[32];
+          tmem_ld32(tmem + lane_off + C::DQ_COL + half * 32, q32);
+          tmem_wait_ld();
+          const int32_t qs0 = (j - 1) * QT + half * 32;  // first q column of this thread, in the segment
+          if (r < D) {
+            float* dst = p.dq_acc + (((int64_t)c.o0 + qs0) * H + tl.h) * D + r;
+            const int64_t step = (int64_t)H * D;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (qs0 + i < c.olen) atomicAdd(dst + i * step, __uint_as_float(q32[i]));
+          }
+        }
+        if (j == nq) break;
+        // ---- P^T and dS^T of step j
+        if (!mbar_wait(&bar.sp_full, gs & 1, abort)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t sv[32], dpv[32];
+        tmem_ld32(tmem + lane_off + C::S_COL + half * 32, sv);
+        tmem_ld32(tmem + lane_off + C::DP_COL + half * 32, dpv);
+        tmem_wait_ld();
+        const int32_t qc0 = j * QT + half * 32;            // first q column (in the segment)
+        const int32_t nvalid = row_valid ? min(32, max(0, c.olen - qc0)) : 0;
+        uint32_t pk[16], dk2[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float pv[2], dsv[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int col = 2 * i + e;
+            float pe = 0.f, de = 0.f;
+            if (col < nvalid) {
+              const int64_t qi = (int64_t)c.o0 + qc0 + col;
+              const float l2 = __ldg(lse2 + qi);
+              const float dl = __ldg(delta + qi);
+              pe = ex2(fmaf(__uint_as_float(sv[col]), c2, -l2));
+              de = pe * (__uint_as_float(dpv[col]) - dl);
+            }
+            pv[e] = pe;
+            dsv[e] = de;
+          }
+          pk[i] = pack_bf16x2(pv[0], pv[1]);
+          dk2[i] = pack_bf16x2(dsv[0], dsv[1]);
+        }
+        // write this thread's 64 bytes of the P^T and dS^T rows (128-byte
+        // swizzle: 16-byte unit u of row r sits at unit u ^ (r % 8))
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int unit = (half * 4 + u) ^ (r & 7);
+          *reinterpret_cast<uint4*>(pt_smem + r * 128 + unit * 16) =
+              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          *reinterpret_cast<uint4*>(dst_smem + r * 128 + unit * 16) =
+              make_uint4(dk2[4 * u], dk2[4 * u + 1], dk2[4 * u + 2], dk2[4 * u + 3]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&bar.ds_ready);
+        ++gs;
+      }
+      if (!ok) break;
+      // ---- epilogue: dV and dK * scale of this kv tile (zeros if no queries)
+      if (row_valid) {
+        __nv_bfloat16* dvrow = p.dv + krow * p.dv_rs + (int64_t)tl.h * p.dv_hs;
+        __nv_bfloat16* dkrow = p.dk + krow * p.dk_rs + (int64_t)tl.h * p.dk_hs;
+        if (nq == 0) {
+          for (int d = half * (D / 2); d < (half + 1) * (D / 2); d += 8) {
+            *reinterpret_cast<uint4*>(dvrow + d) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(dkrow + d) = make_uint4(0, 0, 0, 0);
+          }
+        }
+      }
+      if (nq > 0) {
+        tc_fence_after();
+#pragma unroll
+        for (int d0 = half * (D / 2); d0 < (half + 1) * (D / 2); d0 += 16) {
+          uint32_t a[16], b[16];
+          tmem_ld16(tmem + lane_off + C::DV_COL + d0, a);
+          tmem_ld16(tmem + lane_off + C::DK_COL + d0, b);
+          tmem_wait_ld();
+          if (row_valid) {
+            uint32_t wa[8], wb[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              wa[i] = pack_bf16x2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
+              wb[i] = pack_bf16x2(__uint_as_float(b[2 * i]) * p.scale, __uint_as_float(b[2 * i + 1]) * p.scale);
+            }
+            uint4* dv4 = reinterpret_cast<uint4*>(p.dv + krow * p.dv_rs + (int64_t)tl.h * p.dv_hs + d0);
+            uint4* dk4 = reinterpret_cast<uint4*>(p.dk + krow * p.dk_rs + (int64_t)tl.h * p.dk_hs + d0);
+            dv4[0] = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+            dv4[1] = make_uint4(wa[4], wa[5], wa[6], wa[7]);
+            dk4[0] = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+            dk4[1] = make_uint4(wb[4], wb[5], wb[6], wb[7]);
+          }
+        }
+        tc_fence_before();
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+  if (threadIdx.x == 0 && bar.abort) record_error(p.err, kErrTimeout);
+}
+
+template <int D>
+static cudaError_t launch_bwd_d(const BwdLaunch& L, cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  const int elem_grid = L.grid * 8;
+  auto mark = [&](int i) {
+    if (L.phase_events[i] != nullptr) cudaEventRecord(L.phase_events[i], stream);
+  };
+  auto kern = varlen_bwd_main_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  mark(0);
+  varlen_bwd_prep_kernel<<<elem_grid, 256, 0, stream>>>(L.prep);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  mark(1);
+  kern<<<L.grid, 384, C::SMEM_BYTES, stream>>>(L.tm_q, L.tm_k, L.tm_v, L.tm_do, L.p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  mark(2);
+  varlen_bwd_post_kernel<<<elem_grid, 256, 0, stream>>>(L.post);
+  e = cudaGetLastError();
+  mark(3);
+  return e;
+}
+
+cudaError_t launch_bwd(const BwdLaunch& L, cudaStream_t stream) {
+  switch (L.head_dim) {
+    case 64: return launch_bwd_d<64>(L, stream);
+    case 96: return launch_bwd_d<96>(L, stream);
+    case 128: return launch_bwd_d<128>(L, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 }  // namespace varlen

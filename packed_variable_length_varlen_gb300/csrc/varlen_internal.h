@@ -85,6 +85,7 @@ struct BwdLaunch {
   PostParams post;
   int head_dim;
   int grid;
+  cudaEvent_t phase_events[4];  // optional: recorded before prep / after prep / after main / after post
 };
 
 cudaError_t launch_bwd(const BwdLaunch& L, cudaStream_t stream);

@@ -68,6 +68,8 @@ def _load() -> ctypes.CDLL:
     lib.varlen_attn_debug_schedule.argtypes = [vp, i32, i32, i32, i32, i32, vp, i64, vp]
     lib.varlen_attn_selftest_wait_timeout.restype = ctypes.c_int
     lib.varlen_attn_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+    lib.varlen_attn_debug_set_phase_events.restype = ctypes.c_int
+    lib.varlen_attn_debug_set_phase_events.argtypes = [vp, ctypes.c_int]
     lib.varlen_attn_num_sms.restype = ctypes.c_int
     lib.varlen_attn_num_sms.argtypes = []
     return lib
@@ -78,7 +80,8 @@ LIB_PATH = LIB._name
 
 EXPORTED = ("varlen_attn_fwd", "varlen_attn_bwd_workspace_size", "varlen_attn_bwd",
             "varlen_attn_get_device_status", "varlen_attn_status_string", "varlen_attn_tile_count",
-            "varlen_attn_debug_schedule", "varlen_attn_selftest_wait_timeout", "varlen_attn_num_sms")
+            "varlen_attn_debug_schedule", "varlen_attn_selftest_wait_timeout", "varlen_attn_num_sms",
+            "varlen_attn_debug_set_phase_events")
 
 
 # ---------------------------------------------------------------- marshalling
@@ -148,6 +151,22 @@ def varlen_attn_debug_schedule(cu_seqlens, batch, total, num_heads, tile, grid, 
 
 def varlen_attn_selftest_wait_timeout(budget_ns: int, stream=None) -> int:
     return LIB.varlen_attn_selftest_wait_timeout(budget_ns, _stream(stream))
+
+
+_PHASE_KEEP = None
+
+
+def varlen_attn_debug_set_phase_events(events) -> int:
+    """events: four torch.cuda.Event(enable_timing=True) objects, or None."""
+    global _PHASE_KEEP
+    if not events:
+        _PHASE_KEEP = None
+        return LIB.varlen_attn_debug_set_phase_events(None, 0)
+    for e in events:
+        e.record()  # materialise the handle on the current device
+    arr = (ctypes.c_void_p * 4)(*[e.cuda_event for e in events])
+    _PHASE_KEEP = (events, arr)
+    return LIB.varlen_attn_debug_set_phase_events(arr, 4)
 
 
 def varlen_attn_num_sms() -> int:

@@ -105,4 +105,5 @@ def padding_untouched(t_dev: torch.Tensor, w: W.Workload, canary: float) -> bool
         return True
     buf = t_dev._base
     pad = buf[:, w.num_heads * w.head_dim:]
-    return bool((pad.float() == canary).all().item())
+    want = torch.tensor(canary, dtype=buf.dtype).float().item()
+    return bool((pad.float() == want).all().item())

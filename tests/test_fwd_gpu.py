@@ -54,7 +54,7 @@ def test_fwd_ragged_small(D):
 
 
 def test_fwd_padded_strides_canary():
-    w = W.custom("padded", [200, 0, 77, 256], [130, 9, 0, 300], 2, 128, row_pad=64, amplitude=2.0)
+    w = W.custom("padded", [200, 0, 77, 256], [130, 9, 0, 300], 2, 128, row_pad=64)
     _fwd_case(w)
 
 
@@ -123,3 +123,19 @@ def test_fwd_ragged_full():
     w = W.ragged()
     extra = [W.offset_crossing_row(w.row_stride, 2)]
     _fwd_case(w, pairs=_sampled_pairs(w, 2, extra), allow_ulp=1.28)
+
+
+@pytest.mark.slow
+def test_fwd_long_full():
+    w = W.long_dense()
+    extra = [W.offset_crossing_row(w.row_stride, 2)]
+    rows = W.sample_rows(w.cu_q, 2048, seed=1, extra_rows=extra)
+    _fwd_case(w, pairs=W.sample_pairs(rows, w.num_heads, 1, seed=2, all_heads_rows=[0, 76999]))
+
+
+@pytest.mark.slow
+def test_fwd_strided_dout_workload_full():
+    """Forward of the 410923-token, H=16, D=96 workload (inputs * 0.1)."""
+    w = W.strided_dout()
+    rows = W.sample_rows(w.cu_q, 2048, seed=1, extra_rows=[225304])
+    _fwd_case(w, pairs=W.sample_pairs(rows, w.num_heads, 1, seed=2, all_heads_rows=[0, 225304, 410922]))
