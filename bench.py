@@ -370,12 +370,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="windowed", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--heads", type=int, default=None,
+                    help="override the head count (small cases for profiling captures)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3  # timing rule: at least three warm-up steps
     w = W.get(args.workload)
+    if args.heads is not None and args.heads != w.num_heads:
+        w = w.with_(num_heads=args.heads, name="%s_h%d" % (w.name, args.heads))
     if args.impl == "reference":
         ws = int(os.environ.get("WORLD_SIZE", "1"))
         rank = int(os.environ.get("RANK", "0"))

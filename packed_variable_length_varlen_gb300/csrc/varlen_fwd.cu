@@ -10,9 +10,9 @@
 //                TMEM.  Owns the TMEM allocation.
 //   warps 4..7   softmax / correction / epilogue: thread = one q row = one
 //                TMEM lane.  Masks key columns past the segment end, keeps
-//                the running max m and sum l (of the bf16-rounded P), writes
-//                P = exp2(S*c - m) back into TMEM as bf16 (aliasing S),
-//                rescales O in TMEM when m
+//                the running max m and the row sums of P (fp32, for LSE) and
+//                of bf16(P) (for O's normalisation), writes P = exp2(S*c - m)
+//                back into TMEM as bf16 (aliasing S), rescales O in TMEM when m
 //                grows by more than 2^8 (exact: O and l carry the same
 //                factor), and finally writes O / l (bf16) and LSE.
 //   warps 2,3    idle.
@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(256, 1)
         continue;
       }
       const int32_t nkv = (c.olen + kTileN - 1) / kTileN;
-      float m_use = -INFINITY, l = 0.f;
+      float m_use = -INFINITY, l = 0.f, lr = 0.f;
       for (int32_t j = 0; j < nkv; ++j) {
         const uint32_t gj = g + j;
         const uint32_t sb = gj % C::NSBUF;
@@ -304,20 +304,23 @@ __global__ void __launch_bounds__(256, 1)
           m_use = m_new;
           rescale = true;
         }
-        // The row sum adds the bf16-rounded P values -- the weights the
-        // P V MMA actually applies -- so O / l is a consistently normalised
-        // average and P's rounding cancels in rows dominated by a few keys.
-        float rs0 = 0.f, rs1 = 0.f;
+        // Two row sums: l of the fp32 P (for LSE) and lr of the bf16-rounded
+        // P -- the weights the P V MMA actually applies -- so that O / lr is
+        // a consistently normalised average and P's rounding cancels in rows
+        // dominated by a few keys.
+        float rs = 0.f, rr0 = 0.f, rr1 = 0.f;
         uint32_t pk[64];
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
           const float p0 = ex2(fmaf(x[2 * i], c2, -m_use));
           const float p1 = ex2(fmaf(x[2 * i + 1], c2, -m_use));
           pk[i] = pack_bf16x2(p0, p1);
-          rs0 += __uint_as_float(pk[i] << 16);
-          rs1 += __uint_as_float(pk[i] & 0xffff0000u);
+          rs += p0 + p1;
+          rr0 += __uint_as_float(pk[i] << 16);
+          rr1 += __uint_as_float(pk[i] & 0xffff0000u);
         }
-        l = fmaf(l, alpha, rs0 + rs1);
+        l = fmaf(l, alpha, rs);
+        lr = fmaf(lr, alpha, rr0 + rr1);
         {
           const uint32_t ta = tmem + lane_off + sb * 128;
           tmem_st32(ta + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
@@ -348,7 +351,7 @@ __global__ void __launch_bounds__(256, 1)
       const uint32_t gl = g + nkv - 1;
       if (!mbar_wait(&bar.s_free[gl % C::NSBUF], (gl / C::NSBUF) & 1, abort)) break;
       tc_fence_after();
-      const float inv_l = 1.f / l;
+      const float inv_l = 1.f / lr;
 #pragma unroll
       for (int d0 = 0; d0 < D; d0 += 32) {
         uint32_t o[32];

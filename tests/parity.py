@@ -34,6 +34,17 @@ def bf16_ulp(x: np.ndarray) -> np.ndarray:
     return 2.0 ** (np.floor(np.log2(ax)) - 7)
 
 
+def bf16_ulp_distance(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """Number of bf16 steps between bf16-representable a and b (both given
+    as float64 holding bf16 values): distance of their ordered bit patterns."""
+    def ordered(x):
+        bits = torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16).view(torch.int16).numpy()
+        u = bits.astype(np.int64) & 0xFFFF
+        neg = u >= 0x8000
+        return np.where(neg, 0x8000 - u, u)  # monotone in the value, -0 == +0
+    return np.abs(ordered(a) - ordered(b))
+
+
 def gather(t: torch.Tensor, rows: np.ndarray, heads: np.ndarray) -> np.ndarray:
     """t[rows[i], heads[i], :] as fp64 numpy (t on CPU)."""
     r = torch.from_numpy(rows)
@@ -61,15 +72,27 @@ def fwd_metrics(out_gpu: np.ndarray, lse_gpu: np.ndarray, o_ref: np.ndarray, lse
     m = {
         "pairs": int(o_ref.shape[0]),
         "o_max_abs": float(d.max()) if d.size else 0.0,
-        "o_max_ulps": float((d / bf16_ulp(ref_b)).max()) if d.size else 0.0,
         "o_cosine": float((out_gpu * ref_b).sum() / max(np.linalg.norm(out_gpu) * np.linalg.norm(ref_b), 1e-300))
         if d.size and np.linalg.norm(ref_b) > 0 else 1.0,
         "lse_max_abs": float(np.abs(lse_gpu[finite_l] - lse_ref[finite_l]).max()) if finite_l.any() else 0.0,
         "lse_inf_match": bool(np.array_equal(lse_gpu[~finite_l], lse_ref[~finite_l])),
         "o_beyond_bound": int((d > O_MAX_ABS).sum()),
-        "o_beyond_bound_gt_1ulp": int(((d > O_MAX_ABS) & (d > bf16_ulp(ref_b))).sum()),
+        "o_max_ulp_distance": int(bf16_ulp_distance(out_gpu, ref_b).max()) if d.size else 0,
+        "o_beyond_bound_gt_1ulp": int(((d > O_MAX_ABS) & (bf16_ulp_distance(out_gpu, ref_b) > 1)).sum()),
     }
     return m
+
+
+def worst_elements(out_gpu, o_ref, rows, heads, k=5):
+    """The k largest |gpu - bf16(ref)| entries as (row, head, d, gpu, ref)."""
+    ref_b = bf16_round(o_ref)
+    d = np.abs(out_gpu - ref_b)
+    flat = np.argsort(d, axis=None)[::-1][:k]
+    res = []
+    for f in flat:
+        i, j = np.unravel_index(f, d.shape)
+        res.append((int(rows[i]), int(heads[i]), int(j), float(out_gpu[i, j]), float(o_ref[i, j])))
+    return res
 
 
 def assert_fwd(m: dict, allow_one_ulp_above: float | None = None):

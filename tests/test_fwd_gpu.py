@@ -37,6 +37,7 @@ def _fwd_case(w: W.Workload, seed=0, pairs=None, plant=None, max_seqlen=None, al
     lse_gpu = lse.cpu().numpy()[heads, rows].astype(np.float64)
     m = P.fwd_metrics(o_gpu, lse_gpu, o_ref, lse_ref)
     print(w.name, m)
+    print(w.name, "worst (row, head, d, gpu, exact):", P.worst_elements(o_gpu, o_ref, rows, heads))
     P.assert_fwd(m, allow_one_ulp_above=allow_ulp)
     return out, lse, m
 
