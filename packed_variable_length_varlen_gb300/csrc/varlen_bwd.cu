@@ -111,29 +111,30 @@ struct BwdCfg {
   static constexpr int K_BYTES = KCH * KV_CHUNK;
   static constexpr int V_BYTES = NC * KV_CHUNK;
   static constexpr int Q_BYTES = NC * Q_CHUNK;   // one Q or dO tile
-  static constexpr int NSTAGE = 2;
+  static constexpr int NSTAGE = 3;               // Q / dO ring depth
   static constexpr int PS_BYTES = 128 * 128;     // P^T or dS^T: 128 kv rows x 64 q (bf16)
   static constexpr int SMEM_BYTES = 1024 + 1024 + K_BYTES + V_BYTES + NSTAGE * 2 * Q_BYTES + 2 * PS_BYTES;
-  static constexpr int S_COL = 0, DP_COL = 64, DQ_COL = 128, DV_COL = 256, DK_COL = 384;
+  // TMEM columns: two S^T buffers, dP^T, dQ^T, dV, dK
+  static constexpr int S_COL = 0, DP_COL = 128, DQ_COL = 192, DV_COL = 256, DK_COL = 384;
   static constexpr int TMEM_COLS = 512;
 };
 
 struct BwdBarriers {
   uint64_t kv_full, kv_empty;
-  uint64_t qd_full[2], qd_empty[2];
-  uint64_t sp_full, ds_ready, step_done, mma_done;
+  uint64_t qd_full[3], qd_empty[3];
+  uint64_t s_full[2], dp_full, ds_ready, step_done, mma_done;
   uint32_t tmem_base;
   int abort;
 };
 
+// Clears rows [row_from, row_to) of a tile made of `chunks` chunks of
+// 128-byte rows; the warp's lanes store consecutive 16-byte units.
 __device__ __forceinline__ void zero_rows(uint8_t* tile, int chunks, int chunk_bytes, int row_from, int row_to,
                                           int lane) {
-  for (int r = row_from + lane; r < row_to; r += 32) {
-    for (int cc = 0; cc < chunks; ++cc) {
-      uint4* row = reinterpret_cast<uint4*>(tile + cc * chunk_bytes + r * 128);
-#pragma unroll
-      for (int u = 0; u < 8; ++u) row[u] = make_uint4(0, 0, 0, 0);
-    }
+  const int units = (row_to - row_from) * 8;
+  for (int cc = 0; cc < chunks; ++cc) {
+    uint4* base = reinterpret_cast<uint4*>(tile + cc * chunk_bytes + row_from * 128);
+    for (int u = lane; u < units; u += 32) base[u] = make_uint4(0, 0, 0, 0);
   }
 }
 
@@ -159,11 +160,13 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bar.kv_full, 1);
     mbar_init(&bar.kv_empty, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::NSTAGE; ++i) {
       mbar_init(&bar.qd_full[i], 1);
       mbar_init(&bar.qd_empty[i], 1);
     }
-    mbar_init(&bar.sp_full, 1);
+    mbar_init(&bar.s_full[0], 1);
+    mbar_init(&bar.s_full[1], 1);
+    mbar_init(&bar.dp_full, 1);
     mbar_init(&bar.ds_ready, 256);
     mbar_init(&bar.step_done, 1);
     mbar_init(&bar.mma_done, 1);
@@ -205,8 +208,8 @@ __global__ void __launch_bounds__(384, 1)
         ++tiles;
         const int32_t nq = (c.olen + QT - 1) / QT;
         for (int32_t j = 0; j < nq; ++j, ++gs) {
-          const uint32_t st = gs & 1;
-          if (!mbar_wait(&bar.qd_empty[st], ((gs >> 1) & 1) ^ 1, abort)) { ok = false; break; }
+          const uint32_t st = gs % C::NSTAGE;
+          if (!mbar_wait(&bar.qd_empty[st], ((gs / C::NSTAGE) & 1) ^ 1, abort)) { ok = false; break; }
           mbar_arrive_expect_tx(&bar.qd_full[st], 2 * C::Q_BYTES);
           uint8_t* qs = qd_smem + st * 2 * C::Q_BYTES;
           const int32_t qrow = c.o0 + j * QT;
@@ -220,14 +223,17 @@ __global__ void __launch_bounds__(384, 1)
       if (*abort) {
         int dummy = 0;
         if (tiles > 0) mbar_wait(&bar.kv_full, (tiles - 1) & 1, &dummy, 100000000ull);
-        for (uint32_t s = 0; s < 2 && s < gs; ++s) {
-          const uint32_t last = gs - 1 - ((gs - 1 - s) & 1);
-          mbar_wait(&bar.qd_full[s], (last >> 1) & 1, &dummy, 100000000ull);
+        for (uint32_t s = 0; s < C::NSTAGE && s < gs; ++s) {
+          const uint32_t last = gs - 1 - ((gs - 1 - s) % C::NSTAGE);
+          mbar_wait(&bar.qd_full[s], (last / C::NSTAGE) & 1, &dummy, 100000000ull);
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Per q step j the tensor pipe runs  S^T_{j+1}, dV_j, dK_j, dQ^T_j, dP^T_{j+1}
+    // so that S^T of the next step is ready while the compute warps finish
+    // step j, and P of step j+1 can be built while dV/dK/dQ^T of step j run.
     constexpr uint32_t kIdS = idesc_bf16_f32(128, QT, false, false);   // S^T, dP^T
     constexpr uint32_t kIdG = idesc_bf16_f32(128, D, false, true);     // dV, dK
     constexpr uint32_t kIdQ = idesc_bf16_f32(128, QT, true, true);     // dQ^T
@@ -237,6 +243,44 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t k_base = smem_addr(k_smem), v_base = smem_addr(v_smem);
     const uint32_t pt_base = smem_addr(pt_smem), dst_base = smem_addr(dst_smem);
     bool ok = true;
+
+    // Waits for the Q / dO tiles of global step g (tile-local step j), clears
+    // rows past the segment end; returns the stage's Q base address.
+    auto ready_q = [&](uint32_t g, int32_t j, uint32_t& q_base) -> bool {
+      const uint32_t st = g % C::NSTAGE;
+      if (!mbar_wait(&bar.qd_full[st], (g / C::NSTAGE) & 1, abort)) return false;
+      uint8_t* qs = qd_smem + st * 2 * C::Q_BYTES;
+      const int32_t q_valid = c.olen - j * QT;
+      if (q_valid < QT) {
+        // Q / dO rows past the segment end meet P^T = dS^T = 0 in dK / dV.
+        zero_rows(qs, 2 * C::NC, C::Q_CHUNK, q_valid, QT, lane);
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      q_base = smem_addr(qs);
+      return true;
+    };
+    auto issue_s = [&](uint32_t g, uint32_t q_base) {
+      const uint32_t sc = C::S_COL + (g & 1) * 64;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t ko = (kk >> 2) * C::KV_CHUNK + (kk & 3) * 32;
+        const uint32_t qo = (kk >> 2) * C::Q_CHUNK + (kk & 3) * 32;
+        mma_ss(tmem + sc, sw128_desc(k_base + ko, 16, 1024), sw128_desc(q_base + qo, 16, 1024), kIdS, kk > 0);
+      }
+      mma_commit(&bar.s_full[g & 1]);
+    };
+    auto issue_dp = [&](uint32_t do_base) {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t ko = (kk >> 2) * C::KV_CHUNK + (kk & 3) * 32;
+        const uint32_t qo = (kk >> 2) * C::Q_CHUNK + (kk & 3) * 32;
+        mma_ss(tmem + C::DP_COL, sw128_desc(v_base + ko, 16, 1024), sw128_desc(do_base + qo, 16, 1024), kIdS,
+               kk > 0);
+      }
+      mma_commit(&bar.dp_full);
+    };
+
     for (int64_t t = blockIdx.x;
          ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q); t += G) {
       if (c.olen == 0) continue;
@@ -252,40 +296,28 @@ __global__ void __launch_bounds__(384, 1)
       }
       __syncwarp();
       const int32_t nq = (c.olen + QT - 1) / QT;
+      // prologue: S^T_0 and dP^T_0
+      uint32_t q_cur = 0;
+      if (!ready_q(gs, 0, q_cur)) break;
+      tc_fence_after();
+      if (lane == 0) {
+        issue_s(gs, q_cur);
+        issue_dp(q_cur + C::Q_BYTES);
+      }
+      __syncwarp();
       for (int32_t j = 0; j < nq; ++j, ++gs) {
-        const uint32_t st = gs & 1;
-        if (!mbar_wait(&bar.qd_full[st], (gs >> 1) & 1, abort)) { ok = false; break; }
-        uint8_t* qs = qd_smem + st * 2 * C::Q_BYTES;
-        const int32_t q_valid = c.olen - j * QT;
-        if (q_valid < QT) {
-          // Q / dO rows past the segment end meet P^T = dS^T = 0 in dK / dV.
-          zero_rows(qs, 2 * C::NC, C::Q_CHUNK, q_valid, QT, lane);
-          fence_proxy_async_smem();
+        uint32_t q_next = 0;
+        const bool more = j + 1 < nq;
+        if (more) {
+          if (!ready_q(gs + 1, j + 1, q_next)) { ok = false; break; }
+          tc_fence_after();
+          if (lane == 0) issue_s(gs + 1, q_next);
+          __syncwarp();
         }
-        __syncwarp();
-        tc_fence_after();
-        const uint32_t q_base = smem_addr(qs), do_base = q_base + C::Q_BYTES;
-        if (lane == 0) {
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ko = (kk >> 2) * C::KV_CHUNK + (kk & 3) * 32;
-            const uint32_t qo = (kk >> 2) * C::Q_CHUNK + (kk & 3) * 32;
-            mma_ss(tmem + C::S_COL, sw128_desc(k_base + ko, 16, 1024), sw128_desc(q_base + qo, 16, 1024), kIdS,
-                   kk > 0);
-          }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ko = (kk >> 2) * C::KV_CHUNK + (kk & 3) * 32;
-            const uint32_t qo = (kk >> 2) * C::Q_CHUNK + (kk & 3) * 32;
-            mma_ss(tmem + C::DP_COL, sw128_desc(v_base + ko, 16, 1024), sw128_desc(do_base + qo, 16, 1024), kIdS,
-                   kk > 0);
-          }
-          mma_commit(&bar.sp_full);
-        }
-        __syncwarp();
         if (!mbar_wait(&bar.ds_ready, gs & 1, abort)) { ok = false; break; }
         tc_fence_after();
         if (lane == 0) {
+          const uint32_t do_base = q_cur + C::Q_BYTES;
 #pragma unroll
           for (int kk = 0; kk < QT / 16; ++kk) {
             mma_ss(tmem + C::DV_COL, sw128_desc(pt_base + kk * 32, 16, 1024),
@@ -294,18 +326,20 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int kk = 0; kk < QT / 16; ++kk) {
             mma_ss(tmem + C::DK_COL, sw128_desc(dst_base + kk * 32, 16, 1024),
-                   sw128_desc(q_base + kk * 2048, C::Q_CHUNK, 1024), kIdG, (j > 0 || kk > 0) ? 1u : 0u);
+                   sw128_desc(q_cur + kk * 2048, C::Q_CHUNK, 1024), kIdG, (j > 0 || kk > 0) ? 1u : 0u);
           }
 #pragma unroll
           for (int kk = 0; kk < kTileM / 16; ++kk) {
             mma_ss(tmem + C::DQ_COL, sw128_desc(k_base + kk * 2048, C::KV_CHUNK, 1024),
                    sw128_desc(dst_base + kk * 2048, C::PS_BYTES, 1024), kIdQ, kk > 0 ? 1u : 0u);
           }
-          mma_commit(&bar.qd_empty[st]);
+          mma_commit(&bar.qd_empty[gs % C::NSTAGE]);
           mma_commit(&bar.step_done);
-          if (j == nq - 1) mma_commit(&bar.kv_empty);
+          if (!more) mma_commit(&bar.kv_empty);
+          if (more) issue_dp(q_next + C::Q_BYTES);
         }
         __syncwarp();
+        q_cur = q_next;
       }
     }
     if (lane == 0) {
@@ -326,6 +360,26 @@ __global__ void __launch_bounds__(384, 1)
     cursor_init<kTileM>(c, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q);
     uint32_t gs = 0;
     bool ok = true;
+
+    // dQ^T of global step g (tile-local step j): wait, then add into dq_acc.
+    auto drain_dq = [&](uint32_t g, int32_t j, int32_t h) -> bool {
+      if (!mbar_wait(&bar.step_done, g & 1, abort)) return false;
+      tc_fence_after();
+      uint32_t q32[32];
+      tmem_ld32(tmem + lane_off + C::DQ_COL + half * 32, q32);
+      tmem_wait_ld();
+      const int32_t qs0 = j * QT + half * 32;  // first q column of this thread, in the segment
+      if (r < D) {
+        float* dst = p.dq_acc + (((int64_t)c.o0 + qs0) * H + h) * D + r;
+        const int64_t step = (int64_t)H * D;
+        const int32_t n = min(32, c.olen - qs0);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (i < n) atomicAdd(dst + i * step, __uint_as_float(q32[i]));
+      }
+      return true;
+    };
+
     for (int64_t t = blockIdx.x;
          ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q); t += G) {
       const Tile tl = cursor_tile(c, t);
@@ -333,56 +387,51 @@ __global__ void __launch_bounds__(384, 1)
       const bool row_valid = r < kv_valid;
       const int64_t krow = (int64_t)c.r0 + tl.m * kTileM + r;
       const int32_t nq = (c.olen + QT - 1) / QT;
-      const float* lse2 = p.lse2 + (int64_t)tl.h * p.total_q;
-      const float* delta = p.delta + (int64_t)tl.h * p.total_q;
-      for (int32_t j = 0; j <= nq; ++j) {
-        // ---- dQ^T of step j-1: wait for it, add it into the accumulator
-        if (j > 0) {
-          const uint32_t gp = gs - 1;
-          if (!mbar_wait(&bar.step_done, gp & 1, abort)) { ok = false; break; }
-          tc_fence_after();
-          uint32_t q32[32];
-          tmem_ld32(tmem + lane_off + C::DQ_COL + half * 32, q32);
-          tmem_wait_ld();
-          const int32_t qs0 = (j - 1) * QT + half * 32;  // first q column of this thread, in the segment
-          if (r < D) {
-            float* dst = p.dq_acc + (((int64_t)c.o0 + qs0) * H + tl.h) * D + r;
-            const int64_t step = (int64_t)H * D;
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (qs0 + i < c.olen) atomicAdd(dst + i * step, __uint_as_float(q32[i]));
-          }
+      const float* lse2 = p.lse2 + (int64_t)tl.h * p.total_q + c.o0;
+      const float* delta = p.delta + (int64_t)tl.h * p.total_q + c.o0;
+      for (int32_t j = 0; j < nq; ++j, ++gs) {
+        const int32_t qc0 = j * QT + half * 32;              // first q column (in the segment)
+        const int32_t ncol = min(32, c.olen - qc0);          // valid columns of this thread (may be <= 0)
+        // lane i fetches column i's lse2 / delta; broadcast below
+        float my_l2 = 0.f, my_dl = 0.f;
+        if (lane < ncol) {
+          my_l2 = __ldg(lse2 + qc0 + lane);
+          my_dl = __ldg(delta + qc0 + lane);
         }
-        if (j == nq) break;
-        // ---- P^T and dS^T of step j
-        if (!mbar_wait(&bar.sp_full, gs & 1, abort)) { ok = false; break; }
+        const int32_t nvalid = row_valid ? max(0, ncol) : 0;
+        // ---- P^T = exp2(S^T c - lse2) as soon as S^T_j is ready
+        if (!mbar_wait(&bar.s_full[gs & 1], (gs >> 1) & 1, abort)) { ok = false; break; }
         tc_fence_after();
-        uint32_t sv[32], dpv[32];
-        tmem_ld32(tmem + lane_off + C::S_COL + half * 32, sv);
+        uint32_t sv[32];
+        tmem_ld32(tmem + lane_off + C::S_COL + (gs & 1) * 64 + half * 32, sv);
+        tmem_wait_ld();
+        float pv[32];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float2 l2 = make_float2(__shfl_sync(0xffffffffu, my_l2, i), __shfl_sync(0xffffffffu, my_l2, i + 1));
+          float2 t2 = ffma2(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), make_float2(c2, c2),
+                            make_float2(-l2.x, -l2.y));
+          pv[i] = (i < nvalid) ? ex2(t2.x) : 0.f;
+          pv[i + 1] = (i + 1 < nvalid) ? ex2(t2.y) : 0.f;
+        }
+        // ---- dQ^T of the previous step (finished before dP^T_j in the pipe)
+        if (j > 0 && !drain_dq(gs - 1, j - 1, tl.h)) { ok = false; break; }
+        // ---- dS^T = P^T (dP^T - delta)
+        if (!mbar_wait(&bar.dp_full, gs & 1, abort)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t dpv[32];
         tmem_ld32(tmem + lane_off + C::DP_COL + half * 32, dpv);
         tmem_wait_ld();
-        const int32_t qc0 = j * QT + half * 32;            // first q column (in the segment)
-        const int32_t nvalid = row_valid ? min(32, max(0, c.olen - qc0)) : 0;
         uint32_t pk[16], dk2[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float pv[2], dsv[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int col = 2 * i + e;
-            float pe = 0.f, de = 0.f;
-            if (col < nvalid) {
-              const int64_t qi = (int64_t)c.o0 + qc0 + col;
-              const float l2 = __ldg(lse2 + qi);
-              const float dl = __ldg(delta + qi);
-              pe = ex2(fmaf(__uint_as_float(sv[col]), c2, -l2));
-              de = pe * (__uint_as_float(dpv[col]) - dl);
-            }
-            pv[e] = pe;
-            dsv[e] = de;
-          }
-          pk[i] = pack_bf16x2(pv[0], pv[1]);
-          dk2[i] = pack_bf16x2(dsv[0], dsv[1]);
+        for (int i = 0; i < 32; i += 2) {
+          const float2 dl = make_float2(__shfl_sync(0xffffffffu, my_dl, i), __shfl_sync(0xffffffffu, my_dl, i + 1));
+          const float2 ds = fmul2(make_float2(pv[i], pv[i + 1]),
+                                  fadd2(make_float2(__uint_as_float(dpv[i]), __uint_as_float(dpv[i + 1])),
+                                        make_float2(-dl.x, -dl.y)));
+          // select, not multiply: dP^T rows past the segment end may hold NaN
+          pk[i / 2] = pack_bf16x2(pv[i], pv[i + 1]);
+          dk2[i / 2] = pack_bf16x2(i < nvalid ? ds.x : 0.f, i + 1 < nvalid ? ds.y : 0.f);
         }
         // write this thread's 64 bytes of the P^T and dS^T rows (128-byte
         // swizzle: 16-byte unit u of row r sits at unit u ^ (r % 8))
@@ -397,22 +446,19 @@ __global__ void __launch_bounds__(384, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&bar.ds_ready);
-        ++gs;
       }
       if (!ok) break;
+      if (nq > 0 && !drain_dq(gs - 1, nq - 1, tl.h)) break;
       // ---- epilogue: dV and dK * scale of this kv tile (zeros if no queries)
-      if (row_valid) {
+      if (row_valid && nq == 0) {
         __nv_bfloat16* dvrow = p.dv + krow * p.dv_rs + (int64_t)tl.h * p.dv_hs;
         __nv_bfloat16* dkrow = p.dk + krow * p.dk_rs + (int64_t)tl.h * p.dk_hs;
-        if (nq == 0) {
-          for (int d = half * (D / 2); d < (half + 1) * (D / 2); d += 8) {
-            *reinterpret_cast<uint4*>(dvrow + d) = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(dkrow + d) = make_uint4(0, 0, 0, 0);
-          }
+        for (int d = half * (D / 2); d < (half + 1) * (D / 2); d += 8) {
+          *reinterpret_cast<uint4*>(dvrow + d) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(dkrow + d) = make_uint4(0, 0, 0, 0);
         }
       }
       if (nq > 0) {
-        tc_fence_after();
 #pragma unroll
         for (int d0 = half * (D / 2); d0 < (half + 1) * (D / 2); d0 += 16) {
           uint32_t a[16], b[16];

@@ -10,9 +10,8 @@
 //                TMEM.  Owns the TMEM allocation.
 //   warps 4..7   softmax / correction / epilogue: thread = one q row = one
 //                TMEM lane.  Masks key columns past the segment end, keeps
-//                the running max m and the row sums of P (fp32, for LSE) and
-//                of bf16(P) (for O's normalisation), writes P = exp2(S*c - m)
-//                back into TMEM as bf16 (aliasing S), rescales O in TMEM when m
+//                the running max m and sum l, writes P = exp2(S*c - m) back
+//                into TMEM as bf16 (aliasing S), rescales O in TMEM when m
 //                grows by more than 2^8 (exact: O and l carry the same
 //                factor), and finally writes O / l (bf16) and LSE.
 //   warps 2,3    idle.
@@ -203,13 +202,10 @@ __global__ void __launch_bounds__(256, 1)
             // Rows past the segment end hold the next segment's values (or
             // TMA zero fill).  P is 0 there, but 0 * NaN would still poison
             // O, so clear those rows before the MMA reads them.
-            for (int r = kv_valid + lane; r < kTileN; r += 32) {
 #pragma unroll
-              for (int cc = 0; cc < C::NC; ++cc) {
-                uint4* row = reinterpret_cast<uint4*>(vtile + cc * C::CHUNK + r * 128);
-#pragma unroll
-                for (int u = 0; u < 8; ++u) row[u] = make_uint4(0, 0, 0, 0);
-              }
+            for (int cc = 0; cc < C::NC; ++cc) {
+              uint4* base = reinterpret_cast<uint4*>(vtile + cc * C::CHUNK + kv_valid * 128);
+              for (int u = lane; u < (kTileN - kv_valid) * 8; u += 32) base[u] = make_uint4(0, 0, 0, 0);
             }
             fence_proxy_async_smem();
           }
@@ -264,7 +260,7 @@ __global__ void __launch_bounds__(256, 1)
         continue;
       }
       const int32_t nkv = (c.olen + kTileN - 1) / kTileN;
-      float m_use = -INFINITY, l = 0.f, lr = 0.f;
+      float m_use = -INFINITY, l = 0.f;
       for (int32_t j = 0; j < nkv; ++j) {
         const uint32_t gj = g + j;
         const uint32_t sb = gj % C::NSBUF;
@@ -291,9 +287,16 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
           for (int i = 0; i < 128; ++i) x[i] = (i < kv_valid) ? x[i] : -INFINITY;
         }
-        float mx = x[0];
+        // row max: four independent chains of 3-input max
+        float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
 #pragma unroll
-        for (int i = 1; i < 128; ++i) mx = fmaxf(mx, x[i]);
+        for (int i = 0; i < 128; i += 8) {
+          m0 = fmax3(m0, x[i], x[i + 1]);
+          m1 = fmax3(m1, x[i + 2], x[i + 3]);
+          m2 = fmax3(m2, x[i + 4], x[i + 5]);
+          m3 = fmax3(m3, x[i + 6], x[i + 7]);
+        }
+        const float mx = fmaxf(fmax3(m0, m1, m2), m3);
         const float m_new = fmaxf(m_use, mx * c2);
         float alpha = 1.f;
         bool rescale = false;
@@ -304,23 +307,20 @@ __global__ void __launch_bounds__(256, 1)
           m_use = m_new;
           rescale = true;
         }
-        // Two row sums: l of the fp32 P (for LSE) and lr of the bf16-rounded
-        // P -- the weights the P V MMA actually applies -- so that O / lr is
-        // a consistently normalised average and P's rounding cancels in rows
-        // dominated by a few keys.
-        float rs = 0.f, rr0 = 0.f, rr1 = 0.f;
+        // P = exp2(S*c - m) two lanes at a time; row sum of the fp32 P
+        const float2 cc2 = make_float2(c2, c2), negm = make_float2(-m_use, -m_use);
+        float2 rs2a = make_float2(0.f, 0.f), rs2b = make_float2(0.f, 0.f);
         uint32_t pk[64];
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
-          const float p0 = ex2(fmaf(x[2 * i], c2, -m_use));
-          const float p1 = ex2(fmaf(x[2 * i + 1], c2, -m_use));
-          pk[i] = pack_bf16x2(p0, p1);
-          rs += p0 + p1;
-          rr0 += __uint_as_float(pk[i] << 16);
-          rr1 += __uint_as_float(pk[i] & 0xffff0000u);
+          float2 t = ffma2(make_float2(x[2 * i], x[2 * i + 1]), cc2, negm);
+          t.x = ex2(t.x);
+          t.y = ex2(t.y);
+          pk[i] = pack_bf16x2(t.x, t.y);
+          if (i & 1) rs2b = fadd2(rs2b, t); else rs2a = fadd2(rs2a, t);
         }
+        const float rs = (rs2a.x + rs2a.y) + (rs2b.x + rs2b.y);
         l = fmaf(l, alpha, rs);
-        lr = fmaf(lr, alpha, rr0 + rr1);
         {
           const uint32_t ta = tmem + lane_off + sb * 128;
           tmem_st32(ta + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(256, 1)
       const uint32_t gl = g + nkv - 1;
       if (!mbar_wait(&bar.s_free[gl % C::NSBUF], (gl / C::NSBUF) & 1, abort)) break;
       tc_fence_after();
-      const float inv_l = 1.f / lr;
+      const float inv_l = 1.f / l;
 #pragma unroll
       for (int d0 = 0; d0 < D; d0 += 32) {
         uint32_t o[32];

@@ -78,7 +78,13 @@ def fwd_metrics(out_gpu: np.ndarray, lse_gpu: np.ndarray, o_ref: np.ndarray, lse
         "lse_inf_match": bool(np.array_equal(lse_gpu[~finite_l], lse_ref[~finite_l])),
         "o_beyond_bound": int((d > O_MAX_ABS).sum()),
         "o_max_ulp_distance": int(bf16_ulp_distance(out_gpu, ref_b).max()) if d.size else 0,
-        "o_beyond_bound_gt_1ulp": int(((d > O_MAX_ABS) & (bf16_ulp_distance(out_gpu, ref_b) > 1)).sum()),
+        # beyond 1e-2 by more than one bf16 ulp, measured at the larger of
+        # the two magnitudes (a pair straddling a power of two is one ulp of
+        # the upper binade apart)
+        "o_beyond_bound_gt_1ulp": int(((d > O_MAX_ABS)
+                                       & (d > bf16_ulp(np.maximum(np.abs(out_gpu), np.abs(ref_b))))).sum()),
+        "o_beyond_bound_gt_2ulp": int(((d > O_MAX_ABS)
+                                       & (d > 2 * bf16_ulp(np.maximum(np.abs(out_gpu), np.abs(ref_b))))).sum()),
     }
     return m
 
@@ -95,17 +101,23 @@ def worst_elements(out_gpu, o_ref, rows, heads, k=5):
     return res
 
 
-def assert_fwd(m: dict, allow_one_ulp_above: float | None = None):
-    """Literal bounds; with allow_one_ulp_above, elements whose reference has
-    |value| >= that threshold may exceed 1e-2 by at most one bf16 ulp (the
-    bf16 spacing there is itself above 1e-2)."""
+def assert_fwd(m: dict, allow_one_ulp_above: float | None = None, ulps: int = 1):
+    """Literal bounds.  With allow_one_ulp_above (inputs large enough that
+    |O| reaches 2 and beyond, where one bf16 ulp is itself >= 1.6e-2),
+    elements past 1e-2 may differ from bf16(exact) by at most `ulps` bf16
+    ulps of their magnitude.  The P V product takes P in bf16 (relative
+    rounding 2^-9 per weight), which moves O by up to 2^-9 * max|v| before
+    the output is rounded: 0.016 for the amplitude-2 workload, one ulp at
+    |O| in [2, 4), so two-ulp results are possible there."""
     assert m["lse_inf_match"], m
     assert m["lse_max_abs"] <= LSE_MAX_ABS, m
     assert m["o_cosine"] >= O_COSINE, m
     if allow_one_ulp_above is None:
         assert m["o_max_abs"] <= O_MAX_ABS, m
-    else:
+    elif ulps <= 1:
         assert m["o_beyond_bound_gt_1ulp"] == 0, m
+    else:
+        assert m["o_beyond_bound_gt_2ulp"] == 0, m
 
 
 def rel_fro(a: np.ndarray, ref: np.ndarray) -> float:

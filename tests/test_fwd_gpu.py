@@ -15,7 +15,8 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _fwd_case(w: W.Workload, seed=0, pairs=None, plant=None, max_seqlen=None, allow_ulp=None, canary=12345.0):
+def _fwd_case(w: W.Workload, seed=0, pairs=None, plant=None, max_seqlen=None, allow_ulp=None, ulps=1,
+              canary=12345.0):
     cpu = W.make_inputs(w, seed, with_dout=False)
     if plant is not None:
         plant(cpu)
@@ -38,7 +39,7 @@ def _fwd_case(w: W.Workload, seed=0, pairs=None, plant=None, max_seqlen=None, al
     m = P.fwd_metrics(o_gpu, lse_gpu, o_ref, lse_ref)
     print(w.name, m)
     print(w.name, "worst (row, head, d, gpu, exact):", P.worst_elements(o_gpu, o_ref, rows, heads))
-    P.assert_fwd(m, allow_one_ulp_above=allow_ulp)
+    P.assert_fwd(m, allow_one_ulp_above=allow_ulp, ulps=ulps)
     return out, lse, m
 
 
@@ -123,7 +124,8 @@ def test_fwd_windowed_full():
 def test_fwd_ragged_full():
     w = W.ragged()
     extra = [W.offset_crossing_row(w.row_stride, 2)]
-    _fwd_case(w, pairs=_sampled_pairs(w, 2, extra), allow_ulp=1.28)
+    # amplitude-2 inputs: |O| reaches 8; see parity.assert_fwd for the ulp bound
+    _fwd_case(w, pairs=_sampled_pairs(w, 2, extra), allow_ulp=1.28, ulps=2)
 
 
 @pytest.mark.slow
