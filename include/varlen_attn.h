@@ -115,6 +115,33 @@ int varlen_attn_bwd(const void* q, varlen_stride sq, const void* k, varlen_strid
                     void* dv, varlen_stride sdv, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Backward without a workspace argument, for callers that cannot allocate
+ * device memory (code inside a host framework that owns every device
+ * allocation, or on a path where cudaMalloc is not allowed).  The paper has
+ * no counterpart: this is a deployment variant of varlen_attn_bwd.
+ * Arguments, layouts and results are those of varlen_attn_bwd; the scratch
+ * (the fp32 dQ accumulator, delta and log2-domain LSE) lives in a fixed
+ * file-scope device array of VARLEN_NOALLOC_SCRATCH_BYTES bytes that every
+ * GPU loading the library keeps until exit.  The call allocates nothing.
+ * Returns VARLEN_ERR_WORKSPACE, before anything is enqueued, when the
+ * problem needs more than that (varlen_attn_bwd_workspace_size() >
+ * VARLEN_NOALLOC_SCRATCH_BYTES; at H=16, D=96 that is about 10,700 q rows).
+ * The first call on a device looks up the array's device address (with that
+ * device current) and should come before any stream capture.  Every call
+ * shares the one array: it is fully rewritten by each call before it is
+ * read, but calls that overlap on the GPU (unordered streams) race on it.
+ */
+#define VARLEN_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+int varlen_attn_bwd_noalloc(const void* q, varlen_stride sq, const void* k, varlen_stride sk, const void* v,
+                            varlen_stride sv, const void* out, varlen_stride so, const void* dout,
+                            varlen_stride sdo, const float* lse, const int32_t* cu_seqlens_q,
+                            const int32_t* cu_seqlens_k, int32_t batch, int32_t total_q, int32_t total_k,
+                            int32_t num_heads, int32_t head_dim, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                            float scale, void* dq, varlen_stride sdq, void* dk, varlen_stride sdk, void* dv,
+                            varlen_stride sdv, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device error word:
  * VARLEN_OK, VARLEN_ERR_TIMEOUT, VARLEN_ERR_DEVICE_BOUNDS, or VARLEN_ERR_CUDA
  * if the stream itself reports an error.

@@ -58,6 +58,9 @@ def _load() -> ctypes.CDLL:
     lib.varlen_attn_bwd.restype = ctypes.c_int
     lib.varlen_attn_bwd.argtypes = [vp, S, vp, S, vp, S, vp, S, vp, S, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                     i32, f32, vp, S, vp, S, vp, S, vp, sz, vp]
+    lib.varlen_attn_bwd_noalloc.restype = ctypes.c_int
+    lib.varlen_attn_bwd_noalloc.argtypes = [vp, S, vp, S, vp, S, vp, S, vp, S, vp, vp, vp, i32, i32, i32, i32, i32,
+                                            i32, i32, f32, vp, S, vp, S, vp, S, vp]
     lib.varlen_attn_get_device_status.restype = ctypes.c_int
     lib.varlen_attn_get_device_status.argtypes = [vp]
     lib.varlen_attn_status_string.restype = ctypes.c_char_p
@@ -81,7 +84,10 @@ LIB_PATH = LIB._name
 EXPORTED = ("varlen_attn_fwd", "varlen_attn_bwd_workspace_size", "varlen_attn_bwd",
             "varlen_attn_get_device_status", "varlen_attn_status_string", "varlen_attn_tile_count",
             "varlen_attn_debug_schedule", "varlen_attn_selftest_wait_timeout", "varlen_attn_num_sms",
-            "varlen_attn_debug_set_phase_events")
+            "varlen_attn_debug_set_phase_events", "varlen_attn_bwd_noalloc")
+
+# Size of the fixed device array varlen_attn_bwd_noalloc uses as scratch.
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
 # ---------------------------------------------------------------- marshalling
@@ -128,6 +134,17 @@ def varlen_attn_bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, batch, 
                                _ptr(cu_seqlens_k), batch, total_q, total_k, num_heads, head_dim, max_seqlen_q,
                                max_seqlen_k, scale, _ptr(dq), _stride(dq), _ptr(dk), _stride(dk), _ptr(dv),
                                _stride(dv), _ptr(workspace), workspace_bytes, _stream(stream))
+
+
+def varlen_attn_bwd_noalloc(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k,
+                            num_heads, head_dim, max_seqlen_q, max_seqlen_k, scale, dq, dk, dv, stream=None) -> int:
+    """The backward for callers that cannot allocate device memory: scratch
+    comes from a fixed library-owned device array (see the C header)."""
+    return LIB.varlen_attn_bwd_noalloc(_ptr(q), _stride(q), _ptr(k), _stride(k), _ptr(v), _stride(v), _ptr(out),
+                                       _stride(out), _ptr(dout), _stride(dout), _ptr(lse), _ptr(cu_seqlens_q),
+                                       _ptr(cu_seqlens_k), batch, total_q, total_k, num_heads, head_dim,
+                                       max_seqlen_q, max_seqlen_k, scale, _ptr(dq), _stride(dq), _ptr(dk),
+                                       _stride(dk), _ptr(dv), _stride(dv), _stream(stream))
 
 
 def varlen_attn_get_device_status(stream=None) -> int:
