@@ -151,6 +151,10 @@ int varlen_attn_get_device_status(void* stream);
 /* Static description of a status code. */
 const char* varlen_attn_status_string(int status);
 
+/* Description of the CUDA error behind the last VARLEN_ERR_CUDA returned on
+ * the calling host thread ("no error" if none). */
+const char* varlen_attn_last_cuda_error(void);
+
 /* ---------------------------------------------------------------------------
  * Diagnostics (host logic and scheduler checks; not needed for normal use).
  */
@@ -170,7 +174,8 @@ int64_t varlen_attn_tile_count(const int32_t* cu_seqlens_host, int32_t batch, in
  * one record per visited tile into out_records (device int32, 4 per tile:
  * segment, row-block, head, cta).  Records are written at their global tile
  * index; records at index >= max_records are dropped.  Callers compare the
- * records against varlen_attn_tile_count.  `tile` is the row-block height.
+ * records against varlen_attn_tile_count.  `tile` is the row-block height:
+ * 256 (forward: two 128-row halves per unit), 128 (backward kv tiles) or 64.
  */
 int varlen_attn_debug_schedule(const int32_t* cu_seqlens, int32_t batch, int32_t total, int32_t num_heads,
                                int32_t tile, int32_t grid, int32_t* out_records, int64_t max_records,

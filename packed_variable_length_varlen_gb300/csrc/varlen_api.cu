@@ -123,6 +123,14 @@ int check_common(const int32_t* cu_q, const int32_t* cu_k, int32_t batch, int32_
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Last CUDA error an entry point saw on this host thread (for diagnostics).
+thread_local int g_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return VARLEN_ERR_CUDA;
+}
+
 // Optional profiling events for the three backward kernels (process-wide).
 cudaEvent_t g_phase_events[4] = {nullptr, nullptr, nullptr, nullptr};
 std::mutex g_phase_mu;
@@ -171,7 +179,7 @@ extern "C" int varlen_attn_fwd(const void* q, varlen_stride sq, const void* k, v
   L.head_dim = head_dim;
   L.grid = dev.sms;
   cudaError_t e = launch_fwd(L, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? VARLEN_OK : VARLEN_ERR_CUDA;
+  return e == cudaSuccess ? VARLEN_OK : cuda_fail(e);
 }
 
 extern "C" size_t varlen_attn_bwd_workspace_size(int32_t batch, int32_t total_q, int32_t num_heads,
@@ -249,11 +257,12 @@ extern "C" int varlen_attn_bwd(const void* q, varlen_stride sq, const void* k, v
     for (int i = 0; i < 4; ++i) L.phase_events[i] = g_phase_events[i];
   }
   cudaError_t e = launch_bwd(L, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? VARLEN_OK : VARLEN_ERR_CUDA;
+  return e == cudaSuccess ? VARLEN_OK : cuda_fail(e);
 }
 
 extern "C" int varlen_attn_get_device_status(void* stream) {
-  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return VARLEN_ERR_CUDA;
+  const cudaError_t se = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (se != cudaSuccess) return cuda_fail(se);
   unsigned int word = 0, zero = 0;
   if (cudaMemcpyFromSymbol(&word, g_device_error, sizeof(word)) != cudaSuccess) return VARLEN_ERR_CUDA;
   if (word != 0 && cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero)) != cudaSuccess) return VARLEN_ERR_CUDA;
@@ -297,7 +306,7 @@ extern "C" int varlen_attn_debug_schedule(const int32_t* cu, int32_t batch, int3
                                           void* stream) {
   if (cu == nullptr || out == nullptr) return VARLEN_ERR_NULL;
   if (batch < 1 || total < 0 || num_heads < 1 || grid < 1 || max_records < 0) return VARLEN_ERR_SHAPE;
-  if (tile != 64 && tile != 128) return VARLEN_ERR_SHAPE;
+  if (tile != 64 && tile != 128 && tile != 256) return VARLEN_ERR_SHAPE;
   DeviceInfo dev;
   int st = device_info(&dev);
   if (st != VARLEN_OK) return st;
@@ -320,6 +329,10 @@ extern "C" int varlen_attn_debug_set_phase_events(void* const* events, int count
   std::lock_guard<std::mutex> lock(g_phase_mu);
   for (int i = 0; i < 4; ++i) g_phase_events[i] = count ? static_cast<cudaEvent_t>(events[i]) : nullptr;
   return VARLEN_OK;
+}
+
+extern "C" const char* varlen_attn_last_cuda_error(void) {
+  return g_last_cuda_error == 0 ? "no error" : cudaGetErrorString(static_cast<cudaError_t>(g_last_cuda_error));
 }
 
 extern "C" int varlen_attn_num_sms(void) {

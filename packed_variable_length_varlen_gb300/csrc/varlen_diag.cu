@@ -25,7 +25,9 @@ __global__ void debug_schedule_kernel(const int32_t* cu, int32_t batch, int32_t 
 
 cudaError_t launch_debug_schedule(const int32_t* cu, int32_t batch, int32_t total, int32_t num_heads, int32_t tile,
                                   int32_t grid, int32_t* out, int64_t max_records, cudaStream_t stream) {
-  if (tile == 128)
+  if (tile == 256)
+    debug_schedule_kernel<256><<<grid, 32, 0, stream>>>(cu, batch, total, num_heads, out, max_records);
+  else if (tile == 128)
     debug_schedule_kernel<128><<<grid, 32, 0, stream>>>(cu, batch, total, num_heads, out, max_records);
   else
     debug_schedule_kernel<64><<<grid, 32, 0, stream>>>(cu, batch, total, num_heads, out, max_records);

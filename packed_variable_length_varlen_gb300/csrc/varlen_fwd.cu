@@ -1,20 +1,31 @@
 // varlen_fwd.cu -- forward kernel of packed variable-length attention on
-// sm_103a: persistent exact tile scheduler, TMA-fed Q tile and K/V ring,
+// sm_103a: persistent exact tile scheduler, TMA-fed Q tiles and K/V ring,
 // tcgen05 MMAs with TMEM accumulators, warp-specialised online softmax.
 //
-// Per CTA (256 threads, one CTA per SM):
-//   warp 0       TMA producer: Q tile, then K_j, V_j tiles into a ring of
+// One scheduled unit is 256 q rows of one (segment, head): two 128-row
+// halves A and B that share every K/V tile.  Per CTA (384 threads, one CTA
+// per SM):
+//   warp 0       TMA producer: Q_A, Q_B, then K_j, V_j tiles into a ring of
 //                shared-memory slots (mbarrier full/empty per slot).
-//   warp 1       MMA issuer (one lane): S_j = Q K_j^T into one of three TMEM
-//                score buffers, then O += P_{j-1} V_{j-1} with P read from
-//                TMEM.  Owns the TMEM allocation.
-//   warps 4..7   softmax / correction / epilogue: thread = one q row = one
-//                TMEM lane.  Masks key columns past the segment end, keeps
-//                the running max m and sum l, writes P = exp2(S*c - m) back
-//                into TMEM as bf16 (aliasing S), rescales O in TMEM when m
-//                grows by more than 2^8 (exact: O and l carry the same
-//                factor), and finally writes O / l (bf16) and LSE.
-//   warps 2,3    idle.
+//   warp 1       MMA issuer (one lane), per kv step j:
+//                  O_A += P_A V_j, S_A = Q_A K_{j+1}^T, O_B += P_B V_j,
+//                  S_B = Q_B K_{j+1}^T
+//                with S and P of each half in one 128-column TMEM region (P
+//                is written over S as bf16 and read by the MMA from TMEM).
+//                The next S of a half is issued right after that half's P V
+//                product: tcgen05 MMAs of one thread execute in issue order,
+//                so the new S overwrites P only after the product has read
+//                it.  While half A's softmax runs, the tensor core works on
+//                half B and the other way round.  Owns the TMEM allocation.
+//   warps 4..7   softmax / correction / epilogue of half A; warps 8..11 of
+//                half B.  Warp w reads TMEM lanes 32*(w % 4) .. +31, so each
+//                warpgroup covers all 128 rows; thread = one q row.
+//   warps 2,3    idle (they complete warpgroup 0 for the register split).
+//                Masks key columns past the segment end, keeps the running
+//                max m and sum l, writes P = exp2(S*c - m) into TMEM as
+//                bf16, rescales O in TMEM when m grows by more than 2^8
+//                (exact: O and l carry the same factor), and finally writes
+//                O / l (bf16) and LSE.
 //
 // Semantics: O = softmax(scale * Q_b K_b^T) V_b per segment b, with the
 // natural-log LSE per row -- the varlen attention called on the
@@ -28,22 +39,23 @@
 
 namespace varlen {
 
+constexpr int kFwdUnit = 2 * kTileM;  // q rows per scheduled unit (two halves)
+
 template <int D>
 struct FwdCfg {
   static constexpr int NC = (D + 63) / 64;              // 64-column chunks of a tile
   static constexpr int CHUNK = 128 * 128;               // 128 rows x 128 bytes
   static constexpr int TILE = NC * CHUNK;               // one Q / K / V tile
-  static constexpr int NSLOT = (NC == 1) ? 10 : 5;      // K/V ring slots
-  static constexpr int NSBUF = 3;                       // TMEM score buffers
-  static constexpr int O_COL = 384;                     // TMEM column of O
+  static constexpr int NSLOT = (NC == 1) ? 8 : 4;       // K/V ring slots
+  static constexpr int O_COL = 256;                     // TMEM column of O_A (O_B at +128)
   static constexpr int TMEM_COLS = 512;
-  static constexpr int SMEM_BYTES = 1024 + 1024 + TILE * (1 + NSLOT);
+  static constexpr int SMEM_BYTES = 1024 + 1024 + TILE * (2 + NSLOT);
   static constexpr int KSTEPS = D / 16;                 // K-steps of S = Q K^T
 };
 
 struct FwdBarriers {
   uint64_t q_full, q_empty;
-  uint64_t s_full[3], s_free[3], p_full[3];
+  uint64_t s_full[2], p_full[2], pv_done[2];
   uint64_t mma_done;
   uint64_t kv_full[10], kv_empty[10];
   uint32_t tmem_base;
@@ -51,16 +63,22 @@ struct FwdBarriers {
 };
 static_assert(sizeof(FwdBarriers) <= 1024, "barrier block too large");
 
+// Registers: the block launches 384 threads at 168 registers (64,512).
+// Warpgroup 0 (producer, MMA, two idle warps) drops to 96 and the two
+// softmax warpgroups rise to 176: 96*128 + 2*176*128 = 57,344 <= 64,512, and
+// each SM sub-partition holds one warp of each group: (96+176+176)*32 <= 16K.
+constexpr uint32_t kFwdRegsCtl = 96, kFwdRegsSoftmax = 176;
+
 template <int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     varlen_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   FwdBarriers& bar = *reinterpret_cast<FwdBarriers*>(smem);
-  uint8_t* q_smem = smem + 1024;
-  uint8_t* ring = q_smem + C::TILE;
+  uint8_t* q_smem = smem + 1024;           // Q_A then Q_B
+  uint8_t* ring = q_smem + 2 * C::TILE;
   volatile int* abort = &bar.abort;
 
   const int warp = threadIdx.x >> 5;
@@ -69,10 +87,10 @@ __global__ void __launch_bounds__(256, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bar.q_full, 1);
     mbar_init(&bar.q_empty, 1);
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&bar.s_full[i], 1);
-      mbar_init(&bar.s_free[i], 1);
       mbar_init(&bar.p_full[i], 128);
+      mbar_init(&bar.pv_done[i], 1);
     }
     mbar_init(&bar.mma_done, 1);
     for (int i = 0; i < C::NSLOT; ++i) {
@@ -90,6 +108,8 @@ __global__ void __launch_bounds__(256, 1)
 
   const int64_t G = gridDim.x;
 
+  if (warp < 4) {
+    warpgroup_reg_dealloc<kFwdRegsCtl>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -97,20 +117,24 @@ __global__ void __launch_bounds__(256, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       SegCursor c;
-      cursor_init<kTileM>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k);
+      cursor_init<kFwdUnit>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k);
       uint32_t q_loads = 0;
       uint32_t ring_pos = 0;  // loads issued into the ring so far
       bool ok = true;
-      for (int64_t t = blockIdx.x; ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_q, p.cu_k, p.batch, p.total_q,
-                                                               p.total_k);
+      for (int64_t t = blockIdx.x; ok && cursor_seek<kFwdUnit>(c, t, p.num_heads, p.cu_q, p.cu_k, p.batch,
+                                                                 p.total_q, p.total_k);
            t += G) {
         if (c.olen == 0) continue;  // no keys: the softmax role writes O = 0, LSE = -inf
         const Tile tl = cursor_tile(c, t);
-        const int32_t qrow = c.r0 + tl.m * kTileM;
+        const int32_t qrow = c.r0 + tl.m * kFwdUnit;
         if (q_loads > 0 && !mbar_wait(&bar.q_empty, (q_loads - 1) & 1, abort)) break;
-        mbar_arrive_expect_tx(&bar.q_full, C::TILE);
+        mbar_arrive_expect_tx(&bar.q_full, 2 * C::TILE);
 #pragma unroll
-        for (int cc = 0; cc < C::NC; ++cc) tma_load_3d(q_smem + cc * C::CHUNK, &tm_q, &bar.q_full, cc * 64, tl.h, qrow);
+        for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+          for (int cc = 0; cc < C::NC; ++cc)
+            tma_load_3d(q_smem + hf * C::TILE + cc * C::CHUNK, &tm_q, &bar.q_full, cc * 64, tl.h,
+                        qrow + hf * kTileM);
         ++q_loads;
         const int32_t nkv = (c.olen + kTileN - 1) / kTileN;
         for (int32_t j = 0; ok && j < nkv; ++j) {
@@ -134,7 +158,7 @@ __global__ void __launch_bounds__(256, 1)
       }
       if (*abort) {
         // Let every copy already issued land before the CTA's shared memory
-        // can be released (bounded; a copy that never lands is reported).
+        // can be released (bounded).
         for (uint32_t s = 0; s < C::NSLOT && s < ring_pos; ++s) {
           const uint32_t last = ring_pos - 1 - ((ring_pos - 1 - s) % C::NSLOT);
           int dummy = 0;
@@ -151,78 +175,92 @@ __global__ void __launch_bounds__(256, 1)
     constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
     constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, false, true);
     SegCursor c;
-    cursor_init<kTileM>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k);
+    cursor_init<kFwdUnit>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k);
     uint32_t tiles = 0, g = 0, ring0 = 0;
     const uint32_t q_base = smem_addr(q_smem);
     const uint32_t ring_base = smem_addr(ring);
     bool ok = true;
+    auto issue_s = [&](int hf, uint32_t kslot) {
+      const uint32_t kaddr = ring_base + kslot * C::TILE;
+      const uint32_t qaddr = q_base + hf * C::TILE;
+#pragma unroll
+      for (int kk = 0; kk < C::KSTEPS; ++kk) {
+        const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
+        mma_ss(tmem + hf * 128, sw128_desc(qaddr + off, 16, 1024), sw128_desc(kaddr + off, 16, 1024), kIdescS,
+               kk > 0);
+      }
+      mma_commit(&bar.s_full[hf]);
+    };
+    auto issue_pv = [&](int hf, uint32_t vslot, bool first) {
+      const uint32_t vaddr = ring_base + vslot * C::TILE;
+#pragma unroll
+      for (int kk = 0; kk < kTileN / 16; ++kk) {
+        mma_ts(tmem + C::O_COL + hf * 128, tmem + hf * 128 + kk * 8, sw128_desc(vaddr + kk * 2048, C::CHUNK, 1024),
+               kIdescO, (!first || kk > 0) ? 1u : 0u);
+      }
+      mma_commit(&bar.pv_done[hf]);
+    };
     for (int64_t t = blockIdx.x;
-         ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k); t += G) {
+         ok && cursor_seek<kFwdUnit>(c, t, p.num_heads, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k); t += G) {
       if (c.olen == 0) continue;
       if (!mbar_wait(&bar.q_full, tiles & 1, abort)) break;
       ++tiles;
-      tc_fence_after();
       const int32_t nkv = (c.olen + kTileN - 1) / kTileN;
-      for (int32_t j = 0; j <= nkv; ++j) {
-        if (j < nkv) {
-          // S_j = Q K_j^T into score buffer (g+j) % 3
-          const uint32_t gj = g + j;
-          const uint32_t sb = gj % C::NSBUF;
-          const uint32_t kpos = ring0 + 2 * j;
-          const uint32_t kslot = kpos % C::NSLOT;
-          if (!mbar_wait(&bar.kv_full[kslot], (kpos / C::NSLOT) & 1, abort)) { ok = false; break; }
-          if (gj >= C::NSBUF && !mbar_wait(&bar.s_free[sb], ((gj / C::NSBUF) - 1) & 1, abort)) { ok = false; break; }
+      // prologue: S_A and S_B of kv step 0
+      {
+        const uint32_t kslot = ring0 % C::NSLOT;
+        if (!mbar_wait(&bar.kv_full[kslot], (ring0 / C::NSLOT) & 1, abort)) break;
+        tc_fence_after();
+        if (lane == 0) {
+          issue_s(0, kslot);
+          issue_s(1, kslot);
+          mma_commit(&bar.kv_empty[kslot]);
+          if (nkv == 1) mma_commit(&bar.q_empty);
+        }
+        __syncwarp();
+      }
+      for (int32_t j = 0; j < nkv; ++j) {
+        const uint32_t gj = g + j;
+        const uint32_t vpos = ring0 + 2 * j + 1;
+        const uint32_t vslot = vpos % C::NSLOT;
+        const bool more = j + 1 < nkv;
+        const uint32_t kpos = vpos + 1;
+        const uint32_t kslot = kpos % C::NSLOT;
+        if (!mbar_wait(&bar.kv_full[vslot], (vpos / C::NSLOT) & 1, abort)) { ok = false; break; }
+        const int32_t kv_valid = c.olen - j * kTileN;
+        uint8_t* vtile = ring + vslot * C::TILE;
+        if (kv_valid < kTileN) {
+          // Rows past the segment end hold the next segment's values (or
+          // TMA zero fill).  P is 0 there, but 0 * NaN would still poison
+          // O, so clear those rows before the MMA reads them.
+#pragma unroll
+          for (int cc = 0; cc < C::NC; ++cc) {
+            uint4* base = reinterpret_cast<uint4*>(vtile + cc * C::CHUNK + kv_valid * 128);
+            for (int u = lane; u < (kTileN - kv_valid) * 8; u += 32) base[u] = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (more && !mbar_wait(&bar.kv_full[kslot], (kpos / C::NSLOT) & 1, abort)) { ok = false; break; }
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          if (!mbar_wait(&bar.p_full[hf], gj & 1, abort)) { ok = false; break; }
           tc_fence_after();
           if (lane == 0) {
-            const uint32_t kaddr = ring_base + kslot * C::TILE;
-#pragma unroll
-            for (int kk = 0; kk < C::KSTEPS; ++kk) {
-              const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
-              mma_ss(tmem + sb * 128, sw128_desc(q_base + off, 16, 1024), sw128_desc(kaddr + off, 16, 1024), kIdescS,
-                     kk > 0);
-            }
-            mma_commit(&bar.s_full[sb]);
+            issue_pv(hf, vslot, j == 0);
+            if (more) issue_s(hf, kslot);
+          }
+          __syncwarp();
+        }
+        if (!ok) break;
+        if (lane == 0) {
+          mma_commit(&bar.kv_empty[vslot]);
+          if (more) {
             mma_commit(&bar.kv_empty[kslot]);
-            if (j == nkv - 1) mma_commit(&bar.q_empty);
+            if (j + 1 == nkv - 1) mma_commit(&bar.q_empty);
           }
-          __syncwarp();
         }
-        if (j >= 1) {
-          // O += P_{j-1} V_{j-1}
-          const int32_t jj = j - 1;
-          const uint32_t gj = g + jj;
-          const uint32_t sb = gj % C::NSBUF;
-          const uint32_t vpos = ring0 + 2 * jj + 1;
-          const uint32_t vslot = vpos % C::NSLOT;
-          if (!mbar_wait(&bar.p_full[sb], (gj / C::NSBUF) & 1, abort)) { ok = false; break; }
-          if (!mbar_wait(&bar.kv_full[vslot], (vpos / C::NSLOT) & 1, abort)) { ok = false; break; }
-          const int32_t kv_valid = c.olen - jj * kTileN;
-          uint8_t* vtile = ring + vslot * C::TILE;
-          if (kv_valid < kTileN) {
-            // Rows past the segment end hold the next segment's values (or
-            // TMA zero fill).  P is 0 there, but 0 * NaN would still poison
-            // O, so clear those rows before the MMA reads them.
-#pragma unroll
-            for (int cc = 0; cc < C::NC; ++cc) {
-              uint4* base = reinterpret_cast<uint4*>(vtile + cc * C::CHUNK + kv_valid * 128);
-              for (int u = lane; u < (kTileN - kv_valid) * 8; u += 32) base[u] = make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async_smem();
-          }
-          __syncwarp();
-          tc_fence_after();
-          if (lane == 0) {
-            const uint32_t vaddr = smem_addr(vtile);
-#pragma unroll
-            for (int kk = 0; kk < kTileN / 16; ++kk) {
-              mma_ts(tmem + C::O_COL, tmem + sb * 128 + kk * 8, sw128_desc(vaddr + kk * 2048, C::CHUNK, 1024),
-                     kIdescO, (jj > 0 || kk > 0) ? 1u : 0u);
-            }
-            mma_commit(&bar.kv_empty[vslot]);
-            mma_commit(&bar.s_free[sb]);
-          }
-          __syncwarp();
-        }
+        __syncwarp();
       }
       g += nkv;
       ring0 += 2 * nkv;
@@ -234,25 +272,29 @@ __global__ void __launch_bounds__(256, 1)
       mbar_wait(&bar.mma_done, 0, &dummy);
     }
     __syncwarp();
-  } else if (warp >= 4) {
+  }
+  } else {
+    warpgroup_reg_alloc<kFwdRegsSoftmax>();
     // ------------------------------------------------------------ softmax
-    const int row = threadIdx.x - 128;                 // TMEM lane
-    const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
+    const int hf = (warp - 4) >> 2;                    // 0: half A (warps 4..7), 1: half B (warps 8..11)
+    const int quad = warp & 3;                         // TMEM lane quadrant this warp may access
+    const int row = quad * 32 + lane;                  // TMEM lane = row within the half
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const uint32_t s_col = hf * 128, o_col = C::O_COL + hf * 128;
     const float c2 = p.scale_log2;
     SegCursor c;
-    cursor_init<kTileM>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k);
+    cursor_init<kFwdUnit>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k);
     uint32_t g = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x;
-         ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k); t += G) {
-      const Tile tl = cursor_tile(c, t);
-      const int32_t r_in_seg = tl.m * kTileM + row;
-      const bool row_valid = r_in_seg < c.len;
-      const int64_t grow = (int64_t)c.r0 + r_in_seg;
-      __nv_bfloat16* orow = p.out + grow * p.o_rs + (int64_t)tl.h * p.o_hs;
-      float* lse_out = p.lse + (int64_t)tl.h * p.total_q + grow;
+         ok && cursor_seek<kFwdUnit>(c, t, p.num_heads, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k); t += G) {
       if (c.olen == 0) {
-        if (row_valid) {
+        const Tile tl = cursor_tile(c, t);
+        const int32_t r_in_seg = tl.m * kFwdUnit + hf * kTileM + row;
+        const int64_t grow = (int64_t)c.r0 + r_in_seg;
+        __nv_bfloat16* orow = p.out + grow * p.o_rs + (int64_t)tl.h * p.o_hs;
+        float* lse_out = p.lse + (int64_t)tl.h * p.total_q + grow;
+        if (r_in_seg < c.len) {
 #pragma unroll
           for (int d = 0; d < D; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0, 0, 0, 0);
           *lse_out = -INFINITY;
@@ -263,8 +305,7 @@ __global__ void __launch_bounds__(256, 1)
       float m_use = -INFINITY, l = 0.f;
       for (int32_t j = 0; j < nkv; ++j) {
         const uint32_t gj = g + j;
-        const uint32_t sb = gj % C::NSBUF;
-        if (!mbar_wait(&bar.s_full[sb], (gj / C::NSBUF) & 1, abort)) { ok = false; break; }
+        if (!mbar_wait(&bar.s_full[hf], gj & 1, abort)) { ok = false; break; }
         tc_fence_after();
         uint32_t s[128];
         {
@@ -272,7 +313,7 @@ __global__ void __launch_bounds__(256, 1)
           uint32_t(&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[32]);
           uint32_t(&s2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[64]);
           uint32_t(&s3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[96]);
-          const uint32_t ta = tmem + lane_off + sb * 128;
+          const uint32_t ta = tmem + lane_off + s_col;
           tmem_ld32(ta + 0, s0);
           tmem_ld32(ta + 32, s1);
           tmem_ld32(ta + 64, s2);
@@ -307,55 +348,61 @@ __global__ void __launch_bounds__(256, 1)
           m_use = m_new;
           rescale = true;
         }
-        // P = exp2(S*c - m) two lanes at a time; row sum of the fp32 P
+        // P = exp2(S*c - m) two lanes at a time; row sum of the fp32 P.
+        // P goes to TMEM in two 32-column halves as it is produced, which
+        // keeps the live register set small.  Half h writes P columns
+        // [32h, 32h+32), whose S values were consumed already.
         const float2 cc2 = make_float2(c2, c2), negm = make_float2(-m_use, -m_use);
         float2 rs2a = make_float2(0.f, 0.f), rs2b = make_float2(0.f, 0.f);
-        uint32_t pk[64];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          float2 t = ffma2(make_float2(x[2 * i], x[2 * i + 1]), cc2, negm);
-          t.x = ex2(t.x);
-          t.y = ex2(t.y);
-          pk[i] = pack_bf16x2(t.x, t.y);
-          if (i & 1) rs2b = fadd2(rs2b, t); else rs2a = fadd2(rs2a, t);
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int e = hh * 64 + 2 * i;
+            float2 t2 = ffma2(make_float2(x[e], x[e + 1]), cc2, negm);
+            t2.x = ex2(t2.x);
+            t2.y = ex2(t2.y);
+            pk[i] = pack_bf16x2(t2.x, t2.y);
+            if (i & 1) rs2b = fadd2(rs2b, t2); else rs2a = fadd2(rs2a, t2);
+          }
+          tmem_st32(tmem + lane_off + s_col + hh * 32, pk);
         }
         const float rs = (rs2a.x + rs2a.y) + (rs2b.x + rs2b.y);
         l = fmaf(l, alpha, rs);
-        {
-          const uint32_t ta = tmem + lane_off + sb * 128;
-          tmem_st32(ta + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-          tmem_st32(ta + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-        }
         if (__any_sync(0xffffffffu, rescale)) {
-          // O must hold P_{j-1} V_{j-1} before it is rescaled.
-          const uint32_t gp = gj - 1;
-          if (!mbar_wait(&bar.s_free[gp % C::NSBUF], (gp / C::NSBUF) & 1, abort)) { ok = false; }
-          tc_fence_after();
+          // S_j was issued after O += P_{j-1} V_{j-1} of this half, in MMA
+          // issue order, so O is complete here.
 #pragma unroll
           for (int d0 = 0; d0 < D; d0 += 32) {
             uint32_t o[32];
-            tmem_ld32(tmem + lane_off + C::O_COL + d0, o);
+            tmem_ld32(tmem + lane_off + o_col + d0, o);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(tmem + lane_off + C::O_COL + d0, o);
+            tmem_st32(tmem + lane_off + o_col + d0, o);
           }
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&bar.p_full[sb]);
-        if (!ok) break;
+        mbar_arrive(&bar.p_full[hf]);
       }
       if (!ok) break;
-      // epilogue: wait for the last O += P V, then O / l and LSE
+      // epilogue: wait for the last O += P V of this half, then O / l and LSE
+      const Tile tl = cursor_tile(c, t);
+      const int32_t r_in_seg = tl.m * kFwdUnit + hf * kTileM + row;
+      const bool row_valid = r_in_seg < c.len;
+      const int64_t grow = (int64_t)c.r0 + r_in_seg;
+      __nv_bfloat16* orow = p.out + grow * p.o_rs + (int64_t)tl.h * p.o_hs;
+      float* lse_out = p.lse + (int64_t)tl.h * p.total_q + grow;
       const uint32_t gl = g + nkv - 1;
-      if (!mbar_wait(&bar.s_free[gl % C::NSBUF], (gl / C::NSBUF) & 1, abort)) break;
+      if (!mbar_wait(&bar.pv_done[hf], gl & 1, abort)) break;
       tc_fence_after();
       const float inv_l = 1.f / l;
 #pragma unroll
       for (int d0 = 0; d0 < D; d0 += 32) {
         uint32_t o[32];
-        tmem_ld32(tmem + lane_off + C::O_COL + d0, o);
+        tmem_ld32(tmem + lane_off + o_col + d0, o);
         tmem_wait_ld();
         if (row_valid) {
           uint32_t w[16];
@@ -388,7 +435,7 @@ static cudaError_t launch_fwd_d(const FwdLaunch& L, cudaStream_t stream) {
   auto kern = varlen_fwd_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  kern<<<L.grid, 256, C::SMEM_BYTES, stream>>>(L.tm_q, L.tm_k, L.tm_v, L.p);
+  kern<<<L.grid, 384, C::SMEM_BYTES, stream>>>(L.tm_q, L.tm_k, L.tm_v, L.p);
   return cudaGetLastError();
 }
 

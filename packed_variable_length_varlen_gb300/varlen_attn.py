@@ -38,7 +38,10 @@ class VarlenStride(ctypes.Structure):
 
 class VarlenError(RuntimeError):
     def __init__(self, status: int, where: str):
-        super().__init__("%s failed: %d (%s)" % (where, status, varlen_attn_status_string(status)))
+        msg = "%s failed: %d (%s)" % (where, status, varlen_attn_status_string(status))
+        if status == VARLEN_ERR_CUDA:
+            msg += ": " + varlen_attn_last_cuda_error()
+        super().__init__(msg)
         self.status = status
 
 
@@ -65,6 +68,8 @@ def _load() -> ctypes.CDLL:
     lib.varlen_attn_get_device_status.argtypes = [vp]
     lib.varlen_attn_status_string.restype = ctypes.c_char_p
     lib.varlen_attn_status_string.argtypes = [ctypes.c_int]
+    lib.varlen_attn_last_cuda_error.restype = ctypes.c_char_p
+    lib.varlen_attn_last_cuda_error.argtypes = []
     lib.varlen_attn_tile_count.restype = i64
     lib.varlen_attn_tile_count.argtypes = [vp, i32, i32, i32, i32]
     lib.varlen_attn_debug_schedule.restype = ctypes.c_int
@@ -84,7 +89,7 @@ LIB_PATH = LIB._name
 EXPORTED = ("varlen_attn_fwd", "varlen_attn_bwd_workspace_size", "varlen_attn_bwd",
             "varlen_attn_get_device_status", "varlen_attn_status_string", "varlen_attn_tile_count",
             "varlen_attn_debug_schedule", "varlen_attn_selftest_wait_timeout", "varlen_attn_num_sms",
-            "varlen_attn_debug_set_phase_events", "varlen_attn_bwd_noalloc")
+            "varlen_attn_debug_set_phase_events", "varlen_attn_bwd_noalloc", "varlen_attn_last_cuda_error")
 
 # Size of the fixed device array varlen_attn_bwd_noalloc uses as scratch.
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -153,6 +158,10 @@ def varlen_attn_get_device_status(stream=None) -> int:
 
 def varlen_attn_status_string(status: int) -> str:
     return LIB.varlen_attn_status_string(status).decode()
+
+
+def varlen_attn_last_cuda_error() -> str:
+    return LIB.varlen_attn_last_cuda_error().decode()
 
 
 def varlen_attn_tile_count(cu_seqlens_host, batch, total, num_heads, tile) -> int:

@@ -60,7 +60,7 @@ def run_fwd(inp_dev: W.Inputs, out: torch.Tensor, lse: torch.Tensor, max_seqlen_
                             w.max_q() if max_seqlen_q is None else max_seqlen_q,
                             w.max_k() if max_seqlen_k is None else max_seqlen_k,
                             w.softmax_scale, out, lse)
-    assert st == 0, va.varlen_attn_status_string(st)
+    assert st == 0, (va.varlen_attn_status_string(st), va.varlen_attn_last_cuda_error())
     st = va.varlen_attn_get_device_status()
     assert st == 0, va.varlen_attn_status_string(st)
 

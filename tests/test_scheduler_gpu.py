@@ -57,8 +57,9 @@ def test_windowed_tile_count_pin():
 
 @pytest.mark.parametrize("grid", [1, 7, 152, 1000])
 def test_ragged_with_empty_segments(grid):
-    lens = [0, 1, 127, 128, 129, 0, 0, 300, 5, 0, 0]
+    lens = [0, 1, 127, 128, 129, 0, 0, 300, 5, 0, 0, 256, 257, 511]
     cu = [0] + list(np.cumsum(lens))
+    _run(cu, 3, 256, grid)
     _run(cu, 3, 128, grid)
     _run(cu, 3, 64, grid)
 
@@ -80,7 +81,7 @@ def test_random_ragged():
         lens = rng.integers(0, 700, size=B)
         lens[rng.random(B) < 0.2] = 0
         cu = [0] + list(np.cumsum(lens))
-        _run(cu, int(rng.integers(1, 5)), int(rng.choice([64, 128])), int(rng.integers(1, 300)))
+        _run(cu, int(rng.integers(1, 5)), int(rng.choice([64, 128, 256])), int(rng.integers(1, 300)))
 
 
 def test_malformed_cu_is_clamped():
