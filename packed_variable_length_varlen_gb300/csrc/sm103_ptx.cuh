@@ -198,6 +198,13 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo_byte
          ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// Descriptor of the same layout at a byte offset from `desc`'s start: the
+// start field holds (address >> 4) in 14 bits, and every shared-memory
+// address here is below 2^18, so the offset adds without carrying out.
+__device__ __forceinline__ uint64_t desc_at(uint64_t desc, uint32_t byte_off) {
+  return desc + (uint64_t)(byte_off >> 4);
+}
+
 // TMEM address: lane in bits [16,32), column in bits [0,16).
 __device__ __forceinline__ uint32_t tmem_at(uint32_t base, uint32_t lane, uint32_t col) {
   return base + (lane << 16) + col;

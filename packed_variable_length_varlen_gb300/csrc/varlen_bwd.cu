@@ -260,23 +260,31 @@ __global__ void __launch_bounds__(384, 1)
       q_base = smem_addr(qs);
       return true;
     };
+    // Base descriptors, built once; each k-step adds a constant offset.
+    const uint64_t dK_kmaj = sw128_desc(k_base, 16, 1024);             // K as K-major A
+    const uint64_t dV_kmaj = sw128_desc(v_base, 16, 1024);             // V as K-major A
+    const uint64_t dK_mn = sw128_desc(k_base, C::KV_CHUNK, 1024);      // K^T as MN-major A
+    const uint64_t dPT = sw128_desc(pt_base, 16, 1024);                // P^T, K-major A
+    const uint64_t dST_k = sw128_desc(dst_base, 16, 1024);             // dS^T, K-major A
+    const uint64_t dST_mn = sw128_desc(dst_base, C::PS_BYTES, 1024);   // dS^T, MN-major B
     auto issue_s = [&](uint32_t g, uint32_t q_base) {
       const uint32_t sc = C::S_COL + (g & 1) * 64;
+      const uint64_t dq_k = sw128_desc(q_base, 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t ko = (kk >> 2) * C::KV_CHUNK + (kk & 3) * 32;
         const uint32_t qo = (kk >> 2) * C::Q_CHUNK + (kk & 3) * 32;
-        mma_ss(tmem + sc, sw128_desc(k_base + ko, 16, 1024), sw128_desc(q_base + qo, 16, 1024), kIdS, kk > 0);
+        mma_ss(tmem + sc, desc_at(dK_kmaj, ko), desc_at(dq_k, qo), kIdS, kk > 0);
       }
       mma_commit(&bar.s_full[g & 1]);
     };
     auto issue_dp = [&](uint32_t do_base) {
+      const uint64_t ddo_k = sw128_desc(do_base, 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t ko = (kk >> 2) * C::KV_CHUNK + (kk & 3) * 32;
         const uint32_t qo = (kk >> 2) * C::Q_CHUNK + (kk & 3) * 32;
-        mma_ss(tmem + C::DP_COL, sw128_desc(v_base + ko, 16, 1024), sw128_desc(do_base + qo, 16, 1024), kIdS,
-               kk > 0);
+        mma_ss(tmem + C::DP_COL, desc_at(dV_kmaj, ko), desc_at(ddo_k, qo), kIdS, kk > 0);
       }
       mma_commit(&bar.dp_full);
     };
@@ -317,21 +325,22 @@ __global__ void __launch_bounds__(384, 1)
         if (!mbar_wait(&bar.ds_ready, gs & 1, abort)) { ok = false; break; }
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t do_base = q_cur + C::Q_BYTES;
+          const uint64_t ddo_mn = sw128_desc(q_cur + C::Q_BYTES, C::Q_CHUNK, 1024);  // dO as MN-major B
+          const uint64_t dq_mn = sw128_desc(q_cur, C::Q_CHUNK, 1024);                // Q as MN-major B
 #pragma unroll
           for (int kk = 0; kk < QT / 16; ++kk) {
-            mma_ss(tmem + C::DV_COL, sw128_desc(pt_base + kk * 32, 16, 1024),
-                   sw128_desc(do_base + kk * 2048, C::Q_CHUNK, 1024), kIdG, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_ss(tmem + C::DV_COL, desc_at(dPT, kk * 32), desc_at(ddo_mn, kk * 2048), kIdG,
+                   (j > 0 || kk > 0) ? 1u : 0u);
           }
 #pragma unroll
           for (int kk = 0; kk < QT / 16; ++kk) {
-            mma_ss(tmem + C::DK_COL, sw128_desc(dst_base + kk * 32, 16, 1024),
-                   sw128_desc(q_cur + kk * 2048, C::Q_CHUNK, 1024), kIdG, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_ss(tmem + C::DK_COL, desc_at(dST_k, kk * 32), desc_at(dq_mn, kk * 2048), kIdG,
+                   (j > 0 || kk > 0) ? 1u : 0u);
           }
 #pragma unroll
           for (int kk = 0; kk < kTileM / 16; ++kk) {
-            mma_ss(tmem + C::DQ_COL, sw128_desc(k_base + kk * 2048, C::KV_CHUNK, 1024),
-                   sw128_desc(dst_base + kk * 2048, C::PS_BYTES, 1024), kIdQ, kk > 0 ? 1u : 0u);
+            mma_ss(tmem + C::DQ_COL, desc_at(dK_mn, kk * 2048), desc_at(dST_mn, kk * 2048), kIdQ,
+                   kk > 0 ? 1u : 0u);
           }
           mma_commit(&bar.qd_empty[gs % C::NSTAGE]);
           mma_commit(&bar.step_done);

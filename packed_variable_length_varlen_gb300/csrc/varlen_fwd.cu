@@ -180,22 +180,23 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t q_base = smem_addr(q_smem);
     const uint32_t ring_base = smem_addr(ring);
     bool ok = true;
+    // Base descriptors, built once; each k-step adds a constant offset.
+    const uint64_t dQ0 = sw128_desc(q_base, 16, 1024);                 // Q_A (Q_B at +TILE), K-major
+    const uint64_t dRingK = sw128_desc(ring_base, 16, 1024);           // ring slot 0 as K-major B
+    const uint64_t dRingV = sw128_desc(ring_base, C::CHUNK, 1024);     // ring slot 0 as MN-major B
     auto issue_s = [&](int hf, uint32_t kslot) {
-      const uint32_t kaddr = ring_base + kslot * C::TILE;
-      const uint32_t qaddr = q_base + hf * C::TILE;
 #pragma unroll
       for (int kk = 0; kk < C::KSTEPS; ++kk) {
         const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
-        mma_ss(tmem + hf * 128, sw128_desc(qaddr + off, 16, 1024), sw128_desc(kaddr + off, 16, 1024), kIdescS,
+        mma_ss(tmem + hf * 128, desc_at(dQ0, hf * C::TILE + off), desc_at(dRingK, kslot * C::TILE + off), kIdescS,
                kk > 0);
       }
       mma_commit(&bar.s_full[hf]);
     };
     auto issue_pv = [&](int hf, uint32_t vslot, bool first) {
-      const uint32_t vaddr = ring_base + vslot * C::TILE;
 #pragma unroll
       for (int kk = 0; kk < kTileN / 16; ++kk) {
-        mma_ts(tmem + C::O_COL + hf * 128, tmem + hf * 128 + kk * 8, sw128_desc(vaddr + kk * 2048, C::CHUNK, 1024),
+        mma_ts(tmem + C::O_COL + hf * 128, tmem + hf * 128 + kk * 8, desc_at(dRingV, vslot * C::TILE + kk * 2048),
                kIdescO, (!first || kk > 0) ? 1u : 0u);
       }
       mma_commit(&bar.pv_done[hf]);
