@@ -111,7 +111,7 @@ struct BwdCfg {
   static constexpr int K_BYTES = KCH * KV_CHUNK;
   static constexpr int V_BYTES = NC * KV_CHUNK;
   static constexpr int Q_BYTES = NC * Q_CHUNK;   // one Q or dO tile
-  static constexpr int NSTAGE = 3;               // Q / dO ring depth
+  static constexpr int NSTAGE = 4;               // Q / dO ring depth
   static constexpr int PS_BYTES = 128 * 128;     // P^T or dS^T: 128 kv rows x 64 q (bf16)
   static constexpr int SMEM_BYTES = 1024 + 1024 + K_BYTES + V_BYTES + NSTAGE * 2 * Q_BYTES + 2 * PS_BYTES;
   // TMEM columns: two S^T buffers, dP^T, dQ^T, dV, dK
@@ -121,8 +121,8 @@ struct BwdCfg {
 
 struct BwdBarriers {
   uint64_t kv_full, kv_empty;
-  uint64_t qd_full[3], qd_empty[3];
-  uint64_t s_full[2], dp_full, ds_ready, step_done, mma_done;
+  uint64_t qd_full[4], qd_empty[4];
+  uint64_t s_full[2], dp_full, dp_free, ds_ready, step_done, mma_done;
   uint32_t tmem_base;
   int abort;
 };
@@ -167,6 +167,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&bar.s_full[0], 1);
     mbar_init(&bar.s_full[1], 1);
     mbar_init(&bar.dp_full, 1);
+    mbar_init(&bar.dp_free, 256);
     mbar_init(&bar.ds_ready, 256);
     mbar_init(&bar.step_done, 1);
     mbar_init(&bar.mma_done, 1);
@@ -289,6 +290,10 @@ __global__ void __launch_bounds__(384, 1)
       mma_commit(&bar.dp_full);
     };
 
+    // Per step g the pipe runs  dP^T_{g+1}, dV_g, dK_g, dQ^T_g, S^T_{g+2}:
+    // dP^T_{g+1} goes in as soon as the compute warps have read dP^T_g, so
+    // both S^T and dP^T of the next step are ready when they get to it.
+    uint32_t q_addr[3] = {0, 0, 0};  // Q stage address of steps g, g+1, g+2
     for (int64_t t = blockIdx.x;
          ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q); t += G) {
       if (c.olen == 0) continue;
@@ -304,26 +309,30 @@ __global__ void __launch_bounds__(384, 1)
       }
       __syncwarp();
       const int32_t nq = (c.olen + QT - 1) / QT;
-      // prologue: S^T_0 and dP^T_0
-      uint32_t q_cur = 0;
-      if (!ready_q(gs, 0, q_cur)) break;
+      // prologue: S^T_0, dP^T_0, S^T_1.  Both TMEM score buffers and the dP^T
+      // buffer were last read before the previous step's dp_free arrival.
+      if (gs > 0 && !mbar_wait(&bar.dp_free, (gs - 1) & 1, abort)) break;
+      if (!ready_q(gs, 0, q_addr[0])) break;
+      if (nq > 1 && !ready_q(gs + 1, 1, q_addr[1])) break;
       tc_fence_after();
       if (lane == 0) {
-        issue_s(gs, q_cur);
-        issue_dp(q_cur + C::Q_BYTES);
+        issue_s(gs, q_addr[0]);
+        issue_dp(q_addr[0] + C::Q_BYTES);
+        if (nq > 1) issue_s(gs + 1, q_addr[1]);
       }
       __syncwarp();
       for (int32_t j = 0; j < nq; ++j, ++gs) {
-        uint32_t q_next = 0;
         const bool more = j + 1 < nq;
         if (more) {
-          if (!ready_q(gs + 1, j + 1, q_next)) { ok = false; break; }
+          // dP^T_{g+1} as soon as dP^T_g has been read
+          if (!mbar_wait(&bar.dp_free, gs & 1, abort)) { ok = false; break; }
           tc_fence_after();
-          if (lane == 0) issue_s(gs + 1, q_next);
+          if (lane == 0) issue_dp(q_addr[1] + C::Q_BYTES);
           __syncwarp();
         }
         if (!mbar_wait(&bar.ds_ready, gs & 1, abort)) { ok = false; break; }
         tc_fence_after();
+        const uint32_t q_cur = q_addr[0];
         if (lane == 0) {
           const uint64_t ddo_mn = sw128_desc(q_cur + C::Q_BYTES, C::Q_CHUNK, 1024);  // dO as MN-major B
           const uint64_t dq_mn = sw128_desc(q_cur, C::Q_CHUNK, 1024);                // Q as MN-major B
@@ -345,10 +354,17 @@ __global__ void __launch_bounds__(384, 1)
           mma_commit(&bar.qd_empty[gs % C::NSTAGE]);
           mma_commit(&bar.step_done);
           if (!more) mma_commit(&bar.kv_empty);
-          if (more) issue_dp(q_next + C::Q_BYTES);
         }
         __syncwarp();
-        q_cur = q_next;
+        if (j + 2 < nq) {
+          // S^T_{g+2} into the score buffer S^T_g used (read before dp_free_g)
+          if (!ready_q(gs + 2, j + 2, q_addr[2])) { ok = false; break; }
+          tc_fence_after();
+          if (lane == 0) issue_s(gs + 2, q_addr[2]);
+          __syncwarp();
+        }
+        q_addr[0] = q_addr[1];
+        q_addr[1] = q_addr[2];
       }
     }
     if (lane == 0) {
@@ -423,14 +439,14 @@ __global__ void __launch_bounds__(384, 1)
           pv[i] = (i < nvalid) ? ex2(t2.x) : 0.f;
           pv[i + 1] = (i + 1 < nvalid) ? ex2(t2.y) : 0.f;
         }
-        // ---- dQ^T of the previous step (finished before dP^T_j in the pipe)
-        if (j > 0 && !drain_dq(gs - 1, j - 1, tl.h)) { ok = false; break; }
-        // ---- dS^T = P^T (dP^T - delta)
+        // ---- dS^T = P^T (dP^T - delta); dP^T_g is released right after it is read
         if (!mbar_wait(&bar.dp_full, gs & 1, abort)) { ok = false; break; }
         tc_fence_after();
         uint32_t dpv[32];
         tmem_ld32(tmem + lane_off + C::DP_COL + half * 32, dpv);
         tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&bar.dp_free);
         uint32_t pk[16], dk2[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
@@ -442,6 +458,9 @@ __global__ void __launch_bounds__(384, 1)
           pk[i / 2] = pack_bf16x2(pv[i], pv[i + 1]);
           dk2[i / 2] = pack_bf16x2(i < nvalid ? ds.x : 0.f, i + 1 < nvalid ? ds.y : 0.f);
         }
+        // ---- dQ^T of the previous step; its completion also means the
+        // previous step's MMAs are done reading the P^T / dS^T buffers
+        if (j > 0 && !drain_dq(gs - 1, j - 1, tl.h)) { ok = false; break; }
         // write this thread's 64 bytes of the P^T and dS^T rows (128-byte
         // swizzle: 16-byte unit u of row r sits at unit u ^ (r % 8))
 #pragma unroll
