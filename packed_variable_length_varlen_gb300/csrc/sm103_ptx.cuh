@@ -92,14 +92,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 
 // Re-balance registers between warpgroups (all four warps of a warpgroup
 // execute the same instruction).  The block launches with its compiled
-// per-thread count; the sum over warpgroups must stay within that.
-template <uint32_t N>
-__device__ __forceinline__ void warpgroup_reg_dealloc() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <uint32_t N>
-__device__ __forceinline__ void warpgroup_reg_alloc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+// per-thread count LAUNCH; a warpgroup moving to N registers must use the
+// decrease form when N < LAUNCH and the increase form when N > LAUNCH (the
+// increase form with a smaller count is not allowed), and the sum over
+// warpgroups must stay within the launch allocation.
+template <uint32_t N, uint32_t LAUNCH>
+__device__ __forceinline__ void warpgroup_set_regs() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg count must be a multiple of 8 in [24, 256]");
+  static_assert(LAUNCH % 8 == 0, "launch register count must be a multiple of 8");
+  if constexpr (N < LAUNCH) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+  } else if constexpr (N > LAUNCH) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+  }
 }
 
 // ---------------------------------------------------------------- TMA
@@ -119,6 +124,25 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
+
+// 3-D tiled reduce-add of one fp32 box from shared memory into global memory
+// (performed at L2; rows outside the tensor are dropped).  Tracked per
+// thread as a bulk async-group.
+__device__ __forceinline__ void tma_reduce_add_3d(const void* smem_src, const CUtensorMap* map, int32_t x, int32_t y,
+                                                  int32_t z) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_addr(smem_src)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until this thread's bulk groups have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until this thread's bulk groups have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy (tensor core / TMA) accesses.

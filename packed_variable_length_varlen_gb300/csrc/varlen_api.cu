@@ -111,6 +111,21 @@ int encode_nhd(CUtensorMap* map, const void* base, varlen_stride s, int64_t rows
   return r == CUDA_SUCCESS ? VARLEN_OK : VARLEN_ERR_STRIDE;
 }
 
+// The fp32 dQ accumulator [total_q, H, D] as a 3-D tensor map for bulk
+// reduce-add of 32 (d) x 1 (head) x 32 (rows) boxes.
+int encode_dq_acc(CUtensorMap* map, float* base, int64_t rows, int32_t H, int32_t D) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return VARLEN_ERR_CUDA;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)(rows > 0 ? rows : 1)};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 4u, (cuuint64_t)H * (cuuint64_t)D * 4u};
+  cuuint32_t box[3] = {32u, 1u, 32u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? VARLEN_OK : VARLEN_ERR_STRIDE;
+}
+
 int check_common(const int32_t* cu_q, const int32_t* cu_k, int32_t batch, int32_t total_q, int32_t total_k,
                  int32_t H, int32_t D, float scale) {
   if (cu_q == nullptr || cu_k == nullptr) return VARLEN_ERR_NULL;
@@ -227,6 +242,7 @@ extern "C" int varlen_attn_bwd(const void* q, varlen_stride sq, const void* k, v
   float* delta = reinterpret_cast<float*>(ws + round256((size_t)total_q * num_heads * head_dim * sizeof(float)));
   float* lse2 = reinterpret_cast<float*>(reinterpret_cast<char*>(delta) +
                                          round256((size_t)total_q * num_heads * sizeof(float)));
+  if ((st = encode_dq_acc(&L.tm_dq, dq_acc, total_q, num_heads, head_dim)) != VARLEN_OK) return st;
   L.prep = PrepParams{static_cast<const __nv_bfloat16*>(out), so.row, so.head,
                       static_cast<const __nv_bfloat16*>(dout), sdo.row, sdo.head,
                       lse, delta, lse2, dq_acc, cu_seqlens_q, batch, total_q, num_heads, head_dim};

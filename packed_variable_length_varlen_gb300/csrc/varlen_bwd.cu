@@ -23,9 +23,10 @@
 //     where P^T = exp2(S^T * scale*log2e - lse2) and dS^T = P^T (dP^T - delta)
 //     are computed by eight compute warps (thread = kv row, half of the q
 //     columns) and written to shared memory as bf16.  dQ^T is added into the
-//     fp32 accumulator with coalesced reductions (a warp covers 32
-//     consecutive d of one q row).  At the end of a kv tile, dK * scale and
-//     dV go to their strided outputs; a segment without queries writes zeros.
+//     fp32 accumulator by TMA bulk reduce-add: each compute warp stages its
+//     32 x 32 block and issues one reduction, which the L2 performs while
+//     the warp moves on.  At the end of a kv tile, dK * scale and dV go to
+//     their strided outputs; a segment without queries writes zeros.
 //
 //  3. varlen_bwd_post_kernel (HBM-bound): dq = bf16(scale * dq_acc), strided.
 //
@@ -111,9 +112,11 @@ struct BwdCfg {
   static constexpr int K_BYTES = KCH * KV_CHUNK;
   static constexpr int V_BYTES = NC * KV_CHUNK;
   static constexpr int Q_BYTES = NC * Q_CHUNK;   // one Q or dO tile
-  static constexpr int NSTAGE = 4;               // Q / dO ring depth
+  static constexpr int NSTAGE = 3;               // Q / dO ring depth
   static constexpr int PS_BYTES = 128 * 128;     // P^T or dS^T: 128 kv rows x 64 q (bf16)
-  static constexpr int SMEM_BYTES = 1024 + 1024 + K_BYTES + V_BYTES + NSTAGE * 2 * Q_BYTES + 2 * PS_BYTES;
+  static constexpr int STG_BYTES = 8 * 32 * 32 * 4;  // dQ staging: one 32 x 32 fp32 block per compute warp
+  static constexpr int SMEM_BYTES = 1024 + 1024 + K_BYTES + V_BYTES + NSTAGE * 2 * Q_BYTES + 2 * PS_BYTES + STG_BYTES;
+  static_assert(SMEM_BYTES <= 227 * 1024, "backward tile does not fit one CTA's shared memory");
   // TMEM columns: two S^T buffers, dP^T, dQ^T, dV, dK
   static constexpr int S_COL = 0, DP_COL = 128, DQ_COL = 192, DV_COL = 256, DK_COL = 384;
   static constexpr int TMEM_COLS = 512;
@@ -142,7 +145,7 @@ template <int D>
 __global__ void __launch_bounds__(384, 1)
     varlen_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                           const BwdParams p) {
+                           const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -152,6 +155,7 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* qd_smem = v_smem + C::V_BYTES;                 // [stage][Q, dO]
   uint8_t* pt_smem = qd_smem + C::NSTAGE * 2 * C::Q_BYTES;
   uint8_t* dst_smem = pt_smem + C::PS_BYTES;
+  uint8_t* stg_smem = dst_smem + C::PS_BYTES;
   volatile int* abort = &bar.abort;
 
   const int warp = threadIdx.x >> 5;
@@ -386,18 +390,37 @@ __global__ void __launch_bounds__(384, 1)
     uint32_t gs = 0;
     bool ok = true;
 
-    // dQ^T of global step g (tile-local step j): wait, then add into dq_acc.
+    // dQ^T of global step g (tile-local step j): wait for it, then add this
+    // warp's 32 (d) x 32 (q) block into dq_acc.  A block whose 32 q rows all
+    // lie in the segment is staged row-major [q][d] in the warp's own 4 KB
+    // of shared memory and added with one bulk reduce-add.  The segment's
+    // last, partial block is added row by row with reductions instead: its
+    // columns past the segment end are 0 * K, which is NaN when K is, and
+    // must not reach the next segment's rows.
+    float* stg = reinterpret_cast<float*>(stg_smem) + (warp - 4) * 32 * 32;
+    const bool drains = quad * 32 < D;             // warp-uniform: d block inside head_dim
     auto drain_dq = [&](uint32_t g, int32_t j, int32_t h) -> bool {
       if (!mbar_wait(&bar.step_done, g & 1, abort)) return false;
       tc_fence_after();
       uint32_t q32[32];
       tmem_ld32(tmem + lane_off + C::DQ_COL + half * 32, q32);
       tmem_wait_ld();
-      const int32_t qs0 = j * QT + half * 32;  // first q column of this thread, in the segment
-      if (r < D) {
-        float* dst = p.dq_acc + (((int64_t)c.o0 + qs0) * H + h) * D + r;
+      const int32_t qs0 = j * QT + half * 32;  // first q column of this warp, in the segment
+      if (drains && qs0 + 32 <= c.olen) {
+        if (lane == 0) bulk_wait_read_all();   // the previous reduce has read the staging
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) stg[i * 32 + lane] = __uint_as_float(q32[i]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_3d(stg, &tm_dq, quad * 32, h, c.o0 + qs0);
+          bulk_commit();
+        }
+      } else if (drains && qs0 < c.olen) {
+        float* dst = p.dq_acc + (((int64_t)c.o0 + qs0) * H + h) * D + quad * 32 + lane;
         const int64_t step = (int64_t)H * D;
-        const int32_t n = min(32, c.olen - qs0);
+        const int32_t n = c.olen - qs0;
 #pragma unroll
         for (int i = 0; i < 32; ++i)
           if (i < n) atomicAdd(dst + i * step, __uint_as_float(q32[i]));
@@ -511,6 +534,8 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_before();
       }
     }
+    if (lane == 0) bulk_wait_all();  // this warp's dQ reductions have completed
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -537,7 +562,7 @@ static cudaError_t launch_bwd_d(const BwdLaunch& L, cudaStream_t stream) {
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   mark(1);
-  kern<<<L.grid, 384, C::SMEM_BYTES, stream>>>(L.tm_q, L.tm_k, L.tm_v, L.tm_do, L.p);
+  kern<<<L.grid, 384, C::SMEM_BYTES, stream>>>(L.tm_q, L.tm_k, L.tm_v, L.tm_do, L.tm_dq, L.p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   mark(2);

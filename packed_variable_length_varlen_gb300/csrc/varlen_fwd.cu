@@ -67,7 +67,10 @@ static_assert(sizeof(FwdBarriers) <= 1024, "barrier block too large");
 // Warpgroup 0 (producer, MMA, two idle warps) drops to 96 and the two
 // softmax warpgroups rise to 176: 96*128 + 2*176*128 = 57,344 <= 64,512, and
 // each SM sub-partition holds one warp of each group: (96+176+176)*32 <= 16K.
-constexpr uint32_t kFwdRegsCtl = 96, kFwdRegsSoftmax = 176;
+constexpr uint32_t kFwdRegsLaunch = 168, kFwdRegsCtl = 96, kFwdRegsSoftmax = 176;
+static_assert(kFwdRegsCtl + 2 * kFwdRegsSoftmax <= 3 * kFwdRegsLaunch,
+              "warpgroup register split exceeds the launch allocation");
+static_assert(kFwdRegsLaunch * 384 <= 65536, "launch register count too large for 384 threads");
 
 template <int D>
 __global__ void __launch_bounds__(384, 1)
@@ -109,7 +112,7 @@ __global__ void __launch_bounds__(384, 1)
   const int64_t G = gridDim.x;
 
   if (warp < 4) {
-    warpgroup_reg_dealloc<kFwdRegsCtl>();
+    warpgroup_set_regs<kFwdRegsCtl, kFwdRegsLaunch>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -275,7 +278,7 @@ __global__ void __launch_bounds__(384, 1)
     __syncwarp();
   }
   } else {
-    warpgroup_reg_alloc<kFwdRegsSoftmax>();
+    warpgroup_set_regs<kFwdRegsSoftmax, kFwdRegsLaunch>();
     // ------------------------------------------------------------ softmax
     const int hf = (warp - 4) >> 2;                    // 0: half A (warps 4..7), 1: half B (warps 8..11)
     const int quad = warp & 3;                         // TMEM lane quadrant this warp may access
@@ -434,7 +437,13 @@ template <int D>
 static cudaError_t launch_fwd_d(const FwdLaunch& L, cudaStream_t stream) {
   using C = FwdCfg<D>;
   auto kern = varlen_fwd_kernel<D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  // The warpgroup register split assumes the compiled per-thread count;
+  // refuse to launch a build that came out differently.
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != (int)kFwdRegsLaunch) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   kern<<<L.grid, 384, C::SMEM_BYTES, stream>>>(L.tm_q, L.tm_k, L.tm_v, L.p);
   return cudaGetLastError();

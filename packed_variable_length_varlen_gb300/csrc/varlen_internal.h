@@ -80,6 +80,7 @@ struct PostParams {
 
 struct BwdLaunch {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  CUtensorMap tm_dq;  // fp32 dQ accumulator {D, H, total_q}, 32 x 1 x 32 boxes, for bulk reduce-add
   PrepParams prep;
   BwdParams p;
   PostParams post;
