@@ -92,8 +92,10 @@ int varlen_attn_fwd(const void* q, varlen_stride sq, const void* k, varlen_strid
 /*
  * Bytes of device workspace varlen_attn_bwd needs (256-byte aligned base).
  * It holds the fp32 dQ accumulator ([total_q, H, D] floats) and the per-row
- * delta and log2-domain LSE ([H, total_q] floats each), each region rounded
- * up to 256 bytes.  Returns 0 for negative arguments.
+ * delta and log2-domain LSE ([H, P] floats each, P = 4 * ceil(total_q / 4)
+ * + 4 * batch + 128: each segment's rows start at a 16-byte aligned index,
+ * with room for whole 128-row blocks past its end), each region rounded up
+ * to 256 bytes.  Returns 0 for negative arguments.
  */
 size_t varlen_attn_bwd_workspace_size(int32_t batch, int32_t total_q, int32_t num_heads, int32_t head_dim);
 
@@ -128,8 +130,9 @@ int varlen_attn_bwd(const void* q, varlen_stride sq, const void* k, varlen_strid
  * VARLEN_NOALLOC_SCRATCH_BYTES; at H=16, D=96 that is about 10,700 q rows).
  * The first call on a device looks up the array's device address (with that
  * device current) and should come before any stream capture.  Every call
- * shares the one array: it is fully rewritten by each call before it is
- * read, but calls that overlap on the GPU (unordered streams) race on it.
+ * shares the one array: every entry a result depends on is rewritten by
+ * each call before it is read (entries between segments are read but masked
+ * out), but calls that overlap on the GPU (unordered streams) race on it.
  */
 #define VARLEN_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 

@@ -112,13 +112,13 @@ int encode_nhd(CUtensorMap* map, const void* base, varlen_stride s, int64_t rows
 }
 
 // The fp32 dQ accumulator [total_q, H, D] as a 3-D tensor map for bulk
-// reduce-add of 32 (d) x 1 (head) x 32 (rows) boxes.
+// reduce-add of 32 (d) x 1 (head) x 64 (rows) boxes.
 int encode_dq_acc(CUtensorMap* map, float* base, int64_t rows, int32_t H, int32_t D) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return VARLEN_ERR_CUDA;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)(rows > 0 ? rows : 1)};
   cuuint64_t strides[2] = {(cuuint64_t)D * 4u, (cuuint64_t)H * (cuuint64_t)D * 4u};
-  cuuint32_t box[3] = {32u, 1u, 32u};
+  cuuint32_t box[3] = {32u, 1u, 64u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -201,7 +201,8 @@ extern "C" size_t varlen_attn_bwd_workspace_size(int32_t batch, int32_t total_q,
                                                  int32_t head_dim) {
   if (batch < 0 || total_q < 0 || num_heads < 0 || head_dim < 0) return 0;
   const size_t rows = (size_t)total_q;
-  return round256(rows * num_heads * head_dim * sizeof(float)) + 2 * round256(rows * num_heads * sizeof(float));
+  const size_t prow = (size_t)varlen::bwd_pad_rows(batch, total_q);
+  return round256(rows * num_heads * head_dim * sizeof(float)) + 2 * round256(prow * num_heads * sizeof(float));
 }
 
 extern "C" int varlen_attn_bwd(const void* q, varlen_stride sq, const void* k, varlen_stride sk, const void* v,
@@ -239,13 +240,14 @@ extern "C" int varlen_attn_bwd(const void* q, varlen_stride sq, const void* k, v
   if ((st = encode_nhd(&L.tm_v, v, sv, total_k, num_heads, head_dim, kTileM)) != VARLEN_OK) return st;
   char* ws = static_cast<char*>(workspace);
   float* dq_acc = reinterpret_cast<float*>(ws);
+  const int64_t pad_rows = bwd_pad_rows(batch, total_q);
   float* delta = reinterpret_cast<float*>(ws + round256((size_t)total_q * num_heads * head_dim * sizeof(float)));
   float* lse2 = reinterpret_cast<float*>(reinterpret_cast<char*>(delta) +
-                                         round256((size_t)total_q * num_heads * sizeof(float)));
+                                         round256((size_t)pad_rows * num_heads * sizeof(float)));
   if ((st = encode_dq_acc(&L.tm_dq, dq_acc, total_q, num_heads, head_dim)) != VARLEN_OK) return st;
   L.prep = PrepParams{static_cast<const __nv_bfloat16*>(out), so.row, so.head,
                       static_cast<const __nv_bfloat16*>(dout), sdo.row, sdo.head,
-                      lse, delta, lse2, dq_acc, cu_seqlens_q, batch, total_q, num_heads, head_dim};
+                      lse, delta, lse2, dq_acc, cu_seqlens_q, batch, total_q, num_heads, head_dim, pad_rows};
   L.p.dk = static_cast<__nv_bfloat16*>(dk);
   L.p.dk_rs = sdk.row;
   L.p.dk_hs = sdk.head;
@@ -261,6 +263,7 @@ extern "C" int varlen_attn_bwd(const void* q, varlen_stride sq, const void* k, v
   L.p.total_q = total_q;
   L.p.total_k = total_k;
   L.p.num_heads = num_heads;
+  L.p.pad_rows = pad_rows;
   L.p.scale_log2 = scale * kLog2e;
   L.p.scale = scale;
   L.p.err = dev.err;

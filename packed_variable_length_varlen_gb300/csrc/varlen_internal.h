@@ -18,7 +18,7 @@ enum : unsigned int {
 
 constexpr int kTileM = 128;  // q rows per forward tile / kv rows per backward tile
 constexpr int kTileN = 128;  // kv rows per forward inner step
-constexpr int kBwdTileQ = 64; // q rows per backward inner step
+constexpr int kBwdTileQ = 128; // q rows per backward inner step
 
 struct FwdParams {
   __nv_bfloat16* out;
@@ -46,11 +46,12 @@ struct PrepParams {
   const __nv_bfloat16* dout;
   int64_t do_rs, do_hs;
   const float* lse;
-  float* delta;     // [H, total_q]
-  float* lse2;      // [H, total_q]
+  float* delta;     // [H, pad_rows], segment-padded (see bwd_pad_rows)
+  float* lse2;      // [H, pad_rows], segment-padded
   float* dq_acc;    // [total_q, H, D]
   const int32_t* cu_q;
   int32_t batch, total_q, num_heads, head_dim;
+  int64_t pad_rows;
 };
 
 struct BwdParams {
@@ -58,12 +59,13 @@ struct BwdParams {
   int64_t dk_rs, dk_hs;
   __nv_bfloat16* dv;
   int64_t dv_rs, dv_hs;
-  const float* delta;
-  const float* lse2;
+  const float* delta;  // [H, pad_rows]
+  const float* lse2;   // [H, pad_rows]
   float* dq_acc;
   const int32_t* cu_q;
   const int32_t* cu_k;
   int32_t batch, total_q, total_k, num_heads;
+  int64_t pad_rows;
   float scale_log2;  // softmax scale * log2(e)
   float scale;       // softmax scale (applied to dK)
   unsigned int* err; // device error word
@@ -80,7 +82,7 @@ struct PostParams {
 
 struct BwdLaunch {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;
-  CUtensorMap tm_dq;  // fp32 dQ accumulator {D, H, total_q}, 32 x 1 x 32 boxes, for bulk reduce-add
+  CUtensorMap tm_dq;  // fp32 dQ accumulator {D, H, total_q}, 32 x 1 x 64 boxes, for bulk reduce-add
   PrepParams prep;
   BwdParams p;
   PostParams post;
@@ -90,6 +92,15 @@ struct BwdLaunch {
 };
 
 cudaError_t launch_bwd(const BwdLaunch& L, cudaStream_t stream);
+
+// Length of one head's row of the segment-padded delta / lse2 arrays.
+// Segment b's entries start at 4 * ceil(o0_b / 4) + 4 b (o0_b its first q
+// row), 16-byte aligned; a backward step reads whole 128-row blocks of a
+// segment, so up to 127 entries past its end, which this length covers for
+// any cu_seqlens.
+inline int64_t bwd_pad_rows(int32_t batch, int32_t total_q) {
+  return 4 * (((int64_t)total_q + 3) / 4) + 4 * (int64_t)batch + 128;
+}
 
 cudaError_t launch_debug_schedule(const int32_t* cu, int32_t batch, int32_t total, int32_t num_heads, int32_t tile,
                                   int32_t grid, int32_t* out, int64_t max_records, cudaStream_t stream);

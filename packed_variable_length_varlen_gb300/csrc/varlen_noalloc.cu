@@ -15,10 +15,12 @@
 // device, on the first call made with that device current
 // (cudaGetSymbolAddress); that first call should come before any stream
 // capture.  All calls share the one array and it keeps the last call's
-// contents -- the backward's preprocess kernel rewrites every part of it that
-// is read later (it zeroes the dQ accumulator), so stale contents never
-// matter -- but calls whose work overlaps on the GPU (different streams with
-// no ordering between them) race on it.
+// contents -- the backward's preprocess kernel rewrites every part of it
+// whose value reaches a result (it zeroes the dQ accumulator and writes each
+// segment's delta / LSE entries; padding entries between segments are read
+// but masked out), so stale contents never matter -- but calls whose work
+// overlaps on the GPU (different streams with no ordering between them) race
+// on it.
 #include <mutex>
 
 #include "varlen_attn.h"
