@@ -64,10 +64,11 @@ struct FwdBarriers {
 static_assert(sizeof(FwdBarriers) <= 1024, "barrier block too large");
 
 // Registers: the block launches 384 threads at 168 registers (64,512).
-// Warpgroup 0 (producer, MMA, two idle warps) drops to 96 and the two
-// softmax warpgroups rise to 176: 96*128 + 2*176*128 = 57,344 <= 64,512, and
-// each SM sub-partition holds one warp of each group: (96+176+176)*32 <= 16K.
-constexpr uint32_t kFwdRegsLaunch = 168, kFwdRegsCtl = 96, kFwdRegsSoftmax = 176;
+// Warpgroup 0 (producer, MMA, two idle warps) drops to 112 and the two
+// softmax warpgroups rise to 176: 112*128 + 2*176*128 = 59,392 <= 64,512,
+// and each SM sub-partition holds one warp of each group:
+// (112+176+176)*32 <= 16K.
+constexpr uint32_t kFwdRegsLaunch = 168, kFwdRegsCtl = 112, kFwdRegsSoftmax = 176;
 static_assert(kFwdRegsCtl + 2 * kFwdRegsSoftmax <= 3 * kFwdRegsLaunch,
               "warpgroup register split exceeds the launch allocation");
 static_assert(kFwdRegsLaunch * 384 <= 65536, "launch register count too large for 384 threads");
@@ -173,35 +174,37 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
+    // One thread issues every MMA straight through (the warp's other lanes
+    // wait at the end), with descriptors kept as 32-bit low words: a warp
+    // that rejoins between MMA groups, or spends many integer instructions
+    // per MMA, leaves the tensor pipe idle.
     constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
     constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, false, true);
     SegCursor c;
     cursor_init<kFwdUnit>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k);
     uint32_t tiles = 0, g = 0, ring0 = 0;
-    const uint32_t q_base = smem_addr(q_smem);
-    const uint32_t ring_base = smem_addr(ring);
     bool ok = true;
-    // Base descriptors, built once; each k-step adds a constant offset.
-    const uint64_t dQ0 = sw128_desc(q_base, 16, 1024);                 // Q_A (Q_B at +TILE), K-major
-    const uint64_t dRingK = sw128_desc(ring_base, 16, 1024);           // ring slot 0 as K-major B
-    const uint64_t dRingV = sw128_desc(ring_base, C::CHUNK, 1024);     // ring slot 0 as MN-major B
+    const uint32_t qlo = sw128_desc_lo(smem_addr(q_smem), 16);        // Q_A (Q_B at +TILE), K-major A
+    const uint32_t rK = sw128_desc_lo(smem_addr(ring), 16);           // ring slot 0 as K-major B
+    const uint32_t rV = sw128_desc_lo(smem_addr(ring), C::CHUNK);     // ring slot 0 as MN-major B
     auto issue_s = [&](int hf, uint32_t kslot) {
 #pragma unroll
       for (int kk = 0; kk < C::KSTEPS; ++kk) {
-        const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
-        mma_ss(tmem + hf * 128, desc_at(dQ0, hf * C::TILE + off), desc_at(dRingK, kslot * C::TILE + off), kIdescS,
-               kk > 0);
+        const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
+        mma_ss_lo(tmem + hf * 128, qlo + ((hf * C::TILE) >> 4) + off, rK + ((kslot * C::TILE) >> 4) + off, kIdescS,
+                  kk > 0 ? 1u : 0u);
       }
       mma_commit(&bar.s_full[hf]);
     };
-    auto issue_pv = [&](int hf, uint32_t vslot, bool first) {
+    // O += P V over nk 16-row k-steps of kv (k-steps past the segment end are skipped)
+    auto issue_pv = [&](int hf, uint32_t vslot, bool first, int nk) {
 #pragma unroll
-      for (int kk = 0; kk < kTileN / 16; ++kk) {
-        mma_ts(tmem + C::O_COL + hf * 128, tmem + hf * 128 + kk * 8, desc_at(dRingV, vslot * C::TILE + kk * 2048),
-               kIdescO, (!first || kk > 0) ? 1u : 0u);
-      }
+      for (int kk = 0; kk < kTileN / 16; ++kk)
+        if (kk < nk)
+          mma_ts_lo(tmem + C::O_COL + hf * 128, tmem + hf * 128 + kk * 8, rV + ((vslot * C::TILE + kk * 2048) >> 4),
+                    kIdescO, (!first || kk > 0) ? 1u : 0u);
       mma_commit(&bar.pv_done[hf]);
     };
     for (int64_t t = blockIdx.x;
@@ -215,13 +218,10 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t kslot = ring0 % C::NSLOT;
         if (!mbar_wait(&bar.kv_full[kslot], (ring0 / C::NSLOT) & 1, abort)) break;
         tc_fence_after();
-        if (lane == 0) {
-          issue_s(0, kslot);
-          issue_s(1, kslot);
-          mma_commit(&bar.kv_empty[kslot]);
-          if (nkv == 1) mma_commit(&bar.q_empty);
-        }
-        __syncwarp();
+        issue_s(0, kslot);
+        issue_s(1, kslot);
+        mma_commit(&bar.kv_empty[kslot]);
+        if (nkv == 1) mma_commit(&bar.q_empty);
       }
       for (int32_t j = 0; j < nkv; ++j) {
         const uint32_t gj = g + j;
@@ -231,51 +231,43 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t kpos = vpos + 1;
         const uint32_t kslot = kpos % C::NSLOT;
         if (!mbar_wait(&bar.kv_full[vslot], (vpos / C::NSLOT) & 1, abort)) { ok = false; break; }
-        const int32_t kv_valid = c.olen - j * kTileN;
-        uint8_t* vtile = ring + vslot * C::TILE;
+        const int32_t kv_valid = min(kTileN, c.olen - j * kTileN);
+        const int nk = (kv_valid + 15) >> 4;
         if (kv_valid < kTileN) {
           // Rows past the segment end hold the next segment's values (or
           // TMA zero fill).  P is 0 there, but 0 * NaN would still poison
-          // O, so clear those rows before the MMA reads them.
+          // O: k-steps wholly past the end are skipped, and the rows of the
+          // last partial one are cleared before the MMA reads them.
+          uint8_t* vtile = ring + vslot * C::TILE;
 #pragma unroll
           for (int cc = 0; cc < C::NC; ++cc) {
             uint4* base = reinterpret_cast<uint4*>(vtile + cc * C::CHUNK + kv_valid * 128);
-            for (int u = lane; u < (kTileN - kv_valid) * 8; u += 32) base[u] = make_uint4(0, 0, 0, 0);
+            for (int u = 0; u < (min(kTileN, nk * 16) - kv_valid) * 8; ++u) base[u] = make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async_smem();
         }
-        __syncwarp();
         if (more && !mbar_wait(&bar.kv_full[kslot], (kpos / C::NSLOT) & 1, abort)) { ok = false; break; }
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           if (!mbar_wait(&bar.p_full[hf], gj & 1, abort)) { ok = false; break; }
           tc_fence_after();
-          if (lane == 0) {
-            issue_pv(hf, vslot, j == 0);
-            if (more) issue_s(hf, kslot);
-          }
-          __syncwarp();
+          issue_pv(hf, vslot, j == 0, nk);
+          if (more) issue_s(hf, kslot);
         }
         if (!ok) break;
-        if (lane == 0) {
-          mma_commit(&bar.kv_empty[vslot]);
-          if (more) {
-            mma_commit(&bar.kv_empty[kslot]);
-            if (j + 1 == nkv - 1) mma_commit(&bar.q_empty);
-          }
+        mma_commit(&bar.kv_empty[vslot]);
+        if (more) {
+          mma_commit(&bar.kv_empty[kslot]);
+          if (j + 1 == nkv - 1) mma_commit(&bar.q_empty);
         }
-        __syncwarp();
       }
       g += nkv;
       ring0 += 2 * nkv;
     }
     // Drain: every MMA this thread issued completes before TMEM is freed.
-    if (lane == 0) {
-      mma_commit(&bar.mma_done);
-      int dummy = 0;
-      mbar_wait(&bar.mma_done, 0, &dummy);
-    }
-    __syncwarp();
+    mma_commit(&bar.mma_done);
+    int dummy = 0;
+    mbar_wait(&bar.mma_done, 0, &dummy);
   }
   } else {
     warpgroup_set_regs<kFwdRegsSoftmax, kFwdRegsLaunch>();
