@@ -38,6 +38,7 @@ import torch
 from packed_variable_length_varlen_gb300 import workloads as W
 
 METRIC = "varlen attention TFLOP/s (fwd, bwd) bf16 H=56 D=128; % of GB300 bf16 TC peak"
+BWD_MAIN_DRAM_BYTES_PER_HEAD = {("windowed", 128): (872.579840e6 + 671.620352e6) / 8}
 
 
 def _peaks():
@@ -164,8 +165,10 @@ def _oracle_rate(w: W.Workload, target_s: float, seed: int = 0):
         pb.bwd_q(rows, heads)
         return time.perf_counter() - t0, flops(rows), n
 
-    t, f, n = run(32)
-    n = int(max(32, min(200000, 32 * target_s / max(t, 1e-3))))
+    # calibrate on a probe large enough that fixed per-call costs do not dominate
+    probe = 256
+    t, f, n = run(probe)
+    n = int(max(probe, min(200000, probe * target_s / max(t, 1e-3))))
     return run, n, oracle.num_threads()
 
 
@@ -335,9 +338,16 @@ def ours(args, w, ws, rank, local):
     # (power-capped) figure is reported beside it.
     peak = float(peaks.get("bf16_tflops"))
     sust = float(peaks.get("bf16_tflops_sustained", peak))
+    # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the backward main
+    # kernel, from one ncu capture of the windowed workload at H=8 (kernel as of commit 480887b).
+    # Every head reads its own q, k, v, dout and writes its own dk, dv and dq rows, so the
+    # traffic scales with the number of heads.  Reported only for that workload and head size.
+    traffic = None
+    if dom_name == "varlen_bwd_main_kernel" and (w.name, D) in BWD_MAIN_DRAM_BYTES_PER_HEAD:
+        traffic = BWD_MAIN_DRAM_BYTES_PER_HEAD[(w.name, D)] * H
     roof = {"kernel": dom_name, "bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
             "frac": ach / peak, "peak_source": "%s bf16_tflops (burst)" % src,
-            "frac_of_sustained": ach / sust, "traffic": None}
+            "frac_of_sustained": ach / sust, "traffic": traffic}
 
     cpu_base = None
     if not args.no_cpu_baseline and ws >= 1:
