@@ -11,8 +11,8 @@ each) are larger than L2, so no flush is needed between iterations.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Under torchrun every rank runs the same workload on its own GPU (independent
-batches, no collective on the data path): weak scaling.  Rank 0 prints one
+Under torchrun every rank runs a batch of the same shape (its own seed) on its
+own GPU, with no collective on the data path: weak scaling.  Rank 0 prints one
 JSON line.  ``--impl reference`` times the fp64 CPU oracle (the only other
 implementation of this operation here) on a bounded sample of the same
 workload.
@@ -35,6 +35,7 @@ if ROOT not in sys.path:
 import numpy as np
 import torch
 
+from packed_variable_length_varlen_gb300 import sharding
 from packed_variable_length_varlen_gb300 import workloads as W
 
 METRIC = "varlen attention TFLOP/s (fwd, bwd) bf16 H=56 D=128; % of GB300 bf16 TC peak"
@@ -128,12 +129,7 @@ def _barrier(ws):
 
 
 def _max_over_ranks(x: float, ws: int) -> float:
-    if ws == 1:
-        return x
-    import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+    return x if ws == 1 else sharding.max_over_ranks(x)
 
 
 # ------------------------------------------------------------------ CPU side
@@ -202,7 +198,7 @@ def reference_arm(args, w, ws, rank):
 def ours(args, w, ws, rank, local):
     from packed_variable_length_varlen_gb300 import varlen_attn as va
     dev = torch.device("cuda", local)
-    cpu = W.make_inputs(w, seed=0)
+    cpu = W.make_inputs(w, seed=rank)  # each rank's own batch of the same shape
     d = cpu.to(dev)
     H, D = w.num_heads, w.head_dim
     out = torch.empty_like(d.q)

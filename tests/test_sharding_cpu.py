@@ -1,0 +1,151 @@
+"""Multi-rank partitioning of the packed-attention work, on CPU.
+
+Head and segment ranges partition the work; two gloo ranks that each compute
+their shard (heads, or a contiguous run of segments) with the oracle
+reproduce the unsharded result exactly, because every (segment, head) pair
+is independent -- the multi-GPU path needs no exchange of data, only the
+max of the ranks' times, which is checked here too."""
+import os
+import socket
+import tempfile
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from packed_variable_length_varlen_gb300 import sharding as S
+from packed_variable_length_varlen_gb300 import workloads as W
+
+
+def test_head_range_partitions():
+    for H in (1, 2, 7, 16, 56):
+        for world in (1, 2, 3, 4, 8):
+            ranges = [S.head_range(H, world, r) for r in range(world)]
+            assert ranges[0][0] == 0 and ranges[-1][1] == H
+            assert all(a[1] == b[0] for a, b in zip(ranges, ranges[1:]))
+            sizes = [h1 - h0 for h0, h1 in ranges]
+            assert max(sizes) - min(sizes) <= 1
+    with pytest.raises(ValueError):
+        S.head_range(4, 2, 2)
+
+
+def test_segment_range_partitions():
+    rng = np.random.default_rng(11)
+    for trial in range(40):
+        B = int(rng.integers(1, 25))
+        lq = rng.integers(0, 900, size=B)
+        lk = rng.integers(0, 900, size=B)
+        cu_q = [0] + list(np.cumsum(lq))
+        cu_k = [0] + list(np.cumsum(lk))
+        cost = [S.segment_cost(a, b) for a, b in zip(lq, lk)]
+        total = sum(cost)
+        for world in (1, 2, 3, 5):
+            shards = [S.segment_range(cu_q, cu_k, world, r) for r in range(world)]
+            assert shards[0].b0 == 0 and shards[-1].b1 == B
+            for a, b in zip(shards, shards[1:]):
+                assert a.b1 == b.b0 and a.q1 == b.q0 and a.k1 == b.k0
+            for sh in shards:
+                assert sh.cu_q == [x - cu_q[sh.b0] for x in cu_q[sh.b0:sh.b1 + 1]]
+                assert sh.cu_k == [x - cu_k[sh.b0] for x in cu_k[sh.b0:sh.b1 + 1]]
+                assert (sh.q0, sh.q1, sh.k0, sh.k1) == (cu_q[sh.b0], cu_q[sh.b1], cu_k[sh.b0], cu_k[sh.b1])
+                share = sum(cost[sh.b0:sh.b1])
+                assert share <= total / world + max(cost) + 1e-9
+    with pytest.raises(ValueError):
+        S.segment_range([0, 5, 3], [0, 1, 2], 2, 0)
+
+
+def test_max_over_ranks_without_group():
+    assert S.max_over_ranks(3.5) == 3.5
+
+
+# ---------------------------------------------------------------- two ranks
+
+_CASE = ([130, 0, 77, 256, 5, 64], [129, 9, 0, 300, 40, 64], 4, 64)
+
+
+def _shard_result(w, cpu, mode, world, rank):
+    """The oracle forward and backward of this rank's shard, keyed by global
+    (row, head) pairs."""
+    if mode == "heads":
+        h0, h1 = S.head_range(w.num_heads, world, rank)
+        view = lambda t: t[:, h0:h1]
+        pb = oracle.Problem(view(cpu.q), view(cpu.k), view(cpu.v), w.cu_q, w.cu_k, w.softmax_scale,
+                            dout=view(cpu.dout))
+        rows, heads = oracle.all_pairs(w.total_q, h1 - h0)
+        krows, kheads = oracle.all_pairs(w.total_k, h1 - h0)
+        grows, gheads, gkrows, gkheads = rows, heads + h0, krows, kheads + h0
+    else:
+        sh = S.segment_range(w.cu_q, w.cu_k, world, rank)
+        pb = oracle.Problem(cpu.q[sh.q0:sh.q1], cpu.k[sh.k0:sh.k1], cpu.v[sh.k0:sh.k1], sh.cu_q, sh.cu_k,
+                            w.softmax_scale, dout=cpu.dout[sh.q0:sh.q1])
+        rows, heads = oracle.all_pairs(sh.q1 - sh.q0, w.num_heads)
+        krows, kheads = oracle.all_pairs(sh.k1 - sh.k0, w.num_heads)
+        grows, gheads, gkrows, gkheads = rows + sh.q0, heads, krows + sh.k0, kheads
+    o, lse = pb.fwd(rows, heads)
+    dq, _ = pb.bwd_q(rows, heads)
+    dk, dv = pb.bwd_kv(krows, kheads)
+    return grows, gheads, o, lse, dq, gkrows, gkheads, dk, dv
+
+
+def _worker(rank, world, port, mode, out_path):
+    import torch.distributed as dist
+    dist.init_process_group("gloo", rank=rank, world_size=world, init_method="tcp://127.0.0.1:%d" % port)
+    try:
+        w = W.custom("shard", *_CASE[:2], _CASE[2], _CASE[3])
+        cpu = W.make_inputs(w, 0)
+        res = _shard_result(w, cpu, mode, world, rank)
+        gathered = [None] * world
+        dist.all_gather_object(gathered, res)  # only to bring the shards to one process for checking
+        t_max = S.max_over_ranks(float(rank + 1))
+        if rank == 0:
+            cat = [np.concatenate([g[i] for g in gathered]) for i in range(9)]
+            np.savez(out_path, *cat, t_max=np.float64(t_max))
+    finally:
+        dist.destroy_process_group()
+
+
+def _free_port():
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+@pytest.mark.parametrize("mode", ["heads", "segments"])
+def test_two_rank_shards_match_unsharded(mode):
+    oracle.build()
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    world = 2
+    with tempfile.TemporaryDirectory() as d:
+        out = os.path.join(d, "res.npz")
+        port = _free_port()
+        procs = [ctx.Process(target=_worker, args=(r, world, port, mode, out)) for r in range(world)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(timeout=240)
+        for p in procs:
+            if p.is_alive():
+                p.kill()
+                p.join()
+        assert all(p.exitcode == 0 for p in procs), [p.exitcode for p in procs]
+        z = np.load(out)
+        rows, heads, o, lse, dq, krows, kheads, dk, dv = (z["arr_%d" % i] for i in range(9))
+        assert float(z["t_max"]) == float(world)  # max over ranks of (rank + 1)
+
+    w = W.custom("shard", *_CASE[:2], _CASE[2], _CASE[3])
+    cpu = W.make_inputs(w, 0)
+    full = oracle.Problem(cpu.q, cpu.k, cpu.v, w.cu_q, w.cu_k, w.softmax_scale, dout=cpu.dout)
+    # every (row, head) pair computed exactly once across the ranks
+    assert sorted(zip(rows.tolist(), heads.tolist())) == sorted(zip(*[a.tolist() for a in oracle.all_pairs(w.total_q, w.num_heads)]))
+    assert sorted(zip(krows.tolist(), kheads.tolist())) == sorted(zip(*[a.tolist() for a in oracle.all_pairs(w.total_k, w.num_heads)]))
+    o_ref, lse_ref = full.fwd(rows, heads)
+    dq_ref, _ = full.bwd_q(rows, heads)
+    dk_ref, dv_ref = full.bwd_kv(krows, kheads)
+    # identical fp64 arithmetic per pair: the shards reproduce the full result bit for bit
+    np.testing.assert_array_equal(o, o_ref)
+    np.testing.assert_array_equal(lse, lse_ref)
+    np.testing.assert_array_equal(dq, dq_ref)
+    np.testing.assert_array_equal(dk, dk_ref)
+    np.testing.assert_array_equal(dv, dv_ref)
