@@ -648,8 +648,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           for (int i = 0; i < 64; ++i) blk0[i * 32 + lane] = i < n ? __uint_as_float(v[i]) : 0.f;
           fence_proxy_async_smem();
         }
-        __syncwarp();
-        if (drains && lane == 0) tma_reduce_add_3d(blk0, &tm_dq, quad * 32, tl.h, row0);
         // q columns [64, 128)
         tmem_ld32(tmem + lane_off + C::DP_COL + 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
         tmem_ld32(tmem + lane_off + C::DP_COL + 96, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
@@ -666,11 +664,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         __syncwarp();
         if (lane == 0) {
+          // The block in the dS^T buffer goes first, in a bulk group of its
+          // own: the compute warps wait for that buffer (ds_free), while the
+          // dO stage is not needed again until a later step.
           if (drains && n > 64) tma_reduce_add_3d(blk1, &tm_dq, quad * 32, tl.h, row0 + 64);
           bulk_commit();
-          bulk_wait_read_all();  // the staged blocks have been read
-          mbar_arrive(&bar.do_empty[gs % C::NDO]);
+          if (drains) tma_reduce_add_3d(blk0, &tm_dq, quad * 32, tl.h, row0);
+          bulk_commit();
+          bulk_wait_read_1();  // the dS^T-buffer block has been read
           mbar_arrive(&bar.ds_free);
+          bulk_wait_read_all();  // the dO-stage block has been read
+          mbar_arrive(&bar.do_empty[gs % C::NDO]);
         }
         __syncwarp();
       }
