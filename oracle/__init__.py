@@ -56,6 +56,7 @@ class _Problem(ctypes.Structure):
         ("batch", ctypes.c_int32), ("num_heads", ctypes.c_int32),
         ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32),
         ("scale", ctypes.c_double),
+        ("causal", ctypes.c_int32),
     ]
 
 
@@ -118,7 +119,7 @@ def _view_args(t: torch.Tensor | None, H: int, D: int):
 class Problem:
     """One packed-attention problem, held as CPU tensors (no copies)."""
 
-    def __init__(self, q, k, v, cu_q, cu_k, scale, dout=None):
+    def __init__(self, q, k, v, cu_q, cu_k, scale, dout=None, causal=False):
         dt = q.dtype
         if dt not in (torch.bfloat16, torch.float64):
             raise ValueError("oracle supports bf16 or fp64 inputs")
@@ -141,6 +142,7 @@ class Problem:
         s.num_heads, s.head_dim = self.H, self.D
         s.dtype = 0 if dt == torch.bfloat16 else 1
         s.scale = float(scale)
+        s.causal = 1 if causal else 0
         self._s = s
         self.has_dout = dout is not None
 

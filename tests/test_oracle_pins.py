@@ -72,6 +72,88 @@ def _torch_reference(q, k, v, do, cq, ck, scale):
     return out, lse, dq, dk, dv
 
 
+def _torch_causal_reference(q, k, v, do, cq, ck, scale):
+    """Per segment, causal: masked softmax attention in fp64 torch ops with
+    the mask of the reading (key jj visible to query ii iff
+    jj <= ii + Sk - Sq), gradients by autograd; a row that sees no key gets
+    o = 0 and LSE = -inf."""
+    H, D = q.shape[1], q.shape[2]
+    out = torch.zeros(q.shape, dtype=torch.float64)
+    lse = torch.full((q.shape[0], H), float("-inf"), dtype=torch.float64)
+    dq = torch.zeros(q.shape, dtype=torch.float64)
+    dk = torch.zeros(k.shape, dtype=torch.float64)
+    dv = torch.zeros(v.shape, dtype=torch.float64)
+    for b in range(len(cq) - 1):
+        Sq, Sk = cq[b + 1] - cq[b], ck[b + 1] - ck[b]
+        if Sq == 0 or Sk == 0:
+            continue
+        qs = q[cq[b]:cq[b + 1]].double().transpose(0, 1).clone().requires_grad_()
+        ks = k[ck[b]:ck[b + 1]].double().transpose(0, 1).clone().requires_grad_()
+        vs = v[ck[b]:ck[b + 1]].double().transpose(0, 1).clone().requires_grad_()
+        vis = torch.arange(Sk)[None, :] <= torch.arange(Sq)[:, None] + (Sk - Sq)   # [Sq, Sk]
+        live = vis.any(-1)                                                        # [Sq]
+        s = scale * (qs @ ks.transpose(1, 2))
+        s = torch.where(vis, s, torch.full_like(s, float("-inf")))
+        s = torch.where(live[:, None], s, torch.zeros_like(s))   # dead rows: no NaN in the graph
+        p = torch.where(live[:, None], torch.softmax(s, -1), torch.zeros_like(s))
+        o = p @ vs
+        gq, gk, gv = torch.autograd.grad(o, (qs, ks, vs), do[cq[b]:cq[b + 1]].double().transpose(0, 1))
+        out[cq[b]:cq[b + 1]] = o.detach().transpose(0, 1)
+        l = torch.logsumexp(s.detach(), dim=-1)
+        lse[cq[b]:cq[b + 1]] = torch.where(live[None, :], l, torch.full_like(l, float("-inf"))).T
+        dq[cq[b]:cq[b + 1]] = gq.transpose(0, 1)
+        dk[ck[b]:ck[b + 1]] = gk.transpose(0, 1)
+        dv[ck[b]:ck[b + 1]] = gv.transpose(0, 1)
+    return out, lse, dq, dk, dv
+
+
+def _causal_checks(lib, seed):
+    """Causal-mask pins: the masked torch reference, fp64 SDPA with
+    is_causal on the equal-length segment, rows that see no key, and rows
+    that see every key (identical to the unmasked oracle)."""
+    res = []
+    lq, lk = [5, 9, 6, 1, 0, 4], [9, 4, 6, 3, 2, 0]  # Sq < Sk, Sq > Sk (dead rows), Sq = Sk, one row, empties
+    H, D = 2, 8
+    cq, ck = _cu(lq), _cu(lk)
+    q, k, v = _rand((cq[-1], H, D), seed + 30), _rand((ck[-1], H, D), seed + 31), _rand((ck[-1], H, D), seed + 32)
+    do = _rand((cq[-1], H, D), seed + 33)
+    sc = 0.37
+    pc = oracle.Problem(q, k, v, cq, ck, sc, dout=do, causal=True)
+    pn = oracle.Problem(q, k, v, cq, ck, sc, dout=do)
+    rows, heads = oracle.all_pairs(cq[-1], H)
+    krows, kheads = oracle.all_pairs(ck[-1], H)
+    o, lse = pc.fwd(rows, heads, lib=lib)
+    dq, _ = pc.bwd_q(rows, heads, lib=lib)
+    dk, dv = pc.bwd_kv(krows, kheads, lib=lib)
+    ro, rl, rdq, rdk, rdv = _torch_causal_reference(q, k, v, do, cq, ck, sc)
+    res.append(("causal_out", np.allclose(o, ro.reshape(-1, D).numpy(), rtol=1e-12, atol=1e-13)))
+    res.append(("causal_lse", np.allclose(lse, rl.reshape(-1).numpy(), rtol=1e-12, atol=1e-13)))
+    res.append(("causal_dq", np.allclose(dq, rdq.reshape(-1, D).numpy(), rtol=1e-10, atol=1e-12)))
+    res.append(("causal_dk", np.allclose(dk, rdk.reshape(-1, D).numpy(), rtol=1e-10, atol=1e-12)))
+    res.append(("causal_dv", np.allclose(dv, rdv.reshape(-1, D).numpy(), rtol=1e-10, atol=1e-12)))
+    # equal lengths: fp64 SDPA with is_causal (a library routine)
+    b = 2
+    qs, ks, vs = (t[c[b]:c[b + 1]].transpose(0, 1)[None] for t, c in ((q, cq), (k, ck), (v, ck)))
+    so = F.scaled_dot_product_attention(qs, ks, vs, scale=sc, is_causal=True)[0].transpose(0, 1)
+    sel = (rows >= cq[b]) & (rows < cq[b + 1])
+    res.append(("causal_sdpa_is_causal", np.allclose(o[sel], so.reshape(-1, D).numpy(), rtol=1e-12, atol=1e-13)))
+    # rows that see no key: segment 1 (Sq=9, Sk=4), rows 0..4
+    dead = (rows >= cq[1]) & (rows < cq[1] + 5)
+    res.append(("causal_dead_rows", bool(np.all(np.isneginf(lse[dead])) and np.all(o[dead] == 0)
+                                         and np.all(dq[dead] == 0))))
+    # the last row of every segment with keys sees them all: same numbers as unmasked
+    on, ln = pn.fwd(rows, heads, lib=lib)
+    last = np.zeros(rows.shape, bool)
+    for bb in range(len(lq)):
+        if lq[bb] > 0 and lk[bb] > 0:
+            last |= rows == cq[bb + 1] - 1
+    res.append(("causal_last_row_unmasked", bool(np.array_equal(o[last], on[last]) and np.array_equal(lse[last], ln[last]))))
+    # Sq = Sk: the first row sees only the first key -> o = v_0
+    first = rows == cq[2]
+    res.append(("causal_first_row_v0", bool(np.array_equal(o[first], v[ck[2]].numpy()))))
+    return res
+
+
 def _all(pb, total):
     return oracle.all_pairs(total, pb.H)
 
@@ -181,6 +263,7 @@ def _battery(lib, seed=0):
     res.append(("grad_invariants", bool(inv)))
     # central finite differences of L = sum(O * dO)
     res.append(("finite_differences", _finite_difference_ok(lib, seed)))
+    res += _causal_checks(lib, seed)
     return res
 
 
@@ -291,6 +374,9 @@ MUTANTS = [
      "const int64_t k0 = pb->cu_k[b] + (b > 0), Sk"),
     ("delta from dO.v instead of dO.o", "E[ii] = dot(doi, oi, D);", "E[ii] = dot(doi, doi, D);"),
     ("head stride ignored", "int64_t off = row * rs + (int64_t)h * hs;", "int64_t off = row * rs;"),
+    ("causal diagonal one key early", "const int64_t n = ii + (Sk - Sq) + 1;", "const int64_t n = ii + (Sk - Sq);"),
+    ("causal diagonal aligned top-left", "const int64_t n = ii + (Sk - Sq) + 1;", "const int64_t n = ii + 1;"),
+    ("causal mask missing on the key side", "if (jj >= visible_keys(pb, b, ii)) continue;", "(void)jj;"),
 ]
 
 
