@@ -42,6 +42,10 @@ METRIC = "varlen attention TFLOP/s (fwd, bwd) bf16 H=56 D=128; % of GB300 bf16 T
 BWD_MAIN_DRAM_BYTES_PER_HEAD = {("windowed", 128): (872.579840e6 + 671.620352e6) / 8}
 
 
+def _metric(args) -> str:
+    return METRIC.replace("bf16", "bf16 causal") if getattr(args, "causal", False) else METRIC
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -134,13 +138,14 @@ def _max_over_ranks(x: float, ws: int) -> float:
 
 # ------------------------------------------------------------------ CPU side
 
-def _oracle_rate(w: W.Workload, target_s: float, seed: int = 0):
+def _oracle_rate(w: W.Workload, target_s: float, seed: int = 0, causal: bool = False):
     """Times the oracle (forward + query-side backward) on sampled (row, head)
     pairs of the workload.  Credits each pair with its share of the step's
-    algorithmic flops: 4*Sk*D (forward) + 10*Sk*D (backward)."""
+    algorithmic flops: 4*n*D (forward) + 10*n*D (backward), n = the keys the
+    row sees (Sk, or fewer under the causal mask)."""
     import oracle
     inp = W.make_inputs(w, seed)
-    pb = oracle.Problem(inp.q, inp.k, inp.v, inp.cu_q, inp.cu_k, w.softmax_scale, dout=inp.dout)
+    pb = oracle.Problem(inp.q, inp.k, inp.v, inp.cu_q, inp.cu_k, w.softmax_scale, dout=inp.dout, causal=causal)
     rng = np.random.default_rng(5)
     seg_k = {b: w.cu_k[b + 1] - w.cu_k[b] for b in range(w.batch)}
 
@@ -152,6 +157,10 @@ def _oracle_rate(w: W.Workload, target_s: float, seed: int = 0):
     def flops(rows):
         b = np.searchsorted(np.asarray(w.cu_q), rows, side="right") - 1
         sk = np.array([seg_k[int(x)] for x in b], dtype=np.float64)
+        if causal:  # keys row i of segment b sees: clamp(i + Sk - Sq + 1, 0, Sk)
+            sq = np.array([w.cu_q[int(x) + 1] - w.cu_q[int(x)] for x in b], dtype=np.float64)
+            ii = rows - np.asarray(w.cu_q)[b]
+            sk = np.clip(ii + sk - sq + 1, 0, sk)
         return float((14.0 * sk * w.head_dim).sum())
 
     def run(n):
@@ -173,7 +182,8 @@ def reference_arm(args, w, ws, rank):
     sample of the workload."""
     if rank != 0:
         return
-    run, n, cores = _oracle_rate(w, target_s=max(2.0, 150.0 / max(args.steps + args.warmup, 1)))
+    run, n, cores = _oracle_rate(w, target_s=max(2.0, 150.0 / max(args.steps + args.warmup, 1)),
+                                 causal=args.causal)
     for _ in range(args.warmup):
         run(n)
     tot_t = tot_f = 0.0
@@ -183,7 +193,7 @@ def reference_arm(args, w, ws, rank):
         tot_f += f
     val = tot_f / tot_t / 1e12
     sample = "oracle fwd + dQ backward on %d random (row, head) pairs of the %s workload per step" % (n, w.name)
-    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+    line = {"impl": "reference", "metric": _metric(args), "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": w.name, "sample": sample},
@@ -211,18 +221,20 @@ def ours(args, w, ws, rank, local):
 
     def fwd():
         st = va.varlen_attn_fwd(d.q, d.k, d.v, d.cu_q, d.cu_k, w.batch, w.total_q, w.total_k, H, D, w.max_q(),
-                                w.max_k(), scale, out, lse, stream)
+                                w.max_k(), scale, out, lse, stream, causal=args.causal)
         assert st == 0, va.varlen_attn_status_string(st)
 
     def bwd():
         st = va.varlen_attn_bwd(d.q, d.k, d.v, out, d.dout, lse, d.cu_q, d.cu_k, w.batch, w.total_q, w.total_k,
-                                H, D, w.max_q(), w.max_k(), scale, dq, dk, dv, wsp, ws_bytes, stream)
+                                H, D, w.max_q(), w.max_k(), scale, dq, dk, dv, wsp, ws_bytes, stream,
+                                causal=args.causal)
         assert st == 0, va.varlen_attn_status_string(st)
 
     # does the backward exist in this build?
     fwd()
     has_bwd = va.varlen_attn_bwd(d.q, d.k, d.v, out, d.dout, lse, d.cu_q, d.cu_k, w.batch, w.total_q, w.total_k,
-                                 H, D, w.max_q(), w.max_k(), scale, dq, dk, dv, wsp, ws_bytes, stream) == 0
+                                 H, D, w.max_q(), w.max_k(), scale, dq, dk, dv, wsp, ws_bytes, stream,
+                                 causal=args.causal) == 0
     torch.cuda.synchronize()
     assert va.varlen_attn_get_device_status(stream) == 0
 
@@ -265,7 +277,7 @@ def ours(args, w, ws, rank, local):
     ms_total = _max_over_ranks(e_start.elapsed_time(e_end), ws)
     t_fwd = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     t_bwd = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
-    f_fwd, f_bwd = w.fwd_flops(), (w.bwd_flops() if has_bwd else 0.0)
+    f_fwd, f_bwd = w.fwd_flops(args.causal), (w.bwd_flops(args.causal) if has_bwd else 0.0)
     step_flops = f_fwd + f_bwd
     value = ws * K * step_flops / (ms_total * 1e-3) / 1e12
     fwd_tflops = f_fwd / (statistics.mean(t_fwd) * 1e-3) / 1e12
@@ -339,7 +351,7 @@ def ours(args, w, ws, rank, local):
     # Every head reads its own q, k, v, dout and writes its own dk, dv and dq rows, so the
     # traffic scales with the number of heads.  Reported only for that workload and head size.
     traffic = None
-    if dom_name == "varlen_bwd_main_kernel" and (w.name, D) in BWD_MAIN_DRAM_BYTES_PER_HEAD:
+    if dom_name == "varlen_bwd_main_kernel" and not args.causal and (w.name, D) in BWD_MAIN_DRAM_BYTES_PER_HEAD:
         traffic = BWD_MAIN_DRAM_BYTES_PER_HEAD[(w.name, D)] * H
     roof = {"kernel": dom_name, "bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
             "frac": ach / peak, "peak_source": "%s bf16_tflops (burst)" % src,
@@ -347,7 +359,7 @@ def ours(args, w, ws, rank, local):
 
     cpu_base = None
     if not args.no_cpu_baseline and ws >= 1:
-        run, n, cores = _oracle_rate(w, target_s=12.0)
+        run, n, cores = _oracle_rate(w, target_s=12.0, causal=args.causal)
         t, f, n = run(n)
         cpu_base = {"value": f / t / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                     "sample": "oracle fwd + dQ backward on %d random (row, head) pairs of the %s workload "
@@ -355,11 +367,12 @@ def ours(args, w, ws, rank, local):
 
     burst = float(peaks.get("bf16_tflops"))
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": K, "warmup": Wm,
+        "metric": _metric(args), "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": K, "warmup": Wm,
         "ms_per_step": ms_total / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "batch_segments": w.batch, "total_q": w.total_q, "total_k": w.total_k,
                    "num_heads": H, "head_dim": D, "step": "fwd+bwd" if has_bwd else "fwd only (bwd missing)",
+                   "causal": bool(args.causal),
                    "l2": "inputs larger than L2 (k, v 2 GB each); no flush",
                    "parallelism": "replicas" if ws > 1 else "single GPU"},
         "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
@@ -384,6 +397,8 @@ def main():
     ap.add_argument("--workload", default="windowed", choices=sorted(W.WORKLOADS))
     ap.add_argument("--heads", type=int, default=None,
                     help="override the head count (small cases for profiling captures)")
+    ap.add_argument("--causal", action="store_true",
+                    help="time the causal entry points (FLOPs counted over visible pairs only)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -117,6 +117,30 @@ int varlen_attn_bwd(const void* q, varlen_stride sq, const void* k, varlen_strid
                     void* dv, varlen_stride sdv, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Causal forward and backward.  Arguments, layouts, ownership and errors are
+ * those of varlen_attn_fwd / varlen_attn_bwd.  The pages call the varlen
+ * function with causal=False only ("[FA4] cute varlen backward: int32
+ * overflow in _bwd_preprocess", "Minimal repro"); for causal=True these take
+ * the alignment of that API, the diagonal meeting the last key at the last
+ * query: q row i of a segment (0-based within it) attends to kv rows
+ * j <= i + Sk - Sq of the same segment.  A row that sees no key (possible
+ * when Sq > Sk) gets O = 0, LSE = -inf and dQ = 0, and adds nothing to dK /
+ * dV.  Work past the diagonal is skipped, not masked.
+ */
+int varlen_attn_fwd_causal(const void* q, varlen_stride sq, const void* k, varlen_stride sk, const void* v,
+                           varlen_stride sv, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                           int32_t batch, int32_t total_q, int32_t total_k, int32_t num_heads, int32_t head_dim,
+                           int32_t max_seqlen_q, int32_t max_seqlen_k, float scale, void* out, varlen_stride so,
+                           float* lse, void* stream);
+int varlen_attn_bwd_causal(const void* q, varlen_stride sq, const void* k, varlen_stride sk, const void* v,
+                           varlen_stride sv, const void* out, varlen_stride so, const void* dout,
+                           varlen_stride sdo, const float* lse, const int32_t* cu_seqlens_q,
+                           const int32_t* cu_seqlens_k, int32_t batch, int32_t total_q, int32_t total_k,
+                           int32_t num_heads, int32_t head_dim, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                           float scale, void* dq, varlen_stride sdq, void* dk, varlen_stride sdk, void* dv,
+                           varlen_stride sdv, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Backward without a workspace argument, for callers that cannot allocate
  * device memory (code inside a host framework that owns every device
  * allocation, or on a path where cudaMalloc is not allowed).  The paper has

@@ -157,11 +157,12 @@ size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 using namespace varlen;
 
-extern "C" int varlen_attn_fwd(const void* q, varlen_stride sq, const void* k, varlen_stride sk, const void* v,
-                               varlen_stride sv, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
-                               int32_t batch, int32_t total_q, int32_t total_k, int32_t num_heads, int32_t head_dim,
-                               int32_t max_seqlen_q, int32_t max_seqlen_k, float scale, void* out,
-                               varlen_stride so, float* lse, void* stream) {
+namespace {
+
+int fwd_impl(const void* q, varlen_stride sq, const void* k, varlen_stride sk, const void* v, varlen_stride sv,
+             const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t batch, int32_t total_q,
+             int32_t total_k, int32_t num_heads, int32_t head_dim, int32_t max_seqlen_q, int32_t max_seqlen_k,
+             float scale, void* out, varlen_stride so, float* lse, void* stream, int32_t causal) {
   (void)max_seqlen_q;  // advisory only: the kernels derive lengths from cu_seqlens
   (void)max_seqlen_k;
   int st = check_common(cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads, head_dim, scale);
@@ -189,12 +190,34 @@ extern "C" int varlen_attn_fwd(const void* q, varlen_stride sq, const void* k, v
   L.p.total_q = total_q;
   L.p.total_k = total_k;
   L.p.num_heads = num_heads;
+  L.p.causal = causal;
   L.p.scale_log2 = scale * kLog2e;
   L.p.err = dev.err;
   L.head_dim = head_dim;
   L.grid = dev.sms;
   cudaError_t e = launch_fwd(L, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? VARLEN_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" int varlen_attn_fwd(const void* q, varlen_stride sq, const void* k, varlen_stride sk, const void* v,
+                               varlen_stride sv, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                               int32_t batch, int32_t total_q, int32_t total_k, int32_t num_heads, int32_t head_dim,
+                               int32_t max_seqlen_q, int32_t max_seqlen_k, float scale, void* out,
+                               varlen_stride so, float* lse, void* stream) {
+  return fwd_impl(q, sq, k, sk, v, sv, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads, head_dim,
+                  max_seqlen_q, max_seqlen_k, scale, out, so, lse, stream, 0);
+}
+
+extern "C" int varlen_attn_fwd_causal(const void* q, varlen_stride sq, const void* k, varlen_stride sk,
+                                      const void* v, varlen_stride sv, const int32_t* cu_seqlens_q,
+                                      const int32_t* cu_seqlens_k, int32_t batch, int32_t total_q, int32_t total_k,
+                                      int32_t num_heads, int32_t head_dim, int32_t max_seqlen_q,
+                                      int32_t max_seqlen_k, float scale, void* out, varlen_stride so, float* lse,
+                                      void* stream) {
+  return fwd_impl(q, sq, k, sk, v, sv, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads, head_dim,
+                  max_seqlen_q, max_seqlen_k, scale, out, so, lse, stream, 1);
 }
 
 extern "C" size_t varlen_attn_bwd_workspace_size(int32_t batch, int32_t total_q, int32_t num_heads,
@@ -205,13 +228,14 @@ extern "C" size_t varlen_attn_bwd_workspace_size(int32_t batch, int32_t total_q,
   return round256(rows * num_heads * head_dim * sizeof(float)) + 2 * round256(prow * num_heads * sizeof(float));
 }
 
-extern "C" int varlen_attn_bwd(const void* q, varlen_stride sq, const void* k, varlen_stride sk, const void* v,
-                               varlen_stride sv, const void* out, varlen_stride so, const void* dout,
-                               varlen_stride sdo, const float* lse, const int32_t* cu_seqlens_q,
-                               const int32_t* cu_seqlens_k, int32_t batch, int32_t total_q, int32_t total_k,
-                               int32_t num_heads, int32_t head_dim, int32_t max_seqlen_q, int32_t max_seqlen_k,
-                               float scale, void* dq, varlen_stride sdq, void* dk, varlen_stride sdk, void* dv,
-                               varlen_stride sdv, void* workspace, size_t workspace_bytes, void* stream) {
+namespace {
+
+int bwd_impl(const void* q, varlen_stride sq, const void* k, varlen_stride sk, const void* v, varlen_stride sv,
+             const void* out, varlen_stride so, const void* dout, varlen_stride sdo, const float* lse,
+             const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t batch, int32_t total_q,
+             int32_t total_k, int32_t num_heads, int32_t head_dim, int32_t max_seqlen_q, int32_t max_seqlen_k,
+             float scale, void* dq, varlen_stride sdq, void* dk, varlen_stride sdk, void* dv, varlen_stride sdv,
+             void* workspace, size_t workspace_bytes, void* stream, int32_t causal) {
   (void)max_seqlen_q;
   (void)max_seqlen_k;
   int st = check_common(cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads, head_dim, scale);
@@ -264,6 +288,7 @@ extern "C" int varlen_attn_bwd(const void* q, varlen_stride sq, const void* k, v
   L.p.total_k = total_k;
   L.p.num_heads = num_heads;
   L.p.pad_rows = pad_rows;
+  L.p.causal = causal;
   L.p.scale_log2 = scale * kLog2e;
   L.p.scale = scale;
   L.p.err = dev.err;
@@ -277,6 +302,33 @@ extern "C" int varlen_attn_bwd(const void* q, varlen_stride sq, const void* k, v
   }
   cudaError_t e = launch_bwd(L, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? VARLEN_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" int varlen_attn_bwd(const void* q, varlen_stride sq, const void* k, varlen_stride sk, const void* v,
+                               varlen_stride sv, const void* out, varlen_stride so, const void* dout,
+                               varlen_stride sdo, const float* lse, const int32_t* cu_seqlens_q,
+                               const int32_t* cu_seqlens_k, int32_t batch, int32_t total_q, int32_t total_k,
+                               int32_t num_heads, int32_t head_dim, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                               float scale, void* dq, varlen_stride sdq, void* dk, varlen_stride sdk, void* dv,
+                               varlen_stride sdv, void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_impl(q, sq, k, sk, v, sv, out, so, dout, sdo, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k,
+                  num_heads, head_dim, max_seqlen_q, max_seqlen_k, scale, dq, sdq, dk, sdk, dv, sdv, workspace,
+                  workspace_bytes, stream, 0);
+}
+
+extern "C" int varlen_attn_bwd_causal(const void* q, varlen_stride sq, const void* k, varlen_stride sk,
+                                      const void* v, varlen_stride sv, const void* out, varlen_stride so,
+                                      const void* dout, varlen_stride sdo, const float* lse,
+                                      const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t batch,
+                                      int32_t total_q, int32_t total_k, int32_t num_heads, int32_t head_dim,
+                                      int32_t max_seqlen_q, int32_t max_seqlen_k, float scale, void* dq,
+                                      varlen_stride sdq, void* dk, varlen_stride sdk, void* dv, varlen_stride sdv,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_impl(q, sq, k, sk, v, sv, out, so, dout, sdo, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k,
+                  num_heads, head_dim, max_seqlen_q, max_seqlen_k, scale, dq, sdq, dk, sdk, dv, sdv, workspace,
+                  workspace_bytes, stream, 1);
 }
 
 extern "C" int varlen_attn_get_device_status(void* stream) {

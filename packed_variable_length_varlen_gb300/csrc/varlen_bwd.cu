@@ -154,6 +154,20 @@ struct BwdCfg {
   static constexpr int TMEM_COLS = 512;
 };
 
+// The q steps [j0, nq) a kv tile works through (128 q rows each).  With the
+// causal mask (q row i sees keys j <= i + Sk - Sq) the steps whose rows all
+// precede the tile's first key are skipped; j0 == nq means no query sees
+// the tile (dK = dV = 0).  The cursor's scheduled side is kv.
+__device__ __forceinline__ void bwd_q_steps(const SegCursor& c, int32_t tile_m, int32_t causal, int32_t& j0,
+                                            int32_t& nq) {
+  nq = (c.olen + kBwdTileQ - 1) / kBwdTileQ;
+  j0 = 0;
+  if (causal) {
+    const int32_t first_q = tile_m * kTileM - (c.len - c.olen);  // first q row that sees the tile's first key
+    j0 = first_q <= 0 ? 0 : min(nq, first_q / kBwdTileQ);
+  }
+}
+
 // 512 threads: warpgroup 0 = Q/K/V producer (warp 0), MMA issuer (warp 1),
 // dO producer (warp 2); warpgroups 1-2 = compute; warpgroup 3 = dQ drain.
 constexpr int kBwdThreads = 512;
@@ -182,7 +196,7 @@ __device__ __forceinline__ void clear_rows(uint8_t* tile, int chunks, int chunk_
   }
 }
 
-template <int D>
+template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     varlen_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -256,8 +270,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       bool ok = true;
       for (int64_t t = blockIdx.x;
            ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q); t += G) {
-        if (c.olen == 0) continue;  // no queries: dK = dV = 0, written by the compute warps
         const Tile tl = cursor_tile(c, t);
+        int32_t j0, nq;
+        bwd_q_steps(c, tl.m, CAUSAL, j0, nq);
+        if (j0 == nq) continue;  // no query sees the tile: dK = dV = 0, written by the compute warps
         const int32_t krow = c.r0 + tl.m * kTileM;
         if (tiles > 0 && !mbar_wait(&bar.kv_empty, (tiles - 1) & 1, abort)) break;
         mbar_arrive_expect_tx(&bar.kv_full, C::K_BYTES + C::V_BYTES);
@@ -268,8 +284,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int cc = 0; cc < C::NC; ++cc)
           tma_load_3d(v_smem + cc * C::CHUNK, &tm_v, &bar.kv_full, cc * 64, tl.h, krow);
         ++tiles;
-        const int32_t nq = (c.olen + QT - 1) / QT;
-        for (int32_t j = 0; j < nq; ++j, ++gs) {
+        for (int32_t j = j0; j < nq; ++j, ++gs) {
           const uint32_t st = gs % C::NQ;
           if (!mbar_wait(&bar.q_empty[st], ((gs / C::NQ) & 1) ^ 1, abort)) { ok = false; break; }
           mbar_arrive_expect_tx(&bar.q_full[st], C::T_BYTES + C::ROWV_BYTES);
@@ -299,10 +314,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       bool ok = true;
       for (int64_t t = blockIdx.x;
            ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q); t += G) {
-        if (c.olen == 0) continue;
         const Tile tl = cursor_tile(c, t);
-        const int32_t nq = (c.olen + QT - 1) / QT;
-        for (int32_t j = 0; j < nq; ++j, ++gs) {
+        int32_t j0, nq;
+        bwd_q_steps(c, tl.m, CAUSAL, j0, nq);
+        for (int32_t j = j0; j < nq; ++j, ++gs) {
           const uint32_t st = gs % C::NDO;
           if (!mbar_wait(&bar.do_empty[st], ((gs / C::NDO) & 1) ^ 1, abort)) { ok = false; break; }
           mbar_arrive_expect_tx(&bar.do_full[st], C::T_BYTES + C::ROWV_BYTES);
@@ -403,8 +418,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
       for (int64_t t = blockIdx.x;
            ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q); t += G) {
-        if (c.olen == 0) continue;
         const Tile tl = cursor_tile(c, t);
+        int32_t j0, nq;
+        bwd_q_steps(c, tl.m, CAUSAL, j0, nq);
+        if (j0 == nq) continue;
         if (!mbar_wait(&bar.kv_full, tiles & 1, abort)) break;
         const int32_t kv_valid = min(kTileM, c.len - tl.m * kTileM);
         const int nk_kv = (kv_valid + 15) >> 4;  // kv k-steps of dQ^T
@@ -414,25 +431,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           clear_rows(k_smem, C::KCH, C::CHUNK, kv_valid, min(kTileM, nk_kv * 16));
           fence_proxy_async_smem();
         }
-        const int32_t nq = (c.olen + QT - 1) / QT;
         // prologue: S^T and dP^T of the tile's first step.  The S^T columns
         // were last read by dV of the previous step (earlier in this
         // thread's MMA order); the dP^T columns held the previous dQ^T.
-        if (!ready(&bar.q_full[gs % C::NQ], (gs / C::NQ) & 1, q_smem + (gs % C::NQ) * C::T_BYTES, c.olen)) break;
+        if (!ready(&bar.q_full[gs % C::NQ], (gs / C::NQ) & 1, q_smem + (gs % C::NQ) * C::T_BYTES,
+                   c.olen - j0 * QT)) break;
         tc_fence_after();
         issue_s(gs);
         if (gs > 0 && !mbar_wait(&bar.dq_free, (gs - 1) & 1, abort)) break;
-        if (!ready(&bar.do_full[gs % C::NDO], (gs / C::NDO) & 1, do_smem + (gs % C::NDO) * C::T_BYTES, c.olen)) break;
+        if (!ready(&bar.do_full[gs % C::NDO], (gs / C::NDO) & 1, do_smem + (gs % C::NDO) * C::T_BYTES,
+                   c.olen - j0 * QT)) break;
         tc_fence_after();
         issue_dp(gs);
-        for (int32_t j = 0; j < nq; ++j, ++gs) {
+        for (int32_t j = j0; j < nq; ++j, ++gs) {
           const bool more = j + 1 < nq;
           const int nk_q = (min(QT, c.olen - j * QT) + 15) >> 4;  // q k-steps of dV / dK
           // dV_g += P^T_g dO_g, P^T_g read from TMEM
           if (!mbar_wait(&bar.p_ready, gs & 1, abort)) { ok = false; break; }
-          if (j == 0 && tiles > 0 && !mbar_wait(&bar.acc_free, (tiles - 1) & 1, abort)) { ok = false; break; }
+          if (j == j0 && tiles > 0 && !mbar_wait(&bar.acc_free, (tiles - 1) & 1, abort)) { ok = false; break; }
           tc_fence_after();
-          issue_dv(gs, nk_q, j > 0);
+          issue_dv(gs, nk_q, j > j0);  // the tile's first step starts the accumulation
           // S^T_{g+1}: overwrites P^T_g after dV_g has read it (same-thread MMA order)
           if (more) {
             const uint32_t g1 = gs + 1;
@@ -445,7 +463,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!mbar_wait(&bar.ds_ready, gs & 1, abort)) { ok = false; break; }
           tc_fence_after();
           issue_dq(nk_kv);
-          issue_dk(gs, nk_q, j > 0);
+          issue_dk(gs, nk_q, j > j0);
           mma_commit(&bar.ps_free);
           if (!more) {
             mma_commit(&bar.kv_empty);
@@ -485,8 +503,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int32_t kv_valid = c.len - tl.m * kTileM;
       const bool row_valid = r < kv_valid;
       const int64_t krow = (int64_t)c.r0 + tl.m * kTileM + r;
-      const int32_t nq = (c.olen + QT - 1) / QT;
-      if (nq == 0) {
+      int32_t j0, nq;
+      bwd_q_steps(c, tl.m, CAUSAL, j0, nq);
+      if (j0 == nq) {
         if (row_valid) {
           __nv_bfloat16* dvrow = p.dv + krow * p.dv_rs + (int64_t)tl.h * p.dv_hs;
           __nv_bfloat16* dkrow = p.dk + krow * p.dk_rs + (int64_t)tl.h * p.dk_hs;
@@ -497,9 +516,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         continue;
       }
-      for (int32_t j = 0; j < nq; ++j, ++gs) {
+      // with the causal mask this key (index jr in the segment) is seen by q
+      // rows i >= jr - (Sk - Sq)
+      const int32_t q_first = CAUSAL ? tl.m * kTileM + r - (c.len - c.olen) : 0;
+      for (int32_t j = j0; j < nq; ++j, ++gs) {
         const int32_t qc0 = j * QT + half * 64;             // first q column of this thread (in the segment)
         const int32_t nvalid = row_valid ? max(0, min(64, c.olen - qc0)) : 0;
+        const int32_t lo = CAUSAL ? min(64, max(0, q_first - qc0)) : 0;  // columns [lo, nvalid) are visible
         // this step's lse2 / delta rows arrive with its Q / dO tiles
         const float4* l4 = reinterpret_cast<const float4*>(lse_rows + (gs % C::NQ) * QT + half * 64);
         const float4* d4 = reinterpret_cast<const float4*>(delta_rows + (gs % C::NDO) * QT + half * 64);
@@ -520,10 +543,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                     make_float2(c2, c2), make_float2(-l.x, -l.y));
             const float2 t1 = ffma2(make_float2(__uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3])),
                                     make_float2(c2, c2), make_float2(-l.z, -l.w));
-            pv[i] = (i < nvalid) ? ex2(t0.x) : 0.f;
-            pv[i + 1] = (i + 1 < nvalid) ? ex2(t0.y) : 0.f;
-            pv[i + 2] = (i + 2 < nvalid) ? ex2(t1.x) : 0.f;
-            pv[i + 3] = (i + 3 < nvalid) ? ex2(t1.y) : 0.f;
+            pv[i] = (i >= lo && i < nvalid) ? ex2(t0.x) : 0.f;
+            pv[i + 1] = (i + 1 >= lo && i + 1 < nvalid) ? ex2(t0.y) : 0.f;
+            pv[i + 2] = (i + 2 >= lo && i + 2 < nvalid) ? ex2(t1.x) : 0.f;
+            pv[i + 3] = (i + 3 >= lo && i + 3 < nvalid) ? ex2(t1.y) : 0.f;
           }
         }
         {
@@ -557,8 +580,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                    fadd2(make_float2(__uint_as_float(dpv[i + 2]), __uint_as_float(dpv[i + 3])),
                                          make_float2(-dl.z, -dl.w)));
             // select, not multiply: dP^T and delta past the segment end may hold NaN
-            dk2[ii / 2] = pack_bf16x2(ii < nvalid ? a.x : 0.f, ii + 1 < nvalid ? a.y : 0.f);
-            dk2[ii / 2 + 1] = pack_bf16x2(ii + 2 < nvalid ? b.x : 0.f, ii + 3 < nvalid ? b.y : 0.f);
+            dk2[ii / 2] = pack_bf16x2(ii >= lo && ii < nvalid ? a.x : 0.f, ii + 1 >= lo && ii + 1 < nvalid ? a.y : 0.f);
+            dk2[ii / 2 + 1] =
+                pack_bf16x2(ii + 2 >= lo && ii + 2 < nvalid ? b.x : 0.f, ii + 3 >= lo && ii + 3 < nvalid ? b.y : 0.f);
           }
         }
         // the dS^T buffer is free once dQ^T and dK of the previous step are
@@ -628,10 +652,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bool ok = true;
     for (int64_t t = blockIdx.x;
          ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q); t += G) {
-      if (c.olen == 0) continue;
       const Tile tl = cursor_tile(c, t);
-      const int32_t nq = (c.olen + QT - 1) / QT;
-      for (int32_t j = 0; j < nq; ++j, ++gs) {
+      int32_t j0, nq;
+      bwd_q_steps(c, tl.m, CAUSAL, j0, nq);
+      for (int32_t j = j0; j < nq; ++j, ++gs) {
         if (!mbar_wait(&bar.dq_full, gs & 1, abort)) { ok = false; break; }
         tc_fence_after();
         const int32_t n = min(QT, c.olen - j * QT);  // valid q columns of this step
@@ -692,14 +716,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (threadIdx.x == 0 && bar.abort) record_error(p.err, kErrTimeout);
 }
 
-template <int D>
+template <int D, bool CAUSAL>
 static cudaError_t launch_bwd_d(const BwdLaunch& L, cudaStream_t stream) {
   using C = BwdCfg<D>;
   const int elem_grid = L.grid * 8;
   auto mark = [&](int i) {
     if (L.phase_events[i] != nullptr) cudaEventRecord(L.phase_events[i], stream);
   };
-  auto kern = varlen_bwd_main_kernel<D>;
+  auto kern = varlen_bwd_main_kernel<D, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   // The warpgroup register split assumes the kernel was compiled to exactly
@@ -725,9 +749,9 @@ static cudaError_t launch_bwd_d(const BwdLaunch& L, cudaStream_t stream) {
 
 cudaError_t launch_bwd(const BwdLaunch& L, cudaStream_t stream) {
   switch (L.head_dim) {
-    case 64: return launch_bwd_d<64>(L, stream);
-    case 96: return launch_bwd_d<96>(L, stream);
-    case 128: return launch_bwd_d<128>(L, stream);
+    case 64: return L.p.causal ? launch_bwd_d<64, true>(L, stream) : launch_bwd_d<64, false>(L, stream);
+    case 96: return L.p.causal ? launch_bwd_d<96, true>(L, stream) : launch_bwd_d<96, false>(L, stream);
+    case 128: return L.p.causal ? launch_bwd_d<128, true>(L, stream) : launch_bwd_d<128, false>(L, stream);
     default: return cudaErrorInvalidValue;
   }
 }

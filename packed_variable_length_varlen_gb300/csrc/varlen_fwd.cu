@@ -41,6 +41,20 @@ namespace varlen {
 
 constexpr int kFwdUnit = 2 * kTileM;  // q rows per scheduled unit (two halves)
 
+// kv tiles a unit (256 q rows of one segment and head) works through.  With
+// the causal mask (q row i of the segment sees keys j <= i + Sk - Sq) tiles
+// past the unit's last visible key are skipped; 0 means no row of the unit
+// sees a key (O = 0, LSE = -inf).  The cursor's scheduled side is q.
+__device__ __forceinline__ int32_t fwd_kv_tiles(const SegCursor& c, int32_t unit, int32_t causal) {
+  int32_t nkv = (c.olen + kTileN - 1) / kTileN;
+  if (causal) {
+    const int32_t q_last = min(c.len, (unit + 1) * kFwdUnit) - 1;
+    const int32_t lim = q_last + (c.olen - c.len) + 1;  // keys the unit's last row sees
+    nkv = lim <= 0 ? 0 : min(nkv, (lim + kTileN - 1) / kTileN);
+  }
+  return nkv;
+}
+
 template <int D>
 struct FwdCfg {
   static constexpr int NC = (D + 63) / 64;              // 64-column chunks of a tile
@@ -65,15 +79,15 @@ static_assert(sizeof(FwdBarriers) <= 1024, "barrier block too large");
 
 // Registers: the block launches 384 threads at 168 registers (64,512).
 // Warpgroup 0 (producer, MMA, two idle warps) drops to 112 and the two
-// softmax warpgroups rise to 176: 112*128 + 2*176*128 = 59,392 <= 64,512,
+// softmax warpgroups rise to 192: 112*128 + 2*192*128 = 63,488 <= 64,512,
 // and each SM sub-partition holds one warp of each group:
-// (112+176+176)*32 <= 16K.
-constexpr uint32_t kFwdRegsLaunch = 168, kFwdRegsCtl = 112, kFwdRegsSoftmax = 176;
+// (112+192+192)*32 <= 16K.
+constexpr uint32_t kFwdRegsLaunch = 168, kFwdRegsCtl = 112, kFwdRegsSoftmax = 192;
 static_assert(kFwdRegsCtl + 2 * kFwdRegsSoftmax <= 3 * kFwdRegsLaunch,
               "warpgroup register split exceeds the launch allocation");
 static_assert(kFwdRegsLaunch * 384 <= 65536, "launch register count too large for 384 threads");
 
-template <int D>
+template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(384, 1)
     varlen_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -128,8 +142,9 @@ __global__ void __launch_bounds__(384, 1)
       for (int64_t t = blockIdx.x; ok && cursor_seek<kFwdUnit>(c, t, p.num_heads, p.cu_q, p.cu_k, p.batch,
                                                                  p.total_q, p.total_k);
            t += G) {
-        if (c.olen == 0) continue;  // no keys: the softmax role writes O = 0, LSE = -inf
         const Tile tl = cursor_tile(c, t);
+        const int32_t nkv = fwd_kv_tiles(c, tl.m, CAUSAL);
+        if (nkv == 0) continue;  // no visible keys: the softmax role writes O = 0, LSE = -inf
         const int32_t qrow = c.r0 + tl.m * kFwdUnit;
         if (q_loads > 0 && !mbar_wait(&bar.q_empty, (q_loads - 1) & 1, abort)) break;
         mbar_arrive_expect_tx(&bar.q_full, 2 * C::TILE);
@@ -140,7 +155,6 @@ __global__ void __launch_bounds__(384, 1)
             tma_load_3d(q_smem + hf * C::TILE + cc * C::CHUNK, &tm_q, &bar.q_full, cc * 64, tl.h,
                         qrow + hf * kTileM);
         ++q_loads;
-        const int32_t nkv = (c.olen + kTileN - 1) / kTileN;
         for (int32_t j = 0; ok && j < nkv; ++j) {
           const int32_t krow = c.o0 + j * kTileN;
 #pragma unroll
@@ -209,10 +223,10 @@ __global__ void __launch_bounds__(384, 1)
     };
     for (int64_t t = blockIdx.x;
          ok && cursor_seek<kFwdUnit>(c, t, p.num_heads, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k); t += G) {
-      if (c.olen == 0) continue;
+      const int32_t nkv = fwd_kv_tiles(c, cursor_tile(c, t).m, CAUSAL);
+      if (nkv == 0) continue;
       if (!mbar_wait(&bar.q_full, tiles & 1, abort)) break;
       ++tiles;
-      const int32_t nkv = (c.olen + kTileN - 1) / kTileN;
       // prologue: S_A and S_B of kv step 0
       {
         const uint32_t kslot = ring0 % C::NSLOT;
@@ -284,8 +298,9 @@ __global__ void __launch_bounds__(384, 1)
     bool ok = true;
     for (int64_t t = blockIdx.x;
          ok && cursor_seek<kFwdUnit>(c, t, p.num_heads, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k); t += G) {
-      if (c.olen == 0) {
-        const Tile tl = cursor_tile(c, t);
+      const Tile tl = cursor_tile(c, t);
+      const int32_t nkv = fwd_kv_tiles(c, tl.m, CAUSAL);
+      if (nkv == 0) {
         const int32_t r_in_seg = tl.m * kFwdUnit + hf * kTileM + row;
         const int64_t grow = (int64_t)c.r0 + r_in_seg;
         __nv_bfloat16* orow = p.out + grow * p.o_rs + (int64_t)tl.h * p.o_hs;
@@ -297,7 +312,10 @@ __global__ void __launch_bounds__(384, 1)
         }
         continue;
       }
-      const int32_t nkv = (c.olen + kTileN - 1) / kTileN;
+      // keys this row sees: all Sk, or with the causal mask those with index
+      // <= r + Sk - Sq (r = the row's index within the segment)
+      const int32_t r_seg = tl.m * kFwdUnit + hf * kTileM + row;
+      const int32_t row_keys = CAUSAL ? min(c.olen, max(0, r_seg + (c.olen - c.len) + 1)) : c.olen;
       float m_use = -INFINITY, l = 0.f;
       for (int32_t j = 0; j < nkv; ++j) {
         const uint32_t gj = g + j;
@@ -319,10 +337,12 @@ __global__ void __launch_bounds__(384, 1)
         float x[128];
 #pragma unroll
         for (int i = 0; i < 128; ++i) x[i] = __uint_as_float(s[i]);
-        const int32_t kv_valid = c.olen - j * kTileN;
-        if (kv_valid < kTileN) {
+        // columns past the row's last visible key (the segment end, or the
+        // causal diagonal) are masked to -inf by select
+        const int32_t lim = row_keys - j * kTileN;  // per thread
+        if (__any_sync(0xffffffffu, lim < kTileN)) {
 #pragma unroll
-          for (int i = 0; i < 128; ++i) x[i] = (i < kv_valid) ? x[i] : -INFINITY;
+          for (int i = 0; i < 128; ++i) x[i] = (i < lim) ? x[i] : -INFINITY;
         }
         // row max: four independent chains of 3-input max
         float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
@@ -348,7 +368,10 @@ __global__ void __launch_bounds__(384, 1)
         // P goes to TMEM in two 32-column halves as it is produced, which
         // keeps the live register set small.  Half h writes P columns
         // [32h, 32h+32), whose S values were consumed already.
-        const float2 cc2 = make_float2(c2, c2), negm = make_float2(-m_use, -m_use);
+        // a row that has seen no key yet keeps m = -inf; subtracting 0 then
+        // gives P = exp2(-inf) = 0 instead of NaN
+        const float m_sub = (CAUSAL && m_use == -INFINITY) ? 0.f : m_use;
+        const float2 cc2 = make_float2(c2, c2), negm = make_float2(-m_sub, -m_sub);
         float2 rs2a = make_float2(0.f, 0.f), rs2b = make_float2(0.f, 0.f);
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
@@ -385,8 +408,7 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (!ok) break;
       // epilogue: wait for the last O += P V of this half, then O / l and LSE
-      const Tile tl = cursor_tile(c, t);
-      const int32_t r_in_seg = tl.m * kFwdUnit + hf * kTileM + row;
+      const int32_t r_in_seg = r_seg;
       const bool row_valid = r_in_seg < c.len;
       const int64_t grow = (int64_t)c.r0 + r_in_seg;
       __nv_bfloat16* orow = p.out + grow * p.o_rs + (int64_t)tl.h * p.o_hs;
@@ -394,7 +416,7 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t gl = g + nkv - 1;
       if (!mbar_wait(&bar.pv_done[hf], gl & 1, abort)) break;
       tc_fence_after();
-      const float inv_l = 1.f / l;
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;  // l = 0: the row saw no key (causal): O = 0
 #pragma unroll
       for (int d0 = 0; d0 < D; d0 += 32) {
         uint32_t o[32];
@@ -410,7 +432,7 @@ __global__ void __launch_bounds__(384, 1)
           for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
         }
       }
-      if (row_valid) *lse_out = (m_use + __log2f(l)) * 0.69314718055994531f;
+      if (row_valid) *lse_out = l > 0.f ? (m_use + __log2f(l)) * 0.69314718055994531f : -INFINITY;
       tc_fence_before();
       g += nkv;
     }
@@ -425,10 +447,10 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0 && bar.abort) record_error(p.err, kErrTimeout);
 }
 
-template <int D>
+template <int D, bool CAUSAL>
 static cudaError_t launch_fwd_d(const FwdLaunch& L, cudaStream_t stream) {
   using C = FwdCfg<D>;
-  auto kern = varlen_fwd_kernel<D>;
+  auto kern = varlen_fwd_kernel<D, CAUSAL>;
   // The warpgroup register split assumes the compiled per-thread count;
   // refuse to launch a build that came out differently.
   cudaFuncAttributes fa;
@@ -443,9 +465,9 @@ static cudaError_t launch_fwd_d(const FwdLaunch& L, cudaStream_t stream) {
 
 cudaError_t launch_fwd(const FwdLaunch& L, cudaStream_t stream) {
   switch (L.head_dim) {
-    case 64: return launch_fwd_d<64>(L, stream);
-    case 96: return launch_fwd_d<96>(L, stream);
-    case 128: return launch_fwd_d<128>(L, stream);
+    case 64: return L.p.causal ? launch_fwd_d<64, true>(L, stream) : launch_fwd_d<64, false>(L, stream);
+    case 96: return L.p.causal ? launch_fwd_d<96, true>(L, stream) : launch_fwd_d<96, false>(L, stream);
+    case 128: return L.p.causal ? launch_fwd_d<128, true>(L, stream) : launch_fwd_d<128, false>(L, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -27,6 +27,7 @@ struct FwdParams {
   const int32_t* cu_q;
   const int32_t* cu_k;
   int32_t batch, total_q, total_k, num_heads;
+  int32_t causal;    // 1: q row i of a segment sees keys j <= i + Sk - Sq
   float scale_log2;  // softmax scale * log2(e)
   unsigned int* err; // device error word
 };
@@ -65,6 +66,7 @@ struct BwdParams {
   const int32_t* cu_q;
   const int32_t* cu_k;
   int32_t batch, total_q, total_k, num_heads;
+  int32_t causal;    // 1: q row i of a segment sees keys j <= i + Sk - Sq
   int64_t pad_rows;
   float scale_log2;  // softmax scale * log2(e)
   float scale;       // softmax scale (applied to dK)

@@ -61,6 +61,10 @@ def _load() -> ctypes.CDLL:
     lib.varlen_attn_bwd.restype = ctypes.c_int
     lib.varlen_attn_bwd.argtypes = [vp, S, vp, S, vp, S, vp, S, vp, S, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                     i32, f32, vp, S, vp, S, vp, S, vp, sz, vp]
+    lib.varlen_attn_fwd_causal.restype = ctypes.c_int
+    lib.varlen_attn_fwd_causal.argtypes = lib.varlen_attn_fwd.argtypes
+    lib.varlen_attn_bwd_causal.restype = ctypes.c_int
+    lib.varlen_attn_bwd_causal.argtypes = lib.varlen_attn_bwd.argtypes
     lib.varlen_attn_bwd_noalloc.restype = ctypes.c_int
     lib.varlen_attn_bwd_noalloc.argtypes = [vp, S, vp, S, vp, S, vp, S, vp, S, vp, vp, vp, i32, i32, i32, i32, i32,
                                             i32, i32, f32, vp, S, vp, S, vp, S, vp]
@@ -89,7 +93,8 @@ LIB_PATH = LIB._name
 EXPORTED = ("varlen_attn_fwd", "varlen_attn_bwd_workspace_size", "varlen_attn_bwd",
             "varlen_attn_get_device_status", "varlen_attn_status_string", "varlen_attn_tile_count",
             "varlen_attn_debug_schedule", "varlen_attn_selftest_wait_timeout", "varlen_attn_num_sms",
-            "varlen_attn_debug_set_phase_events", "varlen_attn_bwd_noalloc", "varlen_attn_last_cuda_error")
+            "varlen_attn_debug_set_phase_events", "varlen_attn_bwd_noalloc", "varlen_attn_last_cuda_error",
+            "varlen_attn_fwd_causal", "varlen_attn_bwd_causal")
 
 # Size of the fixed device array varlen_attn_bwd_noalloc uses as scratch.
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -120,11 +125,17 @@ def _stream(stream):
 # ---------------------------------------------------------------- raw ABI
 
 def varlen_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads, head_dim,
-                    max_seqlen_q, max_seqlen_k, scale, out, lse, stream=None) -> int:
-    return LIB.varlen_attn_fwd(_ptr(q), _stride(q), _ptr(k), _stride(k), _ptr(v), _stride(v),
-                               _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), batch, total_q, total_k, num_heads,
-                               head_dim, max_seqlen_q, max_seqlen_k, scale, _ptr(out), _stride(out), _ptr(lse),
-                               _stream(stream))
+                    max_seqlen_q, max_seqlen_k, scale, out, lse, stream=None, causal=False) -> int:
+    fn = LIB.varlen_attn_fwd_causal if causal else LIB.varlen_attn_fwd
+    return fn(_ptr(q), _stride(q), _ptr(k), _stride(k), _ptr(v), _stride(v), _ptr(cu_seqlens_q),
+              _ptr(cu_seqlens_k), batch, total_q, total_k, num_heads, head_dim, max_seqlen_q, max_seqlen_k, scale,
+              _ptr(out), _stride(out), _ptr(lse), _stream(stream))
+
+
+def varlen_attn_fwd_causal(q, k, v, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads, head_dim,
+                           max_seqlen_q, max_seqlen_k, scale, out, lse, stream=None) -> int:
+    return varlen_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads, head_dim,
+                           max_seqlen_q, max_seqlen_k, scale, out, lse, stream, causal=True)
 
 
 def varlen_attn_bwd_workspace_size(batch, total_q, num_heads, head_dim) -> int:
@@ -133,12 +144,20 @@ def varlen_attn_bwd_workspace_size(batch, total_q, num_heads, head_dim) -> int:
 
 def varlen_attn_bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads,
                     head_dim, max_seqlen_q, max_seqlen_k, scale, dq, dk, dv, workspace, workspace_bytes,
-                    stream=None) -> int:
-    return LIB.varlen_attn_bwd(_ptr(q), _stride(q), _ptr(k), _stride(k), _ptr(v), _stride(v), _ptr(out),
-                               _stride(out), _ptr(dout), _stride(dout), _ptr(lse), _ptr(cu_seqlens_q),
-                               _ptr(cu_seqlens_k), batch, total_q, total_k, num_heads, head_dim, max_seqlen_q,
-                               max_seqlen_k, scale, _ptr(dq), _stride(dq), _ptr(dk), _stride(dk), _ptr(dv),
-                               _stride(dv), _ptr(workspace), workspace_bytes, _stream(stream))
+                    stream=None, causal=False) -> int:
+    fn = LIB.varlen_attn_bwd_causal if causal else LIB.varlen_attn_bwd
+    return fn(_ptr(q), _stride(q), _ptr(k), _stride(k), _ptr(v), _stride(v), _ptr(out), _stride(out), _ptr(dout),
+              _stride(dout), _ptr(lse), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), batch, total_q, total_k, num_heads,
+              head_dim, max_seqlen_q, max_seqlen_k, scale, _ptr(dq), _stride(dq), _ptr(dk), _stride(dk), _ptr(dv),
+              _stride(dv), _ptr(workspace), workspace_bytes, _stream(stream))
+
+
+def varlen_attn_bwd_causal(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k,
+                           num_heads, head_dim, max_seqlen_q, max_seqlen_k, scale, dq, dk, dv, workspace,
+                           workspace_bytes, stream=None) -> int:
+    return varlen_attn_bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k,
+                           num_heads, head_dim, max_seqlen_q, max_seqlen_k, scale, dq, dk, dv, workspace,
+                           workspace_bytes, stream, causal=True)
 
 
 def varlen_attn_bwd_noalloc(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k,
@@ -207,8 +226,9 @@ def _check(status, where):
 
 
 def attention_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q=0, max_seqlen_k=0, scale=None,
-                  out=None, lse=None, stream=None):
-    """O and LSE for packed q/k/v ([rows, H, D] bf16 on one CUDA device)."""
+                  out=None, lse=None, stream=None, causal=False):
+    """O and LSE for packed q/k/v ([rows, H, D] bf16 on one CUDA device);
+    `causal` selects varlen_attn_fwd_causal."""
     total_q, H, D = q.shape
     total_k = k.shape[0]
     batch = cu_seqlens_q.numel() - 1
@@ -218,12 +238,12 @@ def attention_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q=0, max_seqle
     if lse is None:
         lse = torch.empty(H, total_q, dtype=torch.float32, device=q.device)
     _check(varlen_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, H, D, max_seqlen_q,
-                           max_seqlen_k, scale, out, lse, stream), "varlen_attn_fwd")
+                           max_seqlen_k, scale, out, lse, stream, causal), "varlen_attn_fwd")
     return out, lse
 
 
 def attention_bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q=0, max_seqlen_k=0,
-                  scale=None, dq=None, dk=None, dv=None, workspace=None, stream=None):
+                  scale=None, dq=None, dk=None, dv=None, workspace=None, stream=None, causal=False):
     """dQ, dK, dV for the forward above (every operand keeps its strides)."""
     total_q, H, D = q.shape
     total_k = k.shape[0]
@@ -236,6 +256,6 @@ def attention_bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, max_seqle
     if workspace is None:
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
     _check(varlen_attn_bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, H, D,
-                           max_seqlen_q, max_seqlen_k, scale, dq, dk, dv, workspace, workspace.numel(), stream),
-           "varlen_attn_bwd")
+                           max_seqlen_q, max_seqlen_k, scale, dq, dk, dv, workspace, workspace.numel(), stream,
+                           causal), "varlen_attn_bwd")
     return dq, dk, dv

@@ -94,13 +94,25 @@ class Workload:
         """sum_b Sq_b * Sk_b (per head)."""
         return sum(a * b for a, b in zip(self.seqlens_q(), self.seqlens_k()))
 
-    def fwd_flops(self) -> float:
-        """4 * sum_b Sq_b Sk_b * H * D: two matmuls of 2 flops per MAC."""
-        return 4.0 * self.pair_products() * self.num_heads * self.head_dim
+    def visible_pairs(self, causal: bool = False) -> int:
+        """(query, key) pairs that take part, per head: sum_b Sq_b * Sk_b, or
+        with the causal mask (q row i of a segment sees keys
+        j <= i + Sk - Sq) sum_b sum_i clamp(i + Sk_b - Sq_b + 1, 0, Sk_b)."""
+        if not causal:
+            return self.pair_products()
+        tot = 0
+        for sq, sk in zip(self.seqlens_q(), self.seqlens_k()):
+            if sq > 0 and sk > 0:
+                tot += int(np.clip(np.arange(sq, dtype=np.int64) + (sk - sq) + 1, 0, sk).sum())
+        return tot
 
-    def bwd_flops(self) -> float:
+    def fwd_flops(self, causal: bool = False) -> float:
+        """4 * (visible pairs) * H * D: two matmuls of 2 flops per MAC."""
+        return 4.0 * self.visible_pairs(causal) * self.num_heads * self.head_dim
+
+    def bwd_flops(self, causal: bool = False) -> float:
         """2.5 x the forward count (five matmuls instead of two)."""
-        return 2.5 * self.fwd_flops()
+        return 2.5 * self.fwd_flops(causal)
 
     def q_tiles(self, tile: int = TILE_ROWS) -> int:
         """Exact tile count H * sum_b ceil(Sq_b / tile)."""
