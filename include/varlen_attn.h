@@ -141,6 +141,40 @@ int varlen_attn_bwd_causal(const void* q, varlen_stride sq, const void* k, varle
                            varlen_stride sdv, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Dense batched attention: q, out, dout, dq are [batch, seqlen_q, H, D] and
+ * k, v, dk, dv are [batch, seqlen_k, H, D] (bf16), each with its own strides
+ * in elements and a unit innermost stride; lse is [H, batch * seqlen_q]
+ * fp32.  The pages' caller uses both this form and the packed one ("[FA4]
+ * [SM120] flash_attn_varlen_func ... illegal memory access at >=4 varlen
+ * segments", "Bug 2 details").  The result is that of the varlen call with
+ * cu_seqlens = {0, S, 2S, ...}; the segment bounds are computed on the
+ * device, never stored, so nothing is allocated.  Requires the batch stride
+ * to be seqlen row strides (the tensor is then the packed
+ * [batch * seqlen, H, D] layout; VARLEN_ERR_STRIDE otherwise) and
+ * batch * seqlen < 2^31 (VARLEN_ERR_SHAPE).  `causal` is 0 or 1, with the
+ * mask of varlen_attn_fwd_causal.
+ */
+typedef struct {
+  int64_t batch;
+  int64_t row;
+  int64_t head;
+} varlen_dense_stride;
+
+int varlen_attn_fwd_dense(const void* q, varlen_dense_stride sq, const void* k, varlen_dense_stride sk,
+                          const void* v, varlen_dense_stride sv, int32_t batch, int32_t seqlen_q, int32_t seqlen_k,
+                          int32_t num_heads, int32_t head_dim, float scale, int32_t causal, void* out,
+                          varlen_dense_stride so, float* lse, void* stream);
+/* Workspace of varlen_attn_bwd_dense: that of the packed call (0 if
+ * batch * seqlen_q overflows int32 or an argument is negative). */
+size_t varlen_attn_bwd_dense_workspace_size(int32_t batch, int32_t seqlen_q, int32_t num_heads, int32_t head_dim);
+int varlen_attn_bwd_dense(const void* q, varlen_dense_stride sq, const void* k, varlen_dense_stride sk,
+                          const void* v, varlen_dense_stride sv, const void* out, varlen_dense_stride so,
+                          const void* dout, varlen_dense_stride sdo, const float* lse, int32_t batch,
+                          int32_t seqlen_q, int32_t seqlen_k, int32_t num_heads, int32_t head_dim, float scale,
+                          int32_t causal, void* dq, varlen_dense_stride sdq, void* dk, varlen_dense_stride sdk,
+                          void* dv, varlen_dense_stride sdv, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Backward without a workspace argument, for callers that cannot allocate
  * device memory (code inside a host framework that owns every device
  * allocation, or on a path where cudaMalloc is not allowed).  The paper has

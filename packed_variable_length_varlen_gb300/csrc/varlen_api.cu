@@ -13,6 +13,8 @@
 //     _bwd_preprocess", sections "Root cause" and "User-side workaround").
 #include <cmath>
 #include <cstring>
+#include <climits>
+#include <cstdint>
 #include <mutex>
 
 #include "varlen_attn.h"
@@ -126,9 +128,7 @@ int encode_dq_acc(CUtensorMap* map, float* base, int64_t rows, int32_t H, int32_
   return r == CUDA_SUCCESS ? VARLEN_OK : VARLEN_ERR_STRIDE;
 }
 
-int check_common(const int32_t* cu_q, const int32_t* cu_k, int32_t batch, int32_t total_q, int32_t total_k,
-                 int32_t H, int32_t D, float scale) {
-  if (cu_q == nullptr || cu_k == nullptr) return VARLEN_ERR_NULL;
+int check_common(int32_t batch, int32_t total_q, int32_t total_k, int32_t H, int32_t D, float scale) {
   if (batch < 1 || total_q < 0 || total_k < 0 || H < 1) return VARLEN_ERR_SHAPE;
   if (D != 64 && D != 96 && D != 128) return VARLEN_ERR_HEAD_DIM;
   if (!(scale > 0.f) || !std::isfinite(scale)) return VARLEN_ERR_SHAPE;
@@ -160,12 +160,12 @@ using namespace varlen;
 namespace {
 
 int fwd_impl(const void* q, varlen_stride sq, const void* k, varlen_stride sk, const void* v, varlen_stride sv,
-             const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t batch, int32_t total_q,
-             int32_t total_k, int32_t num_heads, int32_t head_dim, int32_t max_seqlen_q, int32_t max_seqlen_k,
-             float scale, void* out, varlen_stride so, float* lse, void* stream, int32_t causal) {
+             CuView cu_q, CuView cu_k, int32_t batch, int32_t total_q, int32_t total_k, int32_t num_heads,
+             int32_t head_dim, int32_t max_seqlen_q, int32_t max_seqlen_k, float scale, void* out,
+             varlen_stride so, float* lse, void* stream, int32_t causal) {
   (void)max_seqlen_q;  // advisory only: the kernels derive lengths from cu_seqlens
   (void)max_seqlen_k;
-  int st = check_common(cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads, head_dim, scale);
+  int st = check_common(batch, total_q, total_k, num_heads, head_dim, scale);
   if (st != VARLEN_OK) return st;
   if ((st = check_operand(q, sq, total_q, num_heads, head_dim)) != VARLEN_OK) return st;
   if ((st = check_operand(k, sk, total_k, num_heads, head_dim)) != VARLEN_OK) return st;
@@ -184,8 +184,8 @@ int fwd_impl(const void* q, varlen_stride sq, const void* k, varlen_stride sk, c
   L.p.o_rs = so.row;
   L.p.o_hs = so.head;
   L.p.lse = lse;
-  L.p.cu_q = cu_seqlens_q;
-  L.p.cu_k = cu_seqlens_k;
+  L.p.cu_q = cu_q;
+  L.p.cu_k = cu_k;
   L.p.batch = batch;
   L.p.total_q = total_q;
   L.p.total_k = total_k;
@@ -206,8 +206,9 @@ extern "C" int varlen_attn_fwd(const void* q, varlen_stride sq, const void* k, v
                                int32_t batch, int32_t total_q, int32_t total_k, int32_t num_heads, int32_t head_dim,
                                int32_t max_seqlen_q, int32_t max_seqlen_k, float scale, void* out,
                                varlen_stride so, float* lse, void* stream) {
-  return fwd_impl(q, sq, k, sk, v, sv, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads, head_dim,
-                  max_seqlen_q, max_seqlen_k, scale, out, so, lse, stream, 0);
+  if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr) return VARLEN_ERR_NULL;
+  return fwd_impl(q, sq, k, sk, v, sv, CuView{cu_seqlens_q, 0}, CuView{cu_seqlens_k, 0}, batch, total_q, total_k,
+                  num_heads, head_dim, max_seqlen_q, max_seqlen_k, scale, out, so, lse, stream, 0);
 }
 
 extern "C" int varlen_attn_fwd_causal(const void* q, varlen_stride sq, const void* k, varlen_stride sk,
@@ -216,8 +217,9 @@ extern "C" int varlen_attn_fwd_causal(const void* q, varlen_stride sq, const voi
                                       int32_t num_heads, int32_t head_dim, int32_t max_seqlen_q,
                                       int32_t max_seqlen_k, float scale, void* out, varlen_stride so, float* lse,
                                       void* stream) {
-  return fwd_impl(q, sq, k, sk, v, sv, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads, head_dim,
-                  max_seqlen_q, max_seqlen_k, scale, out, so, lse, stream, 1);
+  if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr) return VARLEN_ERR_NULL;
+  return fwd_impl(q, sq, k, sk, v, sv, CuView{cu_seqlens_q, 0}, CuView{cu_seqlens_k, 0}, batch, total_q, total_k,
+                  num_heads, head_dim, max_seqlen_q, max_seqlen_k, scale, out, so, lse, stream, 1);
 }
 
 extern "C" size_t varlen_attn_bwd_workspace_size(int32_t batch, int32_t total_q, int32_t num_heads,
@@ -232,13 +234,13 @@ namespace {
 
 int bwd_impl(const void* q, varlen_stride sq, const void* k, varlen_stride sk, const void* v, varlen_stride sv,
              const void* out, varlen_stride so, const void* dout, varlen_stride sdo, const float* lse,
-             const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t batch, int32_t total_q,
-             int32_t total_k, int32_t num_heads, int32_t head_dim, int32_t max_seqlen_q, int32_t max_seqlen_k,
-             float scale, void* dq, varlen_stride sdq, void* dk, varlen_stride sdk, void* dv, varlen_stride sdv,
-             void* workspace, size_t workspace_bytes, void* stream, int32_t causal) {
+             CuView cu_q, CuView cu_k, int32_t batch, int32_t total_q, int32_t total_k, int32_t num_heads,
+             int32_t head_dim, int32_t max_seqlen_q, int32_t max_seqlen_k, float scale, void* dq, varlen_stride sdq,
+             void* dk, varlen_stride sdk, void* dv, varlen_stride sdv, void* workspace, size_t workspace_bytes,
+             void* stream, int32_t causal) {
   (void)max_seqlen_q;
   (void)max_seqlen_k;
-  int st = check_common(cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads, head_dim, scale);
+  int st = check_common(batch, total_q, total_k, num_heads, head_dim, scale);
   if (st != VARLEN_OK) return st;
   if ((st = check_operand(q, sq, total_q, num_heads, head_dim)) != VARLEN_OK) return st;
   if ((st = check_operand(k, sk, total_k, num_heads, head_dim)) != VARLEN_OK) return st;
@@ -271,7 +273,7 @@ int bwd_impl(const void* q, varlen_stride sq, const void* k, varlen_stride sk, c
   if ((st = encode_dq_acc(&L.tm_dq, dq_acc, total_q, num_heads, head_dim)) != VARLEN_OK) return st;
   L.prep = PrepParams{static_cast<const __nv_bfloat16*>(out), so.row, so.head,
                       static_cast<const __nv_bfloat16*>(dout), sdo.row, sdo.head,
-                      lse, delta, lse2, dq_acc, cu_seqlens_q, batch, total_q, num_heads, head_dim, pad_rows};
+                      lse, delta, lse2, dq_acc, cu_q, batch, total_q, num_heads, head_dim, pad_rows};
   L.p.dk = static_cast<__nv_bfloat16*>(dk);
   L.p.dk_rs = sdk.row;
   L.p.dk_hs = sdk.head;
@@ -281,8 +283,8 @@ int bwd_impl(const void* q, varlen_stride sq, const void* k, varlen_stride sk, c
   L.p.delta = delta;
   L.p.lse2 = lse2;
   L.p.dq_acc = dq_acc;
-  L.p.cu_q = cu_seqlens_q;
-  L.p.cu_k = cu_seqlens_k;
+  L.p.cu_q = cu_q;
+  L.p.cu_k = cu_k;
   L.p.batch = batch;
   L.p.total_q = total_q;
   L.p.total_k = total_k;
@@ -292,7 +294,7 @@ int bwd_impl(const void* q, varlen_stride sq, const void* k, varlen_stride sk, c
   L.p.scale_log2 = scale * kLog2e;
   L.p.scale = scale;
   L.p.err = dev.err;
-  L.post = PostParams{dq_acc, static_cast<__nv_bfloat16*>(dq), sdq.row, sdq.head, cu_seqlens_q, batch,
+  L.post = PostParams{dq_acc, static_cast<__nv_bfloat16*>(dq), sdq.row, sdq.head, cu_q, batch,
                       total_q, num_heads, head_dim, scale};
   L.head_dim = head_dim;
   L.grid = dev.sms;
@@ -313,9 +315,10 @@ extern "C" int varlen_attn_bwd(const void* q, varlen_stride sq, const void* k, v
                                int32_t num_heads, int32_t head_dim, int32_t max_seqlen_q, int32_t max_seqlen_k,
                                float scale, void* dq, varlen_stride sdq, void* dk, varlen_stride sdk, void* dv,
                                varlen_stride sdv, void* workspace, size_t workspace_bytes, void* stream) {
-  return bwd_impl(q, sq, k, sk, v, sv, out, so, dout, sdo, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k,
-                  num_heads, head_dim, max_seqlen_q, max_seqlen_k, scale, dq, sdq, dk, sdk, dv, sdv, workspace,
-                  workspace_bytes, stream, 0);
+  if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr) return VARLEN_ERR_NULL;
+  return bwd_impl(q, sq, k, sk, v, sv, out, so, dout, sdo, lse, CuView{cu_seqlens_q, 0}, CuView{cu_seqlens_k, 0},
+                  batch, total_q, total_k, num_heads, head_dim, max_seqlen_q, max_seqlen_k, scale, dq, sdq, dk, sdk,
+                  dv, sdv, workspace, workspace_bytes, stream, 0);
 }
 
 extern "C" int varlen_attn_bwd_causal(const void* q, varlen_stride sq, const void* k, varlen_stride sk,
@@ -326,9 +329,83 @@ extern "C" int varlen_attn_bwd_causal(const void* q, varlen_stride sq, const voi
                                       int32_t max_seqlen_q, int32_t max_seqlen_k, float scale, void* dq,
                                       varlen_stride sdq, void* dk, varlen_stride sdk, void* dv, varlen_stride sdv,
                                       void* workspace, size_t workspace_bytes, void* stream) {
-  return bwd_impl(q, sq, k, sk, v, sv, out, so, dout, sdo, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k,
-                  num_heads, head_dim, max_seqlen_q, max_seqlen_k, scale, dq, sdq, dk, sdk, dv, sdv, workspace,
-                  workspace_bytes, stream, 1);
+  if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr) return VARLEN_ERR_NULL;
+  return bwd_impl(q, sq, k, sk, v, sv, out, so, dout, sdo, lse, CuView{cu_seqlens_q, 0}, CuView{cu_seqlens_k, 0},
+                  batch, total_q, total_k, num_heads, head_dim, max_seqlen_q, max_seqlen_k, scale, dq, sdq, dk, sdk,
+                  dv, sdv, workspace, workspace_bytes, stream, 1);
+}
+
+// ------------------------------------------------------------ dense batched
+
+namespace {
+
+// The dense layout [batch, seqlen, H, D] is the packed [batch * seqlen, H, D]
+// layout when the batch stride is seqlen row strides (checked here), so the
+// varlen kernels run it unchanged with uniform segments b * seqlen.
+int dense_view(varlen_dense_stride s, int32_t seqlen, int32_t batch, varlen_stride* out) {
+  if (batch > 1 && s.batch != (int64_t)seqlen * s.row) return VARLEN_ERR_STRIDE;
+  *out = varlen_stride{s.row, s.head};
+  return VARLEN_OK;
+}
+
+int dense_shape(int32_t batch, int32_t seqlen_q, int32_t seqlen_k, int32_t causal, int32_t* total_q,
+                int32_t* total_k) {
+  if (batch < 1 || seqlen_q < 0 || seqlen_k < 0 || (causal != 0 && causal != 1)) return VARLEN_ERR_SHAPE;
+  const int64_t tq = (int64_t)batch * seqlen_q, tk = (int64_t)batch * seqlen_k;
+  if (tq > INT32_MAX || tk > INT32_MAX) return VARLEN_ERR_SHAPE;
+  *total_q = (int32_t)tq;
+  *total_k = (int32_t)tk;
+  return VARLEN_OK;
+}
+
+}  // namespace
+
+extern "C" int varlen_attn_fwd_dense(const void* q, varlen_dense_stride sq, const void* k, varlen_dense_stride sk,
+                                     const void* v, varlen_dense_stride sv, int32_t batch, int32_t seqlen_q,
+                                     int32_t seqlen_k, int32_t num_heads, int32_t head_dim, float scale,
+                                     int32_t causal, void* out, varlen_dense_stride so, float* lse, void* stream) {
+  int32_t total_q = 0, total_k = 0;
+  int st = dense_shape(batch, seqlen_q, seqlen_k, causal, &total_q, &total_k);
+  if (st != VARLEN_OK) return st;
+  varlen_stride vq, vk, vv, vo;
+  if ((st = dense_view(sq, seqlen_q, batch, &vq)) != VARLEN_OK) return st;
+  if ((st = dense_view(sk, seqlen_k, batch, &vk)) != VARLEN_OK) return st;
+  if ((st = dense_view(sv, seqlen_k, batch, &vv)) != VARLEN_OK) return st;
+  if ((st = dense_view(so, seqlen_q, batch, &vo)) != VARLEN_OK) return st;
+  return fwd_impl(q, vq, k, vk, v, vv, CuView{nullptr, seqlen_q}, CuView{nullptr, seqlen_k}, batch, total_q, total_k,
+                  num_heads, head_dim, seqlen_q, seqlen_k, scale, out, vo, lse, stream, causal);
+}
+
+extern "C" size_t varlen_attn_bwd_dense_workspace_size(int32_t batch, int32_t seqlen_q, int32_t num_heads,
+                                                      int32_t head_dim) {
+  if (batch < 0 || seqlen_q < 0) return 0;
+  const int64_t tq = (int64_t)batch * seqlen_q;
+  if (tq > INT32_MAX) return 0;
+  return varlen_attn_bwd_workspace_size(batch, (int32_t)tq, num_heads, head_dim);
+}
+
+extern "C" int varlen_attn_bwd_dense(const void* q, varlen_dense_stride sq, const void* k, varlen_dense_stride sk,
+                                     const void* v, varlen_dense_stride sv, const void* out, varlen_dense_stride so,
+                                     const void* dout, varlen_dense_stride sdo, const float* lse, int32_t batch,
+                                     int32_t seqlen_q, int32_t seqlen_k, int32_t num_heads, int32_t head_dim,
+                                     float scale, int32_t causal, void* dq, varlen_dense_stride sdq, void* dk,
+                                     varlen_dense_stride sdk, void* dv, varlen_dense_stride sdv, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  int32_t total_q = 0, total_k = 0;
+  int st = dense_shape(batch, seqlen_q, seqlen_k, causal, &total_q, &total_k);
+  if (st != VARLEN_OK) return st;
+  varlen_stride vq, vk, vv, vo, vdo, vdq, vdk, vdv;
+  if ((st = dense_view(sq, seqlen_q, batch, &vq)) != VARLEN_OK) return st;
+  if ((st = dense_view(sk, seqlen_k, batch, &vk)) != VARLEN_OK) return st;
+  if ((st = dense_view(sv, seqlen_k, batch, &vv)) != VARLEN_OK) return st;
+  if ((st = dense_view(so, seqlen_q, batch, &vo)) != VARLEN_OK) return st;
+  if ((st = dense_view(sdo, seqlen_q, batch, &vdo)) != VARLEN_OK) return st;
+  if ((st = dense_view(sdq, seqlen_q, batch, &vdq)) != VARLEN_OK) return st;
+  if ((st = dense_view(sdk, seqlen_k, batch, &vdk)) != VARLEN_OK) return st;
+  if ((st = dense_view(sdv, seqlen_k, batch, &vdv)) != VARLEN_OK) return st;
+  return bwd_impl(q, vq, k, vk, v, vv, out, vo, dout, vdo, lse, CuView{nullptr, seqlen_q}, CuView{nullptr, seqlen_k},
+                  batch, total_q, total_k, num_heads, head_dim, seqlen_q, seqlen_k, scale, dq, vdq, dk, vdk, dv, vdv,
+                  workspace, workspace_bytes, stream, causal);
 }
 
 extern "C" int varlen_attn_get_device_status(void* stream) {

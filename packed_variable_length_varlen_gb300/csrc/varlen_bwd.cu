@@ -55,8 +55,8 @@ __device__ __forceinline__ int64_t pad_base(int32_t o0, int32_t b) {
 
 __global__ void __launch_bounds__(256) varlen_bwd_prep_kernel(const PrepParams p) {
   const int32_t B = p.batch;
-  const int32_t lo = clamp_row(__ldg(p.cu_q), p.total_q);
-  const int32_t hi = clamp_row(__ldg(p.cu_q + B), p.total_q);
+  const int32_t lo = clamp_row(cu_at(p.cu_q, 0), p.total_q);
+  const int32_t hi = clamp_row(cu_at(p.cu_q, B), p.total_q);
   if (hi <= lo) return;
   const int H = p.num_heads, D = p.head_dim;
   const int64_t n = (int64_t)(hi - lo) * H;
@@ -85,11 +85,11 @@ __global__ void __launch_bounds__(256) varlen_bwd_prep_kernel(const PrepParams p
     int32_t b0 = 0, b1 = B - 1;
     while (b0 < b1) {
       const int32_t mid = (b0 + b1 + 1) >> 1;
-      if (clamp_row(__ldg(p.cu_q + mid), p.total_q) <= row) b0 = mid;
+      if (clamp_row(cu_at(p.cu_q, mid), p.total_q) <= row) b0 = mid;
       else b1 = mid - 1;
     }
-    const int32_t o0 = clamp_row(__ldg(p.cu_q + b0), p.total_q);
-    const int32_t e = clamp_row(__ldg(p.cu_q + b0 + 1), p.total_q);
+    const int32_t o0 = clamp_row(cu_at(p.cu_q, b0), p.total_q);
+    const int32_t e = clamp_row(cu_at(p.cu_q, b0 + 1), p.total_q);
     if (row >= o0 && row < e) {
       const int64_t idx = (int64_t)h * p.pad_rows + pad_base(o0, b0) + (row - o0);
       p.delta[idx] = acc;
@@ -104,8 +104,8 @@ __global__ void __launch_bounds__(256) varlen_bwd_prep_kernel(const PrepParams p
 
 __global__ void __launch_bounds__(256) varlen_bwd_post_kernel(const PostParams p) {
   const int32_t B = p.batch;
-  const int32_t lo = clamp_row(__ldg(p.cu_q), p.total_q);
-  const int32_t hi = clamp_row(__ldg(p.cu_q + B), p.total_q);
+  const int32_t lo = clamp_row(cu_at(p.cu_q, 0), p.total_q);
+  const int32_t hi = clamp_row(cu_at(p.cu_q, B), p.total_q);
   if (hi <= lo) return;
   const int H = p.num_heads, D = p.head_dim, V = D / 8;
   const int64_t n = (int64_t)(hi - lo) * H * V;

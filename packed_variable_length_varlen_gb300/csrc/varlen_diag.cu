@@ -13,8 +13,9 @@ __global__ void debug_schedule_kernel(const int32_t* cu, int32_t batch, int32_t 
                                       int32_t* out, int64_t max_records) {
   if (threadIdx.x != 0) return;
   SegCursor c;
-  cursor_init<TILE>(c, cu, cu, batch, total, total);
-  for (int64_t t = blockIdx.x; cursor_seek<TILE>(c, t, num_heads, cu, cu, batch, total, total); t += gridDim.x) {
+  const CuView v{cu, 0};
+  cursor_init<TILE>(c, v, v, batch, total, total);
+  for (int64_t t = blockIdx.x; cursor_seek<TILE>(c, t, num_heads, v, v, batch, total, total); t += gridDim.x) {
     const Tile tl = cursor_tile(c, t);
     if (t < max_records) {
       int4 rec = make_int4(tl.b, tl.m, tl.h, (int)blockIdx.x);

@@ -16,6 +16,14 @@ enum : unsigned int {
   kErrBounds = 2u,   // a debug bounds check failed
 };
 
+// Where a launch finds its segment bounds: cu_seqlens in device memory
+// (`ptr`), or, when ptr is null, uniform segments of `uni` rows each (the
+// bounds b * uni of the dense batched entry points, never stored).
+struct CuView {
+  const int32_t* ptr;
+  int32_t uni;
+};
+
 constexpr int kTileM = 128;  // q rows per forward tile / kv rows per backward tile
 constexpr int kTileN = 128;  // kv rows per forward inner step
 constexpr int kBwdTileQ = 128; // q rows per backward inner step
@@ -24,8 +32,8 @@ struct FwdParams {
   __nv_bfloat16* out;
   int64_t o_rs, o_hs;
   float* lse;
-  const int32_t* cu_q;
-  const int32_t* cu_k;
+  CuView cu_q;
+  CuView cu_k;
   int32_t batch, total_q, total_k, num_heads;
   int32_t causal;    // 1: q row i of a segment sees keys j <= i + Sk - Sq
   float scale_log2;  // softmax scale * log2(e)
@@ -50,7 +58,7 @@ struct PrepParams {
   float* delta;     // [H, pad_rows], segment-padded (see bwd_pad_rows)
   float* lse2;      // [H, pad_rows], segment-padded
   float* dq_acc;    // [total_q, H, D]
-  const int32_t* cu_q;
+  CuView cu_q;
   int32_t batch, total_q, num_heads, head_dim;
   int64_t pad_rows;
 };
@@ -63,8 +71,8 @@ struct BwdParams {
   const float* delta;  // [H, pad_rows]
   const float* lse2;   // [H, pad_rows]
   float* dq_acc;
-  const int32_t* cu_q;
-  const int32_t* cu_k;
+  CuView cu_q;
+  CuView cu_k;
   int32_t batch, total_q, total_k, num_heads;
   int32_t causal;    // 1: q row i of a segment sees keys j <= i + Sk - Sq
   int64_t pad_rows;
@@ -77,7 +85,7 @@ struct PostParams {
   const float* dq_acc;
   __nv_bfloat16* dq;
   int64_t dq_rs, dq_hs;
-  const int32_t* cu_q;
+  CuView cu_q;
   int32_t batch, total_q, num_heads, head_dim;
   float scale;
 };

@@ -21,6 +21,8 @@
 
 #include <cstdint>
 
+#include "varlen_internal.h"
+
 namespace varlen {
 
 struct SegCursor {
@@ -33,22 +35,29 @@ struct SegCursor {
 
 __device__ __forceinline__ int32_t clamp_row(int32_t v, int32_t total) { return min(max(v, 0), total); }
 
+// Segment bound b of a view: cu_seqlens[b], or b * uni for uniform segments.
+// For uniform segments b <= batch and batch * uni <= total < 2^31, so the
+// product does not overflow.
+__device__ __forceinline__ int32_t cu_at(const CuView& cu, int32_t b) {
+  return cu.ptr != nullptr ? __ldg(cu.ptr + b) : b * cu.uni;
+}
+
 template <int TILE>
-__device__ __forceinline__ void cursor_load(SegCursor& c, const int32_t* __restrict__ cu_s,
-                                            const int32_t* __restrict__ cu_o, int32_t total_s, int32_t total_o) {
-  const int32_t a = clamp_row(__ldg(cu_s + c.b), total_s);
-  const int32_t e = clamp_row(__ldg(cu_s + c.b + 1), total_s);
+__device__ __forceinline__ void cursor_load(SegCursor& c, const CuView& cu_s, const CuView& cu_o, int32_t total_s,
+                                            int32_t total_o) {
+  const int32_t a = clamp_row(cu_at(cu_s, c.b), total_s);
+  const int32_t e = clamp_row(cu_at(cu_s, c.b + 1), total_s);
   c.r0 = a;
   c.len = max(e - a, 0);
-  const int32_t ao = clamp_row(__ldg(cu_o + c.b), total_o);
-  const int32_t eo = clamp_row(__ldg(cu_o + c.b + 1), total_o);
+  const int32_t ao = clamp_row(cu_at(cu_o, c.b), total_o);
+  const int32_t eo = clamp_row(cu_at(cu_o, c.b + 1), total_o);
   c.o0 = ao;
   c.olen = max(eo - ao, 0);
   c.nb = (c.len + TILE - 1) / TILE;
 }
 
 template <int TILE>
-__device__ __forceinline__ void cursor_init(SegCursor& c, const int32_t* cu_s, const int32_t* cu_o, int32_t batch,
+__device__ __forceinline__ void cursor_init(SegCursor& c, const CuView& cu_s, const CuView& cu_o, int32_t batch,
                                             int32_t total_s, int32_t total_o) {
   c.b = 0;
   c.first = 0;
@@ -60,8 +69,8 @@ __device__ __forceinline__ void cursor_init(SegCursor& c, const int32_t* cu_s, c
 // Moves the cursor to the segment holding global tile t (t never decreases
 // between calls).  Returns false when t is past the last tile.
 template <int TILE>
-__device__ __forceinline__ bool cursor_seek(SegCursor& c, int64_t t, int32_t num_heads, const int32_t* cu_s,
-                                            const int32_t* cu_o, int32_t batch, int32_t total_s, int32_t total_o) {
+__device__ __forceinline__ bool cursor_seek(SegCursor& c, int64_t t, int32_t num_heads, const CuView& cu_s,
+                                            const CuView& cu_o, int32_t batch, int32_t total_s, int32_t total_o) {
   while (c.b < batch) {
     const int64_t span = (int64_t)num_heads * c.nb;
     if (t < c.first + span) return true;

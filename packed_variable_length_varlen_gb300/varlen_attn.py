@@ -36,6 +36,11 @@ class VarlenStride(ctypes.Structure):
     _fields_ = [("row", ctypes.c_int64), ("head", ctypes.c_int64)]
 
 
+class VarlenDenseStride(ctypes.Structure):
+    """Batch, row and head strides of one [batch, seqlen, H, D] tensor, in elements."""
+    _fields_ = [("batch", ctypes.c_int64), ("row", ctypes.c_int64), ("head", ctypes.c_int64)]
+
+
 class VarlenError(RuntimeError):
     def __init__(self, status: int, where: str):
         msg = "%s failed: %d (%s)" % (where, status, varlen_attn_status_string(status))
@@ -65,6 +70,14 @@ def _load() -> ctypes.CDLL:
     lib.varlen_attn_fwd_causal.argtypes = lib.varlen_attn_fwd.argtypes
     lib.varlen_attn_bwd_causal.restype = ctypes.c_int
     lib.varlen_attn_bwd_causal.argtypes = lib.varlen_attn_bwd.argtypes
+    DS = VarlenDenseStride
+    lib.varlen_attn_fwd_dense.restype = ctypes.c_int
+    lib.varlen_attn_fwd_dense.argtypes = [vp, DS, vp, DS, vp, DS, i32, i32, i32, i32, i32, f32, i32, vp, DS, vp, vp]
+    lib.varlen_attn_bwd_dense_workspace_size.restype = sz
+    lib.varlen_attn_bwd_dense_workspace_size.argtypes = [i32, i32, i32, i32]
+    lib.varlen_attn_bwd_dense.restype = ctypes.c_int
+    lib.varlen_attn_bwd_dense.argtypes = [vp, DS, vp, DS, vp, DS, vp, DS, vp, DS, vp, i32, i32, i32, i32, i32, f32,
+                                          i32, vp, DS, vp, DS, vp, DS, vp, sz, vp]
     lib.varlen_attn_bwd_noalloc.restype = ctypes.c_int
     lib.varlen_attn_bwd_noalloc.argtypes = [vp, S, vp, S, vp, S, vp, S, vp, S, vp, vp, vp, i32, i32, i32, i32, i32,
                                             i32, i32, f32, vp, S, vp, S, vp, S, vp]
@@ -94,7 +107,8 @@ EXPORTED = ("varlen_attn_fwd", "varlen_attn_bwd_workspace_size", "varlen_attn_bw
             "varlen_attn_get_device_status", "varlen_attn_status_string", "varlen_attn_tile_count",
             "varlen_attn_debug_schedule", "varlen_attn_selftest_wait_timeout", "varlen_attn_num_sms",
             "varlen_attn_debug_set_phase_events", "varlen_attn_bwd_noalloc", "varlen_attn_last_cuda_error",
-            "varlen_attn_fwd_causal", "varlen_attn_bwd_causal")
+            "varlen_attn_fwd_causal", "varlen_attn_bwd_causal", "varlen_attn_fwd_dense",
+            "varlen_attn_bwd_dense_workspace_size", "varlen_attn_bwd_dense")
 
 # Size of the fixed device array varlen_attn_bwd_noalloc uses as scratch.
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -112,6 +126,14 @@ def _stride(t) -> VarlenStride:
     if t.dim() != 3 or t.stride(2) != 1:
         raise ValueError("NHD tensors must be [rows, heads, head_dim] with unit innermost stride")
     return VarlenStride(t.stride(0), t.stride(1))
+
+
+def _dstride(t) -> VarlenDenseStride:
+    if t is None:
+        return VarlenDenseStride(0, 0, 0)
+    if t.dim() != 4 or t.stride(3) != 1:
+        raise ValueError("dense tensors must be [batch, seqlen, heads, head_dim] with unit innermost stride")
+    return VarlenDenseStride(t.stride(0), t.stride(1), t.stride(2))
 
 
 def _stream(stream):
@@ -158,6 +180,26 @@ def varlen_attn_bwd_causal(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, 
     return varlen_attn_bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k,
                            num_heads, head_dim, max_seqlen_q, max_seqlen_k, scale, dq, dk, dv, workspace,
                            workspace_bytes, stream, causal=True)
+
+
+def varlen_attn_fwd_dense(q, k, v, batch, seqlen_q, seqlen_k, num_heads, head_dim, scale, causal, out, lse,
+                          stream=None) -> int:
+    return LIB.varlen_attn_fwd_dense(_ptr(q), _dstride(q), _ptr(k), _dstride(k), _ptr(v), _dstride(v), batch,
+                                     seqlen_q, seqlen_k, num_heads, head_dim, scale, int(bool(causal)), _ptr(out),
+                                     _dstride(out), _ptr(lse), _stream(stream))
+
+
+def varlen_attn_bwd_dense_workspace_size(batch, seqlen_q, num_heads, head_dim) -> int:
+    return int(LIB.varlen_attn_bwd_dense_workspace_size(batch, seqlen_q, num_heads, head_dim))
+
+
+def varlen_attn_bwd_dense(q, k, v, out, dout, lse, batch, seqlen_q, seqlen_k, num_heads, head_dim, scale, causal,
+                          dq, dk, dv, workspace, workspace_bytes, stream=None) -> int:
+    return LIB.varlen_attn_bwd_dense(_ptr(q), _dstride(q), _ptr(k), _dstride(k), _ptr(v), _dstride(v), _ptr(out),
+                                     _dstride(out), _ptr(dout), _dstride(dout), _ptr(lse), batch, seqlen_q, seqlen_k,
+                                     num_heads, head_dim, scale, int(bool(causal)), _ptr(dq), _dstride(dq), _ptr(dk),
+                                     _dstride(dk), _ptr(dv), _dstride(dv), _ptr(workspace), workspace_bytes,
+                                     _stream(stream))
 
 
 def varlen_attn_bwd_noalloc(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k,
@@ -258,4 +300,35 @@ def attention_bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, max_seqle
     _check(varlen_attn_bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, H, D,
                            max_seqlen_q, max_seqlen_k, scale, dq, dk, dv, workspace, workspace.numel(), stream,
                            causal), "varlen_attn_bwd")
+    return dq, dk, dv
+
+
+def attention_fwd_dense(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None):
+    """O and LSE for dense batched q [B, Sq, H, D], k / v [B, Sk, H, D] (bf16,
+    one CUDA device); lse is [H, B * Sq]."""
+    B, Sq, H, D = q.shape
+    Sk = k.shape[1]
+    scale = float(D ** -0.5) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q, memory_format=torch.contiguous_format)
+    if lse is None:
+        lse = torch.empty(H, B * Sq, dtype=torch.float32, device=q.device)
+    _check(varlen_attn_fwd_dense(q, k, v, B, Sq, Sk, H, D, scale, causal, out, lse, stream), "varlen_attn_fwd_dense")
+    return out, lse
+
+
+def attention_bwd_dense(q, k, v, out, dout, lse, scale=None, causal=False, dq=None, dk=None, dv=None,
+                        workspace=None, stream=None):
+    """dQ, dK, dV for attention_fwd_dense."""
+    B, Sq, H, D = q.shape
+    Sk = k.shape[1]
+    scale = float(D ** -0.5) if scale is None else float(scale)
+    dq = torch.empty_like(q, memory_format=torch.contiguous_format) if dq is None else dq
+    dk = torch.empty_like(k, memory_format=torch.contiguous_format) if dk is None else dk
+    dv = torch.empty_like(v, memory_format=torch.contiguous_format) if dv is None else dv
+    nbytes = varlen_attn_bwd_dense_workspace_size(B, Sq, H, D)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    _check(varlen_attn_bwd_dense(q, k, v, out, dout, lse, B, Sq, Sk, H, D, scale, causal, dq, dk, dv, workspace,
+                                 workspace.numel(), stream), "varlen_attn_bwd_dense")
     return dq, dk, dv

@@ -133,3 +133,53 @@ def test_int64_offsets_page_value():
     # the library's offsets are int64 products of row index and row stride
     off = np.int64(g["coord"]) * np.int64(g["dout_stride"][0])
     assert int(off) == g["true_offset"] and int(off) != g["off_signed_i32"]
+
+
+class _Fake4:
+    """A [batch, seqlen, H, D] stand-in: data pointer and element strides."""
+
+    def __init__(self, ptr, batch_stride, row, head):
+        self._p, self._s = ptr, (batch_stride, row, head, 1)
+
+    def data_ptr(self):
+        return self._p
+
+    def stride(self, i=None):
+        return self._s if i is None else self._s[i]
+
+    def dim(self):
+        return 4
+
+
+def test_dense_validation_codes(va):
+    """The dense entry points check that each tensor is the packed
+    [batch * seqlen, H, D] layout (batch stride = seqlen row strides) and
+    that batch * seqlen fits int32, before touching a device."""
+    B, Sq, Sk, H, D = 3, 10, 12, 2, 64
+    good_q = _Fake4(0x1000, Sq * H * D, H * D, D)
+    good_k = _Fake4(0x1000, Sk * H * D, H * D, D)
+
+    class _P:
+        def __init__(self, p):
+            self._p = p
+
+        def data_ptr(self):
+            return self._p
+
+    def fwd(q=good_q, k=good_k, B=B, Sq=Sq, Sk=Sk, causal=0):
+        return va.varlen_attn_fwd_dense(q, k, k, B, Sq, Sk, H, D, 0.125, causal, q, _P(0x3000), 0)
+
+    assert fwd(q=_Fake4(0x1000, Sq * H * D + 8, H * D, D)) == va.VARLEN_ERR_STRIDE
+    assert fwd(k=_Fake4(0x1000, Sq * H * D, H * D, D)) == va.VARLEN_ERR_STRIDE   # k uses seqlen_k
+    assert fwd(B=2 ** 16, Sq=2 ** 16) == va.VARLEN_ERR_SHAPE                        # 2^32 rows
+    # the Python wrapper passes bool(causal); a C caller's causal must be 0 or 1
+    ds = va.VarlenDenseStride(Sq * H * D, H * D, D)
+    dk = va.VarlenDenseStride(Sk * H * D, H * D, D)
+    assert va.LIB.varlen_attn_fwd_dense(0x1000, ds, 0x1000, dk, 0x1000, dk, B, Sq, Sk, H, D, 0.125, 2, 0x1000, ds,
+                                        0x3000, None) == va.VARLEN_ERR_SHAPE
+    assert fwd(B=0) == va.VARLEN_ERR_SHAPE
+    # one batch: the batch stride is never used, so it is not checked
+    assert fwd(q=_Fake4(0x1000, 7, H * D, D), B=1) in (va.VARLEN_ERR_CUDA, va.VARLEN_ERR_ARCH)
+    assert fwd() in (va.VARLEN_ERR_CUDA, va.VARLEN_ERR_ARCH)
+    assert va.varlen_attn_bwd_dense_workspace_size(B, Sq, H, D) == va.varlen_attn_bwd_workspace_size(B, B * Sq, H, D)
+    assert va.varlen_attn_bwd_dense_workspace_size(2 ** 16, 2 ** 16, H, D) == 0
