@@ -39,7 +39,7 @@ from packed_variable_length_varlen_gb300 import sharding
 from packed_variable_length_varlen_gb300 import workloads as W
 
 METRIC = "varlen attention TFLOP/s (fwd, bwd) bf16 H=56 D=128; % of GB300 bf16 TC peak"
-BWD_MAIN_DRAM_BYTES_PER_HEAD = {("windowed", 128): (872.579840e6 + 671.620352e6) / 8}
+BWD_MAIN_DRAM_BYTES_PER_HEAD = {("windowed", 128): (872.408576e6 + 672.020736e6) / 8}
 
 
 def _metric(args) -> str:
@@ -219,22 +219,47 @@ def ours(args, w, ws, rank, local):
     scale = w.softmax_scale
     stream = torch.cuda.current_stream(dev)
 
-    def fwd():
-        st = va.varlen_attn_fwd(d.q, d.k, d.v, d.cu_q, d.cu_k, w.batch, w.total_q, w.total_k, H, D, w.max_q(),
-                                w.max_k(), scale, out, lse, stream, causal=args.causal)
+    if args.dense:
+        sq_, sk_ = w.seqlens_q(), w.seqlens_k()
+        if len(set(sq_)) != 1 or len(set(sk_)) != 1:
+            raise SystemExit("--dense needs a workload with equal segment lengths (e.g. --workload dense)")
+        Sq, Sk = sq_[0], sk_[0]
+        ws_bytes = va.varlen_attn_bwd_dense_workspace_size(w.batch, Sq, H, D)
+        wsp = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+
+        def as4(t, S):  # the [batch, S, H, D] view of a packed [batch*S, H, D] tensor
+            return t.as_strided((w.batch, S, H, D), (S * t.stride(0), t.stride(0), t.stride(1), 1), t.storage_offset())
+
+    def run_fwd(x, o, l):
+        if args.dense:
+            st = va.varlen_attn_fwd_dense(as4(x.q, Sq), as4(x.k, Sk), as4(x.v, Sk), w.batch, Sq, Sk, H, D, scale,
+                                          args.causal, as4(o, Sq), l, stream)
+        else:
+            st = va.varlen_attn_fwd(x.q, x.k, x.v, x.cu_q, x.cu_k, w.batch, w.total_q, w.total_k, H, D, w.max_q(),
+                                    w.max_k(), scale, o, l, stream, causal=args.causal)
         assert st == 0, va.varlen_attn_status_string(st)
 
-    def bwd():
-        st = va.varlen_attn_bwd(d.q, d.k, d.v, out, d.dout, lse, d.cu_q, d.cu_k, w.batch, w.total_q, w.total_k,
-                                H, D, w.max_q(), w.max_k(), scale, dq, dk, dv, wsp, ws_bytes, stream,
-                                causal=args.causal)
+    def run_bwd(x, o, l, gq, gk, gv):
+        if args.dense:
+            st = va.varlen_attn_bwd_dense(as4(x.q, Sq), as4(x.k, Sk), as4(x.v, Sk), as4(o, Sq), as4(x.dout, Sq),
+                                          l, w.batch, Sq, Sk, H, D, scale, args.causal, as4(gq, Sq), as4(gk, Sk),
+                                          as4(gv, Sk), wsp, ws_bytes, stream)
+        else:
+            st = va.varlen_attn_bwd(x.q, x.k, x.v, o, x.dout, l, x.cu_q, x.cu_k, w.batch, w.total_q,
+                                    w.total_k, H, D, w.max_q(), w.max_k(), scale, gq, gk, gv, wsp, ws_bytes, stream,
+                                    causal=args.causal)
         assert st == 0, va.varlen_attn_status_string(st)
+
+    def fwd():
+        run_fwd(d, out, lse)
+
+    def bwd():
+        run_bwd(d, out, lse, dq, dk, dv)
 
     # does the backward exist in this build?
     fwd()
-    has_bwd = va.varlen_attn_bwd(d.q, d.k, d.v, out, d.dout, lse, d.cu_q, d.cu_k, w.batch, w.total_q, w.total_k,
-                                 H, D, w.max_q(), w.max_k(), scale, dq, dk, dv, wsp, ws_bytes, stream,
-                                 causal=args.causal) == 0
+    bwd()
+    has_bwd = True
     torch.cuda.synchronize()
     assert va.varlen_attn_get_device_status(stream) == 0
 
@@ -292,7 +317,7 @@ def ours(args, w, ws, rank, local):
         h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
         h_dq, h_dk, h_dv = (torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv))
-        h2d_bytes = sum(t.numel() * t.element_size() for t in host.values()) + 2 * hcu_q.numel() * 4
+        h2d_bytes = sum(t.numel() * t.element_size() for t in host.values()) + (0 if args.dense else 2 * hcu_q.numel() * 4)
         d2h_bytes = sum(t.numel() * t.element_size() for t in (h_out, h_lse)) + (
             sum(t.numel() * t.element_size() for t in (h_dq, h_dk, h_dv)) if has_bwd else 0)
 
@@ -312,20 +337,16 @@ def ours(args, w, ws, rank, local):
             for n, h in host.items():
                 t = getattr(x, n)
                 (t if t._base is None else t._base).copy_(h, non_blocking=True)
-            x.cu_q.copy_(hcu_q, non_blocking=True)
-            x.cu_k.copy_(hcu_k, non_blocking=True)
+            if not args.dense:  # the dense entry points take no cu_seqlens
+                x.cu_q.copy_(hcu_q, non_blocking=True)
+                x.cu_k.copy_(hcu_k, non_blocking=True)
 
         def compute(i):
             x = sets[i % 2]
             o, l, gq, gk, gv = outs[i % 2]
-            st = va.varlen_attn_fwd(x.q, x.k, x.v, x.cu_q, x.cu_k, w.batch, w.total_q, w.total_k, H, D, w.max_q(),
-                                    w.max_k(), scale, o, l, stream, causal=args.causal)
-            assert st == 0, va.varlen_attn_status_string(st)
+            run_fwd(x, o, l)
             if has_bwd:
-                st = va.varlen_attn_bwd(x.q, x.k, x.v, o, x.dout, l, x.cu_q, x.cu_k, w.batch, w.total_q, w.total_k,
-                                        H, D, w.max_q(), w.max_k(), scale, gq, gk, gv, wsp, ws_bytes, stream,
-                                        causal=args.causal)
-                assert st == 0, va.varlen_attn_status_string(st)
+                run_bwd(x, o, l, gq, gk, gv)
 
         def d2h(i):
             o, l, gq, gk, gv = outs[i % 2]
@@ -397,7 +418,7 @@ def ours(args, w, ws, rank, local):
     peak = float(peaks.get("bf16_tflops"))
     sust = float(peaks.get("bf16_tflops_sustained", peak))
     # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the backward main
-    # kernel, from one ncu capture of the windowed workload at H=8 (kernel as of commit 480887b).
+    # kernel, from one ncu capture of the windowed workload at H=8 (kernel as of commit c057947).
     # Every head reads its own q, k, v, dout and writes its own dk, dv and dq rows, so the
     # traffic scales with the number of heads.  Reported only for that workload and head size.
     traffic = None
@@ -422,7 +443,7 @@ def ours(args, w, ws, rank, local):
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "batch_segments": w.batch, "total_q": w.total_q, "total_k": w.total_k,
                    "num_heads": H, "head_dim": D, "step": "fwd+bwd" if has_bwd else "fwd only (bwd missing)",
-                   "causal": bool(args.causal),
+                   "causal": bool(args.causal), "entry": "dense batched" if args.dense else "packed varlen",
                    "l2": "inputs larger than L2 (k, v 2 GB each); no flush",
                    "parallelism": "replicas" if ws > 1 else "single GPU"},
         "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
@@ -449,6 +470,8 @@ def main():
                     help="override the head count (small cases for profiling captures)")
     ap.add_argument("--causal", action="store_true",
                     help="time the causal entry points (FLOPs counted over visible pairs only)")
+    ap.add_argument("--dense", action="store_true",
+                    help="drive the dense batched entry points (needs equal segment lengths, e.g. --workload dense)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -167,8 +167,15 @@ def ragged(seed: int = 0) -> Workload:
                     row_pad=64, lengths_from_seed=True)
 
 
+def dense_batched() -> Workload:
+    """Uniform segments for the dense batched entry points: 8 x (4096 q, 16384
+    kv), H=56, D=128 -- the windowed workload's size class with equal lengths."""
+    return Workload("dense", _cu([4096] * 8), _cu([16384] * 8), 56, 128)
+
+
 WORKLOADS = {
     "tiny": tiny,
+    "dense": dense_batched,
     "windowed": windowed,
     "long": long_dense,
     "strided_dout": strided_dout,
