@@ -56,7 +56,7 @@ class _Problem(ctypes.Structure):
         ("batch", ctypes.c_int32), ("num_heads", ctypes.c_int32),
         ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32),
         ("scale", ctypes.c_double),
-        ("causal", ctypes.c_int32),
+        ("window_left", ctypes.c_int32), ("window_right", ctypes.c_int32),
     ]
 
 
@@ -119,7 +119,10 @@ def _view_args(t: torch.Tensor | None, H: int, D: int):
 class Problem:
     """One packed-attention problem, held as CPU tensors (no copies)."""
 
-    def __init__(self, q, k, v, cu_q, cu_k, scale, dout=None, causal=False):
+    def __init__(self, q, k, v, cu_q, cu_k, scale, dout=None, causal=False, window=(-1, -1)):
+        """``window = (left, right)``: q row ii of a segment sees the keys jj
+        with ii + Sk - Sq - left <= jj <= ii + Sk - Sq + right, a negative
+        side unbounded; ``causal`` sets right = 0."""
         dt = q.dtype
         if dt not in (torch.bfloat16, torch.float64):
             raise ValueError("oracle supports bf16 or fp64 inputs")
@@ -142,7 +145,10 @@ class Problem:
         s.num_heads, s.head_dim = self.H, self.D
         s.dtype = 0 if dt == torch.bfloat16 else 1
         s.scale = float(scale)
-        s.causal = 1 if causal else 0
+        wl, wr = int(window[0]), int(window[1])
+        if causal:
+            wr = 0
+        s.window_left, s.window_right = (min(max(w, -1), 2**31 - 1) for w in (wl, wr))
         self._s = s
         self.has_dout = dout is not None
 

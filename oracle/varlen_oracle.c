@@ -39,12 +39,16 @@
  *   Empty sums are zero (dq of an empty-key segment, dk/dv of an empty-query
  *   segment).
  *
- *   Causal mask (causal = 1).  The pages call the varlen function with
- *   causal=False only; for causal=True this oracle takes the alignment of
- *   the API they call, the diagonal meeting the last key at the last query:
- *   q row ii of a segment (0-based within it) sees kv rows jj <= ii + Sk - Sq.
- *   Every sum over j above then runs over the visible keys only; a row that
- *   sees none gets LSE = -inf, o = 0 and dq = 0, and adds nothing to dk / dv.
+ *   Masks (window_left, window_right).  The pages call the varlen function
+ *   with causal=False and no window only; for the masked forms this oracle
+ *   takes the conventions of the API they call.  The diagonal meets the last
+ *   key at the last query: with d = Sk - Sq, q row ii of a segment (0-based
+ *   within it) sees the kv rows jj (0-based) with
+ *       ii + d - window_left  <=  jj  <=  ii + d + window_right,
+ *   a negative window side being unbounded.  Causal is window_right = 0
+ *   (jj <= ii + d); no mask is (-1, -1).  Every sum over j above then runs
+ *   over the visible keys only; a row that sees none gets LSE = -inf, o = 0
+ *   and dq = 0, and adds nothing to dk / dv.
  *
  * All index arithmetic is int64.  Rows are looked up in cu_seqlens by a
  * linear scan.  OpenMP parallelises over independent (row, head) pairs only.
@@ -67,7 +71,8 @@ typedef struct {
     int32_t batch, num_heads, head_dim;
     int32_t dtype;                  /* 0 = bf16 bit patterns, 1 = fp64      */
     double scale;
-    int32_t causal;                 /* 1: causal mask (see visible_keys)    */
+    int32_t window_left;            /* mask sides, < 0 unbounded (see       */
+    int32_t window_right;           /* visible_range); causal = (-1, 0)     */
 } oracle_problem;
 
 /* Exact widening of a bf16 bit pattern: the bf16 bits are the top half of an
@@ -105,19 +110,25 @@ static int32_t segment_of(const int32_t *cu, int32_t batch, int64_t i) {
     return -1;
 }
 
-/* Number of keys of segment b that its q row ii (0-based within the
- * segment) sees: all Sk_b without the causal mask, else those with
- * jj <= ii + Sk_b - Sq_b, i.e. ii + Sk_b - Sq_b + 1 clamped to [0, Sk_b]. */
-static int64_t visible_keys(const oracle_problem *pb, int32_t b, int64_t ii) {
+/* The keys [*lo, *hi) of segment b (0-based within it) that its q row ii
+ * sees: all Sk_b without a mask; else, with diag = ii + Sk_b - Sq_b, those
+ * with jj >= diag - window_left (if window_left >= 0) and
+ * jj <= diag + window_right (if window_right >= 0).  Empty: *lo == *hi. */
+static void visible_range(const oracle_problem *pb, int32_t b, int64_t ii,
+                          int64_t *lo, int64_t *hi) {
     const int64_t Sq = (int64_t)pb->cu_q[b + 1] - pb->cu_q[b];
     const int64_t Sk = (int64_t)pb->cu_k[b + 1] - pb->cu_k[b];
-    if (!pb->causal) return Sk;
-    const int64_t n = ii + (Sk - Sq) + 1;
-    return n < 0 ? 0 : (n > Sk ? Sk : n);
+    const int64_t diag = ii + (Sk - Sq);
+    int64_t a = 0, e = Sk;
+    if (pb->window_left >= 0 && diag - pb->window_left > a) a = diag - pb->window_left;
+    if (pb->window_right >= 0 && diag + pb->window_right + 1 < e) e = diag + pb->window_right + 1;
+    if (e < a) e = a;
+    *lo = a;
+    *hi = e;
 }
 
 /* Forward for one (q row, head): s, LSE, P and o by the definition above.
- * s and p are scratch of length >= Sk.  Returns the segment, -1 if the row is
+ * s is scratch of length >= Sk (s[j] for the visible keys j).  Returns the segment, -1 if the row is
  * in none. */
 static int32_t row_forward(const oracle_problem *pb, int64_t i, int32_t h,
                            double *qi, double *kj, double *s, double *out_o,
@@ -125,23 +136,25 @@ static int32_t row_forward(const oracle_problem *pb, int64_t i, int32_t h,
     const int32_t D = pb->head_dim;
     int32_t b = segment_of(pb->cu_q, pb->batch, i);
     if (b < 0) return -1;
-    const int64_t k0 = pb->cu_k[b], Sk = visible_keys(pb, b, i - pb->cu_q[b]);
+    const int64_t k0 = pb->cu_k[b];
+    int64_t jlo, jhi;
+    visible_range(pb, b, i - pb->cu_q[b], &jlo, &jhi);
     load_row(pb->q, pb->dtype, pb->q_rs, pb->q_hs, i, h, D, qi);
     for (int32_t d = 0; d < D; ++d) out_o[d] = 0.0;
-    if (Sk <= 0) {
+    if (jhi <= jlo) {
         *out_lse = -INFINITY;
         return b;
     }
     double m = -INFINITY;
-    for (int64_t j = 0; j < Sk; ++j) {
+    for (int64_t j = jlo; j < jhi; ++j) {
         load_row(pb->k, pb->dtype, pb->k_rs, pb->k_hs, k0 + j, h, D, kj);
         s[j] = pb->scale * dot(qi, kj, D);
         if (s[j] > m) m = s[j];
     }
     double sum = 0.0;
-    for (int64_t j = 0; j < Sk; ++j) sum += exp(s[j] - m);
+    for (int64_t j = jlo; j < jhi; ++j) sum += exp(s[j] - m);
     const double lse = m + log(sum);
-    for (int64_t j = 0; j < Sk; ++j) {
+    for (int64_t j = jlo; j < jhi; ++j) {
         const double p = exp(s[j] - lse);
         load_row(pb->v, pb->dtype, pb->v_rs, pb->v_hs, k0 + j, h, D, kj);
         for (int32_t d = 0; d < D; ++d) out_o[d] += p * kj[d];
@@ -216,8 +229,10 @@ int oracle_bwd_q(const oracle_problem *pb, int64_t n, const int64_t *rows,
             load_row(pb->dout, pb->dtype, pb->do_rs, pb->do_hs, i, h, D, doi);
             const double dlt = dot(doi, oi, D);
             delta[t] = dlt;
-            const int64_t k0 = pb->cu_k[b], Sk = visible_keys(pb, b, i - pb->cu_q[b]);
-            for (int64_t j = 0; j < Sk; ++j) {
+            const int64_t k0 = pb->cu_k[b];
+            int64_t jlo, jhi;
+            visible_range(pb, b, i - pb->cu_q[b], &jlo, &jhi);
+            for (int64_t j = jlo; j < jhi; ++j) {
                 const double p = exp(s[j] - lse);
                 load_row(pb->v, pb->dtype, pb->v_rs, pb->v_hs, k0 + j, h, D, kj);
                 const double dp = dot(doi, kj, D);
@@ -293,7 +308,9 @@ int oracle_bwd_kv(const oracle_problem *pb, int64_t n, const int64_t *rows,
             const int64_t q0 = pb->cu_q[b], Sq = (int64_t)pb->cu_q[b + 1] - pb->cu_q[b];
             const int64_t jj = j - pb->cu_k[b];  /* key index within the segment */
             for (int64_t ii = 0; ii < Sq; ++ii) {
-                if (jj >= visible_keys(pb, b, ii)) continue;  /* masked: P_ij = 0 */
+                int64_t jlo, jhi;
+                visible_range(pb, b, ii, &jlo, &jhi);
+                if (jj < jlo || jj >= jhi) continue;  /* masked: P_ij = 0 */
                 load_row(pb->q, pb->dtype, pb->q_rs, pb->q_hs, q0 + ii, h, D, qi);
                 load_row(pb->dout, pb->dtype, pb->do_rs, pb->do_hs, q0 + ii, h, D, doi);
                 const double sij = pb->scale * dot(qi, kj, D);

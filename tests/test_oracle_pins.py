@@ -73,10 +73,16 @@ def _torch_reference(q, k, v, do, cq, ck, scale):
 
 
 def _torch_causal_reference(q, k, v, do, cq, ck, scale):
-    """Per segment, causal: masked softmax attention in fp64 torch ops with
-    the mask of the reading (key jj visible to query ii iff
-    jj <= ii + Sk - Sq), gradients by autograd; a row that sees no key gets
-    o = 0 and LSE = -inf."""
+    """Per segment, causal: the masked reference with key jj visible to
+    query ii iff jj <= ii + Sk - Sq."""
+    return _torch_masked_reference(q, k, v, do, cq, ck, scale, lambda i, j, d: j <= i + d)
+
+
+def _torch_masked_reference(q, k, v, do, cq, ck, scale, visible):
+    """Per segment: masked softmax attention in fp64 torch ops, key jj
+    visible to query ii iff visible(ii, jj, Sk - Sq) (broadcast index
+    tensors), gradients by autograd; a row that sees no key gets o = 0 and
+    LSE = -inf."""
     H, D = q.shape[1], q.shape[2]
     out = torch.zeros(q.shape, dtype=torch.float64)
     lse = torch.full((q.shape[0], H), float("-inf"), dtype=torch.float64)
@@ -90,7 +96,7 @@ def _torch_causal_reference(q, k, v, do, cq, ck, scale):
         qs = q[cq[b]:cq[b + 1]].double().transpose(0, 1).clone().requires_grad_()
         ks = k[ck[b]:ck[b + 1]].double().transpose(0, 1).clone().requires_grad_()
         vs = v[ck[b]:ck[b + 1]].double().transpose(0, 1).clone().requires_grad_()
-        vis = torch.arange(Sk)[None, :] <= torch.arange(Sq)[:, None] + (Sk - Sq)   # [Sq, Sk]
+        vis = visible(torch.arange(Sq)[:, None], torch.arange(Sk)[None, :], Sk - Sq)   # [Sq, Sk]
         live = vis.any(-1)                                                        # [Sq]
         s = scale * (qs @ ks.transpose(1, 2))
         s = torch.where(vis, s, torch.full_like(s, float("-inf")))
@@ -151,6 +157,106 @@ def _causal_checks(lib, seed):
     # Sq = Sk: the first row sees only the first key -> o = v_0
     first = rows == cq[2]
     res.append(("causal_first_row_v0", bool(np.array_equal(o[first], v[ck[2]].numpy()))))
+    return res
+
+
+def _window_checks(lib, seed):
+    """Sliding-window pins: closed forms that fix each side of the band
+    exactly (a zero-width band gives o_i = v of the diagonal key; a band of
+    two keys is a two-term softmax), windows wider than every segment equal
+    the unmasked oracle, (-1, 0) equals the causal mask, and the masked torch
+    autograd reference for the gradients."""
+    res = []
+    H, D, sc = 2, 8, 0.41
+    lq, lk = [7, 5, 9, 1, 0, 6], [7, 9, 4, 3, 2, 0]  # Sq = Sk, Sq < Sk, Sq > Sk, one row, empties
+    cq, ck = _cu(lq), _cu(lk)
+    q, k, v = _rand((cq[-1], H, D), seed + 40), _rand((ck[-1], H, D), seed + 41), _rand((ck[-1], H, D), seed + 42)
+    do = _rand((cq[-1], H, D), seed + 43)
+    rows, heads = oracle.all_pairs(cq[-1], H)
+    krows, kheads = oracle.all_pairs(ck[-1], H)
+
+    def run(**kw):
+        pb = oracle.Problem(q, k, v, cq, ck, sc, dout=do, **kw)
+        o, lse = pb.fwd(rows, heads, lib=lib)
+        dq, _ = pb.bwd_q(rows, heads, lib=lib)
+        dk, dv = pb.bwd_kv(krows, kheads, lib=lib)
+        return o, lse, dq, dk, dv
+
+    # zero-width band: q row ii sees only key ii + Sk - Sq (when it exists)
+    o, lse, dq, dk, dv = run(window=(0, 0))
+    ok0 = True
+    for b in range(len(lq)):
+        for ii in range(lq[b]):
+            r = cq[b] + ii
+            jj = ii + lk[b] - lq[b]
+            for h in range(H):
+                t = r * H + h
+                if 0 <= jj < lk[b]:
+                    kr = ck[b] + jj
+                    s_exp = sc * float(torch.dot(q[r, h], k[kr, h]))
+                    ok0 &= bool(np.array_equal(o[t], v[kr, h].numpy())) and abs(lse[t] - s_exp) <= 1e-14 * max(1, abs(s_exp))
+                    ok0 &= bool(np.all(dq[t] == 0))
+                else:
+                    ok0 &= bool(np.isneginf(lse[t]) and np.all(o[t] == 0))
+    res.append(("window_zero_width_diagonal", ok0))
+    # one visible key per row: dk = 0 and dv_j = dO of the row that sees key j
+    dv_exp = np.zeros_like(dv)
+    for b in range(len(lq)):
+        for ii in range(lq[b]):
+            jj = ii + lk[b] - lq[b]
+            if 0 <= jj < lk[b]:
+                for h in range(H):
+                    dv_exp[(ck[b] + jj) * H + h] += do[cq[b] + ii, h].numpy()
+    res.append(("window_zero_width_grads", bool(np.all(dk == 0) and np.allclose(dv, dv_exp, rtol=0, atol=1e-15))))
+    # band of the diagonal key and the one before it (window (1, 0)), Sq = Sk segment:
+    # a two-term softmax, o = (e_a v_{i-1} + e_b v_i) / (e_a + e_b)
+    o, lse, *_ = run(window=(1, 0))
+    ok2 = True
+    b = 0
+    for ii in range(1, lq[b]):
+        r = cq[b] + ii
+        for h in range(H):
+            sa = sc * float(torch.dot(q[r, h], k[ck[b] + ii - 1, h]))
+            sb = sc * float(torch.dot(q[r, h], k[ck[b] + ii, h]))
+            mx = max(sa, sb)
+            ea, eb = math.exp(sa - mx), math.exp(sb - mx)
+            o_exp = (ea * v[ck[b] + ii - 1, h].numpy() + eb * v[ck[b] + ii, h].numpy()) / (ea + eb)
+            ok2 &= bool(np.allclose(o[r * H + h], o_exp, rtol=1e-13, atol=1e-14))
+            ok2 &= abs(lse[r * H + h] - (mx + math.log(ea + eb))) <= 1e-13
+    res.append(("window_two_key_band", ok2))
+    # same band, right side: window (0, 1) on the Sq < Sk segment sees keys ii+d and ii+d+1
+    o, lse, *_ = run(window=(0, 1))
+    ok3 = True
+    b = 1
+    d = lk[b] - lq[b]
+    for ii in range(lq[b]):
+        r = cq[b] + ii
+        j0, j1 = ii + d, min(ii + d + 1, lk[b] - 1)
+        for h in range(H):
+            ss = [sc * float(torch.dot(q[r, h], k[ck[b] + j, h])) for j in range(j0, j1 + 1)]
+            mx = max(ss)
+            es = [math.exp(x - mx) for x in ss]
+            o_exp = sum(e * v[ck[b] + j, h].numpy() for e, j in zip(es, range(j0, j1 + 1))) / sum(es)
+            ok3 &= bool(np.allclose(o[r * H + h], o_exp, rtol=1e-13, atol=1e-14))
+    res.append(("window_right_band", ok3))
+    # windows wider than every segment: identical to no mask; (-1, 0): identical to causal
+    full = run()
+    wide = run(window=(64, 64))
+    res.append(("window_wide_is_unmasked", all(np.array_equal(a, b_) for a, b_ in zip(full, wide))))
+    cz = run(causal=True)
+    wc = run(window=(-1, 0))
+    res.append(("window_left_unbounded_is_causal", all(np.array_equal(a, b_) for a, b_ in zip(cz, wc))))
+    # gradients of a general band against masked torch autograd
+    wl, wr = 2, 1
+    o, lse, dq, dk, dv = run(window=(wl, wr))
+    ro, rl, rdq, rdk, rdv = _torch_masked_reference(
+        q, k, v, do, cq, ck, sc,
+        lambda i, j, d: (j >= i + d - wl) & (j <= i + d + wr))
+    res.append(("window_out", np.allclose(o, ro.reshape(-1, D).numpy(), rtol=1e-12, atol=1e-13)))
+    res.append(("window_lse", np.allclose(lse, rl.reshape(-1).numpy(), rtol=1e-12, atol=1e-13)))
+    res.append(("window_dq", np.allclose(dq, rdq.reshape(-1, D).numpy(), rtol=1e-10, atol=1e-12)))
+    res.append(("window_dk", np.allclose(dk, rdk.reshape(-1, D).numpy(), rtol=1e-10, atol=1e-12)))
+    res.append(("window_dv", np.allclose(dv, rdv.reshape(-1, D).numpy(), rtol=1e-10, atol=1e-12)))
     return res
 
 
@@ -264,6 +370,7 @@ def _battery(lib, seed=0):
     # central finite differences of L = sum(O * dO)
     res.append(("finite_differences", _finite_difference_ok(lib, seed)))
     res += _causal_checks(lib, seed)
+    res += _window_checks(lib, seed)
     return res
 
 
@@ -357,6 +464,9 @@ def test_page_values():
     assert max(wl.seqlens_q()) == c["true_max_seqlen_q"] != c["stated_max_seqlen_q"]
 
 
+LEFT_EDGE = "    if (pb->window_left >= 0 && diag - pb->window_left > a) a = diag - pb->window_left;"
+RIGHT_EDGE = "    if (pb->window_right >= 0 && diag + pb->window_right + 1 < e) e = diag + pb->window_right + 1;"
+
 MUTANTS = [
     ("dropped scale in s", "s[j] = pb->scale * dot(qi, kj, D);", "s[j] = dot(qi, kj, D);"),
     ("LSE without the max", "const double lse = m + log(sum);", "const double lse = log(sum);"),
@@ -370,13 +480,21 @@ MUTANTS = [
     ("dK sums dO instead of Q", "gk[d] += pb->scale * ds * qi[d];", "gk[d] += pb->scale * ds * doi[d];"),
     ("segment end off by one", "if ((int64_t)cu[b] <= i && i < (int64_t)cu[b + 1]) return b;",
      "if ((int64_t)cu[b] <= i && i <= (int64_t)cu[b + 1]) return b;"),
-    ("kv segment start of the next segment", "const int64_t k0 = pb->cu_k[b], Sk",
-     "const int64_t k0 = pb->cu_k[b] + (b > 0), Sk"),
+    ("kv segment start of the next segment", "const int64_t k0 = pb->cu_k[b];",
+     "const int64_t k0 = pb->cu_k[b] + (b > 0);"),
     ("delta from dO.v instead of dO.o", "E[ii] = dot(doi, oi, D);", "E[ii] = dot(doi, doi, D);"),
     ("head stride ignored", "int64_t off = row * rs + (int64_t)h * hs;", "int64_t off = row * rs;"),
-    ("causal diagonal one key early", "const int64_t n = ii + (Sk - Sq) + 1;", "const int64_t n = ii + (Sk - Sq);"),
-    ("causal diagonal aligned top-left", "const int64_t n = ii + (Sk - Sq) + 1;", "const int64_t n = ii + 1;"),
-    ("causal mask missing on the key side", "if (jj >= visible_keys(pb, b, ii)) continue;", "(void)jj;"),
+    ("causal diagonal one key early", RIGHT_EDGE, RIGHT_EDGE.replace("+ 1 < e) e = diag + pb->window_right + 1;",
+                                                                     "< e) e = diag + pb->window_right;")),
+    ("causal diagonal aligned top-left", "const int64_t diag = ii + (Sk - Sq);", "const int64_t diag = ii;"),
+    ("mask missing on the key side", "if (jj < jlo || jj >= jhi) continue;", "(void)jj;"),
+    ("key-side mask misses the left edge", "if (jj < jlo || jj >= jhi) continue;", "if (jj >= jhi) continue;"),
+    ("window left edge one key late", LEFT_EDGE, LEFT_EDGE.replace("a = diag - pb->window_left;",
+                                                                   "a = diag - pb->window_left + 1;")),
+    ("window left side ignored", LEFT_EDGE, LEFT_EDGE.replace("if (pb->window_left >= 0 &&", "if (0 &&")),
+    ("window right width ignored", RIGHT_EDGE, RIGHT_EDGE.replace("pb->window_right + 1", "1")),
+    ("window sides swapped", LEFT_EDGE + "\n" + RIGHT_EDGE,
+     LEFT_EDGE.replace("window_left", "window_right") + "\n" + RIGHT_EDGE.replace("window_right", "window_left")),
 ]
 
 
