@@ -42,8 +42,17 @@ METRIC = "varlen attention TFLOP/s (fwd, bwd) bf16 H=56 D=128; % of GB300 bf16 T
 BWD_MAIN_DRAM_BYTES_PER_HEAD = {("windowed", 128): (872.408576e6 + 672.020736e6) / 8}
 
 
+def _window(args):
+    return tuple(args.window) if getattr(args, "window", None) else (-1, -1)
+
+
 def _metric(args) -> str:
-    return METRIC.replace("bf16", "bf16 causal") if getattr(args, "causal", False) else METRIC
+    mask = []
+    if getattr(args, "causal", False):
+        mask.append("causal")
+    if _window(args) != (-1, -1):
+        mask.append("window(%d,%d)" % _window(args))
+    return METRIC.replace("bf16", "bf16 " + " ".join(mask), 1) if mask else METRIC
 
 
 def _peaks():
@@ -138,14 +147,15 @@ def _max_over_ranks(x: float, ws: int) -> float:
 
 # ------------------------------------------------------------------ CPU side
 
-def _oracle_rate(w: W.Workload, target_s: float, seed: int = 0, causal: bool = False):
+def _oracle_rate(w: W.Workload, target_s: float, seed: int = 0, causal: bool = False, window=(-1, -1)):
     """Times the oracle (forward + query-side backward) on sampled (row, head)
     pairs of the workload.  Credits each pair with its share of the step's
     algorithmic flops: 4*n*D (forward) + 10*n*D (backward), n = the keys the
-    row sees (Sk, or fewer under the causal mask)."""
+    row sees (Sk, or fewer under a mask)."""
     import oracle
     inp = W.make_inputs(w, seed)
-    pb = oracle.Problem(inp.q, inp.k, inp.v, inp.cu_q, inp.cu_k, w.softmax_scale, dout=inp.dout, causal=causal)
+    pb = oracle.Problem(inp.q, inp.k, inp.v, inp.cu_q, inp.cu_k, w.softmax_scale, dout=inp.dout, causal=causal,
+                        window=window)
     rng = np.random.default_rng(5)
     seg_k = {b: w.cu_k[b + 1] - w.cu_k[b] for b in range(w.batch)}
 
@@ -156,12 +166,10 @@ def _oracle_rate(w: W.Workload, target_s: float, seed: int = 0, causal: bool = F
 
     def flops(rows):
         b = np.searchsorted(np.asarray(w.cu_q), rows, side="right") - 1
-        sk = np.array([seg_k[int(x)] for x in b], dtype=np.float64)
-        if causal:  # keys row i of segment b sees: clamp(i + Sk - Sq + 1, 0, Sk)
-            sq = np.array([w.cu_q[int(x) + 1] - w.cu_q[int(x)] for x in b], dtype=np.float64)
-            ii = rows - np.asarray(w.cu_q)[b]
-            sk = np.clip(ii + sk - sq + 1, 0, sk)
-        return float((14.0 * sk * w.head_dim).sum())
+        sk = np.array([seg_k[int(x)] for x in b], dtype=np.int64)
+        sq = np.array([w.cu_q[int(x) + 1] - w.cu_q[int(x)] for x in b], dtype=np.int64)
+        n = W.row_keys(rows - np.asarray(w.cu_q)[b], sq, sk, causal, window)
+        return float((14.0 * n * w.head_dim).sum())
 
     def run(n):
         rows, heads = sample(n)
@@ -183,7 +191,7 @@ def reference_arm(args, w, ws, rank):
     if rank != 0:
         return
     run, n, cores = _oracle_rate(w, target_s=max(2.0, 150.0 / max(args.steps + args.warmup, 1)),
-                                 causal=args.causal)
+                                 causal=args.causal, window=_window(args))
     for _ in range(args.warmup):
         run(n)
     tot_t = tot_f = 0.0
@@ -223,6 +231,8 @@ def ours(args, w, ws, rank, local):
         sq_, sk_ = w.seqlens_q(), w.seqlens_k()
         if len(set(sq_)) != 1 or len(set(sk_)) != 1:
             raise SystemExit("--dense needs a workload with equal segment lengths (e.g. --workload dense)")
+        if _window(args) != (-1, -1):
+            raise SystemExit("--dense takes no --window (the dense entry points carry the causal flag only)")
         Sq, Sk = sq_[0], sk_[0]
         ws_bytes = va.varlen_attn_bwd_dense_workspace_size(w.batch, Sq, H, D)
         wsp = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
@@ -236,7 +246,7 @@ def ours(args, w, ws, rank, local):
                                           args.causal, as4(o, Sq), l, stream)
         else:
             st = va.varlen_attn_fwd(x.q, x.k, x.v, x.cu_q, x.cu_k, w.batch, w.total_q, w.total_k, H, D, w.max_q(),
-                                    w.max_k(), scale, o, l, stream, causal=args.causal)
+                                    w.max_k(), scale, o, l, stream, causal=args.causal, window=_window(args))
         assert st == 0, va.varlen_attn_status_string(st)
 
     def run_bwd(x, o, l, gq, gk, gv):
@@ -247,7 +257,7 @@ def ours(args, w, ws, rank, local):
         else:
             st = va.varlen_attn_bwd(x.q, x.k, x.v, o, x.dout, l, x.cu_q, x.cu_k, w.batch, w.total_q,
                                     w.total_k, H, D, w.max_q(), w.max_k(), scale, gq, gk, gv, wsp, ws_bytes, stream,
-                                    causal=args.causal)
+                                    causal=args.causal, window=_window(args))
         assert st == 0, va.varlen_attn_status_string(st)
 
     def fwd():
@@ -302,7 +312,8 @@ def ours(args, w, ws, rank, local):
     ms_total = _max_over_ranks(e_start.elapsed_time(e_end), ws)
     t_fwd = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     t_bwd = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
-    f_fwd, f_bwd = w.fwd_flops(args.causal), (w.bwd_flops(args.causal) if has_bwd else 0.0)
+    f_fwd = w.fwd_flops(args.causal, _window(args))
+    f_bwd = w.bwd_flops(args.causal, _window(args)) if has_bwd else 0.0
     step_flops = f_fwd + f_bwd
     value = ws * K * step_flops / (ms_total * 1e-3) / 1e12
     fwd_tflops = f_fwd / (statistics.mean(t_fwd) * 1e-3) / 1e12
@@ -422,7 +433,7 @@ def ours(args, w, ws, rank, local):
     # Every head reads its own q, k, v, dout and writes its own dk, dv and dq rows, so the
     # traffic scales with the number of heads.  Reported only for that workload and head size.
     traffic = None
-    if dom_name == "varlen_bwd_main_kernel" and not args.causal and (w.name, D) in BWD_MAIN_DRAM_BYTES_PER_HEAD:
+    if dom_name == "varlen_bwd_main_kernel" and not args.causal and _window(args) == (-1, -1) and (w.name, D) in BWD_MAIN_DRAM_BYTES_PER_HEAD:
         traffic = BWD_MAIN_DRAM_BYTES_PER_HEAD[(w.name, D)] * H
     roof = {"kernel": dom_name, "bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
             "frac": ach / peak, "peak_source": "%s bf16_tflops (burst)" % src,
@@ -430,7 +441,7 @@ def ours(args, w, ws, rank, local):
 
     cpu_base = None
     if not args.no_cpu_baseline and ws >= 1:
-        run, n, cores = _oracle_rate(w, target_s=12.0, causal=args.causal)
+        run, n, cores = _oracle_rate(w, target_s=12.0, causal=args.causal, window=_window(args))
         t, f, n = run(n)
         cpu_base = {"value": f / t / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                     "sample": "oracle fwd + dQ backward on %d random (row, head) pairs of the %s workload "
@@ -443,7 +454,7 @@ def ours(args, w, ws, rank, local):
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "batch_segments": w.batch, "total_q": w.total_q, "total_k": w.total_k,
                    "num_heads": H, "head_dim": D, "step": "fwd+bwd" if has_bwd else "fwd only (bwd missing)",
-                   "causal": bool(args.causal), "entry": "dense batched" if args.dense else "packed varlen",
+                   "causal": bool(args.causal), "window": list(_window(args)), "entry": "dense batched" if args.dense else "packed varlen",
                    "l2": "inputs larger than L2 (k, v 2 GB each); no flush",
                    "parallelism": "replicas" if ws > 1 else "single GPU"},
         "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
@@ -470,6 +481,8 @@ def main():
                     help="override the head count (small cases for profiling captures)")
     ap.add_argument("--causal", action="store_true",
                     help="time the causal entry points (FLOPs counted over visible pairs only)")
+    ap.add_argument("--window", type=int, nargs=2, metavar=("LEFT", "RIGHT"), default=None,
+                    help="time the sliding-window entry points with this band (a negative side is unbounded)")
     ap.add_argument("--dense", action="store_true",
                     help="drive the dense batched entry points (needs equal segment lengths, e.g. --workload dense)")
     ap.add_argument("--no-e2e", action="store_true")

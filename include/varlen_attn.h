@@ -141,6 +141,33 @@ int varlen_attn_bwd_causal(const void* q, varlen_stride sq, const void* k, varle
                            varlen_stride sdv, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Sliding-window forward and backward (not on the pages; the window_size
+ * convention of the API they call).  Arguments, layouts, ownership and
+ * errors are those of varlen_attn_fwd / varlen_attn_bwd plus the two sides
+ * of the band: with d = Sk - Sq of a segment, its q row i (0-based) attends
+ * to the kv rows j (0-based) with
+ *     i + d - window_left  <=  j  <=  i + d + window_right,
+ * a negative side being unbounded.  (-1, -1) is no mask (the unmasked
+ * kernels run), (-1, 0) is the causal mask of varlen_attn_fwd_causal.  A row
+ * whose band holds no key gets O = 0, LSE = -inf and dQ = 0, and adds
+ * nothing to dK / dV.  Key tiles outside a q tile's band (and q steps
+ * outside a kv tile's) are skipped, not masked.
+ */
+int varlen_attn_fwd_window(const void* q, varlen_stride sq, const void* k, varlen_stride sk, const void* v,
+                           varlen_stride sv, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                           int32_t batch, int32_t total_q, int32_t total_k, int32_t num_heads, int32_t head_dim,
+                           int32_t max_seqlen_q, int32_t max_seqlen_k, float scale, int32_t window_left,
+                           int32_t window_right, void* out, varlen_stride so, float* lse, void* stream);
+int varlen_attn_bwd_window(const void* q, varlen_stride sq, const void* k, varlen_stride sk, const void* v,
+                           varlen_stride sv, const void* out, varlen_stride so, const void* dout,
+                           varlen_stride sdo, const float* lse, const int32_t* cu_seqlens_q,
+                           const int32_t* cu_seqlens_k, int32_t batch, int32_t total_q, int32_t total_k,
+                           int32_t num_heads, int32_t head_dim, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                           float scale, int32_t window_left, int32_t window_right, void* dq, varlen_stride sdq,
+                           void* dk, varlen_stride sdk, void* dv, varlen_stride sdv, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/*
  * Dense batched attention: q, out, dout, dq are [batch, seqlen_q, H, D] and
  * k, v, dk, dv are [batch, seqlen_k, H, D] (bf16), each with its own strides
  * in elements and a unit innermost stride; lse is [H, batch * seqlen_q]

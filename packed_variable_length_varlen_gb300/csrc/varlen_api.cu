@@ -159,10 +159,25 @@ using namespace varlen;
 
 namespace {
 
+// The visibility band of a launch from the public window sides (negative:
+// unbounded).  No bounded side means no mask: the unmasked kernels run.
+struct Band {
+  int32_t masked;
+  int64_t left, right;
+};
+
+Band band_of(int32_t window_left, int32_t window_right) {
+  return Band{(window_left >= 0 || window_right >= 0) ? 1 : 0, window_left < 0 ? kWinUnbounded : window_left,
+              window_right < 0 ? kWinUnbounded : window_right};
+}
+
+constexpr Band kNoMask{0, kWinUnbounded, kWinUnbounded};
+constexpr Band kCausal{1, kWinUnbounded, 0};
+
 int fwd_impl(const void* q, varlen_stride sq, const void* k, varlen_stride sk, const void* v, varlen_stride sv,
              CuView cu_q, CuView cu_k, int32_t batch, int32_t total_q, int32_t total_k, int32_t num_heads,
              int32_t head_dim, int32_t max_seqlen_q, int32_t max_seqlen_k, float scale, void* out,
-             varlen_stride so, float* lse, void* stream, int32_t causal) {
+             varlen_stride so, float* lse, void* stream, Band band) {
   (void)max_seqlen_q;  // advisory only: the kernels derive lengths from cu_seqlens
   (void)max_seqlen_k;
   int st = check_common(batch, total_q, total_k, num_heads, head_dim, scale);
@@ -190,7 +205,9 @@ int fwd_impl(const void* q, varlen_stride sq, const void* k, varlen_stride sk, c
   L.p.total_q = total_q;
   L.p.total_k = total_k;
   L.p.num_heads = num_heads;
-  L.p.causal = causal;
+  L.p.masked = band.masked;
+  L.p.win_left = band.left;
+  L.p.win_right = band.right;
   L.p.scale_log2 = scale * kLog2e;
   L.p.err = dev.err;
   L.head_dim = head_dim;
@@ -208,7 +225,7 @@ extern "C" int varlen_attn_fwd(const void* q, varlen_stride sq, const void* k, v
                                varlen_stride so, float* lse, void* stream) {
   if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr) return VARLEN_ERR_NULL;
   return fwd_impl(q, sq, k, sk, v, sv, CuView{cu_seqlens_q, 0}, CuView{cu_seqlens_k, 0}, batch, total_q, total_k,
-                  num_heads, head_dim, max_seqlen_q, max_seqlen_k, scale, out, so, lse, stream, 0);
+                  num_heads, head_dim, max_seqlen_q, max_seqlen_k, scale, out, so, lse, stream, kNoMask);
 }
 
 extern "C" int varlen_attn_fwd_causal(const void* q, varlen_stride sq, const void* k, varlen_stride sk,
@@ -219,7 +236,19 @@ extern "C" int varlen_attn_fwd_causal(const void* q, varlen_stride sq, const voi
                                       void* stream) {
   if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr) return VARLEN_ERR_NULL;
   return fwd_impl(q, sq, k, sk, v, sv, CuView{cu_seqlens_q, 0}, CuView{cu_seqlens_k, 0}, batch, total_q, total_k,
-                  num_heads, head_dim, max_seqlen_q, max_seqlen_k, scale, out, so, lse, stream, 1);
+                  num_heads, head_dim, max_seqlen_q, max_seqlen_k, scale, out, so, lse, stream, kCausal);
+}
+
+extern "C" int varlen_attn_fwd_window(const void* q, varlen_stride sq, const void* k, varlen_stride sk,
+                                      const void* v, varlen_stride sv, const int32_t* cu_seqlens_q,
+                                      const int32_t* cu_seqlens_k, int32_t batch, int32_t total_q, int32_t total_k,
+                                      int32_t num_heads, int32_t head_dim, int32_t max_seqlen_q,
+                                      int32_t max_seqlen_k, float scale, int32_t window_left, int32_t window_right,
+                                      void* out, varlen_stride so, float* lse, void* stream) {
+  if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr) return VARLEN_ERR_NULL;
+  return fwd_impl(q, sq, k, sk, v, sv, CuView{cu_seqlens_q, 0}, CuView{cu_seqlens_k, 0}, batch, total_q, total_k,
+                  num_heads, head_dim, max_seqlen_q, max_seqlen_k, scale, out, so, lse, stream,
+                  band_of(window_left, window_right));
 }
 
 extern "C" size_t varlen_attn_bwd_workspace_size(int32_t batch, int32_t total_q, int32_t num_heads,
@@ -237,7 +266,7 @@ int bwd_impl(const void* q, varlen_stride sq, const void* k, varlen_stride sk, c
              CuView cu_q, CuView cu_k, int32_t batch, int32_t total_q, int32_t total_k, int32_t num_heads,
              int32_t head_dim, int32_t max_seqlen_q, int32_t max_seqlen_k, float scale, void* dq, varlen_stride sdq,
              void* dk, varlen_stride sdk, void* dv, varlen_stride sdv, void* workspace, size_t workspace_bytes,
-             void* stream, int32_t causal) {
+             void* stream, Band band) {
   (void)max_seqlen_q;
   (void)max_seqlen_k;
   int st = check_common(batch, total_q, total_k, num_heads, head_dim, scale);
@@ -290,7 +319,9 @@ int bwd_impl(const void* q, varlen_stride sq, const void* k, varlen_stride sk, c
   L.p.total_k = total_k;
   L.p.num_heads = num_heads;
   L.p.pad_rows = pad_rows;
-  L.p.causal = causal;
+  L.p.masked = band.masked;
+  L.p.win_left = band.left;
+  L.p.win_right = band.right;
   L.p.scale_log2 = scale * kLog2e;
   L.p.scale = scale;
   L.p.err = dev.err;
@@ -318,7 +349,7 @@ extern "C" int varlen_attn_bwd(const void* q, varlen_stride sq, const void* k, v
   if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr) return VARLEN_ERR_NULL;
   return bwd_impl(q, sq, k, sk, v, sv, out, so, dout, sdo, lse, CuView{cu_seqlens_q, 0}, CuView{cu_seqlens_k, 0},
                   batch, total_q, total_k, num_heads, head_dim, max_seqlen_q, max_seqlen_k, scale, dq, sdq, dk, sdk,
-                  dv, sdv, workspace, workspace_bytes, stream, 0);
+                  dv, sdv, workspace, workspace_bytes, stream, kNoMask);
 }
 
 extern "C" int varlen_attn_bwd_causal(const void* q, varlen_stride sq, const void* k, varlen_stride sk,
@@ -332,7 +363,22 @@ extern "C" int varlen_attn_bwd_causal(const void* q, varlen_stride sq, const voi
   if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr) return VARLEN_ERR_NULL;
   return bwd_impl(q, sq, k, sk, v, sv, out, so, dout, sdo, lse, CuView{cu_seqlens_q, 0}, CuView{cu_seqlens_k, 0},
                   batch, total_q, total_k, num_heads, head_dim, max_seqlen_q, max_seqlen_k, scale, dq, sdq, dk, sdk,
-                  dv, sdv, workspace, workspace_bytes, stream, 1);
+                  dv, sdv, workspace, workspace_bytes, stream, kCausal);
+}
+
+extern "C" int varlen_attn_bwd_window(const void* q, varlen_stride sq, const void* k, varlen_stride sk,
+                                      const void* v, varlen_stride sv, const void* out, varlen_stride so,
+                                      const void* dout, varlen_stride sdo, const float* lse,
+                                      const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t batch,
+                                      int32_t total_q, int32_t total_k, int32_t num_heads, int32_t head_dim,
+                                      int32_t max_seqlen_q, int32_t max_seqlen_k, float scale, int32_t window_left,
+                                      int32_t window_right, void* dq, varlen_stride sdq, void* dk, varlen_stride sdk,
+                                      void* dv, varlen_stride sdv, void* workspace, size_t workspace_bytes,
+                                      void* stream) {
+  if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr) return VARLEN_ERR_NULL;
+  return bwd_impl(q, sq, k, sk, v, sv, out, so, dout, sdo, lse, CuView{cu_seqlens_q, 0}, CuView{cu_seqlens_k, 0},
+                  batch, total_q, total_k, num_heads, head_dim, max_seqlen_q, max_seqlen_k, scale, dq, sdq, dk, sdk,
+                  dv, sdv, workspace, workspace_bytes, stream, band_of(window_left, window_right));
 }
 
 // ------------------------------------------------------------ dense batched
@@ -373,7 +419,7 @@ extern "C" int varlen_attn_fwd_dense(const void* q, varlen_dense_stride sq, cons
   if ((st = dense_view(sv, seqlen_k, batch, &vv)) != VARLEN_OK) return st;
   if ((st = dense_view(so, seqlen_q, batch, &vo)) != VARLEN_OK) return st;
   return fwd_impl(q, vq, k, vk, v, vv, CuView{nullptr, seqlen_q}, CuView{nullptr, seqlen_k}, batch, total_q, total_k,
-                  num_heads, head_dim, seqlen_q, seqlen_k, scale, out, vo, lse, stream, causal);
+                  num_heads, head_dim, seqlen_q, seqlen_k, scale, out, vo, lse, stream, causal ? kCausal : kNoMask);
 }
 
 extern "C" size_t varlen_attn_bwd_dense_workspace_size(int32_t batch, int32_t seqlen_q, int32_t num_heads,
@@ -405,7 +451,7 @@ extern "C" int varlen_attn_bwd_dense(const void* q, varlen_dense_stride sq, cons
   if ((st = dense_view(sdv, seqlen_k, batch, &vdv)) != VARLEN_OK) return st;
   return bwd_impl(q, vq, k, vk, v, vv, out, vo, dout, vdo, lse, CuView{nullptr, seqlen_q}, CuView{nullptr, seqlen_k},
                   batch, total_q, total_k, num_heads, head_dim, seqlen_q, seqlen_k, scale, dq, vdq, dk, vdk, dv, vdv,
-                  workspace, workspace_bytes, stream, causal);
+                  workspace, workspace_bytes, stream, causal ? kCausal : kNoMask);
 }
 
 extern "C" int varlen_attn_get_device_status(void* stream) {

@@ -154,17 +154,26 @@ struct BwdCfg {
   static constexpr int TMEM_COLS = 512;
 };
 
-// The q steps [j0, nq) a kv tile works through (128 q rows each).  With the
-// causal mask (q row i sees keys j <= i + Sk - Sq) the steps whose rows all
-// precede the tile's first key are skipped; j0 == nq means no query sees
-// the tile (dK = dV = 0).  The cursor's scheduled side is kv.
-__device__ __forceinline__ void bwd_q_steps(const SegCursor& c, int32_t tile_m, int32_t causal, int32_t& j0,
+// The q steps [j0, nq) a kv tile works through (128 q rows each).  With a
+// mask (the band of BwdParams) only the steps holding q rows that see some
+// key of the tile; j0 == nq means no query sees the tile (dK = dV = 0).
+// The cursor's scheduled side is kv.
+template <bool MASKED>
+__device__ __forceinline__ void bwd_q_steps(const SegCursor& c, int32_t tile_m, const BwdParams& p, int32_t& j0,
                                             int32_t& nq) {
   nq = (c.olen + kBwdTileQ - 1) / kBwdTileQ;
   j0 = 0;
-  if (causal) {
-    const int32_t first_q = tile_m * kTileM - (c.len - c.olen);  // first q row that sees the tile's first key
-    j0 = first_q <= 0 ? 0 : min(nq, first_q / kBwdTileQ);
+  if (MASKED) {
+    const int64_t k0 = (int64_t)tile_m * kTileM;
+    const int64_t k1 = min((int64_t)c.len, k0 + kTileM) - 1;
+    int32_t lo, hi;
+    band_rows(k0, k1, c.olen, c.len, p.win_left, p.win_right, &lo, &hi);
+    if (hi <= lo) {
+      j0 = nq = 0;
+      return;
+    }
+    j0 = lo / kBwdTileQ;
+    nq = (hi + kBwdTileQ - 1) / kBwdTileQ;
   }
 }
 
@@ -196,7 +205,7 @@ __device__ __forceinline__ void clear_rows(uint8_t* tile, int chunks, int chunk_
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool MASKED>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     varlen_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -272,7 +281,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
            ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q); t += G) {
         const Tile tl = cursor_tile(c, t);
         int32_t j0, nq;
-        bwd_q_steps(c, tl.m, CAUSAL, j0, nq);
+        bwd_q_steps<MASKED>(c, tl.m, p, j0, nq);
         if (j0 == nq) continue;  // no query sees the tile: dK = dV = 0, written by the compute warps
         const int32_t krow = c.r0 + tl.m * kTileM;
         if (tiles > 0 && !mbar_wait(&bar.kv_empty, (tiles - 1) & 1, abort)) break;
@@ -316,7 +325,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
            ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q); t += G) {
         const Tile tl = cursor_tile(c, t);
         int32_t j0, nq;
-        bwd_q_steps(c, tl.m, CAUSAL, j0, nq);
+        bwd_q_steps<MASKED>(c, tl.m, p, j0, nq);
         for (int32_t j = j0; j < nq; ++j, ++gs) {
           const uint32_t st = gs % C::NDO;
           if (!mbar_wait(&bar.do_empty[st], ((gs / C::NDO) & 1) ^ 1, abort)) { ok = false; break; }
@@ -420,7 +429,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
            ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q); t += G) {
         const Tile tl = cursor_tile(c, t);
         int32_t j0, nq;
-        bwd_q_steps(c, tl.m, CAUSAL, j0, nq);
+        bwd_q_steps<MASKED>(c, tl.m, p, j0, nq);
         if (j0 == nq) continue;
         if (!mbar_wait(&bar.kv_full, tiles & 1, abort)) break;
         const int32_t kv_valid = min(kTileM, c.len - tl.m * kTileM);
@@ -504,7 +513,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const bool row_valid = r < kv_valid;
       const int64_t krow = (int64_t)c.r0 + tl.m * kTileM + r;
       int32_t j0, nq;
-      bwd_q_steps(c, tl.m, CAUSAL, j0, nq);
+      bwd_q_steps<MASKED>(c, tl.m, p, j0, nq);
       if (j0 == nq) {
         if (row_valid) {
           __nv_bfloat16* dvrow = p.dv + krow * p.dv_rs + (int64_t)tl.h * p.dv_hs;
@@ -516,13 +525,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         continue;
       }
-      // with the causal mask this key (index jr in the segment) is seen by q
-      // rows i >= jr - (Sk - Sq)
-      const int32_t q_first = CAUSAL ? tl.m * kTileM + r - (c.len - c.olen) : 0;
+      // q rows [q_lo, q_hi) of the segment see this key: all of them, or
+      // with a mask those whose band holds it
+      int32_t q_lo = 0, q_hi = c.olen;
+      if (MASKED) {
+        const int64_t jr = (int64_t)tl.m * kTileM + r;
+        band_rows(jr, jr, c.olen, c.len, p.win_left, p.win_right, &q_lo, &q_hi);
+      }
       for (int32_t j = j0; j < nq; ++j, ++gs) {
         const int32_t qc0 = j * QT + half * 64;             // first q column of this thread (in the segment)
-        const int32_t nvalid = row_valid ? max(0, min(64, c.olen - qc0)) : 0;
-        const int32_t lo = CAUSAL ? min(64, max(0, q_first - qc0)) : 0;  // columns [lo, nvalid) are visible
+        const int32_t nvalid = row_valid ? max(0, min(64, q_hi - qc0)) : 0;
+        const int32_t lo = MASKED ? min(64, max(0, q_lo - qc0)) : 0;  // columns [lo, nvalid) are visible
         // this step's lse2 / delta rows arrive with its Q / dO tiles
         const float4* l4 = reinterpret_cast<const float4*>(lse_rows + (gs % C::NQ) * QT + half * 64);
         const float4* d4 = reinterpret_cast<const float4*>(delta_rows + (gs % C::NDO) * QT + half * 64);
@@ -654,7 +667,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
          ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q); t += G) {
       const Tile tl = cursor_tile(c, t);
       int32_t j0, nq;
-      bwd_q_steps(c, tl.m, CAUSAL, j0, nq);
+      bwd_q_steps<MASKED>(c, tl.m, p, j0, nq);
       for (int32_t j = j0; j < nq; ++j, ++gs) {
         if (!mbar_wait(&bar.dq_full, gs & 1, abort)) { ok = false; break; }
         tc_fence_after();
@@ -716,14 +729,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (threadIdx.x == 0 && bar.abort) record_error(p.err, kErrTimeout);
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool MASKED>
 static cudaError_t launch_bwd_d(const BwdLaunch& L, cudaStream_t stream) {
   using C = BwdCfg<D>;
   const int elem_grid = L.grid * 8;
   auto mark = [&](int i) {
     if (L.phase_events[i] != nullptr) cudaEventRecord(L.phase_events[i], stream);
   };
-  auto kern = varlen_bwd_main_kernel<D, CAUSAL>;
+  auto kern = varlen_bwd_main_kernel<D, MASKED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   // The warpgroup register split assumes the kernel was compiled to exactly
@@ -749,9 +762,9 @@ static cudaError_t launch_bwd_d(const BwdLaunch& L, cudaStream_t stream) {
 
 cudaError_t launch_bwd(const BwdLaunch& L, cudaStream_t stream) {
   switch (L.head_dim) {
-    case 64: return L.p.causal ? launch_bwd_d<64, true>(L, stream) : launch_bwd_d<64, false>(L, stream);
-    case 96: return L.p.causal ? launch_bwd_d<96, true>(L, stream) : launch_bwd_d<96, false>(L, stream);
-    case 128: return L.p.causal ? launch_bwd_d<128, true>(L, stream) : launch_bwd_d<128, false>(L, stream);
+    case 64: return L.p.masked ? launch_bwd_d<64, true>(L, stream) : launch_bwd_d<64, false>(L, stream);
+    case 96: return L.p.masked ? launch_bwd_d<96, true>(L, stream) : launch_bwd_d<96, false>(L, stream);
+    case 128: return L.p.masked ? launch_bwd_d<128, true>(L, stream) : launch_bwd_d<128, false>(L, stream);
     default: return cudaErrorInvalidValue;
   }
 }

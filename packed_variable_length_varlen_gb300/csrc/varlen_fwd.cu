@@ -41,16 +41,23 @@ namespace varlen {
 
 constexpr int kFwdUnit = 2 * kTileM;  // q rows per scheduled unit (two halves)
 
-// kv tiles a unit (256 q rows of one segment and head) works through.  With
-// the causal mask (q row i of the segment sees keys j <= i + Sk - Sq) tiles
-// past the unit's last visible key are skipped; 0 means no row of the unit
-// sees a key (O = 0, LSE = -inf).  The cursor's scheduled side is q.
-__device__ __forceinline__ int32_t fwd_kv_tiles(const SegCursor& c, int32_t unit, int32_t causal) {
+// kv tiles [j_lo, j_lo + n) a unit (256 q rows of one segment and head)
+// works through, n returned.  With a mask (the band of FwdParams) only the
+// tiles holding keys that some row of the unit sees; 0 means no row of the
+// unit sees a key (O = 0, LSE = -inf).  The cursor's scheduled side is q.
+template <bool MASKED>
+__device__ __forceinline__ int32_t fwd_kv_tiles(const SegCursor& c, int32_t unit, const FwdParams& p,
+                                                int32_t& j_lo) {
+  j_lo = 0;
   int32_t nkv = (c.olen + kTileN - 1) / kTileN;
-  if (causal) {
-    const int32_t q_last = min(c.len, (unit + 1) * kFwdUnit) - 1;
-    const int32_t lim = q_last + (c.olen - c.len) + 1;  // keys the unit's last row sees
-    nkv = lim <= 0 ? 0 : min(nkv, (lim + kTileN - 1) / kTileN);
+  if (MASKED) {
+    const int64_t q0 = (int64_t)unit * kFwdUnit;
+    const int64_t q1 = min((int64_t)c.len, q0 + kFwdUnit) - 1;
+    int32_t lo, hi;
+    band_keys(q0, q1, c.len, c.olen, p.win_left, p.win_right, &lo, &hi);
+    if (hi <= lo) return 0;
+    j_lo = lo / kTileN;
+    nkv = (hi + kTileN - 1) / kTileN - j_lo;
   }
   return nkv;
 }
@@ -87,7 +94,7 @@ static_assert(kFwdRegsCtl + 2 * kFwdRegsSoftmax <= 3 * kFwdRegsLaunch,
               "warpgroup register split exceeds the launch allocation");
 static_assert(kFwdRegsLaunch * 384 <= 65536, "launch register count too large for 384 threads");
 
-template <int D, bool CAUSAL>
+template <int D, bool MASKED>
 __global__ void __launch_bounds__(384, 1)
     varlen_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -143,7 +150,8 @@ __global__ void __launch_bounds__(384, 1)
                                                                  p.total_q, p.total_k);
            t += G) {
         const Tile tl = cursor_tile(c, t);
-        const int32_t nkv = fwd_kv_tiles(c, tl.m, CAUSAL);
+        int32_t j_lo;
+        const int32_t nkv = fwd_kv_tiles<MASKED>(c, tl.m, p, j_lo);
         if (nkv == 0) continue;  // no visible keys: the softmax role writes O = 0, LSE = -inf
         const int32_t qrow = c.r0 + tl.m * kFwdUnit;
         if (q_loads > 0 && !mbar_wait(&bar.q_empty, (q_loads - 1) & 1, abort)) break;
@@ -156,7 +164,7 @@ __global__ void __launch_bounds__(384, 1)
                         qrow + hf * kTileM);
         ++q_loads;
         for (int32_t j = 0; ok && j < nkv; ++j) {
-          const int32_t krow = c.o0 + j * kTileN;
+          const int32_t krow = c.o0 + (j_lo + j) * kTileN;
 #pragma unroll
           for (int which = 0; which < 2; ++which) {
             const uint32_t slot = ring_pos % C::NSLOT;
@@ -223,7 +231,8 @@ __global__ void __launch_bounds__(384, 1)
     };
     for (int64_t t = blockIdx.x;
          ok && cursor_seek<kFwdUnit>(c, t, p.num_heads, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k); t += G) {
-      const int32_t nkv = fwd_kv_tiles(c, cursor_tile(c, t).m, CAUSAL);
+      int32_t j_lo;
+      const int32_t nkv = fwd_kv_tiles<MASKED>(c, cursor_tile(c, t).m, p, j_lo);
       if (nkv == 0) continue;
       if (!mbar_wait(&bar.q_full, tiles & 1, abort)) break;
       ++tiles;
@@ -245,7 +254,7 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t kpos = vpos + 1;
         const uint32_t kslot = kpos % C::NSLOT;
         if (!mbar_wait(&bar.kv_full[vslot], (vpos / C::NSLOT) & 1, abort)) { ok = false; break; }
-        const int32_t kv_valid = min(kTileN, c.olen - j * kTileN);
+        const int32_t kv_valid = min(kTileN, c.olen - (j_lo + j) * kTileN);
         const int nk = (kv_valid + 15) >> 4;
         if (kv_valid < kTileN) {
           // Rows past the segment end hold the next segment's values (or
@@ -299,7 +308,8 @@ __global__ void __launch_bounds__(384, 1)
     for (int64_t t = blockIdx.x;
          ok && cursor_seek<kFwdUnit>(c, t, p.num_heads, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k); t += G) {
       const Tile tl = cursor_tile(c, t);
-      const int32_t nkv = fwd_kv_tiles(c, tl.m, CAUSAL);
+      int32_t j_lo;
+      const int32_t nkv = fwd_kv_tiles<MASKED>(c, tl.m, p, j_lo);
       if (nkv == 0) {
         const int32_t r_in_seg = tl.m * kFwdUnit + hf * kTileM + row;
         const int64_t grow = (int64_t)c.r0 + r_in_seg;
@@ -312,10 +322,10 @@ __global__ void __launch_bounds__(384, 1)
         }
         continue;
       }
-      // keys this row sees: all Sk, or with the causal mask those with index
-      // <= r + Sk - Sq (r = the row's index within the segment)
+      // keys [key_lo, key_hi) this row sees: all Sk, or with a mask its band
       const int32_t r_seg = tl.m * kFwdUnit + hf * kTileM + row;
-      const int32_t row_keys = CAUSAL ? min(c.olen, max(0, r_seg + (c.olen - c.len) + 1)) : c.olen;
+      int32_t key_lo = 0, key_hi = c.olen;
+      if (MASKED) band_keys(r_seg, r_seg, c.len, c.olen, p.win_left, p.win_right, &key_lo, &key_hi);
       float m_use = -INFINITY, l = 0.f;
       for (int32_t j = 0; j < nkv; ++j) {
         const uint32_t gj = g + j;
@@ -337,10 +347,14 @@ __global__ void __launch_bounds__(384, 1)
         float x[128];
 #pragma unroll
         for (int i = 0; i < 128; ++i) x[i] = __uint_as_float(s[i]);
-        // columns past the row's last visible key (the segment end, or the
-        // causal diagonal) are masked to -inf by select
-        const int32_t lim = row_keys - j * kTileN;  // per thread
-        if (__any_sync(0xffffffffu, lim < kTileN)) {
+        // columns outside the row's visible keys (past the segment end, or
+        // outside the mask's band) are set to -inf by select
+        const int32_t lim = key_hi - (j_lo + j) * kTileN;  // per thread
+        const int32_t lim_lo = key_lo - (j_lo + j) * kTileN;
+        if (MASKED && __any_sync(0xffffffffu, lim_lo > 0)) {  // the band's left edge crosses this tile
+#pragma unroll
+          for (int i = 0; i < 128; ++i) x[i] = (i < lim && i >= lim_lo) ? x[i] : -INFINITY;
+        } else if (__any_sync(0xffffffffu, lim < kTileN)) {
 #pragma unroll
           for (int i = 0; i < 128; ++i) x[i] = (i < lim) ? x[i] : -INFINITY;
         }
@@ -370,7 +384,7 @@ __global__ void __launch_bounds__(384, 1)
         // [32h, 32h+32), whose S values were consumed already.
         // a row that has seen no key yet keeps m = -inf; subtracting 0 then
         // gives P = exp2(-inf) = 0 instead of NaN
-        const float m_sub = (CAUSAL && m_use == -INFINITY) ? 0.f : m_use;
+        const float m_sub = (MASKED && m_use == -INFINITY) ? 0.f : m_use;
         const float2 cc2 = make_float2(c2, c2), negm = make_float2(-m_sub, -m_sub);
         float2 rs2a = make_float2(0.f, 0.f), rs2b = make_float2(0.f, 0.f);
 #pragma unroll
@@ -416,7 +430,7 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t gl = g + nkv - 1;
       if (!mbar_wait(&bar.pv_done[hf], gl & 1, abort)) break;
       tc_fence_after();
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;  // l = 0: the row saw no key (causal): O = 0
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;  // l = 0: the row saw no key (masked): O = 0
 #pragma unroll
       for (int d0 = 0; d0 < D; d0 += 32) {
         uint32_t o[32];
@@ -447,10 +461,10 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0 && bar.abort) record_error(p.err, kErrTimeout);
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool MASKED>
 static cudaError_t launch_fwd_d(const FwdLaunch& L, cudaStream_t stream) {
   using C = FwdCfg<D>;
-  auto kern = varlen_fwd_kernel<D, CAUSAL>;
+  auto kern = varlen_fwd_kernel<D, MASKED>;
   // The warpgroup register split assumes the compiled per-thread count;
   // refuse to launch a build that came out differently.
   cudaFuncAttributes fa;
@@ -465,9 +479,9 @@ static cudaError_t launch_fwd_d(const FwdLaunch& L, cudaStream_t stream) {
 
 cudaError_t launch_fwd(const FwdLaunch& L, cudaStream_t stream) {
   switch (L.head_dim) {
-    case 64: return L.p.causal ? launch_fwd_d<64, true>(L, stream) : launch_fwd_d<64, false>(L, stream);
-    case 96: return L.p.causal ? launch_fwd_d<96, true>(L, stream) : launch_fwd_d<96, false>(L, stream);
-    case 128: return L.p.causal ? launch_fwd_d<128, true>(L, stream) : launch_fwd_d<128, false>(L, stream);
+    case 64: return L.p.masked ? launch_fwd_d<64, true>(L, stream) : launch_fwd_d<64, false>(L, stream);
+    case 96: return L.p.masked ? launch_fwd_d<96, true>(L, stream) : launch_fwd_d<96, false>(L, stream);
+    case 128: return L.p.masked ? launch_fwd_d<128, true>(L, stream) : launch_fwd_d<128, false>(L, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -24,6 +24,36 @@ struct CuView {
   int32_t uni;
 };
 
+// Visibility band of a masked launch.  With d = Sk - Sq of a segment, its q
+// row i (0-based) sees the keys j (0-based) with
+//     i + d - win_left  <=  j  <=  i + d + win_right;
+// an unbounded side holds kWinUnbounded, so one formula serves every mask
+// (causal: win_left unbounded, win_right 0).
+constexpr int64_t kWinUnbounded = int64_t(1) << 40;
+
+// Keys [*lo, *hi) of a segment (Sq q rows, Sk keys) seen by at least one of
+// its q rows i0..i1; *lo == *hi when none.
+__host__ __device__ __forceinline__ void band_keys(int64_t i0, int64_t i1, int32_t Sq, int32_t Sk, int64_t win_left,
+                                                   int64_t win_right, int32_t* lo, int32_t* hi) {
+  const int64_t d = (int64_t)Sk - Sq;
+  int64_t a = i0 + d - win_left, e = i1 + d + win_right + 1;
+  a = a < 0 ? 0 : (a > Sk ? Sk : a);
+  e = e < a ? a : (e > Sk ? Sk : e);
+  *lo = (int32_t)a;
+  *hi = (int32_t)e;
+}
+
+// q rows [*lo, *hi) of a segment that see at least one of its keys j0..j1.
+__host__ __device__ __forceinline__ void band_rows(int64_t j0, int64_t j1, int32_t Sq, int32_t Sk, int64_t win_left,
+                                                   int64_t win_right, int32_t* lo, int32_t* hi) {
+  const int64_t d = (int64_t)Sk - Sq;
+  int64_t a = j0 - d - win_right, e = j1 - d + win_left + 1;
+  a = a < 0 ? 0 : (a > Sq ? Sq : a);
+  e = e < a ? a : (e > Sq ? Sq : e);
+  *lo = (int32_t)a;
+  *hi = (int32_t)e;
+}
+
 constexpr int kTileM = 128;  // q rows per forward tile / kv rows per backward tile
 constexpr int kTileN = 128;  // kv rows per forward inner step
 constexpr int kBwdTileQ = 128; // q rows per backward inner step
@@ -35,7 +65,8 @@ struct FwdParams {
   CuView cu_q;
   CuView cu_k;
   int32_t batch, total_q, total_k, num_heads;
-  int32_t causal;    // 1: q row i of a segment sees keys j <= i + Sk - Sq
+  int32_t masked;              // 0: every key of the segment is visible
+  int64_t win_left, win_right; // the band when masked (kWinUnbounded: that side open)
   float scale_log2;  // softmax scale * log2(e)
   unsigned int* err; // device error word
 };
@@ -74,7 +105,8 @@ struct BwdParams {
   CuView cu_q;
   CuView cu_k;
   int32_t batch, total_q, total_k, num_heads;
-  int32_t causal;    // 1: q row i of a segment sees keys j <= i + Sk - Sq
+  int32_t masked;              // 0: every key of the segment is visible
+  int64_t win_left, win_right; // the band when masked (kWinUnbounded: that side open)
   int64_t pad_rows;
   float scale_log2;  // softmax scale * log2(e)
   float scale;       // softmax scale (applied to dK)

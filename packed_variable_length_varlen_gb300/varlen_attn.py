@@ -70,6 +70,12 @@ def _load() -> ctypes.CDLL:
     lib.varlen_attn_fwd_causal.argtypes = lib.varlen_attn_fwd.argtypes
     lib.varlen_attn_bwd_causal.restype = ctypes.c_int
     lib.varlen_attn_bwd_causal.argtypes = lib.varlen_attn_bwd.argtypes
+    lib.varlen_attn_fwd_window.restype = ctypes.c_int
+    lib.varlen_attn_fwd_window.argtypes = [vp, S, vp, S, vp, S, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32,
+                                           i32, i32, vp, S, vp, vp]
+    lib.varlen_attn_bwd_window.restype = ctypes.c_int
+    lib.varlen_attn_bwd_window.argtypes = [vp, S, vp, S, vp, S, vp, S, vp, S, vp, vp, vp, i32, i32, i32, i32, i32,
+                                           i32, i32, f32, i32, i32, vp, S, vp, S, vp, S, vp, sz, vp]
     DS = VarlenDenseStride
     lib.varlen_attn_fwd_dense.restype = ctypes.c_int
     lib.varlen_attn_fwd_dense.argtypes = [vp, DS, vp, DS, vp, DS, i32, i32, i32, i32, i32, f32, i32, vp, DS, vp, vp]
@@ -108,7 +114,8 @@ EXPORTED = ("varlen_attn_fwd", "varlen_attn_bwd_workspace_size", "varlen_attn_bw
             "varlen_attn_debug_schedule", "varlen_attn_selftest_wait_timeout", "varlen_attn_num_sms",
             "varlen_attn_debug_set_phase_events", "varlen_attn_bwd_noalloc", "varlen_attn_last_cuda_error",
             "varlen_attn_fwd_causal", "varlen_attn_bwd_causal", "varlen_attn_fwd_dense",
-            "varlen_attn_bwd_dense_workspace_size", "varlen_attn_bwd_dense")
+            "varlen_attn_bwd_dense_workspace_size", "varlen_attn_bwd_dense", "varlen_attn_fwd_window",
+            "varlen_attn_bwd_window")
 
 # Size of the fixed device array varlen_attn_bwd_noalloc uses as scratch.
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -146,12 +153,37 @@ def _stream(stream):
 
 # ---------------------------------------------------------------- raw ABI
 
+def _band(causal, window):
+    """(left, right) of the window entry points for `causal` / `window`
+    (causal sets right = 0), or None when neither masks anything."""
+    left, right = int(window[0]), int(window[1])
+    if causal:
+        right = 0
+    if left < 0 and right < 0:
+        return None
+    return max(left, -1), max(right, -1)
+
+
 def varlen_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads, head_dim,
-                    max_seqlen_q, max_seqlen_k, scale, out, lse, stream=None, causal=False) -> int:
-    fn = LIB.varlen_attn_fwd_causal if causal else LIB.varlen_attn_fwd
-    return fn(_ptr(q), _stride(q), _ptr(k), _stride(k), _ptr(v), _stride(v), _ptr(cu_seqlens_q),
-              _ptr(cu_seqlens_k), batch, total_q, total_k, num_heads, head_dim, max_seqlen_q, max_seqlen_k, scale,
-              _ptr(out), _stride(out), _ptr(lse), _stream(stream))
+                    max_seqlen_q, max_seqlen_k, scale, out, lse, stream=None, causal=False, window=(-1, -1)) -> int:
+    band = _band(causal, window)
+    head = (_ptr(q), _stride(q), _ptr(k), _stride(k), _ptr(v), _stride(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+            batch, total_q, total_k, num_heads, head_dim, max_seqlen_q, max_seqlen_k, scale)
+    tail = (_ptr(out), _stride(out), _ptr(lse), _stream(stream))
+    if band is None:
+        return LIB.varlen_attn_fwd(*head, *tail)
+    if band == (-1, 0):
+        return LIB.varlen_attn_fwd_causal(*head, *tail)
+    return LIB.varlen_attn_fwd_window(*head, *band, *tail)
+
+
+def varlen_attn_fwd_window(q, k, v, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads, head_dim,
+                           max_seqlen_q, max_seqlen_k, scale, window_left, window_right, out, lse,
+                           stream=None) -> int:
+    return LIB.varlen_attn_fwd_window(_ptr(q), _stride(q), _ptr(k), _stride(k), _ptr(v), _stride(v),
+                                      _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), batch, total_q, total_k, num_heads,
+                                      head_dim, max_seqlen_q, max_seqlen_k, scale, window_left, window_right,
+                                      _ptr(out), _stride(out), _ptr(lse), _stream(stream))
 
 
 def varlen_attn_fwd_causal(q, k, v, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads, head_dim,
@@ -166,12 +198,29 @@ def varlen_attn_bwd_workspace_size(batch, total_q, num_heads, head_dim) -> int:
 
 def varlen_attn_bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads,
                     head_dim, max_seqlen_q, max_seqlen_k, scale, dq, dk, dv, workspace, workspace_bytes,
-                    stream=None, causal=False) -> int:
-    fn = LIB.varlen_attn_bwd_causal if causal else LIB.varlen_attn_bwd
-    return fn(_ptr(q), _stride(q), _ptr(k), _stride(k), _ptr(v), _stride(v), _ptr(out), _stride(out), _ptr(dout),
-              _stride(dout), _ptr(lse), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), batch, total_q, total_k, num_heads,
-              head_dim, max_seqlen_q, max_seqlen_k, scale, _ptr(dq), _stride(dq), _ptr(dk), _stride(dk), _ptr(dv),
-              _stride(dv), _ptr(workspace), workspace_bytes, _stream(stream))
+                    stream=None, causal=False, window=(-1, -1)) -> int:
+    band = _band(causal, window)
+    head = (_ptr(q), _stride(q), _ptr(k), _stride(k), _ptr(v), _stride(v), _ptr(out), _stride(out), _ptr(dout),
+            _stride(dout), _ptr(lse), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), batch, total_q, total_k, num_heads,
+            head_dim, max_seqlen_q, max_seqlen_k, scale)
+    tail = (_ptr(dq), _stride(dq), _ptr(dk), _stride(dk), _ptr(dv), _stride(dv), _ptr(workspace), workspace_bytes,
+            _stream(stream))
+    if band is None:
+        return LIB.varlen_attn_bwd(*head, *tail)
+    if band == (-1, 0):
+        return LIB.varlen_attn_bwd_causal(*head, *tail)
+    return LIB.varlen_attn_bwd_window(*head, *band, *tail)
+
+
+def varlen_attn_bwd_window(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k,
+                           num_heads, head_dim, max_seqlen_q, max_seqlen_k, scale, window_left, window_right, dq, dk,
+                           dv, workspace, workspace_bytes, stream=None) -> int:
+    return LIB.varlen_attn_bwd_window(_ptr(q), _stride(q), _ptr(k), _stride(k), _ptr(v), _stride(v), _ptr(out),
+                                      _stride(out), _ptr(dout), _stride(dout), _ptr(lse), _ptr(cu_seqlens_q),
+                                      _ptr(cu_seqlens_k), batch, total_q, total_k, num_heads, head_dim,
+                                      max_seqlen_q, max_seqlen_k, scale, window_left, window_right, _ptr(dq),
+                                      _stride(dq), _ptr(dk), _stride(dk), _ptr(dv), _stride(dv), _ptr(workspace),
+                                      workspace_bytes, _stream(stream))
 
 
 def varlen_attn_bwd_causal(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k,
@@ -268,9 +317,10 @@ def _check(status, where):
 
 
 def attention_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q=0, max_seqlen_k=0, scale=None,
-                  out=None, lse=None, stream=None, causal=False):
+                  out=None, lse=None, stream=None, causal=False, window=(-1, -1)):
     """O and LSE for packed q/k/v ([rows, H, D] bf16 on one CUDA device);
-    `causal` selects varlen_attn_fwd_causal."""
+    `causal` / `window` = (left, right) select the masked entry points
+    (causal sets right = 0; a negative side is unbounded)."""
     total_q, H, D = q.shape
     total_k = k.shape[0]
     batch = cu_seqlens_q.numel() - 1
@@ -280,12 +330,13 @@ def attention_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q=0, max_seqle
     if lse is None:
         lse = torch.empty(H, total_q, dtype=torch.float32, device=q.device)
     _check(varlen_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, H, D, max_seqlen_q,
-                           max_seqlen_k, scale, out, lse, stream, causal), "varlen_attn_fwd")
+                           max_seqlen_k, scale, out, lse, stream, causal, window), "varlen_attn_fwd")
     return out, lse
 
 
 def attention_bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q=0, max_seqlen_k=0,
-                  scale=None, dq=None, dk=None, dv=None, workspace=None, stream=None, causal=False):
+                  scale=None, dq=None, dk=None, dv=None, workspace=None, stream=None, causal=False,
+                  window=(-1, -1)):
     """dQ, dK, dV for the forward above (every operand keeps its strides)."""
     total_q, H, D = q.shape
     total_k = k.shape[0]
@@ -299,7 +350,7 @@ def attention_bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, max_seqle
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
     _check(varlen_attn_bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, H, D,
                            max_seqlen_q, max_seqlen_k, scale, dq, dk, dv, workspace, workspace.numel(), stream,
-                           causal), "varlen_attn_bwd")
+                           causal, window), "varlen_attn_bwd")
     return dq, dk, dv
 
 

@@ -94,25 +94,25 @@ class Workload:
         """sum_b Sq_b * Sk_b (per head)."""
         return sum(a * b for a, b in zip(self.seqlens_q(), self.seqlens_k()))
 
-    def visible_pairs(self, causal: bool = False) -> int:
+    def visible_pairs(self, causal: bool = False, window=(-1, -1)) -> int:
         """(query, key) pairs that take part, per head: sum_b Sq_b * Sk_b, or
-        with the causal mask (q row i of a segment sees keys
-        j <= i + Sk - Sq) sum_b sum_i clamp(i + Sk_b - Sq_b + 1, 0, Sk_b)."""
-        if not causal:
+        with a mask the sum over rows of row_keys (the keys in each row's
+        band)."""
+        if not causal and window[0] < 0 and window[1] < 0:
             return self.pair_products()
         tot = 0
         for sq, sk in zip(self.seqlens_q(), self.seqlens_k()):
             if sq > 0 and sk > 0:
-                tot += int(np.clip(np.arange(sq, dtype=np.int64) + (sk - sq) + 1, 0, sk).sum())
+                tot += int(row_keys(np.arange(sq, dtype=np.int64), sq, sk, causal, window).sum())
         return tot
 
-    def fwd_flops(self, causal: bool = False) -> float:
+    def fwd_flops(self, causal: bool = False, window=(-1, -1)) -> float:
         """4 * (visible pairs) * H * D: two matmuls of 2 flops per MAC."""
-        return 4.0 * self.visible_pairs(causal) * self.num_heads * self.head_dim
+        return 4.0 * self.visible_pairs(causal, window) * self.num_heads * self.head_dim
 
-    def bwd_flops(self, causal: bool = False) -> float:
+    def bwd_flops(self, causal: bool = False, window=(-1, -1)) -> float:
         """2.5 x the forward count (five matmuls instead of two)."""
-        return 2.5 * self.fwd_flops(causal)
+        return 2.5 * self.fwd_flops(causal, window)
 
     def q_tiles(self, tile: int = TILE_ROWS) -> int:
         """Exact tile count H * sum_b ceil(Sq_b / tile)."""
@@ -122,6 +122,22 @@ class Workload:
         d = dict(self.__dict__)
         d.update(kw)
         return Workload(**d)
+
+
+def row_keys(ii, sq, sk, causal: bool = False, window=(-1, -1)):
+    """Number of keys q rows `ii` (0-based within a segment of sq rows and sk
+    keys) see: row i sees the keys j with i + sk - sq - left <= j <=
+    i + sk - sq + right, a negative side unbounded, causal setting right = 0
+    (all sk without a mask).  Array arguments broadcast."""
+    left, right = int(window[0]), int(window[1])
+    if causal:
+        right = 0
+    ii = np.asarray(ii, dtype=np.int64)
+    sq, sk = np.asarray(sq, dtype=np.int64), np.asarray(sk, dtype=np.int64)
+    diag = ii + (sk - sq)
+    lo = np.clip(diag - left, 0, sk) if left >= 0 else np.zeros_like(diag)
+    hi = np.clip(diag + right + 1, 0, sk) if right >= 0 else np.broadcast_to(sk, diag.shape)
+    return np.maximum(hi - lo, 0)
 
 
 def _cu(lengths):

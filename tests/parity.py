@@ -53,14 +53,14 @@ def gather(t: torch.Tensor, rows: np.ndarray, heads: np.ndarray) -> np.ndarray:
 
 
 def run_fwd(inp_dev: W.Inputs, out: torch.Tensor, lse: torch.Tensor, max_seqlen_q=None, max_seqlen_k=None,
-            causal=False):
+            causal=False, window=(-1, -1)):
     from packed_variable_length_varlen_gb300 import varlen_attn as va
     w = inp_dev.workload
     st = va.varlen_attn_fwd(inp_dev.q, inp_dev.k, inp_dev.v, inp_dev.cu_q, inp_dev.cu_k, w.batch, w.total_q,
                             w.total_k, w.num_heads, w.head_dim,
                             w.max_q() if max_seqlen_q is None else max_seqlen_q,
                             w.max_k() if max_seqlen_k is None else max_seqlen_k,
-                            w.softmax_scale, out, lse, causal=causal)
+                            w.softmax_scale, out, lse, causal=causal, window=window)
     assert st == 0, (va.varlen_attn_status_string(st), va.varlen_attn_last_cuda_error())
     st = va.varlen_attn_get_device_status()
     assert st == 0, va.varlen_attn_status_string(st)
@@ -128,10 +128,10 @@ def rel_fro(a: np.ndarray, ref: np.ndarray) -> float:
     return float(np.linalg.norm(a - ref) / n)
 
 
-def oracle_problem(inp_cpu: W.Inputs, causal=False) -> oracle.Problem:
+def oracle_problem(inp_cpu: W.Inputs, causal=False, window=(-1, -1)) -> oracle.Problem:
     w = inp_cpu.workload
     return oracle.Problem(inp_cpu.q, inp_cpu.k, inp_cpu.v, inp_cpu.cu_q, inp_cpu.cu_k, w.softmax_scale,
-                          dout=inp_cpu.dout, causal=causal)
+                          dout=inp_cpu.dout, causal=causal, window=window)
 
 
 def padding_untouched(t_dev: torch.Tensor, w: W.Workload, canary: float) -> bool:

@@ -10,6 +10,8 @@ import re
 import numpy as np
 import pytest
 
+from packed_variable_length_varlen_gb300 import workloads as W
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "varlen_attn.h")
 GOLDEN = os.path.join(ROOT, "tests", "golden", "page_values.json")
@@ -183,3 +185,19 @@ def test_dense_validation_codes(va):
     assert fwd() in (va.VARLEN_ERR_CUDA, va.VARLEN_ERR_ARCH)
     assert va.varlen_attn_bwd_dense_workspace_size(B, Sq, H, D) == va.varlen_attn_bwd_workspace_size(B, B * Sq, H, D)
     assert va.varlen_attn_bwd_dense_workspace_size(2 ** 16, 2 ** 16, H, D) == 0
+
+
+def test_visible_pairs_band_by_brute_force():
+    """The pair count the benchmark credits for a mask, against a double loop
+    over (query, key) with the band written as two comparisons."""
+    w = W.custom("band", [7, 0, 5, 9, 1], [7, 4, 9, 3, 0], 1, 64)
+    for causal, window in ((False, (-1, -1)), (True, (-1, -1)), (False, (2, 1)), (False, (0, 0)),
+                           (True, (3, 7)), (False, (-1, 2)), (False, (4, -1))):
+        left, right = window[0], 0 if causal else window[1]
+        n = 0
+        for sq, sk in zip(w.seqlens_q(), w.seqlens_k()):
+            for i in range(sq):
+                for j in range(sk):
+                    d = i + sk - sq
+                    n += (left < 0 or j >= d - left) and (right < 0 or j <= d + right)
+        assert w.visible_pairs(causal, window) == n, (causal, window)
