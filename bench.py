@@ -231,8 +231,9 @@ def ours(args, w, ws, rank, local):
         sq_, sk_ = w.seqlens_q(), w.seqlens_k()
         if len(set(sq_)) != 1 or len(set(sk_)) != 1:
             raise SystemExit("--dense needs a workload with equal segment lengths (e.g. --workload dense)")
-        if _window(args) != (-1, -1):
-            raise SystemExit("--dense takes no --window (the dense entry points carry the causal flag only)")
+        if _window(args) != (-1, -1) or args.deterministic:
+            raise SystemExit("--dense takes neither --window nor --deterministic (the dense entry points carry "
+                             "the causal flag only)")
         Sq, Sk = sq_[0], sk_[0]
         ws_bytes = va.varlen_attn_bwd_dense_workspace_size(w.batch, Sq, H, D)
         wsp = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
@@ -257,7 +258,7 @@ def ours(args, w, ws, rank, local):
         else:
             st = va.varlen_attn_bwd(x.q, x.k, x.v, o, x.dout, l, x.cu_q, x.cu_k, w.batch, w.total_q,
                                     w.total_k, H, D, w.max_q(), w.max_k(), scale, gq, gk, gv, wsp, ws_bytes, stream,
-                                    causal=args.causal, window=_window(args))
+                                    causal=args.causal, window=_window(args), deterministic=args.deterministic)
         assert st == 0, va.varlen_attn_status_string(st)
 
     def fwd():
@@ -420,6 +421,11 @@ def ours(args, w, ws, rank, local):
         t_main = statistics.mean(pev[i][1].elapsed_time(pev[i][2]) for i in range(K))
         t_post = statistics.mean(pev[i][2].elapsed_time(pev[i][3]) for i in range(K))
         dom_name, dom_flops, dom_ms = "varlen_bwd_main_kernel", f_bwd, t_main
+        if args.deterministic:
+            # The main kernel runs four of the five products (S^T, dP^T, dV, dK);
+            # the dQ kernel recomputes S and dP and runs dQ (three, 0.6 x the
+            # backward's algorithmic flops).
+            dom_flops = 0.8 * f_bwd
     else:
         dom_name, dom_flops, dom_ms = "varlen_fwd_kernel", f_fwd, statistics.mean(t_fwd)
     ach = dom_flops / (dom_ms * 1e-3) / 1e12
@@ -454,14 +460,16 @@ def ours(args, w, ws, rank, local):
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "batch_segments": w.batch, "total_q": w.total_q, "total_k": w.total_k,
                    "num_heads": H, "head_dim": D, "step": "fwd+bwd" if has_bwd else "fwd only (bwd missing)",
-                   "causal": bool(args.causal), "window": list(_window(args)), "entry": "dense batched" if args.dense else "packed varlen",
+                   "causal": bool(args.causal), "window": list(_window(args)),
+                   "deterministic_bwd": bool(args.deterministic), "entry": "dense batched" if args.dense else "packed varlen",
                    "l2": "inputs larger than L2 (k, v 2 GB each); no flush",
                    "parallelism": "replicas" if ws > 1 else "single GPU"},
         "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
         "fwd_frac_of_burst_peak": fwd_tflops / burst,
         "bwd_frac_of_burst_peak": (bwd_tflops / burst) if bwd_tflops else None,
         "fwd_ms": statistics.mean(t_fwd), "bwd_ms": statistics.mean(t_bwd) if has_bwd else None,
-        "bwd_kernel_ms": {"prep": t_prep, "main": t_main, "post": t_post} if has_bwd else None,
+        "bwd_kernel_ms": ({"prep": t_prep, "main": t_main, ("dq" if args.deterministic else "post"): t_post}
+                          if has_bwd else None),
         "fwd_kernel_roofline": {"achieved": fwd_tflops, "peak": peak, "frac": fwd_tflops / peak,
                                 "frac_of_sustained": fwd_tflops / sust},
         "clocks": clocks, "e2e": e2e, "gpu_launches": K * (1 + (3 if has_bwd else 0)),
@@ -483,6 +491,8 @@ def main():
                     help="time the causal entry points (FLOPs counted over visible pairs only)")
     ap.add_argument("--window", type=int, nargs=2, metavar=("LEFT", "RIGHT"), default=None,
                     help="time the sliding-window entry points with this band (a negative side is unbounded)")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="time the deterministic backward (dQ without atomics, a second q-major kernel)")
     ap.add_argument("--dense", action="store_true",
                     help="drive the dense batched entry points (needs equal segment lengths, e.g. --workload dense)")
     ap.add_argument("--no-e2e", action="store_true")

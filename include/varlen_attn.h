@@ -168,6 +168,27 @@ int varlen_attn_bwd_window(const void* q, varlen_stride sq, const void* k, varle
                            size_t workspace_bytes, void* stream);
 
 /*
+ * Deterministic backward (not on the pages; a plain extension): the same
+ * arguments, layouts, ownership, errors and band as varlen_attn_bwd_window
+ * (window_left = window_right = -1 for no mask, (-1, 0) for causal), and the
+ * same workspace (varlen_attn_bwd_workspace_size bytes).  dK and dV come from
+ * the main backward kernel without its dQ products; dQ comes from a second,
+ * q-major kernel that recomputes S and dP per kv tile and accumulates dQ in
+ * on-chip memory in a fixed kv order, with no atomics.  Repeated calls on the
+ * same inputs return the same bits for dQ, dK and dV (varlen_attn_bwd's dQ
+ * may differ in its last bits from run to run).  Costs two extra matrix
+ * products per (q tile, kv tile) pair.
+ */
+int varlen_attn_bwd_deterministic(const void* q, varlen_stride sq, const void* k, varlen_stride sk, const void* v,
+                                  varlen_stride sv, const void* out, varlen_stride so, const void* dout,
+                                  varlen_stride sdo, const float* lse, const int32_t* cu_seqlens_q,
+                                  const int32_t* cu_seqlens_k, int32_t batch, int32_t total_q, int32_t total_k,
+                                  int32_t num_heads, int32_t head_dim, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                                  float scale, int32_t window_left, int32_t window_right, void* dq,
+                                  varlen_stride sdq, void* dk, varlen_stride sdk, void* dv, varlen_stride sdv,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Dense batched attention: q, out, dout, dq are [batch, seqlen_q, H, D] and
  * k, v, dk, dv are [batch, seqlen_k, H, D] (bf16), each with its own strides
  * in elements and a unit innermost stride; lse is [H, batch * seqlen_q]

@@ -266,7 +266,7 @@ int bwd_impl(const void* q, varlen_stride sq, const void* k, varlen_stride sk, c
              CuView cu_q, CuView cu_k, int32_t batch, int32_t total_q, int32_t total_k, int32_t num_heads,
              int32_t head_dim, int32_t max_seqlen_q, int32_t max_seqlen_k, float scale, void* dq, varlen_stride sdq,
              void* dk, varlen_stride sdk, void* dv, varlen_stride sdv, void* workspace, size_t workspace_bytes,
-             void* stream, Band band) {
+             void* stream, Band band, int deterministic = 0) {
   (void)max_seqlen_q;
   (void)max_seqlen_k;
   int st = check_common(batch, total_q, total_k, num_heads, head_dim, scale);
@@ -302,7 +302,8 @@ int bwd_impl(const void* q, varlen_stride sq, const void* k, varlen_stride sk, c
   if ((st = encode_dq_acc(&L.tm_dq, dq_acc, total_q, num_heads, head_dim)) != VARLEN_OK) return st;
   L.prep = PrepParams{static_cast<const __nv_bfloat16*>(out), so.row, so.head,
                       static_cast<const __nv_bfloat16*>(dout), sdo.row, sdo.head,
-                      lse, delta, lse2, dq_acc, cu_q, batch, total_q, num_heads, head_dim, pad_rows};
+                      lse, delta, lse2, deterministic ? nullptr : dq_acc, cu_q, batch, total_q, num_heads,
+                      head_dim, pad_rows};
   L.p.dk = static_cast<__nv_bfloat16*>(dk);
   L.p.dk_rs = sdk.row;
   L.p.dk_hs = sdk.head;
@@ -312,6 +313,9 @@ int bwd_impl(const void* q, varlen_stride sq, const void* k, varlen_stride sk, c
   L.p.delta = delta;
   L.p.lse2 = lse2;
   L.p.dq_acc = dq_acc;
+  L.p.dq = static_cast<__nv_bfloat16*>(dq);
+  L.p.dq_rs = sdq.row;
+  L.p.dq_hs = sdq.head;
   L.p.cu_q = cu_q;
   L.p.cu_k = cu_k;
   L.p.batch = batch;
@@ -329,6 +333,7 @@ int bwd_impl(const void* q, varlen_stride sq, const void* k, varlen_stride sk, c
                       total_q, num_heads, head_dim, scale};
   L.head_dim = head_dim;
   L.grid = dev.sms;
+  L.deterministic = deterministic;
   {
     std::lock_guard<std::mutex> lock(g_phase_mu);
     for (int i = 0; i < 4; ++i) L.phase_events[i] = g_phase_events[i];
@@ -379,6 +384,19 @@ extern "C" int varlen_attn_bwd_window(const void* q, varlen_stride sq, const voi
   return bwd_impl(q, sq, k, sk, v, sv, out, so, dout, sdo, lse, CuView{cu_seqlens_q, 0}, CuView{cu_seqlens_k, 0},
                   batch, total_q, total_k, num_heads, head_dim, max_seqlen_q, max_seqlen_k, scale, dq, sdq, dk, sdk,
                   dv, sdv, workspace, workspace_bytes, stream, band_of(window_left, window_right));
+}
+
+extern "C" int varlen_attn_bwd_deterministic(
+    const void* q, varlen_stride sq, const void* k, varlen_stride sk, const void* v, varlen_stride sv,
+    const void* out, varlen_stride so, const void* dout, varlen_stride sdo, const float* lse,
+    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t batch, int32_t total_q, int32_t total_k,
+    int32_t num_heads, int32_t head_dim, int32_t max_seqlen_q, int32_t max_seqlen_k, float scale,
+    int32_t window_left, int32_t window_right, void* dq, varlen_stride sdq, void* dk, varlen_stride sdk, void* dv,
+    varlen_stride sdv, void* workspace, size_t workspace_bytes, void* stream) {
+  if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr) return VARLEN_ERR_NULL;
+  return bwd_impl(q, sq, k, sk, v, sv, out, so, dout, sdo, lse, CuView{cu_seqlens_q, 0}, CuView{cu_seqlens_k, 0},
+                  batch, total_q, total_k, num_heads, head_dim, max_seqlen_q, max_seqlen_k, scale, dq, sdq, dk, sdk,
+                  dv, sdv, workspace, workspace_bytes, stream, band_of(window_left, window_right), 1);
 }
 
 // ------------------------------------------------------------ dense batched

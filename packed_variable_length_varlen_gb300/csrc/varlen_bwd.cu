@@ -43,14 +43,6 @@
 
 namespace varlen {
 
-// First index of segment b's entries in the padded per-row arrays (delta,
-// lse2): a multiple of 4 (16 bytes), at least the previous segment's end for
-// non-decreasing cu_seqlens, and below bwd_pad_rows() - 127 - len_b for any
-// cu_seqlens (len_b + o0 <= total_q).
-__device__ __forceinline__ int64_t pad_base(int32_t o0, int32_t b) {
-  return 4 * (((int64_t)o0 + 3) / 4) + 4 * (int64_t)b;
-}
-
 // ------------------------------------------------------------------ prep
 
 __global__ void __launch_bounds__(256) varlen_bwd_prep_kernel(const PrepParams p) {
@@ -95,8 +87,10 @@ __global__ void __launch_bounds__(256) varlen_bwd_prep_kernel(const PrepParams p
       p.delta[idx] = acc;
       p.lse2[idx] = __ldg(p.lse + (int64_t)h * p.total_q + row) * kLog2e;
     }
-    float4* z = reinterpret_cast<float4*>(p.dq_acc + ((int64_t)row * H + h) * D);
-    for (int d = 0; d < D; d += 4) *z++ = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (p.dq_acc != nullptr) {
+      float4* z = reinterpret_cast<float4*>(p.dq_acc + ((int64_t)row * H + h) * D);
+      for (int d = 0; d < D; d += 4) *z++ = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
 }
 
@@ -205,7 +199,7 @@ __device__ __forceinline__ void clear_rows(uint8_t* tile, int chunks, int chunk_
   }
 }
 
-template <int D, bool MASKED>
+template <int D, bool MASKED, bool DQ>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     varlen_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -243,14 +237,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&bar.q_full[i], 1);
       mbar_init(&bar.q_empty[i], 1);
       mbar_init(&bar.do_full[i], 1);
-      mbar_init(&bar.do_empty[i], 4);  // the four drain warps
+      mbar_init(&bar.do_empty[i], DQ ? 4 : 1);  // the four drain warps, or the MMA commit after dV
     }
     mbar_init(&bar.s_full, 1);
     mbar_init(&bar.p_ready, 8);
     mbar_init(&bar.dp_full, 1);
     mbar_init(&bar.ds_ready, 8);
     mbar_init(&bar.ps_free, 1);
-    mbar_init(&bar.ds_free, 4);     // the four drain warps
+    mbar_init(&bar.ds_free, DQ ? 4 : 1);  // the four drain warps, or the MMA commit after dK
     mbar_init(&bar.dq_full, 1);
     mbar_init(&bar.dq_free, 4);     // the four drain warps
     mbar_init(&bar.acc_ready, 1);
@@ -447,7 +441,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                    c.olen - j0 * QT)) break;
         tc_fence_after();
         issue_s(gs);
-        if (gs > 0 && !mbar_wait(&bar.dq_free, (gs - 1) & 1, abort)) break;
+        if (DQ && gs > 0 && !mbar_wait(&bar.dq_free, (gs - 1) & 1, abort)) break;
         if (!ready(&bar.do_full[gs % C::NDO], (gs / C::NDO) & 1, do_smem + (gs % C::NDO) * C::T_BYTES,
                    c.olen - j0 * QT)) break;
         tc_fence_after();
@@ -471,9 +465,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           // dQ^T_g = K^T dS^T_g into the dP^T columns; dK_g += dS^T_g Q_g
           if (!mbar_wait(&bar.ds_ready, gs & 1, abort)) { ok = false; break; }
           tc_fence_after();
-          issue_dq(nk_kv);
+          if (DQ) issue_dq(nk_kv);
           issue_dk(gs, nk_q, j > j0);
-          mma_commit(&bar.ps_free);
+          mma_commit(DQ ? &bar.ps_free : &bar.ds_free);  // without dQ, dK is the last reader of dS^T
+          // Without dQ the dO stage (tile and delta row) is free once dK_g is
+          // done: dK_g follows ds_ready_g, so the compute warps have read
+          // this step's delta row, and dV_g, the tile's last reader, ran first.
+          if (!DQ) mma_commit(&bar.do_empty[gs % C::NDO]);
           if (!more) {
             mma_commit(&bar.kv_empty);
             mma_commit(&bar.acc_ready);
@@ -481,7 +479,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           // dP^T_{g+1} once the drain warps have read dQ^T_g
           if (more) {
             const uint32_t g1 = gs + 1;
-            if (!mbar_wait(&bar.dq_free, gs & 1, abort)) { ok = false; break; }
+            if (DQ && !mbar_wait(&bar.dq_free, gs & 1, abort)) { ok = false; break; }
             if (!ready(&bar.do_full[g1 % C::NDO], (g1 / C::NDO) & 1, do_smem + (g1 % C::NDO) * C::T_BYTES,
                        c.olen - (j + 1) * QT)) { ok = false; break; }
             tc_fence_after();
@@ -659,65 +657,67 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int quad = warp & 3;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const bool drains = quad * 32 < D;             // warp-uniform
-    SegCursor c;
-    cursor_init<kTileM>(c, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q);
-    uint32_t gs = 0;
-    bool ok = true;
-    for (int64_t t = blockIdx.x;
-         ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q); t += G) {
-      const Tile tl = cursor_tile(c, t);
-      int32_t j0, nq;
-      bwd_q_steps<MASKED>(c, tl.m, p, j0, nq);
-      for (int32_t j = j0; j < nq; ++j, ++gs) {
-        if (!mbar_wait(&bar.dq_full, gs & 1, abort)) { ok = false; break; }
-        tc_fence_after();
-        const int32_t n = min(QT, c.olen - j * QT);  // valid q columns of this step
-        const int32_t row0 = c.o0 + j * QT;
-        float* blk0 = reinterpret_cast<float*>(do_smem + (gs % C::NDO) * C::T_BYTES + quad * 8192);
-        float* blk1 = reinterpret_cast<float*>(ds_smem + quad * 8192);
-        uint32_t v[64];
-        // q columns [0, 64) -> dO_g stage
-        tmem_ld32(tmem + lane_off + C::DP_COL, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-        tmem_ld32(tmem + lane_off + C::DP_COL + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-        tmem_wait_ld();
-        if (drains) {
-#pragma unroll
-          for (int i = 0; i < 64; ++i) blk0[i * 32 + lane] = i < n ? __uint_as_float(v[i]) : 0.f;
-          fence_proxy_async_smem();
+    if (DQ) {  // (without dQ -- the deterministic form -- this warpgroup has no work)
+      SegCursor c;
+      cursor_init<kTileM>(c, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q);
+      uint32_t gs = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x;
+           ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q); t += G) {
+        const Tile tl = cursor_tile(c, t);
+        int32_t j0, nq;
+        bwd_q_steps<MASKED>(c, tl.m, p, j0, nq);
+        for (int32_t j = j0; j < nq; ++j, ++gs) {
+          if (!mbar_wait(&bar.dq_full, gs & 1, abort)) { ok = false; break; }
+          tc_fence_after();
+          const int32_t n = min(QT, c.olen - j * QT);  // valid q columns of this step
+          const int32_t row0 = c.o0 + j * QT;
+          float* blk0 = reinterpret_cast<float*>(do_smem + (gs % C::NDO) * C::T_BYTES + quad * 8192);
+          float* blk1 = reinterpret_cast<float*>(ds_smem + quad * 8192);
+          uint32_t v[64];
+          // q columns [0, 64) -> dO_g stage
+          tmem_ld32(tmem + lane_off + C::DP_COL, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+          tmem_ld32(tmem + lane_off + C::DP_COL + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+          tmem_wait_ld();
+          if (drains) {
+  #pragma unroll
+            for (int i = 0; i < 64; ++i) blk0[i * 32 + lane] = i < n ? __uint_as_float(v[i]) : 0.f;
+            fence_proxy_async_smem();
+          }
+          // q columns [64, 128)
+          tmem_ld32(tmem + lane_off + C::DP_COL + 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+          tmem_ld32(tmem + lane_off + C::DP_COL + 96, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar.dq_free);  // every TMEM read done: the columns may take dP^T_{g+1}
+          // ... into the dS^T buffer once dQ^T_g and dK_g are done with it
+          if (!mbar_wait(&bar.ps_free, gs & 1, abort)) { ok = false; break; }
+          if (drains && n > 64) {
+  #pragma unroll
+            for (int i = 0; i < 64; ++i) blk1[i * 32 + lane] = 64 + i < n ? __uint_as_float(v[i]) : 0.f;
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+          if (lane == 0) {
+            // The block in the dS^T buffer goes first, in a bulk group of its
+            // own: the compute warps wait for that buffer (ds_free), while the
+            // dO stage is not needed again until a later step.
+            if (drains && n > 64) tma_reduce_add_3d(blk1, &tm_dq, quad * 32, tl.h, row0 + 64);
+            bulk_commit();
+            if (drains) tma_reduce_add_3d(blk0, &tm_dq, quad * 32, tl.h, row0);
+            bulk_commit();
+            bulk_wait_read_1();  // the dS^T-buffer block has been read
+            mbar_arrive(&bar.ds_free);
+            bulk_wait_read_all();  // the dO-stage block has been read
+            mbar_arrive(&bar.do_empty[gs % C::NDO]);
+          }
+          __syncwarp();
         }
-        // q columns [64, 128)
-        tmem_ld32(tmem + lane_off + C::DP_COL + 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-        tmem_ld32(tmem + lane_off + C::DP_COL + 96, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar.dq_free);  // every TMEM read done: the columns may take dP^T_{g+1}
-        // ... into the dS^T buffer once dQ^T_g and dK_g are done with it
-        if (!mbar_wait(&bar.ps_free, gs & 1, abort)) { ok = false; break; }
-        if (drains && n > 64) {
-#pragma unroll
-          for (int i = 0; i < 64; ++i) blk1[i * 32 + lane] = 64 + i < n ? __uint_as_float(v[i]) : 0.f;
-          fence_proxy_async_smem();
-        }
-        __syncwarp();
-        if (lane == 0) {
-          // The block in the dS^T buffer goes first, in a bulk group of its
-          // own: the compute warps wait for that buffer (ds_free), while the
-          // dO stage is not needed again until a later step.
-          if (drains && n > 64) tma_reduce_add_3d(blk1, &tm_dq, quad * 32, tl.h, row0 + 64);
-          bulk_commit();
-          if (drains) tma_reduce_add_3d(blk0, &tm_dq, quad * 32, tl.h, row0);
-          bulk_commit();
-          bulk_wait_read_1();  // the dS^T-buffer block has been read
-          mbar_arrive(&bar.ds_free);
-          bulk_wait_read_all();  // the dO-stage block has been read
-          mbar_arrive(&bar.do_empty[gs % C::NDO]);
-        }
-        __syncwarp();
       }
+      if (lane == 0) bulk_wait_all();  // this warp's reductions have completed
+      __syncwarp();
     }
-    if (lane == 0) bulk_wait_all();  // this warp's reductions have completed
-    __syncwarp();
   }
 
   tc_fence_before();
@@ -729,14 +729,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (threadIdx.x == 0 && bar.abort) record_error(p.err, kErrTimeout);
 }
 
-template <int D, bool MASKED>
+template <int D, bool MASKED, bool DQ>
 static cudaError_t launch_bwd_d(const BwdLaunch& L, cudaStream_t stream) {
   using C = BwdCfg<D>;
   const int elem_grid = L.grid * 8;
   auto mark = [&](int i) {
     if (L.phase_events[i] != nullptr) cudaEventRecord(L.phase_events[i], stream);
   };
-  auto kern = varlen_bwd_main_kernel<D, MASKED>;
+  auto kern = varlen_bwd_main_kernel<D, MASKED, DQ>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   // The warpgroup register split assumes the kernel was compiled to exactly
@@ -754,17 +754,28 @@ static cudaError_t launch_bwd_d(const BwdLaunch& L, cudaStream_t stream) {
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   mark(2);
-  varlen_bwd_post_kernel<<<elem_grid, 256, 0, stream>>>(L.post);
-  e = cudaGetLastError();
+  if (DQ) {
+    varlen_bwd_post_kernel<<<elem_grid, 256, 0, stream>>>(L.post);
+    e = cudaGetLastError();
+  } else {
+    e = launch_bwd_dq(L, stream);
+  }
   mark(3);
   return e;
 }
 
+template <int D>
+static cudaError_t launch_bwd_dm(const BwdLaunch& L, cudaStream_t stream) {
+  if (L.deterministic)
+    return L.p.masked ? launch_bwd_d<D, true, false>(L, stream) : launch_bwd_d<D, false, false>(L, stream);
+  return L.p.masked ? launch_bwd_d<D, true, true>(L, stream) : launch_bwd_d<D, false, true>(L, stream);
+}
+
 cudaError_t launch_bwd(const BwdLaunch& L, cudaStream_t stream) {
   switch (L.head_dim) {
-    case 64: return L.p.masked ? launch_bwd_d<64, true>(L, stream) : launch_bwd_d<64, false>(L, stream);
-    case 96: return L.p.masked ? launch_bwd_d<96, true>(L, stream) : launch_bwd_d<96, false>(L, stream);
-    case 128: return L.p.masked ? launch_bwd_d<128, true>(L, stream) : launch_bwd_d<128, false>(L, stream);
+    case 64: return launch_bwd_dm<64>(L, stream);
+    case 96: return launch_bwd_dm<96>(L, stream);
+    case 128: return launch_bwd_dm<128>(L, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -88,7 +88,7 @@ struct PrepParams {
   const float* lse;
   float* delta;     // [H, pad_rows], segment-padded (see bwd_pad_rows)
   float* lse2;      // [H, pad_rows], segment-padded
-  float* dq_acc;    // [total_q, H, D]
+  float* dq_acc;    // [total_q, H, D], zeroed here; null: no accumulator (deterministic dQ)
   CuView cu_q;
   int32_t batch, total_q, num_heads, head_dim;
   int64_t pad_rows;
@@ -102,6 +102,8 @@ struct BwdParams {
   const float* delta;  // [H, pad_rows]
   const float* lse2;   // [H, pad_rows]
   float* dq_acc;
+  __nv_bfloat16* dq;   // written directly by the deterministic dQ kernel
+  int64_t dq_rs, dq_hs;
   CuView cu_q;
   CuView cu_k;
   int32_t batch, total_q, total_k, num_heads;
@@ -130,10 +132,14 @@ struct BwdLaunch {
   PostParams post;
   int head_dim;
   int grid;
-  cudaEvent_t phase_events[4];  // optional: recorded before prep / after prep / after main / after post
+  int deterministic;  // 1: dK/dV main kernel + the q-major dQ kernel (no atomics), no post kernel
+  cudaEvent_t phase_events[4];  // optional: recorded before prep / after prep / after main / after post (or dQ)
 };
 
 cudaError_t launch_bwd(const BwdLaunch& L, cudaStream_t stream);
+
+// The deterministic dQ kernel (varlen_bwd_dq.cu) for head size D, masked or not.
+cudaError_t launch_bwd_dq(const BwdLaunch& L, cudaStream_t stream);
 
 // Length of one head's row of the segment-padded delta / lse2 arrays.
 // Segment b's entries start at 4 * ceil(o0_b / 4) + 4 b (o0_b its first q
@@ -142,6 +148,14 @@ cudaError_t launch_bwd(const BwdLaunch& L, cudaStream_t stream);
 // any cu_seqlens.
 inline int64_t bwd_pad_rows(int32_t batch, int32_t total_q) {
   return 4 * (((int64_t)total_q + 3) / 4) + 4 * (int64_t)batch + 128;
+}
+
+// First index of segment b's entries in the padded per-row arrays (delta,
+// lse2), o0 its first q row: a multiple of 4 (16 bytes), at least the
+// previous segment's end for non-decreasing cu_seqlens, and below
+// bwd_pad_rows() - 127 - len_b for any cu_seqlens (len_b + o0 <= total_q).
+__host__ __device__ __forceinline__ int64_t pad_base(int32_t o0, int32_t b) {
+  return 4 * (((int64_t)o0 + 3) / 4) + 4 * (int64_t)b;
 }
 
 cudaError_t launch_debug_schedule(const int32_t* cu, int32_t batch, int32_t total, int32_t num_heads, int32_t tile,

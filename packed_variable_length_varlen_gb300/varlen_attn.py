@@ -76,6 +76,8 @@ def _load() -> ctypes.CDLL:
     lib.varlen_attn_bwd_window.restype = ctypes.c_int
     lib.varlen_attn_bwd_window.argtypes = [vp, S, vp, S, vp, S, vp, S, vp, S, vp, vp, vp, i32, i32, i32, i32, i32,
                                            i32, i32, f32, i32, i32, vp, S, vp, S, vp, S, vp, sz, vp]
+    lib.varlen_attn_bwd_deterministic.restype = ctypes.c_int
+    lib.varlen_attn_bwd_deterministic.argtypes = lib.varlen_attn_bwd_window.argtypes
     DS = VarlenDenseStride
     lib.varlen_attn_fwd_dense.restype = ctypes.c_int
     lib.varlen_attn_fwd_dense.argtypes = [vp, DS, vp, DS, vp, DS, i32, i32, i32, i32, i32, f32, i32, vp, DS, vp, vp]
@@ -115,7 +117,7 @@ EXPORTED = ("varlen_attn_fwd", "varlen_attn_bwd_workspace_size", "varlen_attn_bw
             "varlen_attn_debug_set_phase_events", "varlen_attn_bwd_noalloc", "varlen_attn_last_cuda_error",
             "varlen_attn_fwd_causal", "varlen_attn_bwd_causal", "varlen_attn_fwd_dense",
             "varlen_attn_bwd_dense_workspace_size", "varlen_attn_bwd_dense", "varlen_attn_fwd_window",
-            "varlen_attn_bwd_window")
+            "varlen_attn_bwd_window", "varlen_attn_bwd_deterministic")
 
 # Size of the fixed device array varlen_attn_bwd_noalloc uses as scratch.
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -198,13 +200,15 @@ def varlen_attn_bwd_workspace_size(batch, total_q, num_heads, head_dim) -> int:
 
 def varlen_attn_bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads,
                     head_dim, max_seqlen_q, max_seqlen_k, scale, dq, dk, dv, workspace, workspace_bytes,
-                    stream=None, causal=False, window=(-1, -1)) -> int:
+                    stream=None, causal=False, window=(-1, -1), deterministic=False) -> int:
     band = _band(causal, window)
     head = (_ptr(q), _stride(q), _ptr(k), _stride(k), _ptr(v), _stride(v), _ptr(out), _stride(out), _ptr(dout),
             _stride(dout), _ptr(lse), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), batch, total_q, total_k, num_heads,
             head_dim, max_seqlen_q, max_seqlen_k, scale)
     tail = (_ptr(dq), _stride(dq), _ptr(dk), _stride(dk), _ptr(dv), _stride(dv), _ptr(workspace), workspace_bytes,
             _stream(stream))
+    if deterministic:
+        return LIB.varlen_attn_bwd_deterministic(*head, *(band or (-1, -1)), *tail)
     if band is None:
         return LIB.varlen_attn_bwd(*head, *tail)
     if band == (-1, 0):
@@ -336,7 +340,7 @@ def attention_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q=0, max_seqle
 
 def attention_bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q=0, max_seqlen_k=0,
                   scale=None, dq=None, dk=None, dv=None, workspace=None, stream=None, causal=False,
-                  window=(-1, -1)):
+                  window=(-1, -1), deterministic=False):
     """dQ, dK, dV for the forward above (every operand keeps its strides)."""
     total_q, H, D = q.shape
     total_k = k.shape[0]
@@ -350,7 +354,7 @@ def attention_bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, max_seqle
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
     _check(varlen_attn_bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, H, D,
                            max_seqlen_q, max_seqlen_k, scale, dq, dk, dv, workspace, workspace.numel(), stream,
-                           causal, window), "varlen_attn_bwd")
+                           causal, window, deterministic), "varlen_attn_bwd")
     return dq, dk, dv
 
 
