@@ -123,7 +123,10 @@ __global__ void __launch_bounds__(256) varlen_bwd_post_kernel(const PostParams p
 
 constexpr int QT_ROWS = 128;  // q rows per backward step (kBwdTileQ)
 
-template <int D>
+// DQ: the kernel computes dQ^T (the default form); without it (the
+// deterministic form) dS^T lives in TMEM and its shared-memory buffer
+// becomes a third Q stage.
+template <int D, bool DQ>
 struct BwdCfg {
   static constexpr int NC = (D + 63) / 64;       // 64-column chunks of Q / dO / V
   static constexpr int KCH = 2;                  // K tile always holds 128 columns (dQ^T uses M = 128)
@@ -131,9 +134,9 @@ struct BwdCfg {
   static constexpr int K_BYTES = KCH * CHUNK;
   static constexpr int V_BYTES = NC * CHUNK;
   static constexpr int T_BYTES = NC * CHUNK;     // one Q or dO tile (128 rows)
-  static constexpr int NQ = NC == 1 ? 3 : 2;     // Q ring depth
+  static constexpr int NQ = (NC == 1 || !DQ) ? 3 : 2;  // Q ring depth
   static constexpr int NDO = NC == 1 ? 3 : 2;    // dO ring depth
-  static constexpr int DS_BYTES = 2 * CHUNK;     // dS^T: 128 kv rows x 128 q (bf16), two 64-q chunks
+  static constexpr int DS_BYTES = DQ ? 2 * CHUNK : 0;  // dS^T: 128 kv rows x 128 q (bf16), two 64-q chunks
   static constexpr int ROWV_BYTES = QT_ROWS * 4; // one step's lse2 or delta (128 floats)
   // Tiles from the (1024-byte aligned) base, then the barriers and the
   // per-stage lse2 / delta rows.
@@ -204,7 +207,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     varlen_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                            const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
-  using C = BwdCfg<D>;
+  using C = BwdCfg<D, DQ>;
   constexpr int QT = kBwdTileQ;  // 128
   static_assert(QT == QT_ROWS, "step rows");
   // The 128-byte swizzled tiles need 1024-byte alignment; the declaration
@@ -244,7 +247,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bar.dp_full, 1);
     mbar_init(&bar.ds_ready, 8);
     mbar_init(&bar.ps_free, 1);
-    mbar_init(&bar.ds_free, DQ ? 4 : 1);  // the four drain warps, or the MMA commit after dK
+    mbar_init(&bar.ds_free, 4);  // the four drain warps (with dQ only)
     mbar_init(&bar.dq_full, 1);
     mbar_init(&bar.dq_free, 4);     // the four drain warps
     mbar_init(&bar.acc_ready, 1);
@@ -408,13 +411,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (kk < nk) mma_ss_lo(tmem + C::DP_COL, kM + kk * 128, sM + kk * 128, kIdQ, kk > 0 ? 1u : 0u);
         mma_commit(&bar.dq_full);
       };
-      // dK += dS^T (K-major) Q_g (MN-major); nk q k-steps
+      // dK += dS^T_g Q_g (MN-major); nk q k-steps.  dS^T_g is the K-major
+      // shared-memory buffer, or without dQ the bf16 copy the compute warps
+      // wrote into the dP^T columns (q columns [0, 64) at [0, 32), [64, 128)
+      // at [64, 96)); dP^T_{g+1} is issued after this product.
       auto issue_dk = [&](uint32_t g, int nk, bool acc0) {
         const uint32_t qM = sw128_desc_lo(smem_addr(q_smem + (g % C::NQ) * C::T_BYTES), C::CHUNK);
 #pragma unroll
         for (int kk = 0; kk < QT / 16; ++kk) {
           const uint32_t ao = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
-          if (kk < nk) mma_ss_lo(tmem + C::DK_COL, sK + ao, qM + kk * 128, kIdG, (acc0 || kk > 0) ? 1u : 0u);
+          if (kk < nk) {
+            if (DQ)
+              mma_ss_lo(tmem + C::DK_COL, sK + ao, qM + kk * 128, kIdG, (acc0 || kk > 0) ? 1u : 0u);
+            else
+              mma_ts_lo(tmem + C::DK_COL, tmem + C::DP_COL + (kk >> 2) * 64 + (kk & 3) * 8, qM + kk * 128, kIdG,
+                        (acc0 || kk > 0) ? 1u : 0u);
+          }
         }
         mma_commit(&bar.q_empty[g % C::NQ]);
       };
@@ -467,7 +479,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_fence_after();
           if (DQ) issue_dq(nk_kv);
           issue_dk(gs, nk_q, j > j0);
-          mma_commit(DQ ? &bar.ps_free : &bar.ds_free);  // without dQ, dK is the last reader of dS^T
+          if (DQ) mma_commit(&bar.ps_free);
           // Without dQ the dO stage (tile and delta row) is free once dK_g is
           // done: dK_g follows ds_ready_g, so the compute warps have read
           // this step's delta row, and dV_g, the tile's last reader, ran first.
@@ -534,6 +546,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int32_t qc0 = j * QT + half * 64;             // first q column of this thread (in the segment)
         const int32_t nvalid = row_valid ? max(0, min(64, q_hi - qc0)) : 0;
         const int32_t lo = MASKED ? min(64, max(0, q_lo - qc0)) : 0;  // columns [lo, nvalid) are visible
+        // interior steps (every column of every lane visible) skip the per-element selects
+        const bool all_vis = __all_sync(0xffffffffu, lo == 0 && nvalid == 64);
         // this step's lse2 / delta rows arrive with its Q / dO tiles
         const float4* l4 = reinterpret_cast<const float4*>(lse_rows + (gs % C::NQ) * QT + half * 64);
         const float4* d4 = reinterpret_cast<const float4*>(delta_rows + (gs % C::NDO) * QT + half * 64);
@@ -554,10 +568,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                     make_float2(c2, c2), make_float2(-l.x, -l.y));
             const float2 t1 = ffma2(make_float2(__uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3])),
                                     make_float2(c2, c2), make_float2(-l.z, -l.w));
-            pv[i] = (i >= lo && i < nvalid) ? ex2(t0.x) : 0.f;
-            pv[i + 1] = (i + 1 >= lo && i + 1 < nvalid) ? ex2(t0.y) : 0.f;
-            pv[i + 2] = (i + 2 >= lo && i + 2 < nvalid) ? ex2(t1.x) : 0.f;
-            pv[i + 3] = (i + 3 >= lo && i + 3 < nvalid) ? ex2(t1.y) : 0.f;
+            pv[i] = ex2(t0.x);
+            pv[i + 1] = ex2(t0.y);
+            pv[i + 2] = ex2(t1.x);
+            pv[i + 3] = ex2(t1.y);
+          }
+          if (!all_vis) {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) pv[i] = (i >= lo && i < nvalid) ? pv[i] : 0.f;
           }
         }
         {
@@ -591,21 +609,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                    fadd2(make_float2(__uint_as_float(dpv[i + 2]), __uint_as_float(dpv[i + 3])),
                                          make_float2(-dl.z, -dl.w)));
             // select, not multiply: dP^T and delta past the segment end may hold NaN
-            dk2[ii / 2] = pack_bf16x2(ii >= lo && ii < nvalid ? a.x : 0.f, ii + 1 >= lo && ii + 1 < nvalid ? a.y : 0.f);
-            dk2[ii / 2 + 1] =
-                pack_bf16x2(ii + 2 >= lo && ii + 2 < nvalid ? b.x : 0.f, ii + 3 >= lo && ii + 3 < nvalid ? b.y : 0.f);
+            if (all_vis) {
+              dk2[ii / 2] = pack_bf16x2(a.x, a.y);
+              dk2[ii / 2 + 1] = pack_bf16x2(b.x, b.y);
+            } else {
+              dk2[ii / 2] = pack_bf16x2(ii >= lo && ii < nvalid ? a.x : 0.f, ii + 1 >= lo && ii + 1 < nvalid ? a.y : 0.f);
+              dk2[ii / 2 + 1] = pack_bf16x2(ii + 2 >= lo && ii + 2 < nvalid ? b.x : 0.f,
+                                            ii + 3 >= lo && ii + 3 < nvalid ? b.y : 0.f);
+            }
           }
         }
-        // the dS^T buffer is free once dQ^T and dK of the previous step are
-        // done and the drain has staged (and bulk-read) its dQ there
-        if (gs > 0 && !mbar_wait(&bar.ds_free, (gs - 1) & 1, abort)) { ok = false; break; }
-        // row r of chunk `half` (128-byte swizzle: 16-byte unit u of row r sits at u ^ (r % 8))
-        uint8_t* dsrow = ds_smem + half * C::CHUNK + r * 128;
+        if (DQ) {
+          // the dS^T buffer is free once dQ^T and dK of the previous step are
+          // done and the drain has staged (and bulk-read) its dQ there
+          if (gs > 0 && !mbar_wait(&bar.ds_free, (gs - 1) & 1, abort)) { ok = false; break; }
+          // row r of chunk `half` (128-byte swizzle: 16-byte unit u of row r sits at u ^ (r % 8))
+          uint8_t* dsrow = ds_smem + half * C::CHUNK + r * 128;
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(dsrow + ((u ^ (r & 7)) * 16)) =
-              make_uint4(dk2[4 * u], dk2[4 * u + 1], dk2[4 * u + 2], dk2[4 * u + 3]);
-        fence_proxy_async_smem();
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4*>(dsrow + ((u ^ (r & 7)) * 16)) =
+                make_uint4(dk2[4 * u], dk2[4 * u + 1], dk2[4 * u + 2], dk2[4 * u + 3]);
+          fence_proxy_async_smem();
+        } else {
+          // Without dQ, dS^T only feeds dK: it goes into TMEM over the first
+          // 32 of the dP^T columns this thread read above.  dK_{g-1}, the
+          // last reader of the previous copy, ran before dP^T_g.
+          tmem_st32(tmem + lane_off + C::DP_COL + half * 64, dk2);
+          tmem_wait_st();
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar.ds_ready);
@@ -731,7 +762,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 template <int D, bool MASKED, bool DQ>
 static cudaError_t launch_bwd_d(const BwdLaunch& L, cudaStream_t stream) {
-  using C = BwdCfg<D>;
+  using C = BwdCfg<D, DQ>;
   const int elem_grid = L.grid * 8;
   auto mark = [&](int i) {
     if (L.phase_events[i] != nullptr) cudaEventRecord(L.phase_events[i], stream);

@@ -379,6 +379,7 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t gg = g + i;
         const int32_t col0 = (j_lo + i) * kTileN + half * 64;  // key index of this thread's first column
         const int32_t lim_lo = key_lo - col0, lim_hi = key_hi - col0;  // columns [lim_lo, lim_hi) are visible
+        const bool all_vis = !__any_sync(0xffffffffu, lim_lo > 0 || lim_hi < 64);  // no select needed
         // ---- P = exp2(S c - lse2) on this thread's 64 columns
         if (!mbar_wait(&bar.s_full[gg & 1], (gg >> 1) & 1, abort)) { ok = false; break; }
         tc_fence_after();
@@ -397,7 +398,7 @@ __global__ void __launch_bounds__(384, 1)
             pv[k + 1] = ex2(x.y);
           }
           // columns outside the row's band or past the segment end: P = 0 (by select)
-          if (__any_sync(0xffffffffu, lim_lo > 0 || lim_hi < 64)) {
+          if (!all_vis) {
 #pragma unroll
             for (int k = 0; k < 64; ++k) pv[k] = (k >= lim_lo && k < lim_hi) ? pv[k] : 0.f;
           }
@@ -421,8 +422,11 @@ __global__ void __launch_bounds__(384, 1)
             const float2 a = fmul2(make_float2(pv[k], pv[k + 1]),
                                    fadd2(make_float2(__uint_as_float(dv[k]), __uint_as_float(dv[k + 1])), nd));
             // select, not multiply: dP past the segment end may hold NaN
-            ds2[k / 2] = pack_bf16x2(k >= lim_lo && k < lim_hi ? a.x : 0.f,
-                                     k + 1 >= lim_lo && k + 1 < lim_hi ? a.y : 0.f);
+            if (all_vis)
+              ds2[k / 2] = pack_bf16x2(a.x, a.y);
+            else
+              ds2[k / 2] = pack_bf16x2(k >= lim_lo && k < lim_hi ? a.x : 0.f,
+                                       k + 1 >= lim_lo && k + 1 < lim_hi ? a.y : 0.f);
           }
         }
         // ---- dS into TMEM over the first 32 of this thread's S columns (read above)
