@@ -147,6 +147,37 @@ def _max_over_ranks(x: float, ws: int) -> float:
 
 # ------------------------------------------------------------------ CPU side
 
+def _parse_cpulist(text: str):
+    cpus = set()
+    for part in text.strip().split(","):
+        if not part:
+            continue
+        a, _, b = part.partition("-")
+        cpus.update(range(int(a), int(b or a) + 1))
+    return cpus
+
+
+def _bind_near_gpu(dev_index: int):
+    """Restricts this process to the CPUs the kernel lists as local to the
+    GPU (its PCI device's local_cpulist), intersected with the CPUs it may
+    use, so that pinned host buffers allocated afterwards sit in the memory
+    next to that GPU.  Returns (previous affinity, description) or None when
+    the topology is not readable."""
+    try:
+        p = torch.cuda.get_device_properties(dev_index)
+        bdf = "%04x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+        with open("/sys/bus/pci/devices/%s/local_cpulist" % bdf) as f:
+            local = _parse_cpulist(f.read())
+        before = os.sched_getaffinity(0)
+        use = local & before
+        if not use or use == before:
+            return before, "unchanged (%d CPUs)" % len(before)
+        os.sched_setaffinity(0, use)
+        return before, "%d of %d CPUs local to %s" % (len(use), len(before), bdf)
+    except (OSError, AttributeError, ValueError):
+        return None
+
+
 def _oracle_rate(w: W.Workload, target_s: float, seed: int = 0, causal: bool = False, window=(-1, -1)):
     """Times the oracle (forward + query-side backward) on sampled (row, head)
     pairs of the workload.  Credits each pair with its share of the step's
@@ -323,6 +354,7 @@ def ours(args, w, ws, rank, local):
     # ---- end to end through the C ABI with host buffers (pinned)
     e2e = None
     if not args.no_e2e:
+        bound = _bind_near_gpu(local)
         host = {n: getattr(cpu, n).pin_memory() if getattr(cpu, n)._base is None
                 else getattr(cpu, n)._base.pin_memory() for n in ("q", "k", "v", "dout")}
         hcu_q, hcu_k = cpu.cu_q.pin_memory(), cpu.cu_k.pin_memory()
@@ -409,7 +441,10 @@ def ours(args, w, ws, rank, local):
         ms_e2e = _max_over_ranks(a.elapsed_time(b_), ws)
         e2e = {"value": ws * ke * step_flops / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(d2h_bytes), "ms_per_step": ms_e2e / ke,
-               "pipeline": "step i+1 inputs in and step i-1 results out on two copy streams during step i"}
+               "pipeline": "step i+1 inputs in and step i-1 results out on two copy streams during step i",
+               "host_cpus": bound[1] if bound else "topology not readable"}
+        if bound:
+            os.sched_setaffinity(0, bound[0])  # the CPU baseline below uses every core again
 
     peaks, src = _peaks()
     if rank != 0:
