@@ -201,3 +201,39 @@ def test_visible_pairs_band_by_brute_force():
                     d = i + sk - sq
                     n += (left < 0 or j >= d - left) and (right < 0 or j <= d + right)
         assert w.visible_pairs(causal, window) == n, (causal, window)
+
+
+def test_window_and_deterministic_validation_codes(va):
+    """The window and deterministic entry points validate like the plain
+    ones (any window side is accepted: negative means unbounded) and check
+    the workspace before touching a device."""
+    H, D, tq = 2, 64, 10
+    q = _Fake(0x1000, H * D, D)
+
+    class _P:
+        def __init__(self, p):
+            self._p = p
+
+        def data_ptr(self):
+            return self._p
+
+    cu, lse = _P(0x2000), _P(0x3000)
+    for window in ((-1, -1), (0, 0), (5, -1), (-7, 3), (2 ** 31 - 1, 2 ** 31 - 1)):
+        st = va.varlen_attn_fwd(q, q, q, cu, cu, 1, tq, tq, H, D, 0, 0, 0.125, q, lse, 0, window=window)
+        assert st in (va.VARLEN_ERR_CUDA, va.VARLEN_ERR_ARCH), window
+    assert va.varlen_attn_fwd_window(q, q, q, cu, cu, 1, tq, tq, H, D, 0, 0, 0.125, 3, 1, q, lse, 0) in (
+        va.VARLEN_ERR_CUDA, va.VARLEN_ERR_ARCH)
+    assert va.varlen_attn_fwd_window(q, q, q, cu, cu, 1, tq, tq, 2, 80, 0, 0, 0.125, 3, 1, q, lse, 0) == \
+        va.VARLEN_ERR_HEAD_DIM
+    assert va.varlen_attn_fwd_window(q, q, q, _P(0), cu, 1, tq, tq, H, D, 0, 0, 0.125, 3, 1, q, lse, 0) == \
+        va.VARLEN_ERR_NULL
+    need = va.varlen_attn_bwd_workspace_size(1, tq, H, D)
+    for det in (False, True):
+        def bwd(ws_ptr=0x10000, ws_bytes=need, window=(-1, -1)):
+            return va.varlen_attn_bwd(q, q, q, q, q, lse, cu, cu, 1, tq, tq, H, D, 0, 0, 0.125, q, q, q,
+                                      _P(ws_ptr), ws_bytes, 0, window=window, deterministic=det)
+        assert bwd(ws_bytes=need - 1) == va.VARLEN_ERR_WORKSPACE
+        assert bwd(ws_ptr=0x10010) == va.VARLEN_ERR_WORKSPACE   # not 256-byte aligned
+        assert bwd(ws_ptr=0) == va.VARLEN_ERR_WORKSPACE
+        assert bwd(window=(4, 0)) in (va.VARLEN_ERR_CUDA, va.VARLEN_ERR_ARCH)
+        assert bwd() in (va.VARLEN_ERR_CUDA, va.VARLEN_ERR_ARCH)
