@@ -298,7 +298,7 @@ def ours(args, w, ws, rank, local):
     def bwd():
         run_bwd(d, out, lse, dq, dk, dv)
 
-    # does the backward exist in this build?
+    # one untimed forward and backward, checked for device errors
     fwd()
     bwd()
     has_bwd = True
