@@ -64,21 +64,21 @@ def test_max_over_ranks_without_group():
 _CASE = ([130, 0, 77, 256, 5, 64], [129, 9, 0, 300, 40, 64], 4, 64)
 
 
-def _shard_result(w, cpu, mode, world, rank):
+def _shard_result(w, cpu, mode, world, rank, window=(-1, -1)):
     """The oracle forward and backward of this rank's shard, keyed by global
-    (row, head) pairs."""
+    (row, head) pairs.  Masks are per segment, so they shard unchanged."""
     if mode == "heads":
         h0, h1 = S.head_range(w.num_heads, world, rank)
         view = lambda t: t[:, h0:h1]
         pb = oracle.Problem(view(cpu.q), view(cpu.k), view(cpu.v), w.cu_q, w.cu_k, w.softmax_scale,
-                            dout=view(cpu.dout))
+                            dout=view(cpu.dout), window=window)
         rows, heads = oracle.all_pairs(w.total_q, h1 - h0)
         krows, kheads = oracle.all_pairs(w.total_k, h1 - h0)
         grows, gheads, gkrows, gkheads = rows, heads + h0, krows, kheads + h0
     else:
         sh = S.segment_range(w.cu_q, w.cu_k, world, rank)
         pb = oracle.Problem(cpu.q[sh.q0:sh.q1], cpu.k[sh.k0:sh.k1], cpu.v[sh.k0:sh.k1], sh.cu_q, sh.cu_k,
-                            w.softmax_scale, dout=cpu.dout[sh.q0:sh.q1])
+                            w.softmax_scale, dout=cpu.dout[sh.q0:sh.q1], window=window)
         rows, heads = oracle.all_pairs(sh.q1 - sh.q0, w.num_heads)
         krows, kheads = oracle.all_pairs(sh.k1 - sh.k0, w.num_heads)
         grows, gheads, gkrows, gkheads = rows + sh.q0, heads, krows + sh.k0, kheads
@@ -88,13 +88,13 @@ def _shard_result(w, cpu, mode, world, rank):
     return grows, gheads, o, lse, dq, gkrows, gkheads, dk, dv
 
 
-def _worker(rank, world, port, mode, out_path):
+def _worker(rank, world, port, mode, out_path, window=(-1, -1)):
     import torch.distributed as dist
     dist.init_process_group("gloo", rank=rank, world_size=world, init_method="tcp://127.0.0.1:%d" % port)
     try:
         w = W.custom("shard", *_CASE[:2], _CASE[2], _CASE[3])
         cpu = W.make_inputs(w, 0)
-        res = _shard_result(w, cpu, mode, world, rank)
+        res = _shard_result(w, cpu, mode, world, rank, window)
         gathered = [None] * world
         dist.all_gather_object(gathered, res)  # only to bring the shards to one process for checking
         t_max = S.max_over_ranks(float(rank + 1))
@@ -111,8 +111,9 @@ def _free_port():
         return s.getsockname()[1]
 
 
-@pytest.mark.parametrize("mode", ["heads", "segments"])
-def test_two_rank_shards_match_unsharded(mode):
+@pytest.mark.parametrize("mode,window", [("heads", (-1, -1)), ("segments", (-1, -1)), ("heads", (-1, 0)),
+                                         ("segments", (40, 3))])
+def test_two_rank_shards_match_unsharded(mode, window):
     oracle.build()
     import torch.multiprocessing as mp
     ctx = mp.get_context("spawn")
@@ -120,7 +121,7 @@ def test_two_rank_shards_match_unsharded(mode):
     with tempfile.TemporaryDirectory() as d:
         out = os.path.join(d, "res.npz")
         port = _free_port()
-        procs = [ctx.Process(target=_worker, args=(r, world, port, mode, out)) for r in range(world)]
+        procs = [ctx.Process(target=_worker, args=(r, world, port, mode, out, window)) for r in range(world)]
         for p in procs:
             p.start()
         for p in procs:
@@ -136,7 +137,7 @@ def test_two_rank_shards_match_unsharded(mode):
 
     w = W.custom("shard", *_CASE[:2], _CASE[2], _CASE[3])
     cpu = W.make_inputs(w, 0)
-    full = oracle.Problem(cpu.q, cpu.k, cpu.v, w.cu_q, w.cu_k, w.softmax_scale, dout=cpu.dout)
+    full = oracle.Problem(cpu.q, cpu.k, cpu.v, w.cu_q, w.cu_k, w.softmax_scale, dout=cpu.dout, window=window)
     # every (row, head) pair computed exactly once across the ranks
     assert sorted(zip(rows.tolist(), heads.tolist())) == sorted(zip(*[a.tolist() for a in oracle.all_pairs(w.total_q, w.num_heads)]))
     assert sorted(zip(krows.tolist(), kheads.tolist())) == sorted(zip(*[a.tolist() for a in oracle.all_pairs(w.total_k, w.num_heads)]))
