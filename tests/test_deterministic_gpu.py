@@ -109,3 +109,27 @@ def test_deterministic_windowed_sampled():
     assert r <= P.GRAD_REL_FRO
     _, dk_a, dv_a = _bwd(w, dev, out, lse, False)
     assert torch.equal(dk, dk_a) and torch.equal(dv, dv_a)
+
+
+@pytest.mark.parametrize("sq,sk", [([0, 0, 0], [5, 130, 0]), ([7, 129, 3], [0, 0, 0]), ([0, 200, 0], [1, 0, 257])])
+def test_deterministic_empty_sides(sq, sk):
+    """No queries at all, no keys at all, and alternating empty segments: the
+    deterministic form returns what the default one does (dK / dV bit for
+    bit; dQ = 0 wherever a row sees no key) and never touches padding."""
+    w = W.custom("det_empty", sq, sk, 2, 64)
+    cpu = W.make_inputs(w, 9)
+    dev = cpu.to(DEV)
+    out, lse = _fwd(w, dev)
+    dq, dk, dv = _bwd(w, dev, out, lse, True)
+    dq_a, dk_a, dv_a = _bwd(w, dev, out, lse, False)
+    assert torch.equal(dk, dk_a) and torch.equal(dv, dv_a)
+    if w.total_q:
+        pb = P.oracle_problem(cpu)
+        rows, heads = oracle.all_pairs(w.total_q, w.num_heads)
+        dq_ref, _ = pb.bwd_q(rows, heads)
+        _, lse_ref = pb.fwd(rows, heads)
+        dead = np.isneginf(lse_ref)
+        got = P.gather(dq.cpu(), rows, heads)
+        assert np.all(got[dead] == 0)
+        if (~dead).any():
+            assert P.rel_fro(got[~dead], dq_ref[~dead]) <= P.GRAD_REL_FRO
