@@ -34,6 +34,14 @@
 //
 //  3. varlen_bwd_post_kernel (HBM-bound): dq = bf16(scale * dq_acc), strided.
 //
+// The deterministic form runs the main kernel without dQ^T (template flag
+// DQ = false): dS^T goes into TMEM over the dP^T columns and dK reads it
+// from there, the drain warpgroup idles, and the shared-memory dS^T buffer
+// becomes a third Q stage; dQ then comes from the q-major kernel of
+// varlen_bwd_dq.cu, and neither the accumulator zeroing nor the post kernel
+// runs.  Masks (causal, sliding windows) are the template flag MASKED with
+// the band in BwdParams: kv tiles run only the q steps whose rows see them.
+//
 // The gradient formulas are the standard ones for O = softmax(scale QK^T) V:
 // dP = dO V^T, dS = P (dP - rowsum(dO o O)), dQ = scale dS K,
 // dK = scale dS^T Q, dV = P^T dO.
