@@ -22,7 +22,8 @@ sections "Summary" and "Minimal repro"; "[FA4][SM120] flash_attn_varlen_func
 and the gradients dQ, dK, dV of sum(O * dO).  Every function takes explicit
 (row, head) pairs so that large problems can be checked on samples.
 
-Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py`` and,
+for the FP8 (E4M3) codec and forward, ``tests/test_oracle_fp8_pins.py``
 (torch fp64 SDPA + autograd per segment, closed forms, central finite
 differences, gradient invariants, planted-mistake detection).
 """
@@ -60,6 +61,20 @@ class _Problem(ctypes.Structure):
     ]
 
 
+class _Fp8Problem(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("q_rs", ctypes.c_int64), ("q_hs", ctypes.c_int64),
+        ("k_rs", ctypes.c_int64), ("k_hs", ctypes.c_int64),
+        ("v_rs", ctypes.c_int64), ("v_hs", ctypes.c_int64),
+        ("cu_q", ctypes.c_void_p), ("cu_k", ctypes.c_void_p),
+        ("batch", ctypes.c_int32), ("num_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+        ("scale", ctypes.c_double),
+        ("q_descale", ctypes.c_void_p), ("k_descale", ctypes.c_void_p), ("v_descale", ctypes.c_void_p),
+        ("quantize_p", ctypes.c_int32),
+    ]
+
+
 def library_path(src: str = _SRC, tag: str = "") -> str:
     name = "liboracle%s_%s.so" % (tag, platform.machine())
     return os.path.join(_BUILD_DIR, name)
@@ -87,6 +102,13 @@ def _declare(lib):
         f.argtypes = [P, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
                       ctypes.c_void_p, ctypes.c_void_p]
     lib.oracle_num_threads.restype = ctypes.c_int
+    lib.oracle_fwd_fp8.restype = ctypes.c_int
+    lib.oracle_fwd_fp8.argtypes = [ctypes.POINTER(_Fp8Problem), ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                                   ctypes.c_void_p, ctypes.c_void_p]
+    for name in ("oracle_e4m3_round", "oracle_e4m3_decode", "oracle_e4m3_encode"):
+        f = getattr(lib, name)
+        f.restype = ctypes.c_int
+        f.argtypes = [ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
     return lib
 
 
@@ -196,3 +218,97 @@ def all_pairs(total_rows: int, num_heads: int):
     rows = np.repeat(np.arange(total_rows, dtype=np.int64), num_heads)
     heads = np.tile(np.arange(num_heads, dtype=np.int32), total_rows)
     return rows, heads
+
+
+# ---------------------------------------------------------------- FP8 (E4M3)
+
+def e4m3_round(x, lib=None) -> np.ndarray:
+    """Nearest OCP FP8 E4M3 value of each element (ties to even, saturating at
+    +-448), as fp64."""
+    lib = lib or load_library()
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    out = np.empty_like(a)
+    lib.oracle_e4m3_round(a.size, a.ctypes.data, out.ctypes.data)
+    return out
+
+
+def e4m3_decode(codes, lib=None) -> np.ndarray:
+    """Values of E4M3 codes (uint8), as fp64."""
+    lib = lib or load_library()
+    c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+    out = np.empty(c.shape, dtype=np.float64)
+    lib.oracle_e4m3_decode(c.size, c.ctypes.data, out.ctypes.data)
+    return out
+
+
+def e4m3_encode(x, lib=None) -> np.ndarray:
+    """E4M3 codes (uint8) of the values nearest to x."""
+    lib = lib or load_library()
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    out = np.empty(a.shape, dtype=np.uint8)
+    lib.oracle_e4m3_encode(a.size, a.ctypes.data, out.ctypes.data)
+    return out
+
+
+def quantize_e4m3(x: torch.Tensor, cu_seqlens, lib=None):
+    """Per-(segment, head) E4M3 quantisation of a [rows, H, D] tensor: the
+    descale of (b, h) is amax / 448 over the segment's rows of head h (1 for
+    an all-zero block), the codes are e4m3(x / descale).  Returns the codes
+    as a uint8 [rows, H, D] tensor and the descales as fp64 [batch * H]."""
+    xs = x.double().numpy()
+    cu = [int(c) for c in cu_seqlens]
+    B, H = len(cu) - 1, xs.shape[1]
+    desc = np.ones(B * H, dtype=np.float64)
+    scaled = np.zeros_like(xs)
+    for b in range(B):
+        blk = xs[cu[b]:cu[b + 1]]
+        for h in range(H):
+            amax = float(np.abs(blk[:, h]).max()) if blk.shape[0] else 0.0
+            if amax > 0:
+                desc[b * H + h] = amax / 448.0
+            scaled[cu[b]:cu[b + 1], h] = blk[:, h] / desc[b * H + h]
+    return torch.from_numpy(e4m3_encode(scaled, lib)), desc
+
+
+class Fp8Problem:
+    """One FP8 (E4M3) forward problem: codes as uint8 [rows, H, D] CPU tensors
+    (unit innermost stride) and fp64 descales [batch * H] per tensor."""
+
+    def __init__(self, q8, k8, v8, cu_q, cu_k, scale, q_descale, k_descale, v_descale, quantize_p=True):
+        for t in (q8, k8, v8):
+            if t.dtype != torch.uint8 or t.dim() != 3 or t.stride(2) != 1:
+                raise ValueError("FP8 operands are uint8 [rows, H, D] tensors with unit innermost stride")
+        self.H, self.D = int(q8.shape[1]), int(q8.shape[2])
+        self.cu_q = torch.as_tensor(cu_q, dtype=torch.int32).contiguous()
+        self.cu_k = torch.as_tensor(cu_k, dtype=torch.int32).contiguous()
+        B = self.cu_q.numel() - 1
+        self.desc = [np.ascontiguousarray(np.asarray(d, dtype=np.float64).reshape(-1)) for d in
+                     (q_descale, k_descale, v_descale)]
+        if any(d.size != B * self.H for d in self.desc):
+            raise ValueError("descales need batch * num_heads entries")
+        self._keep = (q8, k8, v8, self.cu_q, self.cu_k, self.desc)
+        s = _Fp8Problem()
+        s.q, s.k, s.v = q8.data_ptr(), k8.data_ptr(), v8.data_ptr()
+        s.q_rs, s.q_hs = q8.stride(0), q8.stride(1)
+        s.k_rs, s.k_hs = k8.stride(0), k8.stride(1)
+        s.v_rs, s.v_hs = v8.stride(0), v8.stride(1)
+        s.cu_q, s.cu_k = self.cu_q.data_ptr(), self.cu_k.data_ptr()
+        s.batch, s.num_heads, s.head_dim = B, self.H, self.D
+        s.scale = float(scale)
+        s.q_descale, s.k_descale, s.v_descale = (d.ctypes.data for d in self.desc)
+        s.quantize_p = 1 if quantize_p else 0
+        self._s = s
+
+    def fwd(self, rows, heads, lib=None):
+        """O rows [n, D] and LSE [n] for (q row, head) pairs."""
+        lib = lib or load_library()
+        rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1))
+        heads = np.ascontiguousarray(np.asarray(heads, dtype=np.int32).reshape(-1))
+        n = rows.size
+        o = np.empty((n, self.D), dtype=np.float64)
+        l = np.empty(n, dtype=np.float64)
+        if n:
+            lib.oracle_fwd_fp8(ctypes.byref(self._s), n, rows.ctypes.data, heads.ctypes.data, o.ctypes.data,
+                               l.ctypes.data)
+        return o, l
+

@@ -338,3 +338,149 @@ int oracle_num_threads(void) {
     return 1;
 #endif
 }
+
+/* ------------------------------------------------------------ FP8 forward
+ *
+ * Low-precision forward.  The pages quote quantised attention only by its
+ * accuracy (the ffpa-attn NVFP4 pull request, "Summary": cos ~0.982 against
+ * SDPA) and mention an fp8 fallback (the "[FA4][SM120]" issue, "Practical
+ * workaround"); neither defines the arithmetic.  This oracle takes the
+ * plainest reading for OCP FP8 E4M3 ("e4m3fn": 1 sign, 4 exponent (bias 7),
+ * 3 mantissa bits, no infinities, largest finite 448, code 0x7F / 0xFF NaN):
+ * Q, K, V are E4M3 codes with one fp32 descale factor per (segment, head)
+ * and tensor, and for q row i of segment b, head h:
+ *     s_ij  = scale * qd[b,h] * kd[b,h] * sum_d q8[i,d] k8[j,d]
+ *     m_i   = max_j s_ij,   p_ij = exp(s_ij - m_i),   l_i = sum_j p_ij
+ *     o_i   = vd[b,h] * sum_j e4m3(p_ij) v8[j] / l_i
+ *     LSE_i = m_i + ln l_i
+ * where e4m3(x) rounds to the nearest E4M3 value, ties to even, saturating
+ * at +-448 (P is rounded to E4M3 for the P V product; the row sum uses the
+ * unrounded p).  quantize_p = 0 skips that rounding.  Empty key sets give
+ * LSE = -inf and o = 0, as above.  No mask.
+ */
+
+/* Value of an E4M3 code. */
+static double e4m3_value(uint8_t c) {
+    const int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);           /* subnormal: m * 2^-9 */
+    else v = ldexp((double)(8 + m), e - 10);        /* (1 + m/8) * 2^(e-7) */
+    return s ? -v : v;
+}
+
+/* Nearest E4M3 value to x (ties to even), saturating at +-448; NaN stays. */
+static double e4m3_round(double x) {
+    if (isnan(x)) return x;
+    const double a = fabs(x);
+    if (a == 0.0) return x;
+    int e;
+    frexp(a, &e);                 /* a = f * 2^e, f in [0.5, 1): a in [2^(e-1), 2^e) */
+    int E = e - 1;
+    if (E < -6) E = -6;           /* below the smallest normal the spacing stays 2^-9 */
+    const double q = ldexp(1.0, E - 3);
+    double r = nearbyint(a / q) * q;   /* default rounding mode: to nearest, ties to even */
+    if (r > 448.0) r = 448.0;
+    return x < 0 ? -r : r;
+}
+
+/* Code of an E4M3 value (x must be one: e4m3_round's output). */
+static uint8_t e4m3_code(double x) {
+    if (isnan(x)) return 0x7F;
+    const uint8_t s = (signbit(x) ? 0x80 : 0);
+    const double a = fabs(x);
+    if (a == 0.0) return s;
+    int e;
+    frexp(a, &e);
+    const int E = e - 1;
+    if (E < -6) return (uint8_t)(s | (uint8_t)(a / ldexp(1.0, -9)));        /* subnormal */
+    const int m = (int)(a / ldexp(1.0, E - 3)) - 8;
+    return (uint8_t)(s | ((E + 7) << 3) | m);
+}
+
+int oracle_e4m3_round(int64_t n, const double *in, double *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = e4m3_round(in[i]);
+    return 0;
+}
+
+int oracle_e4m3_decode(int64_t n, const uint8_t *in, double *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = e4m3_value(in[i]);
+    return 0;
+}
+
+/* Codes of the values nearest to in[i] (rounded as e4m3_round). */
+int oracle_e4m3_encode(int64_t n, const double *in, uint8_t *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = e4m3_code(e4m3_round(in[i]));
+    return 0;
+}
+
+typedef struct {
+    const uint8_t *q, *k, *v;       /* E4M3 codes                           */
+    int64_t q_rs, q_hs;             /* row / head strides, in elements      */
+    int64_t k_rs, k_hs;
+    int64_t v_rs, v_hs;
+    const int32_t *cu_q, *cu_k;     /* batch + 1 entries each               */
+    int32_t batch, num_heads, head_dim;
+    double scale;
+    const double *q_descale, *k_descale, *v_descale;  /* [batch * num_heads] */
+    int32_t quantize_p;             /* 1: P rounded to E4M3 for P V         */
+} oracle_fp8_problem;
+
+static void load_row8(const uint8_t *base, int64_t rs, int64_t hs, int64_t row, int32_t h, int32_t D, double *x) {
+    const int64_t off = row * rs + (int64_t)h * hs;
+    for (int32_t d = 0; d < D; ++d) x[d] = e4m3_value(base[off + d]);
+}
+
+/*
+ * FP8 forward on selected (q row, head) pairs, by the definition above.
+ *   out : [n][D] fp64;  lse : [n] fp64.  Rows outside every segment: NaN.
+ */
+int oracle_fwd_fp8(const oracle_fp8_problem *pb, int64_t n, const int64_t *rows, const int32_t *heads,
+                   double *out, double *lse) {
+    const int32_t D = pb->head_dim, H = pb->num_heads;
+    const int64_t smax = max_seg_len(pb->cu_k, pb->batch);
+#pragma omp parallel
+    {
+        double *qi = malloc(sizeof(double) * D), *kj = malloc(sizeof(double) * D);
+        double *s = malloc(sizeof(double) * smax);
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t t = 0; t < n; ++t) {
+            const int64_t i = rows[t];
+            const int32_t h = heads[t];
+            double *o = out + t * D;
+            const int32_t b = segment_of(pb->cu_q, pb->batch, i);
+            if (b < 0) {
+                for (int32_t d = 0; d < D; ++d) o[d] = NAN;
+                lse[t] = NAN;
+                continue;
+            }
+            const int64_t k0 = pb->cu_k[b], Sk = (int64_t)pb->cu_k[b + 1] - pb->cu_k[b];
+            const int64_t bh = (int64_t)b * H + h;
+            const double sqk = pb->scale * pb->q_descale[bh] * pb->k_descale[bh];
+            for (int32_t d = 0; d < D; ++d) o[d] = 0.0;
+            if (Sk <= 0) {
+                lse[t] = -INFINITY;
+                continue;
+            }
+            load_row8(pb->q, pb->q_rs, pb->q_hs, i, h, D, qi);
+            double m = -INFINITY;
+            for (int64_t j = 0; j < Sk; ++j) {
+                load_row8(pb->k, pb->k_rs, pb->k_hs, k0 + j, h, D, kj);
+                s[j] = sqk * dot(qi, kj, D);
+                if (s[j] > m) m = s[j];
+            }
+            double l = 0.0;
+            for (int64_t j = 0; j < Sk; ++j) l += exp(s[j] - m);
+            for (int64_t j = 0; j < Sk; ++j) {
+                double p = exp(s[j] - m);
+                if (pb->quantize_p) p = e4m3_round(p);
+                load_row8(pb->v, pb->v_rs, pb->v_hs, k0 + j, h, D, kj);
+                for (int32_t d = 0; d < D; ++d) o[d] += p * kj[d];
+            }
+            for (int32_t d = 0; d < D; ++d) o[d] *= pb->v_descale[bh] / l;
+            lse[t] = m + log(l);
+        }
+        free(qi); free(kj); free(s);
+    }
+    return 0;
+}

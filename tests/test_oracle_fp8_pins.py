@@ -1,0 +1,198 @@
+"""Pins for the FP8 (OCP E4M3) part of the fp64 oracle: the codec against
+torch's float8_e4m3fn (a library routine), saturation by the format's
+definition, the quantised forward against the fp64 oracle on the dequantised
+inputs, closed forms (one key, two keys with P rounded by torch), the bound
+that rounding P may move O by, and planted mistakes."""
+import math
+import subprocess
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+
+def _cu(lens):
+    return [0] + list(np.cumsum(lens).astype(int))
+
+
+def _fp8_case(seed, lq=(5, 0, 9, 1, 6), lk=(7, 4, 9, 1, 0), H=2, D=16):
+    """E4M3 operands from per-(segment, head) quantisation of random data,
+    with amplitudes that differ between heads."""
+    g = torch.Generator().manual_seed(seed)
+    cq, ck = _cu(lq), _cu(lk)
+    amp = torch.tensor([1.0, 3.0])[:H].view(1, H, 1)
+    q = torch.randn(cq[-1], H, D, generator=g, dtype=torch.float64) * amp
+    k = torch.randn(ck[-1], H, D, generator=g, dtype=torch.float64) * amp
+    v = torch.randn(ck[-1], H, D, generator=g, dtype=torch.float64) * amp
+    q8, qd = oracle.quantize_e4m3(q, cq)
+    k8, kd = oracle.quantize_e4m3(k, ck)
+    v8, vd = oracle.quantize_e4m3(v, ck)
+    return cq, ck, (q, k, v), (q8, k8, v8), (qd, kd, vd)
+
+
+def _dequant(t8, desc, cu, H, lib=None):
+    x = oracle.e4m3_decode(t8.numpy(), lib)
+    for b in range(len(cu) - 1):
+        for h in range(H):
+            x[cu[b]:cu[b + 1], h] *= desc[b * H + h]
+    return torch.from_numpy(x)
+
+
+def _battery(lib):
+    res = []
+    # codec: every code against torch's float8_e4m3fn view
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_decode(codes, lib)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    res.append(("decode_all_codes", bool(np.array_equal(np.isnan(ours), np.isnan(ref))
+                                         and np.array_equal(ours[~np.isnan(ours)], ref[~np.isnan(ref)]))))
+    # rounding: random values inside the finite range (torch rounds to nearest even there)
+    rng = np.random.default_rng(1)
+    x = np.concatenate([rng.uniform(-464, 464, 20000), rng.normal(0, 1, 20000),
+                        rng.normal(0, 2 ** -8, 20000), np.arange(-40, 41) * 2.0 ** -10])
+    r = oracle.e4m3_round(x, lib)
+    rt = torch.from_numpy(x).to(torch.float8_e4m3fn).double().numpy()
+    res.append(("round_matches_torch", bool(np.array_equal(r, rt))))
+    # saturation (the format has no infinity): beyond 448 the nearest finite value is +-448
+    sat = oracle.e4m3_round([465.0, 1e6, -470.0, -1e30], lib)
+    res.append(("round_saturates", bool(np.array_equal(sat, [448.0, 448.0, -448.0, -448.0]))))
+    # encode is the inverse of decode on every finite value
+    fin = ours[~np.isnan(ours)]
+    res.append(("encode_decode_roundtrip",
+                bool(np.array_equal(oracle.e4m3_decode(oracle.e4m3_encode(fin, lib), lib), fin))))
+
+    cq, ck, (q, k, v), (q8, k8, v8), (qd, kd, vd) = _fp8_case(3)
+    H, D = q.shape[1], q.shape[2]
+    sc = 0.29
+    rows, heads = oracle.all_pairs(cq[-1], H)
+    # quantiser: the block maximum maps to +-448 exactly; every element within half a step
+    deq = _dequant(q8, qd, cq, H, lib)
+    ok_q = True
+    for b in range(len(cq) - 1):
+        for h in range(H):
+            blk, dq = q[cq[b]:cq[b + 1], h], deq[cq[b]:cq[b + 1], h]
+            if blk.numel() == 0:
+                continue
+            d = qd[b * H + h]
+            ok_q &= abs(float(dq.abs().max()) - 448 * d) <= 1e-12 * 448 * d
+            step = torch.clamp(2.0 ** (torch.floor(torch.log2(blk.abs() / d)) - 3), min=2.0 ** -9) * d
+            ok_q &= bool(((dq - blk).abs() <= step / 2 * (1 + 1e-12)).all())
+    res.append(("quantiser_half_step", bool(ok_q)))
+    # without rounding P: the fp64 oracle on the dequantised operands
+    pf = oracle.Fp8Problem(q8, k8, v8, cq, ck, sc, qd, kd, vd, quantize_p=False)
+    o0, l0 = pf.fwd(rows, heads, lib)
+    pr = oracle.Problem(_dequant(q8, qd, cq, H, lib), _dequant(k8, kd, ck, H, lib), _dequant(v8, vd, ck, H, lib),
+                        cq, ck, sc)
+    orf, lrf = pr.fwd(rows, heads)
+    res.append(("unrounded_equals_fp64_oracle", bool(np.allclose(o0, orf, rtol=1e-12, atol=1e-13)
+                                                     and np.allclose(lse_fin(l0), lse_fin(lrf), rtol=1e-12,
+                                                                     atol=1e-13)
+                                                     and np.array_equal(np.isneginf(l0), np.isneginf(lrf)))))
+    # with rounding: O moves by at most 2^-4 of sum_j p_j |v_j| / l per element
+    p1 = oracle.Fp8Problem(q8, k8, v8, cq, ck, sc, qd, kd, vd, quantize_p=True)
+    o1, l1 = p1.fwd(rows, heads, lib)
+    vdq = _dequant(v8, vd, ck, H, lib)
+    ok_b = bool(np.array_equal(l0, l1))
+    for t, (i, h) in enumerate(zip(rows, heads)):
+        b = int(np.searchsorted(cq, i, side="right") - 1)
+        if ck[b + 1] == ck[b]:
+            ok_b &= bool(np.all(o1[t] == 0))
+            continue
+        vb = vdq[ck[b]:ck[b + 1], h].numpy()
+        kb = _dequant(k8, kd, ck, H, lib)[ck[b]:ck[b + 1], h].numpy()
+        qi = _dequant(q8, qd, cq, H, lib)[i, h].numpy()
+        sv = sc * kb @ qi
+        p = np.exp(sv - sv.max())
+        bound = 2.0 ** -4 * (p @ np.abs(vb)) / p.sum()
+        ok_b &= bool(np.all(np.abs(o1[t] - o0[t]) <= bound * (1 + 1e-9) + 1e-15))
+    res.append(("rounding_bound", ok_b))
+    # one key: p = 1 is exact, o = vd * v8 exactly, LSE = s exactly
+    b = 3  # lq = lk = 1
+    sel = rows == cq[b]
+    ok1 = True
+    for t in np.nonzero(sel)[0]:
+        h = heads[t]
+        ok1 &= bool(np.array_equal(o1[t], vdq[ck[b], h].numpy()))
+    res.append(("one_key_exact", ok1))
+    # two keys: closed form with P rounded by torch's float8 conversion
+    cq2, ck2 = [0, 1], [0, 2]
+    q2 = torch.tensor([[[2.0, -1.0, 0.5, 0.0]]])
+    k2 = torch.tensor([[[1.0, 0.25, -2.0, 3.0]], [[-0.5, 1.5, 0.0, 1.0]]])
+    v2 = torch.tensor([[[1.0, -2.0, 4.0, 0.5]], [[-3.0, 0.75, 1.0, 2.0]]])
+    enc = lambda t: torch.from_numpy(oracle.e4m3_encode(t.double().numpy(), lib))
+    qd2, kd2, vd2 = [0.5], [0.25], [2.0]
+    p2 = oracle.Fp8Problem(enc(q2), enc(k2), enc(v2), cq2, ck2, 0.7, qd2, kd2, vd2)
+    o2, l2 = p2.fwd([0], [0], lib)
+    s2 = 0.7 * 0.5 * 0.25 * (k2[:, 0].double() @ q2[0, 0].double())
+    e = torch.exp(s2 - s2.max())
+    pr2 = e.to(torch.float8_e4m3fn).double()
+    o_exp = 2.0 * (pr2 @ v2[:, 0].double()) / e.sum()
+    res.append(("two_key_closed_form", bool(np.allclose(o2[0], o_exp.numpy(), rtol=1e-14, atol=1e-15)
+                                            and abs(l2[0] - float(s2.max() + torch.log(e.sum()))) < 1e-14)))
+    return res
+
+
+def lse_fin(x):
+    return np.where(np.isfinite(x), x, 0.0)
+
+
+def test_fp8_oracle_battery():
+    res = _battery(oracle.load_library())
+    bad = [n for n, ok in res if not ok]
+    assert not bad, bad
+
+
+MUTANTS = [
+    ("rounding truncates", "double r = nearbyint(a / q) * q;", "double r = floor(a / q) * q;"),
+    ("no saturation", "if (r > 448.0) r = 448.0;", "(void)0;"),
+    ("subnormal spacing", "if (E < -6) E = -6;", "if (E < -7) E = -7;"),
+    ("decode exponent bias", "else v = ldexp((double)(8 + m), e - 10);", "else v = ldexp((double)(8 + m), e - 11);"),
+    ("k descale dropped", "const double sqk = pb->scale * pb->q_descale[bh] * pb->k_descale[bh];",
+     "const double sqk = pb->scale * pb->q_descale[bh];"),
+    ("v descale dropped", "o[d] *= pb->v_descale[bh] / l;", "o[d] *= 1.0 / l;"),
+    ("row sum of rounded p", "for (int64_t j = 0; j < Sk; ++j) l += exp(s[j] - m);",
+     "for (int64_t j = 0; j < Sk; ++j) l += e4m3_round(exp(s[j] - m));"),
+    ("descale of the wrong head", "const int64_t bh = (int64_t)b * H + h;", "const int64_t bh = (int64_t)b * H;"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_fp8_planted_mistake_is_caught(tmp_path, name, old, new):
+    src = open(oracle._SRC).read()
+    assert src.count(old) >= 1, "mutation anchor missing: %s" % name
+    mut = tmp_path / "mutant.c"
+    mut.write_text(src.replace(old, new))
+    lib_path = str(tmp_path / "libmutant.so")
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fopenmp", "-shared", "-fPIC", "-o", lib_path, str(mut), "-lm"],
+                   check=True)
+    lib = oracle.load_library(lib_path)
+    try:
+        res = _battery(lib)
+    except Exception:
+        return
+    assert any(not ok for _, ok in res), "planted mistake '%s' not caught" % name
+
+
+def test_fp8_accuracy_envelope():
+    """The method's own error: E4M3 operands with per-(segment, head) scaling,
+    and P rounded to E4M3, against the fp64 oracle on the unquantised bf16
+    inputs (the pages quote cos ~0.982 for NVFP4 against SDPA).  Measured:
+    cos 0.9989 with exact P, 0.9987 with P rounded; bounds with margin."""
+    from packed_variable_length_varlen_gb300 import workloads as W
+    w = W.custom("fp8_envelope", [300, 129, 517, 64], [300, 517, 129, 700], 4, 128)
+    cpu = W.make_inputs(w, 0)
+    q8, qd = oracle.quantize_e4m3(cpu.q, w.cu_q)
+    k8, kd = oracle.quantize_e4m3(cpu.k, w.cu_k)
+    v8, vd = oracle.quantize_e4m3(cpu.v, w.cu_k)
+    rows, heads = oracle.all_pairs(w.total_q, w.num_heads)
+    ref, _ = oracle.Problem(cpu.q, cpu.k, cpu.v, w.cu_q, w.cu_k, w.softmax_scale).fwd(rows, heads)
+    cos = {}
+    for qp in (False, True):
+        o, _ = oracle.Fp8Problem(q8, k8, v8, w.cu_q, w.cu_k, w.softmax_scale, qd, kd, vd, quantize_p=qp).fwd(rows,
+                                                                                                               heads)
+        cos[qp] = float((o * ref).sum() / np.linalg.norm(o) / np.linalg.norm(ref))
+    print("fp8 cosine vs fp64", cos)
+    assert cos[False] >= 0.998 and cos[True] >= 0.998
+    assert cos[False] - cos[True] <= 1e-3
