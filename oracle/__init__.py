@@ -251,23 +251,25 @@ def e4m3_encode(x, lib=None) -> np.ndarray:
 
 
 def quantize_e4m3(x: torch.Tensor, cu_seqlens, lib=None):
-    """Per-(segment, head) E4M3 quantisation of a [rows, H, D] tensor: the
-    descale of (b, h) is amax / 448 over the segment's rows of head h (1 for
-    an all-zero block), the codes are e4m3(x / descale).  Returns the codes
-    as a uint8 [rows, H, D] tensor and the descales as fp64 [batch * H]."""
-    xs = x.double().numpy()
+    """Per-(segment, head) E4M3 quantisation of a [rows, H, D] tensor, in fp32
+    arithmetic (the precision that decides each code): the descale of (b, h)
+    is fp32(amax) / 448 over the segment's rows of head h (1 for an all-zero
+    block), the code of x is e4m3(fp32(x) / descale) with an IEEE fp32
+    division.  Returns the codes as a uint8 [rows, H, D] tensor and the
+    descales [batch * H] (fp32 values held in fp64)."""
+    xs = x.float().numpy()
     cu = [int(c) for c in cu_seqlens]
     B, H = len(cu) - 1, xs.shape[1]
-    desc = np.ones(B * H, dtype=np.float64)
-    scaled = np.zeros_like(xs)
+    desc = np.ones(B * H, dtype=np.float32)
+    scaled = np.zeros(xs.shape, dtype=np.float32)
     for b in range(B):
         blk = xs[cu[b]:cu[b + 1]]
         for h in range(H):
-            amax = float(np.abs(blk[:, h]).max()) if blk.shape[0] else 0.0
+            amax = np.float32(np.abs(blk[:, h]).max()) if blk.shape[0] else np.float32(0)
             if amax > 0:
-                desc[b * H + h] = amax / 448.0
+                desc[b * H + h] = amax / np.float32(448.0)
             scaled[cu[b]:cu[b + 1], h] = blk[:, h] / desc[b * H + h]
-    return torch.from_numpy(e4m3_encode(scaled, lib)), desc
+    return torch.from_numpy(e4m3_encode(scaled.astype(np.float64), lib)), desc.astype(np.float64)
 
 
 class Fp8Problem:
