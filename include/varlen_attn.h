@@ -189,6 +189,37 @@ int varlen_attn_bwd_deterministic(const void* q, varlen_stride sq, const void* k
                                   void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * E4M3 (FP8) forward (not on the pages, which quote quantised attention
+ * only by its accuracy: the ffpa-attn NVFP4 pull request, "Summary", cos
+ * ~0.982 against SDPA).  Arguments, layouts and errors as varlen_attn_fwd;
+ * head_dim must be 128 (else VARLEN_ERR_HEAD_DIM), no mask.  q, k, v (bf16)
+ * are quantised per (segment, head) and tensor into the caller's workspace
+ * (varlen_attn_fwd_fp8_workspace_size bytes, 256-byte aligned, contents on
+ * entry irrelevant): descale = amax / 448 (1 for an all-zero block), code =
+ * E4M3(x / descale), round to nearest even, saturating, in fp32.  Then, per
+ * q row, s = scale * qd * kd * (q8 . k8), P = exp(s - max) (fp32),
+ * O = vd * sum_j E4M3(P_j) v8_j / sum_j P_j (bf16 out), LSE = max + ln sum P.
+ * P is rounded from a running row maximum, so results match that definition
+ * up to the rounding of P (a relative 2^-4 per weight).
+ *
+ * varlen_attn_fwd_fp8_workspace_layout returns the byte offsets of the
+ * workspace sections after a call: offsets[0] amax fp32 [3][batch * H] (q,
+ * k, v; entry b * H + h), offsets[1] q codes [total_q][H][128], offsets[2] k
+ * codes [total_k][H][128], offsets[3] V^T codes [H][128][*vt_cols], where
+ * segment b's key j sits at column 128 * (b + ceil(cu_seqlens_k[b] / 128)) + j
+ * (code 0 past the segment's end up to the next multiple of 128).
+ */
+size_t varlen_attn_fwd_fp8_workspace_size(int32_t batch, int32_t total_q, int32_t total_k, int32_t num_heads,
+                                          int32_t head_dim);
+int varlen_attn_fwd_fp8_workspace_layout(int32_t batch, int32_t total_q, int32_t total_k, int32_t num_heads,
+                                         int32_t head_dim, size_t* offsets, int64_t* vt_cols);
+int varlen_attn_fwd_fp8(const void* q, varlen_stride sq, const void* k, varlen_stride sk, const void* v,
+                        varlen_stride sv, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t batch,
+                        int32_t total_q, int32_t total_k, int32_t num_heads, int32_t head_dim, int32_t max_seqlen_q,
+                        int32_t max_seqlen_k, float scale, void* out, varlen_stride so, float* lse,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Dense batched attention: q, out, dout, dq are [batch, seqlen_q, H, D] and
  * k, v, dk, dv are [batch, seqlen_k, H, D] (bf16), each with its own strides
  * in elements and a unit innermost stride; lse is [H, batch * seqlen_q]

@@ -152,6 +152,46 @@ std::mutex g_phase_mu;
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// E4M3 codes [rows][H][128] as a 3-D uint8 tensor map {128, H, rows} with
+// {128, 1, 128} boxes in the 128-byte swizzle.
+int encode_codes_nhd(CUtensorMap* map, void* base, int64_t rows, int32_t H) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return VARLEN_ERR_CUDA;
+  cuuint64_t dims[3] = {128u, (cuuint64_t)H, (cuuint64_t)(rows > 0 ? rows : 1)};
+  cuuint64_t strides[2] = {128u, (cuuint64_t)H * 128u};
+  cuuint32_t box[3] = {128u, 1u, 128u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? VARLEN_OK : VARLEN_ERR_STRIDE;
+}
+
+// V^T codes [H][128][kp] as {kp, 128, H} with {128, 128, 1} boxes.
+int encode_codes_vt(CUtensorMap* map, void* base, int64_t kp, int32_t H) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return VARLEN_ERR_CUDA;
+  cuuint64_t dims[3] = {(cuuint64_t)kp, 128u, (cuuint64_t)H};
+  cuuint64_t strides[2] = {(cuuint64_t)kp, (cuuint64_t)kp * 128u};
+  cuuint32_t box[3] = {128u, 128u, 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? VARLEN_OK : VARLEN_ERR_STRIDE;
+}
+
+// Workspace sections of the E4M3 forward: amax [3][batch * H] fp32, then
+// the Q and K codes, then V^T; each section 256-byte aligned.
+void fp8_sections(int32_t batch, int32_t total_q, int32_t total_k, int32_t H, size_t off[5]) {
+  const size_t kp = (size_t)fp8_vt_cols(batch, total_k);
+  off[0] = 0;
+  off[1] = off[0] + round256((size_t)3 * batch * H * sizeof(float));
+  off[2] = off[1] + round256((size_t)total_q * H * 128);
+  off[3] = off[2] + round256((size_t)total_k * H * 128);
+  off[4] = off[3] + round256((size_t)H * 128 * kp);
+}
+
 }  // namespace
 }  // namespace varlen
 
@@ -470,6 +510,90 @@ extern "C" int varlen_attn_bwd_dense(const void* q, varlen_dense_stride sq, cons
   return bwd_impl(q, vq, k, vk, v, vv, out, vo, dout, vdo, lse, CuView{nullptr, seqlen_q}, CuView{nullptr, seqlen_k},
                   batch, total_q, total_k, num_heads, head_dim, seqlen_q, seqlen_k, scale, dq, vdq, dk, vdk, dv, vdv,
                   workspace, workspace_bytes, stream, causal ? kCausal : kNoMask);
+}
+
+// ------------------------------------------------------------ FP8 (E4M3)
+
+extern "C" size_t varlen_attn_fwd_fp8_workspace_size(int32_t batch, int32_t total_q, int32_t total_k,
+                                                     int32_t num_heads, int32_t head_dim) {
+  if (batch < 0 || total_q < 0 || total_k < 0 || num_heads < 0 || head_dim != 128) return 0;
+  size_t off[5];
+  fp8_sections(batch, total_q, total_k, num_heads, off);
+  return off[4];
+}
+
+extern "C" int varlen_attn_fwd_fp8_workspace_layout(int32_t batch, int32_t total_q, int32_t total_k,
+                                                    int32_t num_heads, int32_t head_dim, size_t* offsets,
+                                                    int64_t* vt_cols) {
+  if (offsets == nullptr || vt_cols == nullptr) return VARLEN_ERR_NULL;
+  if (batch < 1 || total_q < 0 || total_k < 0 || num_heads < 1) return VARLEN_ERR_SHAPE;
+  if (head_dim != 128) return VARLEN_ERR_HEAD_DIM;
+  size_t off[5];
+  fp8_sections(batch, total_q, total_k, num_heads, off);
+  for (int i = 0; i < 4; ++i) offsets[i] = off[i];
+  *vt_cols = fp8_vt_cols(batch, total_k);
+  return VARLEN_OK;
+}
+
+extern "C" int varlen_attn_fwd_fp8(const void* q, varlen_stride sq, const void* k, varlen_stride sk, const void* v,
+                                   varlen_stride sv, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                   int32_t batch, int32_t total_q, int32_t total_k, int32_t num_heads,
+                                   int32_t head_dim, int32_t max_seqlen_q, int32_t max_seqlen_k, float scale,
+                                   void* out, varlen_stride so, float* lse, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  (void)max_seqlen_q;
+  (void)max_seqlen_k;
+  if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr) return VARLEN_ERR_NULL;
+  int st = check_common(batch, total_q, total_k, num_heads, head_dim, scale);
+  if (st != VARLEN_OK) return st;
+  if (head_dim != 128) return VARLEN_ERR_HEAD_DIM;
+  if ((st = check_operand(q, sq, total_q, num_heads, head_dim)) != VARLEN_OK) return st;
+  if ((st = check_operand(k, sk, total_k, num_heads, head_dim)) != VARLEN_OK) return st;
+  if ((st = check_operand(v, sv, total_k, num_heads, head_dim)) != VARLEN_OK) return st;
+  if ((st = check_operand(out, so, total_q, num_heads, head_dim)) != VARLEN_OK) return st;
+  if (total_q > 0 && lse == nullptr) return VARLEN_ERR_NULL;
+  size_t off[5];
+  fp8_sections(batch, total_q, total_k, num_heads, off);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < off[4])
+    return VARLEN_ERR_WORKSPACE;
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != VARLEN_OK) return st;
+  if (total_q == 0 && total_k == 0) return VARLEN_OK;
+  char* ws = static_cast<char*>(workspace);
+  Fp8Launch L;
+  std::memset(&L, 0, sizeof(L));
+  L.p.q = static_cast<const __nv_bfloat16*>(q);
+  L.p.k = static_cast<const __nv_bfloat16*>(k);
+  L.p.v = static_cast<const __nv_bfloat16*>(v);
+  L.p.q_rs = sq.row;
+  L.p.q_hs = sq.head;
+  L.p.k_rs = sk.row;
+  L.p.k_hs = sk.head;
+  L.p.v_rs = sv.row;
+  L.p.v_hs = sv.head;
+  L.p.out = static_cast<__nv_bfloat16*>(out);
+  L.p.o_rs = so.row;
+  L.p.o_hs = so.head;
+  L.p.lse = lse;
+  L.p.amax = reinterpret_cast<float*>(ws + off[0]);
+  L.p.q8 = reinterpret_cast<uint8_t*>(ws + off[1]);
+  L.p.k8 = reinterpret_cast<uint8_t*>(ws + off[2]);
+  L.p.vt = reinterpret_cast<uint8_t*>(ws + off[3]);
+  L.p.kp = fp8_vt_cols(batch, total_k);
+  L.p.cu_q = CuView{cu_seqlens_q, 0};
+  L.p.cu_k = CuView{cu_seqlens_k, 0};
+  L.p.batch = batch;
+  L.p.total_q = total_q;
+  L.p.total_k = total_k;
+  L.p.num_heads = num_heads;
+  L.p.scale = scale;
+  L.p.err = dev.err;
+  L.grid = dev.sms;
+  if ((st = encode_codes_nhd(&L.tm_q8, L.p.q8, total_q, num_heads)) != VARLEN_OK) return st;
+  if ((st = encode_codes_nhd(&L.tm_k8, L.p.k8, total_k, num_heads)) != VARLEN_OK) return st;
+  if ((st = encode_codes_vt(&L.tm_vt, L.p.vt, L.p.kp, num_heads)) != VARLEN_OK) return st;
+  cudaError_t e = launch_fwd_fp8(L, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? VARLEN_OK : cuda_fail(e);
 }
 
 extern "C" int varlen_attn_get_device_status(void* stream) {

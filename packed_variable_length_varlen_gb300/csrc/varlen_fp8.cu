@@ -1,0 +1,546 @@
+// varlen_fp8.cu -- E4M3 (FP8) forward of packed variable-length attention on
+// sm_103a, head size 128, no mask.
+//
+// Four launches on the caller's stream:
+//  1. varlen_fp8_amax_kernel: max |x| of Q, K and V per (segment, head),
+//     by atomic max on the fp32 bit patterns (non-negative floats order as
+//     unsigned integers).
+//  2. varlen_fp8_quant_kernel: Q and K to E4M3 codes in NHD layout, code of
+//     x = e4m3(x / descale), descale = amax / 448 (1 for an all-zero block),
+//     round to nearest even, saturating (fp32 division and conversion: the
+//     precision that decides each code).
+//  3. varlen_fp8_vt_kernel: V to E4M3 codes transposed to [H][128][kp], one
+//     128-key block per CTA visit through shared memory, so that V is a
+//     K-major operand of the P V product; segment starts are multiples of
+//     128 columns and the columns past a segment's end hold code 0.
+//  4. varlen_fp8_fwd_kernel: the forward of the bf16 kernel (two 128-row
+//     halves per scheduled unit sharing each key tile, online softmax with
+//     lazy rescaling) on the codes:
+//         S = Q8 K8^T          (tcgen05 kind::f8f6f4, E4M3 x E4M3 -> fp32)
+//         P = exp2(S * scale*log2e*qd*kd - m),  l += P   (fp32)
+//         O += e4m3(P) V8      (P written to shared memory as E4M3 codes)
+//     and finally O * vd / l in bf16 and LSE = (m + log2 l) ln 2.  The row
+//     sum l uses the unrounded P.
+//
+// The quantised reading is that of the flash-attention family's FP8 forward
+// (one descale per (segment, head) and tensor); the pages themselves quote
+// quantised attention only by its accuracy (the ffpa-attn NVFP4 pull
+// request, "Summary": cos ~0.982 against SDPA).
+#include <cuda_fp8.h>
+
+#include "sm103_ptx.cuh"
+#include "varlen_internal.h"
+#include "varlen_sched.cuh"
+
+namespace varlen {
+
+namespace {
+
+constexpr float kE4m3Max = 448.0f;
+
+__device__ __forceinline__ float descale_of(float amax) { return amax > 0.f ? amax / kE4m3Max : 1.f; }
+
+// Segment holding `row` (the last b with clamp(cu[b]) <= row); false when the
+// row lies in no segment.  Exact for non-decreasing cu_seqlens.
+__device__ __forceinline__ bool segment_of_row(const CuView& cu, int32_t batch, int32_t total, int32_t row,
+                                               int32_t& b) {
+  int32_t b0 = 0, b1 = batch - 1;
+  while (b0 < b1) {
+    const int32_t mid = (b0 + b1 + 1) >> 1;
+    if (clamp_row(cu_at(cu, mid), total) <= row) b0 = mid;
+    else b1 = mid - 1;
+  }
+  b = b0;
+  return row >= clamp_row(cu_at(cu, b0), total) && row < clamp_row(cu_at(cu, b0 + 1), total);
+}
+
+// Eight bf16 (one 16-byte load) as floats.
+__device__ __forceinline__ void load8(const __nv_bfloat16* src, float (&f)[8]) {
+  const uint4 u = __ldg(reinterpret_cast<const uint4*>(src));
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __bfloat1622float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
+// Four E4M3 codes of a / d, b / d, c / d, e / d packed low byte first.
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float e, float d) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a / d, b / d), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c / d, e / d), __NV_SATFINITE, __NV_E4M3);
+  return lo | (hi << 16);
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ amax
+
+__global__ void __launch_bounds__(256) varlen_fp8_amax_kernel(const Fp8Params p) {
+  const int which = blockIdx.y;  // 0 = q, 1 = k, 2 = v
+  const __nv_bfloat16* x = which == 0 ? p.q : (which == 1 ? p.k : p.v);
+  const int64_t rs = which == 0 ? p.q_rs : (which == 1 ? p.k_rs : p.v_rs);
+  const int64_t hs = which == 0 ? p.q_hs : (which == 1 ? p.k_hs : p.v_hs);
+  const CuView cu = which == 0 ? p.cu_q : p.cu_k;
+  const int32_t total = which == 0 ? p.total_q : p.total_k;
+  const int32_t B = p.batch, H = p.num_heads;
+  unsigned int* amax = reinterpret_cast<unsigned int*>(p.amax) + (int64_t)which * B * H;
+  const int32_t lo = clamp_row(cu_at(cu, 0), total), hi = clamp_row(cu_at(cu, B), total);
+  if (hi <= lo) return;
+  const int64_t n = (int64_t)(hi - lo) * H;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n; t += (int64_t)gridDim.x * blockDim.x) {
+    const int32_t row = lo + (int32_t)(t / H);
+    const int h = (int)(t % H);
+    int32_t b;
+    if (!segment_of_row(cu, B, total, row, b)) continue;
+    const __nv_bfloat16* src = x + (int64_t)row * rs + (int64_t)h * hs;
+    float mx = 0.f;
+#pragma unroll 4
+    for (int d = 0; d < 128; d += 8) {
+      float f[8];
+      load8(src + d, f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx = fmaxf(mx, fabsf(f[i]));
+    }
+    atomicMax(amax + (int64_t)b * H + h, __float_as_uint(mx));
+  }
+}
+
+// ------------------------------------------------------------------ Q, K codes
+
+__global__ void __launch_bounds__(256) varlen_fp8_quant_kernel(const Fp8Params p) {
+  const int which = blockIdx.y;  // 0 = q, 1 = k
+  const __nv_bfloat16* x = which == 0 ? p.q : p.k;
+  const int64_t rs = which == 0 ? p.q_rs : p.k_rs;
+  const int64_t hs = which == 0 ? p.q_hs : p.k_hs;
+  const CuView cu = which == 0 ? p.cu_q : p.cu_k;
+  const int32_t total = which == 0 ? p.total_q : p.total_k;
+  uint8_t* dst8 = which == 0 ? p.q8 : p.k8;
+  const int32_t B = p.batch, H = p.num_heads;
+  const float* amax = p.amax + (int64_t)which * B * H;
+  const int32_t lo = clamp_row(cu_at(cu, 0), total), hi = clamp_row(cu_at(cu, B), total);
+  if (hi <= lo) return;
+  const int64_t n = (int64_t)(hi - lo) * H;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n; t += (int64_t)gridDim.x * blockDim.x) {
+    const int32_t row = lo + (int32_t)(t / H);
+    const int h = (int)(t % H);
+    int32_t b;
+    if (!segment_of_row(cu, B, total, row, b)) continue;
+    const float dsc = descale_of(amax[(int64_t)b * H + h]);
+    const __nv_bfloat16* src = x + (int64_t)row * rs + (int64_t)h * hs;
+    uint4* out = reinterpret_cast<uint4*>(dst8 + ((int64_t)row * H + h) * 128);
+#pragma unroll 2
+    for (int d = 0; d < 128; d += 16) {
+      float f[8], g[8];
+      load8(src + d, f);
+      load8(src + d + 8, g);
+      out[d / 16] = make_uint4(e4m3x4(f[0], f[1], f[2], f[3], dsc), e4m3x4(f[4], f[5], f[6], f[7], dsc),
+                               e4m3x4(g[0], g[1], g[2], g[3], dsc), e4m3x4(g[4], g[5], g[6], g[7], dsc));
+    }
+  }
+}
+
+// ------------------------------------------------------------------ V^T codes
+
+// One visit = (segment, 128-key block, head) of the exact schedule on the key
+// side: 256 threads quantise the block's 128 rows (thread = row, half of d)
+// into a [d][key] shared tile, then write 128 rows of 128 codes to vt.
+__global__ void __launch_bounds__(256) varlen_fp8_vt_kernel(const Fp8Params p) {
+  __shared__ __align__(16) uint8_t tile[128 * 128];
+  const int r = threadIdx.x >> 1, half = threadIdx.x & 1;
+  const int32_t B = p.batch, H = p.num_heads;
+  const float* amax = p.amax + 2 * (int64_t)B * H;
+  SegCursor c;
+  cursor_init<128>(c, p.cu_k, p.cu_q, B, p.total_k, p.total_q);
+  for (int64_t t = blockIdx.x; cursor_seek<128>(c, t, H, p.cu_k, p.cu_q, B, p.total_k, p.total_q);
+       t += gridDim.x) {
+    const Tile tl = cursor_tile(c, t);
+    const int32_t valid = min(128, c.len - tl.m * 128);
+    const float dsc = descale_of(amax[(int64_t)c.b * H + tl.h]);
+    uint8_t code[64];
+    if (r < valid) {
+      const __nv_bfloat16* src = p.v + ((int64_t)c.r0 + tl.m * 128 + r) * p.v_rs + (int64_t)tl.h * p.v_hs + half * 64;
+#pragma unroll
+      for (int d = 0; d < 64; d += 8) {
+        float f[8];
+        load8(src + d, f);
+        const uint32_t a = e4m3x4(f[0], f[1], f[2], f[3], dsc), e = e4m3x4(f[4], f[5], f[6], f[7], dsc);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          code[d + i] = (uint8_t)(a >> (8 * i));
+          code[d + 4 + i] = (uint8_t)(e >> (8 * i));
+        }
+      }
+    } else {
+#pragma unroll
+      for (int d = 0; d < 64; ++d) code[d] = 0;  // keys past the segment end: code 0 (value 0)
+    }
+#pragma unroll
+    for (int d = 0; d < 64; ++d) tile[(half * 64 + d) * 128 + r] = code[d];
+    __syncthreads();
+    // row dd of the tile (128 codes) -> vt[h][dd][base + 128 m ...]; thread = (dd, 64-byte part)
+    const int dd = threadIdx.x >> 1, part = threadIdx.x & 1;
+    uint8_t* dst = p.vt + ((int64_t)tl.h * 128 + dd) * p.kp + fp8_vt_base(c.r0, c.b) + (int64_t)tl.m * 128 + part * 64;
+    const uint4* srow = reinterpret_cast<const uint4*>(tile + dd * 128 + part * 64);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) reinterpret_cast<uint4*>(dst)[i] = srow[i];
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------------ forward
+
+namespace {
+
+constexpr int kF8Unit = 2 * kTileM;           // q rows per scheduled unit (two halves)
+constexpr int kF8Tile = 128 * 128;            // one tile: 128 rows of 128 codes
+constexpr int kF8Slots = 8;                   // K / V^T ring slots
+constexpr int kF8SmemBytes = 1024 + 1024 + kF8Tile * (4 + kF8Slots);  // barriers, align, Q_A Q_B P_A P_B, ring
+constexpr int kF8OCol = 256;                  // TMEM column of O_A (O_B at +128); S_A at 0, S_B at 128
+
+struct F8Barriers {
+  uint64_t q_full, q_empty;
+  uint64_t s_full[2], p_full[2], pv_done[2];
+  uint64_t mma_done;
+  uint64_t kv_full[kF8Slots], kv_empty[kF8Slots];
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(F8Barriers) <= 1024, "barrier block too large");
+
+// Registers: 384 threads at 168; control warpgroup 112, softmax 192.
+constexpr uint32_t kF8RegsLaunch = 168, kF8RegsCtl = 112, kF8RegsSoftmax = 192;
+static_assert(kF8RegsCtl + 2 * kF8RegsSoftmax <= 3 * kF8RegsLaunch, "register split exceeds the launch allocation");
+
+}  // namespace
+
+__global__ void __launch_bounds__(384, 1)
+    varlen_fp8_fwd_kernel(const __grid_constant__ CUtensorMap tm_q8, const __grid_constant__ CUtensorMap tm_k8,
+                          const __grid_constant__ CUtensorMap tm_vt, const Fp8Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  F8Barriers& bar = *reinterpret_cast<F8Barriers*>(smem);
+  uint8_t* q_smem = smem + 1024;              // Q_A, Q_B
+  uint8_t* p_smem = q_smem + 2 * kF8Tile;     // P_A, P_B (E4M3, K-major)
+  uint8_t* ring = p_smem + 2 * kF8Tile;
+  volatile int* abort = &bar.abort;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar.q_full, 1);
+    mbar_init(&bar.q_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar.s_full[i], 1);
+      mbar_init(&bar.p_full[i], 128);
+      mbar_init(&bar.pv_done[i], 1);
+    }
+    mbar_init(&bar.mma_done, 1);
+    for (int i = 0; i < kF8Slots; ++i) {
+      mbar_init(&bar.kv_full[i], 1);
+      mbar_init(&bar.kv_empty[i], 1);
+    }
+    bar.abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(&bar.tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar.tmem_base;
+  const int64_t G = gridDim.x;
+  const int32_t H = p.num_heads;
+
+  if (warp < 4) {
+    warpgroup_set_regs<kF8RegsCtl, kF8RegsLaunch>();
+    if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------------- producer
+      tma_prefetch_desc(&tm_q8);
+      tma_prefetch_desc(&tm_k8);
+      tma_prefetch_desc(&tm_vt);
+      SegCursor c;
+      cursor_init<kF8Unit>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k);
+      uint32_t q_loads = 0, ring_pos = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x;
+           ok && cursor_seek<kF8Unit>(c, t, H, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k); t += G) {
+        const Tile tl = cursor_tile(c, t);
+        const int32_t nkv = (c.olen + kTileN - 1) / kTileN;
+        if (nkv == 0) continue;
+        const int32_t qrow = c.r0 + tl.m * kF8Unit;
+        if (q_loads > 0 && !mbar_wait(&bar.q_empty, (q_loads - 1) & 1, abort)) break;
+        mbar_arrive_expect_tx(&bar.q_full, 2 * kF8Tile);
+        tma_load_3d(q_smem, &tm_q8, &bar.q_full, 0, tl.h, qrow);
+        tma_load_3d(q_smem + kF8Tile, &tm_q8, &bar.q_full, 0, tl.h, qrow + kTileM);
+        ++q_loads;
+        const int32_t vt0 = (int32_t)fp8_vt_base(c.o0, c.b);
+        for (int32_t j = 0; ok && j < nkv; ++j) {
+#pragma unroll
+          for (int which = 0; which < 2; ++which) {
+            const uint32_t slot = ring_pos % kF8Slots;
+            if (!mbar_wait(&bar.kv_empty[slot], ((ring_pos / kF8Slots) & 1) ^ 1, abort)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&bar.kv_full[slot], kF8Tile);
+            uint8_t* dst = ring + slot * kF8Tile;
+            if (which == 0) tma_load_3d(dst, &tm_k8, &bar.kv_full[slot], 0, tl.h, c.o0 + j * kTileN);
+            else tma_load_3d(dst, &tm_vt, &bar.kv_full[slot], vt0 + j * kTileN, 0, tl.h);
+            ++ring_pos;
+          }
+        }
+      }
+      if (*abort) {
+        for (uint32_t s = 0; s < (uint32_t)kF8Slots && s < ring_pos; ++s) {
+          const uint32_t last = ring_pos - 1 - ((ring_pos - 1 - s) % kF8Slots);
+          int dummy = 0;
+          mbar_wait(&bar.kv_full[s], (last / kF8Slots) & 1, &dummy, 100000000ull);
+        }
+        if (q_loads > 0) {
+          int dummy = 0;
+          mbar_wait(&bar.q_full, (q_loads - 1) & 1, &dummy, 100000000ull);
+        }
+      }
+    } else if (warp == 1 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      // Per kv step j and half: O += P V_j (P from shared memory), then
+      // S = Q K_{j+1}^T; 4 k-steps of 32 codes per product.
+      constexpr uint32_t kIdesc = idesc_e4m3_f32(128, 128);
+      SegCursor c;
+      cursor_init<kF8Unit>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k);
+      uint32_t tiles = 0, g = 0, ring0 = 0;
+      bool ok = true;
+      const uint32_t qlo = sw128_desc_lo(smem_addr(q_smem), 16);
+      const uint32_t plo = sw128_desc_lo(smem_addr(p_smem), 16);
+      const uint32_t rlo = sw128_desc_lo(smem_addr(ring), 16);
+      auto issue_s = [&](int hf, uint32_t kslot) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_f8_ss_lo(tmem + hf * 128, qlo + ((hf * kF8Tile + kk * 32) >> 4), rlo + ((kslot * kF8Tile + kk * 32) >> 4),
+                       kIdesc, kk > 0 ? 1u : 0u);
+        mma_commit(&bar.s_full[hf]);
+      };
+      auto issue_pv = [&](int hf, uint32_t vslot, bool first) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_f8_ss_lo(tmem + kF8OCol + hf * 128, plo + ((hf * kF8Tile + kk * 32) >> 4),
+                       rlo + ((vslot * kF8Tile + kk * 32) >> 4), kIdesc, (!first || kk > 0) ? 1u : 0u);
+        mma_commit(&bar.pv_done[hf]);  // also: the P buffer of this half is free again
+      };
+      for (int64_t t = blockIdx.x;
+           ok && cursor_seek<kF8Unit>(c, t, H, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k); t += G) {
+        const int32_t nkv = (c.olen + kTileN - 1) / kTileN;
+        if (nkv == 0) continue;
+        if (!mbar_wait(&bar.q_full, tiles & 1, abort)) break;
+        ++tiles;
+        {
+          const uint32_t kslot = ring0 % kF8Slots;
+          if (!mbar_wait(&bar.kv_full[kslot], (ring0 / kF8Slots) & 1, abort)) break;
+          tc_fence_after();
+          issue_s(0, kslot);
+          issue_s(1, kslot);
+          mma_commit(&bar.kv_empty[kslot]);
+          if (nkv == 1) mma_commit(&bar.q_empty);
+        }
+        for (int32_t j = 0; j < nkv; ++j) {
+          const uint32_t gj = g + j;
+          const uint32_t vpos = ring0 + 2 * j + 1;
+          const uint32_t vslot = vpos % kF8Slots;
+          const bool more = j + 1 < nkv;
+          const uint32_t kpos = vpos + 1;
+          const uint32_t kslot = kpos % kF8Slots;
+          if (!mbar_wait(&bar.kv_full[vslot], (vpos / kF8Slots) & 1, abort)) { ok = false; break; }
+          if (more && !mbar_wait(&bar.kv_full[kslot], (kpos / kF8Slots) & 1, abort)) { ok = false; break; }
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            if (!mbar_wait(&bar.p_full[hf], gj & 1, abort)) { ok = false; break; }
+            tc_fence_after();
+            issue_pv(hf, vslot, j == 0);
+            if (more) issue_s(hf, kslot);
+          }
+          if (!ok) break;
+          mma_commit(&bar.kv_empty[vslot]);
+          if (more) {
+            mma_commit(&bar.kv_empty[kslot]);
+            if (j + 1 == nkv - 1) mma_commit(&bar.q_empty);
+          }
+        }
+        g += nkv;
+        ring0 += 2 * nkv;
+      }
+      mma_commit(&bar.mma_done);
+      int dummy = 0;
+      mbar_wait(&bar.mma_done, 0, &dummy);
+    }
+  } else {
+    warpgroup_set_regs<kF8RegsSoftmax, kF8RegsLaunch>();
+    // ------------------------------------------------------------ softmax
+    const int hf = (warp - 4) >> 2;
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const uint32_t s_col = hf * 128, o_col = kF8OCol + hf * 128;
+    uint8_t* prow = p_smem + hf * kF8Tile + row * 128;  // this row of P (128-byte swizzle)
+    SegCursor c;
+    cursor_init<kF8Unit>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k);
+    uint32_t g = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x;
+         ok && cursor_seek<kF8Unit>(c, t, H, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k); t += G) {
+      const Tile tl = cursor_tile(c, t);
+      const int32_t nkv = (c.olen + kTileN - 1) / kTileN;
+      const int32_t r_seg = tl.m * kF8Unit + hf * kTileM + row;
+      const bool row_valid = r_seg < c.len;
+      const int64_t grow = (int64_t)c.r0 + r_seg;
+      __nv_bfloat16* orow = p.out + grow * p.o_rs + (int64_t)tl.h * p.o_hs;
+      float* lse_out = p.lse + (int64_t)tl.h * p.total_q + grow;
+      if (nkv == 0) {
+        if (row_valid) {
+#pragma unroll
+          for (int d = 0; d < 128; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0, 0, 0, 0);
+          *lse_out = -INFINITY;
+        }
+        continue;
+      }
+      const int64_t bh = (int64_t)c.b * H + tl.h;
+      const int64_t nbh = (int64_t)p.batch * H;
+      const float qd = descale_of(__ldg(p.amax + bh)), kd = descale_of(__ldg(p.amax + nbh + bh));
+      const float vd = descale_of(__ldg(p.amax + 2 * nbh + bh));
+      const float c2 = p.scale * 1.4426950408889634f * qd * kd;
+      float m_use = -INFINITY, l = 0.f;
+      for (int32_t j = 0; j < nkv; ++j) {
+        const uint32_t gj = g + j;
+        if (!mbar_wait(&bar.s_full[hf], gj & 1, abort)) { ok = false; break; }
+        tc_fence_after();
+        float x[128];
+        {
+          uint32_t s[32];
+#pragma unroll
+          for (int c0 = 0; c0 < 128; c0 += 32) {
+            tmem_ld32(tmem + lane_off + s_col + c0, s);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[c0 + i] = __uint_as_float(s[i]);
+          }
+        }
+        const int32_t lim = c.olen - j * kTileN;  // keys past the segment end are -inf
+        if (lim < kTileN) {
+#pragma unroll
+          for (int i = 0; i < 128; ++i) x[i] = (i < lim) ? x[i] : -INFINITY;
+        }
+        float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 128; i += 8) {
+          m0 = fmax3(m0, x[i], x[i + 1]);
+          m1 = fmax3(m1, x[i + 2], x[i + 3]);
+          m2 = fmax3(m2, x[i + 4], x[i + 5]);
+          m3 = fmax3(m3, x[i + 6], x[i + 7]);
+        }
+        const float m_new = fmaxf(m_use, fmaxf(fmax3(m0, m1, m2), m3) * c2);
+        float alpha = 1.f;
+        bool rescale = false;
+        if (j == 0) {
+          m_use = m_new;
+        } else if (m_new > m_use + 8.0f) {
+          alpha = ex2(m_use - m_new);
+          m_use = m_new;
+          rescale = true;
+        }
+        // P = exp2(S c - m) in fp32, row sum of the unrounded P; the codes of
+        // P go to this half's P buffer once the previous P V has read it
+        if (j > 0 && !mbar_wait(&bar.pv_done[hf], (gj - 1) & 1, abort)) { ok = false; break; }
+        float rs = 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {  // 16-byte unit u = columns 16u .. 16u+15
+          uint32_t w[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int e = u * 16 + k * 4;
+            const float p0 = ex2(fmaf(x[e], c2, -m_use)), p1 = ex2(fmaf(x[e + 1], c2, -m_use));
+            const float p2 = ex2(fmaf(x[e + 2], c2, -m_use)), p3 = ex2(fmaf(x[e + 3], c2, -m_use));
+            rs += (p0 + p1) + (p2 + p3);
+            const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(p0, p1), __NV_SATFINITE, __NV_E4M3);
+            const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(p2, p3), __NV_SATFINITE, __NV_E4M3);
+            w[k] = lo | (hi << 16);
+          }
+          *reinterpret_cast<uint4*>(prow + ((u ^ (row & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        fence_proxy_async_smem();
+        l = fmaf(l, alpha, rs);
+        if (__any_sync(0xffffffffu, rescale)) {
+          // S_j was issued after O += P_{j-1} V_{j-1} of this half, so O is complete here
+#pragma unroll
+          for (int d0 = 0; d0 < 128; d0 += 32) {
+            uint32_t o[32];
+            tmem_ld32(tmem + lane_off + o_col + d0, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tmem + lane_off + o_col + d0, o);
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive(&bar.p_full[hf]);
+      }
+      if (!ok) break;
+      // epilogue: the last P V of this half, then O * vd / l and LSE
+      const uint32_t gl = g + nkv - 1;
+      if (!mbar_wait(&bar.pv_done[hf], gl & 1, abort)) break;
+      tc_fence_after();
+      const float f = l > 0.f ? vd / l : 0.f;
+#pragma unroll
+      for (int d0 = 0; d0 < 128; d0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_off + o_col + d0, o);
+        tmem_wait_ld();
+        if (row_valid) {
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * f, __uint_as_float(o[2 * i + 1]) * f);
+          uint4* dst = reinterpret_cast<uint4*>(orow + d0);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+      if (row_valid) *lse_out = l > 0.f ? (m_use + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+      tc_fence_before();
+      g += nkv;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0 && bar.abort) record_error(p.err, kErrTimeout);
+}
+
+cudaError_t launch_fwd_fp8(const Fp8Launch& L, cudaStream_t stream) {
+  const Fp8Params& p = L.p;
+  const int64_t nbh = (int64_t)p.batch * p.num_heads;
+  cudaError_t e = cudaMemsetAsync(p.amax, 0, 3 * nbh * sizeof(float), stream);
+  if (e != cudaSuccess) return e;
+  const int elem_grid = L.grid * 8;
+  varlen_fp8_amax_kernel<<<dim3(elem_grid, 3), 256, 0, stream>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  varlen_fp8_quant_kernel<<<dim3(elem_grid, 2), 256, 0, stream>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  varlen_fp8_vt_kernel<<<L.grid * 4, 256, 0, stream>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (p.total_q == 0) return cudaSuccess;
+  auto kern = varlen_fp8_fwd_kernel;
+  cudaFuncAttributes fa;
+  if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
+  if (fa.numRegs != (int)kF8RegsLaunch) return cudaErrorInvalidConfiguration;
+  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kF8SmemBytes)) != cudaSuccess)
+    return e;
+  kern<<<L.grid, 384, kF8SmemBytes, stream>>>(L.tm_q8, L.tm_k8, L.tm_vt, p);
+  return cudaGetLastError();
+}
+
+}  // namespace varlen

@@ -158,6 +158,48 @@ __host__ __device__ __forceinline__ int64_t pad_base(int32_t o0, int32_t b) {
   return 4 * (((int64_t)o0 + 3) / 4) + 4 * (int64_t)b;
 }
 
+// ------------------------------------------------------------------ FP8
+
+// The E4M3 forward: bf16 operands quantised per (segment, head) into a
+// workspace, then attention on the codes.  Head size 128, no mask.
+struct Fp8Params {
+  const __nv_bfloat16 *q, *k, *v;
+  int64_t q_rs, q_hs, k_rs, k_hs, v_rs, v_hs;
+  __nv_bfloat16* out;
+  int64_t o_rs, o_hs;
+  float* lse;
+  float* amax;     // [3][batch * H]: max |x| of q, k, v per (segment, head)
+  uint8_t* q8;     // [total_q][H][128] codes
+  uint8_t* k8;     // [total_k][H][128] codes
+  uint8_t* vt;     // [H][128][kp] codes, V transposed (see fp8_vt_base)
+  int64_t kp;      // row length of vt
+  CuView cu_q, cu_k;
+  int32_t batch, total_q, total_k, num_heads;
+  float scale;     // softmax scale
+  unsigned int* err;
+};
+
+struct Fp8Launch {
+  CUtensorMap tm_q8, tm_k8, tm_vt;
+  Fp8Params p;
+  int grid;
+};
+
+cudaError_t launch_fwd_fp8(const Fp8Launch& L, cudaStream_t stream);
+
+// V^T layout of the E4M3 forward: segment b's key j (0-based) sits at column
+// fp8_vt_base(k0_b, b) + j of every (head, d) row, k0_b its first key row.
+// Each segment starts on a multiple of 128 columns and owns
+// 128 * ceil(len_b / 128) of them (zero past its end): the start is at
+// least the previous segment's end for non-decreasing cu_seqlens, and below
+// fp8_vt_cols() - 128 * ceil(len_b / 128) for any.
+__host__ __device__ __forceinline__ int64_t fp8_vt_base(int32_t k0, int32_t b) {
+  return 128 * ((int64_t)b + ((int64_t)k0 + 127) / 128);
+}
+inline int64_t fp8_vt_cols(int32_t batch, int32_t total_k) {
+  return 128 * ((int64_t)batch + ((int64_t)total_k + 127) / 128 + 1);
+}
+
 cudaError_t launch_debug_schedule(const int32_t* cu, int32_t batch, int32_t total, int32_t num_heads, int32_t tile,
                                   int32_t grid, int32_t* out, int64_t max_records, cudaStream_t stream);
 

@@ -78,6 +78,13 @@ def _load() -> ctypes.CDLL:
                                            i32, i32, f32, i32, i32, vp, S, vp, S, vp, S, vp, sz, vp]
     lib.varlen_attn_bwd_deterministic.restype = ctypes.c_int
     lib.varlen_attn_bwd_deterministic.argtypes = lib.varlen_attn_bwd_window.argtypes
+    lib.varlen_attn_fwd_fp8_workspace_size.restype = sz
+    lib.varlen_attn_fwd_fp8_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+    lib.varlen_attn_fwd_fp8_workspace_layout.restype = ctypes.c_int
+    lib.varlen_attn_fwd_fp8_workspace_layout.argtypes = [i32, i32, i32, i32, i32, vp, vp]
+    lib.varlen_attn_fwd_fp8.restype = ctypes.c_int
+    lib.varlen_attn_fwd_fp8.argtypes = [vp, S, vp, S, vp, S, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, vp, S,
+                                        vp, vp, sz, vp]
     DS = VarlenDenseStride
     lib.varlen_attn_fwd_dense.restype = ctypes.c_int
     lib.varlen_attn_fwd_dense.argtypes = [vp, DS, vp, DS, vp, DS, i32, i32, i32, i32, i32, f32, i32, vp, DS, vp, vp]
@@ -117,7 +124,8 @@ EXPORTED = ("varlen_attn_fwd", "varlen_attn_bwd_workspace_size", "varlen_attn_bw
             "varlen_attn_debug_set_phase_events", "varlen_attn_bwd_noalloc", "varlen_attn_last_cuda_error",
             "varlen_attn_fwd_causal", "varlen_attn_bwd_causal", "varlen_attn_fwd_dense",
             "varlen_attn_bwd_dense_workspace_size", "varlen_attn_bwd_dense", "varlen_attn_fwd_window",
-            "varlen_attn_bwd_window", "varlen_attn_bwd_deterministic")
+            "varlen_attn_bwd_window", "varlen_attn_bwd_deterministic", "varlen_attn_fwd_fp8_workspace_size",
+            "varlen_attn_fwd_fp8_workspace_layout", "varlen_attn_fwd_fp8")
 
 # Size of the fixed device array varlen_attn_bwd_noalloc uses as scratch.
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -233,6 +241,27 @@ def varlen_attn_bwd_causal(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, 
     return varlen_attn_bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k,
                            num_heads, head_dim, max_seqlen_q, max_seqlen_k, scale, dq, dk, dv, workspace,
                            workspace_bytes, stream, causal=True)
+
+
+def varlen_attn_fwd_fp8_workspace_size(batch, total_q, total_k, num_heads, head_dim) -> int:
+    return int(LIB.varlen_attn_fwd_fp8_workspace_size(batch, total_q, total_k, num_heads, head_dim))
+
+
+def varlen_attn_fwd_fp8_workspace_layout(batch, total_q, total_k, num_heads, head_dim):
+    """(status, [amax, q codes, k codes, V^T codes] byte offsets, V^T row length)."""
+    off = (ctypes.c_size_t * 4)()
+    cols = ctypes.c_int64()
+    st = LIB.varlen_attn_fwd_fp8_workspace_layout(batch, total_q, total_k, num_heads, head_dim,
+                                                  ctypes.addressof(off), ctypes.addressof(cols))
+    return st, list(off), int(cols.value)
+
+
+def varlen_attn_fwd_fp8(q, k, v, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads, head_dim,
+                        max_seqlen_q, max_seqlen_k, scale, out, lse, workspace, workspace_bytes, stream=None) -> int:
+    return LIB.varlen_attn_fwd_fp8(_ptr(q), _stride(q), _ptr(k), _stride(k), _ptr(v), _stride(v), _ptr(cu_seqlens_q),
+                                   _ptr(cu_seqlens_k), batch, total_q, total_k, num_heads, head_dim, max_seqlen_q,
+                                   max_seqlen_k, scale, _ptr(out), _stride(out), _ptr(lse), _ptr(workspace),
+                                   workspace_bytes, _stream(stream))
 
 
 def varlen_attn_fwd_dense(q, k, v, batch, seqlen_q, seqlen_k, num_heads, head_dim, scale, causal, out, lse,

@@ -1,0 +1,106 @@
+"""GPU checks of the E4M3 (FP8) forward (varlen_attn_fwd_fp8) against the
+oracle's FP8 reading:
+
+* the quantiser is integer work decided in fp32 on both sides: amax per
+  (segment, head), the Q / K codes and the transposed V codes (with code 0
+  past each segment's end) equal the oracle's bit for bit;
+* O matches the oracle's FP8 forward within the rounding of P: the kernel
+  rounds P from a running row maximum, the oracle from the final one, each
+  within 2^-4 relative per weight, so |dO| <= 2^-3 vd sum_j p_j |v8_j| / l
+  (computed by the oracle with |V| and unrounded P) plus the bf16 rounding of
+  O; LSE within 1e-3 (P's rounding does not enter it);
+* against the fp64 oracle on the bf16 inputs, cosine >= 0.998 (the method's
+  own envelope)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from packed_variable_length_varlen_gb300 import workloads as W
+from tests import parity as P
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+SQ = [300, 129, 517, 1, 5, 0, 40, 255, 256, 2, 700]
+SK = [300, 517, 129, 5, 1, 40, 0, 256, 255, 2, 130]
+
+
+def _run(w, cpu):
+    from packed_variable_length_varlen_gb300 import varlen_attn as va
+    dev = cpu.to(DEV)
+    H = w.num_heads
+    out = W.output_like(w, "out", DEV, canary=12345.0)
+    lse = torch.full((H, w.total_q), 777.0, dtype=torch.float32, device=DEV)
+    nbytes = va.varlen_attn_fwd_fp8_workspace_size(w.batch, w.total_q, w.total_k, H, 128)
+    ws = torch.full((nbytes,), 0x7F, dtype=torch.uint8, device=DEV)  # NaN codes: every used byte is written
+    st = va.varlen_attn_fwd_fp8(dev.q, dev.k, dev.v, dev.cu_q, dev.cu_k, w.batch, w.total_q, w.total_k, H, 128,
+                                w.max_q(), w.max_k(), w.softmax_scale, out, lse, ws, nbytes)
+    assert st == 0, va.varlen_attn_status_string(st)
+    st = va.varlen_attn_get_device_status()
+    assert st == 0, va.varlen_attn_status_string(st)
+    assert P.padding_untouched(out, w, 12345.0)
+    st, off, cols = va.varlen_attn_fwd_fp8_workspace_layout(w.batch, w.total_q, w.total_k, H, 128)
+    assert st == 0
+    wsc = ws.cpu()
+    nbh = w.batch * H
+    amax = wsc[off[0]:off[0] + 3 * nbh * 4].view(torch.float32).view(3, nbh)
+    q8 = wsc[off[1]:off[1] + w.total_q * H * 128].view(w.total_q, H, 128)
+    k8 = wsc[off[2]:off[2] + w.total_k * H * 128].view(w.total_k, H, 128)
+    vt = wsc[off[3]:off[3] + H * 128 * cols].view(H, 128, cols)
+    return out, lse, amax, q8, k8, vt
+
+
+def _amax_ref(x, cu, H):
+    a = np.zeros(((len(cu) - 1) * H,), dtype=np.float32)
+    xs = x.float().numpy()
+    for b in range(len(cu) - 1):
+        if cu[b + 1] > cu[b]:
+            a[b * H:(b + 1) * H] = np.abs(xs[cu[b]:cu[b + 1]]).max(axis=(0, 2))
+    return a
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_fp8_codes_and_forward(seed):
+    w = W.custom("fp8", SQ, SK, 2, 128)
+    cpu = W.make_inputs(w, seed, with_dout=False)
+    out, lse, amax, q8, k8, vt = _run(w, cpu)
+    H = w.num_heads
+    # quantiser: bit for bit
+    for i, (x, cu) in enumerate(((cpu.q, w.cu_q), (cpu.k, w.cu_k), (cpu.v, w.cu_k))):
+        assert np.array_equal(amax[i].numpy(), _amax_ref(x, cu, H)), i
+    q8r, qd = oracle.quantize_e4m3(cpu.q, w.cu_q)
+    k8r, kd = oracle.quantize_e4m3(cpu.k, w.cu_k)
+    v8r, vd = oracle.quantize_e4m3(cpu.v, w.cu_k)
+    assert torch.equal(q8, q8r) and torch.equal(k8, k8r)
+    for b in range(w.batch):
+        k0, k1 = w.cu_k[b], w.cu_k[b + 1]
+        base = 128 * (b + -(-k0 // 128))
+        n = k1 - k0
+        if n == 0:
+            continue
+        blk = vt[:, :, base:base + n]                       # [H, 128, n]
+        assert torch.equal(blk, v8r[k0:k1].permute(1, 2, 0)), b
+        pad = -(-n // 128) * 128 - n
+        assert bool((vt[:, :, base + n:base + n + pad] == 0).all()), b
+    # forward against the oracle's FP8 reading
+    rows, heads = oracle.all_pairs(w.total_q, H)
+    pf = oracle.Fp8Problem(q8r, k8r, v8r, w.cu_q, w.cu_k, w.softmax_scale, qd, kd, vd, quantize_p=True)
+    o_ref, l_ref = pf.fwd(rows, heads)
+    pa = oracle.Fp8Problem(q8r, k8r, v8r & 0x7F, w.cu_q, w.cu_k, w.softmax_scale, qd, kd, vd, quantize_p=False)
+    o_abs, _ = pa.fwd(rows, heads)
+    o_gpu = P.gather(out.cpu(), rows, heads)
+    l_gpu = lse.cpu().numpy()[heads, rows].astype(np.float64)
+    bound = 2.0 ** -3 * o_abs + 2.0 ** -8 * np.abs(o_ref) + 1e-3
+    excess = np.abs(o_gpu - o_ref) - bound
+    print("fp8 max |dO| %.4g, max excess %.4g" % (np.abs(o_gpu - o_ref).max(), excess.max()))
+    assert (excess <= 0).all()
+    fin = np.isfinite(l_ref)
+    assert np.array_equal(np.isneginf(l_gpu), ~fin)
+    assert np.abs(l_gpu[fin] - l_ref[fin]).max() <= 1e-3
+    assert np.all(o_gpu[~fin] == 0)
+    # the method's envelope against fp64 on the bf16 inputs
+    o64, _ = P.oracle_problem(cpu).fwd(rows, heads)
+    cos = float((o_gpu * o64).sum() / np.linalg.norm(o_gpu) / np.linalg.norm(o64))
+    print("fp8 cosine vs fp64", cos)
+    assert cos >= 0.998

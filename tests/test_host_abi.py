@@ -237,3 +237,40 @@ def test_window_and_deterministic_validation_codes(va):
         assert bwd(ws_ptr=0) == va.VARLEN_ERR_WORKSPACE
         assert bwd(window=(4, 0)) in (va.VARLEN_ERR_CUDA, va.VARLEN_ERR_ARCH)
         assert bwd() in (va.VARLEN_ERR_CUDA, va.VARLEN_ERR_ARCH)
+
+
+def test_fp8_workspace_layout_and_validation(va):
+    """The E4M3 forward's workspace sections (256-byte aligned, in order, V^T
+    rows long enough for every segment's padded start) and its argument
+    checks before touching a device."""
+    B, tq, tk, H = 3, 1000, 777, 4
+    st, off, cols = va.varlen_attn_fwd_fp8_workspace_layout(B, tq, tk, H, 128)
+    assert st == va.VARLEN_OK
+    r = lambda x: (x + 255) // 256 * 256
+    assert cols == 128 * (B + -(-tk // 128) + 1)
+    assert off == [0, r(3 * B * H * 4), r(3 * B * H * 4) + r(tq * H * 128),
+                   r(3 * B * H * 4) + r(tq * H * 128) + r(tk * H * 128)]
+    assert va.varlen_attn_fwd_fp8_workspace_size(B, tq, tk, H, 128) == off[3] + r(H * 128 * cols)
+    assert va.varlen_attn_fwd_fp8_workspace_size(B, tq, tk, H, 64) == 0
+    assert va.varlen_attn_fwd_fp8_workspace_layout(B, tq, tk, H, 64)[0] == va.VARLEN_ERR_HEAD_DIM
+    # every segment's padded V^T block ends inside the rows (the layout's bound)
+    cu = [0, 5, 300, 777]
+    for b in range(B):
+        start = 128 * (b + -(-cu[b] // 128))
+        assert start + 128 * -(-(cu[b + 1] - cu[b]) // 128) <= cols
+
+    class _P:
+        def __init__(self, p):
+            self._p = p
+
+        def data_ptr(self):
+            return self._p
+
+    q = _Fake(0x1000, H * 128, 128, H=H, D=128)
+    need = va.varlen_attn_fwd_fp8_workspace_size(1, 10, 10, H, 128)
+    fwd = lambda D=128, ws=0x10000, nbytes=need: va.varlen_attn_fwd_fp8(
+        q, q, q, _P(0x2000), _P(0x2000), 1, 10, 10, H, D, 0, 0, 0.1, q, _P(0x3000), _P(ws), nbytes, 0)
+    assert fwd(D=64) == va.VARLEN_ERR_HEAD_DIM
+    assert fwd(nbytes=need - 1) == va.VARLEN_ERR_WORKSPACE
+    assert fwd(ws=0x10010) == va.VARLEN_ERR_WORKSPACE
+    assert fwd() in (va.VARLEN_ERR_CUDA, va.VARLEN_ERR_ARCH)
