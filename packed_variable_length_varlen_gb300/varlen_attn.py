@@ -367,6 +367,27 @@ def attention_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q=0, max_seqle
     return out, lse
 
 
+def attention_fwd_fp8(q, k, v, cu_seqlens_q, cu_seqlens_k, scale=None, out=None, lse=None, workspace=None,
+                      stream=None):
+    """E4M3 forward of packed bf16 q/k/v ([rows, H, 128]): quantised per
+    (segment, head) into `workspace` (allocated when None), O in bf16 and
+    LSE.  Returns (out, lse, workspace)."""
+    total_q, H, D = q.shape
+    total_k = k.shape[0]
+    batch = cu_seqlens_q.numel() - 1
+    scale = float(D ** -0.5) if scale is None else float(scale)
+    nbytes = varlen_attn_fwd_fp8_workspace_size(batch, total_q, total_k, H, D)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q, memory_format=torch.contiguous_format)
+    if lse is None:
+        lse = torch.empty(H, total_q, dtype=torch.float32, device=q.device)
+    _check(varlen_attn_fwd_fp8(q, k, v, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, H, D, 0, 0, scale, out,
+                               lse, workspace, workspace.numel(), stream), "varlen_attn_fwd_fp8")
+    return out, lse, workspace
+
+
 def attention_bwd(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q=0, max_seqlen_k=0,
                   scale=None, dq=None, dk=None, dv=None, workspace=None, stream=None, causal=False,
                   window=(-1, -1), deterministic=False):

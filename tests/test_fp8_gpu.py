@@ -104,3 +104,14 @@ def test_fp8_codes_and_forward(seed):
     cos = float((o_gpu * o64).sum() / np.linalg.norm(o_gpu) / np.linalg.norm(o64))
     print("fp8 cosine vs fp64", cos)
     assert cos >= 0.998
+
+
+def test_fp8_python_wrapper_matches_raw_call():
+    """attention_fwd_fp8 (argument marshalling only) returns the raw call's bits."""
+    from packed_variable_length_varlen_gb300 import varlen_attn as va
+    w = W.custom("fp8_wrap", [200, 3, 129], [150, 300, 1], 2, 128)
+    cpu = W.make_inputs(w, 4, with_dout=False)
+    out, lse, *_ = _run(w, cpu)
+    dev = cpu.to(DEV)
+    o2, l2, ws = va.attention_fwd_fp8(dev.q, dev.k, dev.v, dev.cu_q, dev.cu_k, w.softmax_scale)
+    assert torch.equal(o2.cpu(), out.cpu()) and torch.equal(l2.cpu(), lse.cpu())
