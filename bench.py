@@ -147,6 +147,22 @@ def _max_over_ranks(x: float, ws: int) -> float:
 
 # ------------------------------------------------------------------ CPU side
 
+def prep_roofline(total_q: int, num_heads: int, head_dim: int, prep_ms: float, hbm_gbs: float,
+                  zero_accumulator: bool = True) -> dict:
+    """HBM roofline of the backward preprocess: per (q row, head) it reads O
+    and dO (2 D bf16) and LSE, writes delta and lse2 (the algorithmic bytes,
+    4 D + 12), and, on the default path, zeroes the fp32 dQ accumulator
+    (4 D more, reported as moved bytes, not algorithmic)."""
+    pairs = float(total_q) * num_heads
+    alg = pairs * (4 * head_dim + 12)
+    moved = alg + (pairs * 4 * head_dim if zero_accumulator else 0.0)
+    sec = prep_ms * 1e-3
+    return {"kernel": "varlen_bwd_prep_kernel", "bound": "hbm", "unit": "GB/s", "peak": hbm_gbs,
+            "achieved": alg / sec / 1e9, "frac": alg / sec / 1e9 / hbm_gbs,
+            "moved_gbs": moved / sec / 1e9, "moved_frac": moved / sec / 1e9 / hbm_gbs,
+            "algorithmic_bytes": alg, "moved_bytes": moved}
+
+
 def _parse_cpulist(text: str):
     cpus = set()
     for part in text.strip().split(","):
@@ -507,6 +523,8 @@ def ours(args, w, ws, rank, local):
                           if has_bwd else None),
         "fwd_kernel_roofline": {"achieved": fwd_tflops, "peak": peak, "frac": fwd_tflops / peak,
                                 "frac_of_sustained": fwd_tflops / sust},
+        "prep_kernel_roofline": (prep_roofline(w.total_q, H, D, t_prep, float(peaks.get("hbm_gbs", 6800.0)),
+                                               zero_accumulator=not args.deterministic) if has_bwd else None),
         "clocks": clocks, "e2e": e2e, "gpu_launches": K * (1 + (3 if has_bwd else 0)),
         "roofline": roof, "cpu_baseline": cpu_base,
     }

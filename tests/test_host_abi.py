@@ -274,3 +274,14 @@ def test_fp8_workspace_layout_and_validation(va):
     assert fwd(nbytes=need - 1) == va.VARLEN_ERR_WORKSPACE
     assert fwd(ws=0x10010) == va.VARLEN_ERR_WORKSPACE
     assert fwd() in (va.VARLEN_ERR_CUDA, va.VARLEN_ERR_ARCH)
+
+
+def test_prep_roofline_arithmetic():
+    """The preprocess roofline in bench.py: 4 D + 12 algorithmic bytes per
+    (q row, head), plus 4 D of accumulator zeroing moved on the default path."""
+    import bench
+    r = bench.prep_roofline(1000, 4, 128, prep_ms=0.5, hbm_gbs=5000.0)
+    alg = 1000 * 4 * (4 * 128 + 12)
+    assert r["algorithmic_bytes"] == alg and r["moved_bytes"] == alg + 1000 * 4 * 512
+    assert abs(r["achieved"] - alg / 0.5e-3 / 1e9) < 1e-9 and abs(r["frac"] - r["achieved"] / 5000.0) < 1e-12
+    assert bench.prep_roofline(1000, 4, 128, 0.5, 5000.0, zero_accumulator=False)["moved_bytes"] == alg
