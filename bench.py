@@ -531,6 +531,51 @@ def ours(args, w, ws, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def fp8_forward(args, w, ws, rank, local):
+    """Times the E4M3 forward (quantisation passes included) alone: K calls
+    after W warm-up calls, CUDA events on the launching stream, max over
+    ranks; FLOPs at the bf16 forward count."""
+    from packed_variable_length_varlen_gb300 import varlen_attn as va
+    if w.head_dim != 128 or args.causal or _window(args) != (-1, -1):
+        raise SystemExit("--fp8 times the E4M3 forward: head size 128, no mask")
+    dev = torch.device("cuda", local)
+    d = W.make_inputs(w, seed=rank, with_dout=False).to(dev)
+    H = w.num_heads
+    out = torch.empty_like(d.q)
+    lse = torch.empty(H, w.total_q, dtype=torch.float32, device=dev)
+    nbytes = va.varlen_attn_fwd_fp8_workspace_size(w.batch, w.total_q, w.total_k, H, 128)
+    wsp = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def run():
+        st = va.varlen_attn_fwd_fp8(d.q, d.k, d.v, d.cu_q, d.cu_k, w.batch, w.total_q, w.total_k, H, 128,
+                                    w.max_q(), w.max_k(), w.softmax_scale, out, lse, wsp, nbytes, stream)
+        assert st == 0, va.varlen_attn_status_string(st)
+
+    for _ in range(args.warmup):
+        run()
+    torch.cuda.synchronize()
+    assert va.varlen_attn_get_device_status(stream) == 0
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _barrier(ws)
+    a.record(stream)
+    for _ in range(args.steps):
+        run()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = _max_over_ranks(a.elapsed_time(b), ws) / args.steps
+    if rank == 0:
+        print(json.dumps({"metric": "E4M3 varlen attention forward TFLOP/s (bf16 FLOP count, quantisation included)",
+                          "value": ws * w.fwd_flops() / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": ws,
+                          "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+                          "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate)",
+                          "data": "synthetic", "config": {"workload": w.name, "num_heads": H, "head_dim": 128,
+                                                          "step": "fp8 fwd",
+                                                          "l2": "inputs larger than L2 (k, v 2 GB each); no flush"},
+                          "gpu_launches": 4 * args.steps}),
+              flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -548,6 +593,8 @@ def main():
                     help="time the deterministic backward (dQ without atomics, a second q-major kernel)")
     ap.add_argument("--dense", action="store_true",
                     help="drive the dense batched entry points (needs equal segment lengths, e.g. --workload dense)")
+    ap.add_argument("--fp8", action="store_true",
+                    help="time the E4M3 forward alone (head size 128, no mask; quantisation included)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -562,7 +609,10 @@ def main():
         reference_arm(args, w, ws, rank)
         return
     ws, rank, local = _dist()
-    ours(args, w, ws, rank, local)
+    if args.fp8:
+        fp8_forward(args, w, ws, rank, local)
+    else:
+        ours(args, w, ws, rank, local)
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
