@@ -285,3 +285,18 @@ def test_prep_roofline_arithmetic():
     assert r["algorithmic_bytes"] == alg and r["moved_bytes"] == alg + 1000 * 4 * 512
     assert abs(r["achieved"] - alg / 0.5e-3 / 1e9) < 1e-9 and abs(r["frac"] - r["achieved"] / 5000.0) < 1e-12
     assert bench.prep_roofline(1000, 4, 128, 0.5, 5000.0, zero_accumulator=False)["moved_bytes"] == alg
+
+
+def test_bench_helpers():
+    """bench.py's CPU-side helpers: the kernel's cpulist syntax and the metric
+    name of each timed variant."""
+    import argparse
+    import bench
+    assert bench._parse_cpulist("0-3,8,10-11\n") == {0, 1, 2, 3, 8, 10, 11}
+    assert bench._parse_cpulist("5") == {5}
+    base = bench.METRIC
+    ns = lambda **kw: argparse.Namespace(**{"causal": False, "window": None, **kw})
+    assert bench._metric(ns()) == base
+    assert bench._metric(ns(causal=True)).startswith("varlen attention TFLOP/s (fwd, bwd) bf16 causal H=56")
+    assert "window(128,0)" in bench._metric(ns(window=[128, 0]))
+    assert bench._metric(ns(window=[-1, -1])) == base
