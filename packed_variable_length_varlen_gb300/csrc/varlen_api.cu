@@ -547,6 +547,7 @@ extern "C" int varlen_attn_fwd_fp8(const void* q, varlen_stride sq, const void* 
   int st = check_common(batch, total_q, total_k, num_heads, head_dim, scale);
   if (st != VARLEN_OK) return st;
   if (head_dim != 128) return VARLEN_ERR_HEAD_DIM;
+  if (fp8_vt_cols(batch, total_k) > INT32_MAX) return VARLEN_ERR_SHAPE;  // V^T columns are TMA coordinates
   if ((st = check_operand(q, sq, total_q, num_heads, head_dim)) != VARLEN_OK) return st;
   if ((st = check_operand(k, sk, total_k, num_heads, head_dim)) != VARLEN_OK) return st;
   if ((st = check_operand(v, sv, total_k, num_heads, head_dim)) != VARLEN_OK) return st;

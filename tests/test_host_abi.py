@@ -271,6 +271,9 @@ def test_fp8_workspace_layout_and_validation(va):
     fwd = lambda D=128, ws=0x10000, nbytes=need: va.varlen_attn_fwd_fp8(
         q, q, q, _P(0x2000), _P(0x2000), 1, 10, 10, H, D, 0, 0, 0.1, q, _P(0x3000), _P(ws), nbytes, 0)
     assert fwd(D=64) == va.VARLEN_ERR_HEAD_DIM
+    # V^T columns (128 (batch + ceil(total_k / 128) + 1)) must fit a 32-bit TMA coordinate
+    assert va.varlen_attn_fwd_fp8(q, q, q, _P(0x2000), _P(0x2000), 2 ** 24, 10, 2 ** 31 - 1, H, 128, 0, 0, 0.1, q,
+                                  _P(0x3000), _P(0x10000), 1 << 62, 0) == va.VARLEN_ERR_SHAPE
     assert fwd(nbytes=need - 1) == va.VARLEN_ERR_WORKSPACE
     assert fwd(ws=0x10010) == va.VARLEN_ERR_WORKSPACE
     assert fwd() in (va.VARLEN_ERR_CUDA, va.VARLEN_ERR_ARCH)
