@@ -28,7 +28,11 @@
  *     strides are arbitrary non-negative multiples of 8 elements (16 bytes)
  *     and base pointers are 16-byte aligned; no tensor is ever copied to make
  *     it contiguous.  All offset arithmetic is 64-bit, so strides times rows
- *     may exceed 2^31 elements.
+ *     may exceed 2^31 elements.  Inputs may alias themselves (a zero head
+ *     stride broadcasts one head); an output (out, dq, dk, dv) must not:
+ *     ordering its dimensions of extent > 1 by stride, the smaller stride
+ *     must be at least head_dim and the larger at least the smaller's extent
+ *     times the smaller stride, else VARLEN_ERR_STRIDE.
  *   cu_seqlens_q / cu_seqlens_k: device int32 arrays of batch+1 entries.  The
  *     host never reads them (no synchronisation); device code clamps every
  *     entry into [0, total] and never reads index > batch.  Empty segments
@@ -64,7 +68,8 @@ typedef enum {
   VARLEN_ERR_HEAD_DIM = -3,      /* head_dim not in {64, 96, 128}               */
   VARLEN_ERR_ALIGN = -4,         /* base pointer not 16-byte aligned            */
   VARLEN_ERR_STRIDE = -5,        /* stride negative, not a multiple of 8, too
-                                    large for a TMA descriptor (>= 2^40 bytes) */
+                                    large for a TMA descriptor (>= 2^40 bytes),
+                                    or an output layout that overlaps itself  */
   VARLEN_ERR_WORKSPACE = -6,     /* workspace NULL, misaligned or too small     */
   VARLEN_ERR_CUDA = -7,          /* a CUDA runtime/driver call failed           */
   VARLEN_ERR_TIMEOUT = -8,       /* a device-side bounded wait gave up          */
@@ -265,13 +270,20 @@ int varlen_attn_bwd_dense(const void* q, varlen_dense_stride sq, const void* k, 
  * Returns VARLEN_ERR_WORKSPACE, before anything is enqueued, when the
  * problem needs more than that (varlen_attn_bwd_workspace_size() >
  * VARLEN_NOALLOC_SCRATCH_BYTES; at H=16, D=96 that is about 10,700 q rows).
- * The first call on a device looks up the array's device address (with that
- * device current) and should come before any stream capture.  Every call
- * shares the one array: every entry a result depends on is rewritten by
- * each call before it is read (entries between segments are read but masked
- * out), but calls that overlap on the GPU (unordered streams) race on it.
+ * The array's device address belongs to a CUDA context: the first call in
+ * each context (the first call on a device, and the first one after the
+ * caller reset the device or made another context current on it) looks it
+ * up with that device current, so that call should come before any stream
+ * capture.  Every call shares the one array: every entry a result depends
+ * on is rewritten by each call before it is read (entries between segments
+ * are read but masked out), but calls that overlap on the GPU (unordered
+ * streams) race on it.  On a device that is not sm_103 the call returns
+ * VARLEN_ERR_ARCH, like varlen_attn_bwd.
  */
 #define VARLEN_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/* VARLEN_NOALLOC_SCRATCH_BYTES as compiled into the library. */
+size_t varlen_attn_bwd_noalloc_scratch_bytes(void);
 
 int varlen_attn_bwd_noalloc(const void* q, varlen_stride sq, const void* k, varlen_stride sk, const void* v,
                             varlen_stride sv, const void* out, varlen_stride so, const void* dout,
@@ -337,6 +349,16 @@ int varlen_attn_selftest_wait_timeout(uint64_t budget_ns, void* stream);
  * use).  count == 0 turns it off.  Process-wide setting.
  */
 int varlen_attn_debug_set_phase_events(void* const* events, int count);
+
+/*
+ * The device address of varlen_attn_bwd_noalloc's scratch array in the
+ * context current on the calling thread (*addr), and that context's
+ * identity (cuCtxGetId; *ctx_id).  The address is the one the next
+ * varlen_attn_bwd_noalloc call on this thread would use: it is looked up
+ * again whenever the current context differs from the one it was last
+ * looked up in.  Nothing is launched.  Errors as varlen_attn_bwd_noalloc.
+ */
+int varlen_attn_debug_noalloc_scratch(void** addr, unsigned long long* ctx_id);
 
 /* Number of streaming multiprocessors the persistent kernels size their grid
  * by on the current device (cached). Returns <= 0 on failure. */

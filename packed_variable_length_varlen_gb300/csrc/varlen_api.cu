@@ -24,6 +24,43 @@ namespace varlen {
 
 __device__ unsigned int g_device_error = 0;
 
+// Last CUDA error an entry point saw on this host thread (for diagnostics).
+thread_local int g_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return VARLEN_ERR_CUDA;
+}
+
+namespace {
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+}  // namespace
+
+int current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  *id = 0;
+  if (get_current == nullptr || get_id == nullptr) return cuda_fail(cudaErrorNotSupported);
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return cuda_fail(cudaErrorUnknown);
+  if (ctx == nullptr) return VARLEN_OK;
+  if (get_id(ctx, id) != CUDA_SUCCESS) return cuda_fail(cudaErrorUnknown);
+  return VARLEN_OK;
+}
+
 namespace {
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -47,33 +84,65 @@ EncodeTiledFn encode_fn() {
 struct DeviceInfo {
   int sms = 0;
   int major = 0, minor = 0;
-  unsigned int* err = nullptr;  // device address of g_device_error
+  unsigned int* err = nullptr;      // device address of g_device_error in the context below
+  unsigned long long ctx_id = 0;    // the context err was looked up in (0: none yet)
 };
 
 constexpr int kMaxDevices = 64;
 
-// Per-device attribute cache (the only host state of the library).
+// Per-device attribute cache (the only host state of the library besides
+// the optional profiling events).  The device address of g_device_error
+// belongs to a CUDA context, not to the device: it is looked up again
+// whenever the context current on the calling thread differs from the one
+// it was looked up in (after cudaDeviceReset, or under a caller's own
+// driver-API context on the same device).
 int device_info(DeviceInfo* out) {
   static DeviceInfo cache[kMaxDevices];
   static std::mutex mu;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return VARLEN_ERR_CUDA;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice);
   std::lock_guard<std::mutex> lock(mu);
-  if (cache[dev].sms == 0) {
-    DeviceInfo d;
-    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-      return VARLEN_ERR_CUDA;
-    if (d.major == 10 && d.minor == 3 &&
-        cudaGetSymbolAddress(reinterpret_cast<void**>(&d.err), g_device_error) != cudaSuccess)
-      return VARLEN_ERR_CUDA;
-    cache[dev] = d;
+  DeviceInfo& d = cache[dev];
+  if (d.sms == 0) {
+    int sms = 0, major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return cuda_fail(e);
+    d.major = major;
+    d.minor = minor;
+    d.sms = sms;
   }
-  *out = cache[dev];
-  if (out->major != 10 || out->minor != 3) return VARLEN_ERR_ARCH;
+  if (d.major != 10 || d.minor != 3) {
+    *out = d;
+    return VARLEN_ERR_ARCH;
+  }
+  unsigned long long ctx = 0;
+  int st = current_context_id(&ctx);
+  if (st != VARLEN_OK) return st;
+  if (ctx == 0 || ctx != d.ctx_id || d.err == nullptr) {
+    // (the lookup makes the device's primary context current when no
+    // context was, so the identity is read again afterwards)
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, g_device_error)) != cudaSuccess) return cuda_fail(e);
+    if ((st = current_context_id(&ctx)) != VARLEN_OK) return st;
+    d.err = static_cast<unsigned int*>(p);
+    d.ctx_id = ctx;
+  }
+  *out = d;
   return VARLEN_OK;
 }
+
+}  // namespace
+
+int device_ready() {
+  DeviceInfo d;
+  return device_info(&d);
+}
+
+namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -87,6 +156,29 @@ int check_operand(const void* ptr, varlen_stride s, int64_t rows, int32_t H, int
   if (s.row >= (int64_t(1) << 39) || s.head >= (int64_t(1) << 39)) return VARLEN_ERR_STRIDE;
   (void)H;
   (void)D;
+  return VARLEN_OK;
+}
+
+// An output operand must also not overlap itself: its rows * H vectors of
+// D elements go to distinct addresses (else two CTAs would race on one
+// element).  Sufficient condition, over the dimensions of extent > 1
+// ordered by stride: the smaller stride is at least D and the larger at
+// least the smaller's extent times the smaller stride.  (Inputs may
+// overlap: they are only read.)
+int check_output(const void* ptr, varlen_stride s, int64_t rows, int32_t H, int32_t D) {
+  int st = check_operand(ptr, s, rows, H, D);
+  if (st != VARLEN_OK) return st;
+  const bool many_rows = rows > 1, many_heads = H > 1;
+  if (many_rows && many_heads) {
+    const bool heads_inner = s.head <= s.row;
+    const int64_t small = heads_inner ? s.head : s.row, big = heads_inner ? s.row : s.head;
+    const int64_t n_small = heads_inner ? (int64_t)H : rows;
+    if (small < D || big / n_small < small) return VARLEN_ERR_STRIDE;
+  } else if (many_rows) {
+    if (s.row < D) return VARLEN_ERR_STRIDE;
+  } else if (many_heads) {
+    if (s.head < D) return VARLEN_ERR_STRIDE;
+  }
   return VARLEN_OK;
 }
 
@@ -137,14 +229,6 @@ int check_common(int32_t batch, int32_t total_q, int32_t total_k, int32_t H, int
 }
 
 constexpr float kLog2e = 1.4426950408889634f;
-
-// Last CUDA error an entry point saw on this host thread (for diagnostics).
-thread_local int g_last_cuda_error = 0;
-
-int cuda_fail(cudaError_t e) {
-  g_last_cuda_error = static_cast<int>(e);
-  return VARLEN_ERR_CUDA;
-}
 
 // Optional profiling events for the three backward kernels (process-wide).
 cudaEvent_t g_phase_events[4] = {nullptr, nullptr, nullptr, nullptr};
@@ -225,7 +309,7 @@ int fwd_impl(const void* q, varlen_stride sq, const void* k, varlen_stride sk, c
   if ((st = check_operand(q, sq, total_q, num_heads, head_dim)) != VARLEN_OK) return st;
   if ((st = check_operand(k, sk, total_k, num_heads, head_dim)) != VARLEN_OK) return st;
   if ((st = check_operand(v, sv, total_k, num_heads, head_dim)) != VARLEN_OK) return st;
-  if ((st = check_operand(out, so, total_q, num_heads, head_dim)) != VARLEN_OK) return st;
+  if ((st = check_output(out, so, total_q, num_heads, head_dim)) != VARLEN_OK) return st;
   if (total_q > 0 && lse == nullptr) return VARLEN_ERR_NULL;
   DeviceInfo dev;
   if ((st = device_info(&dev)) != VARLEN_OK) return st;
@@ -316,9 +400,9 @@ int bwd_impl(const void* q, varlen_stride sq, const void* k, varlen_stride sk, c
   if ((st = check_operand(v, sv, total_k, num_heads, head_dim)) != VARLEN_OK) return st;
   if ((st = check_operand(out, so, total_q, num_heads, head_dim)) != VARLEN_OK) return st;
   if ((st = check_operand(dout, sdo, total_q, num_heads, head_dim)) != VARLEN_OK) return st;
-  if ((st = check_operand(dq, sdq, total_q, num_heads, head_dim)) != VARLEN_OK) return st;
-  if ((st = check_operand(dk, sdk, total_k, num_heads, head_dim)) != VARLEN_OK) return st;
-  if ((st = check_operand(dv, sdv, total_k, num_heads, head_dim)) != VARLEN_OK) return st;
+  if ((st = check_output(dq, sdq, total_q, num_heads, head_dim)) != VARLEN_OK) return st;
+  if ((st = check_output(dk, sdk, total_k, num_heads, head_dim)) != VARLEN_OK) return st;
+  if ((st = check_output(dv, sdv, total_k, num_heads, head_dim)) != VARLEN_OK) return st;
   if (total_q > 0 && lse == nullptr) return VARLEN_ERR_NULL;
   const size_t need = varlen_attn_bwd_workspace_size(batch, total_q, num_heads, head_dim);
   if (need > 0 && (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
@@ -551,7 +635,7 @@ extern "C" int varlen_attn_fwd_fp8(const void* q, varlen_stride sq, const void* 
   if ((st = check_operand(q, sq, total_q, num_heads, head_dim)) != VARLEN_OK) return st;
   if ((st = check_operand(k, sk, total_k, num_heads, head_dim)) != VARLEN_OK) return st;
   if ((st = check_operand(v, sv, total_k, num_heads, head_dim)) != VARLEN_OK) return st;
-  if ((st = check_operand(out, so, total_q, num_heads, head_dim)) != VARLEN_OK) return st;
+  if ((st = check_output(out, so, total_q, num_heads, head_dim)) != VARLEN_OK) return st;
   if (total_q > 0 && lse == nullptr) return VARLEN_ERR_NULL;
   size_t off[5];
   fp8_sections(batch, total_q, total_k, num_heads, off);

@@ -54,6 +54,21 @@ __host__ __device__ __forceinline__ void band_rows(int64_t j0, int64_t j1, int32
   *hi = (int32_t)e;
 }
 
+// Records `e` as the calling thread's last CUDA error (reported by
+// varlen_attn_last_cuda_error) and returns VARLEN_ERR_CUDA.
+int cuda_fail(cudaError_t e);
+
+// Identity (cuCtxGetId) of the CUDA context current on the calling thread,
+// 0 when none is.  Device addresses of __device__ symbols belong to a
+// context; caches of them are keyed by this identity, which, unlike the
+// CUcontext handle, is never reused by a later context.
+int current_context_id(unsigned long long* id);
+
+// VARLEN_OK when the current device is an sm_103 GPU whose library state
+// (attributes, device error word) is set up for the current context;
+// VARLEN_ERR_ARCH on another device; VARLEN_ERR_CUDA when a call failed.
+int device_ready();
+
 constexpr int kTileM = 128;  // q rows per forward tile / kv rows per backward tile
 constexpr int kTileN = 128;  // kv rows per forward inner step
 constexpr int kBwdTileQ = 128; // q rows per backward inner step

@@ -11,16 +11,18 @@
 //
 // The scratch array is a file-scope __device__ array of
 // VARLEN_NOALLOC_SCRATCH_BYTES bytes; every GPU that loads the library keeps
-// it until the process exits.  Its device address is looked up once per
-// device, on the first call made with that device current
-// (cudaGetSymbolAddress); that first call should come before any stream
-// capture.  All calls share the one array and it keeps the last call's
-// contents -- the backward's preprocess kernel rewrites every part of it
-// whose value reaches a result (it zeroes the dQ accumulator and writes each
-// segment's delta / LSE entries; padding entries between segments are read
-// but masked out), so stale contents never matter -- but calls whose work
-// overlaps on the GPU (different streams with no ordering between them) race
-// on it.
+// it until the process exits.  Its device address belongs to the CUDA
+// context it was looked up in: it is looked up (cudaGetSymbolAddress, with
+// the device current) on the first call in each context -- the first call
+// on a device, and the first one after the caller reset the device or made
+// another context current -- so that first call should come before any
+// stream capture.  All calls share the one array and it keeps the last
+// call's contents -- the backward's preprocess kernel rewrites every part of
+// it whose value reaches a result (it zeroes the dQ accumulator and writes
+// each segment's delta / LSE entries; padding entries between segments are
+// read but masked out), so stale contents never matter -- but calls whose
+// work overlaps on the GPU (different streams with no ordering between
+// them) race on it.
 #include <mutex>
 
 #include "varlen_attn.h"
@@ -32,20 +34,35 @@ namespace {
 __device__ __align__(256) unsigned char g_noalloc_scratch[VARLEN_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDev = 64;
-void* g_scratch_addr[kMaxDev] = {};
+struct ScratchEntry {
+  void* addr;
+  unsigned long long ctx_id;  // context the address was looked up in
+};
+ScratchEntry g_scratch[kMaxDev] = {};
 std::mutex g_scratch_mu;
 
-// Device address of this device's copy of g_noalloc_scratch (set up once).
+// Device address of g_noalloc_scratch in the context current on this
+// thread, looked up again whenever that context is not the one of the
+// cached address.
 int scratch_address(void** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return VARLEN_ERR_CUDA;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDev) return cuda_fail(cudaErrorInvalidDevice);
+  unsigned long long ctx = 0;
+  int st = current_context_id(&ctx);
+  if (st != VARLEN_OK) return st;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  ScratchEntry& ent = g_scratch[dev];
+  if (ent.addr == nullptr || ctx == 0 || ent.ctx_id != ctx) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return VARLEN_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+    if ((e = cudaGetSymbolAddress(&p, g_noalloc_scratch)) != cudaSuccess) return cuda_fail(e);
+    if (p == nullptr) return cuda_fail(cudaErrorInvalidSymbol);
+    if ((st = current_context_id(&ctx)) != VARLEN_OK) return st;
+    ent.addr = p;
+    ent.ctx_id = ctx;
   }
-  *out = g_scratch_addr[dev];
+  *out = ent.addr;
   return VARLEN_OK;
 }
 
@@ -65,10 +82,23 @@ extern "C" int varlen_attn_bwd_noalloc(const void* q, varlen_stride sq, const vo
   if (batch < 1 || total_q < 0 || num_heads < 1 || head_dim < 1) return VARLEN_ERR_SHAPE;
   const size_t need = varlen_attn_bwd_workspace_size(batch, total_q, num_heads, head_dim);
   if (need > (size_t)VARLEN_NOALLOC_SCRATCH_BYTES) return VARLEN_ERR_WORKSPACE;
-  void* scratch = nullptr;
-  const int st = varlen::scratch_address(&scratch);
+  // The device is checked before the lookup: on a GPU that is not sm_103
+  // the call fails like varlen_attn_bwd does (VARLEN_ERR_ARCH).
+  int st = varlen::device_ready();
   if (st != VARLEN_OK) return st;
+  void* scratch = nullptr;
+  if ((st = varlen::scratch_address(&scratch)) != VARLEN_OK) return st;
   return varlen_attn_bwd(q, sq, k, sk, v, sv, out, so, dout, sdo, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q,
                          total_k, num_heads, head_dim, max_seqlen_q, max_seqlen_k, scale, dq, sdq, dk, sdk, dv, sdv,
                          scratch, (size_t)VARLEN_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+extern "C" size_t varlen_attn_bwd_noalloc_scratch_bytes(void) { return (size_t)VARLEN_NOALLOC_SCRATCH_BYTES; }
+
+extern "C" int varlen_attn_debug_noalloc_scratch(void** addr, unsigned long long* ctx_id) {
+  if (addr == nullptr || ctx_id == nullptr) return VARLEN_ERR_NULL;
+  int st = varlen::device_ready();
+  if (st != VARLEN_OK) return st;
+  if ((st = varlen::scratch_address(addr)) != VARLEN_OK) return st;
+  return varlen::current_context_id(ctx_id);
 }

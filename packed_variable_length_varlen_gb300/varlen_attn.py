@@ -96,6 +96,10 @@ def _load() -> ctypes.CDLL:
     lib.varlen_attn_bwd_noalloc.restype = ctypes.c_int
     lib.varlen_attn_bwd_noalloc.argtypes = [vp, S, vp, S, vp, S, vp, S, vp, S, vp, vp, vp, i32, i32, i32, i32, i32,
                                             i32, i32, f32, vp, S, vp, S, vp, S, vp]
+    lib.varlen_attn_bwd_noalloc_scratch_bytes.restype = sz
+    lib.varlen_attn_bwd_noalloc_scratch_bytes.argtypes = []
+    lib.varlen_attn_debug_noalloc_scratch.restype = ctypes.c_int
+    lib.varlen_attn_debug_noalloc_scratch.argtypes = [vp, vp]
     lib.varlen_attn_get_device_status.restype = ctypes.c_int
     lib.varlen_attn_get_device_status.argtypes = [vp]
     lib.varlen_attn_status_string.restype = ctypes.c_char_p
@@ -125,10 +129,12 @@ EXPORTED = ("varlen_attn_fwd", "varlen_attn_bwd_workspace_size", "varlen_attn_bw
             "varlen_attn_fwd_causal", "varlen_attn_bwd_causal", "varlen_attn_fwd_dense",
             "varlen_attn_bwd_dense_workspace_size", "varlen_attn_bwd_dense", "varlen_attn_fwd_window",
             "varlen_attn_bwd_window", "varlen_attn_bwd_deterministic", "varlen_attn_fwd_fp8_workspace_size",
-            "varlen_attn_fwd_fp8_workspace_layout", "varlen_attn_fwd_fp8")
+            "varlen_attn_fwd_fp8_workspace_layout", "varlen_attn_fwd_fp8", "varlen_attn_bwd_noalloc_scratch_bytes",
+            "varlen_attn_debug_noalloc_scratch")
 
-# Size of the fixed device array varlen_attn_bwd_noalloc uses as scratch.
-NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
+# Size of the fixed device array varlen_attn_bwd_noalloc uses as scratch, as
+# compiled into the library.
+NOALLOC_SCRATCH_BYTES = int(LIB.varlen_attn_bwd_noalloc_scratch_bytes())
 
 
 # ---------------------------------------------------------------- marshalling
@@ -293,6 +299,15 @@ def varlen_attn_bwd_noalloc(q, k, v, out, dout, lse, cu_seqlens_q, cu_seqlens_k,
                                        _ptr(cu_seqlens_k), batch, total_q, total_k, num_heads, head_dim,
                                        max_seqlen_q, max_seqlen_k, scale, _ptr(dq), _stride(dq), _ptr(dk),
                                        _stride(dk), _ptr(dv), _stride(dv), _stream(stream))
+
+
+def varlen_attn_debug_noalloc_scratch():
+    """(status, scratch device address, context id) that the next
+    varlen_attn_bwd_noalloc call on this thread would use; launches nothing."""
+    addr = ctypes.c_void_p(0)
+    ctx = ctypes.c_ulonglong(0)
+    st = LIB.varlen_attn_debug_noalloc_scratch(ctypes.byref(addr), ctypes.byref(ctx))
+    return st, int(addr.value or 0), int(ctx.value)
 
 
 def varlen_attn_get_device_status(stream=None) -> int:

@@ -303,3 +303,58 @@ def test_bench_helpers():
     assert bench._metric(ns(causal=True)).startswith("varlen attention TFLOP/s (fwd, bwd) bf16 causal H=56")
     assert "window(128,0)" in bench._metric(ns(window=[128, 0]))
     assert bench._metric(ns(window=[-1, -1])) == base
+
+
+def test_output_overlap_rejected(va):
+    """An output layout whose (row, head) vectors overlap is refused before
+    a device is touched; inputs may alias (a zero head stride broadcasts)."""
+    H, D = 2, 64
+    good = (H * D, D)
+    # out with head stride < D: heads overlap
+    assert _fwd(va, out=_Fake(0x1000, 128, 32)) == va.VARLEN_ERR_STRIDE
+    # out with row stride 0: every row at one address
+    assert _fwd(va, out=_Fake(0x1000, 0, 64)) == va.VARLEN_ERR_STRIDE
+    # rows inner (head stride = rows * row stride) is a valid layout
+    assert _fwd(va, out=_Fake(0x1000, 64, 10 * 64)) in (va.VARLEN_ERR_CUDA, va.VARLEN_ERR_ARCH)
+    # ... but not when the head stride is one row short of the rows' extent
+    assert _fwd(va, out=_Fake(0x1000, 64, 9 * 64)) == va.VARLEN_ERR_STRIDE
+    # an input broadcasting one head (head stride 0) is accepted
+    assert _fwd(va, q=_Fake(0x1000, 64, 0)) in (va.VARLEN_ERR_CUDA, va.VARLEN_ERR_ARCH)
+    # one row, one head: no overlap possible whatever the strides
+    assert _fwd(va, tq=1, H=1, out=_Fake(0x1000, 0, 0), stride=(0, 0)) in (va.VARLEN_ERR_CUDA,
+                                                                          va.VARLEN_ERR_ARCH)
+    assert _fwd(va, stride=good) in (va.VARLEN_ERR_CUDA, va.VARLEN_ERR_ARCH)
+
+
+def test_noalloc_scratch_size_matches_header(va):
+    """The scratch limit the binding reports comes from the library and
+    equals the header's VARLEN_NOALLOC_SCRATCH_BYTES."""
+    m = re.search(r"#define\s+VARLEN_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*\*\s*(\d+)u\s*\*\s*(\d+)u\)",
+                  open(HEADER).read())
+    assert m, "VARLEN_NOALLOC_SCRATCH_BYTES not found in the header"
+    want = int(m.group(1)) * int(m.group(2)) * int(m.group(3))
+    assert va.NOALLOC_SCRATCH_BYTES == want == va.LIB.varlen_attn_bwd_noalloc_scratch_bytes()
+
+
+def test_noalloc_without_gpu_reports_cuda_error(va):
+    """With no usable GPU the allocation-free backward fails like the
+    workspace entry point (device check first), and the failing CUDA call
+    is reported by varlen_attn_last_cuda_error."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present: the non-GPU path is not reachable")
+    q = _Fake(0x1000, 128, 64)
+
+    class _P:
+        def __init__(self, p):
+            self._p = p
+
+        def data_ptr(self):
+            return self._p
+
+    st = va.varlen_attn_bwd_noalloc(q, q, q, q, q, _P(0x3000), _P(0x2000), _P(0x2000), 1, 10, 10, 2, 64, 0, 0,
+                                    0.125, q, q, q, 0)
+    assert st == va.VARLEN_ERR_CUDA
+    assert va.varlen_attn_last_cuda_error() != "no error"
+    st2, addr, ctx = va.varlen_attn_debug_noalloc_scratch()
+    assert st2 == va.VARLEN_ERR_CUDA and addr == 0 and ctx == 0

@@ -54,3 +54,42 @@ def test_noalloc_refuses_problems_beyond_its_scratch():
     st = va.varlen_attn_bwd_noalloc(None, None, None, None, None, None, None, None, 1, big, big, 16, 96, 0, 0,
                                     0.1, None, None, None)
     assert st == va.VARLEN_ERR_WORKSPACE
+
+
+def test_noalloc_scratch_address_follows_the_context():
+    """The scratch array's device address belongs to a CUDA context.  With a
+    second context made current on the same device, the address the next
+    call would use is looked up in that context (its identity is the new
+    context's); back in the first context, the first context's address is
+    used again.  Nothing is launched in the second context."""
+    import ctypes
+    from packed_variable_length_varlen_gb300 import varlen_attn as va
+    torch.zeros(1, device=DEV)
+    torch.cuda.synchronize()
+    cuda = ctypes.CDLL("libcuda.so.1")
+
+    def ctx_id(ctx):
+        v = ctypes.c_ulonglong(0)
+        assert cuda.cuCtxGetId(ctx, ctypes.byref(v)) == 0
+        return v.value
+
+    st, a0, c0 = va.varlen_attn_debug_noalloc_scratch()
+    assert st == 0 and a0 != 0
+    cur = ctypes.c_void_p()
+    assert cuda.cuCtxGetCurrent(ctypes.byref(cur)) == 0 and cur.value
+    assert c0 == ctx_id(cur)
+    dev = ctypes.c_int(0)
+    assert cuda.cuCtxGetDevice(ctypes.byref(dev)) == 0
+    params = ctypes.create_string_buffer(64)  # CUctxCreateParams, all fields null
+    new = ctypes.c_void_p()
+    assert cuda.cuCtxCreate_v4(ctypes.byref(new), params, 0, dev) == 0  # made current
+    try:
+        st, a1, c1 = va.varlen_attn_debug_noalloc_scratch()
+        assert st == 0 and a1 != 0
+        assert c1 == ctx_id(new) and c1 != c0
+    finally:
+        popped = ctypes.c_void_p()
+        assert cuda.cuCtxPopCurrent_v2(ctypes.byref(popped)) == 0
+        assert cuda.cuCtxDestroy_v2(new) == 0
+    st, a2, c2 = va.varlen_attn_debug_noalloc_scratch()
+    assert st == 0 and (a2, c2) == (a0, c0)
