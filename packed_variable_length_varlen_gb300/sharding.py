@@ -15,13 +15,20 @@ of data:
 Either way the outputs land in disjoint slices, so no collective is needed;
 the only cross-rank operation of a benchmark is the max of the ranks' step
 times (``max_over_ranks``).
+
+A shard can be empty: more ranks than heads (``head_range`` gives h0 == h1)
+or than segments, or one segment holding most of the cost
+(``SegmentShard.empty``).  The library refuses num_heads = 0 and batch = 0
+(VARLEN_ERR_SHAPE), so a rank with an empty shard has no call to make: it
+skips the work and still takes part in ``max_over_ranks``.
 """
 from dataclasses import dataclass
 from typing import List, Sequence, Tuple
 
 
 def head_range(num_heads: int, world: int, rank: int) -> Tuple[int, int]:
-    """Contiguous heads [h0, h1) of `rank`; sizes differ by at most one."""
+    """Contiguous heads [h0, h1) of `rank`; sizes differ by at most one.
+    With world > num_heads some ranks get h0 == h1 (nothing to launch)."""
     if world < 1 or not 0 <= rank < world or num_heads < 0:
         raise ValueError("bad world / rank / num_heads")
     base, extra = divmod(num_heads, world)
@@ -39,6 +46,11 @@ class SegmentShard:
     k1: int
     cu_q: List[int]    # cu_seqlens of the shard, starting at 0
     cu_k: List[int]
+
+    @property
+    def empty(self) -> bool:
+        """No segment: the rank has nothing to launch (batch would be 0)."""
+        return self.b1 <= self.b0
 
 
 def segment_cost(sq: int, sk: int) -> float:

@@ -55,6 +55,28 @@ def test_segment_range_partitions():
         S.segment_range([0, 5, 3], [0, 1, 2], 2, 0)
 
 
+def test_empty_shards_are_reported():
+    """More ranks than heads or segments, or one segment dominating the
+    cost, leave some ranks without work: the ranges say so (h0 == h1,
+    SegmentShard.empty) and the non-empty shards still cover everything."""
+    ranges = [S.head_range(3, 5, r) for r in range(5)]
+    assert [h1 - h0 for h0, h1 in ranges] == [1, 1, 1, 0, 0]
+    assert ranges[-1][0] == ranges[-1][1] == 3
+    cu_q, cu_k = [0, 7, 9], [0, 7, 9]
+    shards = [S.segment_range(cu_q, cu_k, 4, r) for r in range(4)]
+    assert sum(not sh.empty for sh in shards) <= 2
+    assert [b for sh in shards if not sh.empty for b in range(sh.b0, sh.b1)] == [0, 1]
+    for sh in shards:
+        if sh.empty:
+            assert sh.q0 == sh.q1 and sh.k0 == sh.k1 and len(sh.cu_q) == 1
+    # one dominant segment: the ranks between the boundaries it spans get nothing
+    dom = S.segment_range([0, 1, 10001, 10002], [0, 1, 10001, 10002], 3, 1)
+    assert dom.b1 - dom.b0 <= 1
+    shards = [S.segment_range([0, 1, 10001, 10002], [0, 1, 10001, 10002], 3, r) for r in range(3)]
+    assert any(sh.empty for sh in shards)
+    assert sorted(b for sh in shards for b in range(sh.b0, sh.b1)) == [0, 1, 2]
+
+
 def test_max_over_ranks_without_group():
     assert S.max_over_ranks(3.5) == 3.5
 
