@@ -101,6 +101,9 @@ def _declare(lib):
         f.restype = ctypes.c_int
         f.argtypes = [P, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
                       ctypes.c_void_p, ctypes.c_void_p]
+    lib.oracle_bwd_kv_stats.restype = ctypes.c_int
+    lib.oracle_bwd_kv_stats.argtypes = [P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p,
+                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
     lib.oracle_num_threads.restype = ctypes.c_int
     lib.oracle_fwd_fp8.restype = ctypes.c_int
     lib.oracle_fwd_fp8.argtypes = [ctypes.POINTER(_Fp8Problem), ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
@@ -157,6 +160,9 @@ class Problem:
         if self.cu_q.numel() != self.cu_k.numel() or self.cu_q.numel() < 1:
             raise ValueError("cu_seqlens_q and cu_seqlens_k need batch+1 entries each")
         self._keep = (q, k, v, dout, self.cu_q, self.cu_k)
+        self._t = {"q": q, "k": k, "v": v, "dout": dout}
+        self.scale = float(scale)
+        self.masked = bool(causal) or int(window[0]) >= 0 or int(window[1]) >= 0
         s = _Problem()
         s.q, s.q_rs, s.q_hs = _view_args(q, self.H, self.D)
         s.k, s.k_rs, s.k_hs = _view_args(k, self.H, self.D)
@@ -211,6 +217,80 @@ class Problem:
             raise ValueError("backward needs dout")
         lib = lib or load_library()
         return self._call(lib.oracle_bwd_kv, rows, heads, self.D, self.D)
+
+
+    def segment_stats(self, b: int, h: int, chunk: int = 256):
+        """LSE_i and delta_i = dO_i . o_i (fp64) of every q row i of segment b,
+        head h (no mask), by the definition: s_ij = scale q_i . k_j over the
+        segment's keys, m_i = max_j s_ij, l_i = sum_j exp(s_ij - m_i),
+        LSE_i = m_i + ln l_i, o_i = sum_j P_ij v_j with P_ij = exp(s_ij - m_i)
+        / l_i (= exp(s_ij - LSE_i)).  The sums over j are fp64 matrix
+        products (a library primitive) over chunks of `chunk` q rows; each
+        row's result depends on that row alone.  Returns two fp64 arrays of
+        Sq_b entries; an empty key set gives LSE = -inf and delta = 0.  This
+        is the same quantity oracle_fwd / oracle_bwd_q compute row by row,
+        at a cost a long segment (10^5 rows) allows."""
+        if self.masked:
+            raise ValueError("segment_stats covers the unmasked problem only")
+        if not self.has_dout:
+            raise ValueError("delta needs dout")
+        cu_q, cu_k = self.cu_q.tolist(), self.cu_k.tolist()
+        q0, q1, k0, k1 = cu_q[b], cu_q[b + 1], cu_k[b], cu_k[b + 1]
+        sq, sk = max(q1 - q0, 0), max(k1 - k0, 0)
+        lse = np.empty(sq, dtype=np.float64)
+        delta = np.empty(sq, dtype=np.float64)
+        if sq == 0:
+            return lse, delta
+        if sk == 0:
+            lse[:] = -np.inf
+            delta[:] = 0.0
+            return lse, delta
+        t = self._t
+        kt = t["k"][k0:k1, h].to(torch.float64).t().contiguous()   # [D, Sk]
+        vv = t["v"][k0:k1, h].to(torch.float64).contiguous()       # [Sk, D]
+        c = min(chunk, sq)
+        s = torch.empty(c, sk, dtype=torch.float64)
+        o = torch.empty(c, self.D, dtype=torch.float64)
+        for i0 in range(0, sq, c):
+            n = min(c, sq - i0)
+            qc = t["q"][q0 + i0:q0 + i0 + n, h].to(torch.float64)
+            sc, oc = s[:n], o[:n]
+            torch.matmul(qc, kt, out=sc)
+            sc.mul_(self.scale)
+            m = sc.max(dim=1, keepdim=True).values
+            sc.sub_(m).exp_()
+            l = sc.sum(dim=1, keepdim=True)
+            lse[i0:i0 + n] = (m + torch.log(l)).reshape(-1).numpy()
+            sc.div_(l)
+            torch.matmul(sc, vv, out=oc)
+            g = t["dout"][q0 + i0:q0 + i0 + n, h].to(torch.float64)
+            delta[i0:i0 + n] = (g * oc).sum(dim=1).numpy()
+        return lse, delta
+
+    def bwd_kv_block(self, b: int, h: int, rows, stats=None, lib=None):
+        """dK rows [n, D] and dV rows [n, D] for kv rows of segment b, head h,
+        with the per-q-row LSE and delta of that segment taken from
+        ``stats`` (default: ``segment_stats(b, h)``); the sums over q rows are
+        those of bwd_kv (oracle_bwd_kv_stats)."""
+        if not self.has_dout:
+            raise ValueError("backward needs dout")
+        lib = lib or load_library()
+        lse, delta = stats if stats is not None else self.segment_stats(b, h)
+        lse = np.ascontiguousarray(lse, dtype=np.float64)
+        delta = np.ascontiguousarray(delta, dtype=np.float64)
+        sq = int(self.cu_q[b + 1]) - int(self.cu_q[b])
+        if lse.size != max(sq, 0) or delta.size != max(sq, 0):
+            raise ValueError("stats need one entry per q row of the segment")
+        rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1))
+        n = rows.size
+        dk = np.empty((n, self.D), dtype=np.float64)
+        dv = np.empty((n, self.D), dtype=np.float64)
+        if n:
+            st = lib.oracle_bwd_kv_stats(ctypes.byref(self._s), int(b), int(h), n, rows.ctypes.data,
+                                         lse.ctypes.data, delta.ctypes.data, dk.ctypes.data, dv.ctypes.data)
+            if st != 0:
+                raise ValueError("segment or head out of range")
+        return dk, dv
 
 
 def all_pairs(total_rows: int, num_heads: int):

@@ -246,6 +246,36 @@ int oracle_bwd_q(const oracle_problem *pb, int64_t n, const int64_t *rows,
     return 0;
 }
 
+/* dk_j and dv_j of kv row j (segment b, head h) by the sums over the
+ * segment's q rows i of the definition, given L[ii] = LSE_i and E[ii] =
+ * delta_i of every q row (ii = i - cu_q[b]).  Scratch: qi, kj, vj, doi of
+ * length D each. */
+static void kv_row_grad(const oracle_problem *pb, int32_t b, int32_t h, int64_t j, const double *L,
+                        const double *E, double *qi, double *kj, double *vj, double *doi,
+                        double *gk, double *gv) {
+    const int32_t D = pb->head_dim;
+    for (int32_t d = 0; d < D; ++d) gk[d] = gv[d] = 0.0;
+    load_row(pb->k, pb->dtype, pb->k_rs, pb->k_hs, j, h, D, kj);
+    load_row(pb->v, pb->dtype, pb->v_rs, pb->v_hs, j, h, D, vj);
+    const int64_t q0 = pb->cu_q[b], Sq = (int64_t)pb->cu_q[b + 1] - pb->cu_q[b];
+    const int64_t jj = j - pb->cu_k[b];  /* key index within the segment */
+    for (int64_t ii = 0; ii < Sq; ++ii) {
+        int64_t jlo, jhi;
+        visible_range(pb, b, ii, &jlo, &jhi);
+        if (jj < jlo || jj >= jhi) continue;  /* masked: P_ij = 0 */
+        load_row(pb->q, pb->dtype, pb->q_rs, pb->q_hs, q0 + ii, h, D, qi);
+        load_row(pb->dout, pb->dtype, pb->do_rs, pb->do_hs, q0 + ii, h, D, doi);
+        const double sij = pb->scale * dot(qi, kj, D);
+        const double p = exp(sij - L[ii]);
+        const double dp = dot(doi, vj, D);
+        const double ds = p * (dp - E[ii]);
+        for (int32_t d = 0; d < D; ++d) {
+            gv[d] += p * doi[d];
+            gk[d] += pb->scale * ds * qi[d];
+        }
+    }
+}
+
 /*
  * Backward, key/value side, on selected (kv row, head) pairs:
  *   dk : [n][D]   scale * sum_i dS_ij q_i
@@ -303,30 +333,44 @@ int oracle_bwd_kv(const oracle_problem *pb, int64_t n, const int64_t *rows,
                 continue;
             }
             const double *L = st_lse[(int64_t)b * H + h], *E = st_dlt[(int64_t)b * H + h];
-            load_row(pb->k, pb->dtype, pb->k_rs, pb->k_hs, j, h, D, kj);
-            load_row(pb->v, pb->dtype, pb->v_rs, pb->v_hs, j, h, D, vj);
-            const int64_t q0 = pb->cu_q[b], Sq = (int64_t)pb->cu_q[b + 1] - pb->cu_q[b];
-            const int64_t jj = j - pb->cu_k[b];  /* key index within the segment */
-            for (int64_t ii = 0; ii < Sq; ++ii) {
-                int64_t jlo, jhi;
-                visible_range(pb, b, ii, &jlo, &jhi);
-                if (jj < jlo || jj >= jhi) continue;  /* masked: P_ij = 0 */
-                load_row(pb->q, pb->dtype, pb->q_rs, pb->q_hs, q0 + ii, h, D, qi);
-                load_row(pb->dout, pb->dtype, pb->do_rs, pb->do_hs, q0 + ii, h, D, doi);
-                const double sij = pb->scale * dot(qi, kj, D);
-                const double p = exp(sij - L[ii]);
-                const double dp = dot(doi, vj, D);
-                const double ds = p * (dp - E[ii]);
-                for (int32_t d = 0; d < D; ++d) {
-                    gv[d] += p * doi[d];
-                    gk[d] += pb->scale * ds * qi[d];
-                }
-            }
+            kv_row_grad(pb, b, h, j, L, E, qi, kj, vj, doi, gk, gv);
         }
         free(qi); free(kj); free(vj); free(doi);
     }
     for (int64_t x = 0; x < (int64_t)B * H; ++x) { free(st_lse[x]); free(st_dlt[x]); }
     free(st_lse); free(st_dlt); free(seg);
+    return 0;
+}
+
+/*
+ * Backward, key/value side, for kv rows of one (segment b, head h), given the
+ * statistics of every q row of that segment: lse[ii] = LSE_i and
+ * delta[ii] = delta_i for ii = 0 .. Sq_b - 1 (the values oracle_fwd and
+ * oracle_bwd_q return for those rows).  The sums over i are those of
+ * oracle_bwd_kv; only where LSE_i and delta_i come from differs, so that a
+ * caller can compute them once per (segment, head) of a long segment.
+ *   dk, dv : [n][D].  Rows outside segment b's kv rows get NaN.
+ */
+int oracle_bwd_kv_stats(const oracle_problem *pb, int32_t b, int32_t h, int64_t n, const int64_t *rows,
+                        const double *lse, const double *delta, double *dk, double *dv) {
+    const int32_t D = pb->head_dim;
+    if (b < 0 || b >= pb->batch || h < 0 || h >= pb->num_heads) return -1;
+#pragma omp parallel
+    {
+        double *qi = malloc(sizeof(double) * D), *kj = malloc(sizeof(double) * D);
+        double *vj = malloc(sizeof(double) * D), *doi = malloc(sizeof(double) * D);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t t = 0; t < n; ++t) {
+            const int64_t j = rows[t];
+            double *gk = dk + t * D, *gv = dv + t * D;
+            if (j < pb->cu_k[b] || j >= pb->cu_k[b + 1]) {
+                for (int32_t d = 0; d < D; ++d) gk[d] = gv[d] = NAN;
+                continue;
+            }
+            kv_row_grad(pb, b, h, j, lse, delta, qi, kj, vj, doi, gk, gv);
+        }
+        free(qi); free(kj); free(vj); free(doi);
+    }
     return 0;
 }
 

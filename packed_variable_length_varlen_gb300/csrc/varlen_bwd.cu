@@ -45,6 +45,8 @@
 // The gradient formulas are the standard ones for O = softmax(scale QK^T) V:
 // dP = dO V^T, dS = P (dP - rowsum(dO o O)), dQ = scale dS K,
 // dK = scale dS^T Q, dV = P^T dO.
+#include <algorithm>
+
 #include "sm103_ptx.cuh"
 #include "varlen_internal.h"
 #include "varlen_sched.cuh"
@@ -53,35 +55,47 @@ namespace varlen {
 
 // ------------------------------------------------------------------ prep
 
-__global__ void __launch_bounds__(256) varlen_bwd_prep_kernel(const PrepParams p) {
+// One CTA per tile of R consecutive q rows (all heads).  Every global access
+// is coalesced:
+//   * the tile's slice of the fp32 dQ accumulator is one contiguous region
+//     (rows x H x D floats), zeroed with 16-byte stores;
+//   * each (row, head) pair's O and dO vectors are read by a group of G lanes
+//     (16 bytes per lane, D / 8 lanes active), adjacent groups taking
+//     adjacent heads of the same row, so a warp reads whole rows;
+//   * delta is reduced within the group by shuffles, transposed through
+//     shared memory, and written with LSE * log2(e) head by head, rows
+//     fastest, at the segment-padded positions (a row's segment is found once
+//     per row by a binary search over cu_seqlens_q).
+// All offsets are 64-bit.
+constexpr int kPrepThreads = 256;
+
+template <int D>
+__global__ void __launch_bounds__(kPrepThreads) varlen_bwd_prep_kernel(const PrepParams p) {
+  constexpr int G = D == 64 ? 8 : 16;  // lanes per (row, head) pair
+  constexpr int NCH = D / 8;           // 16-byte chunks per vector
+  constexpr int PAIRS_PER_WARP = 32 / G;
+  extern __shared__ __align__(16) uint8_t prep_smem[];
+  const int H = p.num_heads, R = p.rows_per_tile;
+  int64_t* s_pidx = reinterpret_cast<int64_t*>(prep_smem);           // [R] padded index, -1: no segment
+  float* s_delta = reinterpret_cast<float*>(prep_smem + 8 * R);      // [H][R]
   const int32_t B = p.batch;
   const int32_t lo = clamp_row(cu_at(p.cu_q, 0), p.total_q);
   const int32_t hi = clamp_row(cu_at(p.cu_q, B), p.total_q);
-  if (hi <= lo) return;
-  const int H = p.num_heads, D = p.head_dim;
-  const int64_t n = (int64_t)(hi - lo) * H;
-  const float kLog2e = 1.4426950408889634f;
-  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n; t += (int64_t)gridDim.x * blockDim.x) {
-    const int32_t row = lo + (int32_t)(t / H);
-    const int h = (int)(t % H);
-    const __nv_bfloat16* o = p.out + (int64_t)row * p.o_rs + (int64_t)h * p.o_hs;
-    const __nv_bfloat16* g = p.dout + (int64_t)row * p.do_rs + (int64_t)h * p.do_hs;
-    float acc = 0.f;
-    for (int d = 0; d < D; d += 8) {
-      const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + d));
-      const uint4 c = __ldg(reinterpret_cast<const uint4*>(g + d));
-      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-      const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(&c);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 x = __bfloat1622float2(a2[i]);
-        const float2 y = __bfloat1622float2(c2[i]);
-        acc = fmaf(x.x, y.x, acc);
-        acc = fmaf(x.y, y.y, acc);
-      }
-    }
-    // segment of `row`: the last b with clamp(cu_q[b]) <= row (binary search;
-    // exact for non-decreasing cu_seqlens)
+  const int64_t row0 = (int64_t)lo + (int64_t)blockIdx.x * R;
+  if (row0 >= hi) return;
+  const int nrows = (int)min((int64_t)R, (int64_t)hi - row0);
+  const int tid = threadIdx.x;
+
+  // 1. the accumulator rows of the tile, one contiguous region
+  if (p.dq_acc != nullptr) {
+    float4* z = reinterpret_cast<float4*>(p.dq_acc + row0 * H * D);
+    const int64_t n4 = (int64_t)nrows * H * (D / 4);
+    for (int64_t i = tid; i < n4; i += kPrepThreads) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  // 2. padded index of each row: the last b with clamp(cu_q[b]) <= row
+  //    (exact for non-decreasing cu_seqlens); -1 when no segment holds it
+  for (int r = tid; r < nrows; r += kPrepThreads) {
+    const int32_t row = (int32_t)(row0 + r);
     int32_t b0 = 0, b1 = B - 1;
     while (b0 < b1) {
       const int32_t mid = (b0 + b1 + 1) >> 1;
@@ -90,17 +104,66 @@ __global__ void __launch_bounds__(256) varlen_bwd_prep_kernel(const PrepParams p
     }
     const int32_t o0 = clamp_row(cu_at(p.cu_q, b0), p.total_q);
     const int32_t e = clamp_row(cu_at(p.cu_q, b0 + 1), p.total_q);
-    if (row >= o0 && row < e) {
-      const int64_t idx = (int64_t)h * p.pad_rows + pad_base(o0, b0) + (row - o0);
-      p.delta[idx] = acc;
-      p.lse2[idx] = __ldg(p.lse + (int64_t)h * p.total_q + row) * kLog2e;
+    s_pidx[r] = (row >= o0 && row < e) ? pad_base(o0, b0) + (row - o0) : -1;
+  }
+  // 3. delta of every (row, head) pair of the tile; all lanes of a warp run
+  //    the same iterations (the shuffles need the whole warp)
+  const int warp = tid >> 5, lane = tid & 31;
+  const int sub = lane / G, gl = lane % G;
+  const int npairs = nrows * H;
+  constexpr int kWarps = kPrepThreads / 32;
+  for (int base = warp * PAIRS_PER_WARP; base < npairs; base += 2 * kWarps * PAIRS_PER_WARP) {
+    float acc[2] = {0.f, 0.f};
+    uint4 a[2], c[2];
+    int pr[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {  // both pairs' loads are issued before the arithmetic
+      pr[u] = base + u * kWarps * PAIRS_PER_WARP + sub;
+      a[u] = c[u] = make_uint4(0, 0, 0, 0);
+      if (pr[u] < npairs && gl < NCH) {
+        const int r = pr[u] / H, h = pr[u] - r * H;
+        const int64_t row = row0 + r;
+        a[u] = __ldg(reinterpret_cast<const uint4*>(p.out + row * p.o_rs + (int64_t)h * p.o_hs + gl * 8));
+        c[u] = __ldg(reinterpret_cast<const uint4*>(p.dout + row * p.do_rs + (int64_t)h * p.do_hs + gl * 8));
+      }
     }
-    if (p.dq_acc != nullptr) {
-      float4* z = reinterpret_cast<float4*>(p.dq_acc + ((int64_t)row * H + h) * D);
-      for (int d = 0; d < D; d += 4) *z++ = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[u]);
+      const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(&c[u]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 x = __bfloat1622float2(a2[i]);
+        const float2 y = __bfloat1622float2(c2[i]);
+        acc[u] = fmaf(x.x, y.x, acc[u]);
+        acc[u] = fmaf(x.y, y.y, acc[u]);
+      }
+#pragma unroll
+      for (int o = G / 2; o >= 1; o >>= 1) acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], o);
+      if (gl == 0 && pr[u] < npairs) {
+        const int r = pr[u] / H, h = pr[u] - r * H;
+        s_delta[h * R + r] = acc[u];
+      }
+    }
+  }
+  __syncthreads();
+  // 4. delta and lse2 head by head, rows fastest
+  const float kLog2e = 1.4426950408889634f;
+  for (int i = tid; i < npairs; i += kPrepThreads) {
+    const int h = i / nrows, r = i - h * nrows;
+    const int64_t pi = s_pidx[r];
+    if (pi >= 0) {
+      const int64_t idx = (int64_t)h * p.pad_rows + pi;
+      p.delta[idx] = s_delta[h * R + r];
+      p.lse2[idx] = __ldg(p.lse + (int64_t)h * p.total_q + row0 + r) * kLog2e;
     }
   }
 }
+
+// Rows per preprocess tile: up to 32, fewer for many heads so that the
+// transposed delta tile stays within 16 KB of shared memory.
+inline int prep_rows_per_tile(int H) { return H >= 4096 ? 1 : min(32, 4096 / H); }
+inline size_t prep_smem_bytes(int H, int R) { return (size_t)8 * R + (size_t)4 * H * R; }
 
 // ------------------------------------------------------------------ post
 
@@ -772,6 +835,12 @@ template <int D, bool MASKED, bool DQ>
 static cudaError_t launch_bwd_d(const BwdLaunch& L, cudaStream_t stream) {
   using C = BwdCfg<D, DQ>;
   const int elem_grid = L.grid * 8;
+  PrepParams prep = L.prep;
+  prep.rows_per_tile = prep_rows_per_tile(prep.num_heads);
+  const size_t prep_smem = prep_smem_bytes(prep.num_heads, prep.rows_per_tile);
+  const int32_t prep_rows = L.p.total_q;  // rows [cu[0], cu[B]) lie within [0, total_q)
+  const unsigned prep_grid = (unsigned)std::max<int64_t>(1, ((int64_t)prep_rows + prep.rows_per_tile - 1) /
+                                                                prep.rows_per_tile);
   auto mark = [&](int i) {
     if (L.phase_events[i] != nullptr) cudaEventRecord(L.phase_events[i], stream);
   };
@@ -785,7 +854,7 @@ static cudaError_t launch_bwd_d(const BwdLaunch& L, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   if (fa.numRegs != (int)kBwdRegsLaunch) return cudaErrorInvalidConfiguration;
   mark(0);
-  varlen_bwd_prep_kernel<<<elem_grid, 256, 0, stream>>>(L.prep);
+  varlen_bwd_prep_kernel<D><<<prep_grid, kPrepThreads, prep_smem, stream>>>(prep);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   mark(1);

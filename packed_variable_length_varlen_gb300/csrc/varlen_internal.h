@@ -107,6 +107,7 @@ struct PrepParams {
   CuView cu_q;
   int32_t batch, total_q, num_heads, head_dim;
   int64_t pad_rows;
+  int32_t rows_per_tile;  // q rows per CTA (set at launch)
 };
 
 struct BwdParams {
