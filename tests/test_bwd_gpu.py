@@ -44,21 +44,40 @@ def _run_gpu(w: W.Workload, cpu: W.Inputs, canary=12345.0):
     return out, lse, dq, dk, dv
 
 
-def _compare(w, cpu, dq, dk, dv, qpairs=None, kpairs=None, tag=""):
+def _compare(w, cpu, dq, dk, dv, qpairs=None, kpairs=None, tag="", kblock=None):
+    """Relative Frobenius error of dQ over the q pairs and of dK, dV over the
+    kv pairs (all pairs by default).  ``kblock = (b, h, rows)`` compares the
+    kv rows `rows` of one long (segment, head) block instead, with the
+    oracle's per-segment statistics path (LSE and delta of every q row of
+    the segment computed once)."""
     pb = P.oracle_problem(cpu)
     rows, heads = qpairs if qpairs is not None else oracle.all_pairs(w.total_q, w.num_heads)
-    krows, kheads = kpairs if kpairs is not None else oracle.all_pairs(w.total_k, w.num_heads)
+    if kblock is not None:
+        krows, kheads = (np.zeros(0, np.int64), np.zeros(0, np.int32))
+    else:
+        krows, kheads = kpairs if kpairs is not None else oracle.all_pairs(w.total_k, w.num_heads)
     res = {}
     if rows.size:
         dq_ref, _ = pb.bwd_q(rows, heads)
         res["dq"] = P.rel_fro(P.gather(dq.cpu(), rows, heads), dq_ref)
+        res["dq_rows"] = int(np.unique(rows).size)
     if krows.size:
         dk_ref, dv_ref = pb.bwd_kv(krows, kheads)
         res["dk"] = P.rel_fro(P.gather(dk.cpu(), krows, kheads), dk_ref)
         res["dv"] = P.rel_fro(P.gather(dv.cpu(), krows, kheads), dv_ref)
+        res["kv_rows"] = int(np.unique(krows).size)
+    if kblock is not None:
+        b, h, brows = kblock
+        brows = np.asarray(brows, dtype=np.int64)
+        dk_ref, dv_ref = pb.bwd_kv_block(b, h, brows)
+        hh = np.full(brows.size, h, np.int32)
+        res["dk"] = P.rel_fro(P.gather(dk.cpu(), brows, hh), dk_ref)
+        res["dv"] = P.rel_fro(P.gather(dv.cpu(), brows, hh), dv_ref)
+        res["kv_block"] = (int(b), int(h), int(brows.size))
     print(w.name, tag, res)
-    for k_, v_ in res.items():
-        assert v_ <= P.GRAD_REL_FRO, (k_, res)
+    for k_ in ("dq", "dk", "dv"):
+        if k_ in res:
+            assert res[k_] <= P.GRAD_REL_FRO, (k_, res)
     return res
 
 
@@ -153,34 +172,46 @@ def test_bwd_deterministic_dk_dv():
 
 # ---------------------------------------------------------------- full size
 
-def _qpairs(w, n=1024, hpr=1, extra=()):
+def _qpairs(w, n=4096, hpr=1, extra=()):
     rows = W.sample_rows(w.cu_q, n, seed=1, extra_rows=extra)
     return W.sample_pairs(rows, w.num_heads, hpr, seed=2)
+
+
+def _kv_block_rows(w, b, n=128, seed=5):
+    """Sampled kv rows of segment b: its first and last rows, tile
+    multiples +-1 and random rows (at least n)."""
+    return W.sample_rows([w.cu_k[b], w.cu_k[b + 1]], n, seed=seed)
 
 
 @pytest.mark.slow
 def test_bwd_strided_dout_full():
     """410923 tokens, H=16, D=96, dout row stride 9728: the dout offset of
     segment 1's first row is 225304 * 9728 = 2,191,757,312 elements, past
-    2^31 (the page's failing case).  dQ sampled, including the rows where
-    the dout element offset and the dQ accumulator byte offset cross 2^31;
-    dK / dV through the invariants over every row."""
+    2^31 (the page's failing case).  dQ on 4096 sampled rows spanning both
+    segments, including the rows where the dout element offset and the dQ
+    accumulator byte offset cross 2^31; dK / dV element-wise on sampled kv
+    rows of segment 1 (every one of its q rows, whose dout the gradients sum
+    over, lies past the 2^31 element offset) and through the invariants over
+    every row."""
     w = W.strided_dout()
     cpu = W.make_inputs(w, 0)
     _, _, dq, dk, dv = _run_gpu(w, cpu)
     extra = [225304, W.offset_crossing_row(9728, 1), W.offset_crossing_row(16 * 96, 4),
              W.offset_crossing_row(16 * 96, 2)]
-    _compare(w, cpu, dq, dk, dv, _qpairs(w, 512, 1, extra), (np.zeros(0, np.int64), np.zeros(0, np.int32)))
+    _compare(w, cpu, dq, dk, dv, _qpairs(w, 4096, 1, extra), kblock=(1, 11, _kv_block_rows(w, 1)))
     _invariants(w, cpu, dk, dv)
 
 
 @pytest.mark.slow
 def test_bwd_long_full():
+    """One 77000-row segment, H=56, D=128: dQ on 4096 sampled rows
+    (including where the accumulator byte offset crosses 2^31), dK / dV
+    element-wise on sampled kv rows of one head, invariants over all rows."""
     w = W.long_dense()
     cpu = W.make_inputs(w, 0)
     _, _, dq, dk, dv = _run_gpu(w, cpu)
     extra = [W.offset_crossing_row(56 * 128, 4)]
-    _compare(w, cpu, dq, dk, dv, _qpairs(w, 512, 1, extra), (np.zeros(0, np.int64), np.zeros(0, np.int32)))
+    _compare(w, cpu, dq, dk, dv, _qpairs(w, 4096, 1, extra), kblock=(0, 37, _kv_block_rows(w, 0)))
     _invariants(w, cpu, dk, dv)
 
 
@@ -200,7 +231,7 @@ def test_bwd_ragged_full():
         kh.append(np.full(rows.size, h, np.int32))
     kp = (np.concatenate(kr), np.concatenate(kh))
     extra = [W.offset_crossing_row(w.row_stride, 2)]
-    _compare(w, cpu, dq, dk, dv, _qpairs(w, 1024, 1, extra), kp)
+    _compare(w, cpu, dq, dk, dv, _qpairs(w, 4096, 1, extra), kp)
     _invariants(w, cpu, dk, dv)
 
 
@@ -212,5 +243,5 @@ def test_bwd_windowed_full():
     b, h = 3, 17
     rows = W.sample_rows([w.cu_k[b], w.cu_k[b + 1]], 128, seed=9)
     kp = (rows, np.full(rows.size, h, np.int32))
-    _compare(w, cpu, dq, dk, dv, _qpairs(w, 1024, 1), kp)
+    _compare(w, cpu, dq, dk, dv, _qpairs(w, 4096, 1), kp)
     _invariants(w, cpu, dk, dv)

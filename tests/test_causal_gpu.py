@@ -115,9 +115,9 @@ def test_causal_windowed_full():
     w = W.windowed()
     cpu = W.make_inputs(w, 0)
     res = _run(w, cpu)
-    rows = W.sample_rows(w.cu_q, 1024, seed=1)
+    rows = W.sample_rows(w.cu_q, 4096, seed=1)
     _check_fwd(w, cpu, res, W.sample_pairs(rows, w.num_heads, 1, seed=2))
-    qp = W.sample_pairs(W.sample_rows(w.cu_q, 512, seed=3), w.num_heads, 1, seed=4)
+    qp = W.sample_pairs(W.sample_rows(w.cu_q, 4096, seed=3), w.num_heads, 1, seed=4)
     kr, kh = [], []
     for b, h in ((1, 5), (6, 40)):
         rr = W.sample_rows([w.cu_k[b], w.cu_k[b + 1]], 64, seed=b)

@@ -102,7 +102,7 @@ def test_deterministic_windowed_sampled():
     dev = cpu.to(DEV)
     out, lse = _fwd(w, dev)
     dq, dk, dv = _bwd(w, dev, out, lse, True)
-    qp = W.sample_pairs(W.sample_rows(w.cu_q, 512, seed=3), w.num_heads, 1, seed=4)
+    qp = W.sample_pairs(W.sample_rows(w.cu_q, 4096, seed=3), w.num_heads, 1, seed=4)
     dq_ref, _ = P.oracle_problem(cpu).bwd_q(*qp)
     r = P.rel_fro(P.gather(dq.cpu(), *qp), dq_ref)
     print("windowed deterministic dq", r)

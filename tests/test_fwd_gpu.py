@@ -132,7 +132,7 @@ def test_fwd_ragged_full():
 def test_fwd_long_full():
     w = W.long_dense()
     extra = [W.offset_crossing_row(w.row_stride, 2)]
-    rows = W.sample_rows(w.cu_q, 2048, seed=1, extra_rows=extra)
+    rows = W.sample_rows(w.cu_q, 4096, seed=1, extra_rows=extra)
     _fwd_case(w, pairs=W.sample_pairs(rows, w.num_heads, 1, seed=2, all_heads_rows=[0, 76999]))
 
 
@@ -140,5 +140,5 @@ def test_fwd_long_full():
 def test_fwd_strided_dout_workload_full():
     """Forward of the 410923-token, H=16, D=96 workload (inputs * 0.1)."""
     w = W.strided_dout()
-    rows = W.sample_rows(w.cu_q, 2048, seed=1, extra_rows=[225304])
+    rows = W.sample_rows(w.cu_q, 4096, seed=1, extra_rows=[225304])
     _fwd_case(w, pairs=W.sample_pairs(rows, w.num_heads, 1, seed=2, all_heads_rows=[0, 225304, 410922]))

@@ -196,3 +196,32 @@ def test_fp8_accuracy_envelope():
     print("fp8 cosine vs fp64", cos)
     assert cos[False] >= 0.998 and cos[True] >= 0.998
     assert cos[False] - cos[True] <= 1e-3
+
+
+def test_quantiser_decides_codes_in_fp32():
+    """The quantiser's precision: descale = fp32(amax) / 448 and the quotient
+    x / descale are IEEE fp32 operations, then rounded to E4M3.  The two
+    blocks below sit where that choice decides the code (found by a search
+    over bf16 values):
+      * amax = 5.817413330078125e-05, x = 8.521601557731628e-08: in fp32 the
+        quotient is 0.65625 exactly, the E4M3 midpoint between 0.625 and
+        0.6875, a tie that goes to the even neighbour 0.625; in fp64 it is
+        0.6562500000000001, which rounds up to 0.6875;
+      * amax = 5.91278076171875e-05, x = 8.66129994392395e-08: the other way
+        round (fp32 0.65625006 -> 0.6875, fp64 exactly 0.65625 -> 0.625).
+    The expected codes come from torch: an fp32 division followed by
+    torch's float8_e4m3fn conversion (a library routine)."""
+    pairs = [(5.817413330078125e-05, 8.521601557731628e-08, 0.625, 0.6875),
+             (5.91278076171875e-05, 8.66129994392395e-08, 0.6875, 0.625)]
+    t = torch.tensor([[[a]] for p in pairs for a in p[:2]], dtype=torch.bfloat16)
+    assert t.float().flatten().tolist() == [a for p in pairs for a in p[:2]]  # exact bf16 values
+    codes, desc = oracle.quantize_e4m3(t, [0, 2, 4])
+    for b, (amax, x, v32, v64) in enumerate(pairs):
+        d32 = torch.tensor(amax, dtype=torch.float32) / torch.tensor(448.0, dtype=torch.float32)
+        assert desc[b] == float(d32)
+        want = (torch.tensor(x, dtype=torch.float32) / d32).to(torch.float8_e4m3fn)
+        assert float(want.float()) == v32
+        assert int(codes[2 * b + 1, 0, 0]) == int(want.view(torch.uint8))
+        assert oracle.e4m3_decode(codes[2 * b + 1:2 * b + 2, 0, 0].numpy()).tolist() == [v32]
+        # the same block quantised in fp64 takes the other code
+        assert oracle.e4m3_round([x / (amax / 448.0)]).tolist() == [v64] and v64 != v32
