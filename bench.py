@@ -194,6 +194,63 @@ def _bind_near_gpu(dev_index: int):
         return None
 
 
+def _cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), e.g. an x86
+    'model name' or an Arm 'Neoverse-V2'."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def _copy_rates(dev_t: torch.Tensor, host_in: torch.Tensor, host_out: torch.Tensor, stream) -> dict:
+    """Pinned host <-> device copy bandwidth in GB/s, measured with CUDA
+    events: host_in -> dev_t alone, dev_t -> host_out alone, and both at once
+    on two streams (into a second device buffer), best of three each."""
+    dev = dev_t.device
+    nbytes = dev_t.numel() * dev_t.element_size()
+    other = torch.empty_like(dev_t)
+    s2 = torch.cuda.Stream(dev)
+
+    def timed(fn):
+        best = None
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b)
+            best = ms if best is None else min(best, ms)
+        return best
+
+    def both():
+        s2.wait_stream(stream)
+        with torch.cuda.stream(s2):
+            other.copy_(host_in, non_blocking=True)
+        host_out.copy_(dev_t, non_blocking=True)
+        stream.wait_stream(s2)
+
+    with torch.cuda.stream(stream):
+        h2d = timed(lambda: dev_t.copy_(host_in, non_blocking=True))
+        d2h = timed(lambda: host_out.copy_(dev_t, non_blocking=True))
+        conc = timed(both)
+    return {"bytes": int(nbytes), "h2d_gbs": nbytes / h2d / 1e6, "d2h_gbs": nbytes / d2h / 1e6,
+            "concurrent_each_gbs": nbytes / conc / 1e6}
+
+
 def _oracle_rate(w: W.Workload, target_s: float, seed: int = 0, causal: bool = False, window=(-1, -1)):
     """Times the oracle (forward + query-side backward) on sampled (row, head)
     pairs of the workload.  Credits each pair with its share of the step's
@@ -252,7 +309,8 @@ def reference_arm(args, w, ws, rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": w.name, "sample": sample},
-            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "cpu_model": _cpu_model(),
+                             "kind": "oracle", "sample": sample},
             "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
     print(json.dumps(line), flush=True)
@@ -447,6 +505,9 @@ def ours(args, w, ws, rank, local):
             stream.wait_event(in_done[(n - 1) % 2])
             end.record(stream)
 
+        # the copy rates of this machine, measured on the largest input (k)
+        rates = _copy_rates(d.k if d.k._base is None else d.k._base, host["k"],
+                            torch.empty(host["k"].shape, dtype=host["k"].dtype).pin_memory(), stream)
         a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e2e_run(2, a, b_)
         torch.cuda.synchronize()
@@ -455,9 +516,17 @@ def ours(args, w, ws, rank, local):
         e2e_run(ke, a, b_)
         torch.cuda.synchronize()
         ms_e2e = _max_over_ranks(a.elapsed_time(b_), ws)
+        # What the copies alone cost per step at the measured concurrent
+        # rate: with the copies overlapped, a step takes about the larger of
+        # this and the kernels' time.
+        copy_ms = 1e3 * max(h2d_bytes, d2h_bytes) / (rates["concurrent_each_gbs"] * 1e9)
+        kern_ms = ms_total / K
         e2e = {"value": ws * ke * step_flops / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(d2h_bytes), "ms_per_step": ms_e2e / ke,
                "pipeline": "step i+1 inputs in and step i-1 results out on two copy streams during step i",
+               "copy_rates": rates, "copy_ms_per_step_at_concurrent_rate": copy_ms,
+               "kernel_ms_per_step": kern_ms, "exposed_ms_per_step": ms_e2e / ke - kern_ms,
+               "bound": "copies" if copy_ms > kern_ms else "kernels",
                "host_cpus": bound[1] if bound else "topology not readable"}
         if bound:
             os.sched_setaffinity(0, bound[0])  # the CPU baseline below uses every core again
@@ -500,7 +569,8 @@ def ours(args, w, ws, rank, local):
     if not args.no_cpu_baseline and ws == 1:  # the CPU baseline is reported at N = 1 only
         run, n, cores = _oracle_rate(w, target_s=12.0, causal=args.causal, window=_window(args))
         t, f, n = run(n)
-        cpu_base = {"value": f / t / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+        cpu_base = {"value": f / t / 1e12, "unit": "TFLOP/s", "cores": cores, "cpu_model": _cpu_model(),
+                    "kind": "oracle",
                     "sample": "oracle fwd + dQ backward on %d random (row, head) pairs of the %s workload "
                               "(%.1f s); each pair credited with 14*Sk*D flops" % (n, w.name, t)}
 

@@ -267,6 +267,56 @@ class Problem:
             delta[i0:i0 + n] = (g * oc).sum(dim=1).numpy()
         return lse, delta
 
+    def rows_block(self, b: int, h: int, rows, chunk: int = 128):
+        """Forward and query-side backward of the q rows ``rows`` (packed
+        indices, all in segment b) of head h, no mask, by the definition:
+        s_ij = scale q_i . k_j over the segment's keys, m_i = max_j s_ij,
+        LSE_i = m_i + ln sum_j exp(s_ij - m_i), P_ij = exp(s_ij - LSE_i),
+        o_i = sum_j P_ij v_j, delta_i = dO_i . o_i, dS_ij = P_ij (dO_i . v_j -
+        delta_i), dq_i = scale sum_j dS_ij k_j.  The sums over j are fp64
+        matrix products (a library primitive) over chunks of rows; each
+        row's result depends on that row alone.  Returns o [n, D], lse [n],
+        dq [n, D] and delta [n] (dq and delta None without dout).  An empty
+        key set gives o = 0, LSE = -inf, dq = 0, delta = 0.  The same
+        quantities as fwd / bwd_q, at a cost long segments allow."""
+        if self.masked:
+            raise ValueError("rows_block covers the unmasked problem only")
+        cu_q, cu_k = self.cu_q.tolist(), self.cu_k.tolist()
+        rows = np.asarray(rows, dtype=np.int64).reshape(-1)
+        q0, q1, k0, k1 = cu_q[b], cu_q[b + 1], cu_k[b], cu_k[b + 1]
+        if rows.size and (rows.min() < q0 or rows.max() >= q1):
+            raise ValueError("rows outside segment %d" % b)
+        n, D, sk = rows.size, self.D, max(k1 - k0, 0)
+        o = np.zeros((n, D), dtype=np.float64)
+        lse = np.full(n, -np.inf, dtype=np.float64)
+        dq = np.zeros((n, D), dtype=np.float64) if self.has_dout else None
+        delta = np.zeros(n, dtype=np.float64) if self.has_dout else None
+        if n == 0 or sk == 0:
+            return o, lse, dq, delta
+        t = self._t
+        kk = t["k"][k0:k1, h].to(torch.float64).contiguous()   # [Sk, D]
+        vv = t["v"][k0:k1, h].to(torch.float64).contiguous()   # [Sk, D]
+        kt, vt = kk.t().contiguous(), vv.t().contiguous()      # [D, Sk]
+        ridx = torch.from_numpy(rows)
+        for i0 in range(0, n, chunk):
+            r = ridx[i0:i0 + chunk]
+            qc = t["q"][r, h].to(torch.float64)
+            sc = torch.matmul(qc, kt).mul_(self.scale)
+            m = sc.max(dim=1, keepdim=True).values
+            l = torch.exp(sc - m).sum(dim=1, keepdim=True)
+            lc = m + torch.log(l)
+            p = torch.exp(sc.sub_(lc))                           # P = exp(s - LSE)
+            oc = torch.matmul(p, vv)
+            o[i0:i0 + r.numel()] = oc.numpy()
+            lse[i0:i0 + r.numel()] = lc.reshape(-1).numpy()
+            if self.has_dout:
+                g = t["dout"][r, h].to(torch.float64)
+                dl = (g * oc).sum(dim=1, keepdim=True)
+                ds = torch.matmul(g, vt).sub_(dl).mul_(p)       # P (dP - delta)
+                dq[i0:i0 + r.numel()] = (torch.matmul(ds, kk) * self.scale).numpy()
+                delta[i0:i0 + r.numel()] = dl.reshape(-1).numpy()
+        return o, lse, dq, delta
+
     def bwd_kv_block(self, b: int, h: int, rows, stats=None, lib=None):
         """dK rows [n, D] and dV rows [n, D] for kv rows of segment b, head h,
         with the per-q-row LSE and delta of that segment taken from

@@ -143,3 +143,25 @@ def padding_untouched(t_dev: torch.Tensor, w: W.Workload, canary: float) -> bool
     pad = buf[:, w.num_heads * w.head_dim:]
     want = torch.tensor(canary, dtype=buf.dtype).float().item()
     return bool((pad.float() == want).all().item())
+
+
+def oracle_rows(pb: oracle.Problem, w: W.Workload, rows: np.ndarray, heads: np.ndarray):
+    """O, LSE, dQ and delta of sampled (q row, head) pairs of a long unmasked
+    workload, through the oracle's matrix-product path (Problem.rows_block),
+    grouped by (segment, head); aligned with the input pairs.  dQ and delta
+    are None without dout."""
+    rows = np.asarray(rows, dtype=np.int64)
+    heads = np.asarray(heads, dtype=np.int64)
+    seg = np.searchsorted(np.asarray(w.cu_q, dtype=np.int64), rows, side="right") - 1
+    n, D = rows.size, w.head_dim
+    o = np.empty((n, D))
+    lse = np.empty(n)
+    dq = np.empty((n, D)) if pb.has_dout else None
+    delta = np.empty(n) if pb.has_dout else None
+    for b, h in sorted(set(zip(seg.tolist(), heads.tolist()))):
+        idx = np.nonzero((seg == b) & (heads == h))[0]
+        ob, lb, qb, db = pb.rows_block(b, h, rows[idx])
+        o[idx], lse[idx] = ob, lb
+        if pb.has_dout:
+            dq[idx], delta[idx] = qb, db
+    return o, lse, dq, delta

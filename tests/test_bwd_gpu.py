@@ -44,12 +44,13 @@ def _run_gpu(w: W.Workload, cpu: W.Inputs, canary=12345.0):
     return out, lse, dq, dk, dv
 
 
-def _compare(w, cpu, dq, dk, dv, qpairs=None, kpairs=None, tag="", kblock=None):
+def _compare(w, cpu, dq, dk, dv, qpairs=None, kpairs=None, tag="", kblock=None, rows_path=False):
     """Relative Frobenius error of dQ over the q pairs and of dK, dV over the
     kv pairs (all pairs by default).  ``kblock = (b, h, rows)`` compares the
     kv rows `rows` of one long (segment, head) block instead, with the
     oracle's per-segment statistics path (LSE and delta of every q row of
-    the segment computed once)."""
+    the segment computed once).  ``rows_path`` computes the sampled dQ rows
+    with the oracle's matrix-product path (long unmasked segments)."""
     pb = P.oracle_problem(cpu)
     rows, heads = qpairs if qpairs is not None else oracle.all_pairs(w.total_q, w.num_heads)
     if kblock is not None:
@@ -58,7 +59,7 @@ def _compare(w, cpu, dq, dk, dv, qpairs=None, kpairs=None, tag="", kblock=None):
         krows, kheads = kpairs if kpairs is not None else oracle.all_pairs(w.total_k, w.num_heads)
     res = {}
     if rows.size:
-        dq_ref, _ = pb.bwd_q(rows, heads)
+        dq_ref = P.oracle_rows(pb, w, rows, heads)[2] if rows_path else pb.bwd_q(rows, heads)[0]
         res["dq"] = P.rel_fro(P.gather(dq.cpu(), rows, heads), dq_ref)
         res["dq_rows"] = int(np.unique(rows).size)
     if krows.size:
@@ -198,7 +199,7 @@ def test_bwd_strided_dout_full():
     _, _, dq, dk, dv = _run_gpu(w, cpu)
     extra = [225304, W.offset_crossing_row(9728, 1), W.offset_crossing_row(16 * 96, 4),
              W.offset_crossing_row(16 * 96, 2)]
-    _compare(w, cpu, dq, dk, dv, _qpairs(w, 4096, 1, extra), kblock=(1, 11, _kv_block_rows(w, 1)))
+    _compare(w, cpu, dq, dk, dv, _qpairs(w, 4096, 1, extra), kblock=(1, 11, _kv_block_rows(w, 1)), rows_path=True)
     _invariants(w, cpu, dk, dv)
 
 
@@ -211,7 +212,7 @@ def test_bwd_long_full():
     cpu = W.make_inputs(w, 0)
     _, _, dq, dk, dv = _run_gpu(w, cpu)
     extra = [W.offset_crossing_row(56 * 128, 4)]
-    _compare(w, cpu, dq, dk, dv, _qpairs(w, 4096, 1, extra), kblock=(0, 37, _kv_block_rows(w, 0)))
+    _compare(w, cpu, dq, dk, dv, _qpairs(w, 4096, 1, extra), kblock=(0, 37, _kv_block_rows(w, 0)), rows_path=True)
     _invariants(w, cpu, dk, dv)
 
 

@@ -16,7 +16,7 @@ DEV = "cuda"
 
 
 def _fwd_case(w: W.Workload, seed=0, pairs=None, plant=None, max_seqlen=None, allow_ulp=None, ulps=1,
-              canary=12345.0):
+              canary=12345.0, rows_path=False):
     cpu = W.make_inputs(w, seed, with_dout=False)
     if plant is not None:
         plant(cpu)
@@ -32,7 +32,10 @@ def _fwd_case(w: W.Workload, seed=0, pairs=None, plant=None, max_seqlen=None, al
     else:
         rows, heads = pairs
     pb = P.oracle_problem(cpu)
-    o_ref, lse_ref = pb.fwd(rows, heads)
+    if rows_path:  # long unmasked segments: the oracle's matrix-product path
+        o_ref, lse_ref = P.oracle_rows(pb, w, rows, heads)[:2]
+    else:
+        o_ref, lse_ref = pb.fwd(rows, heads)
     out_c = out.cpu()
     o_gpu = P.gather(out_c, rows, heads)
     lse_gpu = lse.cpu().numpy()[heads, rows].astype(np.float64)
@@ -133,7 +136,7 @@ def test_fwd_long_full():
     w = W.long_dense()
     extra = [W.offset_crossing_row(w.row_stride, 2)]
     rows = W.sample_rows(w.cu_q, 4096, seed=1, extra_rows=extra)
-    _fwd_case(w, pairs=W.sample_pairs(rows, w.num_heads, 1, seed=2, all_heads_rows=[0, 76999]))
+    _fwd_case(w, pairs=W.sample_pairs(rows, w.num_heads, 1, seed=2, all_heads_rows=[0, 76999]), rows_path=True)
 
 
 @pytest.mark.slow
@@ -141,4 +144,5 @@ def test_fwd_strided_dout_workload_full():
     """Forward of the 410923-token, H=16, D=96 workload (inputs * 0.1)."""
     w = W.strided_dout()
     rows = W.sample_rows(w.cu_q, 4096, seed=1, extra_rows=[225304])
-    _fwd_case(w, pairs=W.sample_pairs(rows, w.num_heads, 1, seed=2, all_heads_rows=[0, 225304, 410922]))
+    _fwd_case(w, pairs=W.sample_pairs(rows, w.num_heads, 1, seed=2, all_heads_rows=[0, 225304, 410922]),
+              rows_path=True)

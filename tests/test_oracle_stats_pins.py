@@ -117,3 +117,43 @@ def test_stats_refuse_masks_and_bad_blocks():
         pb.bwd_kv_block(0, 0, [0], stats=(np.zeros(4), np.zeros(4)))
     dk, dv = pb.bwd_kv_block(0, 0, [7])  # a row outside the segment
     assert np.all(np.isnan(dk)) and np.all(np.isnan(dv))
+
+
+@pytest.mark.parametrize("D,amp", [(64, 1.0), (96, 0.1), (128, 2.0)])
+def test_rows_block_equals_row_by_row_oracle(D, amp):
+    """O, LSE, dQ and delta of every q row of every (segment, head) by the
+    matrix-product path equal the row-by-row oracle's."""
+    w = W.custom("rows_d%d" % D, [0, 1, 37, 129, 5, 200], [4, 0, 1, 130, 77, 64], 2, D,
+                 amplitude=amp, dout_amplitude=amp)
+    cpu = W.make_inputs(w, 0)
+    pb = _problem(w, cpu)
+    for b in range(w.batch):
+        q0, q1 = w.cu_q[b], w.cu_q[b + 1]
+        for h in range(w.num_heads):
+            rows = np.arange(q0, q1, dtype=np.int64)[::-1].copy()  # any order
+            o, lse, dq, delta = pb.rows_block(b, h, rows, chunk=16)
+            heads = np.full(rows.size, h, np.int32)
+            o_ref, lse_ref = pb.fwd(rows, heads)
+            dq_ref, delta_ref = pb.bwd_q(rows, heads)
+            for a, ref in ((o, o_ref), (lse, lse_ref), (dq, dq_ref), (delta, delta_ref)):
+                _close(a, ref)
+
+
+def test_rows_block_closed_forms():
+    """Q = 0 gives LSE = ln Sk and o = mean_j v_j; a one-key segment gives
+    o = v exactly, LSE = scale q . k and dq = 0."""
+    w = W.custom("rows_cf", [9, 4], [21, 1], 2, 64)
+    cpu = W.make_inputs(w, 0)
+    cpu.q[:9].zero_()
+    pb = _problem(w, cpu)
+    o, lse, _, _ = pb.rows_block(0, 1, np.arange(9))
+    assert np.allclose(lse, math.log(21), rtol=0, atol=1e-14)
+    assert np.allclose(o, np.broadcast_to(cpu.v[:21, 1].double().mean(0).numpy(), o.shape), rtol=1e-12,
+                       atol=1e-14)
+    o, lse, dq, _ = pb.rows_block(1, 0, np.arange(9, 13))
+    assert np.array_equal(o, np.broadcast_to(cpu.v[21, 0].double().numpy(), o.shape))
+    want = w.softmax_scale * (cpu.q[9:13, 0].double() * cpu.k[21, 0].double()).sum(1).numpy()
+    assert np.allclose(lse, want, rtol=1e-13, atol=1e-15)
+    assert np.allclose(dq, 0.0, atol=1e-15)
+    with pytest.raises(ValueError):
+        pb.rows_block(0, 0, [9])  # row of another segment
