@@ -360,6 +360,39 @@ int varlen_attn_debug_set_phase_events(void* const* events, int count);
  */
 int varlen_attn_debug_noalloc_scratch(void** addr, unsigned long long* ctx_id);
 
+/*
+ * 1 when this library was built with device-side bounds checks
+ * (-DVARLEN_DEBUG_BOUNDS; python -m packed_variable_length_varlen_gb300.build
+ * --bounds): every plain (non-TMA) global load and store of its kernels is
+ * checked against the bytes its operand occupies, and an access outside is
+ * skipped (a load reads 0) and reported as VARLEN_ERR_DEVICE_BOUNDS by
+ * varlen_attn_get_device_status.  0 for the normal build, whose kernels
+ * carry no checks.
+ */
+int varlen_attn_bounds_checked(void);
+
+/*
+ * Bounds checker self test: every operand extent handed to the kernels of
+ * later calls is `bytes` shorter (0 restores; negative: VARLEN_ERR_SHAPE).
+ * In a bounds-checking build the last accesses of each operand then fail
+ * their check, are skipped, and the call reports VARLEN_ERR_DEVICE_BOUNDS;
+ * in the normal build it has no effect.  Process-wide; for tests only.
+ */
+int varlen_attn_debug_set_span_slack(int64_t bytes);
+
+/*
+ * Failure test of the bounded waits: with which = 0 the K/V producer of the
+ * forward's CTA 0 leaves out its load number n (0-based, K and V loads
+ * counted alike); with which = 1 the Q producer of the backward's CTA 0
+ * leaves out the Q load of its step n.  The waits for that load give up
+ * after their budget (2 s), every role of the CTA unwinds (the producer
+ * waits, bounded, for its copies in flight; the MMA issuer drains its
+ * products; TMEM is freed) and varlen_attn_get_device_status returns
+ * VARLEN_ERR_TIMEOUT; the context stays usable.  n < 0 turns it off; an
+ * unknown `which` returns VARLEN_ERR_SHAPE.  Process-wide; for tests only.
+ */
+int varlen_attn_debug_skip_load(int which, int64_t n);
+
 /* Number of streaming multiprocessors the persistent kernels size their grid
  * by on the current device (cached). Returns <= 0 on failure. */
 int varlen_attn_num_sms(void);

@@ -15,6 +15,8 @@
 #include <cstring>
 #include <climits>
 #include <cstdint>
+#include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "varlen_attn.h"
@@ -234,6 +236,27 @@ constexpr float kLog2e = 1.4426950408889634f;
 cudaEvent_t g_phase_events[4] = {nullptr, nullptr, nullptr, nullptr};
 std::mutex g_phase_mu;
 
+// Debug knobs (process-wide): bytes taken off every operand span (the
+// bounds checker's self test) and the load the forward / backward producer
+// of CTA 0 leaves out (the failure test).
+std::atomic<int64_t> g_span_slack{0};
+std::atomic<int64_t> g_skip_fwd_load{-1}, g_skip_bwd_step{-1};
+
+// Bytes an NHD operand of `rows` rows occupies from its base: up to the end
+// of its last (row, head) vector.
+Span nhd_span(const void* base, varlen_stride s, int64_t rows, int32_t H, int32_t D) {
+  if (base == nullptr || rows <= 0 || H <= 0) return Span{base, 0};
+  const int64_t last = (rows - 1) * s.row + (int64_t)(H - 1) * s.head + D;
+  return Span{base, std::max<int64_t>(0, 2 * last - g_span_slack.load())};
+}
+Span flat_span(const void* base, int64_t bytes) {
+  return Span{base, std::max<int64_t>(0, bytes - g_span_slack.load())};
+}
+int32_t skip_knob(const std::atomic<int64_t>& k) {
+  const int64_t v = k.load();
+  return v < 0 || v > INT32_MAX ? -1 : (int32_t)v;
+}
+
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // E4M3 codes [rows][H][128] as a 3-D uint8 tensor map {128, H, rows} with
@@ -334,6 +357,9 @@ int fwd_impl(const void* q, varlen_stride sq, const void* k, varlen_stride sk, c
   L.p.win_right = band.right;
   L.p.scale_log2 = scale * kLog2e;
   L.p.err = dev.err;
+  L.p.out_span = nhd_span(out, so, total_q, num_heads, head_dim);
+  L.p.lse_span = flat_span(lse, (int64_t)num_heads * total_q * 4);
+  L.p.debug_skip_load = skip_knob(g_skip_fwd_load);
   L.head_dim = head_dim;
   L.grid = dev.sms;
   cudaError_t e = launch_fwd(L, static_cast<cudaStream_t>(stream));
@@ -455,6 +481,22 @@ int bwd_impl(const void* q, varlen_stride sq, const void* k, varlen_stride sk, c
   L.p.err = dev.err;
   L.post = PostParams{dq_acc, static_cast<__nv_bfloat16*>(dq), sdq.row, sdq.head, cu_q, batch,
                       total_q, num_heads, head_dim, scale};
+  const int64_t acc_bytes = (int64_t)total_q * num_heads * head_dim * 4;
+  const int64_t row_bytes = pad_rows * num_heads * 4;
+  L.prep.out_span = nhd_span(out, so, total_q, num_heads, head_dim);
+  L.prep.dout_span = nhd_span(dout, sdo, total_q, num_heads, head_dim);
+  L.prep.lse_span = flat_span(lse, (int64_t)num_heads * total_q * 4);
+  L.prep.delta_span = flat_span(delta, row_bytes);
+  L.prep.lse2_span = flat_span(lse2, row_bytes);
+  L.prep.acc_span = flat_span(dq_acc, acc_bytes);
+  L.prep.err = dev.err;
+  L.p.dk_span = nhd_span(dk, sdk, total_k, num_heads, head_dim);
+  L.p.dv_span = nhd_span(dv, sdv, total_k, num_heads, head_dim);
+  L.p.dq_span = nhd_span(dq, sdq, total_q, num_heads, head_dim);
+  L.p.debug_skip_step = skip_knob(g_skip_bwd_step);
+  L.post.acc_span = flat_span(dq_acc, acc_bytes);
+  L.post.dq_span = nhd_span(dq, sdq, total_q, num_heads, head_dim);
+  L.post.err = dev.err;
   L.head_dim = head_dim;
   L.grid = dev.sms;
   L.deterministic = deterministic;
@@ -673,6 +715,15 @@ extern "C" int varlen_attn_fwd_fp8(const void* q, varlen_stride sq, const void* 
   L.p.num_heads = num_heads;
   L.p.scale = scale;
   L.p.err = dev.err;
+  L.p.q_span = nhd_span(q, sq, total_q, num_heads, head_dim);
+  L.p.k_span = nhd_span(k, sk, total_k, num_heads, head_dim);
+  L.p.v_span = nhd_span(v, sv, total_k, num_heads, head_dim);
+  L.p.out_span = nhd_span(out, so, total_q, num_heads, head_dim);
+  L.p.lse_span = flat_span(lse, (int64_t)num_heads * total_q * 4);
+  L.p.amax_span = flat_span(L.p.amax, (int64_t)3 * batch * num_heads * 4);
+  L.p.q8_span = flat_span(L.p.q8, (int64_t)total_q * num_heads * 128);
+  L.p.k8_span = flat_span(L.p.k8, (int64_t)total_k * num_heads * 128);
+  L.p.vt_span = flat_span(L.p.vt, (int64_t)num_heads * 128 * L.p.kp);
   L.grid = dev.sms;
   if ((st = encode_codes_nhd(&L.tm_q8, L.p.q8, total_q, num_heads)) != VARLEN_OK) return st;
   if ((st = encode_codes_nhd(&L.tm_k8, L.p.k8, total_k, num_heads)) != VARLEN_OK) return st;
@@ -761,4 +812,25 @@ extern "C" int varlen_attn_num_sms(void) {
   int st = device_info(&dev);
   if (st != VARLEN_OK && st != VARLEN_ERR_ARCH) return st;
   return dev.sms;
+}
+
+extern "C" int varlen_attn_bounds_checked(void) {
+#ifdef VARLEN_DEBUG_BOUNDS
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+extern "C" int varlen_attn_debug_set_span_slack(int64_t bytes) {
+  if (bytes < 0) return VARLEN_ERR_SHAPE;
+  g_span_slack.store(bytes);
+  return VARLEN_OK;
+}
+
+extern "C" int varlen_attn_debug_skip_load(int which, int64_t n) {
+  if (which == 0) g_skip_fwd_load.store(n < 0 ? -1 : n);
+  else if (which == 1) g_skip_bwd_step.store(n < 0 ? -1 : n);
+  else return VARLEN_ERR_SHAPE;
+  return VARLEN_OK;
 }

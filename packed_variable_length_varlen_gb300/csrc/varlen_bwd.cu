@@ -55,8 +55,9 @@ namespace varlen {
 
 // ------------------------------------------------------------------ prep
 
-// One CTA per tile of R consecutive q rows (all heads).  Every global access
-// is coalesced:
+// Persistent CTAs walk tiles of R consecutive q rows (all heads), tile t, t +
+// gridDim.x, ...; small tiles keep the CTAs' shares even.  Every global
+// access is coalesced:
 //   * the tile's slice of the fp32 dQ accumulator is one contiguous region
 //     (rows x H x D floats), zeroed with 16-byte stores;
 //   * each (row, head) pair's O and dO vectors are read by a group of G lanes
@@ -68,9 +69,10 @@ namespace varlen {
 //     per row by a binary search over cu_seqlens_q).
 // All offsets are 64-bit.
 constexpr int kPrepThreads = 256;
+constexpr int kPrepBlocksPerSm = 8;  // persistent CTAs per SM (32 registers per thread)
 
 template <int D>
-__global__ void __launch_bounds__(kPrepThreads) varlen_bwd_prep_kernel(const PrepParams p) {
+__global__ void __launch_bounds__(kPrepThreads, kPrepBlocksPerSm) varlen_bwd_prep_kernel(const PrepParams p) {
   constexpr int G = D == 64 ? 8 : 16;  // lanes per (row, head) pair
   constexpr int NCH = D / 8;           // 16-byte chunks per vector
   constexpr int PAIRS_PER_WARP = 32 / G;
@@ -81,16 +83,16 @@ __global__ void __launch_bounds__(kPrepThreads) varlen_bwd_prep_kernel(const Pre
   const int32_t B = p.batch;
   const int32_t lo = clamp_row(cu_at(p.cu_q, 0), p.total_q);
   const int32_t hi = clamp_row(cu_at(p.cu_q, B), p.total_q);
-  const int64_t row0 = (int64_t)lo + (int64_t)blockIdx.x * R;
-  if (row0 >= hi) return;
-  const int nrows = (int)min((int64_t)R, (int64_t)hi - row0);
   const int tid = threadIdx.x;
+  for (int64_t row0 = (int64_t)lo + (int64_t)blockIdx.x * R; row0 < hi; row0 += (int64_t)gridDim.x * R) {
+  const int nrows = (int)min((int64_t)R, (int64_t)hi - row0);
 
   // 1. the accumulator rows of the tile, one contiguous region
   if (p.dq_acc != nullptr) {
     float4* z = reinterpret_cast<float4*>(p.dq_acc + row0 * H * D);
     const int64_t n4 = (int64_t)nrows * H * (D / 4);
-    for (int64_t i = tid; i < n4; i += kPrepThreads) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t i = tid; i < n4; i += kPrepThreads)
+      if (in_span(p.acc_span, z + i, 16, p.err)) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   // 2. padded index of each row: the last b with clamp(cu_q[b]) <= row
   //    (exact for non-decreasing cu_seqlens); -1 when no segment holds it
@@ -123,8 +125,10 @@ __global__ void __launch_bounds__(kPrepThreads) varlen_bwd_prep_kernel(const Pre
       if (pr[u] < npairs && gl < NCH) {
         const int r = pr[u] / H, h = pr[u] - r * H;
         const int64_t row = row0 + r;
-        a[u] = __ldg(reinterpret_cast<const uint4*>(p.out + row * p.o_rs + (int64_t)h * p.o_hs + gl * 8));
-        c[u] = __ldg(reinterpret_cast<const uint4*>(p.dout + row * p.do_rs + (int64_t)h * p.do_hs + gl * 8));
+        const uint4* pa = reinterpret_cast<const uint4*>(p.out + row * p.o_rs + (int64_t)h * p.o_hs + gl * 8);
+        const uint4* pc = reinterpret_cast<const uint4*>(p.dout + row * p.do_rs + (int64_t)h * p.do_hs + gl * 8);
+        if (in_span(p.out_span, pa, 16, p.err)) a[u] = __ldg(pa);
+        if (in_span(p.dout_span, pc, 16, p.err)) c[u] = __ldg(pc);
       }
     }
 #pragma unroll
@@ -154,15 +158,20 @@ __global__ void __launch_bounds__(kPrepThreads) varlen_bwd_prep_kernel(const Pre
     const int64_t pi = s_pidx[r];
     if (pi >= 0) {
       const int64_t idx = (int64_t)h * p.pad_rows + pi;
-      p.delta[idx] = s_delta[h * R + r];
-      p.lse2[idx] = __ldg(p.lse + (int64_t)h * p.total_q + row0 + r) * kLog2e;
+      const float* pl = p.lse + (int64_t)h * p.total_q + row0 + r;
+      const float lv = in_span(p.lse_span, pl, 4, p.err) ? __ldg(pl) : 0.f;
+      if (in_span(p.delta_span, p.delta + idx, 4, p.err)) p.delta[idx] = s_delta[h * R + r];
+      if (in_span(p.lse2_span, p.lse2 + idx, 4, p.err)) p.lse2[idx] = lv * kLog2e;
     }
+  }
+  __syncthreads();  // the next tile rewrites s_pidx and s_delta
   }
 }
 
-// Rows per preprocess tile: up to 32, fewer for many heads so that the
-// transposed delta tile stays within 16 KB of shared memory.
-inline int prep_rows_per_tile(int H) { return H >= 4096 ? 1 : min(32, 4096 / H); }
+// Rows per preprocess tile: 8 (32-byte runs of delta per head), fewer for
+// many heads so that the transposed delta tile stays within 16 KB of shared
+// memory.
+inline int prep_rows_per_tile(int H) { return H >= 4096 ? 1 : min(8, 4096 / H); }
 inline size_t prep_smem_bytes(int H, int R) { return (size_t)8 * R + (size_t)4 * H * R; }
 
 // ------------------------------------------------------------------ post
@@ -180,13 +189,16 @@ __global__ void __launch_bounds__(256) varlen_bwd_post_kernel(const PostParams p
     const int64_t row = lo + rh / H;
     const int h = (int)(rh % H);
     const float4* s = reinterpret_cast<const float4*>(p.dq_acc + (row * H + h) * D + v * 8);
-    const float4 a = s[0], b = s[1];
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 a = in_span(p.acc_span, s, 16, p.err) ? s[0] : z4;
+    const float4 b = in_span(p.acc_span, s + 1, 16, p.err) ? s[1] : z4;
     uint4 w;
     w.x = pack_bf16x2(a.x * p.scale, a.y * p.scale);
     w.y = pack_bf16x2(a.z * p.scale, a.w * p.scale);
     w.z = pack_bf16x2(b.x * p.scale, b.y * p.scale);
     w.w = pack_bf16x2(b.z * p.scale, b.w * p.scale);
-    *reinterpret_cast<uint4*>(p.dq + row * p.dq_rs + (int64_t)h * p.dq_hs + v * 8) = w;
+    uint4* dst = reinterpret_cast<uint4*>(p.dq + row * p.dq_rs + (int64_t)h * p.dq_hs + v * 8);
+    if (in_span(p.dq_span, dst, 16, p.err)) *dst = w;
   }
 }
 
@@ -364,6 +376,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int32_t j = j0; j < nq; ++j, ++gs) {
           const uint32_t st = gs % C::NQ;
           if (!mbar_wait(&bar.q_empty[st], ((gs / C::NQ) & 1) ^ 1, abort)) { ok = false; break; }
+          // (failure test: CTA 0 leaves one step's Q load out; the waits for
+          // it give up and the kernel unwinds, reporting a timeout)
+          if (blockIdx.x == 0 && (int64_t)gs == (int64_t)p.debug_skip_step) continue;
           mbar_arrive_expect_tx(&bar.q_full[st], C::T_BYTES + C::ROWV_BYTES);
 #pragma unroll
           for (int cc = 0; cc < C::NC; ++cc)
@@ -600,8 +615,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           __nv_bfloat16* dvrow = p.dv + krow * p.dv_rs + (int64_t)tl.h * p.dv_hs;
           __nv_bfloat16* dkrow = p.dk + krow * p.dk_rs + (int64_t)tl.h * p.dk_hs;
           for (int d = half * (D / 2); d < (half + 1) * (D / 2); d += 8) {
-            *reinterpret_cast<uint4*>(dvrow + d) = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(dkrow + d) = make_uint4(0, 0, 0, 0);
+            if (in_span(p.dv_span, dvrow + d, 16, p.err)) *reinterpret_cast<uint4*>(dvrow + d) = make_uint4(0, 0, 0, 0);
+            if (in_span(p.dk_span, dkrow + d, 16, p.err)) *reinterpret_cast<uint4*>(dkrow + d) = make_uint4(0, 0, 0, 0);
           }
         }
         continue;
@@ -731,10 +746,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           uint4* dv4 = reinterpret_cast<uint4*>(p.dv + krow * p.dv_rs + (int64_t)tl.h * p.dv_hs + d0);
           uint4* dk4 = reinterpret_cast<uint4*>(p.dk + krow * p.dk_rs + (int64_t)tl.h * p.dk_hs + d0);
-          dv4[0] = make_uint4(wa[0], wa[1], wa[2], wa[3]);
-          dv4[1] = make_uint4(wa[4], wa[5], wa[6], wa[7]);
-          dk4[0] = make_uint4(wb[0], wb[1], wb[2], wb[3]);
-          dk4[1] = make_uint4(wb[4], wb[5], wb[6], wb[7]);
+          if (in_span(p.dv_span, dv4, 16, p.err)) dv4[0] = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+          if (in_span(p.dv_span, dv4 + 1, 16, p.err)) dv4[1] = make_uint4(wa[4], wa[5], wa[6], wa[7]);
+          if (in_span(p.dk_span, dk4, 16, p.err)) dk4[0] = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+          if (in_span(p.dk_span, dk4 + 1, 16, p.err)) dk4[1] = make_uint4(wb[4], wb[5], wb[6], wb[7]);
         }
       }
       tc_fence_before();
@@ -839,8 +854,9 @@ static cudaError_t launch_bwd_d(const BwdLaunch& L, cudaStream_t stream) {
   prep.rows_per_tile = prep_rows_per_tile(prep.num_heads);
   const size_t prep_smem = prep_smem_bytes(prep.num_heads, prep.rows_per_tile);
   const int32_t prep_rows = L.p.total_q;  // rows [cu[0], cu[B]) lie within [0, total_q)
-  const unsigned prep_grid = (unsigned)std::max<int64_t>(1, ((int64_t)prep_rows + prep.rows_per_tile - 1) /
-                                                                prep.rows_per_tile);
+  const unsigned prep_grid = (unsigned)std::max<int64_t>(
+      1, std::min<int64_t>(((int64_t)prep_rows + prep.rows_per_tile - 1) / prep.rows_per_tile,
+                           (int64_t)L.grid * kPrepBlocksPerSm));
   auto mark = [&](int i) {
     if (L.phase_events[i] != nullptr) cudaEventRecord(L.phase_events[i], stream);
   };

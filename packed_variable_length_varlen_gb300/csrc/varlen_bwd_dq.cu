@@ -364,7 +364,7 @@ __global__ void __launch_bounds__(384, 1)
       if (nkv == 0) {
         if (row_valid)
           for (int d = half * DH; d < (half + 1) * DH; d += 8)
-            *reinterpret_cast<uint4*>(dqrow + d) = make_uint4(0, 0, 0, 0);
+            if (in_span(p.dq_span, dqrow + d, 16, p.err)) *reinterpret_cast<uint4*>(dqrow + d) = make_uint4(0, 0, 0, 0);
         continue;
       }
       if (!mbar_wait(&bar.q_full, tiles & 1, abort)) break;
@@ -451,8 +451,8 @@ __global__ void __launch_bounds__(384, 1)
           for (int k = 0; k < 8; ++k)
             w[k] = pack_bf16x2(__uint_as_float(a[2 * k]) * p.scale, __uint_as_float(a[2 * k + 1]) * p.scale);
           uint4* dst = reinterpret_cast<uint4*>(dqrow + d0);
-          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          if (in_span(p.dq_span, dst, 16, p.err)) dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          if (in_span(p.dq_span, dst + 1, 16, p.err)) dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
         }
       }
       tc_fence_before();

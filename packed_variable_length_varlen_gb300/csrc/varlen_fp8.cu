@@ -54,9 +54,10 @@ __device__ __forceinline__ bool segment_of_row(const CuView& cu, int32_t batch, 
   return row >= clamp_row(cu_at(cu, b0), total) && row < clamp_row(cu_at(cu, b0 + 1), total);
 }
 
-// Eight bf16 (one 16-byte load) as floats.
-__device__ __forceinline__ void load8(const __nv_bfloat16* src, float (&f)[8]) {
-  const uint4 u = __ldg(reinterpret_cast<const uint4*>(src));
+// Eight bf16 (one 16-byte load) as floats (zeros when a bounds-checking
+// build finds the load outside `span`).
+__device__ __forceinline__ void load8(const __nv_bfloat16* src, float (&f)[8], const Span& span, unsigned int* err) {
+  const uint4 u = in_span(span, src, 16, err) ? __ldg(reinterpret_cast<const uint4*>(src)) : make_uint4(0, 0, 0, 0);
   const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -84,6 +85,7 @@ __global__ void __launch_bounds__(256) varlen_fp8_amax_kernel(const Fp8Params p)
   const int64_t hs = which == 0 ? p.q_hs : (which == 1 ? p.k_hs : p.v_hs);
   const CuView cu = which == 0 ? p.cu_q : p.cu_k;
   const int32_t total = which == 0 ? p.total_q : p.total_k;
+  const Span xs = which == 0 ? p.q_span : (which == 1 ? p.k_span : p.v_span);
   const int32_t B = p.batch, H = p.num_heads;
   unsigned int* amax = reinterpret_cast<unsigned int*>(p.amax) + (int64_t)which * B * H;
   const int32_t lo = clamp_row(cu_at(cu, 0), total), hi = clamp_row(cu_at(cu, B), total);
@@ -99,11 +101,12 @@ __global__ void __launch_bounds__(256) varlen_fp8_amax_kernel(const Fp8Params p)
 #pragma unroll 4
     for (int d = 0; d < 128; d += 8) {
       float f[8];
-      load8(src + d, f);
+      load8(src + d, f, xs, p.err);
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx = fmaxf(mx, fabsf(f[i]));
     }
-    atomicMax(amax + (int64_t)b * H + h, __float_as_uint(mx));
+    unsigned int* slot = amax + (int64_t)b * H + h;
+    if (in_span(p.amax_span, slot, 4, p.err)) atomicMax(slot, __float_as_uint(mx));
   }
 }
 
@@ -117,6 +120,8 @@ __global__ void __launch_bounds__(256) varlen_fp8_quant_kernel(const Fp8Params p
   const CuView cu = which == 0 ? p.cu_q : p.cu_k;
   const int32_t total = which == 0 ? p.total_q : p.total_k;
   uint8_t* dst8 = which == 0 ? p.q8 : p.k8;
+  const Span xs = which == 0 ? p.q_span : p.k_span;
+  const Span ds = which == 0 ? p.q8_span : p.k8_span;
   const int32_t B = p.batch, H = p.num_heads;
   const float* amax = p.amax + (int64_t)which * B * H;
   const int32_t lo = clamp_row(cu_at(cu, 0), total), hi = clamp_row(cu_at(cu, B), total);
@@ -127,16 +132,18 @@ __global__ void __launch_bounds__(256) varlen_fp8_quant_kernel(const Fp8Params p
     const int h = (int)(t % H);
     int32_t b;
     if (!segment_of_row(cu, B, total, row, b)) continue;
-    const float dsc = descale_of(amax[(int64_t)b * H + h]);
+    const float* am = amax + (int64_t)b * H + h;
+    const float dsc = descale_of(in_span(p.amax_span, am, 4, p.err) ? *am : 0.f);
     const __nv_bfloat16* src = x + (int64_t)row * rs + (int64_t)h * hs;
     uint4* out = reinterpret_cast<uint4*>(dst8 + ((int64_t)row * H + h) * 128);
 #pragma unroll 2
     for (int d = 0; d < 128; d += 16) {
       float f[8], g[8];
-      load8(src + d, f);
-      load8(src + d + 8, g);
-      out[d / 16] = make_uint4(e4m3x4(f[0], f[1], f[2], f[3], dsc), e4m3x4(f[4], f[5], f[6], f[7], dsc),
-                               e4m3x4(g[0], g[1], g[2], g[3], dsc), e4m3x4(g[4], g[5], g[6], g[7], dsc));
+      load8(src + d, f, xs, p.err);
+      load8(src + d + 8, g, xs, p.err);
+      if (in_span(ds, out + d / 16, 16, p.err))
+        out[d / 16] = make_uint4(e4m3x4(f[0], f[1], f[2], f[3], dsc), e4m3x4(f[4], f[5], f[6], f[7], dsc),
+                                 e4m3x4(g[0], g[1], g[2], g[3], dsc), e4m3x4(g[4], g[5], g[6], g[7], dsc));
     }
   }
 }
@@ -157,14 +164,15 @@ __global__ void __launch_bounds__(256) varlen_fp8_vt_kernel(const Fp8Params p) {
        t += gridDim.x) {
     const Tile tl = cursor_tile(c, t);
     const int32_t valid = min(128, c.len - tl.m * 128);
-    const float dsc = descale_of(amax[(int64_t)c.b * H + tl.h]);
+    const float* am = amax + (int64_t)c.b * H + tl.h;
+    const float dsc = descale_of(in_span(p.amax_span, am, 4, p.err) ? *am : 0.f);
     uint8_t code[64];
     if (r < valid) {
       const __nv_bfloat16* src = p.v + ((int64_t)c.r0 + tl.m * 128 + r) * p.v_rs + (int64_t)tl.h * p.v_hs + half * 64;
 #pragma unroll
       for (int d = 0; d < 64; d += 8) {
         float f[8];
-        load8(src + d, f);
+        load8(src + d, f, p.v_span, p.err);
         const uint32_t a = e4m3x4(f[0], f[1], f[2], f[3], dsc), e = e4m3x4(f[4], f[5], f[6], f[7], dsc);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -184,7 +192,8 @@ __global__ void __launch_bounds__(256) varlen_fp8_vt_kernel(const Fp8Params p) {
     uint8_t* dst = p.vt + ((int64_t)tl.h * 128 + dd) * p.kp + fp8_vt_base(c.r0, c.b) + (int64_t)tl.m * 128 + part * 64;
     const uint4* srow = reinterpret_cast<const uint4*>(tile + dd * 128 + part * 64);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) reinterpret_cast<uint4*>(dst)[i] = srow[i];
+    for (int i = 0; i < 4; ++i)
+      if (in_span(p.vt_span, reinterpret_cast<uint4*>(dst) + i, 16, p.err)) reinterpret_cast<uint4*>(dst)[i] = srow[i];
     __syncthreads();
   }
 }
@@ -398,15 +407,20 @@ __global__ void __launch_bounds__(384, 1)
       if (nkv == 0) {
         if (row_valid) {
 #pragma unroll
-          for (int d = 0; d < 128; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0, 0, 0, 0);
-          *lse_out = -INFINITY;
+          for (int d = 0; d < 128; d += 8)
+            if (in_span(p.out_span, orow + d, 16, p.err)) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0, 0, 0, 0);
+          if (in_span(p.lse_span, lse_out, 4, p.err)) *lse_out = -INFINITY;
         }
         continue;
       }
       const int64_t bh = (int64_t)c.b * H + tl.h;
       const int64_t nbh = (int64_t)p.batch * H;
-      const float qd = descale_of(__ldg(p.amax + bh)), kd = descale_of(__ldg(p.amax + nbh + bh));
-      const float vd = descale_of(__ldg(p.amax + 2 * nbh + bh));
+      const float* aq = p.amax + bh;
+      const float* ak = p.amax + nbh + bh;
+      const float* av = p.amax + 2 * nbh + bh;
+      const float qd = descale_of(in_span(p.amax_span, aq, 4, p.err) ? __ldg(aq) : 0.f);
+      const float kd = descale_of(in_span(p.amax_span, ak, 4, p.err) ? __ldg(ak) : 0.f);
+      const float vd = descale_of(in_span(p.amax_span, av, 4, p.err) ? __ldg(av) : 0.f);
       const float c2 = p.scale * 1.4426950408889634f * qd * kd;
       float m_use = -INFINITY, l = 0.f;
       for (int32_t j = 0; j < nkv; ++j) {
@@ -502,10 +516,12 @@ __global__ void __launch_bounds__(384, 1)
             w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * f, __uint_as_float(o[2 * i + 1]) * f);
           uint4* dst = reinterpret_cast<uint4*>(orow + d0);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          for (int i = 0; i < 4; ++i)
+            if (in_span(p.out_span, dst + i, 16, p.err)) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
         }
       }
-      if (row_valid) *lse_out = l > 0.f ? (m_use + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+      if (row_valid && in_span(p.lse_span, lse_out, 4, p.err))
+        *lse_out = l > 0.f ? (m_use + __log2f(l)) * 0.69314718055994531f : -INFINITY;
       tc_fence_before();
       g += nkv;
     }

@@ -173,11 +173,16 @@ __global__ void __launch_bounds__(384, 1)
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&bar.kv_full[slot], C::TILE);
-            uint8_t* dst = ring + slot * C::TILE;
-            const CUtensorMap* m = which ? &tm_v : &tm_k;
+            // (failure test: CTA 0 leaves one load out; its consumer's bounded
+            // wait then gives up and the kernel unwinds, reporting a timeout)
+            if (!(blockIdx.x == 0 && (int64_t)ring_pos == (int64_t)p.debug_skip_load)) {
+              mbar_arrive_expect_tx(&bar.kv_full[slot], C::TILE);
+              uint8_t* dst = ring + slot * C::TILE;
+              const CUtensorMap* m = which ? &tm_v : &tm_k;
 #pragma unroll
-            for (int cc = 0; cc < C::NC; ++cc) tma_load_3d(dst + cc * C::CHUNK, m, &bar.kv_full[slot], cc * 64, tl.h, krow);
+              for (int cc = 0; cc < C::NC; ++cc)
+                tma_load_3d(dst + cc * C::CHUNK, m, &bar.kv_full[slot], cc * 64, tl.h, krow);
+            }
             ++ring_pos;
           }
         }
@@ -317,8 +322,9 @@ __global__ void __launch_bounds__(384, 1)
         float* lse_out = p.lse + (int64_t)tl.h * p.total_q + grow;
         if (r_in_seg < c.len) {
 #pragma unroll
-          for (int d = 0; d < D; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0, 0, 0, 0);
-          *lse_out = -INFINITY;
+          for (int d = 0; d < D; d += 8)
+            if (in_span(p.out_span, orow + d, 16, p.err)) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0, 0, 0, 0);
+          if (in_span(p.lse_span, lse_out, 4, p.err)) *lse_out = -INFINITY;
         }
         continue;
       }
@@ -443,10 +449,12 @@ __global__ void __launch_bounds__(384, 1)
             w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
           uint4* dst = reinterpret_cast<uint4*>(orow + d0);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          for (int i = 0; i < 4; ++i)
+            if (in_span(p.out_span, dst + i, 16, p.err)) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
         }
       }
-      if (row_valid) *lse_out = l > 0.f ? (m_use + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+      if (row_valid && in_span(p.lse_span, lse_out, 4, p.err))
+        *lse_out = l > 0.f ? (m_use + __log2f(l)) * 0.69314718055994531f : -INFINITY;
       tc_fence_before();
       g += nkv;
     }

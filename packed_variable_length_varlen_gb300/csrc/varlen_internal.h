@@ -16,6 +16,33 @@ enum : unsigned int {
   kErrBounds = 2u,   // a debug bounds check failed
 };
 
+// The bytes [base, base + bytes) one operand of a launch occupies.  In a
+// build with -DVARLEN_DEBUG_BOUNDS every plain (non-TMA) global load and
+// store of the kernels checks the bytes it touches against its operand's
+// span (in_span); an access outside is skipped (a load reads 0) and
+// kErrBounds is recorded in the device error word.  In the normal build the
+// check compiles away.
+struct Span {
+  const void* base;
+  int64_t bytes;
+};
+
+__device__ __forceinline__ bool in_span(const Span& s, const void* p, int n, unsigned int* err) {
+#ifdef VARLEN_DEBUG_BOUNDS
+  const int64_t off = static_cast<const char*>(p) - static_cast<const char*>(s.base);
+  if (off < 0 || off + n > s.bytes) {
+    if (err != nullptr) atomicOr(err, (unsigned int)kErrBounds);
+    return false;
+  }
+#else
+  (void)s;
+  (void)p;
+  (void)n;
+  (void)err;
+#endif
+  return true;
+}
+
 // Where a launch finds its segment bounds: cu_seqlens in device memory
 // (`ptr`), or, when ptr is null, uniform segments of `uni` rows each (the
 // bounds b * uni of the dense batched entry points, never stored).
@@ -77,6 +104,7 @@ struct FwdParams {
   __nv_bfloat16* out;
   int64_t o_rs, o_hs;
   float* lse;
+  Span out_span, lse_span;     // checked in a bounds-checking build
   CuView cu_q;
   CuView cu_k;
   int32_t batch, total_q, total_k, num_heads;
@@ -84,6 +112,7 @@ struct FwdParams {
   int64_t win_left, win_right; // the band when masked (kWinUnbounded: that side open)
   float scale_log2;  // softmax scale * log2(e)
   unsigned int* err; // device error word
+  int32_t debug_skip_load;  // < 0: off; else CTA 0's producer skips its K/V load number n (failure test)
 };
 
 struct FwdLaunch {
@@ -108,6 +137,8 @@ struct PrepParams {
   int32_t batch, total_q, num_heads, head_dim;
   int64_t pad_rows;
   int32_t rows_per_tile;  // q rows per CTA (set at launch)
+  Span out_span, dout_span, lse_span, delta_span, lse2_span, acc_span;  // checked in a bounds-checking build
+  unsigned int* err;      // device error word
 };
 
 struct BwdParams {
@@ -129,6 +160,8 @@ struct BwdParams {
   float scale_log2;  // softmax scale * log2(e)
   float scale;       // softmax scale (applied to dK)
   unsigned int* err; // device error word
+  Span dk_span, dv_span, dq_span;  // checked in a bounds-checking build
+  int32_t debug_skip_step;  // < 0: off; else CTA 0's Q producer skips the load of this step (failure test)
 };
 
 struct PostParams {
@@ -138,6 +171,8 @@ struct PostParams {
   CuView cu_q;
   int32_t batch, total_q, num_heads, head_dim;
   float scale;
+  Span acc_span, dq_span;  // checked in a bounds-checking build
+  unsigned int* err;       // device error word
 };
 
 struct BwdLaunch {
@@ -193,6 +228,7 @@ struct Fp8Params {
   int32_t batch, total_q, total_k, num_heads;
   float scale;     // softmax scale
   unsigned int* err;
+  Span q_span, k_span, v_span, out_span, lse_span, amax_span, q8_span, k8_span, vt_span;  // bounds-checking build
 };
 
 struct Fp8Launch {

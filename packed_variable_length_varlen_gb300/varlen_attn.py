@@ -100,6 +100,12 @@ def _load() -> ctypes.CDLL:
     lib.varlen_attn_bwd_noalloc_scratch_bytes.argtypes = []
     lib.varlen_attn_debug_noalloc_scratch.restype = ctypes.c_int
     lib.varlen_attn_debug_noalloc_scratch.argtypes = [vp, vp]
+    lib.varlen_attn_bounds_checked.restype = ctypes.c_int
+    lib.varlen_attn_bounds_checked.argtypes = []
+    lib.varlen_attn_debug_set_span_slack.restype = ctypes.c_int
+    lib.varlen_attn_debug_set_span_slack.argtypes = [i64]
+    lib.varlen_attn_debug_skip_load.restype = ctypes.c_int
+    lib.varlen_attn_debug_skip_load.argtypes = [ctypes.c_int, i64]
     lib.varlen_attn_get_device_status.restype = ctypes.c_int
     lib.varlen_attn_get_device_status.argtypes = [vp]
     lib.varlen_attn_status_string.restype = ctypes.c_char_p
@@ -130,7 +136,8 @@ EXPORTED = ("varlen_attn_fwd", "varlen_attn_bwd_workspace_size", "varlen_attn_bw
             "varlen_attn_bwd_dense_workspace_size", "varlen_attn_bwd_dense", "varlen_attn_fwd_window",
             "varlen_attn_bwd_window", "varlen_attn_bwd_deterministic", "varlen_attn_fwd_fp8_workspace_size",
             "varlen_attn_fwd_fp8_workspace_layout", "varlen_attn_fwd_fp8", "varlen_attn_bwd_noalloc_scratch_bytes",
-            "varlen_attn_debug_noalloc_scratch")
+            "varlen_attn_debug_noalloc_scratch", "varlen_attn_bounds_checked", "varlen_attn_debug_set_span_slack",
+            "varlen_attn_debug_skip_load")
 
 # Size of the fixed device array varlen_attn_bwd_noalloc uses as scratch, as
 # compiled into the library.
@@ -308,6 +315,19 @@ def varlen_attn_debug_noalloc_scratch():
     ctx = ctypes.c_ulonglong(0)
     st = LIB.varlen_attn_debug_noalloc_scratch(ctypes.byref(addr), ctypes.byref(ctx))
     return st, int(addr.value or 0), int(ctx.value)
+
+
+def varlen_attn_bounds_checked() -> bool:
+    """True for a library built with device-side bounds checks."""
+    return bool(LIB.varlen_attn_bounds_checked())
+
+
+def varlen_attn_debug_set_span_slack(nbytes: int) -> int:
+    return LIB.varlen_attn_debug_set_span_slack(int(nbytes))
+
+
+def varlen_attn_debug_skip_load(which: int, n: int) -> int:
+    return LIB.varlen_attn_debug_skip_load(int(which), int(n))
 
 
 def varlen_attn_get_device_status(stream=None) -> int:

@@ -295,9 +295,11 @@ def sample_rows(cu, n_target: int = 4096, seed: int = 1, extra_rows=()) -> np.nd
     """Rows spanning every segment: per segment the first two and last two
     rows and rows at tile multiples +-1 (subsampled), the ``extra_rows``
     (e.g. where an offset first crosses 2^31), then uniform random rows from
-    ``seed`` up to ``n_target``.  Sorted and unique."""
+    ``seed`` up to ``n_target``, all within [cu[0], cu[-1]) (a slice of
+    cu_seqlens, e.g. one segment's bounds, samples that slice only).  Sorted
+    and unique."""
     cu = [int(c) for c in cu]
-    total = cu[-1]
+    first, total = cu[0], cu[-1]
     rng = np.random.default_rng(seed)
     picked = set()
     for b in range(len(cu) - 1):
@@ -315,13 +317,13 @@ def sample_rows(cu, n_target: int = 4096, seed: int = 1, extra_rows=()) -> np.nd
                 if a <= r < e:
                     picked.add(int(r))
     for r in extra_rows:
-        if 0 <= r < total:
+        if first <= r < total:
             picked.add(int(r))
             if r + 1 < total:
                 picked.add(int(r) + 1)
-    if total > 0:
-        while len(picked) < min(n_target, total):
-            picked.update(int(x) for x in rng.integers(0, total, size=n_target - len(picked)))
+    if total > first:
+        while len(picked) < min(n_target, total - first):
+            picked.update(int(x) for x in rng.integers(first, total, size=n_target - len(picked)))
     return np.array(sorted(picked), dtype=np.int64)
 
 
