@@ -321,7 +321,21 @@ def reference_arm(args, w, ws, rank):
 def ours(args, w, ws, rank, local):
     from packed_variable_length_varlen_gb300 import varlen_attn as va
     dev = torch.device("cuda", local)
-    cpu = W.make_inputs(w, seed=rank)  # each rank's own batch of the same shape
+    full_flops = None
+    if args.shard == "heads":
+        # one problem split by heads: every rank draws the same inputs and
+        # runs its head range as views t[:, h0:h1] (no copies, no collective)
+        h0, h1 = sharding.head_range(w.num_heads, ws, rank)
+        if h1 == h0:
+            raise SystemExit("--shard heads needs at most num_heads ranks")
+        full_flops = (w.fwd_flops(args.causal, _window(args)), w.bwd_flops(args.causal, _window(args)))
+        cpu = W.make_inputs(w, seed=0)
+        for n in ("q", "k", "v", "dout"):
+            setattr(cpu, n, getattr(cpu, n)[:, h0:h1])
+        w = w.with_(num_heads=h1 - h0)
+        args.no_e2e = True
+    else:
+        cpu = W.make_inputs(w, seed=rank)  # each rank's own batch of the same shape
     d = cpu.to(dev)
     H, D = w.num_heads, w.head_dim
     out = torch.empty_like(d.q)
@@ -422,6 +436,8 @@ def ours(args, w, ws, rank, local):
     f_bwd = w.bwd_flops(args.causal, _window(args)) if has_bwd else 0.0
     step_flops = f_fwd + f_bwd
     value = ws * K * step_flops / (ms_total * 1e-3) / 1e12
+    if full_flops is not None:  # a head split: all ranks together did the one problem's flops
+        value = K * (full_flops[0] + (full_flops[1] if has_bwd else 0.0)) / (ms_total * 1e-3) / 1e12
     fwd_tflops = f_fwd / (statistics.mean(t_fwd) * 1e-3) / 1e12
     bwd_tflops = f_bwd / (statistics.mean(t_bwd) * 1e-3) / 1e12 if has_bwd else None
 
@@ -577,14 +593,16 @@ def ours(args, w, ws, rank, local):
     burst = float(peaks.get("bf16_tflops"))
     line = {
         "metric": _metric(args), "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": K, "warmup": Wm,
-        "ms_per_step": ms_total / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "ms_per_step": ms_total / K, "higher_is_better": True,
+        "scaling": "strong" if full_flops is not None else "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "batch_segments": w.batch, "total_q": w.total_q, "total_k": w.total_k,
                    "num_heads": H, "head_dim": D, "step": "fwd+bwd" if has_bwd else "fwd only (bwd missing)",
                    "causal": bool(args.causal), "window": list(_window(args)),
                    "deterministic_bwd": bool(args.deterministic), "entry": "dense batched" if args.dense else "packed varlen",
                    "l2": "inputs larger than L2 (k, v 2 GB each); no flush",
-                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+                   "parallelism": ("heads split over %d ranks (this rank %d heads)" % (ws, H) if full_flops is not None
+                                   else ("replicas" if ws > 1 else "single GPU"))},
         "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
         "fwd_frac_of_burst_peak": fwd_tflops / burst,
         "bwd_frac_of_burst_peak": (bwd_tflops / burst) if bwd_tflops else None,
@@ -665,6 +683,9 @@ def main():
                     help="drive the dense batched entry points (needs equal segment lengths, e.g. --workload dense)")
     ap.add_argument("--fp8", action="store_true",
                     help="time the E4M3 forward alone (head size 128, no mask; quantisation included)")
+    ap.add_argument("--shard", choices=["replicas", "heads"], default="replicas",
+                    help="under torchrun: every rank a batch of its own (replicas, weak scaling) or one problem "
+                         "split by heads across the ranks (strong scaling); no collective on the data path either way")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
