@@ -227,7 +227,10 @@ struct BwdCfg {
   static constexpr int BAR_OFF = TILE_BYTES;
   static constexpr int LSE_OFF = BAR_OFF + 256;
   static constexpr int DELTA_OFF = LSE_OFF + NQ * ROWV_BYTES;
-  static constexpr int SMEM_BYTES = DELTA_OFF + NDO * ROWV_BYTES;
+  static constexpr int ORDER_OFF = DELTA_OFF + NDO * ROWV_BYTES;  // LPT order table
+  static constexpr int ORDER_ROOM = (227 * 1024 - ORDER_OFF) / 2;    // entries that still fit
+  static constexpr int ORDER_CAP = ORDER_ROOM < kLptCapNarrow ? ORDER_ROOM / 8 * 8 : kLptCapNarrow;
+  static constexpr int SMEM_BYTES = ORDER_OFF + 2 * ORDER_CAP;
   static_assert(SMEM_BYTES <= 227 * 1024, "backward tile does not fit one CTA's shared memory");
   // TMEM columns: S^T (later P^T, bf16), dP^T (later dQ^T), dV, dK
   static constexpr int S_COL = 0, DP_COL = 128, DV_COL = 256, DK_COL = 384;
@@ -339,6 +342,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bar.abort = 0;
     fence_barrier_init();
   }
+  const WalkOrder order{reinterpret_cast<const uint16_t*>(smem_raw + C::ORDER_OFF), C::ORDER_CAP};
+  build_lpt_order(order, p.cu_q, p.batch, p.total_q);
   if (warp == 1) tmem_alloc(&bar.tmem_base, C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
@@ -354,11 +359,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       SegCursor c;
-      cursor_init<kTileM>(c, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q);
+      cursor_init<kTileM>(c, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q, order);
       uint32_t tiles = 0, gs = 0;
       bool ok = true;
       for (int64_t t = blockIdx.x;
-           ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q); t += G) {
+           ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q, order); t += G) {
         const Tile tl = cursor_tile(c, t);
         int32_t j0, nq;
         bwd_q_steps<MASKED>(c, tl.m, p, j0, nq);
@@ -401,11 +406,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // ---------------------------------------------------- dO producer
       tma_prefetch_desc(&tm_do);
       SegCursor c;
-      cursor_init<kTileM>(c, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q);
+      cursor_init<kTileM>(c, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q, order);
       uint32_t gs = 0;
       bool ok = true;
       for (int64_t t = blockIdx.x;
-           ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q); t += G) {
+           ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q, order); t += G) {
         const Tile tl = cursor_tile(c, t);
         int32_t j0, nq;
         bwd_q_steps<MASKED>(c, tl.m, p, j0, nq);
@@ -441,7 +446,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t kIdG = idesc_bf16_f32(128, D, false, true);    // dV, dK
       constexpr uint32_t kIdQ = idesc_bf16_f32(128, QT, true, true);    // dQ^T
       SegCursor c;
-      cursor_init<kTileM>(c, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q);
+      cursor_init<kTileM>(c, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q, order);
       uint32_t tiles = 0, gs = 0;
       // descriptor low words (the high word is the constant of the 128-byte swizzle)
       const uint32_t kK = sw128_desc_lo(smem_addr(k_smem), 16);        // K as K-major A
@@ -518,7 +523,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       };
 
       for (int64_t t = blockIdx.x;
-           ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q); t += G) {
+           ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q, order); t += G) {
         const Tile tl = cursor_tile(c, t);
         int32_t j0, nq;
         bwd_q_steps<MASKED>(c, tl.m, p, j0, nq);
@@ -599,11 +604,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const float c2 = p.scale_log2;
     SegCursor c;
-    cursor_init<kTileM>(c, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q);
+    cursor_init<kTileM>(c, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q, order);
     uint32_t gs = 0, tiles = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x;
-         ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q); t += G) {
+         ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q, order); t += G) {
       const Tile tl = cursor_tile(c, t);
       const int32_t kv_valid = c.len - tl.m * kTileM;
       const bool row_valid = r < kv_valid;
@@ -776,11 +781,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const bool drains = quad * 32 < D;             // warp-uniform
     if (DQ) {  // (without dQ -- the deterministic form -- this warpgroup has no work)
       SegCursor c;
-      cursor_init<kTileM>(c, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q);
+      cursor_init<kTileM>(c, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q, order);
       uint32_t gs = 0;
       bool ok = true;
       for (int64_t t = blockIdx.x;
-           ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q); t += G) {
+           ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_k, p.cu_q, p.batch, p.total_k, p.total_q, order); t += G) {
         const Tile tl = cursor_tile(c, t);
         int32_t j0, nq;
         bwd_q_steps<MASKED>(c, tl.m, p, j0, nq);

@@ -51,7 +51,8 @@ struct DqCfg {
   static constexpr int BAR_OFF = V_OFF + NV * TILE;
   static constexpr int LSE_OFF = BAR_OFF + 256;
   static constexpr int DELTA_OFF = LSE_OFF + ROWV;
-  static constexpr int SMEM_BYTES = DELTA_OFF + ROWV;
+  static constexpr int ORDER_OFF = DELTA_OFF + ROWV;  // LPT order table
+  static constexpr int SMEM_BYTES = ORDER_OFF + 2 * kLptCapNarrow;
   static_assert(SMEM_BYTES <= 227 * 1024, "dQ tiles do not fit one CTA's shared memory");
   // TMEM columns: S_0 / S_1 (double buffer, dS over S), dP, dQ (D columns)
   static constexpr int S_COL = 0, DP_COL = 256, DQ_COL = 384;
@@ -143,6 +144,8 @@ __global__ void __launch_bounds__(384, 1)
     bar.abort = 0;
     fence_barrier_init();
   }
+  const WalkOrder order{reinterpret_cast<const uint16_t*>(smem_raw + C::ORDER_OFF), kLptCapNarrow};
+  build_lpt_order(order, p.cu_k, p.batch, p.total_k);
   if (warp == 1) tmem_alloc(&bar.tmem_base, C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
@@ -159,11 +162,11 @@ __global__ void __launch_bounds__(384, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       SegCursor c;
-      cursor_init<kTileM>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k);
+      cursor_init<kTileM>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k, order);
       uint32_t tiles = 0, kn = 0, vn = 0;  // K and V loads issued (load n goes to slot n % NK / n % NV)
       bool ok = true;
       for (int64_t t = blockIdx.x; ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_q, p.cu_k, p.batch,
-                                                                p.total_q, p.total_k);
+                                                                p.total_q, p.total_k, order);
            t += G) {
         const Tile tl = cursor_tile(c, t);
         int32_t j_lo;
@@ -233,7 +236,7 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t vB = sw128_desc_lo(smem_addr(v_ring), 16);           // V slot 0, K-major
       const uint32_t kBm = sw128_desc_lo(smem_addr(k_ring), C::CHUNK);    // K slot 0, MN-major
       SegCursor c;
-      cursor_init<kTileM>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k);
+      cursor_init<kTileM>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k, order);
       uint32_t tiles = 0, g = 0;
       bool ok = true;
 
@@ -293,7 +296,7 @@ __global__ void __launch_bounds__(384, 1)
       };
 
       for (int64_t t = blockIdx.x; ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_q, p.cu_k, p.batch,
-                                                                p.total_q, p.total_k);
+                                                                p.total_q, p.total_k, order);
            t += G) {
         const Tile tl = cursor_tile(c, t);
         int32_t j_lo;
@@ -349,11 +352,11 @@ __global__ void __launch_bounds__(384, 1)
     const float c2 = p.scale_log2;
     constexpr int DH = D / 2;                    // dQ columns written by each warpgroup
     SegCursor c;
-    cursor_init<kTileM>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k);
+    cursor_init<kTileM>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k, order);
     uint32_t tiles = 0, g = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x; ok && cursor_seek<kTileM>(c, t, p.num_heads, p.cu_q, p.cu_k, p.batch,
-                                                              p.total_q, p.total_k);
+                                                              p.total_q, p.total_k, order);
          t += G) {
       const Tile tl = cursor_tile(c, t);
       int32_t j_lo;

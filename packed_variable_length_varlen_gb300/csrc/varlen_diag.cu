@@ -11,11 +11,15 @@ namespace varlen {
 template <int TILE>
 __global__ void debug_schedule_kernel(const int32_t* cu, int32_t batch, int32_t total, int32_t num_heads,
                                       int32_t* out, int64_t max_records) {
+  __shared__ uint16_t order_tab[kLptCapWide];
+  const CuView v{cu, 0};
+  const WalkOrder order{order_tab, kLptCapWide};
+  build_lpt_order(order, v, batch, total);
+  __syncthreads();
   if (threadIdx.x != 0) return;
   SegCursor c;
-  const CuView v{cu, 0};
-  cursor_init<TILE>(c, v, v, batch, total, total);
-  for (int64_t t = blockIdx.x; cursor_seek<TILE>(c, t, num_heads, v, v, batch, total, total); t += gridDim.x) {
+  cursor_init<TILE>(c, v, v, batch, total, total, order);
+  for (int64_t t = blockIdx.x; cursor_seek<TILE>(c, t, num_heads, v, v, batch, total, total, order); t += gridDim.x) {
     const Tile tl = cursor_tile(c, t);
     if (t < max_records) {
       int4 rec = make_int4(tl.b, tl.m, tl.h, (int)blockIdx.x);

@@ -205,7 +205,8 @@ namespace {
 constexpr int kF8Unit = 2 * kTileM;           // q rows per scheduled unit (two halves)
 constexpr int kF8Tile = 128 * 128;            // one tile: 128 rows of 128 codes
 constexpr int kF8Slots = 8;                   // K / V^T ring slots
-constexpr int kF8SmemBytes = 1024 + 1024 + kF8Tile * (4 + kF8Slots);  // barriers, align, Q_A Q_B P_A P_B, ring
+constexpr int kF8OrderOff = 1024 + kF8Tile * (4 + kF8Slots);  // LPT order table (from the aligned base)
+constexpr int kF8SmemBytes = 1024 + kF8OrderOff + 2 * kLptCapWide;  // align, barriers, Q_A Q_B P_A P_B, ring, order
 constexpr int kF8OCol = 256;                  // TMEM column of O_A (O_B at +128); S_A at 0, S_B at 128
 
 struct F8Barriers {
@@ -253,6 +254,8 @@ __global__ void __launch_bounds__(384, 1)
     bar.abort = 0;
     fence_barrier_init();
   }
+  const WalkOrder order{reinterpret_cast<const uint16_t*>(smem + kF8OrderOff), kLptCapWide};
+  build_lpt_order(order, p.cu_k, p.batch, p.total_k);
   if (warp == 1) tmem_alloc(&bar.tmem_base, 512);
   tc_fence_before();
   __syncthreads();
@@ -269,11 +272,11 @@ __global__ void __launch_bounds__(384, 1)
       tma_prefetch_desc(&tm_k8);
       tma_prefetch_desc(&tm_vt);
       SegCursor c;
-      cursor_init<kF8Unit>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k);
+      cursor_init<kF8Unit>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k, order);
       uint32_t q_loads = 0, ring_pos = 0;
       bool ok = true;
       for (int64_t t = blockIdx.x;
-           ok && cursor_seek<kF8Unit>(c, t, H, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k); t += G) {
+           ok && cursor_seek<kF8Unit>(c, t, H, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k, order); t += G) {
         const Tile tl = cursor_tile(c, t);
         const int32_t nkv = (c.olen + kTileN - 1) / kTileN;
         if (nkv == 0) continue;
@@ -317,7 +320,7 @@ __global__ void __launch_bounds__(384, 1)
       // S = Q K_{j+1}^T; 4 k-steps of 32 codes per product.
       constexpr uint32_t kIdesc = idesc_e4m3_f32(128, 128);
       SegCursor c;
-      cursor_init<kF8Unit>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k);
+      cursor_init<kF8Unit>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k, order);
       uint32_t tiles = 0, g = 0, ring0 = 0;
       bool ok = true;
       const uint32_t qlo = sw128_desc_lo(smem_addr(q_smem), 16);
@@ -338,7 +341,7 @@ __global__ void __launch_bounds__(384, 1)
         mma_commit(&bar.pv_done[hf]);  // also: the P buffer of this half is free again
       };
       for (int64_t t = blockIdx.x;
-           ok && cursor_seek<kF8Unit>(c, t, H, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k); t += G) {
+           ok && cursor_seek<kF8Unit>(c, t, H, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k, order); t += G) {
         const int32_t nkv = (c.olen + kTileN - 1) / kTileN;
         if (nkv == 0) continue;
         if (!mbar_wait(&bar.q_full, tiles & 1, abort)) break;
@@ -392,11 +395,11 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t s_col = hf * 128, o_col = kF8OCol + hf * 128;
     uint8_t* prow = p_smem + hf * kF8Tile + row * 128;  // this row of P (128-byte swizzle)
     SegCursor c;
-    cursor_init<kF8Unit>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k);
+    cursor_init<kF8Unit>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k, order);
     uint32_t g = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x;
-         ok && cursor_seek<kF8Unit>(c, t, H, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k); t += G) {
+         ok && cursor_seek<kF8Unit>(c, t, H, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k, order); t += G) {
       const Tile tl = cursor_tile(c, t);
       const int32_t nkv = (c.olen + kTileN - 1) / kTileN;
       const int32_t r_seg = tl.m * kF8Unit + hf * kTileM + row;

@@ -70,7 +70,8 @@ struct FwdCfg {
   static constexpr int NSLOT = (NC == 1) ? 8 : 4;       // K/V ring slots
   static constexpr int O_COL = 256;                     // TMEM column of O_A (O_B at +128)
   static constexpr int TMEM_COLS = 512;
-  static constexpr int SMEM_BYTES = 1024 + 1024 + TILE * (2 + NSLOT);
+  static constexpr int ORDER_OFF = 1024 + TILE * (2 + NSLOT);         // LPT order table
+  static constexpr int SMEM_BYTES = ORDER_OFF + 2 * kLptCapWide;
   static constexpr int KSTEPS = D / 16;                 // K-steps of S = Q K^T
 };
 
@@ -85,11 +86,11 @@ struct FwdBarriers {
 static_assert(sizeof(FwdBarriers) <= 1024, "barrier block too large");
 
 // Registers: the block launches 384 threads at 168 registers (64,512).
-// Warpgroup 0 (producer, MMA, two idle warps) drops to 112 and the two
-// softmax warpgroups rise to 192: 112*128 + 2*192*128 = 63,488 <= 64,512,
-// and each SM sub-partition holds one warp of each group:
-// (112+192+192)*32 <= 16K.
-constexpr uint32_t kFwdRegsLaunch = 168, kFwdRegsCtl = 112, kFwdRegsSoftmax = 192;
+// Warpgroup 0 (producer, MMA, two idle warps) drops to 120 and the two
+// softmax warpgroups rise to 192: 120*128 + 2*192*128 = 64,512, the launch
+// allocation, and each SM sub-partition holds one warp of each group:
+// (120+192+192)*32 <= 16K.
+constexpr uint32_t kFwdRegsLaunch = 168, kFwdRegsCtl = 120, kFwdRegsSoftmax = 192;
 static_assert(kFwdRegsCtl + 2 * kFwdRegsSoftmax <= 3 * kFwdRegsLaunch,
               "warpgroup register split exceeds the launch allocation");
 static_assert(kFwdRegsLaunch * 384 <= 65536, "launch register count too large for 384 threads");
@@ -99,8 +100,14 @@ __global__ void __launch_bounds__(384, 1)
     varlen_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using C = FwdCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // The 128-byte swizzled tiles need 1024-byte alignment; the declaration
+  // asks for it and the kernel refuses to run without it.
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if ((smem_addr(smem_raw) & 1023u) != 0) {
+    if (threadIdx.x == 0) record_error(p.err, kErrBounds);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   FwdBarriers& bar = *reinterpret_cast<FwdBarriers*>(smem);
   uint8_t* q_smem = smem + 1024;           // Q_A then Q_B
   uint8_t* ring = q_smem + 2 * C::TILE;
@@ -125,6 +132,8 @@ __global__ void __launch_bounds__(384, 1)
     bar.abort = 0;
     fence_barrier_init();
   }
+  const WalkOrder order{reinterpret_cast<const uint16_t*>(smem_raw + C::ORDER_OFF), kLptCapWide};
+  build_lpt_order(order, p.cu_k, p.batch, p.total_k);
   if (warp == 1) tmem_alloc(&bar.tmem_base, C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
@@ -142,12 +151,12 @@ __global__ void __launch_bounds__(384, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       SegCursor c;
-      cursor_init<kFwdUnit>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k);
+      cursor_init<kFwdUnit>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k, order);
       uint32_t q_loads = 0;
       uint32_t ring_pos = 0;  // loads issued into the ring so far
       bool ok = true;
       for (int64_t t = blockIdx.x; ok && cursor_seek<kFwdUnit>(c, t, p.num_heads, p.cu_q, p.cu_k, p.batch,
-                                                                 p.total_q, p.total_k);
+                                                                 p.total_q, p.total_k, order);
            t += G) {
         const Tile tl = cursor_tile(c, t);
         int32_t j_lo;
@@ -210,7 +219,7 @@ __global__ void __launch_bounds__(384, 1)
     constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
     constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, false, true);
     SegCursor c;
-    cursor_init<kFwdUnit>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k);
+    cursor_init<kFwdUnit>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k, order);
     uint32_t tiles = 0, g = 0, ring0 = 0;
     bool ok = true;
     const uint32_t qlo = sw128_desc_lo(smem_addr(q_smem), 16);        // Q_A (Q_B at +TILE), K-major A
@@ -235,7 +244,7 @@ __global__ void __launch_bounds__(384, 1)
       mma_commit(&bar.pv_done[hf]);
     };
     for (int64_t t = blockIdx.x;
-         ok && cursor_seek<kFwdUnit>(c, t, p.num_heads, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k); t += G) {
+         ok && cursor_seek<kFwdUnit>(c, t, p.num_heads, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k, order); t += G) {
       int32_t j_lo;
       const int32_t nkv = fwd_kv_tiles<MASKED>(c, cursor_tile(c, t).m, p, j_lo);
       if (nkv == 0) continue;
@@ -307,11 +316,11 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t s_col = hf * 128, o_col = C::O_COL + hf * 128;
     const float c2 = p.scale_log2;
     SegCursor c;
-    cursor_init<kFwdUnit>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k);
+    cursor_init<kFwdUnit>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k, order);
     uint32_t g = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x;
-         ok && cursor_seek<kFwdUnit>(c, t, p.num_heads, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k); t += G) {
+         ok && cursor_seek<kFwdUnit>(c, t, p.num_heads, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k, order); t += G) {
       const Tile tl = cursor_tile(c, t);
       int32_t j_lo;
       const int32_t nkv = fwd_kv_tiles<MASKED>(c, tl.m, p, j_lo);

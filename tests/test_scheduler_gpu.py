@@ -1,8 +1,9 @@
 """The device tile scheduler run on its own: every (segment, row-block, head)
 tile is visited exactly once, by the CTA the static persistent order assigns,
-and the count equals H * sum_b ceil(len_b / tile) -- 15680 for the windowed
-workload, the valid-tile count printed on the "[FA4][SM120] ... >=4 varlen
-segments" issue (section "Interpretation")."""
+in the longest-processing-time-first order of the segments, and the count
+equals H * sum_b ceil(len_b / tile) -- 15680 for the windowed workload, the
+valid-tile count printed on the "[FA4][SM120] ... >=4 varlen segments" issue
+(section "Interpretation")."""
 import json
 import os
 
@@ -16,9 +17,18 @@ pytestmark = pytest.mark.gpu
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "page_values.json")
 
 
+def _lpt(cu):
+    """The walk order of the segments: longest processing time first, by
+    ceil(len / 128) descending (each tile of a segment iterates over 128-row
+    steps of its length), ties by index; the index order for one segment."""
+    B = len(cu) - 1
+    cost = [-(-max(0, cu[b + 1] - cu[b]) // 128) for b in range(B)]
+    return sorted(range(B), key=lambda b: (-cost[b], b)) if B > 1 else list(range(B))
+
+
 def _expected(cu, H, tile):
     recs = []
-    for b in range(len(cu) - 1):
+    for b in _lpt(cu):
         n = -(-max(0, cu[b + 1] - cu[b]) // tile)
         for h in range(H):
             for m in range(n):
@@ -95,3 +105,15 @@ def test_malformed_cu_is_clamped():
     assert va.varlen_attn_debug_schedule(cu.cuda(), 5, total, 2, 128, 3, out, n + 100) == 0
     got = out.cpu().numpy()
     assert np.all(got[n:] == -1) and np.all(got[:n, 0] >= 0) and np.all(got[:n, 0] < 5)
+    # clamped lengths 260, 0, 160, 0, 260: the walk takes segments 0, 4, 2
+    segs = [int(b) for b in got[:n, 0]]
+    assert [b for i, b in enumerate(segs) if i == 0 or segs[i - 1] != b] == [0, 4, 2]
+
+
+def test_lpt_order_many_segments():
+    """Hundreds of segments of mixed lengths: exact coverage in the LPT walk
+    (the order table holds up to 4096 segments)."""
+    rng = np.random.default_rng(5)
+    lens = rng.integers(0, 3000, size=600)
+    cu = [0] + list(np.cumsum(lens))
+    _run(cu, 2, 128, 152)
