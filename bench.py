@@ -39,7 +39,7 @@ from packed_variable_length_varlen_gb300 import sharding
 from packed_variable_length_varlen_gb300 import workloads as W
 
 METRIC = "varlen attention TFLOP/s (fwd, bwd) bf16 H=56 D=128; % of GB300 bf16 TC peak"
-BWD_MAIN_DRAM_BYTES_PER_HEAD = {("windowed", 128): (873.125120e6 + 672.273920e6) / 8}
+BWD_MAIN_DRAM_BYTES_PER_HEAD = {("windowed", 128): (874.832640e6 + 671.547392e6) / 8}
 
 
 def _window(args):
@@ -571,7 +571,7 @@ def ours(args, w, ws, rank, local):
     peak = float(peaks.get("bf16_tflops"))
     sust = float(peaks.get("bf16_tflops_sustained", peak))
     # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the backward main
-    # kernel, from one ncu capture of the windowed workload at H=8 (kernel as of commit eb33260).
+    # kernel, from one ncu capture of the windowed workload at H=8 (kernel as of commit af71323).
     # Every head reads its own q, k, v, dout and writes its own dk, dv and dq rows, so the
     # traffic scales with the number of heads.  Reported only for that workload and head size.
     traffic = None
