@@ -358,3 +358,25 @@ def test_noalloc_without_gpu_reports_cuda_error(va):
     assert va.varlen_attn_last_cuda_error() != "no error"
     st2, addr, ctx = va.varlen_attn_debug_noalloc_scratch()
     assert st2 == va.VARLEN_ERR_CUDA and addr == 0 and ctx == 0
+
+
+def test_debug_knobs_validate_without_a_gpu(va):
+    """The bounds-checking query and the debug knobs answer on the host: the
+    normal build carries no checks, a negative span slack and an unknown
+    producer are refused, and every knob can be reset."""
+    assert va.varlen_attn_bounds_checked() is False
+    assert va.varlen_attn_debug_set_span_slack(-1) == va.VARLEN_ERR_SHAPE
+    assert va.varlen_attn_debug_set_span_slack(16) == va.VARLEN_OK
+    assert va.varlen_attn_debug_set_span_slack(0) == va.VARLEN_OK
+    assert va.varlen_attn_debug_skip_load(2, 1) == va.VARLEN_ERR_SHAPE
+    for which in (0, 1):
+        assert va.varlen_attn_debug_skip_load(which, 3) == va.VARLEN_OK
+        assert va.varlen_attn_debug_skip_load(which, -1) == va.VARLEN_OK
+
+
+def test_bounds_build_is_separate():
+    """The bounds-checking variant builds into its own directory from the
+    same sources with -DVARLEN_DEBUG_BOUNDS (compiled here, not loaded)."""
+    from packed_variable_length_varlen_gb300 import build
+    assert build.BOUNDS_LIB != build.LIB
+    assert os.path.dirname(build.BOUNDS_LIB).endswith(os.path.join("_build", "bounds"))
