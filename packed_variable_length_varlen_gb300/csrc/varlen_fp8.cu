@@ -205,8 +205,8 @@ namespace {
 constexpr int kF8Unit = 2 * kTileM;           // q rows per scheduled unit (two halves)
 constexpr int kF8Tile = 128 * 128;            // one tile: 128 rows of 128 codes
 constexpr int kF8Slots = 8;                   // K / V^T ring slots
-constexpr int kF8OrderOff = 1024 + kF8Tile * (4 + kF8Slots);  // LPT order table (from the aligned base)
-constexpr int kF8SmemBytes = 1024 + kF8OrderOff + 2 * kLptCapWide;  // align, barriers, Q_A Q_B P_A P_B, ring, order
+constexpr int kF8OrderOff = 1024 + kF8Tile * (2 + kF8Slots);  // LPT order table (from the aligned base)
+constexpr int kF8SmemBytes = 1024 + kF8OrderOff + 2 * kLptCapWide;  // align, barriers, Q_A Q_B, ring, order
 constexpr int kF8OCol = 256;                  // TMEM column of O_A (O_B at +128); S_A at 0, S_B at 128
 
 struct F8Barriers {
@@ -232,8 +232,7 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   F8Barriers& bar = *reinterpret_cast<F8Barriers*>(smem);
   uint8_t* q_smem = smem + 1024;              // Q_A, Q_B
-  uint8_t* p_smem = q_smem + 2 * kF8Tile;     // P_A, P_B (E4M3, K-major)
-  uint8_t* ring = p_smem + 2 * kF8Tile;
+  uint8_t* ring = q_smem + 2 * kF8Tile;
   volatile int* abort = &bar.abort;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -316,15 +315,17 @@ __global__ void __launch_bounds__(384, 1)
       }
     } else if (warp == 1 && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
-      // Per kv step j and half: O += P V_j (P from shared memory), then
-      // S = Q K_{j+1}^T; 4 k-steps of 32 codes per product.
+      // Per kv step j and half: O += P V_j (P from TMEM, E4M3 codes written
+      // over the first 32 of the half's S columns), then S = Q K_{j+1}^T,
+      // which overwrites them only after the product has read them (the
+      // MMAs of one thread execute in issue order); 4 k-steps of 32 codes
+      // per product.
       constexpr uint32_t kIdesc = idesc_e4m3_f32(128, 128);
       SegCursor c;
       cursor_init<kF8Unit>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k, order);
       uint32_t tiles = 0, g = 0, ring0 = 0;
       bool ok = true;
       const uint32_t qlo = sw128_desc_lo(smem_addr(q_smem), 16);
-      const uint32_t plo = sw128_desc_lo(smem_addr(p_smem), 16);
       const uint32_t rlo = sw128_desc_lo(smem_addr(ring), 16);
       auto issue_s = [&](int hf, uint32_t kslot) {
 #pragma unroll
@@ -336,9 +337,9 @@ __global__ void __launch_bounds__(384, 1)
       auto issue_pv = [&](int hf, uint32_t vslot, bool first) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_f8_ss_lo(tmem + kF8OCol + hf * 128, plo + ((hf * kF8Tile + kk * 32) >> 4),
-                       rlo + ((vslot * kF8Tile + kk * 32) >> 4), kIdesc, (!first || kk > 0) ? 1u : 0u);
-        mma_commit(&bar.pv_done[hf]);  // also: the P buffer of this half is free again
+          mma_f8_ts_lo(tmem + kF8OCol + hf * 128, tmem + hf * 128 + kk * 8, rlo + ((vslot * kF8Tile + kk * 32) >> 4),
+                       kIdesc, (!first || kk > 0) ? 1u : 0u);
+        mma_commit(&bar.pv_done[hf]);
       };
       for (int64_t t = blockIdx.x;
            ok && cursor_seek<kF8Unit>(c, t, H, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k, order); t += G) {
@@ -393,7 +394,6 @@ __global__ void __launch_bounds__(384, 1)
     const int row = quad * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t s_col = hf * 128, o_col = kF8OCol + hf * 128;
-    uint8_t* prow = p_smem + hf * kF8Tile + row * 128;  // this row of P (128-byte swizzle)
     SegCursor c;
     cursor_init<kF8Unit>(c, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k, order);
     uint32_t g = 0;
@@ -465,28 +465,33 @@ __global__ void __launch_bounds__(384, 1)
           rescale = true;
         }
         // P = exp2(S c - m) in fp32, row sum of the unrounded P; the codes of
-        // P go to this half's P buffer once the previous P V has read it
-        if (j > 0 && !mbar_wait(&bar.pv_done[hf], (gj - 1) & 1, abort)) { ok = false; break; }
-        float rs = 0.f;
+        // P go into TMEM over the first 32 S columns (already read), four
+        // consecutive keys per 32-bit column, the A operand of P V.
+        // (two lanes at a time: packed fma / add, as in the bf16 kernel)
+        const float2 cc2 = make_float2(c2, c2), negm = make_float2(-m_use, -m_use);
+        float2 rs2a = make_float2(0.f, 0.f), rs2b = make_float2(0.f, 0.f);
+        uint32_t pw[32];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {  // 16-byte unit u = columns 16u .. 16u+15
-          uint32_t w[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int e = u * 16 + k * 4;
-            const float p0 = ex2(fmaf(x[e], c2, -m_use)), p1 = ex2(fmaf(x[e + 1], c2, -m_use));
-            const float p2 = ex2(fmaf(x[e + 2], c2, -m_use)), p3 = ex2(fmaf(x[e + 3], c2, -m_use));
-            rs += (p0 + p1) + (p2 + p3);
-            const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(p0, p1), __NV_SATFINITE, __NV_E4M3);
-            const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(p2, p3), __NV_SATFINITE, __NV_E4M3);
-            w[k] = lo | (hi << 16);
-          }
-          *reinterpret_cast<uint4*>(prow + ((u ^ (row & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int k = 0; k < 32; ++k) {
+          const int e = k * 4;
+          float2 t0 = ffma2(make_float2(x[e], x[e + 1]), cc2, negm);
+          float2 t1 = ffma2(make_float2(x[e + 2], x[e + 3]), cc2, negm);
+          t0.x = ex2(t0.x);
+          t0.y = ex2(t0.y);
+          t1.x = ex2(t1.x);
+          t1.y = ex2(t1.y);
+          rs2a = fadd2(rs2a, t0);
+          rs2b = fadd2(rs2b, t1);
+          const uint32_t lo = __nv_cvt_float2_to_fp8x2(t0, __NV_SATFINITE, __NV_E4M3);
+          const uint32_t hi = __nv_cvt_float2_to_fp8x2(t1, __NV_SATFINITE, __NV_E4M3);
+          pw[k] = lo | (hi << 16);
         }
-        fence_proxy_async_smem();
+        const float rs = (rs2a.x + rs2a.y) + (rs2b.x + rs2b.y);
+        tmem_st32(tmem + lane_off + s_col, pw);
         l = fmaf(l, alpha, rs);
         if (__any_sync(0xffffffffu, rescale)) {
-          // S_j was issued after O += P_{j-1} V_{j-1} of this half, so O is complete here
+          // S_j was issued after O += P_{j-1} V_{j-1} of this half (issue
+          // order), so O is complete here
 #pragma unroll
           for (int d0 = 0; d0 < 128; d0 += 32) {
             uint32_t o[32];
@@ -496,8 +501,8 @@ __global__ void __launch_bounds__(384, 1)
             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
             tmem_st32(tmem + lane_off + o_col + d0, o);
           }
-          tmem_wait_st();
         }
+        tmem_wait_st();  // P (and a rescaled O) are in TMEM
         tc_fence_before();
         mbar_arrive(&bar.p_full[hf]);
       }
