@@ -4,15 +4,24 @@
 // Four launches on the caller's stream:
 //  1. varlen_fp8_amax_kernel: max |x| of Q, K and V per (segment, head),
 //     by atomic max on the fp32 bit patterns (non-negative floats order as
-//     unsigned integers).
+//     unsigned integers); a grid-wide sweep, as a copy kernel reads.
 //  2. varlen_fp8_quant_kernel: Q and K to E4M3 codes in NHD layout, code of
 //     x = e4m3(x / descale), descale = amax / 448 (1 for an all-zero block),
 //     round to nearest even, saturating (fp32 division and conversion: the
-//     precision that decides each code).
+//     precision that decides each code); the same sweep.
 //  3. varlen_fp8_vt_kernel: V to E4M3 codes transposed to [H][128][kp], one
-//     128-key block per CTA visit through shared memory, so that V is a
-//     K-major operand of the P V product; segment starts are multiples of
-//     128 columns and the columns past a segment's end hold code 0.
+//     128-key block of one head per CTA visit through shared memory, so that
+//     V is a K-major operand of the P V product; segment starts are
+//     multiples of 128 columns and the columns past a segment's end hold
+//     code 0.
+//  The fp32 quotient x / descale is the IEEE one; it is formed from the
+//  correctly rounded reciprocal of the descale and one fma remainder
+//  correction (Markstein's division step: q0 = x * y, r = x - q0 * d exact,
+//  q = q0 + r * y, given x's sign), which gives the correctly rounded
+//  quotient while the remainder stays a normal number: for descales below
+//  2^-100 the kernels divide.  Checked for every positive bf16 amax and every
+//  bf16 x of magnitude at most amax: the two quotients have the same sign and
+//  differ only below 2^-11 in magnitude, where both codes are a signed 0.
 //  4. varlen_fp8_fwd_kernel: the forward of the bf16 kernel (two 128-row
 //     halves per scheduled unit sharing each key tile, online softmax with
 //     lazy rescaling) on the codes:
@@ -27,6 +36,8 @@
 // quantised attention only by its accuracy (the ffpa-attn NVFP4 pull
 // request, "Summary": cos ~0.982 against SDPA).
 #include <cuda_fp8.h>
+
+#include <algorithm>
 
 #include "sm103_ptx.cuh"
 #include "varlen_internal.h"
@@ -67,133 +78,293 @@ __device__ __forceinline__ void load8(const __nv_bfloat16* src, float (&f)[8], c
   }
 }
 
+// x / d in fp32, correctly rounded, for one descale d and many x.
+struct Divider {
+  float d, y;  // descale and its correctly rounded reciprocal
+  bool fast;   // d >= 2^-100: Markstein's step is exact
+  __device__ __forceinline__ float operator()(float x) const {
+    if (!fast) return x / d;
+    const float q0 = __fmul_rn(x, y);
+    const float r = __fmaf_rn(-q0, d, x);
+    return copysignf(__fmaf_rn(r, y, q0), x);  // the quotient's sign, zeros included, is x's (d > 0)
+  }
+};
+
+__device__ __forceinline__ Divider divider(float descale) {
+  Divider v;
+  v.d = descale;
+  v.y = __frcp_rn(descale);
+  v.fast = descale >= 0x1p-100f;
+  return v;
+}
+
 // Four E4M3 codes of a / d, b / d, c / d, e / d packed low byte first.
-__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float e, float d) {
-  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a / d, b / d), __NV_SATFINITE, __NV_E4M3);
-  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c / d, e / d), __NV_SATFINITE, __NV_E4M3);
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float e, const Divider& d) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(d(a), d(b)), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(d(c), d(e)), __NV_SATFINITE, __NV_E4M3);
   return lo | (hi << 16);
 }
 
 }  // namespace
 
-// ------------------------------------------------------------------ amax
+// ------------------------------------------------------------------ amax, Q / K codes
+//
+// Both passes sweep q, k (and v) in turn with the whole grid, the way a copy
+// kernel does: the threads are cut into slots of 16 lanes per (head, row),
+// 16 bytes per lane, H * 16 slots per row and R = (threads / (H * 16)) rows
+// per sweep step, so that each step reads R consecutive rows, all heads, and
+// every lane keeps its head and 8-value slice for the whole sweep while its
+// row advances by R.  A lane keeps the state of its current segment (the
+// running max, or the descale) in registers and looks the segment up again
+// only when its row leaves it.  Each lane issues kSweepUnroll rows' loads
+// before it uses any.
 
-__global__ void __launch_bounds__(256) varlen_fp8_amax_kernel(const Fp8Params p) {
-  const int which = blockIdx.y;  // 0 = q, 1 = k, 2 = v
-  const __nv_bfloat16* x = which == 0 ? p.q : (which == 1 ? p.k : p.v);
-  const int64_t rs = which == 0 ? p.q_rs : (which == 1 ? p.k_rs : p.v_rs);
-  const int64_t hs = which == 0 ? p.q_hs : (which == 1 ? p.k_hs : p.v_hs);
-  const CuView cu = which == 0 ? p.cu_q : p.cu_k;
-  const int32_t total = which == 0 ? p.total_q : p.total_k;
-  const Span xs = which == 0 ? p.q_span : (which == 1 ? p.k_span : p.v_span);
-  const int32_t B = p.batch, H = p.num_heads;
-  unsigned int* amax = reinterpret_cast<unsigned int*>(p.amax) + (int64_t)which * B * H;
-  const int32_t lo = clamp_row(cu_at(cu, 0), total), hi = clamp_row(cu_at(cu, B), total);
-  if (hi <= lo) return;
-  const int64_t n = (int64_t)(hi - lo) * H;
-  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n; t += (int64_t)gridDim.x * blockDim.x) {
-    const int32_t row = lo + (int32_t)(t / H);
-    const int h = (int)(t % H);
-    int32_t b;
-    if (!segment_of_row(cu, B, total, row, b)) continue;
-    const __nv_bfloat16* src = x + (int64_t)row * rs + (int64_t)h * hs;
-    float mx = 0.f;
-#pragma unroll 4
-    for (int d = 0; d < 128; d += 8) {
-      float f[8];
-      load8(src + d, f, xs, p.err);
+constexpr int kSweepThreads = 256;
+constexpr int kAmaxBlocksPerSm = 5;   // CTAs per SM (48 registers)
+constexpr int kQuantBlocksPerSm = 4;  // CTAs per SM (64 registers)
+constexpr int kSweepUnroll = 4;
+
+struct Sweep {
+  const __nv_bfloat16* x;
+  int64_t rs, hs;
+  CuView cu;
+  int32_t total, lo, hi;
+  Span span;
+};
+
+__device__ __forceinline__ Sweep sweep_of(const Fp8Params& p, int which) {
+  Sweep t;
+  t.x = which == 0 ? p.q : (which == 1 ? p.k : p.v);
+  t.rs = which == 0 ? p.q_rs : (which == 1 ? p.k_rs : p.v_rs);
+  t.hs = which == 0 ? p.q_hs : (which == 1 ? p.k_hs : p.v_hs);
+  t.cu = which == 0 ? p.cu_q : p.cu_k;
+  t.total = which == 0 ? p.total_q : p.total_k;
+  t.span = which == 0 ? p.q_span : (which == 1 ? p.k_span : p.v_span);
+  t.lo = clamp_row(cu_at(t.cu, 0), t.total);
+  t.hi = clamp_row(cu_at(t.cu, p.batch), t.total);
+  return t;
+}
+
+// Slot of this thread: head h, lane gl of the head's 16, first row offset
+// row_off, rows per step R; false for the few threads past the last whole row
+// of slots (they still take part in warp shuffles).
+__device__ __forceinline__ bool sweep_slot(int32_t H, int& h, int& gl, int64_t& row_off, int64_t& R) {
+  const int64_t S = (int64_t)H * 16;
+  const int64_t T = (int64_t)gridDim.x * blockDim.x;
+  const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  R = T / S;
+  const bool active = g < R * S;
+  h = (int)((g % S) / 16);
+  gl = (int)(g % 16);
+  row_off = active ? g / S : INT64_MAX / 4;  // inactive: no row
+  return active;
+}
+
+__device__ __forceinline__ float absmax8(const uint4& u) {
+  const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&u);
+  float m = 0.f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx = fmaxf(mx, fabsf(f[i]));
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __bfloat1622float2(hv[i]);
+    m = fmaxf(m, fmaxf(fabsf(t.x), fabsf(t.y)));
+  }
+  return m;
+}
+
+// amax: max |x| per (segment, head) of q, k and v, by an atomic max on the
+// fp32 bit pattern (non-negative floats order as unsigned integers) into a
+// zeroed [3][batch * H] array: a 16-lane slot group reduces its lanes' maxima
+// by shuffles and adds one atomic each time its row leaves a segment, and
+// once at the end.
+__global__ void __launch_bounds__(kSweepThreads, kAmaxBlocksPerSm) varlen_fp8_amax_kernel(const Fp8Params p) {
+  const int32_t B = p.batch, H = p.num_heads;
+  int h, gl;
+  int64_t row_off, R;
+  sweep_slot(H, h, gl, row_off, R);
+  for (int which = 0; which < 3; ++which) {
+    const Sweep X = sweep_of(p, which);
+    unsigned int* amax = reinterpret_cast<unsigned int*>(p.amax) + (int64_t)which * B * H;
+    const __nv_bfloat16* base = X.x + (int64_t)h * X.hs + gl * 8;
+    int32_t b = -1, seg_lo = 0, seg_hi = 0;  // current segment and its rows
+    float m = 0.f;
+    for (int64_t r = X.lo + row_off;; r += kSweepUnroll * R) {
+      if (!__any_sync(0xffffffffu, r < X.hi)) break;
+      uint4 u[kSweepUnroll];
+#pragma unroll
+      for (int k = 0; k < kSweepUnroll; ++k) {
+        const int64_t rk = r + k * R;
+        const __nv_bfloat16* a = base + rk * X.rs;
+        u[k] = (rk < X.hi && in_span(X.span, a, 16, p.err)) ? __ldg(reinterpret_cast<const uint4*>(a))
+                                                            : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int k = 0; k < kSweepUnroll; ++k) {
+        const int64_t rk = r + k * R;
+        const bool valid = rk < X.hi;
+        const bool leave = valid && (rk < seg_lo || rk >= seg_hi);  // same for the 16 lanes of a slot group
+        if (__any_sync(0xffffffffu, leave)) {
+          float mx = m;
+#pragma unroll
+          for (int o = 8; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          if (leave) {
+            if (gl == 0 && b >= 0) {
+              unsigned int* slot = amax + (int64_t)b * H + h;
+              if (in_span(p.amax_span, slot, 4, p.err)) atomicMax(slot, __float_as_uint(mx));
+            }
+            m = 0.f;
+            if (segment_of_row(X.cu, B, X.total, (int32_t)rk, b)) {
+              seg_lo = clamp_row(cu_at(X.cu, b), X.total);
+              seg_hi = clamp_row(cu_at(X.cu, b + 1), X.total);
+            } else {  // no segment holds the row: look again at the next one
+              b = -1;
+              seg_lo = (int32_t)rk;
+              seg_hi = (int32_t)rk + 1;
+            }
+          }
+        }
+        if (valid && b >= 0) m = fmaxf(m, absmax8(u[k]));
+      }
     }
-    unsigned int* slot = amax + (int64_t)b * H + h;
-    if (in_span(p.amax_span, slot, 4, p.err)) atomicMax(slot, __float_as_uint(mx));
+    float mx = m;
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (gl == 0 && b >= 0) {
+      unsigned int* slot = amax + (int64_t)b * H + h;
+      if (in_span(p.amax_span, slot, 4, p.err)) atomicMax(slot, __float_as_uint(mx));
+    }
   }
 }
 
-// ------------------------------------------------------------------ Q, K codes
-
-__global__ void __launch_bounds__(256) varlen_fp8_quant_kernel(const Fp8Params p) {
-  const int which = blockIdx.y;  // 0 = q, 1 = k
-  const __nv_bfloat16* x = which == 0 ? p.q : p.k;
-  const int64_t rs = which == 0 ? p.q_rs : p.k_rs;
-  const int64_t hs = which == 0 ? p.q_hs : p.k_hs;
-  const CuView cu = which == 0 ? p.cu_q : p.cu_k;
-  const int32_t total = which == 0 ? p.total_q : p.total_k;
-  uint8_t* dst8 = which == 0 ? p.q8 : p.k8;
-  const Span xs = which == 0 ? p.q_span : p.k_span;
-  const Span ds = which == 0 ? p.q8_span : p.k8_span;
+// Q and K to E4M3 codes [rows][H][128]: code = e4m3(x / descale), an IEEE
+// fp32 division, descale = amax / 448 of the row's (segment, head).  Each
+// lane writes the 8 codes of its 8 values: a slot group writes the 128-byte
+// code row of its (row, head).
+__global__ void __launch_bounds__(kSweepThreads, kQuantBlocksPerSm) varlen_fp8_quant_kernel(const Fp8Params p) {
   const int32_t B = p.batch, H = p.num_heads;
-  const float* amax = p.amax + (int64_t)which * B * H;
-  const int32_t lo = clamp_row(cu_at(cu, 0), total), hi = clamp_row(cu_at(cu, B), total);
-  if (hi <= lo) return;
-  const int64_t n = (int64_t)(hi - lo) * H;
-  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n; t += (int64_t)gridDim.x * blockDim.x) {
-    const int32_t row = lo + (int32_t)(t / H);
-    const int h = (int)(t % H);
-    int32_t b;
-    if (!segment_of_row(cu, B, total, row, b)) continue;
-    const float* am = amax + (int64_t)b * H + h;
-    const float dsc = descale_of(in_span(p.amax_span, am, 4, p.err) ? *am : 0.f);
-    const __nv_bfloat16* src = x + (int64_t)row * rs + (int64_t)h * hs;
-    uint4* out = reinterpret_cast<uint4*>(dst8 + ((int64_t)row * H + h) * 128);
-#pragma unroll 2
-    for (int d = 0; d < 128; d += 16) {
-      float f[8], g[8];
-      load8(src + d, f, xs, p.err);
-      load8(src + d + 8, g, xs, p.err);
-      if (in_span(ds, out + d / 16, 16, p.err))
-        out[d / 16] = make_uint4(e4m3x4(f[0], f[1], f[2], f[3], dsc), e4m3x4(f[4], f[5], f[6], f[7], dsc),
-                                 e4m3x4(g[0], g[1], g[2], g[3], dsc), e4m3x4(g[4], g[5], g[6], g[7], dsc));
+  int h, gl;
+  int64_t row_off, R;
+  if (!sweep_slot(H, h, gl, row_off, R)) return;  // no warp collectives below
+  for (int which = 0; which < 2; ++which) {
+    const Sweep X = sweep_of(p, which);
+    uint8_t* dst8 = (which == 0 ? p.q8 : p.k8) + (int64_t)h * 128 + gl * 8;
+    const Span ds = which == 0 ? p.q8_span : p.k8_span;
+    const float* amax = p.amax + (int64_t)which * B * H + h;
+    const __nv_bfloat16* base = X.x + (int64_t)h * X.hs + gl * 8;
+    int32_t b = -1, seg_lo = 0, seg_hi = 0;
+    Divider dsc = divider(1.f);
+    for (int64_t r = X.lo + row_off; r < X.hi; r += kSweepUnroll * R) {
+      uint4 u[kSweepUnroll];
+#pragma unroll
+      for (int k = 0; k < kSweepUnroll; ++k) {
+        const int64_t rk = r + k * R;
+        const __nv_bfloat16* a = base + rk * X.rs;
+        u[k] = (rk < X.hi && in_span(X.span, a, 16, p.err)) ? __ldg(reinterpret_cast<const uint4*>(a))
+                                                            : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int k = 0; k < kSweepUnroll; ++k) {
+        const int64_t rk = r + k * R;
+        if (rk >= X.hi) break;
+        if (rk < seg_lo || rk >= seg_hi) {
+          if (segment_of_row(X.cu, B, X.total, (int32_t)rk, b)) {
+            seg_lo = clamp_row(cu_at(X.cu, b), X.total);
+            seg_hi = clamp_row(cu_at(X.cu, b + 1), X.total);
+            const float* am = amax + (int64_t)b * H;
+            dsc = divider(descale_of(in_span(p.amax_span, am, 4, p.err) ? *am : 0.f));
+          } else {
+            b = -1;
+            seg_lo = (int32_t)rk;
+            seg_hi = (int32_t)rk + 1;
+          }
+        }
+        if (b < 0) continue;  // no segment holds the row
+        const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&u[k]);
+        float f[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 t2 = __bfloat1622float2(hv[i]);
+          f[2 * i] = t2.x;
+          f[2 * i + 1] = t2.y;
+        }
+        uint2* out = reinterpret_cast<uint2*>(dst8 + rk * H * 128);
+        if (in_span(ds, out, 8, p.err))
+          *out = make_uint2(e4m3x4(f[0], f[1], f[2], f[3], dsc), e4m3x4(f[4], f[5], f[6], f[7], dsc));
+      }
     }
   }
 }
 
 // ------------------------------------------------------------------ V^T codes
 
-// One visit = (segment, 128-key block, head) of the exact schedule on the key
-// side: 256 threads quantise the block's 128 rows (thread = row, half of d)
-// into a [d][key] shared tile, then write 128 rows of 128 codes to vt.
-__global__ void __launch_bounds__(256) varlen_fp8_vt_kernel(const Fp8Params p) {
-  __shared__ __align__(16) uint8_t tile[128 * 128];
-  const int r = threadIdx.x >> 1, half = threadIdx.x & 1;
+// One CTA visit = one 128-key block of one (segment, head).  Thread
+// (row group g = lane, d slice s = warp) quantises keys 4g..4g+3 at
+// d = 16s..16s+15 and packs, per d, the four keys' codes into one 32-bit
+// word of the transposed tile (a warp's words fill a 128-byte tile row:
+// conflict-free); the tile then leaves as 128-byte rows of vt.
+__global__ void __launch_bounds__(256, 4) varlen_fp8_vt_kernel(const Fp8Params p) {
+  __shared__ __align__(16) uint32_t tile[128 * 32];  // [d][128 keys] codes
+  const int g = threadIdx.x & 31, s = threadIdx.x >> 5;
   const int32_t B = p.batch, H = p.num_heads;
   const float* amax = p.amax + 2 * (int64_t)B * H;
   SegCursor c;
   cursor_init<128>(c, p.cu_k, p.cu_q, B, p.total_k, p.total_q);
   for (int64_t t = blockIdx.x; cursor_seek<128>(c, t, H, p.cu_k, p.cu_q, B, p.total_k, p.total_q);
        t += gridDim.x) {
-    const Tile tl = cursor_tile(c, t);
+    // the segment's tiles in (key block, head) order, heads fastest: the
+    // grid's concurrent visits read whole rows of adjacent key blocks
+    Tile tl;
+    tl.b = c.b;
+    tl.m = (int32_t)((t - c.first) / H);
+    tl.h = (int32_t)(t - c.first - (int64_t)tl.m * H);
     const int32_t valid = min(128, c.len - tl.m * 128);
     const float* am = amax + (int64_t)c.b * H + tl.h;
-    const float dsc = descale_of(in_span(p.amax_span, am, 4, p.err) ? *am : 0.f);
-    uint8_t code[64];
-    if (r < valid) {
-      const __nv_bfloat16* src = p.v + ((int64_t)c.r0 + tl.m * 128 + r) * p.v_rs + (int64_t)tl.h * p.v_hs + half * 64;
-#pragma unroll
-      for (int d = 0; d < 64; d += 8) {
-        float f[8];
-        load8(src + d, f, p.v_span, p.err);
-        const uint32_t a = e4m3x4(f[0], f[1], f[2], f[3], dsc), e = e4m3x4(f[4], f[5], f[6], f[7], dsc);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          code[d + i] = (uint8_t)(a >> (8 * i));
-          code[d + 4 + i] = (uint8_t)(e >> (8 * i));
-        }
-      }
-    } else {
-#pragma unroll
-      for (int d = 0; d < 64; ++d) code[d] = 0;  // keys past the segment end: code 0 (value 0)
-    }
-#pragma unroll
-    for (int d = 0; d < 64; ++d) tile[(half * 64 + d) * 128 + r] = code[d];
-    __syncthreads();
-    // row dd of the tile (128 codes) -> vt[h][dd][base + 128 m ...]; thread = (dd, 64-byte part)
-    const int dd = threadIdx.x >> 1, part = threadIdx.x & 1;
-    uint8_t* dst = p.vt + ((int64_t)tl.h * 128 + dd) * p.kp + fp8_vt_base(c.r0, c.b) + (int64_t)tl.m * 128 + part * 64;
-    const uint4* srow = reinterpret_cast<const uint4*>(tile + dd * 128 + part * 64);
+    const Divider dsc = divider(descale_of(in_span(p.amax_span, am, 4, p.err) ? *am : 0.f));
+    const __nv_bfloat16* src =
+        p.v + ((int64_t)c.r0 + tl.m * 128 + 4 * g) * p.v_rs + (int64_t)tl.h * p.v_hs + s * 16;
+    uint4 u[4][2];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      if (in_span(p.vt_span, reinterpret_cast<uint4*>(dst) + i, 16, p.err)) reinterpret_cast<uint4*>(dst)[i] = srow[i];
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const __nv_bfloat16* a = src + i * p.v_rs + hf * 8;
+        u[i][hf] = (4 * g + i < valid && in_span(p.v_span, a, 16, p.err)) ? __ldg(reinterpret_cast<const uint4*>(a))
+                                                                          : make_uint4(0, 0, 0, 0);
+      }
+    uint32_t w[16];  // w[j]: codes of keys 4g..4g+3 at d = 16s + j (keys past the segment end: 0)
+#pragma unroll
+    for (int j = 0; j < 16; ++j) w[j] = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (4 * g + i >= valid) continue;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&u[i][hf]);
+        float f[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 t2 = __bfloat1622float2(hv[k]);
+          f[2 * k] = t2.x;
+          f[2 * k + 1] = t2.y;
+        }
+        const uint32_t a = e4m3x4(f[0], f[1], f[2], f[3], dsc), e = e4m3x4(f[4], f[5], f[6], f[7], dsc);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          w[hf * 8 + k] |= ((a >> (8 * k)) & 0xffu) << (8 * i);
+          w[hf * 8 + 4 + k] |= ((e >> (8 * k)) & 0xffu) << (8 * i);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) tile[(s * 16 + j) * 32 + g] = w[j];
+    __syncthreads();
+    // tile row dd (128 codes) -> vt[h][dd][base + 128 m ...]: 8 lanes per row, 16 bytes each
+    const int64_t col0 = fp8_vt_base(c.r0, c.b) + (int64_t)tl.m * 128;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int dd = s * 16 + k * 4 + (g >> 3), part = g & 7;
+      uint4* dst = reinterpret_cast<uint4*>(p.vt + ((int64_t)tl.h * 128 + dd) * p.kp + col0) + part;
+      if (in_span(p.vt_span, dst, 16, p.err)) *dst = reinterpret_cast<const uint4*>(tile + dd * 32)[part];
+    }
     __syncthreads();
   }
 }
@@ -549,10 +720,13 @@ cudaError_t launch_fwd_fp8(const Fp8Launch& L, cudaStream_t stream) {
   const int64_t nbh = (int64_t)p.batch * p.num_heads;
   cudaError_t e = cudaMemsetAsync(p.amax, 0, 3 * nbh * sizeof(float), stream);
   if (e != cudaSuccess) return e;
-  const int elem_grid = L.grid * 8;
-  varlen_fp8_amax_kernel<<<dim3(elem_grid, 3), 256, 0, stream>>>(p);
+  // grid-wide sweeps: a few CTAs per SM, and at least one row of slots (H * 16 threads)
+  const int64_t min_blocks = ((int64_t)p.num_heads * 16 + kSweepThreads - 1) / kSweepThreads;
+  const int64_t amax_blocks = std::max<int64_t>((int64_t)L.grid * kAmaxBlocksPerSm, min_blocks);
+  const int64_t quant_blocks = std::max<int64_t>((int64_t)L.grid * kQuantBlocksPerSm, min_blocks);
+  varlen_fp8_amax_kernel<<<(unsigned)amax_blocks, kSweepThreads, 0, stream>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  varlen_fp8_quant_kernel<<<dim3(elem_grid, 2), 256, 0, stream>>>(p);
+  varlen_fp8_quant_kernel<<<(unsigned)quant_blocks, kSweepThreads, 0, stream>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   varlen_fp8_vt_kernel<<<L.grid * 4, 256, 0, stream>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -26,7 +26,7 @@ SQ = [300, 129, 517, 1, 5, 0, 40, 255, 256, 2, 700]
 SK = [300, 517, 129, 5, 1, 40, 0, 256, 255, 2, 130]
 
 
-def _run(w, cpu):
+def _run(w, cpu, scale=None):
     from packed_variable_length_varlen_gb300 import varlen_attn as va
     dev = cpu.to(DEV)
     H = w.num_heads
@@ -35,7 +35,8 @@ def _run(w, cpu):
     nbytes = va.varlen_attn_fwd_fp8_workspace_size(w.batch, w.total_q, w.total_k, H, 128)
     ws = torch.full((nbytes,), 0x7F, dtype=torch.uint8, device=DEV)  # NaN codes: every used byte is written
     st = va.varlen_attn_fwd_fp8(dev.q, dev.k, dev.v, dev.cu_q, dev.cu_k, w.batch, w.total_q, w.total_k, H, 128,
-                                w.max_q(), w.max_k(), w.softmax_scale, out, lse, ws, nbytes)
+                                w.max_q(), w.max_k(), w.softmax_scale if scale is None else scale, out, lse, ws,
+                                nbytes)
     assert st == 0, va.varlen_attn_status_string(st)
     st = va.varlen_attn_get_device_status()
     assert st == 0, va.varlen_attn_status_string(st)
@@ -60,19 +61,23 @@ def _amax_ref(x, cu, H):
     return a
 
 
-@pytest.mark.parametrize("seed", [0, 1])
-def test_fp8_codes_and_forward(seed):
-    w = W.custom("fp8", SQ, SK, 2, 128)
-    cpu = W.make_inputs(w, seed, with_dout=False)
-    out, lse, amax, q8, k8, vt = _run(w, cpu)
+def _check_codes(w, cpu, amax, q8, k8, vt):
+    """amax, Q / K codes and the transposed V codes equal the oracle's bit for
+    bit; returns the oracle's codes and descales."""
     H = w.num_heads
-    # quantiser: bit for bit
     for i, (x, cu) in enumerate(((cpu.q, w.cu_q), (cpu.k, w.cu_k), (cpu.v, w.cu_k))):
         assert np.array_equal(amax[i].numpy(), _amax_ref(x, cu, H)), i
     q8r, qd = oracle.quantize_e4m3(cpu.q, w.cu_q)
     k8r, kd = oracle.quantize_e4m3(cpu.k, w.cu_k)
     v8r, vd = oracle.quantize_e4m3(cpu.v, w.cu_k)
-    assert torch.equal(q8, q8r) and torch.equal(k8, k8r)
+    for name, got, ref, x, d, cu in (("q", q8, q8r, cpu.q, qd, w.cu_q), ("k", k8, k8r, cpu.k, kd, w.cu_k)):
+        bad = (got != ref).nonzero()
+        if len(bad):
+            r, h, e = (int(t) for t in bad[0])
+            b = int(np.searchsorted(np.asarray(cu), r, side="right")) - 1
+            raise AssertionError("%s codes: %d differ; first at row %d head %d d %d: x %r descale %r gpu %d oracle %d"
+                                 % (name, len(bad), r, h, e, float(x[r, h, e].float()), float(d[b * H + h]),
+                                    int(got[r, h, e]), int(ref[r, h, e])))
     for b in range(w.batch):
         k0, k1 = w.cu_k[b], w.cu_k[b + 1]
         base = 128 * (b + -(-k0 // 128))
@@ -83,6 +88,17 @@ def test_fp8_codes_and_forward(seed):
         assert torch.equal(blk, v8r[k0:k1].permute(1, 2, 0)), b
         pad = -(-n // 128) * 128 - n
         assert bool((vt[:, :, base + n:base + n + pad] == 0).all()), b
+    return q8r, k8r, v8r, qd, kd, vd
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_fp8_codes_and_forward(seed):
+    w = W.custom("fp8", SQ, SK, 2, 128)
+    cpu = W.make_inputs(w, seed, with_dout=False)
+    out, lse, amax, q8, k8, vt = _run(w, cpu)
+    H = w.num_heads
+    # quantiser: bit for bit
+    q8r, k8r, v8r, qd, kd, vd = _check_codes(w, cpu, amax, q8, k8, vt)
     # forward against the oracle's FP8 reading
     rows, heads = oracle.all_pairs(w.total_q, H)
     pf = oracle.Fp8Problem(q8r, k8r, v8r, w.cu_q, w.cu_k, w.softmax_scale, qd, kd, vd, quantize_p=True)
@@ -104,6 +120,42 @@ def test_fp8_codes_and_forward(seed):
     cos = float((o_gpu * o64).sum() / np.linalg.norm(o_gpu) / np.linalg.norm(o64))
     print("fp8 cosine vs fp64", cos)
     assert cos >= 0.998
+
+
+# Segment maxima (bf16 bit patterns) for the every-value test: a subnormal,
+# the smallest normal, the three around a descale of 2^-100 (448 * 2^-100 is
+# 0x11E0), 1, 448, 2^63 and the largest finite bf16.
+ALL_VALUE_AMAX = [0x0005, 0x0080, 0x11DF, 0x11E0, 0x11E1, 0x3F80, 0x43E0, 0x5F00, 0x7F7F]
+
+
+def _every_value_rows(amax_bits, rows):
+    """[rows, 128] bf16 holding every finite bf16 of magnitude <= the bf16
+    amax_bits, both signs, then zeros."""
+    pos = torch.arange(amax_bits + 1, dtype=torch.int32)
+    vals = torch.cat([pos, pos | 0x8000]).to(torch.int16).view(torch.bfloat16)
+    out = torch.zeros(rows * 128, dtype=torch.bfloat16)
+    out[:vals.numel()] = vals
+    return out.view(rows, 128)
+
+
+def test_fp8_codes_every_bf16_value():
+    """Q and V segments whose heads hold every finite bf16 value up to their
+    maximum, for maxima from a subnormal to the largest finite bf16 (descales
+    on both sides of 2^-100 among them): every code equals the oracle's IEEE
+    fp32 division and conversion.  K is ordinary data; the softmax scale is
+    small enough that S stays finite."""
+    lens = [-(-2 * (a + 1) // 128) for a in ALL_VALUE_AMAX]
+    w = W.custom("fp8_every_value", lens, lens, 2, 128)
+    cpu = W.make_inputs(w, 3, with_dout=False)
+    for b, a in enumerate(ALL_VALUE_AMAX):
+        r0, r1 = w.cu_q[b], w.cu_q[b + 1]
+        blk = _every_value_rows(a, r1 - r0)
+        cpu.q[r0:r1, 0] = blk
+        cpu.q[r0:r1, 1] = blk.flip(0)
+        cpu.v[r0:r1, 0] = blk.flip(0)
+        cpu.v[r0:r1, 1] = blk
+    _, _, amax, q8, k8, vt = _run(w, cpu, scale=1e-37)
+    _check_codes(w, cpu, amax, q8, k8, vt)
 
 
 def test_fp8_python_wrapper_matches_raw_call():
