@@ -63,6 +63,65 @@ def test_fwd_padded_strides_canary():
     _fwd_case(w)
 
 
+RESCALE_AMP = (0.05, 3.0, 10.0, 30.0)  # K amplitude per 128-key tile of a segment (last one onwards)
+
+
+def _plant_rising_scores(w):
+    """K rows scaled up tile by tile, so that a row's running max of
+    S * scale * log2(e) grows by more than 8 at tiles 1, 2 and 3: the
+    forward must rescale O (exactly, by alpha = 2^(m_old - m_new))."""
+    def plant(cpu):
+        for b in range(w.batch):
+            k0, k1 = w.cu_k[b], w.cu_k[b + 1]
+            for t, r in enumerate(range(k0, k1, 128)):
+                cpu.k[r:min(r + 128, k1)] *= RESCALE_AMP[min(t, len(RESCALE_AMP) - 1)]
+    return plant
+
+
+def _rescale_rows(cpu, w):
+    """Fraction of (row, head) pairs whose running tile max of S * c grows by
+    more than 8 at some tile (unmasked)."""
+    c = w.softmax_scale / np.log(2.0)
+    hits = total = 0
+    for b in range(w.batch):
+        q0, q1, k0, k1 = w.cu_q[b], w.cu_q[b + 1], w.cu_k[b], w.cu_k[b + 1]
+        if q1 == q0 or k1 - k0 <= 128:
+            continue
+        for h in range(w.num_heads):
+            s = (cpu.q[q0:q1, h].double() @ cpu.k[k0:k1, h].double().T).numpy() * c
+            m = np.maximum.accumulate(np.stack([s[:, t:t + 128].max(1) for t in range(0, k1 - k0, 128)], 1), 1)
+            hits += int((np.diff(m, axis=1) > 8).any(1).sum())
+            total += q1 - q0
+    return hits / max(total, 1)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fwd_rescale_path(causal):
+    """Scores that rise by more than 2^8 from one key tile to the next: every
+    such step has O rescaled in TMEM before the step's P V is added; O and LSE
+    match the oracle."""
+    w = W.custom("rising_scores", [300, 129, 600, 1], [640, 300, 1100, 513], 2, 128)
+    cpu = W.make_inputs(w, 5, with_dout=False)
+    _plant_rising_scores(w)(cpu)
+    if not causal:
+        assert _rescale_rows(cpu, w) > 0.9
+    dev = cpu.to(DEV)
+    out = W.output_like(w, "out", DEV, canary=12345.0)
+    lse = torch.full((w.num_heads, w.total_q), 777.0, dtype=torch.float32, device=DEV)
+    P.run_fwd(dev, out, lse, causal=causal)
+    torch.cuda.synchronize()
+    assert P.padding_untouched(out, w, 12345.0)
+    rows, heads = oracle.all_pairs(w.total_q, w.num_heads)
+    o_ref, lse_ref = P.oracle_problem(cpu, causal=causal).fwd(rows, heads)
+    o_gpu = P.gather(out.cpu(), rows, heads)
+    lse_gpu = lse.cpu().numpy()[heads, rows].astype(np.float64)
+    m = P.fwd_metrics(o_gpu, lse_gpu, o_ref, lse_ref)
+    print("rescale", causal, m)
+    # near one-hot rows: O is close to single V rows, |O| reaches 2 and more,
+    # where one bf16 ulp (>= 1.6e-2) is above 1e-2: one ulp from bf16(exact)
+    P.assert_fwd(m, allow_one_ulp_above=True, ulps=1)
+
+
 def test_fwd_segment_isolation_nan():
     """NaN in the rows of the segment after a ragged tail must not reach the
     tail's outputs (rows past a segment end are masked / cleared)."""
