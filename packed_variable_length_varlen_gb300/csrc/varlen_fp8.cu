@@ -27,7 +27,8 @@
 //     lazy rescaling) on the codes:
 //         S = Q8 K8^T          (tcgen05 kind::f8f6f4, E4M3 x E4M3 -> fp32)
 //         P = exp2(S * scale*log2e*qd*kd - m),  l += P   (fp32)
-//         O += e4m3(P) V8      (P written to shared memory as E4M3 codes)
+//         O += e4m3(P) V8      (P written into TMEM over S as E4M3 codes,
+//                               read from there as the A operand)
 //     and finally O * vd / l in bf16 and LSE = (m + log2 l) ln 2.  The row
 //     sum l uses the unrounded P.
 //
