@@ -10,7 +10,10 @@ oracle's FP8 reading:
   (computed by the oracle with |V| and unrounded P) plus the bf16 rounding of
   O; LSE within 1e-3 (P's rounding does not enter it);
 * against the fp64 oracle on the bf16 inputs, cosine >= 0.998 (the method's
-  own envelope)."""
+  own envelope);
+* at full size (the windowed workload, H=56), one head per segment: the
+  segment's amax and codes bit for bit, and O / LSE on 4096 sampled rows
+  spanning every segment."""
 import numpy as np
 import pytest
 import torch
@@ -156,6 +159,60 @@ def test_fp8_codes_every_bf16_value():
         cpu.v[r0:r1, 1] = blk
     _, _, amax, q8, k8, vt = _run(w, cpu, scale=1e-37)
     _check_codes(w, cpu, amax, q8, k8, vt)
+
+
+@pytest.mark.slow
+def test_fp8_windowed_full_size_sampled():
+    """The E4M3 forward on the windowed workload (8 segments, H=56, D=128, the
+    size the benchmark times).  Per segment b one head h_b: the oracle
+    quantises that (segment, head) block on its own (its descale depends on
+    nothing else), the block's amax and Q, K and transposed V codes must equal
+    the kernel's bit for bit, and 512 sampled rows of it (4096 in all) must
+    match the oracle's FP8 forward within the P-rounding bound, LSE within
+    1e-3, and the fp64 forward on the bf16 inputs with cosine >= 0.998."""
+    w = W.windowed()
+    H = w.num_heads
+    cpu = W.make_inputs(w, 0, with_dout=False)
+    out, lse, amax, q8, k8, vt = _run(w, cpu)
+    out_c, lse_c = out.cpu(), lse.cpu().numpy()
+    pb64 = P.oracle_problem(cpu)
+    rng = np.random.default_rng(7)
+    all_gpu, all_64 = [], []
+    for b in range(w.batch):
+        h = (5 + 7 * b) % H
+        q0, q1, k0, k1 = w.cu_q[b], w.cu_q[b + 1], w.cu_k[b], w.cu_k[b + 1]
+        blk = [t[r0:r1, h:h + 1] for t, r0, r1 in ((cpu.q, q0, q1), (cpu.k, k0, k1), (cpu.v, k0, k1))]
+        codes, desc = [], []
+        for i, x in enumerate(blk):
+            assert np.float32(amax[i][b * H + h]) == np.float32(x.float().abs().max()), (b, h, i)
+            c, d = oracle.quantize_e4m3(x, [0, x.shape[0]])
+            codes.append(c)
+            desc.append(d)
+        assert torch.equal(q8[q0:q1, h], codes[0][:, 0]), (b, h)
+        assert torch.equal(k8[k0:k1, h], codes[1][:, 0]), (b, h)
+        base = 128 * (b + -(-k0 // 128))
+        assert torch.equal(vt[h, :, base:base + (k1 - k0)], codes[2][:, 0].T), (b, h)
+        rows = np.sort(np.concatenate([1 + rng.choice(q1 - q0 - 2, 510, replace=False), [0, q1 - q0 - 1]]))
+        zeros = np.zeros(rows.size, dtype=np.int64)
+        pf = oracle.Fp8Problem(*codes, [0, q1 - q0], [0, k1 - k0], w.softmax_scale, *desc, quantize_p=True)
+        o_ref, l_ref = pf.fwd(rows, zeros)
+        pa = oracle.Fp8Problem(codes[0], codes[1], codes[2] & 0x7F, [0, q1 - q0], [0, k1 - k0], w.softmax_scale,
+                               *desc, quantize_p=False)
+        o_abs, _ = pa.fwd(rows, zeros)
+        grow, gh = q0 + rows, np.full(rows.size, h)
+        o_gpu = P.gather(out_c, grow, gh)
+        l_gpu = lse_c[gh, grow].astype(np.float64)
+        excess = np.abs(o_gpu - o_ref) - (2.0 ** -3 * o_abs + 2.0 ** -8 * np.abs(o_ref) + 1e-3)
+        assert (excess <= 0).all(), (b, h, excess.max())
+        assert np.abs(l_gpu - l_ref).max() <= 1e-3, (b, h)
+        o64 = P.oracle_rows(pb64, w, grow, gh)[0]
+        all_gpu.append(o_gpu)
+        all_64.append(o64)
+    o_gpu, o64 = np.concatenate(all_gpu), np.concatenate(all_64)
+    assert o_gpu.shape[0] >= 4096
+    cos = float((o_gpu * o64).sum() / np.linalg.norm(o_gpu) / np.linalg.norm(o64))
+    print("fp8 full size: %d rows, cosine vs fp64 %.6f" % (o_gpu.shape[0], cos))
+    assert cos >= 0.998
 
 
 def test_fp8_python_wrapper_matches_raw_call():
