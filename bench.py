@@ -491,14 +491,28 @@ def ours(args, w, ws, rank, local):
                 h_dk.copy_(gk, non_blocking=True)
                 h_dv.copy_(gv, non_blocking=True)
 
-        def e2e_run(n, start, end):
+        def e2e_run(n, start, end, spans=None):
+            """n pipelined steps between start and end; with `spans`, timing
+            events around every copy and every step's kernels are appended to
+            it as (kind, begin, end)."""
             ev = lambda: torch.cuda.Event()
             in_done, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+
+            def span(kind, s, fn):
+                if spans is None:
+                    fn()
+                    return
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(s)
+                fn()
+                b.record(s)
+                spans.append((kind, a, b))
+
             start.record(stream)
             copy_in.wait_event(start)
             copy_out.wait_event(start)
             with torch.cuda.stream(copy_in):
-                h2d(0)
+                span("h2d", copy_in, lambda: h2d(0))
                 in_done[0].record(copy_in)
             for i in range(n):
                 b = i % 2
@@ -506,16 +520,16 @@ def ours(args, w, ws, rank, local):
                     with torch.cuda.stream(copy_in):
                         if i >= 1:
                             copy_in.wait_event(comp_done[(i + 1) % 2])
-                        h2d(i + 1)
+                        span("h2d", copy_in, lambda: h2d(i + 1))
                         in_done[(i + 1) % 2].record(copy_in)
                 stream.wait_event(in_done[b])
                 if i >= 2:
                     stream.wait_event(out_done[b])  # step i-2's results have left this output set
-                compute(i)
+                span("kernels", stream, lambda: compute(i))
                 comp_done[b].record(stream)
                 with torch.cuda.stream(copy_out):
                     copy_out.wait_event(comp_done[b])
-                    d2h(i)
+                    span("d2h", copy_out, lambda: d2h(i))
                     out_done[b].record(copy_out)
             stream.wait_event(out_done[(n - 1) % 2])
             stream.wait_event(in_done[(n - 1) % 2])
@@ -529,9 +543,14 @@ def ours(args, w, ws, rank, local):
         torch.cuda.synchronize()
         _barrier(ws)
         ke = K  # the same K steps as the device-timed value; the first copy-in and last copy-out are not hidden
-        e2e_run(ke, a, b_)
+        spans = []
+        e2e_run(ke, a, b_, spans)
         torch.cuda.synchronize()
         ms_e2e = _max_over_ranks(a.elapsed_time(b_), ws)
+        # what each copy and each step's kernels took inside the pipeline (a
+        # box whose copies slow the kernels, or the other way round, shows here)
+        in_pipe = {k: statistics.mean(x.elapsed_time(y) for kk, x, y in spans if kk == k)
+                   for k in ("h2d", "kernels", "d2h")}
         # What the copies alone cost per step at the measured concurrent
         # rate: with the copies overlapped, a step takes about the larger of
         # this and the kernels' time.
@@ -542,6 +561,7 @@ def ours(args, w, ws, rank, local):
                "pipeline": "step i+1 inputs in and step i-1 results out on two copy streams during step i",
                "copy_rates": rates, "copy_ms_per_step_at_concurrent_rate": copy_ms,
                "kernel_ms_per_step": kern_ms, "exposed_ms_per_step": ms_e2e / ke - kern_ms,
+               "in_pipeline_ms": in_pipe,
                "bound": "copies" if copy_ms > kern_ms else "kernels",
                "host_cpus": bound[1] if bound else "topology not readable"}
         if bound:
