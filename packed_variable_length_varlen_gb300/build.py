@@ -55,8 +55,9 @@ def up_to_date(lib: str | None = None) -> bool:
     stamp = lib + ".arch"
     if not (os.path.exists(lib) and os.path.exists(stamp)):
         return False
-    if open(stamp).read().strip() != platform.machine():
-        return False
+    with open(stamp) as f:
+        if f.read().strip() != platform.machine():
+            return False
     t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 

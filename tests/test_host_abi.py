@@ -5,6 +5,7 @@ matches the page values.  Pointers passed here are never dereferenced: every
 call either fails validation or stops at the device query (no GPU here)."""
 import json
 import os
+import pathlib
 import re
 
 import numpy as np
@@ -26,7 +27,7 @@ def va():
 
 
 def _declared():
-    src = open(HEADER).read()
+    src = pathlib.Path(HEADER).read_text()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(varlen_attn_\w+)\s*\(", src)))
 
@@ -47,7 +48,7 @@ def test_status_strings(va):
 
 
 def test_tile_count_page_values(va):
-    g = json.load(open(GOLDEN))["windowed_tile_count"]
+    g = json.loads(pathlib.Path(GOLDEN).read_text())["windowed_tile_count"]
     cu = g["cu_seqlens_q"]
     assert va.varlen_attn_tile_count(cu, len(cu) - 1, cu[-1], g["num_heads"], g["tile_m"]) == g["valid_tiles"]
 
@@ -131,7 +132,7 @@ def test_large_strides_pass_validation(va):
 
 
 def test_int64_offsets_page_value():
-    g = json.load(open(GOLDEN))["dout_offset_wrap"]
+    g = json.loads(pathlib.Path(GOLDEN).read_text())["dout_offset_wrap"]
     # the library's offsets are int64 products of row index and row stride
     off = np.int64(g["coord"]) * np.int64(g["dout_stride"][0])
     assert int(off) == g["true_offset"] and int(off) != g["off_signed_i32"]
@@ -330,7 +331,7 @@ def test_noalloc_scratch_size_matches_header(va):
     """The scratch limit the binding reports comes from the library and
     equals the header's VARLEN_NOALLOC_SCRATCH_BYTES."""
     m = re.search(r"#define\s+VARLEN_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*\*\s*(\d+)u\s*\*\s*(\d+)u\)",
-                  open(HEADER).read())
+                  pathlib.Path(HEADER).read_text())
     assert m, "VARLEN_NOALLOC_SCRATCH_BYTES not found in the header"
     want = int(m.group(1)) * int(m.group(2)) * int(m.group(3))
     assert va.NOALLOC_SCRATCH_BYTES == want == va.LIB.varlen_attn_bwd_noalloc_scratch_bytes()

@@ -4,6 +4,7 @@ definition, the quantised forward against the fp64 oracle on the dequantised
 inputs, closed forms (one key, two keys with P rounded by torch), the bound
 that rounding P may move O by, and planted mistakes."""
 import math
+import pathlib
 import subprocess
 
 import numpy as np
@@ -160,7 +161,7 @@ MUTANTS = [
 
 @pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
 def test_fp8_planted_mistake_is_caught(tmp_path, name, old, new):
-    src = open(oracle._SRC).read()
+    src = pathlib.Path(oracle._SRC).read_text()
     assert src.count(old) >= 1, "mutation anchor missing: %s" % name
     mut = tmp_path / "mutant.c"
     mut.write_text(src.replace(old, new))

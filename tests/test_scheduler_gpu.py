@@ -6,6 +6,7 @@ valid-tile count printed on the "[FA4][SM120] ... >=4 varlen segments" issue
 (section "Interpretation")."""
 import json
 import os
+import pathlib
 
 import numpy as np
 import pytest
@@ -61,7 +62,7 @@ def _run(cu, H, tile, grid, guard=64):
 
 
 def test_windowed_tile_count_pin():
-    g = json.load(open(GOLDEN))["windowed_tile_count"]
+    g = json.loads(pathlib.Path(GOLDEN).read_text())["windowed_tile_count"]
     _run(g["cu_seqlens_q"], g["num_heads"], g["tile_m"], 152)
 
 
