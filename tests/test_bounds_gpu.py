@@ -1,8 +1,8 @@
 """The bounds-checking build (compiled with -DVARLEN_DEBUG_BOUNDS): every
 plain global load and store of every kernel checks the bytes it touches
 against its operand's extent and records VARLEN_ERR_DEVICE_BOUNDS instead of
-accessing outside.  compute-sanitizer is closed on this machine; this build is
-the out-of-bounds evidence in its place.  Ragged, padded, strided-dout,
+accessing outside; it is the out-of-bounds check that stands in for a
+sanitizer's memory check.  Ragged, padded, strided-dout,
 causal, windowed, deterministic and E4M3 calls run in a child process on
 that build and must report VARLEN_OK and give the normal build's results
 (the same bits, except the atomic path's dQ, whose additions may come in
