@@ -141,16 +141,21 @@ def _every_value_rows(amax_bits, rows):
     return out.view(rows, 128)
 
 
-def test_fp8_codes_every_bf16_value():
+# 32 more maxima drawn over the whole positive finite bf16 range (seeded)
+SPREAD_AMAX = sorted(int(a) for a in np.random.default_rng(11).integers(1, 0x7F80, 32))
+
+
+@pytest.mark.parametrize("maxima", [ALL_VALUE_AMAX, SPREAD_AMAX], ids=["edges", "spread"])
+def test_fp8_codes_every_bf16_value(maxima):
     """Q and V segments whose heads hold every finite bf16 value up to their
     maximum, for maxima from a subnormal to the largest finite bf16 (descales
-    on both sides of 2^-100 among them): every code equals the oracle's IEEE
-    fp32 division and conversion.  K is ordinary data; the softmax scale is
-    small enough that S stays finite."""
-    lens = [-(-2 * (a + 1) // 128) for a in ALL_VALUE_AMAX]
+    on both sides of 2^-100 among them, and 32 spread over the range): every
+    code equals the oracle's IEEE fp32 division and conversion.  K is
+    ordinary data; the softmax scale is small enough that S stays finite."""
+    lens = [-(-2 * (a + 1) // 128) for a in maxima]
     w = W.custom("fp8_every_value", lens, lens, 2, 128)
     cpu = W.make_inputs(w, 3, with_dout=False)
-    for b, a in enumerate(ALL_VALUE_AMAX):
+    for b, a in enumerate(maxima):
         r0, r1 = w.cu_q[b], w.cu_q[b + 1]
         blk = _every_value_rows(a, r1 - r0)
         cpu.q[r0:r1, 0] = blk
