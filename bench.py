@@ -685,6 +685,31 @@ def fp8_forward(args, w, ws, rank, local):
               flush=True)
 
 
+def mma_rates(args):
+    """Cycles per tcgen05 MMA (M = 128, K = 16, bf16 -> fp32) issued by one
+    thread, for N = 64 / 128 / 256 and the three issue forms of
+    varlen_attn_debug_mma_cycles (best of three runs of 4096 MMAs each)."""
+    from packed_variable_length_varlen_gb300 import varlen_attn as va
+    dev = torch.device("cuda", 0)
+    cyc = torch.zeros(1, dtype=torch.int64, device=dev)
+    n = 4096
+    res = {}
+    for mode, name in ((0, "smem A, low-word descriptors"), (1, "TMEM A"), (2, "smem A, descriptors rebuilt per MMA")):
+        for n_cols in (64, 128, 256):
+            best = None
+            for _ in range(3):
+                st = va.varlen_attn_debug_mma_cycles(n, n_cols, mode, cyc)
+                assert st == 0, va.varlen_attn_status_string(st)
+                torch.cuda.synchronize()
+                assert va.varlen_attn_get_device_status() == 0
+                v = int(cyc.item()) / n
+                best = v if best is None else min(best, v)
+            res["%s, N=%d" % (name, n_cols)] = {"cycles_per_mma": round(best, 2),
+                                                "flops_per_cycle": round(2 * 128 * n_cols * 16 / best, 1)}
+    print(json.dumps({"probe": "tcgen05.mma issue rate, one CTA, one issuing thread", "n_mma": n,
+                      "shape": "M=128, K=16, bf16 x bf16 -> fp32", "results": res}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -702,6 +727,8 @@ def main():
                     help="time the deterministic backward (dQ without atomics, a second q-major kernel)")
     ap.add_argument("--dense", action="store_true",
                     help="drive the dense batched entry points (needs equal segment lengths, e.g. --workload dense)")
+    ap.add_argument("--mma-rates", action="store_true",
+                    help="print cycles per tcgen05 MMA for N = 64/128/256 and three issue forms (one CTA)")
     ap.add_argument("--fp8", action="store_true",
                     help="time the E4M3 forward alone (head size 128, no mask; quantisation included)")
     ap.add_argument("--shard", choices=["replicas", "heads"], default="replicas",
@@ -721,6 +748,10 @@ def main():
         reference_arm(args, w, ws, rank)
         return
     ws, rank, local = _dist()
+    if args.mma_rates:
+        if rank == 0:
+            mma_rates(args)
+        return
     if args.fp8:
         fp8_forward(args, w, ws, rank, local)
     else:

@@ -342,6 +342,22 @@ int varlen_attn_debug_schedule(const int32_t* cu_seqlens, int32_t batch, int32_t
 int varlen_attn_selftest_wait_timeout(uint64_t budget_ns, void* stream);
 
 /*
+ * tcgen05 issue-rate probe (the measurements behind the kernels' MMA shapes
+ * and their single issuing thread): one CTA, one thread issues n_mma MMAs of
+ * M = 128, N = n_cols, K = 16 (bf16 x bf16 -> fp32, zero operands) into one
+ * TMEM accumulator and writes to *cycles (a device pointer, 8 bytes) the
+ * clock64 cycles from the first issue to the completion of the last.
+ * mode 0: both operands from shared memory, descriptors kept as 32-bit low
+ * words advanced by an immediate; 1: A from TMEM; 2: as 0, with both 64-bit
+ * descriptors rebuilt from the shared-memory address for every MMA.
+ * n_mma a multiple of 4 in [4, 2^20], n_cols 64, 128 or 256, else
+ * VARLEN_ERR_SHAPE; a completion wait that gives up records
+ * VARLEN_ERR_TIMEOUT (varlen_attn_get_device_status).
+ */
+int varlen_attn_debug_mma_cycles(int32_t n_mma, int32_t n_cols, int32_t mode, unsigned long long* cycles,
+                                 void* stream);
+
+/*
  * Profiling hook: with count == 4, every later varlen_attn_bwd call records
  * events[0] before its preprocess kernel, events[1] after it, events[2] after
  * the main kernel and events[3] after the dQ conversion, on the call's

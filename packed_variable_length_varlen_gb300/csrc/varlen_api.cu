@@ -795,6 +795,19 @@ extern "C" int varlen_attn_selftest_wait_timeout(uint64_t budget_ns, void* strea
   return e == cudaSuccess ? VARLEN_OK : VARLEN_ERR_CUDA;
 }
 
+extern "C" int varlen_attn_debug_mma_cycles(int32_t n_mma, int32_t n_cols, int32_t mode,
+                                            unsigned long long* cycles, void* stream) {
+  if (cycles == nullptr) return VARLEN_ERR_NULL;
+  if (n_mma < 4 || n_mma > (1 << 20) || n_mma % 4 != 0) return VARLEN_ERR_SHAPE;
+  if (n_cols != 64 && n_cols != 128 && n_cols != 256) return VARLEN_ERR_SHAPE;
+  if (mode < 0 || mode > 2) return VARLEN_ERR_SHAPE;
+  DeviceInfo dev;
+  int st = device_info(&dev);
+  if (st != VARLEN_OK) return st;
+  cudaError_t e = launch_debug_mma_rate(n_mma, n_cols, mode, cycles, dev.err, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? VARLEN_OK : cuda_fail(e);
+}
+
 extern "C" int varlen_attn_debug_set_phase_events(void* const* events, int count) {
   if (count != 0 && count != 4) return VARLEN_ERR_SHAPE;
   if (count == 4 && events == nullptr) return VARLEN_ERR_NULL;

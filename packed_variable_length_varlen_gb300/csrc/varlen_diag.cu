@@ -1,7 +1,7 @@
 // varlen_diag.cu -- diagnostic kernels: the tile scheduler run on its own
 // (so tests can check that every tile is visited exactly once and that no
-// cu_seqlens entry past `batch` is read), and a failure-detection self test
-// whose bounded wait is never satisfied.
+// cu_seqlens entry past `batch` is read), a failure-detection self test
+// whose bounded wait is never satisfied, and a tcgen05 issue-rate probe.
 #include "sm103_ptx.cuh"
 #include "varlen_internal.h"
 #include "varlen_sched.cuh"
@@ -57,6 +57,79 @@ __global__ void selftest_timeout_kernel(uint64_t budget_ns, unsigned int* err) {
 
 cudaError_t launch_selftest_timeout(uint64_t budget_ns, unsigned int* err, cudaStream_t stream) {
   selftest_timeout_kernel<<<1, 32, 0, stream>>>(budget_ns, err);
+  return cudaGetLastError();
+}
+
+// tcgen05 issue-rate probe: one thread issues n_mma MMAs of M = 128, N =
+// n_cols, K = 16 (bf16 x bf16 -> fp32) into one TMEM accumulator, on zero
+// operands, and the kernel reports the issuing thread's clock64 cycles from
+// the first issue to the completion of the last (tcgen05.commit on an
+// mbarrier, bounded wait).  mode 0: A and B from shared memory, descriptors
+// as the kernels keep them (a constant high word, the low word advanced by
+// an immediate per k-step); mode 1: A from TMEM; mode 2: as mode 0, but each
+// MMA's two 64-bit descriptors are rebuilt from the shared-memory address.
+constexpr int kMmaProbeA = 16384, kMmaProbeB = 32768;  // A: 128 x 64 bf16; B: 256 x 64 bf16
+constexpr int kMmaProbeSmem = 1024 + kMmaProbeA + kMmaProbeB;
+
+__global__ void __launch_bounds__(128, 1) mma_rate_kernel(int32_t n_mma, int32_t n_cols, int32_t mode,
+                                                          unsigned long long* cycles, unsigned int* err) {
+  extern __shared__ __align__(1024) uint8_t probe_smem[];
+  __shared__ uint64_t done;
+  __shared__ uint32_t tbase;
+  __shared__ int abort_flag;
+  uint8_t* base = probe_smem + ((1024u - (smem_addr(probe_smem) & 1023u)) & 1023u);  // 1024-byte aligned
+  uint8_t* a_s = base;
+  uint8_t* b_s = base + kMmaProbeA;
+  for (int i = threadIdx.x; i < (kMmaProbeA + kMmaProbeB) / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(base)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
+  if (threadIdx.x == 0) {
+    mbar_init(&done, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (threadIdx.x < 32) tmem_alloc(&tbase, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tbase;
+  if (threadIdx.x == 0) {
+    const uint32_t idesc = idesc_bf16_f32(128, n_cols, false, false);
+    const uint32_t alo = sw128_desc_lo(smem_addr(a_s), 16), blo = sw128_desc_lo(smem_addr(b_s), 16);
+    const long long t0 = clock64();
+    for (int32_t i = 0; i < n_mma; i += 4) {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {  // the four 16-wide k-steps of a 64-column chunk
+        const uint32_t acc = (i + kk) > 0 ? 1u : 0u;
+        if (mode == 1) {
+          mma_ts_lo(tmem, tmem + 256 + kk * 8, blo + ((kk * 32) >> 4), idesc, acc);
+        } else if (mode == 2) {
+          const uint64_t ad = sw128_desc(smem_addr(a_s) + kk * 32, 16, 1024);
+          const uint64_t bd = sw128_desc(smem_addr(b_s) + kk * 32, 16, 1024);
+          mma_ss(tmem, ad, bd, idesc, acc);
+        } else {
+          mma_ss_lo(tmem, alo + ((kk * 32) >> 4), blo + ((kk * 32) >> 4), idesc, acc);
+        }
+      }
+    }
+    mma_commit(&done);
+    mbar_wait(&done, 0, &abort_flag);
+    cycles[0] = (unsigned long long)(clock64() - t0);
+    if (abort_flag) record_error(err, kErrTimeout);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+cudaError_t launch_debug_mma_rate(int32_t n_mma, int32_t n_cols, int32_t mode, unsigned long long* cycles,
+                                  unsigned int* err, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(mma_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaProbeSmem);
+  if (e != cudaSuccess) return e;
+  mma_rate_kernel<<<1, 128, kMmaProbeSmem, stream>>>(n_mma, n_cols, mode, cycles, err);
   return cudaGetLastError();
 }
 

@@ -257,4 +257,7 @@ cudaError_t launch_debug_schedule(const int32_t* cu, int32_t batch, int32_t tota
 
 cudaError_t launch_selftest_timeout(uint64_t budget_ns, unsigned int* err, cudaStream_t stream);
 
+cudaError_t launch_debug_mma_rate(int32_t n_mma, int32_t n_cols, int32_t mode, unsigned long long* cycles,
+                                  unsigned int* err, cudaStream_t stream);
+
 }  // namespace varlen

@@ -118,6 +118,8 @@ def _load() -> ctypes.CDLL:
     lib.varlen_attn_debug_schedule.argtypes = [vp, i32, i32, i32, i32, i32, vp, i64, vp]
     lib.varlen_attn_selftest_wait_timeout.restype = ctypes.c_int
     lib.varlen_attn_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+    lib.varlen_attn_debug_mma_cycles.restype = ctypes.c_int
+    lib.varlen_attn_debug_mma_cycles.argtypes = [i32, i32, i32, vp, vp]
     lib.varlen_attn_debug_set_phase_events.restype = ctypes.c_int
     lib.varlen_attn_debug_set_phase_events.argtypes = [vp, ctypes.c_int]
     lib.varlen_attn_num_sms.restype = ctypes.c_int
@@ -137,7 +139,7 @@ EXPORTED = ("varlen_attn_fwd", "varlen_attn_bwd_workspace_size", "varlen_attn_bw
             "varlen_attn_bwd_window", "varlen_attn_bwd_deterministic", "varlen_attn_fwd_fp8_workspace_size",
             "varlen_attn_fwd_fp8_workspace_layout", "varlen_attn_fwd_fp8", "varlen_attn_bwd_noalloc_scratch_bytes",
             "varlen_attn_debug_noalloc_scratch", "varlen_attn_bounds_checked", "varlen_attn_debug_set_span_slack",
-            "varlen_attn_debug_skip_load")
+            "varlen_attn_debug_skip_load", "varlen_attn_debug_mma_cycles")
 
 # Size of the fixed device array varlen_attn_bwd_noalloc uses as scratch, as
 # compiled into the library.
@@ -355,6 +357,11 @@ def varlen_attn_debug_schedule(cu_seqlens, batch, total, num_heads, tile, grid, 
 
 def varlen_attn_selftest_wait_timeout(budget_ns: int, stream=None) -> int:
     return LIB.varlen_attn_selftest_wait_timeout(budget_ns, _stream(stream))
+
+
+def varlen_attn_debug_mma_cycles(n_mma, n_cols, mode, cycles, stream=None) -> int:
+    """cycles: a CUDA int64 tensor (one element) that receives the count."""
+    return LIB.varlen_attn_debug_mma_cycles(n_mma, n_cols, mode, _ptr(cycles), _stream(stream))
 
 
 _PHASE_KEEP = None

@@ -3,6 +3,7 @@ every function include/varlen_attn.h declares, validates arguments with the
 documented status codes before touching a device, and its host tile count
 matches the page values.  Pointers passed here are never dereferenced: every
 call either fails validation or stops at the device query (no GPU here)."""
+import ctypes
 import json
 import os
 import pathlib
@@ -381,3 +382,13 @@ def test_bounds_build_is_separate():
     from packed_variable_length_varlen_gb300 import build
     assert build.BOUNDS_LIB != build.LIB
     assert os.path.dirname(build.BOUNDS_LIB).endswith(os.path.join("_build", "bounds"))
+
+
+def test_mma_probe_argument_checks():
+    """The issue-rate probe rejects its bad arguments before touching a device."""
+    from packed_variable_length_varlen_gb300 import varlen_attn as va
+    fake = ctypes.c_void_p(16)
+    assert va.LIB.varlen_attn_debug_mma_cycles(256, 128, 0, None, None) == va.VARLEN_ERR_NULL
+    for n_mma, n_cols, mode in ((0, 128, 0), (6, 128, 0), (1 << 21, 128, 0), (256, 96, 0), (256, 128, 3),
+                                (256, 128, -1)):
+        assert va.LIB.varlen_attn_debug_mma_cycles(n_mma, n_cols, mode, fake, None) == va.VARLEN_ERR_SHAPE
