@@ -694,8 +694,9 @@ def mma_rates(args):
     cyc = torch.zeros(1, dtype=torch.int64, device=dev)
     n = 4096
     res = {}
-    for mode, name in ((0, "smem A, low-word descriptors"), (1, "TMEM A"), (2, "smem A, descriptors rebuilt per MMA")):
-        for n_cols in (64, 128, 256):
+    for mode, name in ((0, "smem A, low-word descriptors"), (1, "TMEM A"), (2, "smem A, descriptors rebuilt per MMA"),
+                       (5, "TMEM A, B MN-major"), (6, "TMEM A, four warps loading TMEM meanwhile")):
+        for n_cols in ((64, 128) if mode == 5 else (128,) if mode == 6 else (64, 128, 256)):
             best = None
             for _ in range(3):
                 st = va.varlen_attn_debug_mma_cycles(n, n_cols, mode, cyc)
@@ -706,8 +707,20 @@ def mma_rates(args):
                 best = v if best is None else min(best, v)
             res["%s, N=%d" % (name, n_cols)] = {"cycles_per_mma": round(best, 2),
                                                 "flops_per_cycle": round(2 * 128 * n_cols * 16 / best, 1)}
-    print(json.dumps({"probe": "tcgen05.mma issue rate, one CTA, one issuing thread", "n_mma": n,
-                      "shape": "M=128, K=16, bf16 x bf16 -> fp32", "results": res}), flush=True)
+    for mode, name in ((3, "tcgen05.ld 32x32b.x32"), (4, "tcgen05.st 32x32b.x32")):
+        best = None
+        for _ in range(3):
+            st = va.varlen_attn_debug_mma_cycles(n, 128, mode, cyc)
+            assert st == 0, va.varlen_attn_status_string(st)
+            torch.cuda.synchronize()
+            assert va.varlen_attn_get_device_status() == 0
+            v = int(cyc.item()) / n
+            best = v if best is None else min(best, v)
+        # four warps move 4 KB each per iteration
+        res["%s, 4 warps, wait after each" % name] = {"cycles_per_iteration": round(best, 2),
+                                                       "bytes_per_cycle": round(4 * 4096 / best, 1)}
+    print(json.dumps({"probe": "tcgen05.mma issue rate, one CTA, one issuing thread; TMEM load/store rate",
+                      "n_mma": n, "shape": "M=128, K=16, bf16 x bf16 -> fp32", "results": res}), flush=True)
 
 
 def main():

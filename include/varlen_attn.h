@@ -350,6 +350,12 @@ int varlen_attn_selftest_wait_timeout(uint64_t budget_ns, void* stream);
  * mode 0: both operands from shared memory, descriptors kept as 32-bit low
  * words advanced by an immediate; 1: A from TMEM; 2: as 0, with both 64-bit
  * descriptors rebuilt from the shared-memory address for every MMA.
+ * Modes 3 and 4 time TMEM <-> register traffic instead: each of four warps
+ * loads (3) or stores (4) its 32 lanes x 32 columns (4 KB) n_mma times,
+ * waiting for each; *cycles spans all four warps' loops.  Mode 5: as 1 with
+ * B MN-major (the V operand layout of O += P V), n_cols 64 or 128.  Mode
+ * 6: as 1 while four more warps keep loading TMEM columns the MMAs do not
+ * use (as a softmax does beside the tensor core).
  * n_mma a multiple of 4 in [4, 2^20], n_cols 64, 128 or 256, else
  * VARLEN_ERR_SHAPE; a completion wait that gives up records
  * VARLEN_ERR_TIMEOUT (varlen_attn_get_device_status).
