@@ -281,14 +281,24 @@ __global__ void __launch_bounds__(384, 1)
       };
       // dQ += dS_gg (bf16 in TMEM: kv columns [0, 64) at the buffer's columns
       // [0, 32), [64, 128) at [64, 96)) K_gg (MN-major B) over nk kv k-steps
+      // (a whole tile takes a loop without a branch: a branch per MMA slows
+      // the single issuing thread enough to leave the tensor core waiting)
       auto issue_dq = [&](uint32_t gg, int nk, bool acc0) {
         const uint32_t so = ((gg % C::NK) * C::TILE) >> 4;
         const uint32_t sbuf = tmem + C::S_COL + (gg & 1) * 128;
+        const uint32_t a0 = acc0 ? 1u : 0u;
+        if (nk == kTileN / 16) {
 #pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk)
-          if (kk < nk)
+          for (int kk = 0; kk < kTileN / 16; ++kk)
             mma_ts_lo(tmem + C::DQ_COL, sbuf + (kk >> 2) * 64 + (kk & 3) * 8, kBm + so + ((kk * 2048) >> 4), kIdQ,
-                      (acc0 || kk > 0) ? 1u : 0u);
+                      kk > 0 ? 1u : a0);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < kTileN / 16; ++kk)
+            if (kk < nk)
+              mma_ts_lo(tmem + C::DQ_COL, sbuf + (kk >> 2) * 64 + (kk & 3) * 8, kBm + so + ((kk * 2048) >> 4),
+                        kIdQ, kk > 0 ? 1u : a0);
+        }
         mma_commit(&bar.k_empty[gg % C::NK]);
       };
       auto v_ready = [&](uint32_t gg) -> bool {
