@@ -695,8 +695,9 @@ def mma_rates(args):
     n = 4096
     res = {}
     for mode, name in ((0, "smem A, low-word descriptors"), (1, "TMEM A"), (2, "smem A, descriptors rebuilt per MMA"),
-                       (5, "TMEM A, B MN-major"), (6, "TMEM A, four warps loading TMEM meanwhile")):
-        for n_cols in ((64, 128) if mode == 5 else (128,) if mode == 6 else (64, 128, 256)):
+                       (5, "TMEM A, B MN-major"), (6, "TMEM A, four warps loading TMEM meanwhile"),
+                       (7, "TMEM A, four warps storing to shared memory meanwhile")):
+        for n_cols in ((64, 128) if mode == 5 else (128,) if mode >= 6 else (64, 128, 256)):
             best = None
             for _ in range(3):
                 st = va.varlen_attn_debug_mma_cycles(n, n_cols, mode, cyc)

@@ -355,7 +355,8 @@ int varlen_attn_selftest_wait_timeout(uint64_t budget_ns, void* stream);
  * waiting for each; *cycles spans all four warps' loops.  Mode 5: as 1 with
  * B MN-major (the V operand layout of O += P V), n_cols 64 or 128.  Mode
  * 6: as 1 while four more warps keep loading TMEM columns the MMAs do not
- * use (as a softmax does beside the tensor core).
+ * use (as a softmax does beside the tensor core); 7: as 1 while four more
+ * warps keep storing into a separate 16 KB of shared memory.
  * n_mma a multiple of 4 in [4, 2^20], n_cols 64, 128 or 256, else
  * VARLEN_ERR_SHAPE; a completion wait that gives up records
  * VARLEN_ERR_TIMEOUT (varlen_attn_get_device_status).

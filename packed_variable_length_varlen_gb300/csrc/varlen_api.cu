@@ -800,7 +800,7 @@ extern "C" int varlen_attn_debug_mma_cycles(int32_t n_mma, int32_t n_cols, int32
   if (cycles == nullptr) return VARLEN_ERR_NULL;
   if (n_mma < 4 || n_mma > (1 << 20) || n_mma % 4 != 0) return VARLEN_ERR_SHAPE;
   if (n_cols != 64 && n_cols != 128 && n_cols != 256) return VARLEN_ERR_SHAPE;
-  if (mode < 0 || mode > 6 || (mode == 5 && n_cols > 128)) return VARLEN_ERR_SHAPE;
+  if (mode < 0 || mode > 7 || (mode == 5 && n_cols > 128)) return VARLEN_ERR_SHAPE;
   DeviceInfo dev;
   int st = device_info(&dev);
   if (st != VARLEN_OK) return st;

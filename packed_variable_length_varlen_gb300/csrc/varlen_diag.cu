@@ -75,9 +75,13 @@ cudaError_t launch_selftest_timeout(uint64_t budget_ns, unsigned int* err, cudaS
 // one per K index, 64-element N blocks 16 KB apart; n_cols at most 128).
 // Mode 6: as mode 1 while four more warps keep loading TMEM columns the
 // MMAs do not touch (tcgen05.ld 32 lanes x 32 columns and a wait, over and
-// over), as a softmax does beside the tensor core.
+// over), as a softmax does beside the tensor core.  Mode 7: as mode 1 while
+// four more warps keep storing 16-byte words into a separate 16 KB of
+// shared memory (shared-memory writes beside the operand reads, as K/V tile
+// loads arrive during the products).
 constexpr int kMmaProbeA = 16384, kMmaProbeB = 32768;  // A: 128 x 64 bf16; B: 256 x 64 bf16
-constexpr int kMmaProbeSmem = 1024 + kMmaProbeA + kMmaProbeB;
+constexpr int kMmaProbeW = 16384;  // mode 7's write target
+constexpr int kMmaProbeSmem = 1024 + kMmaProbeA + kMmaProbeB + kMmaProbeW;
 
 template <int MODE>
 __global__ void __launch_bounds__(256, 1) mma_rate_kernel(int32_t n_mma, int32_t n_cols,
@@ -105,7 +109,16 @@ __global__ void __launch_bounds__(256, 1) mma_rate_kernel(int32_t n_mma, int32_t
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tbase;
-  if (threadIdx.x >= 128) {  // mode 6: TMEM loads beside the MMAs, until they complete
+  if (threadIdx.x >= 128) {  // modes 6, 7: TMEM loads / shared-memory stores beside the MMAs, until they complete
+    if constexpr (mode == 7) {
+      uint4* wbuf = reinterpret_cast<uint4*>(base + kMmaProbeA + kMmaProbeB);
+      const int t = threadIdx.x - 128;
+      uint4 v = make_uint4(t, 1, 2, 3);
+      for (int32_t i = 0; i < 256 * n_mma && !*reinterpret_cast<volatile int*>(&stop); ++i) {
+        wbuf[(t + 128 * (i & 7)) & (kMmaProbeW / 16 - 1)] = v;
+        v.x += 1;
+      }
+    }
     if constexpr (mode == 6) {
       const uint32_t lane_off = (uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16;
       uint32_t r[32];
@@ -143,7 +156,7 @@ __global__ void __launch_bounds__(256, 1) mma_rate_kernel(int32_t n_mma, int32_t
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {  // the four 16-wide k-steps of a 64-column chunk
         const uint32_t acc = (i + kk) > 0 ? 1u : 0u;
-        if constexpr (mode == 1 || mode == 6) {
+        if constexpr (mode == 1 || mode == 6 || mode == 7) {
           mma_ts_lo(tmem, tmem + 256 + kk * 8, blo + ((kk * 32) >> 4), idesc, acc);
         } else if constexpr (mode == 5) {
           mma_ts_lo(tmem, tmem + 256 + kk * 8, blo + ((kk * 2048) >> 4), idesc, acc);
@@ -176,7 +189,7 @@ static cudaError_t launch_mma_rate(int32_t n_mma, int32_t n_cols, unsigned long 
   cudaError_t e =
       cudaFuncSetAttribute(mma_rate_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaProbeSmem);
   if (e != cudaSuccess) return e;
-  mma_rate_kernel<MODE><<<1, MODE == 6 ? 256 : 128, kMmaProbeSmem, stream>>>(n_mma, n_cols, cycles, err);
+  mma_rate_kernel<MODE><<<1, MODE >= 6 ? 256 : 128, kMmaProbeSmem, stream>>>(n_mma, n_cols, cycles, err);
   return cudaGetLastError();
 }
 
@@ -190,6 +203,7 @@ cudaError_t launch_debug_mma_rate(int32_t n_mma, int32_t n_cols, int32_t mode, u
     case 4: return launch_mma_rate<4>(n_mma, n_cols, cycles, err, stream);
     case 5: return launch_mma_rate<5>(n_mma, n_cols, cycles, err, stream);
     case 6: return launch_mma_rate<6>(n_mma, n_cols, cycles, err, stream);
+    case 7: return launch_mma_rate<7>(n_mma, n_cols, cycles, err, stream);
     default: return cudaErrorInvalidValue;
   }
 }

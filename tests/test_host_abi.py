@@ -389,6 +389,6 @@ def test_mma_probe_argument_checks():
     from packed_variable_length_varlen_gb300 import varlen_attn as va
     fake = ctypes.c_void_p(16)
     assert va.LIB.varlen_attn_debug_mma_cycles(256, 128, 0, None, None) == va.VARLEN_ERR_NULL
-    for n_mma, n_cols, mode in ((0, 128, 0), (6, 128, 0), (1 << 21, 128, 0), (256, 96, 0), (256, 128, 7), (256, 256, 5),
+    for n_mma, n_cols, mode in ((0, 128, 0), (6, 128, 0), (1 << 21, 128, 0), (256, 96, 0), (256, 128, 8), (256, 256, 5),
                                 (256, 128, -1)):
         assert va.LIB.varlen_attn_debug_mma_cycles(n_mma, n_cols, mode, fake, None) == va.VARLEN_ERR_SHAPE

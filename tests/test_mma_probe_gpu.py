@@ -9,7 +9,7 @@ import torch
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("mode,n_cols", [(m, n) for m in (0, 1, 2) for n in (64, 128, 256)] + [(5, 64), (5, 128), (6, 128)])
+@pytest.mark.parametrize("mode,n_cols", [(m, n) for m in (0, 1, 2) for n in (64, 128, 256)] + [(5, 64), (5, 128), (6, 128), (7, 128)])
 def test_mma_probe_runs(mode, n_cols):
     from packed_variable_length_varlen_gb300 import varlen_attn as va
     cyc = torch.zeros(1, dtype=torch.int64, device="cuda")
