@@ -17,7 +17,8 @@
 //  The fp32 quotient x / descale is the IEEE one; it is formed from the
 //  correctly rounded reciprocal of the descale and one fma remainder
 //  correction (Markstein's division step: q0 = x * y, r = x - q0 * d exact,
-//  q = q0 + r * y, given x's sign), which gives the correctly rounded
+//  q = q0 + r * y, given x's sign; two lanes at a time with packed f32x2
+//  operations, each lane rounded as the scalar ones), which gives the correctly rounded
 //  quotient while the remainder stays a normal number: for descales below
 //  2^-100 the kernels divide.  Checked for every positive bf16 amax and every
 //  bf16 x of magnitude at most amax: the two quotients have the same sign and
@@ -89,6 +90,15 @@ struct Divider {
     const float r = __fmaf_rn(-q0, d, x);
     return copysignf(__fmaf_rn(r, y, q0), x);  // the quotient's sign, zeros included, is x's (d > 0)
   }
+  // the same two lanes at a time (packed f32x2 multiply and fmas, each lane
+  // rounded exactly as the scalar operations round it)
+  __device__ __forceinline__ float2 two(float2 x) const {
+    if (!fast) return make_float2(x.x / d, x.y / d);
+    const float2 q0 = fmul2_rn(x, make_float2(y, y));
+    const float2 r = ffma2(q0, make_float2(-d, -d), x);
+    const float2 q = ffma2(r, make_float2(y, y), q0);
+    return make_float2(copysignf(q.x, x.x), copysignf(q.y, x.y));
+  }
 };
 
 __device__ __forceinline__ Divider divider(float descale) {
@@ -101,8 +111,8 @@ __device__ __forceinline__ Divider divider(float descale) {
 
 // Four E4M3 codes of a / d, b / d, c / d, e / d packed low byte first.
 __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float e, const Divider& d) {
-  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(d(a), d(b)), __NV_SATFINITE, __NV_E4M3);
-  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(d(c), d(e)), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(d.two(make_float2(a, b)), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(d.two(make_float2(c, e)), __NV_SATFINITE, __NV_E4M3);
   return lo | (hi << 16);
 }
 
