@@ -116,6 +116,16 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float e, c
   return lo | (hi << 16);
 }
 
+// out[k] = byte k of in[0], in[1], in[2], in[3] (in[i] in byte i).
+__device__ __forceinline__ void transpose4x4(const uint32_t (&in)[4], uint32_t* out) {
+  const uint32_t t0 = __byte_perm(in[0], in[1], 0x5140), t1 = __byte_perm(in[2], in[3], 0x5140);
+  const uint32_t t2 = __byte_perm(in[0], in[1], 0x7362), t3 = __byte_perm(in[2], in[3], 0x7362);
+  out[0] = __byte_perm(t0, t1, 0x5410);
+  out[1] = __byte_perm(t0, t1, 0x7632);
+  out[2] = __byte_perm(t2, t3, 0x5410);
+  out[3] = __byte_perm(t2, t3, 0x7632);
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------ amax, Q / K codes
@@ -343,12 +353,10 @@ __global__ void __launch_bounds__(256, 4) varlen_fp8_vt_kernel(const Fp8Params p
       }
     uint32_t w[16];  // w[j]: codes of keys 4g..4g+3 at d = 16s + j (keys past the segment end: 0)
 #pragma unroll
-    for (int j = 0; j < 16; ++j) w[j] = 0;
+    for (int hf = 0; hf < 2; ++hf) {
+      uint32_t a[4], e[4];  // key 4g+i: codes of d = 16s + 8hf + 0..3 (a) and + 4..7 (e), low byte first
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (4 * g + i >= valid) continue;
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
+      for (int i = 0; i < 4; ++i) {
         const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&u[i][hf]);
         float f[8];
 #pragma unroll
@@ -357,13 +365,14 @@ __global__ void __launch_bounds__(256, 4) varlen_fp8_vt_kernel(const Fp8Params p
           f[2 * k] = t2.x;
           f[2 * k + 1] = t2.y;
         }
-        const uint32_t a = e4m3x4(f[0], f[1], f[2], f[3], dsc), e = e4m3x4(f[4], f[5], f[6], f[7], dsc);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          w[hf * 8 + k] |= ((a >> (8 * k)) & 0xffu) << (8 * i);
-          w[hf * 8 + 4 + k] |= ((e >> (8 * k)) & 0xffu) << (8 * i);
-        }
+        const bool in = 4 * g + i < valid;
+        a[i] = in ? e4m3x4(f[0], f[1], f[2], f[3], dsc) : 0u;
+        e[i] = in ? e4m3x4(f[4], f[5], f[6], f[7], dsc) : 0u;
       }
+      // 4 x 4 byte transposes: word k of the result holds byte k of the
+      // four keys' words, key 4g+i in byte i
+      transpose4x4(a, &w[hf * 8]);
+      transpose4x4(e, &w[hf * 8 + 4]);
     }
 #pragma unroll
     for (int j = 0; j < 16; ++j) tile[(s * 16 + j) * 32 + g] = w[j];
