@@ -261,8 +261,8 @@ int varlen_attn_bwd_dense(const void* q, varlen_dense_stride sq, const void* k, 
 /*
  * Backward without a workspace argument, for callers that cannot allocate
  * device memory (code inside a host framework that owns every device
- * allocation, or on a path where cudaMalloc is not allowed).  The paper has
- * no counterpart: this is a deployment variant of varlen_attn_bwd.
+ * allocation, or on a path where cudaMalloc is not allowed).  The attention
+ * pages describe no such call: this is a deployment variant of varlen_attn_bwd.
  * Arguments, layouts and results are those of varlen_attn_bwd; the scratch
  * (the fp32 dQ accumulator, delta and log2-domain LSE) lives in a fixed
  * file-scope device array of VARLEN_NOALLOC_SCRATCH_BYTES bytes that every
