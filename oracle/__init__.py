@@ -72,6 +72,7 @@ class _Fp8Problem(ctypes.Structure):
         ("scale", ctypes.c_double),
         ("q_descale", ctypes.c_void_p), ("k_descale", ctypes.c_void_p), ("v_descale", ctypes.c_void_p),
         ("quantize_p", ctypes.c_int32),
+        ("window_left", ctypes.c_int32), ("window_right", ctypes.c_int32),
     ]
 
 
@@ -406,7 +407,9 @@ class Fp8Problem:
     """One FP8 (E4M3) forward problem: codes as uint8 [rows, H, D] CPU tensors
     (unit innermost stride) and fp64 descales [batch * H] per tensor."""
 
-    def __init__(self, q8, k8, v8, cu_q, cu_k, scale, q_descale, k_descale, v_descale, quantize_p=True):
+    def __init__(self, q8, k8, v8, cu_q, cu_k, scale, q_descale, k_descale, v_descale, quantize_p=True,
+                 causal=False, window=(-1, -1)):
+        """``causal`` and ``window = (left, right)`` as in ``Problem``."""
         for t in (q8, k8, v8):
             if t.dtype != torch.uint8 or t.dim() != 3 or t.stride(2) != 1:
                 raise ValueError("FP8 operands are uint8 [rows, H, D] tensors with unit innermost stride")
@@ -429,6 +432,10 @@ class Fp8Problem:
         s.scale = float(scale)
         s.q_descale, s.k_descale, s.v_descale = (d.ctypes.data for d in self.desc)
         s.quantize_p = 1 if quantize_p else 0
+        wl, wr = int(window[0]), int(window[1])
+        if causal:
+            wr = 0
+        s.window_left, s.window_right = (min(max(w, -1), 2**31 - 1) for w in (wl, wr))
         self._s = s
 
     def fwd(self, rows, heads, lib=None):

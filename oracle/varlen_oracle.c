@@ -110,21 +110,27 @@ static int32_t segment_of(const int32_t *cu, int32_t batch, int64_t i) {
     return -1;
 }
 
-/* The keys [*lo, *hi) of segment b (0-based within it) that its q row ii
- * sees: all Sk_b without a mask; else, with diag = ii + Sk_b - Sq_b, those
- * with jj >= diag - window_left (if window_left >= 0) and
- * jj <= diag + window_right (if window_right >= 0).  Empty: *lo == *hi. */
-static void visible_range(const oracle_problem *pb, int32_t b, int64_t ii,
-                          int64_t *lo, int64_t *hi) {
-    const int64_t Sq = (int64_t)pb->cu_q[b + 1] - pb->cu_q[b];
-    const int64_t Sk = (int64_t)pb->cu_k[b + 1] - pb->cu_k[b];
+/* The keys [*lo, *hi) (0-based within the segment) that q row ii of a
+ * segment with Sq query and Sk key rows sees: all Sk without a mask; else,
+ * with diag = ii + Sk - Sq, those with jj >= diag - window_left (if
+ * window_left >= 0) and jj <= diag + window_right (if window_right >= 0).
+ * Empty: *lo == *hi. */
+static void band_range(int64_t Sq, int64_t Sk, int64_t ii, int32_t window_left, int32_t window_right,
+                       int64_t *lo, int64_t *hi) {
     const int64_t diag = ii + (Sk - Sq);
     int64_t a = 0, e = Sk;
-    if (pb->window_left >= 0 && diag - pb->window_left > a) a = diag - pb->window_left;
-    if (pb->window_right >= 0 && diag + pb->window_right + 1 < e) e = diag + pb->window_right + 1;
+    if (window_left >= 0 && diag - window_left > a) a = diag - window_left;
+    if (window_right >= 0 && diag + window_right + 1 < e) e = diag + window_right + 1;
     if (e < a) e = a;
     *lo = a;
     *hi = e;
+}
+
+/* band_range for q row ii of segment b of a bf16 / fp64 problem. */
+static void visible_range(const oracle_problem *pb, int32_t b, int64_t ii,
+                          int64_t *lo, int64_t *hi) {
+    band_range((int64_t)pb->cu_q[b + 1] - pb->cu_q[b], (int64_t)pb->cu_k[b + 1] - pb->cu_k[b], ii,
+               pb->window_left, pb->window_right, lo, hi);
 }
 
 /* Forward for one (q row, head): s, LSE, P and o by the definition above.
@@ -400,7 +406,9 @@ int oracle_num_threads(void) {
  * where e4m3(x) rounds to the nearest E4M3 value, ties to even, saturating
  * at +-448 (P is rounded to E4M3 for the P V product; the row sum uses the
  * unrounded p).  quantize_p = 0 skips that rounding.  Empty key sets give
- * LSE = -inf and o = 0, as above.  No mask.
+ * LSE = -inf and o = 0, as above.  With a mask (window_left, window_right,
+ * the band of the bf16 forward above: band_range) j runs over the keys row
+ * i sees; a row that sees none gets LSE = -inf and o = 0.
  */
 
 /* Value of an E4M3 code. */
@@ -468,6 +476,8 @@ typedef struct {
     double scale;
     const double *q_descale, *k_descale, *v_descale;  /* [batch * num_heads] */
     int32_t quantize_p;             /* 1: P rounded to E4M3 for P V         */
+    int32_t window_left;            /* mask sides, < 0 unbounded            */
+    int32_t window_right;           /* (band_range); causal = (-1, 0)       */
 } oracle_fp8_problem;
 
 static void load_row8(const uint8_t *base, int64_t rs, int64_t hs, int64_t row, int32_t h, int32_t D, double *x) {
@@ -499,23 +509,26 @@ int oracle_fwd_fp8(const oracle_fp8_problem *pb, int64_t n, const int64_t *rows,
                 continue;
             }
             const int64_t k0 = pb->cu_k[b], Sk = (int64_t)pb->cu_k[b + 1] - pb->cu_k[b];
+            const int64_t Sq = (int64_t)pb->cu_q[b + 1] - pb->cu_q[b];
             const int64_t bh = (int64_t)b * H + h;
             const double sqk = pb->scale * pb->q_descale[bh] * pb->k_descale[bh];
+            int64_t jlo, jhi;
+            band_range(Sq, Sk, i - pb->cu_q[b], pb->window_left, pb->window_right, &jlo, &jhi);
             for (int32_t d = 0; d < D; ++d) o[d] = 0.0;
-            if (Sk <= 0) {
+            if (jhi <= jlo) {
                 lse[t] = -INFINITY;
                 continue;
             }
             load_row8(pb->q, pb->q_rs, pb->q_hs, i, h, D, qi);
             double m = -INFINITY;
-            for (int64_t j = 0; j < Sk; ++j) {
+            for (int64_t j = jlo; j < jhi; ++j) {
                 load_row8(pb->k, pb->k_rs, pb->k_hs, k0 + j, h, D, kj);
                 s[j] = sqk * dot(qi, kj, D);
                 if (s[j] > m) m = s[j];
             }
             double l = 0.0;
-            for (int64_t j = 0; j < Sk; ++j) l += exp(s[j] - m);
-            for (int64_t j = 0; j < Sk; ++j) {
+            for (int64_t j = jlo; j < jhi; ++j) l += exp(s[j] - m);
+            for (int64_t j = jlo; j < jhi; ++j) {
                 double p = exp(s[j] - m);
                 if (pb->quantize_p) p = e4m3_round(p);
                 load_row8(pb->v, pb->v_rs, pb->v_hs, k0 + j, h, D, kj);

@@ -1,8 +1,9 @@
 """Pins for the FP8 (OCP E4M3) part of the fp64 oracle: the codec against
 torch's float8_e4m3fn (a library routine), saturation by the format's
 definition, the quantised forward against the fp64 oracle on the dequantised
-inputs, closed forms (one key, two keys with P rounded by torch), the bound
-that rounding P may move O by, and planted mistakes."""
+inputs (unmasked, and under causal and sliding-window bands against the
+pinned masked fp64 oracle), closed forms (one key, two keys with P rounded
+by torch), the bound that rounding P may move O by, and planted mistakes."""
 import math
 import pathlib
 import subprocess
@@ -91,6 +92,26 @@ def _battery(lib):
                                                      and np.allclose(lse_fin(l0), lse_fin(lrf), rtol=1e-12,
                                                                      atol=1e-13)
                                                      and np.array_equal(np.isneginf(l0), np.isneginf(lrf)))))
+    # with a band: the fp64 oracle's masked forward on the dequantised operands
+    # (segments with Sq > Sk, so that causal rows without a key occur)
+    cqm, ckm, _, (q8m, k8m, v8m), (qdm, kdm, vdm) = _fp8_case(5, lq=(8, 3, 6, 0, 9), lk=(3, 8, 6, 4, 9))
+    rowsm, headsm = oracle.all_pairs(cqm[-1], H)
+    deqm = [_dequant(t, d_, c_, H, lib) for t, d_, c_ in ((q8m, qdm, cqm), (k8m, kdm, ckm), (v8m, vdm, ckm))]
+    ok_m, n_empty = True, 0
+    for causal, window in ((True, (-1, -1)), (False, (2, 0)), (False, (0, 0)), (False, (1, 3)),
+                           (False, (-1, 2)), (True, (3, -1))):
+        kw = dict(causal=causal, window=window)
+        pm = oracle.Fp8Problem(q8m, k8m, v8m, cqm, ckm, sc, qdm, kdm, vdm, quantize_p=False, **kw)
+        om, lm = pm.fwd(rowsm, headsm, lib)
+        orm, lrm = oracle.Problem(*deqm, cqm, ckm, sc, **kw).fwd(rowsm, headsm)
+        ok_m &= bool(np.allclose(om, orm, rtol=1e-12, atol=1e-13)
+                     and np.allclose(lse_fin(lm), lse_fin(lrm), rtol=1e-12, atol=1e-13)
+                     and np.array_equal(np.isneginf(lm), np.isneginf(lrm)))
+        # P rounding leaves LSE (the unrounded row sum) and the rows without keys alone
+        omq, lmq = oracle.Fp8Problem(q8m, k8m, v8m, cqm, ckm, sc, qdm, kdm, vdm, **kw).fwd(rowsm, headsm, lib)
+        ok_m &= bool(np.array_equal(lmq, lm) and np.all(omq[np.isneginf(lm)] == 0))
+        n_empty += int(np.isneginf(lm).sum())
+    res.append(("masked_unrounded_equals_fp64_oracle", bool(ok_m and n_empty > 0)))
     # with rounding: O moves by at most 2^-4 of sum_j p_j |v_j| / l per element
     p1 = oracle.Fp8Problem(q8, k8, v8, cq, ck, sc, qd, kd, vd, quantize_p=True)
     o1, l1 = p1.fwd(rows, heads, lib)
@@ -153,8 +174,12 @@ MUTANTS = [
     ("k descale dropped", "const double sqk = pb->scale * pb->q_descale[bh] * pb->k_descale[bh];",
      "const double sqk = pb->scale * pb->q_descale[bh];"),
     ("v descale dropped", "o[d] *= pb->v_descale[bh] / l;", "o[d] *= 1.0 / l;"),
-    ("row sum of rounded p", "for (int64_t j = 0; j < Sk; ++j) l += exp(s[j] - m);",
-     "for (int64_t j = 0; j < Sk; ++j) l += e4m3_round(exp(s[j] - m));"),
+    ("row sum of rounded p", "for (int64_t j = jlo; j < jhi; ++j) l += exp(s[j] - m);",
+     "for (int64_t j = jlo; j < jhi; ++j) l += e4m3_round(exp(s[j] - m));"),
+    ("band ignored", "band_range(Sq, Sk, i - pb->cu_q[b], pb->window_left, pb->window_right, &jlo, &jhi);",
+     "jlo = 0; jhi = Sk;"),
+    ("band from the packed row index", "band_range(Sq, Sk, i - pb->cu_q[b], pb->window_left,",
+     "band_range(Sq, Sk, i, pb->window_left,"),
     ("descale of the wrong head", "const int64_t bh = (int64_t)b * H + h;", "const int64_t bh = (int64_t)b * H;"),
 ]
 

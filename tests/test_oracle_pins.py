@@ -466,8 +466,8 @@ def test_page_values():
     assert max(wl.seqlens_q()) == c["true_max_seqlen_q"] != c["stated_max_seqlen_q"]
 
 
-LEFT_EDGE = "    if (pb->window_left >= 0 && diag - pb->window_left > a) a = diag - pb->window_left;"
-RIGHT_EDGE = "    if (pb->window_right >= 0 && diag + pb->window_right + 1 < e) e = diag + pb->window_right + 1;"
+LEFT_EDGE = "    if (window_left >= 0 && diag - window_left > a) a = diag - window_left;"
+RIGHT_EDGE = "    if (window_right >= 0 && diag + window_right + 1 < e) e = diag + window_right + 1;"
 
 MUTANTS = [
     ("dropped scale in s", "s[j] = pb->scale * dot(qi, kj, D);", "s[j] = dot(qi, kj, D);"),
@@ -486,15 +486,15 @@ MUTANTS = [
      "const int64_t k0 = pb->cu_k[b] + (b > 0);"),
     ("delta from dO.v instead of dO.o", "E[ii] = dot(doi, oi, D);", "E[ii] = dot(doi, doi, D);"),
     ("head stride ignored", "int64_t off = row * rs + (int64_t)h * hs;", "int64_t off = row * rs;"),
-    ("causal diagonal one key early", RIGHT_EDGE, RIGHT_EDGE.replace("+ 1 < e) e = diag + pb->window_right + 1;",
-                                                                     "< e) e = diag + pb->window_right;")),
+    ("causal diagonal one key early", RIGHT_EDGE, RIGHT_EDGE.replace("+ 1 < e) e = diag + window_right + 1;",
+                                                                     "< e) e = diag + window_right;")),
     ("causal diagonal aligned top-left", "const int64_t diag = ii + (Sk - Sq);", "const int64_t diag = ii;"),
     ("mask missing on the key side", "if (jj < jlo || jj >= jhi) continue;", "(void)jj;"),
     ("key-side mask misses the left edge", "if (jj < jlo || jj >= jhi) continue;", "if (jj >= jhi) continue;"),
-    ("window left edge one key late", LEFT_EDGE, LEFT_EDGE.replace("a = diag - pb->window_left;",
-                                                                   "a = diag - pb->window_left + 1;")),
-    ("window left side ignored", LEFT_EDGE, LEFT_EDGE.replace("if (pb->window_left >= 0 &&", "if (0 &&")),
-    ("window right width ignored", RIGHT_EDGE, RIGHT_EDGE.replace("pb->window_right + 1", "1")),
+    ("window left edge one key late", LEFT_EDGE, LEFT_EDGE.replace("a = diag - window_left;",
+                                                                   "a = diag - window_left + 1;")),
+    ("window left side ignored", LEFT_EDGE, LEFT_EDGE.replace("if (window_left >= 0 &&", "if (0 &&")),
+    ("window right width ignored", RIGHT_EDGE, RIGHT_EDGE.replace("window_right + 1", "1")),
     ("window sides swapped", LEFT_EDGE + "\n" + RIGHT_EDGE,
      LEFT_EDGE.replace("window_left", "window_right") + "\n" + RIGHT_EDGE.replace("window_right", "window_left")),
 ]
