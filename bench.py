@@ -643,10 +643,12 @@ def ours(args, w, ws, rank, local):
 def fp8_forward(args, w, ws, rank, local):
     """Times the E4M3 forward (quantisation passes included) alone: K calls
     after W warm-up calls, CUDA events on the launching stream, max over
-    ranks; FLOPs at the bf16 forward count."""
+    ranks; FLOPs at the bf16 forward count (over the visible pairs under
+    --causal / --window)."""
     from packed_variable_length_varlen_gb300 import varlen_attn as va
-    if w.head_dim != 128 or args.causal or _window(args) != (-1, -1):
-        raise SystemExit("--fp8 times the E4M3 forward: head size 128, no mask")
+    if w.head_dim != 128:
+        raise SystemExit("--fp8 times the E4M3 forward: head size 128")
+    causal, window = bool(args.causal), _window(args)
     dev = torch.device("cuda", local)
     d = W.make_inputs(w, seed=rank, with_dout=False).to(dev)
     H = w.num_heads
@@ -658,7 +660,8 @@ def fp8_forward(args, w, ws, rank, local):
 
     def run():
         st = va.varlen_attn_fwd_fp8(d.q, d.k, d.v, d.cu_q, d.cu_k, w.batch, w.total_q, w.total_k, H, 128,
-                                    w.max_q(), w.max_k(), w.softmax_scale, out, lse, wsp, nbytes, stream)
+                                    w.max_q(), w.max_k(), w.softmax_scale, out, lse, wsp, nbytes, stream,
+                                    causal=causal, window=window)
         assert st == 0, va.varlen_attn_status_string(st)
 
     for _ in range(args.warmup):
@@ -674,12 +677,15 @@ def fp8_forward(args, w, ws, rank, local):
     torch.cuda.synchronize()
     ms = _max_over_ranks(a.elapsed_time(b), ws) / args.steps
     if rank == 0:
-        print(json.dumps({"metric": "E4M3 varlen attention forward TFLOP/s (bf16 FLOP count, quantisation included)",
-                          "value": ws * w.fwd_flops() / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": ws,
+        mask = ("causal " if causal else "") + ("window(%d,%d) " % window if window != (-1, -1) else "")
+        print(json.dumps({"metric": "E4M3 varlen attention forward TFLOP/s (%sbf16 FLOP count, quantisation "
+                                    "included)" % mask,
+                          "value": ws * w.fwd_flops(causal, window) / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                          "n_gpus": ws,
                           "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
                           "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate)",
                           "data": "synthetic", "config": {"workload": w.name, "num_heads": H, "head_dim": 128,
-                                                          "step": "fp8 fwd",
+                                                          "step": "fp8 fwd", "causal": causal, "window": list(window),
                                                           "l2": "inputs larger than L2 (k, v 2 GB each); no flush"},
                           "gpu_launches": 4 * args.steps}),
               flush=True)

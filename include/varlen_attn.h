@@ -197,7 +197,8 @@ int varlen_attn_bwd_deterministic(const void* q, varlen_stride sq, const void* k
  * E4M3 (FP8) forward (not on the pages, which quote quantised attention
  * only by its accuracy: the ffpa-attn NVFP4 pull request, "Summary", cos
  * ~0.982 against SDPA).  Arguments, layouts and errors as varlen_attn_fwd;
- * head_dim must be 128 (else VARLEN_ERR_HEAD_DIM), no mask.  q, k, v (bf16)
+ * head_dim must be 128 (else VARLEN_ERR_HEAD_DIM); no mask (the window form
+ * below takes one).  q, k, v (bf16)
  * are quantised per (segment, head) and tensor into the caller's workspace
  * (varlen_attn_fwd_fp8_workspace_size bytes, 256-byte aligned, contents on
  * entry irrelevant): descale = amax / 448 (1 for an all-zero block), code =
@@ -206,6 +207,13 @@ int varlen_attn_bwd_deterministic(const void* q, varlen_stride sq, const void* k
  * O = vd * sum_j E4M3(P_j) v8_j / sum_j P_j (bf16 out), LSE = max + ln sum P.
  * P is rounded from a running row maximum, so results match that definition
  * up to the rounding of P (a relative 2^-4 per weight).
+ *
+ * varlen_attn_fwd_fp8_window is the same call under the band of
+ * varlen_attn_fwd_window (window_left, window_right after scale; a negative
+ * side unbounded, (-1, 0) causal, (-1, -1) no mask): the max, the sums and
+ * O run over each row's visible keys only, and a row that sees none gets
+ * O = 0 and LSE = -inf.  The quantisation is that of the unmasked call (amax
+ * over every row of the segment).
  *
  * varlen_attn_fwd_fp8_workspace_layout returns the byte offsets of the
  * workspace sections after a call: offsets[0] amax fp32 [3][batch * H] (q,
@@ -223,6 +231,12 @@ int varlen_attn_fwd_fp8(const void* q, varlen_stride sq, const void* k, varlen_s
                         int32_t total_q, int32_t total_k, int32_t num_heads, int32_t head_dim, int32_t max_seqlen_q,
                         int32_t max_seqlen_k, float scale, void* out, varlen_stride so, float* lse,
                         void* workspace, size_t workspace_bytes, void* stream);
+int varlen_attn_fwd_fp8_window(const void* q, varlen_stride sq, const void* k, varlen_stride sk, const void* v,
+                               varlen_stride sv, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                               int32_t batch, int32_t total_q, int32_t total_k, int32_t num_heads, int32_t head_dim,
+                               int32_t max_seqlen_q, int32_t max_seqlen_k, float scale, int32_t window_left,
+                               int32_t window_right, void* out, varlen_stride so, float* lse, void* workspace,
+                               size_t workspace_bytes, void* stream);
 
 /*
  * Dense batched attention: q, out, dout, dq are [batch, seqlen_q, H, D] and

@@ -661,14 +661,12 @@ extern "C" int varlen_attn_fwd_fp8_workspace_layout(int32_t batch, int32_t total
   return VARLEN_OK;
 }
 
-extern "C" int varlen_attn_fwd_fp8(const void* q, varlen_stride sq, const void* k, varlen_stride sk, const void* v,
-                                   varlen_stride sv, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
-                                   int32_t batch, int32_t total_q, int32_t total_k, int32_t num_heads,
-                                   int32_t head_dim, int32_t max_seqlen_q, int32_t max_seqlen_k, float scale,
-                                   void* out, varlen_stride so, float* lse, void* workspace,
-                                   size_t workspace_bytes, void* stream) {
-  (void)max_seqlen_q;
-  (void)max_seqlen_k;
+namespace {
+
+int fwd_fp8_impl(const void* q, varlen_stride sq, const void* k, varlen_stride sk, const void* v, varlen_stride sv,
+                 const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t batch, int32_t total_q,
+                 int32_t total_k, int32_t num_heads, int32_t head_dim, float scale, void* out, varlen_stride so,
+                 float* lse, void* workspace, size_t workspace_bytes, void* stream, Band band) {
   if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr) return VARLEN_ERR_NULL;
   int st = check_common(batch, total_q, total_k, num_heads, head_dim, scale);
   if (st != VARLEN_OK) return st;
@@ -714,6 +712,9 @@ extern "C" int varlen_attn_fwd_fp8(const void* q, varlen_stride sq, const void* 
   L.p.total_k = total_k;
   L.p.num_heads = num_heads;
   L.p.scale = scale;
+  L.p.masked = band.masked;
+  L.p.win_left = band.left;
+  L.p.win_right = band.right;
   L.p.err = dev.err;
   L.p.q_span = nhd_span(q, sq, total_q, num_heads, head_dim);
   L.p.k_span = nhd_span(k, sk, total_k, num_heads, head_dim);
@@ -730,6 +731,33 @@ extern "C" int varlen_attn_fwd_fp8(const void* q, varlen_stride sq, const void* 
   if ((st = encode_codes_vt(&L.tm_vt, L.p.vt, L.p.kp, num_heads)) != VARLEN_OK) return st;
   cudaError_t e = launch_fwd_fp8(L, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? VARLEN_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" int varlen_attn_fwd_fp8(const void* q, varlen_stride sq, const void* k, varlen_stride sk, const void* v,
+                                   varlen_stride sv, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                   int32_t batch, int32_t total_q, int32_t total_k, int32_t num_heads,
+                                   int32_t head_dim, int32_t max_seqlen_q, int32_t max_seqlen_k, float scale,
+                                   void* out, varlen_stride so, float* lse, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  (void)max_seqlen_q;
+  (void)max_seqlen_k;
+  return fwd_fp8_impl(q, sq, k, sk, v, sv, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads, head_dim,
+                      scale, out, so, lse, workspace, workspace_bytes, stream, kNoMask);
+}
+
+extern "C" int varlen_attn_fwd_fp8_window(const void* q, varlen_stride sq, const void* k, varlen_stride sk,
+                                          const void* v, varlen_stride sv, const int32_t* cu_seqlens_q,
+                                          const int32_t* cu_seqlens_k, int32_t batch, int32_t total_q,
+                                          int32_t total_k, int32_t num_heads, int32_t head_dim,
+                                          int32_t max_seqlen_q, int32_t max_seqlen_k, float scale,
+                                          int32_t window_left, int32_t window_right, void* out, varlen_stride so,
+                                          float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  (void)max_seqlen_q;
+  (void)max_seqlen_k;
+  return fwd_fp8_impl(q, sq, k, sk, v, sv, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads, head_dim,
+                      scale, out, so, lse, workspace, workspace_bytes, stream, band_of(window_left, window_right));
 }
 
 extern "C" int varlen_attn_get_device_status(void* stream) {

@@ -1,5 +1,5 @@
 // varlen_fp8.cu -- E4M3 (FP8) forward of packed variable-length attention on
-// sm_103a, head size 128, no mask.
+// sm_103a, head size 128, unmasked or under a causal / sliding-window band.
 //
 // Four launches on the caller's stream:
 //  1. varlen_fp8_amax_kernel: max |x| of Q, K and V per (segment, head),
@@ -31,7 +31,9 @@
 //         O += e4m3(P) V8      (P written into TMEM over S as E4M3 codes,
 //                               read from there as the A operand)
 //     and finally O * vd / l in bf16 and LSE = (m + log2 l) ln 2.  The row
-//     sum l uses the unrounded P.
+//     sum l uses the unrounded P.  Under a band (the bf16 kernels' causal /
+//     sliding-window reading) a unit walks only the key tiles some of its
+//     rows see, and each row's keys outside its band are -inf by select.
 //
 // The quantised reading is that of the flash-attention family's FP8 forward
 // (one descale per (segment, head) and tensor); the pages themselves quote
@@ -40,6 +42,7 @@
 #include <cuda_fp8.h>
 
 #include <algorithm>
+#include <cfloat>
 
 #include "sm103_ptx.cuh"
 #include "varlen_internal.h"
@@ -67,31 +70,13 @@ __device__ __forceinline__ bool segment_of_row(const CuView& cu, int32_t batch, 
   return row >= clamp_row(cu_at(cu, b0), total) && row < clamp_row(cu_at(cu, b0 + 1), total);
 }
 
-// Eight bf16 (one 16-byte load) as floats (zeros when a bounds-checking
-// build finds the load outside `span`).
-__device__ __forceinline__ void load8(const __nv_bfloat16* src, float (&f)[8], const Span& span, unsigned int* err) {
-  const uint4 u = in_span(span, src, 16, err) ? __ldg(reinterpret_cast<const uint4*>(src)) : make_uint4(0, 0, 0, 0);
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 t = __bfloat1622float2(h[i]);
-    f[2 * i] = t.x;
-    f[2 * i + 1] = t.y;
-  }
-}
-
 // x / d in fp32, correctly rounded, for one descale d and many x.
 struct Divider {
   float d, y;  // descale and its correctly rounded reciprocal
   bool fast;   // d >= 2^-100: Markstein's step is exact
-  __device__ __forceinline__ float operator()(float x) const {
-    if (!fast) return x / d;
-    const float q0 = __fmul_rn(x, y);
-    const float r = __fmaf_rn(-q0, d, x);
-    return copysignf(__fmaf_rn(r, y, q0), x);  // the quotient's sign, zeros included, is x's (d > 0)
-  }
-  // the same two lanes at a time (packed f32x2 multiply and fmas, each lane
-  // rounded exactly as the scalar operations round it)
+  // Two quotients at a time: q0 = x * y, r = x - q0 * d (exact), q = q0 + r * y,
+  // by packed f32x2 multiply and fmas (each lane rounded as the scalar
+  // operation rounds it); the quotient's sign, zeros included, is x's (d > 0).
   __device__ __forceinline__ float2 two(float2 x) const {
     if (!fast) return make_float2(x.x / d, x.y / d);
     const float2 q0 = fmul2_rn(x, make_float2(y, y));
@@ -414,8 +399,30 @@ static_assert(sizeof(F8Barriers) <= 1024, "barrier block too large");
 constexpr uint32_t kF8RegsLaunch = 168, kF8RegsCtl = 112, kF8RegsSoftmax = 192;
 static_assert(kF8RegsCtl + 2 * kF8RegsSoftmax <= 3 * kF8RegsLaunch, "register split exceeds the launch allocation");
 
+// kv tiles [j_lo, j_lo + n) a unit (kF8Unit q rows of one segment and
+// head) works through, n returned.  With a mask (the band of Fp8Params) only
+// the tiles holding keys that some row of the unit sees; 0 means no row of
+// the unit sees a key (O = 0, LSE = -inf).
+template <bool MASKED>
+__device__ __forceinline__ int32_t fp8_kv_tiles(const SegCursor& c, int32_t unit, const Fp8Params& p,
+                                                int32_t& j_lo) {
+  j_lo = 0;
+  int32_t nkv = (c.olen + kTileN - 1) / kTileN;
+  if (MASKED) {
+    const int64_t q0 = (int64_t)unit * kF8Unit;
+    const int64_t q1 = min((int64_t)c.len, q0 + kF8Unit) - 1;
+    int32_t lo, hi;
+    band_keys(q0, q1, c.len, c.olen, p.win_left, p.win_right, &lo, &hi);
+    if (hi <= lo) return 0;
+    j_lo = lo / kTileN;
+    nkv = (hi + kTileN - 1) / kTileN - j_lo;
+  }
+  return nkv;
+}
+
 }  // namespace
 
+template <bool MASKED>
 __global__ void __launch_bounds__(384, 1)
     varlen_fp8_fwd_kernel(const __grid_constant__ CUtensorMap tm_q8, const __grid_constant__ CUtensorMap tm_k8,
                           const __grid_constant__ CUtensorMap tm_vt, const Fp8Params p) {
@@ -468,7 +475,8 @@ __global__ void __launch_bounds__(384, 1)
       for (int64_t t = blockIdx.x;
            ok && cursor_seek<kF8Unit>(c, t, H, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k, order); t += G) {
         const Tile tl = cursor_tile(c, t);
-        const int32_t nkv = (c.olen + kTileN - 1) / kTileN;
+        int32_t j_lo;
+        const int32_t nkv = fp8_kv_tiles<MASKED>(c, tl.m, p, j_lo);
         if (nkv == 0) continue;
         const int32_t qrow = c.r0 + tl.m * kF8Unit;
         if (q_loads > 0 && !mbar_wait(&bar.q_empty, (q_loads - 1) & 1, abort)) break;
@@ -487,8 +495,8 @@ __global__ void __launch_bounds__(384, 1)
             }
             mbar_arrive_expect_tx(&bar.kv_full[slot], kF8Tile);
             uint8_t* dst = ring + slot * kF8Tile;
-            if (which == 0) tma_load_3d(dst, &tm_k8, &bar.kv_full[slot], 0, tl.h, c.o0 + j * kTileN);
-            else tma_load_3d(dst, &tm_vt, &bar.kv_full[slot], vt0 + j * kTileN, 0, tl.h);
+            if (which == 0) tma_load_3d(dst, &tm_k8, &bar.kv_full[slot], 0, tl.h, c.o0 + (j_lo + j) * kTileN);
+            else tma_load_3d(dst, &tm_vt, &bar.kv_full[slot], vt0 + (j_lo + j) * kTileN, 0, tl.h);
             ++ring_pos;
           }
         }
@@ -534,7 +542,8 @@ __global__ void __launch_bounds__(384, 1)
       };
       for (int64_t t = blockIdx.x;
            ok && cursor_seek<kF8Unit>(c, t, H, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k, order); t += G) {
-        const int32_t nkv = (c.olen + kTileN - 1) / kTileN;
+        int32_t j_lo;
+        const int32_t nkv = fp8_kv_tiles<MASKED>(c, cursor_tile(c, t).m, p, j_lo);
         if (nkv == 0) continue;
         if (!mbar_wait(&bar.q_full, tiles & 1, abort)) break;
         ++tiles;
@@ -592,7 +601,8 @@ __global__ void __launch_bounds__(384, 1)
     for (int64_t t = blockIdx.x;
          ok && cursor_seek<kF8Unit>(c, t, H, p.cu_q, p.cu_k, p.batch, p.total_q, p.total_k, order); t += G) {
       const Tile tl = cursor_tile(c, t);
-      const int32_t nkv = (c.olen + kTileN - 1) / kTileN;
+      int32_t j_lo;
+      const int32_t nkv = fp8_kv_tiles<MASKED>(c, tl.m, p, j_lo);
       const int32_t r_seg = tl.m * kF8Unit + hf * kTileM + row;
       const bool row_valid = r_seg < c.len;
       const int64_t grow = (int64_t)c.r0 + r_seg;
@@ -615,7 +625,13 @@ __global__ void __launch_bounds__(384, 1)
       const float qd = descale_of(in_span(p.amax_span, aq, 4, p.err) ? __ldg(aq) : 0.f);
       const float kd = descale_of(in_span(p.amax_span, ak, 4, p.err) ? __ldg(ak) : 0.f);
       const float vd = descale_of(in_span(p.amax_span, av, 4, p.err) ? __ldg(av) : 0.f);
-      const float c2 = p.scale * 1.4426950408889634f * qd * kd;
+      // (at least the smallest normal float, so that a masked score times c2
+      // stays -inf when scale * qd * kd underflows; the scores are then
+      // below 3e-31 in magnitude and P is 1 either way)
+      const float c2 = fmaxf(p.scale * 1.4426950408889634f * qd * kd, FLT_MIN);
+      // keys [key_lo, key_hi) this row sees: all Sk, or with a mask its band
+      int32_t key_lo = 0, key_hi = c.olen;
+      if (MASKED) band_keys(r_seg, r_seg, c.len, c.olen, p.win_left, p.win_right, &key_lo, &key_hi);
       float m_use = -INFINITY, l = 0.f;
       for (int32_t j = 0; j < nkv; ++j) {
         const uint32_t gj = g + j;
@@ -632,8 +648,19 @@ __global__ void __launch_bounds__(384, 1)
             for (int i = 0; i < 32; ++i) x[c0 + i] = __uint_as_float(s[i]);
           }
         }
-        const int32_t lim = c.olen - j * kTileN;  // keys past the segment end are -inf
-        if (lim < kTileN) {
+        // keys the row does not see (past the segment end, or outside the
+        // mask's band) are -inf, by select
+        const int32_t lim = key_hi - (j_lo + j) * kTileN;
+        if constexpr (MASKED) {
+          const int32_t lim_lo = key_lo - (j_lo + j) * kTileN;
+          if (__any_sync(0xffffffffu, lim_lo > 0)) {  // the band's left edge crosses this tile
+#pragma unroll
+            for (int i = 0; i < 128; ++i) x[i] = (i < lim && i >= lim_lo) ? x[i] : -INFINITY;
+          } else if (__any_sync(0xffffffffu, lim < kTileN)) {
+#pragma unroll
+            for (int i = 0; i < 128; ++i) x[i] = (i < lim) ? x[i] : -INFINITY;
+          }
+        } else if (lim < kTileN) {
 #pragma unroll
           for (int i = 0; i < 128; ++i) x[i] = (i < lim) ? x[i] : -INFINITY;
         }
@@ -659,7 +686,10 @@ __global__ void __launch_bounds__(384, 1)
         // P go into TMEM over the first 32 S columns (already read), four
         // consecutive keys per 32-bit column, the A operand of P V.
         // (two lanes at a time: packed fma / add, as in the bf16 kernel)
-        const float2 cc2 = make_float2(c2, c2), negm = make_float2(-m_use, -m_use);
+        // a row that has seen no key yet keeps m = -inf; subtracting 0 then
+        // gives P = exp2(-inf) = 0 instead of NaN
+        const float m_sub = (MASKED && m_use == -INFINITY) ? 0.f : m_use;
+        const float2 cc2 = make_float2(c2, c2), negm = make_float2(-m_sub, -m_sub);
         float2 rs2a = make_float2(0.f, 0.f), rs2b = make_float2(0.f, 0.f);
         uint32_t pw[32];
 #pragma unroll
@@ -751,7 +781,7 @@ cudaError_t launch_fwd_fp8(const Fp8Launch& L, cudaStream_t stream) {
   varlen_fp8_vt_kernel<<<L.grid * 4, 256, 0, stream>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (p.total_q == 0) return cudaSuccess;
-  auto kern = varlen_fp8_fwd_kernel;
+  auto kern = p.masked ? varlen_fp8_fwd_kernel<true> : varlen_fp8_fwd_kernel<false>;
   cudaFuncAttributes fa;
   if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
   if (fa.numRegs != (int)kF8RegsLaunch) return cudaErrorInvalidConfiguration;

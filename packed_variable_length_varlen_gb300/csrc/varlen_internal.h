@@ -227,6 +227,8 @@ struct Fp8Params {
   CuView cu_q, cu_k;
   int32_t batch, total_q, total_k, num_heads;
   float scale;     // softmax scale
+  int32_t masked;              // 0: every key of the segment is visible
+  int64_t win_left, win_right; // the band when masked (kWinUnbounded: that side open)
   unsigned int* err;
   Span q_span, k_span, v_span, out_span, lse_span, amax_span, q8_span, k8_span, vt_span;  // bounds-checking build
 };

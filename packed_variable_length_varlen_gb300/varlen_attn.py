@@ -85,6 +85,9 @@ def _load() -> ctypes.CDLL:
     lib.varlen_attn_fwd_fp8.restype = ctypes.c_int
     lib.varlen_attn_fwd_fp8.argtypes = [vp, S, vp, S, vp, S, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, vp, S,
                                         vp, vp, sz, vp]
+    lib.varlen_attn_fwd_fp8_window.restype = ctypes.c_int
+    lib.varlen_attn_fwd_fp8_window.argtypes = [vp, S, vp, S, vp, S, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32,
+                                               i32, i32, vp, S, vp, vp, sz, vp]
     DS = VarlenDenseStride
     lib.varlen_attn_fwd_dense.restype = ctypes.c_int
     lib.varlen_attn_fwd_dense.argtypes = [vp, DS, vp, DS, vp, DS, i32, i32, i32, i32, i32, f32, i32, vp, DS, vp, vp]
@@ -139,7 +142,7 @@ EXPORTED = ("varlen_attn_fwd", "varlen_attn_bwd_workspace_size", "varlen_attn_bw
             "varlen_attn_bwd_window", "varlen_attn_bwd_deterministic", "varlen_attn_fwd_fp8_workspace_size",
             "varlen_attn_fwd_fp8_workspace_layout", "varlen_attn_fwd_fp8", "varlen_attn_bwd_noalloc_scratch_bytes",
             "varlen_attn_debug_noalloc_scratch", "varlen_attn_bounds_checked", "varlen_attn_debug_set_span_slack",
-            "varlen_attn_debug_skip_load", "varlen_attn_debug_mma_cycles")
+            "varlen_attn_debug_skip_load", "varlen_attn_debug_mma_cycles", "varlen_attn_fwd_fp8_window")
 
 # Size of the fixed device array varlen_attn_bwd_noalloc uses as scratch, as
 # compiled into the library.
@@ -272,11 +275,25 @@ def varlen_attn_fwd_fp8_workspace_layout(batch, total_q, total_k, num_heads, hea
 
 
 def varlen_attn_fwd_fp8(q, k, v, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads, head_dim,
-                        max_seqlen_q, max_seqlen_k, scale, out, lse, workspace, workspace_bytes, stream=None) -> int:
-    return LIB.varlen_attn_fwd_fp8(_ptr(q), _stride(q), _ptr(k), _stride(k), _ptr(v), _stride(v), _ptr(cu_seqlens_q),
-                                   _ptr(cu_seqlens_k), batch, total_q, total_k, num_heads, head_dim, max_seqlen_q,
-                                   max_seqlen_k, scale, _ptr(out), _stride(out), _ptr(lse), _ptr(workspace),
-                                   workspace_bytes, _stream(stream))
+                        max_seqlen_q, max_seqlen_k, scale, out, lse, workspace, workspace_bytes, stream=None,
+                        causal=False, window=(-1, -1)) -> int:
+    band = _band(causal, window)
+    head = (_ptr(q), _stride(q), _ptr(k), _stride(k), _ptr(v), _stride(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+            batch, total_q, total_k, num_heads, head_dim, max_seqlen_q, max_seqlen_k, scale)
+    tail = (_ptr(out), _stride(out), _ptr(lse), _ptr(workspace), workspace_bytes, _stream(stream))
+    if band is None:
+        return LIB.varlen_attn_fwd_fp8(*head, *tail)
+    return LIB.varlen_attn_fwd_fp8_window(*head, *band, *tail)
+
+
+def varlen_attn_fwd_fp8_window(q, k, v, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads, head_dim,
+                               max_seqlen_q, max_seqlen_k, scale, window_left, window_right, out, lse, workspace,
+                               workspace_bytes, stream=None) -> int:
+    return LIB.varlen_attn_fwd_fp8_window(_ptr(q), _stride(q), _ptr(k), _stride(k), _ptr(v), _stride(v),
+                                          _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), batch, total_q, total_k, num_heads,
+                                          head_dim, max_seqlen_q, max_seqlen_k, scale, window_left, window_right,
+                                          _ptr(out), _stride(out), _ptr(lse), _ptr(workspace), workspace_bytes,
+                                          _stream(stream))
 
 
 def varlen_attn_fwd_dense(q, k, v, batch, seqlen_q, seqlen_k, num_heads, head_dim, scale, causal, out, lse,
@@ -410,10 +427,11 @@ def attention_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q=0, max_seqle
 
 
 def attention_fwd_fp8(q, k, v, cu_seqlens_q, cu_seqlens_k, scale=None, out=None, lse=None, workspace=None,
-                      stream=None):
+                      stream=None, causal=False, window=(-1, -1)):
     """E4M3 forward of packed bf16 q/k/v ([rows, H, 128]): quantised per
     (segment, head) into `workspace` (allocated when None), O in bf16 and
-    LSE.  Returns (out, lse, workspace)."""
+    LSE, optionally under a causal or sliding-window band.  Returns (out,
+    lse, workspace)."""
     total_q, H, D = q.shape
     total_k = k.shape[0]
     batch = cu_seqlens_q.numel() - 1
@@ -426,7 +444,7 @@ def attention_fwd_fp8(q, k, v, cu_seqlens_q, cu_seqlens_k, scale=None, out=None,
     if lse is None:
         lse = torch.empty(H, total_q, dtype=torch.float32, device=q.device)
     _check(varlen_attn_fwd_fp8(q, k, v, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, H, D, 0, 0, scale, out,
-                               lse, workspace, workspace.numel(), stream), "varlen_attn_fwd_fp8")
+                               lse, workspace, workspace.numel(), stream, causal, window), "varlen_attn_fwd_fp8")
     return out, lse, workspace
 
 

@@ -56,10 +56,11 @@ def run_cases(va) -> dict:
     lse = torch.full((2, w.total_q), 777.0, device=DEV)
     nb = va.varlen_attn_fwd_fp8_workspace_size(w.batch, w.total_q, w.total_k, 2, 128)
     ws = torch.empty(nb, dtype=torch.uint8, device=DEV)
-    st = va.varlen_attn_fwd_fp8(d.q, d.k, d.v, d.cu_q, d.cu_k, w.batch, w.total_q, w.total_k, 2, 128, w.max_q(),
-                                w.max_k(), w.softmax_scale, out, lse, ws, nb)
-    res["fp8"] = {"status": (st, va.varlen_attn_get_device_status()), "out": out.clone().cpu(),
-                  "lse": lse.clone().cpu()}
+    for mask, kwm in (("none", {}), ("causal", {"causal": True}), ("window", {"window": (40, 7)})):
+        st = va.varlen_attn_fwd_fp8(d.q, d.k, d.v, d.cu_q, d.cu_k, w.batch, w.total_q, w.total_k, 2, 128,
+                                    w.max_q(), w.max_k(), w.softmax_scale, out, lse, ws, nb, **kwm)
+        res["fp8" if mask == "none" else "fp8/" + mask] = {
+            "status": (st, va.varlen_attn_get_device_status()), "out": out.clone().cpu(), "lse": lse.clone().cpu()}
     # the checker's self test: extents 16 bytes short make the last accesses fail
     w = W.custom("slack", [70], [90], 2, 64)
     d = W.make_inputs(w, 0).to(DEV)

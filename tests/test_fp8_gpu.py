@@ -29,7 +29,7 @@ SQ = [300, 129, 517, 1, 5, 0, 40, 255, 256, 2, 700]
 SK = [300, 517, 129, 5, 1, 40, 0, 256, 255, 2, 130]
 
 
-def _run(w, cpu, scale=None):
+def _run(w, cpu, scale=None, causal=False, window=(-1, -1)):
     from packed_variable_length_varlen_gb300 import varlen_attn as va
     dev = cpu.to(DEV)
     H = w.num_heads
@@ -39,7 +39,7 @@ def _run(w, cpu, scale=None):
     ws = torch.full((nbytes,), 0x7F, dtype=torch.uint8, device=DEV)  # NaN codes: every used byte is written
     st = va.varlen_attn_fwd_fp8(dev.q, dev.k, dev.v, dev.cu_q, dev.cu_k, w.batch, w.total_q, w.total_k, H, 128,
                                 w.max_q(), w.max_k(), w.softmax_scale if scale is None else scale, out, lse, ws,
-                                nbytes)
+                                nbytes, causal=causal, window=window)
     assert st == 0, va.varlen_attn_status_string(st)
     st = va.varlen_attn_get_device_status()
     assert st == 0, va.varlen_attn_status_string(st)
@@ -92,6 +92,78 @@ def _check_codes(w, cpu, amax, q8, k8, vt):
         pad = -(-n // 128) * 128 - n
         assert bool((vt[:, :, base + n:base + n + pad] == 0).all()), b
     return q8r, k8r, v8r, qd, kd, vd
+
+
+def _check_forward(w, cpu, out, lse, codes, causal=False, window=(-1, -1), min_cos=0.998):
+    """O within the P-rounding bound of the oracle's FP8 forward (under the
+    same band), LSE within 1e-3, rows without keys exactly O = 0 and
+    LSE = -inf, and the fp64 forward on the bf16 inputs within the method's
+    cosine envelope."""
+    H = w.num_heads
+    q8r, k8r, v8r, qd, kd, vd = codes
+    band = dict(causal=causal, window=window)
+    rows, heads = oracle.all_pairs(w.total_q, H)
+    pf = oracle.Fp8Problem(q8r, k8r, v8r, w.cu_q, w.cu_k, w.softmax_scale, qd, kd, vd, quantize_p=True, **band)
+    o_ref, l_ref = pf.fwd(rows, heads)
+    pa = oracle.Fp8Problem(q8r, k8r, v8r & 0x7F, w.cu_q, w.cu_k, w.softmax_scale, qd, kd, vd, quantize_p=False,
+                           **band)
+    o_abs, _ = pa.fwd(rows, heads)
+    o_gpu = P.gather(out.cpu(), rows, heads)
+    l_gpu = lse.cpu().numpy()[heads, rows].astype(np.float64)
+    bound = 2.0 ** -3 * o_abs + 2.0 ** -8 * np.abs(o_ref) + 1e-3
+    excess = np.abs(o_gpu - o_ref) - bound
+    fin = np.isfinite(l_ref)
+    print("fp8 %s: max |dO| %.4g, max excess %.4g, %d rows without keys"
+          % (band, np.abs(o_gpu - o_ref).max(), excess.max(), int((~fin).sum())))
+    assert (excess <= 0).all()
+    assert np.array_equal(np.isneginf(l_gpu), ~fin)
+    assert np.abs(l_gpu[fin] - l_ref[fin]).max() <= 1e-3
+    assert np.all(o_gpu[~fin] == 0)
+    o64, _ = P.oracle_problem(cpu, **band).fwd(rows, heads)
+    cos = float((o_gpu * o64).sum() / np.linalg.norm(o_gpu) / np.linalg.norm(o64))
+    print("fp8 cosine vs fp64", cos)
+    assert cos >= min_cos
+    return int((~fin).sum())
+
+
+# Bands for the masked E4M3 forward: causal, windows whose edges cross key
+# tiles on one or both sides, the diagonal alone, and causal with a left
+# width (SQ / SK include segments with Sq > Sk, whose first causal rows see
+# no key).
+FP8_BANDS = [(True, (-1, -1)), (False, (200, 0)), (False, (0, 0)), (False, (130, 257)), (False, (-1, 40)),
+             (True, (300, -1))]
+
+
+@pytest.mark.parametrize("causal,window", FP8_BANDS, ids=["causal", "w200_0", "w0_0", "w130_257", "w-1_40",
+                                                          "causal_w300"])
+def test_fp8_masked_forward(causal, window):
+    """The E4M3 forward under a band: codes as unmasked (the quantisation
+    does not depend on the band), O / LSE against the oracle's masked FP8
+    forward."""
+    w = W.custom("fp8_masked", SQ, SK, 2, 128)
+    cpu = W.make_inputs(w, 2, with_dout=False)
+    out, lse, amax, q8, k8, vt = _run(w, cpu, causal=causal, window=window)
+    codes = _check_codes(w, cpu, amax, q8, k8, vt)
+    empty = _check_forward(w, cpu, out, lse, codes, causal=causal, window=window)
+    if causal:
+        assert empty > 0  # segments with Sq > Sk start with rows that see no key
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["unmasked", "causal"])
+def test_fp8_tiny_descales(causal):
+    """Q and K of magnitude ~1e-22, so that scale * log2(e) * qd * kd rounds
+    to 0 in fp32: the scores are ~0, P is 1 for every visible key, and the
+    keys past a segment's end (or outside the band) must still count as
+    -inf, not NaN."""
+    w = W.custom("fp8_tiny", [300, 129, 40], [300, 517, 5], 2, 128)
+    cpu = W.make_inputs(w, 6, with_dout=False)
+    cpu.q.mul_(1e-22)
+    cpu.k.mul_(1e-22)
+    out, lse, amax, q8, k8, vt = _run(w, cpu, causal=causal)
+    codes = _check_codes(w, cpu, amax, q8, k8, vt)
+    assert float(codes[3].max()) * float(codes[4].max()) * w.softmax_scale * 1.4427 < 2.0 ** -150
+    assert bool(torch.isfinite(out.float()).all())
+    _check_forward(w, cpu, out, lse, codes, causal=causal)
 
 
 @pytest.mark.parametrize("seed", [0, 1])
@@ -220,12 +292,23 @@ def test_fp8_windowed_full_size_sampled():
     assert cos >= 0.998
 
 
-def test_fp8_python_wrapper_matches_raw_call():
-    """attention_fwd_fp8 (argument marshalling only) returns the raw call's bits."""
+@pytest.mark.parametrize("causal,window", [(False, (-1, -1)), (True, (-1, -1)), (False, (64, 0))],
+                         ids=["unmasked", "causal", "window"])
+def test_fp8_python_wrapper_matches_raw_call(causal, window):
+    """attention_fwd_fp8 (argument marshalling only) returns the raw call's
+    bits; the window form with (-1, -1) is the unmasked call."""
     from packed_variable_length_varlen_gb300 import varlen_attn as va
     w = W.custom("fp8_wrap", [200, 3, 129], [150, 300, 1], 2, 128)
     cpu = W.make_inputs(w, 4, with_dout=False)
-    out, lse, *_ = _run(w, cpu)
+    out, lse, *_ = _run(w, cpu, causal=causal, window=window)
     dev = cpu.to(DEV)
-    o2, l2, ws = va.attention_fwd_fp8(dev.q, dev.k, dev.v, dev.cu_q, dev.cu_k, w.softmax_scale)
+    o2, l2, ws = va.attention_fwd_fp8(dev.q, dev.k, dev.v, dev.cu_q, dev.cu_k, w.softmax_scale, causal=causal,
+                                      window=window)
     assert torch.equal(o2.cpu(), out.cpu()) and torch.equal(l2.cpu(), lse.cpu())
+    if not causal and window == (-1, -1):
+        o3 = torch.empty_like(out)
+        l3 = torch.empty_like(lse)
+        st = va.varlen_attn_fwd_fp8_window(dev.q, dev.k, dev.v, dev.cu_q, dev.cu_k, w.batch, w.total_q, w.total_k,
+                                           2, 128, 0, 0, w.softmax_scale, -1, -1, o3, l3, ws, ws.numel())
+        assert st == 0
+        assert torch.equal(o3.cpu(), out.cpu()) and torch.equal(l3.cpu(), lse.cpu())

@@ -279,6 +279,15 @@ def test_fp8_workspace_layout_and_validation(va):
     assert fwd(nbytes=need - 1) == va.VARLEN_ERR_WORKSPACE
     assert fwd(ws=0x10010) == va.VARLEN_ERR_WORKSPACE
     assert fwd() in (va.VARLEN_ERR_CUDA, va.VARLEN_ERR_ARCH)
+    # the window form: the same checks, then the same device query
+    win = lambda D=128, ws=0x10000, nbytes=need, cu=0x2000, band=(-1, 0): va.varlen_attn_fwd_fp8_window(
+        q, q, q, _P(cu), _P(0x2000), 1, 10, 10, H, D, 0, 0, 0.1, *band, q, _P(0x3000), _P(ws), nbytes, 0)
+    assert win(D=96) == va.VARLEN_ERR_HEAD_DIM
+    assert win(cu=0) == va.VARLEN_ERR_NULL
+    assert win(nbytes=need - 1) == va.VARLEN_ERR_WORKSPACE
+    assert win(ws=0x10008) == va.VARLEN_ERR_WORKSPACE
+    for band in ((-1, 0), (4, 0), (0, 0), (-1, -1), (3, 7)):
+        assert win(band=band) in (va.VARLEN_ERR_CUDA, va.VARLEN_ERR_ARCH)
 
 
 def test_prep_roofline_arithmetic():
