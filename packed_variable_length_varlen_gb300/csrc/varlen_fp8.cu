@@ -639,14 +639,20 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_after();
         float x[128];
         {
-          uint32_t s[32];
+          // the four 32-column loads in flight together, one wait
+          uint32_t s[128];
+          uint32_t(&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[0]);
+          uint32_t(&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[32]);
+          uint32_t(&s2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[64]);
+          uint32_t(&s3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[96]);
+          const uint32_t ta = tmem + lane_off + s_col;
+          tmem_ld32(ta + 0, s0);
+          tmem_ld32(ta + 32, s1);
+          tmem_ld32(ta + 64, s2);
+          tmem_ld32(ta + 96, s3);
+          tmem_wait_ld();
 #pragma unroll
-          for (int c0 = 0; c0 < 128; c0 += 32) {
-            tmem_ld32(tmem + lane_off + s_col + c0, s);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) x[c0 + i] = __uint_as_float(s[i]);
-          }
+          for (int i = 0; i < 128; ++i) x[i] = __uint_as_float(s[i]);
         }
         // keys the row does not see (past the segment end, or outside the
         // mask's band) are -inf, by select
