@@ -239,20 +239,22 @@ def test_fp8_codes_every_bf16_value(maxima):
 
 
 @pytest.mark.slow
-def test_fp8_windowed_full_size_sampled():
+@pytest.mark.parametrize("causal", [False, True], ids=["unmasked", "causal"])
+def test_fp8_windowed_full_size_sampled(causal):
     """The E4M3 forward on the windowed workload (8 segments, H=56, D=128, the
-    size the benchmark times).  Per segment b one head h_b: the oracle
-    quantises that (segment, head) block on its own (its descale depends on
-    nothing else), the block's amax and Q, K and transposed V codes must equal
-    the kernel's bit for bit, and 512 sampled rows of it (4096 in all) must
-    match the oracle's FP8 forward within the P-rounding bound, LSE within
+    size the benchmark times), unmasked and causal.  Per segment b one head
+    h_b: the oracle quantises that (segment, head) block on its own (its
+    descale depends on nothing else), the block's amax and Q, K and
+    transposed V codes must equal the kernel's bit for bit, and 512 sampled
+    rows of it (4096 in all) must match the oracle's FP8 forward (under the
+    same band, which is per segment) within the P-rounding bound, LSE within
     1e-3, and the fp64 forward on the bf16 inputs with cosine >= 0.998."""
     w = W.windowed()
     H = w.num_heads
     cpu = W.make_inputs(w, 0, with_dout=False)
-    out, lse, amax, q8, k8, vt = _run(w, cpu)
+    out, lse, amax, q8, k8, vt = _run(w, cpu, causal=causal)
     out_c, lse_c = out.cpu(), lse.cpu().numpy()
-    pb64 = P.oracle_problem(cpu)
+    pb64 = P.oracle_problem(cpu, causal=causal)
     rng = np.random.default_rng(7)
     all_gpu, all_64 = [], []
     for b in range(w.batch):
@@ -271,10 +273,11 @@ def test_fp8_windowed_full_size_sampled():
         assert torch.equal(vt[h, :, base:base + (k1 - k0)], codes[2][:, 0].T), (b, h)
         rows = np.sort(np.concatenate([1 + rng.choice(q1 - q0 - 2, 510, replace=False), [0, q1 - q0 - 1]]))
         zeros = np.zeros(rows.size, dtype=np.int64)
-        pf = oracle.Fp8Problem(*codes, [0, q1 - q0], [0, k1 - k0], w.softmax_scale, *desc, quantize_p=True)
+        pf = oracle.Fp8Problem(*codes, [0, q1 - q0], [0, k1 - k0], w.softmax_scale, *desc, quantize_p=True,
+                               causal=causal)
         o_ref, l_ref = pf.fwd(rows, zeros)
         pa = oracle.Fp8Problem(codes[0], codes[1], codes[2] & 0x7F, [0, q1 - q0], [0, k1 - k0], w.softmax_scale,
-                               *desc, quantize_p=False)
+                               *desc, quantize_p=False, causal=causal)
         o_abs, _ = pa.fwd(rows, zeros)
         grow, gh = q0 + rows, np.full(rows.size, h)
         o_gpu = P.gather(out_c, grow, gh)
@@ -282,13 +285,14 @@ def test_fp8_windowed_full_size_sampled():
         excess = np.abs(o_gpu - o_ref) - (2.0 ** -3 * o_abs + 2.0 ** -8 * np.abs(o_ref) + 1e-3)
         assert (excess <= 0).all(), (b, h, excess.max())
         assert np.abs(l_gpu - l_ref).max() <= 1e-3, (b, h)
-        o64 = P.oracle_rows(pb64, w, grow, gh)[0]
+        # the matrix-product path covers unmasked problems; the band takes the row-by-row oracle
+        o64 = pb64.fwd(grow, gh)[0] if causal else P.oracle_rows(pb64, w, grow, gh)[0]
         all_gpu.append(o_gpu)
         all_64.append(o64)
     o_gpu, o64 = np.concatenate(all_gpu), np.concatenate(all_64)
     assert o_gpu.shape[0] >= 4096
     cos = float((o_gpu * o64).sum() / np.linalg.norm(o_gpu) / np.linalg.norm(o64))
-    print("fp8 full size: %d rows, cosine vs fp64 %.6f" % (o_gpu.shape[0], cos))
+    print("fp8 full size (causal=%s): %d rows, cosine vs fp64 %.6f" % (causal, o_gpu.shape[0], cos))
     assert cos >= 0.998
 
 
