@@ -212,7 +212,8 @@ __host__ __device__ __forceinline__ int64_t pad_base(int32_t o0, int32_t b) {
 // ------------------------------------------------------------------ FP8
 
 // The E4M3 forward: bf16 operands quantised per (segment, head) into a
-// workspace, then attention on the codes.  Head size 128, no mask.
+// workspace, then attention on the codes.  Head size 128, unmasked or under
+// a band (masked, win_left, win_right as in FwdParams).
 struct Fp8Params {
   const __nv_bfloat16 *q, *k, *v;
   int64_t q_rs, q_hs, k_rs, k_hs, v_rs, v_hs;
