@@ -11,9 +11,14 @@ oracle's FP8 reading:
   O; LSE within 1e-3 (P's rounding does not enter it);
 * against the fp64 oracle on the bf16 inputs, cosine >= 0.998 (the method's
   own envelope);
-* at full size (the windowed workload, H=56), one head per segment: the
-  segment's amax and codes bit for bit, and O / LSE on 4096 sampled rows
-  spanning every segment."""
+* under causal and sliding-window bands (varlen_attn_fwd_fp8_window), the
+  same bounds against the oracle's masked FP8 forward, rows that see no key
+  exactly O = 0 and LSE = -inf;
+* Q and K small enough (~1e-22) that scale * qd * kd underflows fp32: finite
+  results within the same bounds;
+* at full size (the windowed workload, H=56), unmasked and causal, one head
+  per segment: the segment's amax and codes bit for bit, and O / LSE on
+  4096 sampled rows spanning every segment."""
 import numpy as np
 import pytest
 import torch
