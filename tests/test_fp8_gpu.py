@@ -18,7 +18,8 @@ oracle's FP8 reading:
   results within the same bounds;
 * at full size (the windowed workload, H=56), unmasked and causal, one head
   per segment: the segment's amax and codes bit for bit, and O / LSE on
-  4096 sampled rows spanning every segment."""
+  4096 sampled rows spanning every segment; on the long-sequence workload
+  (one 77000-row segment) the same for four heads on 2048 rows."""
 import numpy as np
 import pytest
 import torch
@@ -298,6 +299,55 @@ def test_fp8_windowed_full_size_sampled(causal):
     assert o_gpu.shape[0] >= 4096
     cos = float((o_gpu * o64).sum() / np.linalg.norm(o_gpu) / np.linalg.norm(o64))
     print("fp8 full size (causal=%s): %d rows, cosine vs fp64 %.6f" % (causal, o_gpu.shape[0], cos))
+    assert cos >= 0.998
+
+
+@pytest.mark.slow
+def test_fp8_long_full_size_sampled():
+    """The E4M3 forward on the long-sequence workload: one 77000-row segment,
+    H=56, D=128, the size at which the ffpa-attn NVFP4 launcher aborted
+    ("Minimal reproduction").  For four heads: amax and the Q, K and
+    transposed V codes of the head's block bit for bit (code 0 past the
+    segment end), and 512 sampled rows each (2048 in all; the oracle decodes
+    every key's codes per row, about 35 ms a row on one core) within the
+    P-rounding bound of the oracle's FP8 forward, LSE within 1e-3, and the
+    fp64 forward on the bf16 inputs with cosine >= 0.998."""
+    w = W.long_dense()
+    H, n = w.num_heads, w.total_q
+    cpu = W.make_inputs(w, 0, with_dout=False)
+    out, lse, amax, q8, k8, vt = _run(w, cpu)
+    out_c, lse_c = out.cpu(), lse.cpu().numpy()
+    pb64 = P.oracle_problem(cpu)
+    rng = np.random.default_rng(9)
+    all_gpu, all_64 = [], []
+    for h in (0, 19, 38, 55):
+        codes, desc = [], []
+        for i, x in enumerate((cpu.q[:, h:h + 1], cpu.k[:, h:h + 1], cpu.v[:, h:h + 1])):
+            assert np.float32(amax[i][h]) == np.float32(x.float().abs().max()), (h, i)
+            c, d = oracle.quantize_e4m3(x, [0, n])
+            codes.append(c)
+            desc.append(d)
+        assert torch.equal(q8[:, h], codes[0][:, 0]), h
+        assert torch.equal(k8[:, h], codes[1][:, 0]), h
+        assert torch.equal(vt[h, :, :n], codes[2][:, 0].T), h
+        assert bool((vt[h, :, n:-(-n // 128) * 128] == 0).all()), h
+        rows = np.sort(np.concatenate([1 + rng.choice(n - 2, 510, replace=False), [0, n - 1]]))
+        zeros = np.zeros(rows.size, dtype=np.int64)
+        o_ref, l_ref = oracle.Fp8Problem(*codes, [0, n], [0, n], w.softmax_scale, *desc,
+                                         quantize_p=True).fwd(rows, zeros)
+        o_abs, _ = oracle.Fp8Problem(codes[0], codes[1], codes[2] & 0x7F, [0, n], [0, n], w.softmax_scale, *desc,
+                                     quantize_p=False).fwd(rows, zeros)
+        gh = np.full(rows.size, h)
+        o_gpu = P.gather(out_c, rows, gh)
+        l_gpu = lse_c[gh, rows].astype(np.float64)
+        excess = np.abs(o_gpu - o_ref) - (2.0 ** -3 * o_abs + 2.0 ** -8 * np.abs(o_ref) + 1e-3)
+        assert (excess <= 0).all(), (h, excess.max())
+        assert np.abs(l_gpu - l_ref).max() <= 1e-3, h
+        all_gpu.append(o_gpu)
+        all_64.append(P.oracle_rows(pb64, w, rows, gh)[0])
+    o_gpu, o64 = np.concatenate(all_gpu), np.concatenate(all_64)
+    cos = float((o_gpu * o64).sum() / np.linalg.norm(o_gpu) / np.linalg.norm(o64))
+    print("fp8 long: %d rows, cosine vs fp64 %.6f" % (o_gpu.shape[0], cos))
     assert cos >= 0.998
 
 
