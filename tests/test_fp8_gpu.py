@@ -156,6 +156,20 @@ def test_fp8_masked_forward(causal, window):
 
 
 @pytest.mark.parametrize("causal", [False, True], ids=["unmasked", "causal"])
+def test_fp8_padded_rows(causal):
+    """Inputs and output with rows padded past H * D (NaN in the inputs'
+    padding, a canary in the output's): the quantiser reads only each row's
+    H * D elements, the codes and O / LSE match the oracle as for packed
+    rows, and the output's padding is untouched."""
+    w = W.custom("fp8_padded", SQ[:7], SK[:7], 2, 128, row_pad=64)
+    cpu = W.make_inputs(w, 8, with_dout=False)
+    assert cpu.q._base is not None and bool(torch.isnan(cpu.q._base[:, 256:]).all())
+    out, lse, amax, q8, k8, vt = _run(w, cpu, causal=causal)
+    codes = _check_codes(w, cpu, amax, q8, k8, vt)
+    _check_forward(w, cpu, out, lse, codes, causal=causal)
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["unmasked", "causal"])
 def test_fp8_tiny_descales(causal):
     """Q and K of magnitude ~1e-22, so that scale * log2(e) * qd * kd rounds
     to 0 in fp32: the scores are ~0, P is 1 for every visible key, and the
