@@ -658,10 +658,24 @@ def fp8_forward(args, w, ws, rank, local):
     wsp = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    if args.dense:
+        sq_, sk_ = w.seqlens_q(), w.seqlens_k()
+        if len(set(sq_)) != 1 or len(set(sk_)) != 1 or window != (-1, -1):
+            raise SystemExit("--fp8 --dense needs equal segment lengths (e.g. --workload dense) and no --window")
+        Sq, Sk = sq_[0], sk_[0]
+
+        def as4(t, S):  # the [batch, S, H, D] view of a packed [batch*S, H, D] tensor
+            return t.as_strided((w.batch, S, H, 128), (S * t.stride(0), t.stride(0), t.stride(1), 1),
+                                t.storage_offset())
+
     def run():
-        st = va.varlen_attn_fwd_fp8(d.q, d.k, d.v, d.cu_q, d.cu_k, w.batch, w.total_q, w.total_k, H, 128,
-                                    w.max_q(), w.max_k(), w.softmax_scale, out, lse, wsp, nbytes, stream,
-                                    causal=causal, window=window)
+        if args.dense:
+            st = va.varlen_attn_fwd_fp8_dense(as4(d.q, Sq), as4(d.k, Sk), as4(d.v, Sk), w.batch, Sq, Sk, H, 128,
+                                              w.softmax_scale, causal, as4(out, Sq), lse, wsp, nbytes, stream)
+        else:
+            st = va.varlen_attn_fwd_fp8(d.q, d.k, d.v, d.cu_q, d.cu_k, w.batch, w.total_q, w.total_k, H, 128,
+                                        w.max_q(), w.max_k(), w.softmax_scale, out, lse, wsp, nbytes, stream,
+                                        causal=causal, window=window)
         assert st == 0, va.varlen_attn_status_string(st)
 
     for _ in range(args.warmup):
@@ -686,6 +700,7 @@ def fp8_forward(args, w, ws, rank, local):
                           "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate)",
                           "data": "synthetic", "config": {"workload": w.name, "num_heads": H, "head_dim": 128,
                                                           "step": "fp8 fwd", "causal": causal, "window": list(window),
+                                                          "entry": "dense batched" if args.dense else "packed varlen",
                                                           "l2": "inputs larger than L2 (k, v 2 GB each); no flush"},
                           "gpu_launches": 4 * args.steps}),
               flush=True)

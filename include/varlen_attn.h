@@ -273,6 +273,26 @@ int varlen_attn_bwd_dense(const void* q, varlen_dense_stride sq, const void* k, 
                           void* dv, varlen_dense_stride sdv, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * E4M3 forward in the dense batched layout of varlen_attn_fwd_dense
+ * ([batch, seqlen, H, 128] tensors with {batch, row, head} strides, batch
+ * stride = seqlen row strides, causal 0 or 1; the same checks and status
+ * codes): the result of varlen_attn_fwd_fp8 (causal: varlen_attn_fwd_fp8_window
+ * with (-1, 0)) on cu_seqlens = [0, S, 2S, ...] over the same rows, segment
+ * bounds computed on the device.  The workspace holds
+ * varlen_attn_fwd_fp8_dense_workspace_size(batch, seqlen_q, seqlen_k, H, 128)
+ * bytes (0 for a size that does not fit) and has the layout
+ * varlen_attn_fwd_fp8_workspace_layout gives for batch, batch * seqlen_q and
+ * batch * seqlen_k.
+ */
+size_t varlen_attn_fwd_fp8_dense_workspace_size(int32_t batch, int32_t seqlen_q, int32_t seqlen_k, int32_t num_heads,
+                                                int32_t head_dim);
+int varlen_attn_fwd_fp8_dense(const void* q, varlen_dense_stride sq, const void* k, varlen_dense_stride sk,
+                              const void* v, varlen_dense_stride sv, int32_t batch, int32_t seqlen_q,
+                              int32_t seqlen_k, int32_t num_heads, int32_t head_dim, float scale, int32_t causal,
+                              void* out, varlen_dense_stride so, float* lse, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/*
  * Backward without a workspace argument, for callers that cannot allocate
  * device memory (code inside a host framework that owns every device
  * allocation, or on a path where cudaMalloc is not allowed).  The attention

@@ -663,11 +663,12 @@ extern "C" int varlen_attn_fwd_fp8_workspace_layout(int32_t batch, int32_t total
 
 namespace {
 
+// The E4M3 forward on segments given by cu_seqlens arrays, or (dense) by
+// uniform lengths (CuView with a null pointer).
 int fwd_fp8_impl(const void* q, varlen_stride sq, const void* k, varlen_stride sk, const void* v, varlen_stride sv,
-                 const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t batch, int32_t total_q,
-                 int32_t total_k, int32_t num_heads, int32_t head_dim, float scale, void* out, varlen_stride so,
-                 float* lse, void* workspace, size_t workspace_bytes, void* stream, Band band) {
-  if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr) return VARLEN_ERR_NULL;
+                 CuView cu_q, CuView cu_k, int32_t batch, int32_t total_q, int32_t total_k, int32_t num_heads,
+                 int32_t head_dim, float scale, void* out, varlen_stride so, float* lse, void* workspace,
+                 size_t workspace_bytes, void* stream, Band band) {
   int st = check_common(batch, total_q, total_k, num_heads, head_dim, scale);
   if (st != VARLEN_OK) return st;
   if (head_dim != 128) return VARLEN_ERR_HEAD_DIM;
@@ -705,8 +706,8 @@ int fwd_fp8_impl(const void* q, varlen_stride sq, const void* k, varlen_stride s
   L.p.k8 = reinterpret_cast<uint8_t*>(ws + off[2]);
   L.p.vt = reinterpret_cast<uint8_t*>(ws + off[3]);
   L.p.kp = fp8_vt_cols(batch, total_k);
-  L.p.cu_q = CuView{cu_seqlens_q, 0};
-  L.p.cu_k = CuView{cu_seqlens_k, 0};
+  L.p.cu_q = cu_q;
+  L.p.cu_k = cu_k;
   L.p.batch = batch;
   L.p.total_q = total_q;
   L.p.total_k = total_k;
@@ -743,8 +744,9 @@ extern "C" int varlen_attn_fwd_fp8(const void* q, varlen_stride sq, const void* 
                                    size_t workspace_bytes, void* stream) {
   (void)max_seqlen_q;
   (void)max_seqlen_k;
-  return fwd_fp8_impl(q, sq, k, sk, v, sv, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads, head_dim,
-                      scale, out, so, lse, workspace, workspace_bytes, stream, kNoMask);
+  if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr) return VARLEN_ERR_NULL;
+  return fwd_fp8_impl(q, sq, k, sk, v, sv, CuView{cu_seqlens_q, 0}, CuView{cu_seqlens_k, 0}, batch, total_q, total_k,
+                      num_heads, head_dim, scale, out, so, lse, workspace, workspace_bytes, stream, kNoMask);
 }
 
 extern "C" int varlen_attn_fwd_fp8_window(const void* q, varlen_stride sq, const void* k, varlen_stride sk,
@@ -756,8 +758,36 @@ extern "C" int varlen_attn_fwd_fp8_window(const void* q, varlen_stride sq, const
                                           float* lse, void* workspace, size_t workspace_bytes, void* stream) {
   (void)max_seqlen_q;
   (void)max_seqlen_k;
-  return fwd_fp8_impl(q, sq, k, sk, v, sv, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads, head_dim,
-                      scale, out, so, lse, workspace, workspace_bytes, stream, band_of(window_left, window_right));
+  if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr) return VARLEN_ERR_NULL;
+  return fwd_fp8_impl(q, sq, k, sk, v, sv, CuView{cu_seqlens_q, 0}, CuView{cu_seqlens_k, 0}, batch, total_q, total_k,
+                      num_heads, head_dim, scale, out, so, lse, workspace, workspace_bytes, stream,
+                      band_of(window_left, window_right));
+}
+
+extern "C" size_t varlen_attn_fwd_fp8_dense_workspace_size(int32_t batch, int32_t seqlen_q, int32_t seqlen_k,
+                                                           int32_t num_heads, int32_t head_dim) {
+  if (batch < 0 || seqlen_q < 0 || seqlen_k < 0) return 0;
+  const int64_t tq = (int64_t)batch * seqlen_q, tk = (int64_t)batch * seqlen_k;
+  if (tq > INT32_MAX || tk > INT32_MAX) return 0;
+  return varlen_attn_fwd_fp8_workspace_size(batch, (int32_t)tq, (int32_t)tk, num_heads, head_dim);
+}
+
+extern "C" int varlen_attn_fwd_fp8_dense(const void* q, varlen_dense_stride sq, const void* k, varlen_dense_stride sk,
+                                         const void* v, varlen_dense_stride sv, int32_t batch, int32_t seqlen_q,
+                                         int32_t seqlen_k, int32_t num_heads, int32_t head_dim, float scale,
+                                         int32_t causal, void* out, varlen_dense_stride so, float* lse,
+                                         void* workspace, size_t workspace_bytes, void* stream) {
+  int32_t total_q = 0, total_k = 0;
+  int st = dense_shape(batch, seqlen_q, seqlen_k, causal, &total_q, &total_k);
+  if (st != VARLEN_OK) return st;
+  varlen_stride vq, vk, vv, vo;
+  if ((st = dense_view(sq, seqlen_q, batch, &vq)) != VARLEN_OK) return st;
+  if ((st = dense_view(sk, seqlen_k, batch, &vk)) != VARLEN_OK) return st;
+  if ((st = dense_view(sv, seqlen_k, batch, &vv)) != VARLEN_OK) return st;
+  if ((st = dense_view(so, seqlen_q, batch, &vo)) != VARLEN_OK) return st;
+  return fwd_fp8_impl(q, vq, k, vk, v, vv, CuView{nullptr, seqlen_q}, CuView{nullptr, seqlen_k}, batch, total_q,
+                      total_k, num_heads, head_dim, scale, out, vo, lse, workspace, workspace_bytes, stream,
+                      causal ? kCausal : kNoMask);
 }
 
 extern "C" int varlen_attn_get_device_status(void* stream) {

@@ -89,6 +89,11 @@ def _load() -> ctypes.CDLL:
     lib.varlen_attn_fwd_fp8_window.argtypes = [vp, S, vp, S, vp, S, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32,
                                                i32, i32, vp, S, vp, vp, sz, vp]
     DS = VarlenDenseStride
+    lib.varlen_attn_fwd_fp8_dense_workspace_size.restype = sz
+    lib.varlen_attn_fwd_fp8_dense_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+    lib.varlen_attn_fwd_fp8_dense.restype = ctypes.c_int
+    lib.varlen_attn_fwd_fp8_dense.argtypes = [vp, DS, vp, DS, vp, DS, i32, i32, i32, i32, i32, f32, i32, vp, DS, vp,
+                                              vp, sz, vp]
     lib.varlen_attn_fwd_dense.restype = ctypes.c_int
     lib.varlen_attn_fwd_dense.argtypes = [vp, DS, vp, DS, vp, DS, i32, i32, i32, i32, i32, f32, i32, vp, DS, vp, vp]
     lib.varlen_attn_bwd_dense_workspace_size.restype = sz
@@ -142,7 +147,8 @@ EXPORTED = ("varlen_attn_fwd", "varlen_attn_bwd_workspace_size", "varlen_attn_bw
             "varlen_attn_bwd_window", "varlen_attn_bwd_deterministic", "varlen_attn_fwd_fp8_workspace_size",
             "varlen_attn_fwd_fp8_workspace_layout", "varlen_attn_fwd_fp8", "varlen_attn_bwd_noalloc_scratch_bytes",
             "varlen_attn_debug_noalloc_scratch", "varlen_attn_bounds_checked", "varlen_attn_debug_set_span_slack",
-            "varlen_attn_debug_skip_load", "varlen_attn_debug_mma_cycles", "varlen_attn_fwd_fp8_window")
+            "varlen_attn_debug_skip_load", "varlen_attn_debug_mma_cycles", "varlen_attn_fwd_fp8_window",
+            "varlen_attn_fwd_fp8_dense_workspace_size", "varlen_attn_fwd_fp8_dense")
 
 # Size of the fixed device array varlen_attn_bwd_noalloc uses as scratch, as
 # compiled into the library.
@@ -294,6 +300,18 @@ def varlen_attn_fwd_fp8_window(q, k, v, cu_seqlens_q, cu_seqlens_k, batch, total
                                           head_dim, max_seqlen_q, max_seqlen_k, scale, window_left, window_right,
                                           _ptr(out), _stride(out), _ptr(lse), _ptr(workspace), workspace_bytes,
                                           _stream(stream))
+
+
+def varlen_attn_fwd_fp8_dense_workspace_size(batch, seqlen_q, seqlen_k, num_heads, head_dim) -> int:
+    return int(LIB.varlen_attn_fwd_fp8_dense_workspace_size(batch, seqlen_q, seqlen_k, num_heads, head_dim))
+
+
+def varlen_attn_fwd_fp8_dense(q, k, v, batch, seqlen_q, seqlen_k, num_heads, head_dim, scale, causal, out, lse,
+                              workspace, workspace_bytes, stream=None) -> int:
+    return LIB.varlen_attn_fwd_fp8_dense(_ptr(q), _dstride(q), _ptr(k), _dstride(k), _ptr(v), _dstride(v), batch,
+                                         seqlen_q, seqlen_k, num_heads, head_dim, scale, int(bool(causal)), _ptr(out),
+                                         _dstride(out), _ptr(lse), _ptr(workspace), workspace_bytes,
+                                         _stream(stream))
 
 
 def varlen_attn_fwd_dense(q, k, v, batch, seqlen_q, seqlen_k, num_heads, head_dim, scale, causal, out, lse,
@@ -480,6 +498,25 @@ def attention_fwd_dense(q, k, v, scale=None, causal=False, out=None, lse=None, s
         lse = torch.empty(H, B * Sq, dtype=torch.float32, device=q.device)
     _check(varlen_attn_fwd_dense(q, k, v, B, Sq, Sk, H, D, scale, causal, out, lse, stream), "varlen_attn_fwd_dense")
     return out, lse
+
+
+def attention_fwd_fp8_dense(q, k, v, scale=None, causal=False, out=None, lse=None, workspace=None, stream=None):
+    """E4M3 forward of dense batched bf16 q [B, Sq, H, 128], k / v
+    [B, Sk, H, 128]: quantised per (batch entry, head) into `workspace`
+    (allocated when None); returns (out, lse [H, B * Sq], workspace)."""
+    B, Sq, H, D = q.shape
+    Sk = k.shape[1]
+    scale = float(D ** -0.5) if scale is None else float(scale)
+    nbytes = varlen_attn_fwd_fp8_dense_workspace_size(B, Sq, Sk, H, D)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q, memory_format=torch.contiguous_format)
+    if lse is None:
+        lse = torch.empty(H, B * Sq, dtype=torch.float32, device=q.device)
+    _check(varlen_attn_fwd_fp8_dense(q, k, v, B, Sq, Sk, H, D, scale, causal, out, lse, workspace,
+                                     workspace.numel(), stream), "varlen_attn_fwd_fp8_dense")
+    return out, lse, workspace
 
 
 def attention_bwd_dense(q, k, v, out, dout, lse, scale=None, causal=False, dq=None, dk=None, dv=None,

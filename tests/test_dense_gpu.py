@@ -81,3 +81,28 @@ def test_dense_bit_identical_to_packed():
     assert torch.equal(out_d.reshape(B * Sq, H, D), out_p) and torch.equal(lse_d, lse_p)
     assert torch.equal(dk_d.reshape(B * Sk, H, D), dk_p) and torch.equal(dv_d.reshape(B * Sk, H, D), dv_p)
     assert (dq_d.reshape(B * Sq, H, D).float() - dq_p.float()).abs().max().item() < 1e-2
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["unmasked", "causal"])
+def test_fp8_dense_matches_packed_fp8(causal):
+    """varlen_attn_fwd_fp8_dense on [B, S, H, 128] (padded rows) returns the
+    packed E4M3 call's bits on cu_seqlens = {0, S, 2S, ...} over the same
+    memory (same kernels, segment bounds computed on the device), codes
+    included; the packed E4M3 call is checked against the oracle in
+    tests/test_fp8_gpu.py."""
+    from packed_variable_length_varlen_gb300 import varlen_attn as va
+    B, Sq, Sk, H, D = 3, 200, 333, 2, 128
+    q, k, v = _dense(B, Sq, H, D, 11), _dense(B, Sk, H, D, 12), _dense(B, Sk, H, D, 13)
+    qd, kd, vd = (_dev(t) for t in (q, k, v))
+    out, lse, ws = va.attention_fwd_fp8_dense(qd, kd, vd, causal=causal)
+    assert va.varlen_attn_get_device_status() == 0
+    assert ws.numel() >= va.varlen_attn_fwd_fp8_dense_workspace_size(B, Sq, Sk, H, D) > 0
+    cu_q = torch.tensor([b * Sq for b in range(B + 1)], dtype=torch.int32, device=DEV)
+    cu_k = torch.tensor([b * Sk for b in range(B + 1)], dtype=torch.int32, device=DEV)
+    o2, l2, ws2 = va.attention_fwd_fp8(_packed(qd), _packed(kd), _packed(vd), cu_q, cu_k, causal=causal)
+    assert va.varlen_attn_get_device_status() == 0
+    assert torch.equal(out.reshape(B * Sq, H, D).cpu(), o2.cpu())
+    assert torch.equal(lse.cpu(), l2.cpu())
+    n = va.varlen_attn_fwd_fp8_workspace_size(B, B * Sq, B * Sk, H, D)
+    assert torch.equal(ws[:n].cpu(), ws2[:n].cpu())
+    assert bool(torch.isfinite(out.float()).all())

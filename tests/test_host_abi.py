@@ -187,6 +187,31 @@ def test_dense_validation_codes(va):
     assert fwd() in (va.VARLEN_ERR_CUDA, va.VARLEN_ERR_ARCH)
     assert va.varlen_attn_bwd_dense_workspace_size(B, Sq, H, D) == va.varlen_attn_bwd_workspace_size(B, B * Sq, H, D)
     assert va.varlen_attn_bwd_dense_workspace_size(2 ** 16, 2 ** 16, H, D) == 0
+    # the dense E4M3 forward: the same layout checks, head size 128, its workspace that of the packed call
+    q8 = _Fake4(0x1000, Sq * H * 128, H * 128, 128)
+    k8 = _Fake4(0x1000, Sk * H * 128, H * 128, 128)
+    nb = va.varlen_attn_fwd_fp8_dense_workspace_size(B, Sq, Sk, H, 128)
+    assert nb == va.varlen_attn_fwd_fp8_workspace_size(B, B * Sq, B * Sk, H, 128) > 0
+    assert va.varlen_attn_fwd_fp8_dense_workspace_size(2 ** 16, 2 ** 16, 1, H, 128) == 0
+    assert va.varlen_attn_fwd_fp8_dense_workspace_size(B, Sq, Sk, H, 64) == 0
+
+    def fwd8(q=q8, k=k8, D=128, causal=0, B=B, Sq=Sq, nbytes=nb, ws=0x10000):
+        return va.varlen_attn_fwd_fp8_dense(q, k, k, B, Sq, Sk, H, D, 0.125, causal, q, _P(0x3000), _P(ws), nbytes,
+                                            0)
+
+    assert fwd8(q=_Fake4(0x1000, Sq * H * 128 + 16, H * 128, 128)) == va.VARLEN_ERR_STRIDE
+    assert fwd8(D=64, q=_Fake4(0x1000, Sq * H * 64, H * 64, 64), k=_Fake4(0x1000, Sk * H * 64, H * 64, 64)) \
+        == va.VARLEN_ERR_HEAD_DIM
+    assert fwd8(B=2 ** 16, Sq=2 ** 16) == va.VARLEN_ERR_SHAPE
+    assert fwd8(nbytes=nb - 1) == va.VARLEN_ERR_WORKSPACE
+    assert fwd8(ws=0x10010) == va.VARLEN_ERR_WORKSPACE
+    for causal in (0, 1):
+        assert fwd8(causal=causal) in (va.VARLEN_ERR_CUDA, va.VARLEN_ERR_ARCH)
+    assert va.LIB.varlen_attn_fwd_fp8_dense(0x1000, va.VarlenDenseStride(Sq * H * 128, H * 128, 128), 0x1000,
+                                            va.VarlenDenseStride(Sk * H * 128, H * 128, 128), 0x1000,
+                                            va.VarlenDenseStride(Sk * H * 128, H * 128, 128), B, Sq, Sk, H, 128,
+                                            0.125, 2, 0x1000, va.VarlenDenseStride(Sq * H * 128, H * 128, 128),
+                                            0x3000, 0x10000, nb, None) == va.VARLEN_ERR_SHAPE
 
 
 def test_visible_pairs_band_by_brute_force():
