@@ -61,6 +61,23 @@ def run_cases(va) -> dict:
                                     w.max_q(), w.max_k(), w.softmax_scale, out, lse, ws, nb, **kwm)
         res["fp8" if mask == "none" else "fp8/" + mask] = {
             "status": (st, va.varlen_attn_get_device_status()), "out": out.clone().cpu(), "lse": lse.clone().cpu()}
+    # the dense batched E4M3 forward (uniform segments, bounds computed on the device), rows padded
+    B, Sq, Sk, H = 2, 130, 77, 2
+    w = W.custom("fp8_dense", [Sq] * B, [Sk] * B, H, 128, row_pad=32)
+    d = W.make_inputs(w, 1, with_dout=False).to(DEV)
+    out = W.output_like(w, "out", DEV)
+    lse = torch.full((H, w.total_q), 777.0, device=DEV)
+    nb = va.varlen_attn_fwd_fp8_dense_workspace_size(B, Sq, Sk, H, 128)
+    ws = torch.empty(nb, dtype=torch.uint8, device=DEV)
+
+    def as4(t, S):
+        return t.as_strided((B, S, H, 128), (S * t.stride(0), t.stride(0), t.stride(1), 1), t.storage_offset())
+
+    for causal in (0, 1):
+        st = va.varlen_attn_fwd_fp8_dense(as4(d.q, Sq), as4(d.k, Sk), as4(d.v, Sk), B, Sq, Sk, H, 128,
+                                          w.softmax_scale, causal, as4(out, Sq), lse, ws, nb)
+        res["fp8_dense/%d" % causal] = {"status": (st, va.varlen_attn_get_device_status()),
+                                        "out": out.clone().cpu(), "lse": lse.clone().cpu()}
     # the checker's self test: extents 16 bytes short make the last accesses fail
     w = W.custom("slack", [70], [90], 2, 64)
     d = W.make_inputs(w, 0).to(DEV)
