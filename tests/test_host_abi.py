@@ -2,7 +2,9 @@
 every function include/varlen_attn.h declares, validates arguments with the
 documented status codes before touching a device, and its host tile count
 matches the page values.  Pointers passed here are never dereferenced: every
-call either fails validation or stops at the device query (no GPU here)."""
+call either fails validation or stops at the device query, which fails for
+want of a GPU; where a GPU is visible the tests that call the library skip
+themselves rather than launch on fake pointers."""
 import ctypes
 import json
 import os
@@ -19,8 +21,22 @@ HEADER = os.path.join(ROOT, "include", "varlen_attn.h")
 GOLDEN = os.path.join(ROOT, "tests", "golden", "page_values.json")
 
 
+def _gpu_visible() -> bool:
+    try:
+        import torch
+        return bool(torch.cuda.is_available())
+    except Exception:
+        return False
+
+
 @pytest.fixture(scope="module")
 def va():
+    # Every call below passes fake device pointers and relies on the device
+    # query failing.  Where a GPU is visible, a call that passes validation
+    # would launch kernels on those addresses, so these checks run only on a
+    # machine without one (the GPU tests cover the calls that reach a device).
+    if _gpu_visible():
+        pytest.skip("fake-pointer ABI checks run only where no GPU is visible")
     from packed_variable_length_varlen_gb300 import build
     build.build()
     from packed_variable_length_varlen_gb300 import varlen_attn
