@@ -765,8 +765,8 @@ def main():
     ap.add_argument("--mma-rates", action="store_true",
                     help="print cycles per tcgen05 MMA for N = 64/128/256 and three issue forms (one CTA)")
     ap.add_argument("--fp8", action="store_true",
-                    help="time the E4M3 forward alone (head size 128; with --causal / --window its banded form; "
-                         "quantisation included)")
+                    help="time the E4M3 forward alone (head size 128; with --causal / --window its banded form, "
+                         "with --dense the dense batched entry point; quantisation included)")
     ap.add_argument("--shard", choices=["replicas", "heads"], default="replicas",
                     help="under torchrun: every rank a batch of its own (replicas, weak scaling) or one problem "
                          "split by heads across the ranks (strong scaling); no collective on the data path either way")
