@@ -143,3 +143,39 @@ def test_window_long_segments_sampled():
         kr.append(rr)
         kh.append(np.full(rr.size, h, np.int32))
     _check(w, cpu, res, window, qp, (np.concatenate(kr), np.concatenate(kh)))
+
+
+@pytest.mark.slow
+def test_window_windowed_full():
+    """The windowed workload (8 segments, H=56, D=128, Sq < Sk) with the band
+    (1024, 0) that the benchmark times: forward and dQ on 4096 sampled rows
+    over every segment; dK / dV on sampled kv rows of two (segment, head)
+    blocks that start a little before the first key any query sees; and, over
+    the whole dK / dV outputs, exact zeros for every key no query sees (with
+    this band most of each segment's keys)."""
+    w = W.windowed()
+    cpu = W.make_inputs(w, 0)
+    window = (1024, 0)
+    res = _run(w, cpu, window)
+    qp = W.sample_pairs(W.sample_rows(w.cu_q, 4096, seed=1), w.num_heads, 1, seed=2)
+    first_seen = []  # per segment: the first key (0-based) some query's band holds
+    for b in range(w.batch):
+        sq, sk = w.cu_q[b + 1] - w.cu_q[b], w.cu_k[b + 1] - w.cu_k[b]
+        first_seen.append(max(0, sk - sq - window[0]))
+    kr, kh = [], []
+    for b, h in ((2, 7), (5, 44)):
+        lo = w.cu_k[b] + max(0, first_seen[b] - 64)
+        rr = W.sample_rows([lo, w.cu_k[b + 1]], 128, seed=b)
+        kr.append(rr)
+        kh.append(np.full(rr.size, h, np.int32))
+    _check(w, cpu, res, window, qp, (np.concatenate(kr), np.concatenate(kh)))
+    dk, dv = res["dk"].cpu(), res["dv"].cpu()
+    unseen = 0
+    for b in range(w.batch):
+        k0 = w.cu_k[b]
+        assert first_seen[b] > 0
+        assert int(torch.count_nonzero(dk[k0:k0 + first_seen[b]])) == 0, b
+        assert int(torch.count_nonzero(dv[k0:k0 + first_seen[b]])) == 0, b
+        assert int(torch.count_nonzero(dv[k0 + first_seen[b]])) > 0, b  # the first seen key has gradients
+        unseen += first_seen[b]
+    print("window (1024, 0) full size: %d of %d keys seen by no query, dK = dV = 0 there" % (unseen, w.total_k))
