@@ -21,6 +21,20 @@
  *            with no keys, whose O rows are 0),
  * and the backward returns dQ, dK, dV of sum(O * dO).
  *
+ * Entry points, by family (each declared below with its own contract):
+ *   packed bf16        varlen_attn_fwd / _bwd (+ _bwd_workspace_size), their
+ *                      causal and sliding-window forms (_causal, _window), the
+ *                      deterministic backward, and a backward without a
+ *                      workspace argument (_bwd_noalloc);
+ *   dense batched bf16 varlen_attn_fwd_dense / _bwd_dense ([B, S, H, D]);
+ *   E4M3 (FP8) forward varlen_attn_fwd_fp8, _fp8_window, _fp8_dense (D = 128,
+ *                      quantised from bf16 into a caller workspace);
+ *   status             varlen_attn_get_device_status, _status_string,
+ *                      _last_cuda_error;
+ *   diagnostics        tile counts and schedules, the bounded-wait self test,
+ *                      phase events, the tensor-core issue-rate probe, and the
+ *                      knobs of the bounds-checking build and failure tests.
+ *
  * Conventions shared by every entry point
  *   Layout.  Every q/k/v/out/dout/dq/dk/dv tensor is "NHD": element (row r,
  *     head h, dim d) lives at  base + r*stride.row + h*stride.head + d
