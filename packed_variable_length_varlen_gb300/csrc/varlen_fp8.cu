@@ -625,9 +625,10 @@ __global__ void __launch_bounds__(384, 1)
       const float qd = descale_of(in_span(p.amax_span, aq, 4, p.err) ? __ldg(aq) : 0.f);
       const float kd = descale_of(in_span(p.amax_span, ak, 4, p.err) ? __ldg(ak) : 0.f);
       const float vd = descale_of(in_span(p.amax_span, av, 4, p.err) ? __ldg(av) : 0.f);
-      // (at least the smallest normal float, so that a masked score times c2
-      // stays -inf when scale * qd * kd underflows; the scores are then
-      // below 3e-31 in magnitude and P is 1 either way)
+      // The score factor in the log2 domain, floored at the smallest normal
+      // float: a masked score (-inf) times c2 must stay -inf when
+      // scale * qd * kd underflows.  The scores are then below 3e-31 in
+      // magnitude, so P is 1 either way.
       const float c2 = fmaxf(p.scale * 1.4426950408889634f * qd * kd, FLT_MIN);
       // keys [key_lo, key_hi) this row sees: all Sk, or with a mask its band
       int32_t key_lo = 0, key_hi = c.olen;
