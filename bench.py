@@ -536,7 +536,7 @@ def ours(args, w, ws, rank, local):
             stream.wait_event(in_done[(n - 1) % 2])
             end.record(stream)
 
-        # the copy rates of this box, measured on the largest input (k)
+        # the copy rates of this machine, measured on the largest input (k)
         rates = _copy_rates(d.k if d.k._base is None else d.k._base, host["k"],
                             torch.empty(host["k"].shape, dtype=host["k"].dtype).pin_memory(), stream)
         a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -549,7 +549,7 @@ def ours(args, w, ws, rank, local):
         torch.cuda.synchronize()
         ms_e2e = _max_over_ranks(a.elapsed_time(b_), ws)
         # what each copy and each step's kernels took inside the pipeline (a
-        # box whose copies slow the kernels, or the other way round, shows here)
+        # machine whose copies slow the kernels, or the other way round, shows here)
         in_pipe = {k: statistics.mean(x.elapsed_time(y) for kk, x, y in spans if kk == k)
                    for k in ("h2d", "kernels", "d2h")}
         # What the copies alone cost per step at the measured concurrent
