@@ -699,23 +699,28 @@ __global__ void __launch_bounds__(384, 1)
         const float2 cc2 = make_float2(c2, c2), negm = make_float2(-m_sub, -m_sub);
         float2 rs2a = make_float2(0.f, 0.f), rs2b = make_float2(0.f, 0.f);
         uint32_t pw[32];
+        // each 16-word half goes to TMEM as soon as it is packed, so the
+        // first store overlaps the second half's arithmetic
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const int e = k * 4;
-          float2 t0 = ffma2(make_float2(x[e], x[e + 1]), cc2, negm);
-          float2 t1 = ffma2(make_float2(x[e + 2], x[e + 3]), cc2, negm);
-          t0.x = ex2(t0.x);
-          t0.y = ex2(t0.y);
-          t1.x = ex2(t1.x);
-          t1.y = ex2(t1.y);
-          rs2a = fadd2(rs2a, t0);
-          rs2b = fadd2(rs2b, t1);
-          const uint32_t lo = __nv_cvt_float2_to_fp8x2(t0, __NV_SATFINITE, __NV_E4M3);
-          const uint32_t hi = __nv_cvt_float2_to_fp8x2(t1, __NV_SATFINITE, __NV_E4M3);
-          pw[k] = lo | (hi << 16);
+        for (int hk = 0; hk < 2; ++hk) {
+#pragma unroll
+          for (int k = hk * 16; k < hk * 16 + 16; ++k) {
+            const int e = k * 4;
+            float2 t0 = ffma2(make_float2(x[e], x[e + 1]), cc2, negm);
+            float2 t1 = ffma2(make_float2(x[e + 2], x[e + 3]), cc2, negm);
+            t0.x = ex2(t0.x);
+            t0.y = ex2(t0.y);
+            t1.x = ex2(t1.x);
+            t1.y = ex2(t1.y);
+            rs2a = fadd2(rs2a, t0);
+            rs2b = fadd2(rs2b, t1);
+            const uint32_t lo = __nv_cvt_float2_to_fp8x2(t0, __NV_SATFINITE, __NV_E4M3);
+            const uint32_t hi = __nv_cvt_float2_to_fp8x2(t1, __NV_SATFINITE, __NV_E4M3);
+            pw[k] = lo | (hi << 16);
+          }
+          tmem_st16(tmem + lane_off + s_col + hk * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pw[hk * 16]));
         }
         const float rs = (rs2a.x + rs2a.y) + (rs2b.x + rs2b.y);
-        tmem_st32(tmem + lane_off + s_col, pw);
         l = fmaf(l, alpha, rs);
         if (__any_sync(0xffffffffu, rescale)) {
           // S_j was issued after O += P_{j-1} V_{j-1} of this half (issue
