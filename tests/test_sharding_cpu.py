@@ -4,7 +4,9 @@ Head and segment ranges partition the work; two gloo ranks that each compute
 their shard (heads, or a contiguous run of segments) with the oracle
 reproduce the unsharded result exactly, because every (segment, head) pair
 is independent -- the multi-GPU path needs no exchange of data, only the
-max of the ranks' times, which is checked here too."""
+max of the ranks' times, which is checked here too.  The same holds for the
+E4M3 forward, whose descales are per (segment, head): ranks that quantise
+their own shard reproduce the unsharded codes and results."""
 import os
 import socket
 import tempfile
@@ -172,3 +174,80 @@ def test_two_rank_shards_match_unsharded(mode, window):
     np.testing.assert_array_equal(dq, dq_ref)
     np.testing.assert_array_equal(dk, dk_ref)
     np.testing.assert_array_equal(dv, dv_ref)
+
+
+# ---------------------------------------------------------------- two ranks, E4M3 forward
+
+def _fp8_shard_result(w, cpu, mode, world, rank, causal=False):
+    """The oracle's E4M3 forward of this rank's shard, keyed by global (row,
+    head) pairs.  The rank quantises its own (segment, head) blocks: their
+    descales depend on nothing outside the block, so a shard's codes are the
+    unsharded codes of its blocks."""
+    if mode == "heads":
+        h0, h1 = S.head_range(w.num_heads, world, rank)
+        q, k, v = (t[:, h0:h1] for t in (cpu.q, cpu.k, cpu.v))
+        cu_q, cu_k = list(w.cu_q), list(w.cu_k)
+        rows, heads = oracle.all_pairs(w.total_q, h1 - h0)
+        grows, gheads = rows, heads + h0
+    else:
+        sh = S.segment_range(w.cu_q, w.cu_k, world, rank)
+        q, k, v = cpu.q[sh.q0:sh.q1], cpu.k[sh.k0:sh.k1], cpu.v[sh.k0:sh.k1]
+        cu_q, cu_k = sh.cu_q, sh.cu_k
+        rows, heads = oracle.all_pairs(sh.q1 - sh.q0, w.num_heads)
+        grows, gheads = rows + sh.q0, heads
+    quant = [oracle.quantize_e4m3(x, cu) for x, cu in ((q, cu_q), (k, cu_k), (v, cu_k))]
+    codes, desc = [c for c, _ in quant], [d for _, d in quant]
+    o, lse = oracle.Fp8Problem(*codes, cu_q, cu_k, w.softmax_scale, *desc, causal=causal).fwd(rows, heads)
+    return grows, gheads, o, lse
+
+
+def _fp8_worker(rank, world, port, mode, out_path, causal):
+    import torch.distributed as dist
+    dist.init_process_group("gloo", rank=rank, world_size=world, init_method="tcp://127.0.0.1:%d" % port)
+    try:
+        w = W.custom("shard", *_CASE[:2], _CASE[2], _CASE[3])
+        cpu = W.make_inputs(w, 0, with_dout=False)
+        res = _fp8_shard_result(w, cpu, mode, world, rank, causal)
+        gathered = [None] * world
+        dist.all_gather_object(gathered, res)  # only to bring the shards to one process for checking
+        if rank == 0:
+            np.savez(out_path, *[np.concatenate([g[i] for g in gathered]) for i in range(4)])
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("mode,causal", [("heads", False), ("segments", False), ("heads", True),
+                                         ("segments", True)])
+def test_two_rank_fp8_shards_match_unsharded(mode, causal):
+    """Two gloo ranks each quantise and run their shard of the E4M3 forward
+    (the oracle's reading); together they reproduce the unsharded
+    quantisation and forward bit for bit, with no exchange of data."""
+    oracle.build()
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    world = 2
+    with tempfile.TemporaryDirectory() as d:
+        out = os.path.join(d, "res.npz")
+        port = _free_port()
+        procs = [ctx.Process(target=_fp8_worker, args=(r, world, port, mode, out, causal)) for r in range(world)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(timeout=240)
+        for p in procs:
+            if p.is_alive():
+                p.kill()
+                p.join()
+        assert all(p.exitcode == 0 for p in procs), [p.exitcode for p in procs]
+        z = np.load(out)
+        rows, heads, o, lse = (z["arr_%d" % i] for i in range(4))
+
+    w = W.custom("shard", *_CASE[:2], _CASE[2], _CASE[3])
+    cpu = W.make_inputs(w, 0, with_dout=False)
+    quant = [oracle.quantize_e4m3(x, cu) for x, cu in ((cpu.q, w.cu_q), (cpu.k, w.cu_k), (cpu.v, w.cu_k))]
+    full = oracle.Fp8Problem(*[c for c, _ in quant], list(w.cu_q), list(w.cu_k), w.softmax_scale,
+                             *[d for _, d in quant], causal=causal)
+    assert sorted(zip(rows.tolist(), heads.tolist())) == sorted(zip(*[a.tolist() for a in oracle.all_pairs(w.total_q, w.num_heads)]))
+    o_ref, lse_ref = full.fwd(rows, heads)
+    np.testing.assert_array_equal(o, o_ref)
+    np.testing.assert_array_equal(lse, lse_ref)
