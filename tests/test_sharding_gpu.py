@@ -94,3 +94,43 @@ def test_segment_shards_reproduce_the_unsharded_call():
         assert torch.equal(o2, out) and torch.equal(l2, lse), world
         assert torch.equal(g2[1], dk) and torch.equal(g2[2], dv), world
         _dq_close(g2[0], dq)
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["unmasked", "causal"])
+def test_fp8_shards_reproduce_the_unsharded_call(causal):
+    """The E4M3 forward split by heads (views t[:, h0:h1], lse rows h0:h1) and
+    by segments (row slices, rebased cu_seqlens): each shard quantises its
+    own (segment, head) blocks, whose descales depend on nothing else, so
+    together the shards reproduce the unsharded O and LSE bit for bit."""
+    from packed_variable_length_varlen_gb300 import varlen_attn as va
+    w = W.custom("shard_fp8", [300, 0, 129, 517, 1, 77], [257, 5, 300, 517, 64, 0], 4, 128)
+    H = w.num_heads
+    d = W.make_inputs(w, 0, with_dout=False).to(DEV)
+    out, lse, _ = va.attention_fwd_fp8(d.q, d.k, d.v, d.cu_q, d.cu_k, w.softmax_scale, causal=causal)
+    assert va.varlen_attn_get_device_status() == 0
+    for world in (2, 4):
+        o2, l2 = torch.full_like(out, float("nan")), torch.full_like(lse, float("nan"))
+        for rank in range(world):
+            h0, h1 = S.head_range(H, world, rank)
+            if h1 == h0:
+                continue
+            sl = slice(h0, h1)
+            va.attention_fwd_fp8(d.q[:, sl], d.k[:, sl], d.v[:, sl], d.cu_q, d.cu_k, w.softmax_scale, out=o2[:, sl],
+                                 lse=l2[sl], causal=causal)
+            assert va.varlen_attn_get_device_status() == 0
+        assert torch.equal(o2, out) and torch.equal(l2, lse), ("heads", world)
+    for world in (2, 3):
+        o2, l2 = torch.full_like(out, float("nan")), torch.full_like(lse, float("nan"))
+        for rank in range(world):
+            sh = S.segment_range(w.cu_q, w.cu_k, world, rank)
+            if sh.empty:
+                continue
+            qs, ks = slice(sh.q0, sh.q1), slice(sh.k0, sh.k1)
+            cu_q = torch.tensor(sh.cu_q, dtype=torch.int32, device=DEV)
+            cu_k = torch.tensor(sh.cu_k, dtype=torch.int32, device=DEV)
+            lse_sh = torch.empty(H, sh.q1 - sh.q0, device=DEV)
+            va.attention_fwd_fp8(d.q[qs], d.k[ks], d.v[ks], cu_q, cu_k, w.softmax_scale, out=o2[qs], lse=lse_sh,
+                                 causal=causal)
+            assert va.varlen_attn_get_device_status() == 0
+            l2[:, qs] = lse_sh
+        assert torch.equal(o2, out) and torch.equal(l2, lse), ("segments", world)
