@@ -112,6 +112,24 @@ def _battery(lib):
         ok_m &= bool(np.array_equal(lmq, lm) and np.all(omq[np.isneginf(lm)] == 0))
         n_empty += int(np.isneginf(lm).sum())
     res.append(("masked_unrounded_equals_fp64_oracle", bool(ok_m and n_empty > 0)))
+    # the diagonal band (0, 0) in closed form: row i of a segment sees only key
+    # i + Sk - Sq, so P = 1 (exact in E4M3), o = vd * v8 of that key exactly and
+    # LSE = its score scale * qd * kd * (q8 . k8), computed here in the same order
+    od, ld = oracle.Fp8Problem(q8m, k8m, v8m, cqm, ckm, sc, qdm, kdm, vdm, window=(0, 0)).fwd(rowsm, headsm, lib)
+    qdec, kdec, vdec = (oracle.e4m3_decode(t.numpy(), lib) for t in (q8m, k8m, v8m))
+    ok_d, n_diag = True, 0
+    for t, (i, h) in enumerate(zip(rowsm, headsm)):
+        b = int(np.searchsorted(cqm, i, side="right") - 1)
+        sq_, sk_ = cqm[b + 1] - cqm[b], ckm[b + 1] - ckm[b]
+        j = i - cqm[b] + sk_ - sq_
+        if not 0 <= j < sk_:
+            ok_d &= bool(np.isneginf(ld[t]) and np.all(od[t] == 0))
+            continue
+        n_diag += 1
+        bh = b * H + h
+        s_ij = sc * qdm[bh] * kdm[bh] * float(np.dot(qdec[i, h], kdec[ckm[b] + j, h]))
+        ok_d &= bool(np.array_equal(od[t], vdm[bh] * vdec[ckm[b] + j, h]) and ld[t] == s_ij)
+    res.append(("diagonal_band_closed_form", bool(ok_d and n_diag > 0)))
     # with rounding: O moves by at most 2^-4 of sum_j p_j |v_j| / l per element
     p1 = oracle.Fp8Problem(q8, k8, v8, cq, ck, sc, qd, kd, vd, quantize_p=True)
     o1, l1 = p1.fwd(rows, heads, lib)
